@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Batch-1 greedy decode throughput of the K2-Horizon-3.7B-shape dense GQA
+decoder (bf16 weights, fp16 KV) at context 4096 on one GB300, through libk2.
+
+One step = one token: embedding, 36 decoder layers (QKV + RoPE, attention +
+KV append, o_proj, gate/up + SwiGLU, down), final norm, lm_head, argmax.
+Weights are random-init of the published shape (no checkpoint exists here);
+the KV cache is filled by prefilling 4096 seeded random token ids.
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+
+Prints one JSON line.  With --gpus N > 1 (under torchrun) every rank runs an
+independent replica (weak scaling; the path has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 decode tok/s (3.7B dense GQA, bf16) and achieved HBM GB/s vs peak"
+WORKLOAD = "k2-horizon-3.7b-shape greedy decode, batch 1, context 4096, fp16 KV, bf16 weights"
+CTX = 4096
+SHAPE_NAME = "k2_3p7b"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=128)
+    p.add_argument("--warmup", type=int, default=8)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--ctx", type=int, default=CTX)
+    p.add_argument("--profile-steps", type=int, default=4)
+    p.add_argument("--e2e-steps", type=int, default=32)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--layers", type=int, default=0, help="override layer count (debug)")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(s, ctx_len: int) -> dict:
+    """Bytes the decode step must move at context ctx_len (weights once, the
+    KV history once, plus the small activations)."""
+    H, d, I, V = s.hidden, s.head_dim, s.intermediate, s.vocab
+    qkv_n = (s.n_heads + 2 * s.n_kv_heads) * d
+    wb = 2 if s.weight_dtype == "bf16" else 4
+    per_layer = (qkv_n * H + H * s.n_heads * d + 2 * I * H + H * I + 2 * H) * wb
+    weights = s.n_layers * per_layer + V * H * wb + H * wb
+    kv_row = 2 * s.n_kv_heads * d * 2  # fp16 K and V of one position, one layer
+    kv = s.n_layers * kv_row * ctx_len
+    return {
+        "weights": weights,
+        "kv": kv,
+        "total": weights + kv,
+        # the gate/up GEMV: W [2I, H] + x [H] fp32 + gain [H] + act [I] fp32
+        "gate_up_launch": 2 * I * H * wb + H * 4 + H * wb + I * 4,
+    }
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_from_profiles(kernel_sources):
+    """dram bytes per launch of the gate/up GEMV from the committed ncu summary,
+    only if the kernel source is unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    h = hashlib.sha256()
+    for src in kernel_sources:
+        with open(src, "rb") as f:
+            h.update(f.read())
+    sha = h.hexdigest()[:16]
+    try:
+        for line in open(path):
+            kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
+            if kv.get("kernel") == "gemv_gate_up" and kv.get("source_sha") == sha:
+                return float(kv["dram_bytes_per_launch"]), sha
+    except OSError:
+        pass
+    return None, sha
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.out.name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs (the oracle as it stands, on this host's cores)
+# ---------------------------------------------------------------------------
+
+def oracle_decode_sample(n_layers_sample: int = 2, vocab_fraction: float = 1.0, ctx_len: int = CTX):
+    """Times the oracle's single-token decode at context ctx_len on a sample of
+    the model: n_layers_sample layers (each with its own weights) and a
+    fraction of the lm_head rows; returns seconds per full token (the sample
+    scaled to 36 layers and the whole vocab) and a description."""
+    import numpy as np
+
+    import k2_inputs as ki
+    from oracle import k2_oracle as O
+
+    s = ki.K2_3P7B
+    rng = np.random.default_rng(5)
+    kv = rng.standard_normal((ctx_len, s.n_kv_heads, s.head_dim)).astype(np.float16).astype(np.float64)
+    x = ki.hidden_f32(s.hidden, seed=3).astype(np.float64)
+    t_layers = 0.0
+    for l in range(n_layers_sample):
+        w = {n: ki.weight(s, n, l).values for n in ki.LAYER_TENSORS}
+        t0 = time.perf_counter()
+        x, _, _ = O.layer_decode_step(s, w, x, ctx_len, kv, kv, "f16")
+        t_layers += time.perf_counter() - t0
+    rows = max(1, int(s.vocab * vocab_fraction))
+    W = ki.weight(s, "lm_head", -1).values[:rows]
+    fn = np.ones(s.hidden, np.float32)
+    m = O.OracleModel(s.replace(vocab=rows), lambda n, l: {"final_norm": fn, "lm_head": W}[n], "f16")
+    t0 = time.perf_counter()
+    lg = m.head(x[None, :])
+    O.argmax_first(lg[0])
+    t_head = time.perf_counter() - t0
+    per_token = t_layers / n_layers_sample * s.n_layers + t_head / (rows / s.vocab)
+    desc = (f"oracle single-token decode at context {ctx_len}: {n_layers_sample} of {s.n_layers} layers and "
+            f"{rows} of {s.vocab} lm_head rows timed, scaled to one full token")
+    return per_token, desc, t_layers + t_head
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, world, rank, pg):
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+    # each step: one oracle decode over one layer and 1/36 of the lm_head rows
+    # (a 36th of a token); value = tokens per second of the whole model
+    for _ in range(args.warmup):
+        oracle_decode_sample(1, 1.0 / 36, args.ctx)
+    per_tok, times = [], []
+    for _ in range(args.steps):
+        pt, desc, wall = oracle_decode_sample(1, 1.0 / 36, args.ctx)
+        per_tok.append(pt)
+        times.append(wall)
+    sec_per_token = statistics.mean(per_tok)
+    value = 1.0 / sec_per_token
+    cores = blas_threads()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": statistics.mean(times) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": WORKLOAD, "batch": 1, "context": args.ctx},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                         "sample": desc + "; each step is 1/36 of a token"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def random_device_weights(s, seed: int = 0):
+    import torch
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    dt = torch.bfloat16 if s.weight_dtype == "bf16" else torch.float32
+
+    def rnd(*shape):
+        return (torch.randn(*shape, generator=g, device="cuda", dtype=torch.float32) * 0.02).to(dt)
+
+    H, d = s.hidden, s.head_dim
+    w = {"embed": rnd(s.vocab, H), "lm_head": rnd(s.vocab, H), "final_norm": torch.ones(H, device="cuda", dtype=dt)}
+    for n in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down"):
+        w[n] = []
+    for _ in range(s.n_layers):
+        w["attn_norm"].append(torch.ones(H, device="cuda", dtype=dt))
+        w["mlp_norm"].append(torch.ones(H, device="cuda", dtype=dt))
+        w["wq"].append(rnd(s.n_heads * d, H))
+        w["wk"].append(rnd(s.n_kv_heads * d, H))
+        w["wv"].append(rnd(s.n_kv_heads * d, H))
+        w["wo"].append(rnd(H, s.n_heads * d))
+        w["w_gate"].append(rnd(s.intermediate, H))
+        w["w_up"].append(rnd(s.intermediate, H))
+        w["w_down"].append(rnd(H, s.intermediate))
+    return w
+
+
+def run_ours(args, world, rank, local, pg):
+    import numpy as np
+    import torch
+
+    import k2_inputs as ki
+    from dense_gqa_decoder_gb300 import k2
+
+    torch.cuda.set_device(local)
+    s = ki.SHAPES[SHAPE_NAME]
+    if args.layers:
+        s = s.replace(n_layers=args.layers)
+    budget = args.ctx + args.warmup + args.steps + args.profile_steps + args.e2e_steps + 16
+    cfg = k2.make_config(s, max_context=budget, max_batch=1, kv_dtype="f16")
+    ctx = k2.Context(cfg, random_device_weights(s, seed=1234 + rank))
+    stream = torch.cuda.Stream()
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    prompt = torch.from_numpy(ki.prompt_ids(s.vocab, args.ctx, seed=1 + rank)).cuda()
+    with torch.cuda.stream(stream):
+        ctx.prefill(0, prompt, tok, stream=stream)
+    stream.synchronize()
+    ctx.set_option(k2.K2_OPT_GRAPH, 1)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            ctx.decode_step(tok, 1, tok, stream=stream)
+    stream.synchronize()
+    if ctx.sync_status(stream) != k2.K2_OK:
+        raise RuntimeError("device guard after warm-up: " + ctx.last_error())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    ctx_start = ctx.kv_view(0, 0)[4]
+    e0.record(stream)
+    for _ in range(args.steps):
+        ctx.decode_step(tok, 1, tok, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    if ctx.sync_status(stream) != k2.K2_OK:
+        raise RuntimeError("device guard after the timed steps: " + ctx.last_error())
+    ms_per_step = ms / args.steps
+    value = world * args.steps / (ms / 1e3)
+    mean_ctx = ctx_start + (args.steps - 1) / 2 + 1
+    by = algorithmic_bytes(s, int(round(mean_ctx)))
+
+    # per-kernel durations: one un-graphed step with an event pair per kernel
+    ms_k = {k: 0.0 for k in k2.KERNEL_CLASSES}
+    n_k = {k: 0 for k in k2.KERNEL_CLASSES}
+    for _ in range(args.profile_steps):
+        a, b = ctx.profile_decode(tok, 1, tok, stream=stream)
+        for k in ms_k:
+            ms_k[k] += a[k]
+            n_k[k] += b[k]
+    gu_ms = ms_k["gate_up"] / max(1, n_k["gate_up"])
+    peak, peak_src = measured_peaks()
+    achieved = by["gate_up_launch"] / (gu_ms * 1e-3) / 1e9
+    src = [os.path.join(ROOT, "dense_gqa_decoder_gb300", "csrc", f) for f in ("k2_gemv.cu", "k2_common.cuh")]
+    traffic, sha = traffic_from_profiles(src)
+
+    # end to end through the C ABI with host buffers: token H2D, step, token D2H
+    host_in = torch.zeros(1, dtype=torch.int32).pin_memory()
+    host_out = torch.zeros(1, dtype=torch.int32).pin_memory()
+    host_in.copy_(tok.cpu())
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        with torch.cuda.stream(stream):
+            tok.copy_(host_in, non_blocking=True)
+            ctx.decode_step(tok, 1, tok, stream=stream)
+            host_out.copy_(tok, non_blocking=True)
+        stream.synchronize()
+        host_in.copy_(host_out)
+    e2e_s = time.perf_counter() - t0
+    e2e_value = world * args.e2e_steps / e2e_s
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        per_token, desc, _ = oracle_decode_sample(2, 1.0, args.ctx)
+        cpu = {"value": 1.0 / per_token, "unit": "tok/s", "cores": blas_threads(), "kind": "oracle", "sample": desc}
+
+    launches_per_step = 1 + 5 * s.n_layers + 1
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 1, "context": args.ctx, "layers": s.n_layers,
+                   "kv_dtype": "f16", "activations": "fp32", "cuda_graph": True, "pdl": True,
+                   "l2": "no flush: every step streams 8.8 GB of weights, far above the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "hbm": {"bytes_per_step": by["total"], "achieved_gbs": by["total"] / (ms_per_step * 1e-3) / 1e9,
+                "peak_gbs": peak, "frac": by["total"] / (ms_per_step * 1e-3) / 1e9 / peak,
+                "frac_of_8tbs_nominal": by["total"] / (ms_per_step * 1e-3) / 1e9 / 7900.0},
+        "roofline": {"bound": "hbm", "kernel": "gemv_gate_up (norm + gate/up GEMV + SwiGLU)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": peak_src, "algorithmic_bytes": by["gate_up_launch"],
+                     "launch_ms": gu_ms, "source_sha": sha},
+        "kernel_ms_per_step": {k: ms_k[k] / args.profile_steps for k in ms_k},
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local, pg = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank, pg)
+    else:
+        run_ours(args, world, rank, local, pg)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

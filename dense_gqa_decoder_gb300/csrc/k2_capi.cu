@@ -1,0 +1,699 @@
+// Host side of libk2: config validation, workspace layout, the decode-step
+// launch sequence, graph caching, and the C ABI declared in include/k2.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/k2.h"
+#include "k2_kernels.h"
+
+using namespace k2;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kGemvSmem = 96 * 1024;  // per-CTA ring budget: two CTAs of consecutive kernels fit one SM
+constexpr size_t kAttnSmem = 96 * 1024;
+constexpr int kSplitMax = 64;
+constexpr int kArgmaxPartsMax = 1024;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int elt_bytes(int dt) { return dt == K2_F32 ? 4 : (dt == K2_BF16 || dt == K2_F16) ? 2 : 1; }
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+struct Layout {
+  size_t seq_len, guard, attn_counter, am_counter, rope, resid, qkv, attn_out, act, attn_part, am_val, am_idx;
+  size_t wqkv, wgu;  // per-layer stride below
+  size_t wqkv_layer, wgu_layer;
+  size_t kc, vc, ks, vs;  // first layer; per-layer stride kv_layer / sc_layer
+  size_t kv_layer, sc_layer;
+  size_t total;
+  size_t repack_bytes, kv_bytes;
+  int cap;
+};
+
+struct Sizes {
+  int H, L, nq, nkv, d, I, G, V, ctx, B, qkv_n, rep, wb, kvb;
+};
+
+Sizes sizes_of(const k2_config& c) {
+  Sizes s;
+  s.H = c.hidden; s.L = c.n_layers; s.nq = c.n_heads; s.nkv = c.n_kv_heads; s.d = c.head_dim;
+  s.I = c.intermediate; s.G = c.norm_groups; s.V = c.vocab; s.ctx = c.max_context; s.B = c.max_batch;
+  s.qkv_n = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  s.rep = c.n_kv_heads > 0 ? c.n_heads / c.n_kv_heads : 0;
+  s.wb = elt_bytes(c.weight_dtype);
+  s.kvb = elt_bytes(c.kv_dtype);
+  return s;
+}
+
+Layout layout_of(const k2_config& c) {
+  const Sizes s = sizes_of(c);
+  Layout l = {};
+  // rows of KV per sequence: room for max_context rows plus the 16-byte
+  // rounding of int8 scale copies, in whole 64-row tiles
+  l.cap = static_cast<int>(align_up(static_cast<size_t>(s.ctx) + 8, 64));
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, kAlign);
+    return at;
+  };
+  l.seq_len = take(sizeof(int) * s.B);
+  l.guard = take(sizeof(unsigned));
+  l.attn_counter = take(sizeof(unsigned) * s.B * s.nkv);
+  l.am_counter = take(sizeof(unsigned) * s.B);
+  l.rope = take(sizeof(float2) * static_cast<size_t>(l.cap) * (s.d / 2));
+  l.resid = take(sizeof(float) * static_cast<size_t>(s.B) * s.H);
+  l.qkv = take(sizeof(float) * static_cast<size_t>(s.B) * s.qkv_n);
+  l.attn_out = take(sizeof(float) * static_cast<size_t>(s.B) * s.nq * s.d);
+  l.act = take(sizeof(float) * static_cast<size_t>(s.B) * s.I);
+  l.attn_part = take(sizeof(float) * static_cast<size_t>(s.B) * s.nkv * kSplitMax * s.rep * (s.d + 2));
+  l.am_val = take(sizeof(float) * static_cast<size_t>(s.B) * kArgmaxPartsMax);
+  l.am_idx = take(sizeof(int) * static_cast<size_t>(s.B) * kArgmaxPartsMax);
+  const size_t scratch_end = o;
+  l.wqkv_layer = align_up(static_cast<size_t>(s.qkv_n) * s.H * s.wb, kAlign);
+  l.wgu_layer = align_up(static_cast<size_t>(2) * s.I * s.H * s.wb, kAlign);
+  l.wqkv = take(l.wqkv_layer * s.L);
+  l.wgu = take(l.wgu_layer * s.L);
+  l.repack_bytes = o - scratch_end;
+  const size_t kv_start = o;
+  l.kv_layer = align_up(static_cast<size_t>(s.B) * s.nkv * l.cap * s.d * s.kvb, kAlign);
+  l.sc_layer = c.kv_dtype == K2_I8 ? align_up(static_cast<size_t>(s.B) * s.nkv * l.cap * 2, kAlign) : 0;
+  l.kc = take(l.kv_layer * s.L);
+  l.vc = take(l.kv_layer * s.L);
+  l.ks = take(l.sc_layer * s.L);
+  l.vs = take(l.sc_layer * s.L);
+  l.kv_bytes = o - kv_start;
+  l.total = o;
+  return l;
+}
+
+std::string check_config(const k2_config* c) {
+  if (!c) return "config is NULL";
+  if (c->hidden <= 0 || c->n_layers <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
+      c->intermediate <= 0 || c->norm_groups <= 0 || c->vocab <= 0 || c->max_context <= 0 || c->max_batch <= 0)
+    return "every size in the config must be positive";
+  if (c->hidden % c->norm_groups) return "hidden must be a multiple of norm_groups";
+  if (c->n_heads % c->n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
+  if (c->head_dim % 2) return "head_dim must be even (split-half RoPE)";
+  if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) return "eps must be >= 0 and rope_theta > 0";
+  if (c->weight_dtype != K2_F32 && c->weight_dtype != K2_BF16) return "weight_dtype must be K2_F32 or K2_BF16";
+  if (c->kv_dtype != K2_F32 && c->kv_dtype != K2_F16 && c->kv_dtype != K2_I8)
+    return "kv_dtype must be K2_F32, K2_F16 or K2_I8";
+  if (c->max_batch > 64) return "max_batch above 64 is not supported";
+  if (c->max_context > (1 << 24)) return "max_context above 2^24 is not supported";
+  if (!attn_supported(c->head_dim, c->n_heads / c->n_kv_heads, c->kv_dtype == K2_F32 ? 0 : c->kv_dtype))
+    return "attention kernel not built for this head_dim / GQA ratio / kv dtype";
+  return "";
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// the context
+// ---------------------------------------------------------------------------
+struct k2_ctx {
+  k2_config cfg;
+  Sizes s;
+  Layout lay;
+  int sms = 0;
+  uint8_t* ws = nullptr;
+  // weights
+  const void* embed = nullptr;
+  const void* lm_head = nullptr;
+  const void* final_norm = nullptr;
+  std::vector<const void*> attn_norm, wo, mlp_norm, w_down;
+  // workspace pointers
+  int* seq_len = nullptr;
+  unsigned* guard = nullptr;
+  unsigned* attn_counter = nullptr;
+  unsigned* am_counter = nullptr;
+  float2* rope = nullptr;
+  float *resid = nullptr, *qkv = nullptr, *attn_out = nullptr, *act = nullptr, *attn_part = nullptr,
+        *am_val = nullptr;
+  int* am_idx = nullptr;
+  // plans
+  GemvArgs p_qkv = {}, p_o = {}, p_gu = {}, p_down = {}, p_lm = {};
+  int grid_qkv = 0, grid_o = 0, grid_gu = 0, grid_down = 0, grid_lm = 0;
+  AttnArgs p_attn = {};
+  int attn_splits_b1 = 1;
+  int force_splits = 0;
+  // state
+  std::vector<int> len;
+  bool pdl = true;
+  bool graph = false;
+  std::map<std::tuple<int, const void*, const void*, const void*, void*>, cudaGraphExec_t> graphs;
+  std::string err;
+  // profiling
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+
+  void* wqkv(int l) const { return ws + lay.wqkv + lay.wqkv_layer * l; }
+  void* wgu(int l) const { return ws + lay.wgu + lay.wgu_layer * l; }
+  void* kc(int l) const { return ws + lay.kc + lay.kv_layer * l; }
+  void* vc(int l) const { return ws + lay.vc + lay.kv_layer * l; }
+  void* ks(int l) const { return lay.sc_layer ? ws + lay.ks + lay.sc_layer * l : nullptr; }
+  void* vs(int l) const { return lay.sc_layer ? ws + lay.vs + lay.sc_layer * l : nullptr; }
+
+  k2_status fail(k2_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    err = buf;
+    return st;
+  }
+  k2_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(K2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  }
+};
+
+namespace {
+
+int attn_splits(const k2_ctx* c, int batch) {
+  if (c->force_splits > 0) return c->force_splits < kSplitMax ? c->force_splits : kSplitMax;
+  int n = (c->sms + c->s.nkv * batch - 1) / (c->s.nkv * batch);
+  const int cap_splits = c->lay.cap / 8;
+  if (n > cap_splits) n = cap_splits;
+  if (n > kSplitMax) n = kSplitMax;
+  return n < 1 ? 1 : n;
+}
+
+// Kernel launch recorder: plain launches, or with a CUDA event pair per kernel.
+struct Launcher {
+  k2_ctx* c;
+  cudaStream_t s;
+  bool pdl;
+  float* ms = nullptr;      // profiling output (null = not profiling)
+  int* launches = nullptr;
+  cudaError_t err = cudaSuccess;
+
+  template <typename F>
+  void run(int cls, F&& f) {
+    if (err != cudaSuccess) return;
+    if (ms) {
+      if ((err = cudaEventRecord(c->ev[0], s))) return;
+      if ((err = f())) return;
+      if ((err = cudaEventRecord(c->ev[1], s))) return;
+      if ((err = cudaEventSynchronize(c->ev[1]))) return;
+      float t = 0.f;
+      if ((err = cudaEventElapsedTime(&t, c->ev[0], c->ev[1]))) return;
+      ms[cls] += t;
+      launches[cls] += 1;
+    } else {
+      err = f();
+    }
+  }
+};
+
+// One token of one sequence through the model with the batch-1 kernels.
+//   tok: device token (null when x_in is given); x_in: caller's residual
+//   stream (layers only); head: run final norm + lm_head + argmax (else only
+//   advance the length).
+void chain_b1(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in, int* next, float* logits, bool head) {
+  const Sizes& s = c->s;
+  const int wb = s.wb;
+  float* x = x_in ? x_in : c->resid;
+  cudaStream_t st = ln.s;
+  const bool pdl = ln.pdl;
+  if (!x_in)
+    ln.run(K2_K_EMBED, [&] { return launch_embed(c->embed, wb, s.V, s.H, tok, 1, x, c->guard, st, pdl); });
+  const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
+  const int splits = attn_splits(c, 1);
+  for (int l = 0; l < s.L; ++l) {
+    GemvArgs q = c->p_qkv;
+    q.W = c->wqkv(l);
+    q.x = x;
+    q.gain = c->attn_norm[l];
+    q.out = c->qkv;
+    q.seq = seq;
+    ln.run(K2_K_QKV, [&] { return launch_gemv(q, wb, EPI_QKV, c->grid_qkv, st, pdl); });
+
+    AttnArgs at = c->p_attn;
+    at.kc = at.kc_w = c->kc(l);
+    at.vc = at.vc_w = c->vc(l);
+    at.ks = c->ks(l);
+    at.vs = c->vs(l);
+    at.seq0 = seq;
+    ln.run(K2_K_ATTN, [&] { return launch_attn(at, s.d, s.rep, kvdt, splits, 1, st, pdl); });
+
+    GemvArgs o = c->p_o;
+    o.W = c->wo[l];
+    o.x = c->attn_out;
+    o.out = x;
+    ln.run(K2_K_OPROJ, [&] { return launch_gemv(o, wb, EPI_RESID, c->grid_o, st, pdl); });
+
+    GemvArgs gu = c->p_gu;
+    gu.W = c->wgu(l);
+    gu.x = x;
+    gu.gain = c->mlp_norm[l];
+    gu.out = c->act;
+    ln.run(K2_K_GATEUP, [&] { return launch_gemv(gu, wb, EPI_SWIGLU, c->grid_gu, st, pdl); });
+
+    GemvArgs dn = c->p_down;
+    dn.W = c->w_down[l];
+    dn.x = c->act;
+    dn.out = x;
+    ln.run(K2_K_DOWN, [&] { return launch_gemv(dn, wb, EPI_RESID, c->grid_down, st, pdl); });
+  }
+  if (head) {
+    GemvArgs lm = c->p_lm;
+    lm.x = x;
+    lm.logits = logits;
+    lm.next_token = next;
+    lm.counter = c->am_counter + seq;
+    lm.part_val = c->am_val + static_cast<size_t>(seq) * kArgmaxPartsMax;
+    lm.part_idx = c->am_idx + static_cast<size_t>(seq) * kArgmaxPartsMax;
+    lm.seq = seq;
+    lm.advance = 1;
+    ln.run(K2_K_LMHEAD, [&] { return launch_gemv(lm, wb, EPI_ARGMAX, c->grid_lm, st, pdl); });
+  } else {
+    ln.run(K2_K_EMBED, [&] { return launch_advance(c->seq_len, seq, 1, st, pdl); });
+  }
+}
+
+void enqueue_decode(k2_ctx* c, Launcher& ln, const int* d_tokens, int batch, int* d_next, float* d_logits) {
+  for (int b = 0; b < batch; ++b)
+    chain_b1(c, ln, b, d_tokens + b, nullptr, d_next + b,
+             d_logits ? d_logits + static_cast<size_t>(b) * c->s.V : nullptr, true);
+}
+
+bool plan_all(k2_ctx* c) {
+  const Sizes& s = c->s;
+  const int wb = s.wb;
+  GemvArgs base = {};
+  base.groups = s.G;
+  base.eps = c->cfg.eps;
+  base.rope = c->rope;
+  base.cap = c->lay.cap;
+  base.seq_len = c->seq_len;
+  base.head_dim = s.d;
+  base.n_rot_heads = s.nq + s.nkv;
+  base.guard = c->guard;
+  base.part_val = c->am_val;
+  base.part_idx = c->am_idx;
+  base.counter = c->am_counter;
+  auto grid_for = [&](const GemvArgs& a) {
+    const int units = a.N / a.align;
+    int g = c->sms;
+    if (g > units) g = units;
+    if (g > kArgmaxPartsMax) g = kArgmaxPartsMax;
+    return g < 1 ? 1 : g;
+  };
+  const void* dummy_gain = c->final_norm;  // any non-null: plans check the norm constraints
+  c->p_qkv = base; c->p_qkv.N = s.qkv_n; c->p_qkv.K = s.H; c->p_qkv.gain = dummy_gain;
+  c->p_o = base; c->p_o.N = s.H; c->p_o.K = s.nq * s.d;
+  c->p_gu = base; c->p_gu.N = 2 * s.I; c->p_gu.K = s.H; c->p_gu.gain = dummy_gain;
+  c->p_down = base; c->p_down.N = s.H; c->p_down.K = s.I;
+  c->p_lm = base; c->p_lm.N = s.V; c->p_lm.K = s.H; c->p_lm.W = c->lm_head; c->p_lm.gain = c->final_norm;
+  if (!gemv_plan(c->p_qkv, wb, EPI_QKV, kGemvSmem) || !gemv_plan(c->p_o, wb, EPI_RESID, kGemvSmem) ||
+      !gemv_plan(c->p_gu, wb, EPI_SWIGLU, kGemvSmem) || !gemv_plan(c->p_down, wb, EPI_RESID, kGemvSmem) ||
+      !gemv_plan(c->p_lm, wb, EPI_ARGMAX, kGemvSmem))
+    return false;
+  c->p_o.gain = nullptr;
+  c->p_down.gain = nullptr;
+  c->grid_qkv = grid_for(c->p_qkv);
+  c->grid_o = grid_for(c->p_o);
+  c->grid_gu = grid_for(c->p_gu);
+  c->grid_down = grid_for(c->p_down);
+  c->grid_lm = grid_for(c->p_lm);
+
+  AttnArgs& at = c->p_attn;
+  at = {};
+  at.cap = c->lay.cap;
+  at.qkv = c->qkv;
+  at.qkv_stride = s.qkv_n;
+  at.nq = s.nq;
+  at.nkv = s.nkv;
+  at.seq_len = c->seq_len;
+  at.part = c->attn_part;
+  at.counter = c->attn_counter;
+  at.out = c->attn_out;
+  at.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(s.d)));
+  const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
+  at.stage_bytes = static_cast<uint32_t>(attn_stage_bytes(s.d, kvdt));
+  int nst = static_cast<int>(kAttnSmem / at.stage_bytes);
+  if (nst > 4) nst = 4;
+  if (nst < 2) return false;
+  at.nstage = nst;
+  at.guard = c->guard;
+  c->attn_splits_b1 = attn_splits(c, 1);
+  return true;
+}
+
+k2_status validate_weights(k2_ctx* c, const k2_weights* w) {
+  auto ok = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % 16) == 0; };
+  if (!w) return c->fail(K2_ERR_ARG, "weights is NULL");
+  if (!ok(w->embed) || !ok(w->lm_head) || !ok(w->final_norm))
+    return c->fail(K2_ERR_ARG, "embed / lm_head / final_norm must be non-null 16-byte aligned device pointers");
+  const void* const* arrs[] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->mlp_norm, w->w_gate, w->w_up, w->w_down};
+  const char* names[] = {"attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down"};
+  for (int i = 0; i < 9; ++i) {
+    if (!arrs[i]) return c->fail(K2_ERR_ARG, "weights.%s is NULL", names[i]);
+    for (int l = 0; l < c->s.L; ++l)
+      if (!ok(arrs[i][l]))
+        return c->fail(K2_ERR_ARG, "weights.%s[%d] must be a non-null 16-byte aligned device pointer", names[i], l);
+  }
+  return K2_OK;
+}
+
+thread_local std::string g_init_error;
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+size_t k2_workspace_bytes(const k2_config* cfg) {
+  g_init_error = check_config(cfg);
+  if (!g_init_error.empty()) return 0;
+  return layout_of(*cfg).total;
+}
+
+k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_workspace, size_t ws_bytes, void* stream,
+                          k2_ctx** out) {
+  if (!out) return K2_ERR_ARG;
+  *out = nullptr;
+  const std::string why = check_config(cfg);
+  if (!why.empty()) {
+    g_init_error = why;
+    const bool shape = why.find("multiple") != std::string::npos || why.find("even") != std::string::npos;
+    return why.find("not built") != std::string::npos || why.find("not supported") != std::string::npos
+               ? K2_ERR_UNSUPPORTED
+               : (shape ? K2_ERR_SHAPE : K2_ERR_ARG);
+  }
+  k2_ctx* c = new k2_ctx();
+  c->cfg = *cfg;
+  c->s = sizes_of(*cfg);
+  c->lay = layout_of(*cfg);
+  k2_status st = validate_weights(c, w);
+  if (st != K2_OK) {
+    g_init_error = c->err;
+    delete c;
+    return st;
+  }
+  if (!d_workspace || reinterpret_cast<uintptr_t>(d_workspace) % kAlign) {
+    g_init_error = "workspace must be a non-null 256-byte aligned device pointer";
+    delete c;
+    return K2_ERR_WORKSPACE;
+  }
+  if (ws_bytes < c->lay.total) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "workspace too small: %zu bytes given, %zu needed", ws_bytes, c->lay.total);
+    g_init_error = buf;
+    delete c;
+    return K2_ERR_WORKSPACE;
+  }
+  c->sms = num_sms();
+  if (c->sms <= 0) {
+    g_init_error = "no CUDA device";
+    delete c;
+    return K2_ERR_CUDA;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  c->ws = ws;
+  c->seq_len = reinterpret_cast<int*>(ws + c->lay.seq_len);
+  c->guard = reinterpret_cast<unsigned*>(ws + c->lay.guard);
+  c->attn_counter = reinterpret_cast<unsigned*>(ws + c->lay.attn_counter);
+  c->am_counter = reinterpret_cast<unsigned*>(ws + c->lay.am_counter);
+  c->rope = reinterpret_cast<float2*>(ws + c->lay.rope);
+  c->resid = reinterpret_cast<float*>(ws + c->lay.resid);
+  c->qkv = reinterpret_cast<float*>(ws + c->lay.qkv);
+  c->attn_out = reinterpret_cast<float*>(ws + c->lay.attn_out);
+  c->act = reinterpret_cast<float*>(ws + c->lay.act);
+  c->attn_part = reinterpret_cast<float*>(ws + c->lay.attn_part);
+  c->am_val = reinterpret_cast<float*>(ws + c->lay.am_val);
+  c->am_idx = reinterpret_cast<int*>(ws + c->lay.am_idx);
+  c->embed = w->embed;
+  c->lm_head = w->lm_head;
+  c->final_norm = w->final_norm;
+  for (int l = 0; l < c->s.L; ++l) {
+    c->attn_norm.push_back(w->attn_norm[l]);
+    c->wo.push_back(w->wo[l]);
+    c->mlp_norm.push_back(w->mlp_norm[l]);
+    c->w_down.push_back(w->w_down[l]);
+  }
+  c->len.assign(c->s.B, 0);
+  if (!plan_all(c)) {
+    g_init_error = "no GEMV/attention tiling fits this shape";
+    delete c;
+    return K2_ERR_UNSUPPORTED;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if ((e = gemv_init_attrs()) || (e = attn_init_attrs())) {
+    g_init_error = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+    delete c;
+    return K2_ERR_CUDA;
+  }
+  // zero the state words (lengths, guard, counters) and build the rope table
+  if ((e = cudaMemsetAsync(ws, 0, c->lay.rope, s)) ||
+      (e = launch_rope_table(c->rope, c->lay.cap, c->s.d, static_cast<double>(cfg->rope_theta), s))) {
+    g_init_error = std::string("init: ") + cudaGetErrorString(e);
+    delete c;
+    return K2_ERR_CUDA;
+  }
+  for (int l = 0; l < c->s.L && e == cudaSuccess; ++l) {
+    e = launch_repack_qkv(c->wqkv(l), w->wq[l], w->wk[l], w->wv[l], c->s.wb, c->s.nq, c->s.nkv, c->s.d, c->s.H, s);
+    if (e == cudaSuccess) e = launch_repack_gateup(c->wgu(l), w->w_gate[l], w->w_up[l], c->s.wb, c->s.I, c->s.H, s);
+  }
+  if (e == cudaSuccess) e = cudaEventCreate(&c->ev[0]);
+  if (e == cudaSuccess) e = cudaEventCreate(&c->ev[1]);
+  if (e != cudaSuccess) {
+    g_init_error = std::string("repack: ") + cudaGetErrorString(e);
+    delete c;
+    return K2_ERR_CUDA;
+  }
+  *out = c;
+  return K2_OK;
+}
+
+void k2_free(k2_ctx* c) {
+  if (!c) return;
+  for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
+  if (c->ev[0]) cudaEventDestroy(c->ev[0]);
+  if (c->ev[1]) cudaEventDestroy(c->ev[1]);
+  delete c;
+}
+
+const char* k2_last_error(const k2_ctx* c) { return c ? c->err.c_str() : g_init_error.c_str(); }
+
+k2_status k2_get_info(const k2_ctx* c, k2_info* info) {
+  if (!c || !info) return K2_ERR_ARG;
+  info->kv_capacity = c->lay.cap;
+  info->num_sms = c->sms;
+  info->attn_splits = attn_splits(c, 1);
+  info->gemv_grid = c->grid_gu;
+  info->kv_bytes = static_cast<int64_t>(c->lay.kv_bytes);
+  info->repack_bytes = static_cast<int64_t>(c->lay.repack_bytes);
+  info->scratch_bytes = static_cast<int64_t>(c->lay.total - c->lay.kv_bytes - c->lay.repack_bytes);
+  return K2_OK;
+}
+
+k2_status k2_prefill(k2_ctx* c, int32_t seq, const int32_t* d_tokens, int32_t n, int32_t* d_next_token,
+                     float* d_logits, void* stream) {
+  if (!c) return K2_ERR_ARG;
+  if (seq < 0 || seq >= c->s.B) return c->fail(K2_ERR_ARG, "seq %d outside [0, %d)", seq, c->s.B);
+  if (n < 1) return c->fail(K2_ERR_ARG, "n must be >= 1 (got %d)", n);
+  if (!d_tokens || !d_next_token) return c->fail(K2_ERR_ARG, "d_tokens and d_next_token must be non-null");
+  if (static_cast<long long>(c->len[seq]) + n > c->s.ctx)
+    return c->fail(K2_ERR_CONTEXT_FULL, "prompt of %d tokens does not fit: sequence %d holds %d of %d", n, seq,
+                   c->len[seq], c->s.ctx);
+  Launcher ln{c, static_cast<cudaStream_t>(stream), c->pdl};
+  for (int i = 0; i < n; ++i) {
+    const bool last = i == n - 1;
+    chain_b1(c, ln, seq, d_tokens + i, nullptr, d_next_token, last ? d_logits : nullptr, last);
+  }
+  if (ln.err != cudaSuccess) return c->cuda_fail(ln.err, "prefill launch");
+  c->len[seq] += n;
+  return K2_OK;
+}
+
+k2_status k2_decode_step(k2_ctx* c, const int32_t* d_tokens, int32_t batch, int32_t* d_next, float* d_logits,
+                         void* stream) {
+  if (!c) return K2_ERR_ARG;
+  if (batch < 1 || batch > c->s.B) return c->fail(K2_ERR_ARG, "batch %d outside [1, %d]", batch, c->s.B);
+  if (!d_tokens || !d_next) return c->fail(K2_ERR_ARG, "d_tokens and d_next must be non-null");
+  for (int b = 0; b < batch; ++b)
+    if (c->len[b] >= c->s.ctx)
+      return c->fail(K2_ERR_CONTEXT_FULL, "sequence %d is at max_context %d", b, c->s.ctx);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c->graph) {
+    if (!s) return c->fail(K2_ERR_ARG, "graph mode needs a non-default stream");
+    auto key = std::make_tuple(batch, static_cast<const void*>(d_tokens), static_cast<const void*>(d_next),
+                               static_cast<const void*>(d_logits), stream);
+    auto it = c->graphs.find(key);
+    if (it == c->graphs.end()) {
+      cudaError_t e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+      if (e) return c->cuda_fail(e, "cudaStreamBeginCapture");
+      Launcher ln{c, s, c->pdl};
+      enqueue_decode(c, ln, d_tokens, batch, d_next, d_logits);
+      cudaGraph_t g = nullptr;
+      e = cudaStreamEndCapture(s, &g);
+      if (ln.err) {
+        if (g) cudaGraphDestroy(g);
+        return c->cuda_fail(ln.err, "decode capture");
+      }
+      if (e) return c->cuda_fail(e, "cudaStreamEndCapture");
+      cudaGraphExec_t ge = nullptr;
+      e = cudaGraphInstantiate(&ge, g, 0);
+      cudaGraphDestroy(g);
+      if (e) return c->cuda_fail(e, "cudaGraphInstantiate");
+      it = c->graphs.emplace(key, ge).first;
+    }
+    cudaError_t e = cudaGraphLaunch(it->second, s);
+    if (e) return c->cuda_fail(e, "cudaGraphLaunch");
+  } else {
+    Launcher ln{c, s, c->pdl};
+    enqueue_decode(c, ln, d_tokens, batch, d_next, d_logits);
+    if (ln.err) return c->cuda_fail(ln.err, "decode launch");
+  }
+  for (int b = 0; b < batch; ++b) c->len[b] += 1;
+  return K2_OK;
+}
+
+k2_status k2_decode_layers(k2_ctx* c, float* d_x, int32_t batch, void* stream) {
+  if (!c) return K2_ERR_ARG;
+  if (batch < 1 || batch > c->s.B) return c->fail(K2_ERR_ARG, "batch %d outside [1, %d]", batch, c->s.B);
+  if (!d_x || reinterpret_cast<uintptr_t>(d_x) % 16) return c->fail(K2_ERR_ARG, "d_x must be 16-byte aligned");
+  for (int b = 0; b < batch; ++b)
+    if (c->len[b] >= c->s.ctx)
+      return c->fail(K2_ERR_CONTEXT_FULL, "sequence %d is at max_context %d", b, c->s.ctx);
+  Launcher ln{c, static_cast<cudaStream_t>(stream), c->pdl};
+  for (int b = 0; b < batch; ++b)
+    chain_b1(c, ln, b, nullptr, d_x + static_cast<size_t>(b) * c->s.H, nullptr, nullptr, false);
+  if (ln.err) return c->cuda_fail(ln.err, "layers launch");
+  for (int b = 0; b < batch; ++b) c->len[b] += 1;
+  return K2_OK;
+}
+
+k2_status k2_kv_reset(k2_ctx* c, int32_t seq, void* stream) {
+  if (!c) return K2_ERR_ARG;
+  if (seq < -1 || seq >= c->s.B) return c->fail(K2_ERR_ARG, "seq %d outside [-1, %d)", seq, c->s.B);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (seq == -1) {
+    e = cudaMemsetAsync(c->seq_len, 0, sizeof(int) * c->s.B, s);
+    if (e) return c->cuda_fail(e, "kv_reset");
+    c->len.assign(c->s.B, 0);
+  } else {
+    e = cudaMemsetAsync(c->seq_len + seq, 0, sizeof(int), s);
+    if (e) return c->cuda_fail(e, "kv_reset");
+    c->len[seq] = 0;
+  }
+  return K2_OK;
+}
+
+k2_status k2_kv_set_len(k2_ctx* c, int32_t seq, int32_t len, void* stream) {
+  if (!c) return K2_ERR_ARG;
+  if (seq < 0 || seq >= c->s.B) return c->fail(K2_ERR_ARG, "seq %d outside [0, %d)", seq, c->s.B);
+  if (len < 0 || len > c->s.ctx) return c->fail(K2_ERR_CONTEXT_FULL, "len %d outside [0, %d]", len, c->s.ctx);
+  // a kernel-free host->device write of one int: pageable copies are staged
+  // synchronously by the driver, so the source may go out of scope
+  static thread_local int v;
+  v = len;
+  cudaError_t e = cudaMemcpyAsync(c->seq_len + seq, &v, sizeof(int), cudaMemcpyHostToDevice,
+                                  static_cast<cudaStream_t>(stream));
+  if (e) return c->cuda_fail(e, "kv_set_len");
+  e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e) return c->cuda_fail(e, "kv_set_len");
+  c->len[seq] = len;
+  return K2_OK;
+}
+
+k2_status k2_kv_view(k2_ctx* c, int32_t layer, int32_t seq, void** k, void** v, void** k_scale, void** v_scale,
+                     int32_t* len) {
+  if (!c) return K2_ERR_ARG;
+  if (layer < 0 || layer >= c->s.L || seq < 0 || seq >= c->s.B)
+    return c->fail(K2_ERR_ARG, "layer %d / seq %d out of range", layer, seq);
+  const size_t per_seq = static_cast<size_t>(c->s.nkv) * c->lay.cap;
+  const size_t off = static_cast<size_t>(seq) * per_seq;
+  if (k) *k = static_cast<uint8_t*>(c->kc(layer)) + off * c->s.d * c->s.kvb;
+  if (v) *v = static_cast<uint8_t*>(c->vc(layer)) + off * c->s.d * c->s.kvb;
+  if (k_scale) *k_scale = c->ks(layer) ? static_cast<uint8_t*>(c->ks(layer)) + off * 2 : nullptr;
+  if (v_scale) *v_scale = c->vs(layer) ? static_cast<uint8_t*>(c->vs(layer)) + off * 2 : nullptr;
+  if (len) *len = c->len[seq];
+  return K2_OK;
+}
+
+k2_status k2_hidden_view(k2_ctx* c, int32_t b, float** d_x) {
+  if (!c || !d_x) return K2_ERR_ARG;
+  if (b < 0 || b >= c->s.B) return c->fail(K2_ERR_ARG, "slot %d out of range", b);
+  *d_x = c->resid + static_cast<size_t>(b) * c->s.H;
+  return K2_OK;
+}
+
+k2_status k2_sync_status(k2_ctx* c, void* stream) {
+  if (!c) return K2_ERR_ARG;
+  unsigned g = 0;
+  cudaError_t e = cudaMemcpyAsync(&g, c->guard, sizeof g, cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream));
+  if (!e) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e) return c->cuda_fail(e, "sync_status");
+  if (g == 0) return K2_OK;
+  std::string why;
+  if (g & GUARD_TOKEN) why += " token-id-out-of-range";
+  if (g & GUARD_TIMEOUT) why += " bounded-wait-timeout";
+  if (g & GUARD_NAN) why += " nan-logit";
+  if (g & GUARD_POS) why += " position-outside-cache";
+  return c->fail(K2_ERR_DEVICE_GUARD, "device guard 0x%x:%s", g, why.c_str());
+}
+
+k2_status k2_clear_status(k2_ctx* c, void* stream) {
+  if (!c) return K2_ERR_ARG;
+  cudaError_t e = cudaMemsetAsync(c->guard, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream));
+  if (e) return c->cuda_fail(e, "clear_status");
+  return K2_OK;
+}
+
+k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
+  if (!c) return K2_ERR_ARG;
+  switch (option) {
+    case K2_OPT_PDL: c->pdl = value != 0; break;
+    case K2_OPT_GRAPH: c->graph = value != 0; break;
+    case K2_OPT_ATTN_SPLITS:
+      if (value < 0 || value > kSplitMax) return c->fail(K2_ERR_ARG, "splits %lld outside [0, %d]", (long long)value, kSplitMax);
+      c->force_splits = static_cast<int>(value);
+      break;
+    default: return c->fail(K2_ERR_ARG, "unknown option %d", option);
+  }
+  for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
+  c->graphs.clear();
+  return K2_OK;
+}
+
+k2_status k2_profile_decode(k2_ctx* c, const int32_t* d_tokens, int32_t batch, int32_t* d_next, float* ms,
+                            int32_t* launches, void* stream) {
+  if (!c || !ms || !launches) return K2_ERR_ARG;
+  if (batch < 1 || batch > c->s.B) return c->fail(K2_ERR_ARG, "batch %d outside [1, %d]", batch, c->s.B);
+  if (!d_tokens || !d_next) return c->fail(K2_ERR_ARG, "d_tokens and d_next must be non-null");
+  for (int b = 0; b < batch; ++b)
+    if (c->len[b] >= c->s.ctx)
+      return c->fail(K2_ERR_CONTEXT_FULL, "sequence %d is at max_context %d", b, c->s.ctx);
+  Launcher ln{c, static_cast<cudaStream_t>(stream), false, ms, launches};
+  enqueue_decode(c, ln, d_tokens, batch, d_next, nullptr);
+  if (ln.err) return c->cuda_fail(ln.err, "profile launch");
+  for (int b = 0; b < batch; ++b) c->len[b] += 1;
+  return K2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// Argument blocks and launchers of the sm_103a kernels (internal to libk2).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace k2 {
+
+// bits of the device guard word (read back by k2_sync_status)
+enum : uint32_t {
+  GUARD_TOKEN = 1u,    // a token id outside [0, vocab)
+  GUARD_TIMEOUT = 2u,  // a bounded wait ran out
+  GUARD_NAN = 4u,      // a NaN logit
+  GUARD_POS = 8u,      // a position outside the cache
+};
+
+// ---------------------------------------------------------------------------
+// streaming GEMV: y = W . norm(x), W [N, K] row-major, one fp32 vector x
+// ---------------------------------------------------------------------------
+enum GemvEpi : int {
+  EPI_STORE = 0,   // out[row] = y
+  EPI_RESID = 1,   // out[row] += y   (residual add, in place)
+  EPI_QKV = 2,     // row pairs (i, i + d/2) of a head -> split-half RoPE -> out
+  EPI_SWIGLU = 3,  // row pairs (gate_i, up_i) -> out[i] = silu(gate) * up
+  EPI_ARGMAX = 4,  // logits (optional store) + first-index argmax -> token
+};
+
+struct GemvArgs {
+  const void* W;
+  int N, K;
+  const float* x;       // [K]
+  const void* gain;     // [K] norm gain in the weight dtype, or null (no norm)
+  int groups;
+  float eps;
+  // tiling (host-chosen)
+  int R;       // rows per stage
+  int nslice;  // K slices; R * nslice == 8 warps
+  int kc;      // 16-byte chunks per lane per slice (<= kGemvKcMax)
+  int align;   // CTA row ranges are multiples of this (2 for pair epilogues)
+  int nstage;  // ring depth
+  uint32_t stage_bytes;
+  // epilogue
+  float* out;
+  const float2* rope;  // [cap][d/2] (cos, sin)
+  int cap;             // rows of the rope table (positions 0 .. cap-1)
+  int* seq_len;        // position of the token = seq_len[seq] (advanced by EPI_ARGMAX)
+  int seq;
+  int head_dim;
+  int n_rot_heads;  // heads [0, n_rot_heads) are rotated (q and k), the rest (v) are not
+  // argmax
+  float* logits;      // nullable
+  float* part_val;    // [gridDim]
+  int* part_idx;      // [gridDim]
+  unsigned* counter;  // zero between launches
+  int* next_token;    // where the token goes
+  int advance;        // last CTA does seq_len[seq] += 1
+  unsigned* guard;
+};
+constexpr int kGemvKcMax = 10;
+constexpr int kGemvThreads = 256;
+
+// chooses R / nslice / kc / stages for a weight shape; false if unsupported
+bool gemv_plan(GemvArgs& a, int wbytes, int epi, size_t smem_budget);
+cudaError_t gemv_init_attrs();
+cudaError_t launch_gemv(const GemvArgs& a, int wbytes, int epi, int grid, cudaStream_t s, bool pdl);
+size_t gemv_smem_bytes(const GemvArgs& a);
+
+// ---------------------------------------------------------------------------
+// split-K flash-decode GQA attention with the KV append of the new token
+// ---------------------------------------------------------------------------
+struct AttnArgs {
+  const void* kc;  // K cache of this layer: [batch][nkv][cap][D] in the KV dtype
+  const void* vc;
+  void* kc_w;  // same pointers, written at row pos
+  void* vc_w;
+  void* ks;  // int8 scales [batch][nkv][cap] fp16 (null otherwise)
+  void* vs;
+  int cap;
+  const float* qkv;  // [batch][qkv_stride] fp32: q (nq*D, rotated) | k (nkv*D, rotated) | v (nkv*D)
+  int qkv_stride;
+  int nq, nkv;
+  const int* seq_len;
+  int seq0;          // sequences seq0 .. seq0 + gridDim.z - 1
+  float* part;       // [batch][nkv][nsplit][REP*(D+2)]
+  unsigned* counter; // [batch][nkv]
+  float* out;        // [batch][nq*D]
+  float scale;       // 1/sqrt(D)
+  int nstage;
+  uint32_t stage_bytes;
+  unsigned* guard;
+};
+constexpr int kAttnThreads = 256;
+constexpr int kAttnTK = 64;  // keys per tile
+
+bool attn_supported(int head_dim, int rep, int kv_dtype);
+size_t attn_stage_bytes(int head_dim, int kv_dtype);
+cudaError_t attn_init_attrs();
+cudaError_t launch_attn(const AttnArgs& a, int head_dim, int rep, int kv_dtype, int nsplit, int batch,
+                        cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------------------
+// small kernels
+// ---------------------------------------------------------------------------
+cudaError_t launch_embed(const void* E, int wbytes, int vocab, int hidden, const int* tokens, int batch,
+                         float* resid, unsigned* guard, cudaStream_t s, bool pdl);
+cudaError_t launch_rope_table(float2* tab, int cap, int head_dim, double theta, cudaStream_t s);
+cudaError_t launch_repack_qkv(void* dst, const void* wq, const void* wk, const void* wv, int wbytes, int nq,
+                              int nkv, int d, int hidden, cudaStream_t s);
+cudaError_t launch_repack_gateup(void* dst, const void* wg, const void* wu, int wbytes, int inter, int hidden,
+                                 cudaStream_t s);
+cudaError_t launch_advance(int* seq_len, int seq0, int batch, cudaStream_t s, bool pdl);
+
+}  // namespace k2

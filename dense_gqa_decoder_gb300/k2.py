@@ -1,0 +1,211 @@
+"""Thin ctypes binding of libk2 (include/k2.h).
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels of libk2.so.  torch is used for device memory and streams.  If the
+library is missing the import fails loudly -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libk2.so")
+
+K2_OK, K2_ERR_ARG, K2_ERR_SHAPE, K2_ERR_UNSUPPORTED, K2_ERR_TOKEN_RANGE, K2_ERR_CONTEXT_FULL, \
+    K2_ERR_WORKSPACE, K2_ERR_CUDA, K2_ERR_DEVICE_GUARD = range(9)
+K2_F32, K2_BF16, K2_F16, K2_I8 = range(4)
+K2_OPT_PDL, K2_OPT_GRAPH, K2_OPT_ATTN_SPLITS = range(3)
+KERNEL_CLASSES = ("embed", "qkv", "attn", "o_proj", "gate_up", "down", "lm_head")
+DTYPES = {"f32": K2_F32, "bf16": K2_BF16, "f16": K2_F16, "i8": K2_I8}
+
+
+class K2Error(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"k2 status {status}: {msg}")
+        self.status = status
+
+
+class Config(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in (
+        "hidden", "n_layers", "n_heads", "n_kv_heads", "head_dim", "intermediate", "norm_groups", "vocab",
+        "max_context", "max_batch")] + [("eps", C.c_float), ("rope_theta", C.c_float),
+                                        ("weight_dtype", C.c_int32), ("kv_dtype", C.c_int32)]
+
+
+_PP = C.POINTER(C.c_void_p)
+
+
+class Weights(C.Structure):
+    _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("final_norm", C.c_void_p)] + [
+        (n, _PP) for n in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down")]
+
+
+class Info(C.Structure):
+    _fields_ = [("kv_capacity", C.c_int32), ("num_sms", C.c_int32), ("attn_splits", C.c_int32),
+                ("gemv_grid", C.c_int32), ("kv_bytes", C.c_int64), ("repack_bytes", C.c_int64),
+                ("scratch_bytes", C.c_int64)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libk2.so is not built ({LIB_PATH}); run dense_gqa_decoder_gb300.build")
+    lib = C.CDLL(LIB_PATH)
+    vp, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
+    sig = {
+        "k2_workspace_bytes": (C.c_size_t, [C.POINTER(Config)]),
+        "k2_init_weights": (C.c_int, [C.POINTER(Config), C.POINTER(Weights), vp, C.c_size_t, vp, C.POINTER(vp)]),
+        "k2_free": (None, [vp]),
+        "k2_last_error": (C.c_char_p, [vp]),
+        "k2_get_info": (C.c_int, [vp, C.POINTER(Info)]),
+        "k2_prefill": (C.c_int, [vp, i32, vp, i32, vp, vp, vp]),
+        "k2_decode_step": (C.c_int, [vp, vp, i32, vp, vp, vp]),
+        "k2_decode_layers": (C.c_int, [vp, vp, i32, vp]),
+        "k2_kv_reset": (C.c_int, [vp, i32, vp]),
+        "k2_kv_set_len": (C.c_int, [vp, i32, i32, vp]),
+        "k2_kv_view": (C.c_int, [vp, i32, i32, C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), C.POINTER(vp),
+                                 C.POINTER(i32)]),
+        "k2_hidden_view": (C.c_int, [vp, i32, C.POINTER(vp)]),
+        "k2_sync_status": (C.c_int, [vp, vp]),
+        "k2_clear_status": (C.c_int, [vp, vp]),
+        "k2_set_option": (C.c_int, [vp, i32, i64]),
+        "k2_profile_decode": (C.c_int, [vp, vp, i32, vp, C.POINTER(C.c_float), C.POINTER(i32), vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+LIB = _load()
+EXPORTED = ("k2_workspace_bytes", "k2_init_weights", "k2_free", "k2_last_error", "k2_get_info", "k2_prefill",
+            "k2_decode_step", "k2_decode_layers", "k2_kv_reset", "k2_kv_set_len", "k2_kv_view", "k2_hidden_view",
+            "k2_sync_status", "k2_clear_status", "k2_set_option", "k2_profile_decode")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_config(shape, max_context: int, max_batch: int = 1, kv_dtype: str = "f16") -> Config:
+    return Config(hidden=shape.hidden, n_layers=shape.n_layers, n_heads=shape.n_heads, n_kv_heads=shape.n_kv_heads,
+                  head_dim=shape.head_dim, intermediate=shape.intermediate, norm_groups=shape.norm_groups,
+                  vocab=shape.vocab, max_context=max_context, max_batch=max_batch, eps=shape.eps,
+                  rope_theta=shape.rope_theta, weight_dtype=DTYPES[shape.weight_dtype], kv_dtype=DTYPES[kv_dtype])
+
+
+def workspace_bytes(cfg: Config) -> int:
+    return int(LIB.k2_workspace_bytes(C.byref(cfg)))
+
+
+class Context:
+    """Owns a k2_ctx plus the torch tensors whose memory it uses (workspace,
+    weights).  Methods mirror the C calls of the same name (k2_ prefix dropped)."""
+
+    def __init__(self, cfg: Config, weights: dict, stream=None):
+        self.cfg = cfg
+        self.weights = weights  # keeps device memory alive
+        nbytes = workspace_bytes(cfg)
+        if nbytes == 0:
+            raise K2Error(K2_ERR_ARG, "invalid config: " + (LIB.k2_last_error(None) or b"").decode())
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        L = cfg.n_layers
+        arrs = {}
+        for n in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down"):
+            arrs[n] = (C.c_void_p * L)(*[_ptr(weights[n][l]) for l in range(L)])
+        self._arrs = arrs
+        w = Weights(embed=_ptr(weights["embed"]), lm_head=_ptr(weights["lm_head"]),
+                    final_norm=_ptr(weights["final_norm"]),
+                    **{n: C.cast(a, _PP) for n, a in arrs.items()})
+        ctx = C.c_void_p()
+        st = LIB.k2_init_weights(C.byref(cfg), C.byref(w), _ptr(self.workspace), nbytes, _stream(stream),
+                                 C.byref(ctx))
+        if st != K2_OK:
+            raise K2Error(st, (LIB.k2_last_error(None) or b"").decode())
+        self.ctx = ctx
+
+    def __del__(self):
+        ctx = getattr(self, "ctx", None)
+        if ctx:
+            LIB.k2_free(ctx)
+            self.ctx = None
+
+    def _check(self, st):
+        if st != K2_OK:
+            raise K2Error(st, LIB.k2_last_error(self.ctx).decode())
+
+    def last_error(self) -> str:
+        return LIB.k2_last_error(self.ctx).decode()
+
+    def info(self) -> Info:
+        i = Info()
+        self._check(LIB.k2_get_info(self.ctx, C.byref(i)))
+        return i
+
+    def prefill(self, seq, tokens, next_token, logits=None, stream=None):
+        self._check(LIB.k2_prefill(self.ctx, seq, _ptr(tokens), tokens.numel(), _ptr(next_token), _ptr(logits),
+                                   _stream(stream)))
+
+    def decode_step(self, tokens, batch, next_tokens, logits=None, stream=None):
+        self._check(LIB.k2_decode_step(self.ctx, _ptr(tokens), batch, _ptr(next_tokens), _ptr(logits),
+                                       _stream(stream)))
+
+    def decode_layers(self, x, batch, stream=None):
+        self._check(LIB.k2_decode_layers(self.ctx, _ptr(x), batch, _stream(stream)))
+
+    def kv_reset(self, seq=-1, stream=None):
+        self._check(LIB.k2_kv_reset(self.ctx, seq, _stream(stream)))
+
+    def kv_set_len(self, seq, n, stream=None):
+        self._check(LIB.k2_kv_set_len(self.ctx, seq, n, _stream(stream)))
+
+    def kv_view(self, layer, seq):
+        k, v, ks, vs = C.c_void_p(), C.c_void_p(), C.c_void_p(), C.c_void_p()
+        n = C.c_int32()
+        self._check(LIB.k2_kv_view(self.ctx, layer, seq, C.byref(k), C.byref(v), C.byref(ks), C.byref(vs),
+                                   C.byref(n)))
+        return k.value, v.value, ks.value, vs.value, n.value
+
+    def hidden_view(self, b=0):
+        p = C.c_void_p()
+        self._check(LIB.k2_hidden_view(self.ctx, b, C.byref(p)))
+        return p.value
+
+    def sync_status(self, stream=None):
+        return LIB.k2_sync_status(self.ctx, _stream(stream))
+
+    def clear_status(self, stream=None):
+        self._check(LIB.k2_clear_status(self.ctx, _stream(stream)))
+
+    def set_option(self, opt, value):
+        self._check(LIB.k2_set_option(self.ctx, opt, value))
+
+    def profile_decode(self, tokens, batch, next_tokens, stream=None):
+        ms = (C.c_float * len(KERNEL_CLASSES))()
+        n = (C.c_int32 * len(KERNEL_CLASSES))()
+        self._check(LIB.k2_profile_decode(self.ctx, _ptr(tokens), batch, _ptr(next_tokens), ms, n,
+                                          _stream(stream)))
+        return dict(zip(KERNEL_CLASSES, ms)), dict(zip(KERNEL_CLASSES, n))
+
+
+def device_view(ptr: int, numel: int, dtype: torch.dtype) -> torch.Tensor:
+    """A torch tensor over device memory inside a k2 workspace (test hooks)."""
+    storage_bytes = numel * torch.empty((), dtype=dtype).element_size()
+
+    class _Holder:
+        __cuda_array_interface__ = {
+            "shape": (storage_bytes,), "typestr": "|u1", "data": (ptr, False), "version": 3}
+    return torch.as_tensor(_Holder(), device="cuda").view(dtype)[:numel]

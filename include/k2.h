@@ -1,0 +1,212 @@
+/*
+ * k2.h -- C ABI of libk2, the GB300 (sm_103a) token-generation hot path of a
+ * dense decoder-only GQA transformer of the K2-Horizon-3.7B shape.
+ *
+ * What the calls compute is the model of the k2-burn README:
+ *   - "Model shape": hidden 2560, 36 layers, 32 query heads over 8 KV heads
+ *     (GQA, 4x repeat), head_dim 128, SwiGLU intermediate 10240,
+ *     layernorm_num_groups 2, vocab 250624, rms_norm_eps 1e-6, untied lm_head;
+ *   - "Status: v0": GroupedRMSNorm, split-half RoPE, GQA attention, SwiGLU MLP,
+ *     a preallocated per-layer KV cache with a configurable context window and
+ *     storage dtype, prefill + single-token decode, temperature 0 = greedy
+ *     argmax;
+ *   - "KV cache storage": the context bounds the cache; a prompt that does not
+ *     fit is rejected, not truncated; KV stored as fp32, f16, or symmetric int8
+ *     with per-row fp16 scales;
+ *   - "Project layout": decoder layer = norm+attn residual, norm+mlp residual;
+ *     model = embed -> layers -> norm -> lm_head.
+ * The error conventions follow kimi-k3-in-c k3_run.c: refuse rather than
+ * clamp (argument validation), and never hand back an output that was not
+ * written (forward failure / "RUN INVALID").
+ *
+ * Conventions common to every call:
+ *   - Pointers named d_* and every weight pointer are DEVICE pointers of the
+ *     current CUDA device; all other pointers are host pointers.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued asynchronously on it; outputs are valid once
+ *     the stream has reached the end of the call's work.
+ *   - The library allocates no device memory.  The caller provides the
+ *     workspace (k2_workspace_bytes) and every input/output buffer, and keeps
+ *     them alive until k2_free.  Weights passed to k2_init_weights are used in
+ *     place (except Wq/Wk/Wv and W_gate/W_up, which are repacked into the
+ *     workspace) and must also outlive the context.
+ *   - A non-zero k2_status means the call had no effect on the context and
+ *     enqueued no work; k2_last_error(ctx) says why.  Faults detected on the
+ *     device (a token id outside the vocabulary, a NaN logit, a bounded wait
+ *     that ran out) never trap: they set a device guard word that
+ *     k2_sync_status reports.
+ */
+#ifndef K2_H
+#define K2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  K2_OK = 0,
+  K2_ERR_ARG = 1,          /* null pointer, bad index, bad option */
+  K2_ERR_SHAPE = 2,        /* inconsistent shape (e.g. hidden % norm_groups != 0) */
+  K2_ERR_UNSUPPORTED = 3,  /* a shape/dtype the kernels are not built for */
+  K2_ERR_TOKEN_RANGE = 4,  /* reserved for host-checked token ids */
+  K2_ERR_CONTEXT_FULL = 5, /* the tokens do not fit the remaining context */
+  K2_ERR_WORKSPACE = 6,    /* workspace missing, misaligned or too small */
+  K2_ERR_CUDA = 7,         /* a CUDA runtime call failed */
+  K2_ERR_DEVICE_GUARD = 8  /* the device guard word is set (k2_sync_status) */
+} k2_status;
+
+typedef enum { K2_F32 = 0, K2_BF16 = 1, K2_F16 = 2, K2_I8 = 3 } k2_dtype;
+
+/* Model shape and run limits (k2-burn README, "Model shape" and "KV cache
+ * storage").  weight_dtype is K2_F32 or K2_BF16; kv_dtype is K2_F32, K2_F16
+ * or K2_I8.  max_context = KV rows per sequence (prompt + generated tokens);
+ * max_batch = number of independent sequences. */
+typedef struct {
+  int32_t hidden, n_layers, n_heads, n_kv_heads, head_dim, intermediate, norm_groups, vocab;
+  int32_t max_context, max_batch;
+  float eps, rope_theta;
+  int32_t weight_dtype, kv_dtype;
+} k2_config;
+
+/* Device pointers to the weights, nn.Linear layout [out_features, in_features],
+ * row-major, in weight_dtype.  The per-layer members are HOST arrays of
+ * n_layers device pointers.  Shapes: embed, lm_head [vocab, hidden];
+ * *_norm [hidden]; wq [n_heads*head_dim, hidden]; wk, wv
+ * [n_kv_heads*head_dim, hidden]; wo [hidden, n_heads*head_dim];
+ * w_gate, w_up [intermediate, hidden]; w_down [hidden, intermediate].
+ * Every pointer must be 16-byte aligned. */
+typedef struct {
+  const void* embed;
+  const void* lm_head;
+  const void* final_norm;
+  const void* const* attn_norm;
+  const void* const* wq;
+  const void* const* wk;
+  const void* const* wv;
+  const void* const* wo;
+  const void* const* mlp_norm;
+  const void* const* w_gate;
+  const void* const* w_up;
+  const void* const* w_down;
+} k2_weights;
+
+typedef struct k2_ctx k2_ctx;
+
+/* Facts about a context, for tests and measurement. */
+typedef struct {
+  int32_t kv_capacity;   /* allocated KV rows per sequence (>= max_context) */
+  int32_t num_sms;
+  int32_t attn_splits;   /* key-range splits of the batch-1 attention launch */
+  int32_t gemv_grid;     /* CTAs of the batch-1 GEMV launches */
+  int64_t kv_bytes;      /* bytes of the KV cache region */
+  int64_t repack_bytes;  /* bytes of the repacked QKV and gate/up weights */
+  int64_t scratch_bytes; /* everything else in the workspace */
+} k2_info;
+
+/* ---- set-up -------------------------------------------------------------- */
+
+/* Bytes of workspace k2_init_weights needs for this config on the current
+ * device: repacked weights + KV cache + rope table + activations.  0 if the
+ * config is invalid or unsupported (k2_init_weights then says why). */
+size_t k2_workspace_bytes(const k2_config* cfg);
+
+/* Validates the config (kimi-k3-in-c k3_run.c: an untrusted config aborts
+ * rather than falls back; k2-burn README "Limitations": out-of-scope
+ * checkpoints hard-error), carves the workspace (256-byte aligned, at least
+ * k2_workspace_bytes), repacks the fused QKV and interleaved gate/up weights
+ * into it, builds the RoPE table and zeroes the sequence lengths.  Enqueued on
+ * `stream`.  On success *out owns host memory only; release with k2_free. */
+k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_workspace, size_t ws_bytes,
+                          void* stream, k2_ctx** out);
+
+/* Releases the host-side context.  The workspace is the caller's. */
+void k2_free(k2_ctx* ctx);
+
+/* Message of the last failed call on this context ("" if none). */
+const char* k2_last_error(const k2_ctx* ctx);
+
+k2_status k2_get_info(const k2_ctx* ctx, k2_info* info);
+
+/* ---- the hot path --------------------------------------------------------- */
+
+/* Prefill: appends the n tokens d_tokens[0..n) to sequence `seq` at its
+ * current length (k2-burn README, "Status: v0": prefill + single-token decode)
+ * and writes the greedy next token (first index of the max logit, kimi-k3-in-c
+ * k3_run.c `argmax_`) to *d_next_token.  If d_logits is not NULL, the last
+ * position's fp32 logits [vocab] are written there (kimi-k3-in-c k3_run.c:
+ * `forward` returns last-position logits).  K2_ERR_CONTEXT_FULL if
+ * length + n > max_context: the prompt is rejected, not truncated. */
+k2_status k2_prefill(k2_ctx* ctx, int32_t seq, const int32_t* d_tokens, int32_t n, int32_t* d_next_token,
+                     float* d_logits, void* stream);
+
+/* One decode step for sequences 0..batch-1: sequence b consumes d_tokens[b]
+ * at position length(b), appends its K/V, and gets its greedy next token in
+ * d_next[b] (logits in d_logits[b*vocab ..] if d_logits is not NULL).
+ * d_next may equal d_tokens (the step then feeds itself when replayed).
+ * K2_ERR_CONTEXT_FULL if any of the sequences is at max_context. */
+k2_status k2_decode_step(k2_ctx* ctx, const int32_t* d_tokens, int32_t batch, int32_t* d_next, float* d_logits,
+                         void* stream);
+
+/* The decoder layers alone for one new token per sequence: d_x [batch, hidden]
+ * fp32 is the residual stream entering layer 0 and is overwritten with the
+ * residual leaving the last layer.  K/V are appended and lengths advance as
+ * in k2_decode_step; no embedding, final norm or lm_head. */
+k2_status k2_decode_layers(k2_ctx* ctx, float* d_x, int32_t batch, void* stream);
+
+/* ---- cache management ------------------------------------------------------ */
+
+/* Sets the length of sequence `seq` (or of all sequences, seq = -1) to 0.
+ * Memory is not cleared. */
+k2_status k2_kv_reset(k2_ctx* ctx, int32_t seq, void* stream);
+
+/* Sets the length of sequence `seq` to len (0 <= len <= max_context): rows
+ * 0..len-1 are taken to be valid (e.g. filled through k2_kv_view). */
+k2_status k2_kv_set_len(k2_ctx* ctx, int32_t seq, int32_t len, void* stream);
+
+/* Device pointers of the cache of (layer, seq): K and V are
+ * [n_kv_heads][kv_capacity][head_dim] in kv_dtype; for K2_I8 the fp16 row
+ * scales are [n_kv_heads][kv_capacity] (NULL otherwise).  *len = current
+ * length (host view). */
+k2_status k2_kv_view(k2_ctx* ctx, int32_t layer, int32_t seq, void** k, void** v, void** k_scale, void** v_scale,
+                     int32_t* len);
+
+/* Device pointer of the fp32 residual stream of launch slot b ([hidden]); after
+ * a decode step it holds the residual leaving the last layer for sequence b
+ * (before the final norm). */
+k2_status k2_hidden_view(k2_ctx* ctx, int32_t b, float** d_x);
+
+/* ---- status, options, measurement ------------------------------------------- */
+
+/* Waits for `stream` and reads the device guard word: K2_OK if clear,
+ * K2_ERR_DEVICE_GUARD (with the reasons in k2_last_error) otherwise. */
+k2_status k2_sync_status(k2_ctx* ctx, void* stream);
+
+/* Clears the device guard word (enqueued on stream). */
+k2_status k2_clear_status(k2_ctx* ctx, void* stream);
+
+typedef enum {
+  K2_OPT_PDL = 0,         /* 1 (default): programmatic dependent launch between kernels */
+  K2_OPT_GRAPH = 1,       /* 1: k2_decode_step records a CUDA graph per (batch, buffers,
+                             stream) on first use and replays it (stream must not be NULL) */
+  K2_OPT_ATTN_SPLITS = 2  /* > 0: force the number of attention key splits (tests) */
+} k2_option;
+k2_status k2_set_option(k2_ctx* ctx, int32_t option, int64_t value);
+
+/* Kernel classes timed by k2_profile_decode. */
+enum { K2_K_EMBED = 0, K2_K_QKV, K2_K_ATTN, K2_K_OPROJ, K2_K_GATEUP, K2_K_DOWN, K2_K_LMHEAD, K2_K_COUNT };
+
+/* One decode step (as k2_decode_step) launched without graph or PDL, with a
+ * CUDA event pair around every kernel; waits for the stream and adds the
+ * measured milliseconds of each kernel class to ms[K2_K_COUNT] and the number
+ * of launches to launches[K2_K_COUNT]. */
+k2_status k2_profile_decode(k2_ctx* ctx, const int32_t* d_tokens, int32_t batch, int32_t* d_next, float* ms,
+                            int32_t* launches, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K2_H */

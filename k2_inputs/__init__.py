@@ -154,24 +154,47 @@ class Tensor:
     values: np.ndarray
 
 
+def _chunked(n: int, fn):
+    """Runs fn(lo, hi, chunk_index) over 4 Mi-element chunks, in threads."""
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+    jobs = [(c * _CHUNK, min(n, (c + 1) * _CHUNK), c) for c in range(nchunks)]
+    if nchunks <= 1:
+        for j in jobs:
+            fn(*j)
+    else:
+        list(_pool().map(lambda j: fn(*j), jobs))
+
+
 def weight(s: ModelShape, name: str, layer: int = -1, seed: int = 0,
            scale: float = 0.02, gain_scale: float = 0.0) -> Tensor:
     shape = tensor_shape(s, name)
     n = int(np.prod(shape))
-    if name.endswith("norm"):
-        if gain_scale > 0:
-            v = 1.0 + normal_f32(seed, tensor_id(s, name, layer), n) * np.float32(gain_scale)
+    tid = tensor_id(s, name, layer)
+    is_norm = name.endswith("norm")
+    bf16 = s.weight_dtype == "bf16"
+    assert bf16 or s.weight_dtype == "f32"
+    values = np.empty(n, dtype=np.float32)
+    stored = np.empty(n, dtype=np.uint16) if bf16 else values
+
+    def fill(lo, hi, c):
+        if is_norm and gain_scale <= 0:
+            v = np.ones(hi - lo, dtype=np.float32)
         else:
-            v = np.ones(n, dtype=np.float32)
-    else:
-        v = normal_f32(seed, tensor_id(s, name, layer), n)
-        v *= np.float32(scale)
-    v = v.reshape(shape)
-    if s.weight_dtype == "bf16":
-        bits = bf16_bits(v)
-        return Tensor(stored=bits, values=bf16_to_f32(bits))
-    assert s.weight_dtype == "f32"
-    return Tensor(stored=v, values=v)
+            g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tid, c])))
+            v = g.standard_normal(hi - lo, dtype=np.float32)
+            if is_norm:
+                v = np.float32(1.0) + v * np.float32(gain_scale)
+            else:
+                v *= np.float32(scale)
+        if bf16:
+            b = bf16_bits(v)
+            stored[lo:hi] = b
+            values[lo:hi] = bf16_to_f32(b)
+        else:
+            values[lo:hi] = v
+
+    _chunked(n, fill)
+    return Tensor(stored=stored.reshape(shape), values=values.reshape(shape))
 
 
 def prompt_ids(vocab: int, n: int, seed: int = 1) -> np.ndarray:

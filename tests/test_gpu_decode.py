@@ -1,0 +1,238 @@
+"""Parity of the CUDA decode path (through the C ABI) with the CPU oracle.
+
+Tolerances (written here, derived in the design doc):
+  * fp32 tiny model: greedy tokens identical, logits max-abs <= 1e-4;
+  * bf16 weights + fp16 KV: hidden-state relative L2 <= 2e-2 and teacher-forced
+    argmax agreement >= 99%; the kernels keep fp32 activations, so the tests
+    also hold them to a much tighter bound that catches real bugs;
+  * int8 KV: relative L2 <= 5e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import k2_inputs as ki
+from oracle import k2_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def k2():
+    from dense_gqa_decoder_gb300 import k2 as mod
+    return mod
+
+
+@pytest.fixture(scope="module")
+def mio():
+    from dense_gqa_decoder_gb300 import model_io
+    return model_io
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def run_greedy(ctx, prompt, n_new, vocab, seq=0):
+    d_prompt = torch.tensor(prompt, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    logits = torch.empty(vocab, dtype=torch.float32, device="cuda")
+    ctx.prefill(seq, d_prompt, nxt, logits)
+    toks, lgs = [int(nxt.item())], [logits.cpu().numpy().copy()]
+    for _ in range(n_new):
+        ctx.decode_step(nxt, 1, nxt, logits)
+        toks.append(int(nxt.item()))
+        lgs.append(logits.cpu().numpy().copy())
+    return np.array(toks), np.stack(lgs)
+
+
+# ---------------------------------------------------------------------------
+# tiny fp32 model: 16 prompt ids, then 16 greedy steps, fp32 KV
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_tiny_fp32_greedy_matches_oracle(k2, mio, splits):
+    s = ki.TINY
+    ctx, host = mio.build_context(s, max_context=32, kv_dtype="f32", keep_host=True)
+    if splits:
+        ctx.set_option(k2.K2_OPT_ATTN_SPLITS, splits)
+    oracle = O.OracleModel(s, lambda n, l: host[(n, l)], "f32")
+    prompt = ki.prompt_ids(s.vocab, 16)
+    toks_ref, lg_ref = oracle.generate_greedy(prompt, 16, capacity=32)
+    toks, lg = run_greedy(ctx, prompt, 16, s.vocab)
+    np.testing.assert_array_equal(toks, toks_ref)
+    assert np.max(np.abs(lg - lg_ref)) <= 1e-4
+    assert ctx.sync_status() == k2.K2_OK
+
+
+def test_tiny_fp32_gains_and_planted_mutants(k2, mio):
+    # random norm gains (a dropped gain must show), and the GPU must NOT match
+    # an oracle with a planted mistake (each mutant moves logits > 1e-3)
+    s = ki.TINY
+    ctx, host = mio.build_context(s, max_context=40, kv_dtype="f32", gain_scale=0.2, keep_host=True)
+    get = lambda n, l: host[(n, l)]  # noqa: E731
+    prompt = ki.prompt_ids(s.vocab, 20, seed=7)
+    toks, lg = run_greedy(ctx, prompt, 8, s.vocab)
+    seq = np.concatenate([prompt, toks[:-1]])
+    _, lg_ref, _ = O.OracleModel(s, get, "f32").teacher_forced(seq, len(prompt) - 1)
+    assert np.max(np.abs(lg - lg_ref)) <= 1e-4
+    for m in O.MUTANTS[1:]:
+        _, lg_bad, _ = O.OracleModel(s, get, "f32", mutant=m).teacher_forced(seq, len(prompt) - 1)
+        assert np.max(np.abs(lg - lg_bad)) > 1e-3, m
+
+
+def test_gate3_incremental_equals_full_prefix_on_gpu(k2, mio):
+    # kimi-k3-in-c GATE 3 on the device: the logits of each decode step equal
+    # those of a prefill of the whole prefix into an empty cache
+    s = ki.TINY
+    ctx, _ = mio.build_context(s, max_context=48, kv_dtype="f32")
+    prompt = ki.prompt_ids(s.vocab, 9, seed=3)
+    toks, lg = run_greedy(ctx, prompt, 6, s.vocab)
+    seq = np.concatenate([prompt, toks])
+    for i in range(len(toks)):
+        ctx.kv_reset(-1)
+        t2, l2 = run_greedy(ctx, seq[:9 + i], 0, s.vocab)
+        assert t2[0] == toks[i]
+        assert np.max(np.abs(l2[0] - lg[i])) <= 1e-5
+
+
+# ---------------------------------------------------------------------------
+# medium bf16 model: several GEMV stages per CTA, a ragged vocab, 64-key tiles
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kv,splits,tol", [("f16", 0, 2e-4), ("f16", 7, 2e-4), ("i8", 0, 5e-2), ("f32", 2, 2e-4)])
+def test_medium_bf16_teacher_forced(k2, mio, kv, splits, tol):
+    s = ki.MEDIUM
+    ctx, host = mio.build_context(s, max_context=160, kv_dtype=kv, gain_scale=0.1, keep_host=True)
+    if splits:
+        ctx.set_option(k2.K2_OPT_ATTN_SPLITS, splits)
+    prompt = ki.prompt_ids(s.vocab, 70, seed=11)  # crosses a 64-key tile
+    toks, lg = run_greedy(ctx, prompt, 60, s.vocab)
+    seq = np.concatenate([prompt, toks[:-1]])
+    am, lg_ref, _ = O.OracleModel(s, lambda n, l: host[(n, l)], kv).teacher_forced(seq, len(prompt) - 1)
+    assert rel_l2(lg, lg_ref) <= tol
+    agree = np.mean(am == toks)
+    assert agree >= 0.99 if kv != "i8" else agree >= 0.95
+    assert ctx.sync_status() == k2.K2_OK
+
+
+def test_graph_and_pdl_modes_give_identical_tokens(k2, mio):
+    s = ki.MEDIUM
+    prompt = ki.prompt_ids(s.vocab, 30, seed=5)
+    outs = []
+    for pdl, graph in ((1, 0), (0, 0), (1, 1)):
+        ctx, _ = mio.build_context(s, max_context=64, kv_dtype="f16")
+        ctx.set_option(k2.K2_OPT_PDL, pdl)
+        ctx.set_option(k2.K2_OPT_GRAPH, graph)
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            toks, lg = run_greedy(ctx, prompt, 20, s.vocab)
+        stream.synchronize()
+        outs.append((toks, lg))
+    for toks, lg in outs[1:]:
+        np.testing.assert_array_equal(toks, outs[0][0])
+        np.testing.assert_array_equal(lg, outs[0][1])  # same kernels, same order: bitwise
+
+
+# ---------------------------------------------------------------------------
+# one decoder layer of the 3.7B shape, fp16 KV of 4096 N(0,1) rows
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kv,tol", [("f16", 2e-2), ("i8", 5e-2)])
+def test_layer_3p7b_shape_ctx4096(k2, mio, kv, tol):
+    s = ki.K2_LAYER
+    ctx_len = 4096
+    ctx, host = mio.build_context(s, max_context=ctx_len + 1, kv_dtype=kv, keep_host=True)
+    nkv, d = s.n_kv_heads, s.head_dim
+    kp, vp, ksp, vsp, _ = ctx.kv_view(0, 0)
+    cap = ctx.info().kv_capacity
+    kvals = ki.kv_fill_f16((2, nkv, ctx_len, d), seed=2).astype(np.float32)
+    if kv == "f16":
+        for ptr, arr in ((kp, kvals[0]), (vp, kvals[1])):
+            dev = k2.device_view(ptr, nkv * cap * d, torch.float16).view(nkv, cap, d)
+            dev[:, :ctx_len].copy_(torch.from_numpy(arr.astype(np.float16)))
+        kst, vst = kvals[0], kvals[1]
+    else:
+        stored = []
+        for ptr, sptr, arr in ((kp, ksp, kvals[0]), (vp, vsp, kvals[1])):
+            codes, scales = O.int8_quantize(arr)
+            k2.device_view(ptr, nkv * cap * d, torch.int8).view(nkv, cap, d)[:, :ctx_len].copy_(
+                torch.from_numpy(codes))
+            k2.device_view(sptr, nkv * cap, torch.float16).view(nkv, cap)[:, :ctx_len].copy_(
+                torch.from_numpy(scales))
+            stored.append(O.int8_dequantize(codes, scales))
+        kst, vst = stored
+    ctx.kv_set_len(0, ctx_len)
+    x = ki.hidden_f32(s.hidden, seed=3)
+    dx = torch.from_numpy(x.copy()).cuda()
+    ctx.decode_layers(dx, 1)
+    got = dx.cpu().numpy()
+    w = {n: host[(n, 0)] for n in ki.LAYER_TENSORS}
+    ref, kref, vref = O.layer_decode_step(s, w, x, ctx_len, kst.transpose(1, 0, 2), vst.transpose(1, 0, 2), kv)
+    err = rel_l2(got - x, ref - x)  # the layer's update, the harder comparison
+    assert err <= tol
+    assert err <= (1e-3 if kv == "f16" else 2e-2)
+    # the appended row, read back from the cache
+    if kv == "f16":
+        knew = k2.device_view(kp, nkv * cap * d, torch.float16).view(nkv, cap, d)[:, ctx_len].float().cpu().numpy()
+        assert rel_l2(knew, kref) <= 1e-3
+    assert ctx.sync_status() == k2.K2_OK
+
+
+# ---------------------------------------------------------------------------
+# boundary behaviour
+# ---------------------------------------------------------------------------
+
+def test_context_full_is_refused_without_effect(k2, mio):
+    s = ki.TINY
+    ctx, _ = mio.build_context(s, max_context=20, kv_dtype="f32")
+    nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(k2.K2Error) as e:
+        ctx.prefill(0, torch.zeros(21, dtype=torch.int32, device="cuda"), nxt)
+    assert e.value.status == k2.K2_ERR_CONTEXT_FULL
+    assert ctx.kv_view(0, 0)[4] == 0
+    ctx.prefill(0, torch.zeros(19, dtype=torch.int32, device="cuda"), nxt)
+    ctx.decode_step(nxt, 1, nxt)
+    with pytest.raises(k2.K2Error) as e:
+        ctx.decode_step(nxt, 1, nxt)
+    assert e.value.status == k2.K2_ERR_CONTEXT_FULL
+    assert ctx.kv_view(0, 0)[4] == 20
+    with pytest.raises(k2.K2Error) as e:
+        ctx.prefill(0, torch.zeros(0, dtype=torch.int32, device="cuda"), nxt)
+    assert e.value.status == k2.K2_ERR_ARG
+    assert ctx.sync_status() == k2.K2_OK
+
+
+def test_bad_token_sets_guard_not_fault(k2, mio):
+    s = ki.TINY
+    ctx, _ = mio.build_context(s, max_context=8, kv_dtype="f32")
+    nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ctx.prefill(0, torch.tensor([3, s.vocab + 5], dtype=torch.int32, device="cuda"), nxt)
+    assert ctx.sync_status() == k2.K2_ERR_DEVICE_GUARD
+    assert "token" in ctx.last_error()
+    ctx.clear_status()
+    assert ctx.sync_status() == k2.K2_OK
+
+
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_argmax_ties_go_to_lowest_index(k2, mio, sign):
+    # lm_head rows 5 and 9 are the same vector, every other row is zero, so
+    # logits 5 and 9 tie (and every other logit ties at 0)
+    s = ki.TINY
+    dev, host = mio.device_weights(s, keep_host=True)
+    W = np.zeros((s.vocab, s.hidden), np.float32)
+    v = ki.normal_f32(9, 9, s.hidden) * np.float32(sign)
+    W[5] = v
+    W[9] = v
+    dev["lm_head"] = torch.from_numpy(W).cuda()
+    host[("lm_head", -1)] = W
+    cfg = k2.make_config(s, max_context=8, kv_dtype="f32")
+    ctx = k2.Context(cfg, dev)
+    prompt = np.array([1, 2, 3], np.int32)
+    toks, lg = run_greedy(ctx, prompt, 2, s.vocab)
+    oracle = O.OracleModel(s, lambda n, l: host[(n, l)], "f32")
+    ref, _ = oracle.generate_greedy(prompt, 2, capacity=8)
+    np.testing.assert_array_equal(toks, ref)
+    assert set(toks.tolist()) <= {0, 5}
