@@ -72,6 +72,7 @@ def _load():
         "k2_clear_status": (C.c_int, [vp, vp]),
         "k2_set_option": (C.c_int, [vp, i32, i64]),
         "k2_profile_decode": (C.c_int, [vp, vp, i32, vp, C.POINTER(C.c_float), C.POINTER(i32), vp]),
+        "k2_greedy_head_noalloc": (C.c_int, [C.POINTER(Config), vp, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -83,7 +84,7 @@ def _load():
 LIB = _load()
 EXPORTED = ("k2_workspace_bytes", "k2_init_weights", "k2_free", "k2_last_error", "k2_get_info", "k2_prefill",
             "k2_decode_step", "k2_decode_layers", "k2_kv_reset", "k2_kv_set_len", "k2_kv_view", "k2_hidden_view",
-            "k2_sync_status", "k2_clear_status", "k2_set_option", "k2_profile_decode")
+            "k2_sync_status", "k2_clear_status", "k2_set_option", "k2_profile_decode", "k2_greedy_head_noalloc")
 
 
 def _ptr(t):
@@ -199,6 +200,12 @@ class Context:
         self._check(LIB.k2_profile_decode(self.ctx, _ptr(tokens), batch, _ptr(next_tokens), ms, n,
                                           _stream(stream)))
         return dict(zip(KERNEL_CLASSES, ms)), dict(zip(KERNEL_CLASSES, n))
+
+
+def greedy_head_noalloc(cfg: Config, lm_head, final_norm, x, logits, token, stream=None) -> int:
+    """k2_greedy_head_noalloc: returns the k2 status (no context, no workspace)."""
+    return LIB.k2_greedy_head_noalloc(C.byref(cfg), _ptr(lm_head), _ptr(final_norm), _ptr(x), _ptr(logits),
+                                      _ptr(token), _stream(stream))
 
 
 def device_view(ptr: int, numel: int, dtype: torch.dtype) -> torch.Tensor:

@@ -205,6 +205,32 @@ enum { K2_K_EMBED = 0, K2_K_QKV, K2_K_ATTN, K2_K_OPROJ, K2_K_GATEUP, K2_K_DOWN, 
 k2_status k2_profile_decode(k2_ctx* ctx, const int32_t* d_tokens, int32_t batch, int32_t* d_next, float* ms,
                             int32_t* launches, void* stream);
 
+/* ---- without a workspace ---------------------------------------------------- */
+
+/* The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory -- code inside a host runtime that owns every
+ * device buffer and offers no allocator (a plugin in a pre-planned memory
+ * arena), or code that must not call cudaMalloc because it may synchronise
+ * the device.
+ *
+ * It computes what the end of k2_decode_step computes for one hidden state:
+ * logits = lm_head . GroupedRMSNorm(d_x; final_norm) and the first index of
+ * their maximum, using cfg->hidden, vocab, norm_groups, eps and weight_dtype
+ * (other config fields are ignored).  d_x [hidden] fp32, lm_head
+ * [vocab, hidden] and final_norm [hidden] (weight_dtype, 16-byte aligned) are
+ * device inputs; d_logits [vocab] (nullable) and d_token [1] are device
+ * outputs.  No context is needed and nothing is allocated: the kernel's
+ * scratch (one partial maximum per CTA) is a static device array of
+ * K2_NOALLOC_MAX_CTAS entries that every device loading the library holds
+ * until exit; K2_ERR_WORKSPACE if the launch would need more CTAs than that.
+ * The first call on a device looks up that array's address and sets kernel
+ * attributes; make it before any stream capture.  All calls share the array
+ * and each clears its counter before launching, so calls that overlap on the
+ * GPU race: serialise them (one stream, one thread). */
+#define K2_NOALLOC_MAX_CTAS 1024
+k2_status k2_greedy_head_noalloc(const k2_config* cfg, const void* lm_head, const void* final_norm, const float* d_x,
+                                 float* d_logits, int32_t* d_token, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
