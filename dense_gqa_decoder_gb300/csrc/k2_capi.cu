@@ -19,7 +19,7 @@ using namespace k2;
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr size_t kGemvSmem = 96 * 1024;  // per-CTA ring budget: two CTAs of consecutive kernels fit one SM
+constexpr size_t kGemvSmem = 104 * 1024;  // per-CTA budget: CTAs of two consecutive kernels share one SM
 constexpr size_t kAttnSmem = 96 * 1024;
 constexpr int kSplitMax = 64;
 constexpr int kArgmaxPartsMax = 1024;
@@ -33,8 +33,8 @@ int elt_bytes(int dt) { return dt == K2_F32 ? 4 : (dt == K2_BF16 || dt == K2_F16
 // ---------------------------------------------------------------------------
 struct Layout {
   size_t seq_len, guard, attn_counter, am_counter, rope, resid, qkv, attn_out, act, attn_part, am_val, am_idx;
-  size_t wqkv, wgu;  // per-layer stride below
-  size_t wqkv_layer, wgu_layer;
+  size_t wqkv, wo, wgu, wdown, wlm;  // packed weights; per-layer strides below
+  size_t wqkv_layer, wo_layer, wgu_layer, wdown_layer;
   size_t kc, vc, ks, vs;  // first layer; per-layer stride kv_layer / sc_layer
   size_t kv_layer, sc_layer;
   size_t total;
@@ -82,10 +82,15 @@ Layout layout_of(const k2_config& c) {
   l.am_val = take(sizeof(float) * static_cast<size_t>(s.B) * kArgmaxPartsMax);
   l.am_idx = take(sizeof(int) * static_cast<size_t>(s.B) * kArgmaxPartsMax);
   const size_t scratch_end = o;
-  l.wqkv_layer = align_up(static_cast<size_t>(s.qkv_n) * s.H * s.wb, kAlign);
-  l.wgu_layer = align_up(static_cast<size_t>(2) * s.I * s.H * s.wb, kAlign);
+  l.wqkv_layer = align_up(packed_bytes(s.qkv_n, s.H, s.wb), kAlign);
+  l.wo_layer = align_up(packed_bytes(s.H, s.nq * s.d, s.wb), kAlign);
+  l.wgu_layer = align_up(packed_bytes(2 * s.I, s.H, s.wb), kAlign);
+  l.wdown_layer = align_up(packed_bytes(s.H, s.I, s.wb), kAlign);
   l.wqkv = take(l.wqkv_layer * s.L);
+  l.wo = take(l.wo_layer * s.L);
   l.wgu = take(l.wgu_layer * s.L);
+  l.wdown = take(l.wdown_layer * s.L);
+  l.wlm = take(packed_bytes(s.V, s.H, s.wb));
   l.repack_bytes = o - scratch_end;
   const size_t kv_start = o;
   l.kv_layer = align_up(static_cast<size_t>(s.B) * s.nkv * l.cap * s.d * s.kvb, kAlign);
@@ -140,7 +145,7 @@ struct k2_ctx {
   const void* embed = nullptr;
   const void* lm_head = nullptr;
   const void* final_norm = nullptr;
-  std::vector<const void*> attn_norm, wo, mlp_norm, w_down;
+  std::vector<const void*> attn_norm, mlp_norm;
   // workspace pointers
   int* seq_len = nullptr;
   unsigned* guard = nullptr;
@@ -151,7 +156,7 @@ struct k2_ctx {
         *am_val = nullptr;
   int* am_idx = nullptr;
   // plans
-  GemvArgs p_qkv = {}, p_o = {}, p_gu = {}, p_down = {}, p_lm = {};
+  PackedGemvArgs p_qkv = {}, p_o = {}, p_gu = {}, p_down = {}, p_lm = {};
   int grid_qkv = 0, grid_o = 0, grid_gu = 0, grid_down = 0, grid_lm = 0;
   AttnArgs p_attn = {};
   int attn_splits_b1 = 1;
@@ -166,7 +171,10 @@ struct k2_ctx {
   cudaEvent_t ev[2] = {nullptr, nullptr};
 
   void* wqkv(int l) const { return ws + lay.wqkv + lay.wqkv_layer * l; }
+  void* wop(int l) const { return ws + lay.wo + lay.wo_layer * l; }
   void* wgu(int l) const { return ws + lay.wgu + lay.wgu_layer * l; }
+  void* wdown(int l) const { return ws + lay.wdown + lay.wdown_layer * l; }
+  void* wlm() const { return ws + lay.wlm; }
   void* kc(int l) const { return ws + lay.kc + lay.kv_layer * l; }
   void* vc(int l) const { return ws + lay.vc + lay.kv_layer * l; }
   void* ks(int l) const { return lay.sc_layer ? ws + lay.ks + lay.sc_layer * l : nullptr; }
@@ -239,13 +247,13 @@ void chain_b1(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in, int
   const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
   const int splits = attn_splits(c, 1);
   for (int l = 0; l < s.L; ++l) {
-    GemvArgs q = c->p_qkv;
-    q.W = c->wqkv(l);
+    PackedGemvArgs q = c->p_qkv;
+    q.Wp = c->wqkv(l);
     q.x = x;
     q.gain = c->attn_norm[l];
     q.out = c->qkv;
     q.seq = seq;
-    ln.run(K2_K_QKV, [&] { return launch_gemv(q, wb, EPI_QKV, c->grid_qkv, st, pdl); });
+    ln.run(K2_K_QKV, [&] { return launch_packed_gemv(q, wb, EPI_QKV, c->grid_qkv, st, pdl); });
 
     AttnArgs at = c->p_attn;
     at.kc = at.kc_w = c->kc(l);
@@ -255,27 +263,27 @@ void chain_b1(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in, int
     at.seq0 = seq;
     ln.run(K2_K_ATTN, [&] { return launch_attn(at, s.d, s.rep, kvdt, splits, 1, st, pdl); });
 
-    GemvArgs o = c->p_o;
-    o.W = c->wo[l];
+    PackedGemvArgs o = c->p_o;
+    o.Wp = c->wop(l);
     o.x = c->attn_out;
     o.out = x;
-    ln.run(K2_K_OPROJ, [&] { return launch_gemv(o, wb, EPI_RESID, c->grid_o, st, pdl); });
+    ln.run(K2_K_OPROJ, [&] { return launch_packed_gemv(o, wb, EPI_RESID, c->grid_o, st, pdl); });
 
-    GemvArgs gu = c->p_gu;
-    gu.W = c->wgu(l);
+    PackedGemvArgs gu = c->p_gu;
+    gu.Wp = c->wgu(l);
     gu.x = x;
     gu.gain = c->mlp_norm[l];
     gu.out = c->act;
-    ln.run(K2_K_GATEUP, [&] { return launch_gemv(gu, wb, EPI_SWIGLU, c->grid_gu, st, pdl); });
+    ln.run(K2_K_GATEUP, [&] { return launch_packed_gemv(gu, wb, EPI_SWIGLU, c->grid_gu, st, pdl); });
 
-    GemvArgs dn = c->p_down;
-    dn.W = c->w_down[l];
+    PackedGemvArgs dn = c->p_down;
+    dn.Wp = c->wdown(l);
     dn.x = c->act;
     dn.out = x;
-    ln.run(K2_K_DOWN, [&] { return launch_gemv(dn, wb, EPI_RESID, c->grid_down, st, pdl); });
+    ln.run(K2_K_DOWN, [&] { return launch_packed_gemv(dn, wb, EPI_RESID, c->grid_down, st, pdl); });
   }
   if (head) {
-    GemvArgs lm = c->p_lm;
+    PackedGemvArgs lm = c->p_lm;
     lm.x = x;
     lm.logits = logits;
     lm.next_token = next;
@@ -284,7 +292,7 @@ void chain_b1(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in, int
     lm.part_idx = c->am_idx + static_cast<size_t>(seq) * kArgmaxPartsMax;
     lm.seq = seq;
     lm.advance = 1;
-    ln.run(K2_K_LMHEAD, [&] { return launch_gemv(lm, wb, EPI_ARGMAX, c->grid_lm, st, pdl); });
+    ln.run(K2_K_LMHEAD, [&] { return launch_packed_gemv(lm, wb, EPI_ARGMAX, c->grid_lm, st, pdl); });
   } else {
     ln.run(K2_K_EMBED, [&] { return launch_advance(c->seq_len, seq, 1, st, pdl); });
   }
@@ -299,7 +307,7 @@ void enqueue_decode(k2_ctx* c, Launcher& ln, const int* d_tokens, int batch, int
 bool plan_all(k2_ctx* c) {
   const Sizes& s = c->s;
   const int wb = s.wb;
-  GemvArgs base = {};
+  PackedGemvArgs base = {};
   base.groups = s.G;
   base.eps = c->cfg.eps;
   base.rope = c->rope;
@@ -311,30 +319,24 @@ bool plan_all(k2_ctx* c) {
   base.part_val = c->am_val;
   base.part_idx = c->am_idx;
   base.counter = c->am_counter;
-  auto grid_for = [&](const GemvArgs& a) {
-    const int units = a.N / a.align;
-    int g = c->sms;
-    if (g > units) g = units;
-    if (g > kArgmaxPartsMax) g = kArgmaxPartsMax;
-    return g < 1 ? 1 : g;
-  };
   const void* dummy_gain = c->final_norm;  // any non-null: plans check the norm constraints
   c->p_qkv = base; c->p_qkv.N = s.qkv_n; c->p_qkv.K = s.H; c->p_qkv.gain = dummy_gain;
   c->p_o = base; c->p_o.N = s.H; c->p_o.K = s.nq * s.d;
   c->p_gu = base; c->p_gu.N = 2 * s.I; c->p_gu.K = s.H; c->p_gu.gain = dummy_gain;
   c->p_down = base; c->p_down.N = s.H; c->p_down.K = s.I;
-  c->p_lm = base; c->p_lm.N = s.V; c->p_lm.K = s.H; c->p_lm.W = c->lm_head; c->p_lm.gain = c->final_norm;
-  if (!gemv_plan(c->p_qkv, wb, EPI_QKV, kGemvSmem) || !gemv_plan(c->p_o, wb, EPI_RESID, kGemvSmem) ||
-      !gemv_plan(c->p_gu, wb, EPI_SWIGLU, kGemvSmem) || !gemv_plan(c->p_down, wb, EPI_RESID, kGemvSmem) ||
-      !gemv_plan(c->p_lm, wb, EPI_ARGMAX, kGemvSmem))
+  c->p_lm = base; c->p_lm.N = s.V; c->p_lm.K = s.H; c->p_lm.Wp = c->wlm(); c->p_lm.gain = c->final_norm;
+  if (s.qkv_n % 2 || (2 * s.I) % 2) return false;  // pair epilogues
+  if (!packed_plan(c->p_qkv, wb, kGemvSmem) || !packed_plan(c->p_o, wb, kGemvSmem) ||
+      !packed_plan(c->p_gu, wb, kGemvSmem) || !packed_plan(c->p_down, wb, kGemvSmem) ||
+      !packed_plan(c->p_lm, wb, kGemvSmem))
     return false;
   c->p_o.gain = nullptr;
   c->p_down.gain = nullptr;
-  c->grid_qkv = grid_for(c->p_qkv);
-  c->grid_o = grid_for(c->p_o);
-  c->grid_gu = grid_for(c->p_gu);
-  c->grid_down = grid_for(c->p_down);
-  c->grid_lm = grid_for(c->p_lm);
+  c->grid_qkv = packed_grid(c->p_qkv.N, c->sms);
+  c->grid_o = packed_grid(c->p_o.N, c->sms);
+  c->grid_gu = packed_grid(c->p_gu.N, c->sms);
+  c->grid_down = packed_grid(c->p_down.N, c->sms);
+  c->grid_lm = packed_grid(c->p_lm.N, c->sms);
 
   AttnArgs& at = c->p_attn;
   at = {};
@@ -449,9 +451,7 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   c->final_norm = w->final_norm;
   for (int l = 0; l < c->s.L; ++l) {
     c->attn_norm.push_back(w->attn_norm[l]);
-    c->wo.push_back(w->wo[l]);
     c->mlp_norm.push_back(w->mlp_norm[l]);
-    c->w_down.push_back(w->w_down[l]);
   }
   c->len.assign(c->s.B, 0);
   if (!plan_all(c)) {
@@ -461,7 +461,7 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if ((e = gemv_init_attrs()) || (e = attn_init_attrs())) {
+  if ((e = packed_init_attrs()) || (e = attn_init_attrs())) {
     g_init_error = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     delete c;
     return K2_ERR_CUDA;
@@ -473,10 +473,18 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     delete c;
     return K2_ERR_CUDA;
   }
-  for (int l = 0; l < c->s.L && e == cudaSuccess; ++l) {
-    e = launch_repack_qkv(c->wqkv(l), w->wq[l], w->wk[l], w->wv[l], c->s.wb, c->s.nq, c->s.nkv, c->s.d, c->s.H, s);
-    if (e == cudaSuccess) e = launch_repack_gateup(c->wgu(l), w->w_gate[l], w->w_up[l], c->s.wb, c->s.I, c->s.H, s);
+  const Sizes& z = c->s;
+  for (int l = 0; l < z.L && e == cudaSuccess; ++l) {
+    e = launch_pack(c->wqkv(l), w->wq[l], w->wk[l], w->wv[l], PACK_QKV, z.qkv_n, z.H, z.wb, z.nq, z.nkv, z.d, s);
+    if (e == cudaSuccess)
+      e = launch_pack(c->wop(l), w->wo[l], nullptr, nullptr, PACK_PLAIN, z.H, z.nq * z.d, z.wb, 0, 0, 1, s);
+    if (e == cudaSuccess)
+      e = launch_pack(c->wgu(l), w->w_gate[l], w->w_up[l], nullptr, PACK_GATEUP, 2 * z.I, z.H, z.wb, 0, 0, 1, s);
+    if (e == cudaSuccess)
+      e = launch_pack(c->wdown(l), w->w_down[l], nullptr, nullptr, PACK_PLAIN, z.H, z.I, z.wb, 0, 0, 1, s);
   }
+  if (e == cudaSuccess)
+    e = launch_pack(c->wlm(), w->lm_head, nullptr, nullptr, PACK_PLAIN, z.V, z.H, z.wb, 0, 0, 1, s);
   if (e == cudaSuccess) e = cudaEventCreate(&c->ev[0]);
   if (e == cudaSuccess) e = cudaEventCreate(&c->ev[1]);
   if (e != cudaSuccess) {

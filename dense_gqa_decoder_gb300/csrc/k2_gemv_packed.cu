@@ -1,0 +1,467 @@
+// Packed streaming GEMV: the batch-1 decode projections y = W . norm(x) with
+// the epilogue of each step fused in (QKV + split-half RoPE, o_proj and
+// down_proj + residual, gate/up + SwiGLU, lm_head + first-index argmax).
+//
+// The decode step is bound by HBM: each weight byte is read once per token for
+// one multiply-add (k2-burn README, "Model shape": 8.8 GB of bf16 weights per
+// token at the 3.7B shape).  Measured on this GPU, a read stream reaches about
+// 7.2-7.5 TB/s either with many plain 128-bit loads in flight or with 1-D bulk
+// TMA copies of at least 4 KB and about 64 KB in flight per SM; 1 KB copies
+// stall near 3 TB/s.  The kernel is shaped by that:
+//   * at set-up every matrix is packed pair-interleaved in 512-byte chunks:
+//     [row pair][chunk][row 0 | row 1], zero-padded, so the (pair, chunk) units
+//     of any contiguous range are one contiguous run of bytes (1 KB per unit);
+//   * a CTA owns a band of row pairs; its units are cut into 8 equal
+//     contiguous ranges, one per warp (exact balance for any shape); each warp
+//     streams its range through its own ring of shared-memory slots with one
+//     bulk copy of 4-5 KB per slot, refilled by lane 0 as soon as the warp has
+//     read it: no CTA barrier inside the loop;
+//   * the first slots are requested before griddepcontrol.wait, while the
+//     previous kernel of the step is still finishing (weights never depend on
+//     it);
+//   * x is normalised once per CTA (GroupedRMSNorm, k2-burn README "Status:
+//     v0") from the fp32 residual stream into shared memory, lane-interleaved
+//     per chunk, so every 128-bit read of x and W is conflict-free and each x
+//     chunk serves both rows of a pair;
+//   * a pair is finished by the warp that read all of it; the few pairs cut by
+//     a warp boundary are summed piece by piece in warp order at the end, so
+//     results are deterministic.
+#include <math.h>
+
+#include "k2_kernels.h"
+#include "k2_common.cuh"
+
+namespace k2 {
+
+namespace {
+
+constexpr int kUnitB = 1024;  // one chunk of both rows of a pair
+
+struct Best {
+  float v;
+  int i;
+};
+__device__ __forceinline__ Best better(Best a, Best b) {
+  if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+  return a;
+}
+__device__ __forceinline__ Best warp_best(Best p) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Best q;
+    q.v = __shfl_xor_sync(0xffffffffu, p.v, o);
+    q.i = __shfl_xor_sync(0xffffffffu, p.i, o);
+    p = better(p, q);
+  }
+  return p;
+}
+
+template <typename WT>
+__device__ __forceinline__ float4 load_gain4(const void* g, int e);
+template <>
+__device__ __forceinline__ float4 load_gain4<__nv_bfloat16>(const void* g, int e) {
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(g) + e));
+  return make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+}
+template <>
+__device__ __forceinline__ float4 load_gain4<float>(const void* g, int e) {
+  return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(g) + e));
+}
+
+template <typename WT, int EPI>
+__global__ void __launch_bounds__(kPackedThreads, 1) packed_gemv_kernel(const PackedGemvArgs a) {
+  constexpr int EPL = Unpack<WT>::N;  // elements per 16-byte load
+  constexpr int CH = 32 * EPL;        // elements per chunk
+  constexpr int NPL = EPL / 4;        // float4 planes of x per chunk
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t full[kPackedWarps][kPackedMaxSlots];
+  __shared__ float ss_sh[kPackedWarps][4];
+  __shared__ float rs_sh[4];
+  __shared__ int rec_pair[kPackedWarps][2];
+  __shared__ float rec_val[kPackedWarps][2][2];
+  __shared__ int rec_n[kPackedWarps];
+  __shared__ Best best_sh[kPackedWarps];
+  __shared__ int last_sh;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int CT = a.CT, K = a.K, SU = a.SU, NS = a.NS;
+  const int npairs = (a.N + 1) / 2;
+  const int p0 = static_cast<int>((static_cast<long long>(npairs) * cta) / G);
+  const int p1 = static_cast<int>((static_cast<long long>(npairs) * (cta + 1)) / G);
+  const long long U = static_cast<long long>(p1 - p0) * CT;
+  const int ua = static_cast<int>((U * warp) / kPackedWarps);
+  const int ub = static_cast<int>((U * (warp + 1)) / kPackedWarps);
+  const int nslots = (ub - ua + SU - 1) / SU;
+  const uint8_t* src = reinterpret_cast<const uint8_t*>(a.Wp) + static_cast<size_t>(p0) * CT * kUnitB;
+  uint8_t* ring = smem + static_cast<size_t>(warp) * NS * SU * kUnitB;
+  float* xs = reinterpret_cast<float*>(smem + static_cast<size_t>(kPackedWarps) * NS * SU * kUnitB);
+
+  auto issue = [&](int k) {
+    const int u0 = ua + k * SU;
+    const int n = min(SU, ub - u0);
+    const int slot = k % NS;
+    mbar_arrive_expect_tx(&full[warp][slot], static_cast<uint32_t>(n) * kUnitB);
+    bulk_g2s(ring + static_cast<size_t>(slot) * SU * kUnitB, src + static_cast<size_t>(u0) * kUnitB,
+             static_cast<uint32_t>(n) * kUnitB, &full[warp][slot]);
+  };
+
+  if (lane == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&full[warp][i], 1);
+    fence_mbar_init();
+    for (int k = 0; k < NS && k < nslots; ++k) issue(k);
+    rec_n[warp] = 0;
+  }
+  __syncwarp();
+  pdl_wait();
+  pdl_trigger();
+
+  // ---- normalised x, lane-interleaved per chunk, zero past K ---------------------
+  {
+    const int gsz = a.gain ? K / a.groups : K;
+    float ssq[4] = {0.f, 0.f, 0.f, 0.f};
+    const int KP = CT * CH;
+    for (int e = tid * 4; e < KP; e += kPackedThreads * 4) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < K) v = __ldcg(reinterpret_cast<const float4*>(a.x + e));
+      const int c = e / CH, r = e - c * CH, l = r / EPL, j = r - l * EPL;
+      *reinterpret_cast<float4*>(xs + ((c * NPL + j / 4) * 32 + l) * 4) = v;
+      const float t = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      const int grp = e < K ? e / gsz : 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q == grp) ssq[q] += t;
+    }
+    if (a.gain != nullptr) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ssq[q] = warp_sum(ssq[q]);
+      if (lane == 0)
+        for (int q = 0; q < 4; ++q) ss_sh[warp][q] = ssq[q];
+      __syncthreads();
+      if (tid < a.groups) {
+        float t = 0.f;
+        for (int w = 0; w < kPackedWarps; ++w) t += ss_sh[w][tid];
+        rs_sh[tid] = 1.0f / sqrtf(t / static_cast<float>(gsz) + a.eps);
+      }
+      __syncthreads();
+      for (int e = tid * 4; e < K; e += kPackedThreads * 4) {
+        const int c = e / CH, r = e - c * CH, l = r / EPL, j = r - l * EPL;
+        float4* p = reinterpret_cast<float4*>(xs + ((c * NPL + j / 4) * 32 + l) * 4);
+        const float rs = rs_sh[e / gsz];
+        const float4 gn = load_gain4<WT>(a.gain, e);
+        float4 v = *p;
+        v.x = v.x * rs * gn.x; v.y = v.y * rs * gn.y; v.z = v.z * rs * gn.z; v.w = v.w * rs * gn.w;
+        *p = v;
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- epilogue of one finished pair (lane 0 / thread 0) ----------------------------
+  Best best{-INFINITY, 0x7fffffff};
+  auto finish = [&](int g, float v0, float v1) {
+    const int row = 2 * g;
+    if constexpr (EPI == EPI_SWIGLU) {
+      a.out[g] = v0 / (1.0f + expf(-v0)) * v1;
+    } else if constexpr (EPI == EPI_QKV) {
+      const int half = a.head_dim / 2;
+      const int head = g / half, i = g - head * half;
+      float o0 = v0, o1 = v1;
+      if (head < a.n_rot_heads) {
+        int pos = a.seq_len[a.seq];
+        if (pos < 0 || pos >= a.cap) {
+          atomicOr(a.guard, GUARD_POS);
+          pos = 0;
+        }
+        const float2 cs = a.rope[static_cast<size_t>(pos) * half + i];
+        o0 = v0 * cs.x - v1 * cs.y;
+        o1 = v1 * cs.x + v0 * cs.y;
+      }
+      a.out[head * a.head_dim + i] = o0;
+      a.out[head * a.head_dim + i + half] = o1;
+    } else {
+      const int rows = min(2, a.N - row);
+      const float v[2] = {v0, v1};
+      for (int r = 0; r < rows; ++r) {
+        if constexpr (EPI == EPI_STORE) {
+          a.out[row + r] = v[r];
+        } else if constexpr (EPI == EPI_RESID) {
+          a.out[row + r] += v[r];
+        } else {
+          if (a.logits) a.logits[row + r] = v[r];
+          if (v[r] != v[r]) atomicOr(a.guard, GUARD_NAN);
+          else best = better(best, Best{v[r], row + r});
+        }
+      }
+    }
+  };
+
+  // ---- stream this warp's units ---------------------------------------------------------
+  int pl = ua / CT, c = ua - (ua / CT) * CT;  // current pair (CTA-local) and chunk
+  bool pair_whole = (c == 0);                 // this warp saw the pair from its first chunk
+  float acc0 = 0.f, acc1 = 0.f;
+  bool bad = false;
+  int k = 0;
+  for (; k < nslots; ++k) {
+    const int slot = k % NS;
+    const bool ok = mbar_wait(&full[warp][slot], static_cast<uint32_t>(k / NS) & 1u);
+    if (__any_sync(0xffffffffu, !ok)) {
+      bad = true;
+      break;
+    }
+    const uint8_t* buf = ring + static_cast<size_t>(slot) * SU * kUnitB;
+    const int u0 = ua + k * SU;
+    const int n = min(SU, ub - u0);
+    int j = 0;
+    while (j < n) {
+      const int seg = min(n - j, CT - c);  // units of the current pair in this slot
+#pragma unroll 2
+      for (int q = 0; q < seg; ++q) {
+        const int cc = c + q;
+        float xv[EPL];
+#pragma unroll
+        for (int p = 0; p < NPL; ++p) {
+          const float4 t = *reinterpret_cast<const float4*>(xs + ((cc * NPL + p) * 32 + lane) * 4);
+          xv[4 * p] = t.x; xv[4 * p + 1] = t.y; xv[4 * p + 2] = t.z; xv[4 * p + 3] = t.w;
+        }
+        const uint8_t* ub8 = buf + (j + q) * kUnitB + lane * 16;
+        float w0[EPL], w1[EPL];
+        Unpack<WT>::run(*reinterpret_cast<const uint4*>(ub8), w0);
+        Unpack<WT>::run(*reinterpret_cast<const uint4*>(ub8 + 512), w1);
+        float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          t0 = fmaf(w0[e], xv[e], t0);
+          t1 = fmaf(w1[e], xv[e], t1);
+        }
+        acc0 += t0;
+        acc1 += t1;
+      }
+      j += seg;
+      c += seg;
+      const bool pair_end = (c == CT);
+      const bool range_end = (u0 + j == ub);
+      if (pair_end || range_end) {
+        const float s0 = warp_sum(acc0), s1 = warp_sum(acc1);
+        acc0 = acc1 = 0.f;
+        if (lane == 0) {
+          if (pair_whole && pair_end) {
+            finish(p0 + pl, s0, s1);
+          } else {  // a piece of a pair cut by a warp boundary
+            const int r = rec_n[warp];
+            rec_pair[warp][r] = pl;
+            rec_val[warp][r][0] = s0;
+            rec_val[warp][r][1] = s1;
+            rec_n[warp] = r + 1;
+          }
+        }
+        if (pair_end) {
+          ++pl;
+          c = 0;
+          pair_whole = true;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && k + NS < nslots) {
+      fence_proxy_async();
+      issue(k + NS);
+    }
+  }
+
+  if (bad && lane == 0) {
+    atomicOr(a.guard, GUARD_TIMEOUT);
+    // let the copies still in flight land before shared memory is released
+    const int issued = min(nslots, k + NS);
+    for (int k2 = k; k2 < issued; ++k2)
+      (void)mbar_wait(&full[warp][k2 % NS], static_cast<uint32_t>(k2 / NS) & 1u);
+  }
+  __syncthreads();
+
+  // ---- pairs cut by warp boundaries: pieces summed in warp order ------------------------
+  if (tid == 0) {
+    int cur = -1;
+    float v0 = 0.f, v1 = 0.f;
+    for (int w = 0; w < kPackedWarps; ++w) {
+      for (int r = 0; r < rec_n[w]; ++r) {
+        if (rec_pair[w][r] != cur) {
+          if (cur >= 0) finish(p0 + cur, v0, v1);
+          cur = rec_pair[w][r];
+          v0 = v1 = 0.f;
+        }
+        v0 += rec_val[w][r][0];
+        v1 += rec_val[w][r][1];
+      }
+    }
+    if (cur >= 0) finish(p0 + cur, v0, v1);
+  }
+
+  if constexpr (EPI == EPI_ARGMAX) {
+    best = warp_best(best);
+    if (lane == 0) best_sh[warp] = best;
+    __syncthreads();
+    if (tid == 0) {
+      Best b = best_sh[0];
+      for (int w = 1; w < kPackedWarps; ++w) b = better(b, best_sh[w]);
+      a.part_val[cta] = b.v;
+      a.part_idx[cta] = b.i;
+      __threadfence();
+      const unsigned t = atomicAdd(a.counter, 1u);
+      last_sh = (t == static_cast<unsigned>(G - 1));
+    }
+    __syncthreads();
+    if (last_sh) {
+      __threadfence();
+      Best b{-INFINITY, 0x7fffffff};
+      for (int i = tid; i < G; i += kPackedThreads) b = better(b, Best{__ldcg(a.part_val + i), __ldcg(a.part_idx + i)});
+      b = warp_best(b);
+      if (lane == 0) best_sh[warp] = b;
+      __syncthreads();
+      if (tid == 0) {
+        Best f = best_sh[0];
+        for (int w = 1; w < kPackedWarps; ++w) f = better(f, best_sh[w]);
+        if (f.i == 0x7fffffff) {  // every logit was NaN
+          atomicOr(a.guard, GUARD_NAN);
+          f.i = 0;
+        }
+        *a.next_token = f.i;
+        if (a.advance) a.seq_len[a.seq] += 1;
+        *a.counter = 0u;
+      }
+    }
+  }
+}
+
+// ---- packing (set-up) ----------------------------------------------------------------------
+template <typename WT>
+__global__ void pack_kernel(WT* __restrict__ dst, const WT* __restrict__ s0, const WT* __restrict__ s1,
+                            const WT* __restrict__ s2, int mode, int N, int K, int CT, int nq, int nkv, int d) {
+  constexpr int CH = 512 / sizeof(WT);
+  const int R = blockIdx.x;  // packed row index (2 * pair + r)
+  const int pair = R >> 1, r = R & 1;
+  const WT* src = nullptr;
+  if (R < N) {
+    if (mode == PACK_PLAIN) {
+      src = s0 + static_cast<size_t>(R) * K;
+    } else if (mode == PACK_GATEUP) {
+      src = ((R & 1) ? s1 : s0) + static_cast<size_t>(R >> 1) * K;
+    } else {
+      const int head = R / d, rr = R - head * d;
+      const int sr = (rr & 1) ? (rr >> 1) + d / 2 : (rr >> 1);
+      if (head < nq) src = s0 + (static_cast<size_t>(head) * d + sr) * K;
+      else if (head < nq + nkv) src = s1 + (static_cast<size_t>(head - nq) * d + sr) * K;
+      else src = s2 + (static_cast<size_t>(head - nq - nkv) * d + sr) * K;
+    }
+  }
+  WT* out = dst + static_cast<size_t>(pair) * CT * 2 * CH + r * CH;
+  for (int e = threadIdx.x; e < CT * CH; e += blockDim.x) {
+    const int c = e / CH, i = e - c * CH;
+    out[static_cast<size_t>(c) * 2 * CH + i] = (src != nullptr && e < K) ? src[e] : WT(0.f);
+  }
+}
+
+template <typename WT>
+cudaError_t launch_typed(const PackedGemvArgs& a, int epi, const cudaLaunchConfig_t& cfg) {
+  switch (epi) {
+    case EPI_STORE: return cudaLaunchKernelEx(&cfg, packed_gemv_kernel<WT, EPI_STORE>, a);
+    case EPI_RESID: return cudaLaunchKernelEx(&cfg, packed_gemv_kernel<WT, EPI_RESID>, a);
+    case EPI_QKV: return cudaLaunchKernelEx(&cfg, packed_gemv_kernel<WT, EPI_QKV>, a);
+    case EPI_SWIGLU: return cudaLaunchKernelEx(&cfg, packed_gemv_kernel<WT, EPI_SWIGLU>, a);
+    case EPI_ARGMAX: return cudaLaunchKernelEx(&cfg, packed_gemv_kernel<WT, EPI_ARGMAX>, a);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename WT>
+cudaError_t set_attr(int bytes) {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(packed_gemv_kernel<WT, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+    return e;
+  if ((e = cudaFuncSetAttribute(packed_gemv_kernel<WT, EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+    return e;
+  if ((e = cudaFuncSetAttribute(packed_gemv_kernel<WT, EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+    return e;
+  if ((e = cudaFuncSetAttribute(packed_gemv_kernel<WT, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+    return e;
+  return cudaFuncSetAttribute(packed_gemv_kernel<WT, EPI_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
+
+size_t packed_bytes(int N, int K, int wbytes) {
+  const int CH = 512 / wbytes;
+  const size_t CT = (static_cast<size_t>(K) + CH - 1) / CH;
+  const size_t npairs = (static_cast<size_t>(N) + 1) / 2;
+  return npairs * CT * kUnitB;
+}
+
+int packed_grid(int N, int sms) {
+  const int npairs = (N + 1) / 2;
+  int g = sms < npairs ? sms : npairs;
+  if (g > 1024) g = 1024;
+  return g < 1 ? 1 : g;
+}
+
+bool packed_plan(PackedGemvArgs& a, int wbytes, size_t smem_budget) {
+  if (wbytes != 2 && wbytes != 4) return false;
+  const int EPL = 16 / wbytes;
+  const int CH = 32 * EPL;
+  if (a.N <= 0 || a.K <= 0 || a.K % 4) return false;
+  if (a.gain && (a.groups < 1 || a.groups > 4 || a.K % a.groups || (a.K / a.groups) % 4)) return false;
+  a.CT = (a.K + CH - 1) / CH;
+  a.x_bytes = static_cast<uint32_t>(a.CT) * CH * 4;
+  if (a.x_bytes >= smem_budget) return false;
+  const size_t ring = smem_budget - a.x_bytes;
+  // the largest copies (up to 5 KB) that still leave two slots per warp
+  for (int su = 5; su >= 1; --su) {
+    const size_t ns = ring / (static_cast<size_t>(kPackedWarps) * su * kUnitB);
+    if (ns >= 2) {
+      a.SU = su;
+      a.NS = static_cast<int>(ns > 3 ? 3 : ns);
+      return true;
+    }
+  }
+  return false;
+}
+
+size_t packed_smem_bytes(const PackedGemvArgs& a) {
+  return static_cast<size_t>(kPackedWarps) * a.NS * a.SU * kUnitB + a.x_bytes;
+}
+
+cudaError_t packed_init_attrs() {
+  cudaError_t e = set_attr<__nv_bfloat16>(200 * 1024);
+  if (e != cudaSuccess) return e;
+  return set_attr<float>(200 * 1024);
+}
+
+cudaError_t launch_packed_gemv(const PackedGemvArgs& a, int wbytes, int epi, int grid, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPackedThreads);
+  cfg.dynamicSmemBytes = packed_smem_bytes(a);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return wbytes == 2 ? launch_typed<__nv_bfloat16>(a, epi, cfg) : launch_typed<float>(a, epi, cfg);
+}
+
+cudaError_t launch_pack(void* dst, const void* src0, const void* src1, const void* src2, int mode, int N, int K,
+                        int wbytes, int nq, int nkv, int d, cudaStream_t s) {
+  const int CH = 512 / wbytes;
+  const int CT = (K + CH - 1) / CH;
+  const int rows = 2 * ((N + 1) / 2);
+  if (wbytes == 2)
+    pack_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>(
+        static_cast<__nv_bfloat16*>(dst), static_cast<const __nv_bfloat16*>(src0),
+        static_cast<const __nv_bfloat16*>(src1), static_cast<const __nv_bfloat16*>(src2), mode, N, K, CT, nq, nkv, d);
+  else
+    pack_kernel<float><<<rows, 256, 0, s>>>(static_cast<float*>(dst), static_cast<const float*>(src0),
+                                            static_cast<const float*>(src1), static_cast<const float*>(src2), mode, N,
+                                            K, CT, nq, nkv, d);
+  return cudaGetLastError();
+}
+
+}  // namespace k2

@@ -67,6 +67,59 @@ cudaError_t launch_gemv(const GemvArgs& a, int wbytes, int epi, int grid, cudaSt
 size_t gemv_smem_bytes(const GemvArgs& a);
 
 // ---------------------------------------------------------------------------
+// packed streaming GEMV (the decode hot path): W is stored pair-interleaved,
+// [ceil(N/2) pairs][CT chunks][2 rows][CH elements], CH = 512 bytes / element
+// size, zero-padded to whole chunks and pairs, so that any run of (pair, chunk)
+// units is one contiguous byte range (1 KB per unit)
+// ---------------------------------------------------------------------------
+struct PackedGemvArgs {
+  const void* Wp;
+  int N, K, CT;
+  const float* x;    // [K] fp32
+  const void* gain;  // [K] norm gain (weight dtype) or null
+  int groups;
+  float eps;
+  int SU;  // units (1 KB) per slot = bytes of one bulk copy / 1024
+  int NS;  // slots per warp ring
+  uint32_t x_bytes;
+  // epilogue (as GemvArgs)
+  float* out;
+  const float2* rope;
+  int cap;
+  int* seq_len;
+  int seq;
+  int head_dim;
+  int n_rot_heads;
+  float* logits;
+  float* part_val;
+  int* part_idx;
+  unsigned* counter;
+  int* next_token;
+  int advance;
+  unsigned* guard;
+};
+constexpr int kPackedThreads = 256;
+constexpr int kPackedWarps = 8;
+constexpr int kPackedMaxSlots = 8;
+
+// bytes of the packed copy of an [N, K] matrix
+size_t packed_bytes(int N, int K, int wbytes);
+bool packed_plan(PackedGemvArgs& a, int wbytes, size_t smem_budget);
+int packed_grid(int N, int sms);
+cudaError_t packed_init_attrs();
+cudaError_t launch_packed_gemv(const PackedGemvArgs& a, int wbytes, int epi, int grid, cudaStream_t s, bool pdl);
+size_t packed_smem_bytes(const PackedGemvArgs& a);
+
+// pack kernels: logical row R of the packed matrix comes from
+//   PACK_PLAIN:  src0 row R
+//   PACK_QKV:    heads of [src0 (nq heads); src1 (nkv); src2 (nkv)], rows of
+//                each head ordered (0, d/2), (1, d/2 + 1), ... (split-half RoPE pairs)
+//   PACK_GATEUP: row 2i = src0 row i, row 2i + 1 = src1 row i
+enum PackMode : int { PACK_PLAIN = 0, PACK_QKV = 1, PACK_GATEUP = 2 };
+cudaError_t launch_pack(void* dst, const void* src0, const void* src1, const void* src2, int mode, int N, int K,
+                        int wbytes, int nq, int nkv, int d, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
 // split-K flash-decode GQA attention with the KV append of the new token
 // ---------------------------------------------------------------------------
 struct AttnArgs {

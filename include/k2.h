@@ -27,9 +27,11 @@
  *     the stream has reached the end of the call's work.
  *   - The library allocates no device memory.  The caller provides the
  *     workspace (k2_workspace_bytes) and every input/output buffer, and keeps
- *     them alive until k2_free.  Weights passed to k2_init_weights are used in
- *     place (except Wq/Wk/Wv and W_gate/W_up, which are repacked into the
- *     workspace) and must also outlive the context.
+ *     them alive until k2_free.  k2_init_weights packs every projection
+ *     matrix (Wq, Wk, Wv, Wo, W_gate, W_up, W_down, lm_head) into the
+ *     workspace in the layout the kernels stream; once its work has completed
+ *     on the stream the caller may free those.  The embedding table and the
+ *     norm gains are read in place and must outlive the context.
  *   - A non-zero k2_status means the call had no effect on the context and
  *     enqueued no work; k2_last_error(ctx) says why.  Faults detected on the
  *     device (a token id outside the vocabulary, a NaN logit, a bounded wait
@@ -102,7 +104,7 @@ typedef struct {
   int32_t attn_splits;   /* key-range splits of the batch-1 attention launch */
   int32_t gemv_grid;     /* CTAs of the batch-1 GEMV launches */
   int64_t kv_bytes;      /* bytes of the KV cache region */
-  int64_t repack_bytes;  /* bytes of the repacked QKV and gate/up weights */
+  int64_t repack_bytes;  /* bytes of the packed projection weights */
   int64_t scratch_bytes; /* everything else in the workspace */
 } k2_info;
 
@@ -116,8 +118,9 @@ size_t k2_workspace_bytes(const k2_config* cfg);
 /* Validates the config (kimi-k3-in-c k3_run.c: an untrusted config aborts
  * rather than falls back; k2-burn README "Limitations": out-of-scope
  * checkpoints hard-error), carves the workspace (256-byte aligned, at least
- * k2_workspace_bytes), repacks the fused QKV and interleaved gate/up weights
- * into it, builds the RoPE table and zeroes the sequence lengths.  Enqueued on
+ * k2_workspace_bytes), packs the projection weights into it (QKV fused with
+ * RoPE pair order, gate/up interleaved, every matrix in row pairs of
+ * 512-byte chunks), builds the RoPE table and zeroes the sequence lengths.  Enqueued on
  * `stream`.  On success *out owns host memory only; release with k2_free. */
 k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_workspace, size_t ws_bytes,
                           void* stream, k2_ctx** out);

@@ -37,11 +37,12 @@ def test_every_declared_call_is_exported(k2):
 def test_workspace_bytes_valid_and_invalid(k2):
     cfg = k2.make_config(ki.K2_3P7B, max_context=4096 + 256, max_batch=1, kv_dtype="f16")
     n = k2.workspace_bytes(cfg)
-    # repacked QKV + gate/up (4.9 GB) + fp16 KV 36 x 2 x 8 x cap x 128 x 2 bytes
+    # packed projections (every weight but the embedding) + fp16 KV
+    # 36 x 2 x 8 x cap x 128 x 2 bytes
     cap = (4096 + 256 + 8 + 63) // 64 * 64
     kv = 36 * 2 * 8 * cap * 128 * 2
-    repack = 36 * (6144 + 2 * 10240) * 2560 * 2
-    assert repack + kv < n < repack + kv + 64 * 2 ** 20
+    packed = (36 * ((6144 + 2 * 10240) * 2560 + 2560 * 4096 + 2560 * 10240) + 250624 * 2560) * 2
+    assert packed + kv < n < packed + kv + 64 * 2 ** 20
     for bad in (dict(head_dim=96), dict(n_heads=30), dict(hidden=2561), dict(norm_groups=0),
                 dict(vocab=0), dict(head_dim=127)):
         c = k2.make_config(ki.K2_3P7B.replace(**bad), max_context=4096)
