@@ -7,23 +7,28 @@
 // g = h / REP, o_h = softmax_j(q_h . k_j / sqrt(D)) . v_j over j = 0..pos.
 //
 // Layout and schedule:
-//   * grid = (splits, KV heads, sequences); a CTA owns one KV head of one
-//     sequence and a contiguous key range, so every K/V byte is read from HBM
-//     once per step and shared by the REP query heads of its group;
-//   * the key range is streamed in 64-key tiles through a ring of shared-memory
-//     stages with 1-D bulk TMA copies; cached rows never depend on the
-//     previous kernel, so the first tiles are in flight before
-//     griddepcontrol.wait;
+//   * grid = (splits, KV heads, sequences), and the splits of one (sequence,
+//     KV head) form one thread-block cluster; a CTA owns a contiguous key
+//     range, so every K/V byte is read from HBM once per step and shared by
+//     the REP query heads of the group;
+//   * the range is cut into 32-key tiles dealt round-robin to the 8 warps;
+//     each warp streams its tiles through its own shared-memory slot with
+//     bulk TMA copies (K rows, V rows), the first one requested before
+//     griddepcontrol.wait (cached rows never depend on the previous kernel);
+//   * per tile a warp computes the 32 scores (8 lanes per key), one fp32
+//     online-softmax update (one lane per key) and the P.V product (lanes own
+//     output dims), keeping its own (m, l, o) per head: no CTA barrier inside
+//     the loop;
 //   * the new token's K/V (already rotated by the QKV kernel) are stored in the
 //     cache format (fp32, fp16 round-to-nearest, or int8 with one fp16 scale
-//     per row, k2-burn README "KV cache storage") by the CTA whose range holds
-//     position pos, which also uses the stored values itself: no CTA reads a
-//     row another CTA writes in the same launch;
-//   * int8 rows are dequantised inside the kernel (code * row scale), so no
-//     dequantised copy of the history is ever materialised;
-//   * fp32 online softmax per tile; each split writes (m, l, o) and the last
-//     CTA of a KV head to finish (atomic counter, no spin) merges the splits
-//     with their log-sum-exp weights and writes the head outputs.
+//     per row, k2-burn README "KV cache storage") by the warp whose tile holds
+//     position pos, which also uses the stored values itself;
+//   * int8 rows are dequantised inside the kernel (code * row scale);
+//   * the 8 warp states are merged in shared memory, then the splits of the
+//     cluster merge through distributed shared memory: after a cluster
+//     barrier each CTA finalises a slice of the head outputs from its peers'
+//     (m, l, o) with log-sum-exp weights -- no partials in global memory, no
+//     atomics, no fences.
 #include <math.h>
 
 #include <type_traits>
@@ -50,41 +55,76 @@ struct KVTraits<int8_t> {
   static constexpr bool kI8 = true;
 };
 
-__device__ __forceinline__ float2 load2(const float* p) { return *reinterpret_cast<const float2*>(p); }
-__device__ __forceinline__ float2 load2(const __half* p) {
-  return __half22float2(*reinterpret_cast<const __half2*>(p));
+template <int DPL>
+__device__ __forceinline__ void load_dims(const float* p, float* f) {
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) f[i] = p[i];
 }
-__device__ __forceinline__ float2 load2(const int8_t* p) {
-  const char2 c = *reinterpret_cast<const char2*>(p);
-  return make_float2(static_cast<float>(c.x), static_cast<float>(c.y));
+template <int DPL>
+__device__ __forceinline__ void load_dims(const __half* p, float* f) {
+  if constexpr (DPL % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < DPL; i += 2) {
+      const float2 t = __half22float2(*reinterpret_cast<const __half2*>(p + i));
+      f[i] = t.x;
+      f[i + 1] = t.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) f[i] = __half2float(p[i]);
+  }
 }
+template <int DPL>
+__device__ __forceinline__ void load_dims(const int8_t* p, float* f) {
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) f[i] = static_cast<float>(p[i]);
+}
+
+// ---- thread-block cluster helpers (distributed shared memory) -----------------
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_peer(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+constexpr int kWarps = kAttnThreads / 32;
 
 template <int D, int REP, typename KVT>
 __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArgs a) {
   constexpr int TK = kAttnTK;
   constexpr int ELT = sizeof(KVT);
-  constexpr int EPL = 16 / ELT;  // elements per 16-byte load
-  constexpr int LPK = D / EPL;   // lanes that share one key row
-  static_assert(LPK >= 1 && LPK <= 32 && (32 % LPK) == 0, "head_dim / dtype");
-  constexpr int KPW = 32 / LPK;  // keys per warp per pass
-  constexpr int KPP = KPW * (kAttnThreads / 32);
-  constexpr int NPASS = (TK + KPP - 1) / KPP;
+  constexpr int EPL = 16 / ELT;              // elements per 16-byte load
+  constexpr int ROWB = D * ELT;              // bytes of one K or V row
+  constexpr int NV = ROWB / 16;              // 16-byte vectors per row
+  constexpr int LPK = NV >= 8 ? 8 : NV;      // lanes sharing one key in the score step
+  constexpr int VPL = NV / LPK;              // 16-byte vectors per lane per key
+  constexpr int KPS = 32 / LPK;              // keys per score step
+  constexpr int QD = VPL * EPL;              // q dims per lane
+  constexpr int DPL = D >= 32 ? D / 32 : 1;  // output dims per lane
+  constexpr int DL = D / DPL;                // lanes holding output dims
   constexpr bool I8 = KVTraits<KVT>::kI8;
-  constexpr int DP = D / 2;
-  static_assert(kAttnThreads % DP == 0, "head_dim");
-  constexpr int KG = kAttnThreads / DP;  // key groups of the PV product
-  constexpr uint32_t ROWB = D * ELT;
-  constexpr uint32_t KV_TILE = TK * ROWB;
+  constexpr uint32_t KVB = TK * ROWB;        // bytes of the K (or V) rows of a tile
+  constexpr int PSTR = REP * (D + 2);        // a partial state: m[REP], l[REP], o[REP][D]
+  static_assert(NV % LPK == 0 && 32 % LPK == 0 && TK == 32, "head_dim / dtype");
 
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t full[4];
-  __shared__ float S[REP][TK];
-  __shared__ float P[REP][TK];
-  __shared__ float m_sh[REP], l_sh[REP], al_sh[REP];
-  __shared__ float red[KG * REP * D];
-  __shared__ __align__(16) KVT newkv[2][D];
-  __shared__ __half newsc[2];
-  __shared__ int last_sh;
+  extern __shared__ __align__(128) uint8_t smem[];  // kWarps slots of a.slot_bytes
+  __shared__ uint64_t full[kWarps];
+  __shared__ float Sw[kWarps][REP][TK];
+  __shared__ __align__(16) float Pw[kWarps][TK][REP];
+  __shared__ float cpart[PSTR];  // this CTA's (m, l, o), read by the cluster peers
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.z, g = blockIdx.y, sp = blockIdx.x, ns = gridDim.x;
@@ -93,148 +133,136 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   const int pos = a.seq_len[seq];
   if (pos < 0 || pos >= a.cap) {
     if (tid == 0) atomicOr(a.guard, GUARD_POS);
-    return;  // every CTA of the launch sees the same pos and leaves the same way
+    return;  // every CTA of the launch sees the same pos and leaves before any cluster barrier
   }
   const int L = pos + 1;
   const int k0 = min(L, static_cast<int>((static_cast<long long>(L) * sp) / ns) & ~7);
   const int k1 = (sp == ns - 1) ? L : min(L, static_cast<int>((static_cast<long long>(L) * (sp + 1)) / ns) & ~7);
   const int ntile = k1 > k0 ? (k1 - k0 + TK - 1) / TK : 0;
+  const int nmine = ntile > warp ? (ntile - warp + kWarps - 1) / kWarps : 0;
   const size_t head_row = (static_cast<size_t>(seq) * a.nkv + g) * a.cap;
   const uint8_t* Kg = reinterpret_cast<const uint8_t*>(a.kc) + head_row * ROWB;
   const uint8_t* Vg = reinterpret_cast<const uint8_t*>(a.vc) + head_row * ROWB;
   const __half* KSg = I8 ? reinterpret_cast<const __half*>(a.ks) + head_row : nullptr;
   const __half* VSg = I8 ? reinterpret_cast<const __half*>(a.vs) + head_row : nullptr;
+  uint8_t* slot = smem + static_cast<size_t>(warp) * a.slot_bytes;
 
-  auto issue = [&](int t) {
-    const int buf = t % a.nstage;
-    uint8_t* stg = smem + static_cast<size_t>(buf) * a.stage_bytes;
+  auto issue = [&](int t) {  // lane 0: tile t of this CTA into this warp's slot
     const int j0 = k0 + t * TK;
     const int rows = min(TK, k1 - j0);
     const int crow = max(0, min(rows, pos - j0));  // cached rows; row pos is the new one
     const int srow = (crow + 7) & ~7;             // scale copies in 16-byte units
-    uint32_t bytes = 2u * crow * ROWB + (I8 && crow > 0 ? 2u * srow * 2u : 0u);
+    const uint32_t bytes = 2u * crow * ROWB + (I8 && crow > 0 ? 2u * srow * 2u : 0u);
     if (bytes == 0) {
-      mbar_arrive(&full[buf]);
+      mbar_arrive(&full[warp]);
       return;
     }
-    mbar_arrive_expect_tx(&full[buf], bytes);
-    bulk_g2s(stg, Kg + static_cast<size_t>(j0) * ROWB, crow * ROWB, &full[buf]);
-    bulk_g2s(stg + KV_TILE, Vg + static_cast<size_t>(j0) * ROWB, crow * ROWB, &full[buf]);
+    mbar_arrive_expect_tx(&full[warp], bytes);
+    bulk_g2s(slot, Kg + static_cast<size_t>(j0) * ROWB, crow * ROWB, &full[warp]);
+    bulk_g2s(slot + KVB, Vg + static_cast<size_t>(j0) * ROWB, crow * ROWB, &full[warp]);
     if constexpr (I8) {
-      bulk_g2s(stg + 2 * KV_TILE, KSg + j0, srow * 2u, &full[buf]);
-      bulk_g2s(stg + 2 * KV_TILE + TK * 2, VSg + j0, srow * 2u, &full[buf]);
+      bulk_g2s(slot + 2 * KVB, KSg + j0, srow * 2u, &full[warp]);
+      bulk_g2s(slot + 2 * KVB + TK * 2, VSg + j0, srow * 2u, &full[warp]);
     }
   };
 
-  if (tid == 0) {
-    for (int i = 0; i < a.nstage; ++i) mbar_init(&full[i], 1);
+  if (lane == 0) {
+    mbar_init(&full[warp], 1);
     fence_mbar_init();
-    const int pre = min(a.nstage, ntile);
-    for (int t = 0; t < pre; ++t) issue(t);
+    if (nmine > 0) issue(warp);
   }
-  if (tid < REP) {
-    m_sh[tid] = -INFINITY;
-    l_sh[tid] = 0.f;
-  }
-  __syncthreads();
+  __syncwarp();
   pdl_wait();
-  pdl_trigger();
 
-  // ---- query slice (pre-scaled by 1/sqrt(D)) --------------------------------------
-  const int kl = lane % LPK;
+  // query slice (pre-scaled by 1/sqrt(D)): dims [kl*QD, kl*QD + QD) of every head
   const float* qkv = a.qkv + static_cast<size_t>(b) * a.qkv_stride;
-  float q[REP][EPL];
+  const int kl = lane % LPK;
+  float q[REP][QD];
 #pragma unroll
   for (int h = 0; h < REP; ++h)
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) q[h][e] = qkv[(g * REP + h) * D + kl * EPL + e] * a.scale;
+    for (int e = 0; e < QD; ++e) q[h][e] = qkv[(g * REP + h) * D + kl * QD + e] * a.scale;
+  pdl_trigger();
 
-  // ---- the new token's K/V in cache format ------------------------------------------
-  const bool has_new = ntile > 0 && k1 == L;
-  if (has_new && warp < 2) {
-    const float* src = qkv + (warp == 0 ? a.nq * D : (a.nq + a.nkv) * D) + g * D;
-    KVT* dst = reinterpret_cast<KVT*>(warp == 0 ? a.kc_w : a.vc_w) + (head_row + pos) * D;
-    if constexpr (I8) {
-      float amax = 0.f;
-      for (int i = lane; i < D; i += 32) amax = fmaxf(amax, fabsf(src[i]));
-      amax = warp_max(amax);
-      const __half sh = __float2half_rn(fminf(amax / 127.0f, 65504.0f));
-      const float sf = __half2float(sh);
-      for (int i = lane; i < D; i += 32) {
-        float c = sf > 0.f ? rintf(src[i] / sf) : 0.f;
-        c = fminf(fmaxf(c, -127.f), 127.f);
-        const int8_t ci = static_cast<int8_t>(c);
-        dst[i] = ci;
-        newkv[warp][i] = ci;
-      }
-      if (lane == 0) {
-        (warp == 0 ? reinterpret_cast<__half*>(a.ks) : reinterpret_cast<__half*>(a.vs))[head_row + pos] = sh;
-        newsc[warp] = sh;
-      }
-    } else if constexpr (std::is_same<KVT, __half>::value) {
-      for (int i = lane; i < D; i += 32) {
-        const __half hv = __float2half_rn(src[i]);
-        dst[i] = hv;
-        newkv[warp][i] = hv;
-      }
-    } else {
-      for (int i = lane; i < D; i += 32) {
-        dst[i] = src[i];
-        newkv[warp][i] = src[i];
-      }
-    }
+  float m[REP], l[REP], acc[REP][DPL];
+#pragma unroll
+  for (int h = 0; h < REP; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[h][d] = 0.f;
   }
 
-  // ---- tiles ----------------------------------------------------------------------------
-  const int kg = tid / DP, dp = tid % DP;
-  float acc[REP][2];
-#pragma unroll
-  for (int h = 0; h < REP; ++h) acc[h][0] = acc[h][1] = 0.f;
-
-  int t = 0;
-  bool timed_out = false;
-  for (; t < ntile; ++t) {
-    const int buf = t % a.nstage;
-    const uint32_t par = static_cast<uint32_t>(t / a.nstage) & 1u;
-    const bool ok = mbar_wait(&full[buf], par);
-    if (__syncthreads_or(!ok)) {
-      timed_out = true;
-      break;
-    }
-    uint8_t* stg = smem + static_cast<size_t>(buf) * a.stage_bytes;
-    const __half* ksc = reinterpret_cast<const __half*>(stg + 2 * KV_TILE);
-    const __half* vsc = ksc + TK;
+  bool bad = false;
+  int it = 0;
+  for (; it < nmine; ++it) {
+    const int t = warp + it * kWarps;
     const int j0 = k0 + t * TK;
     const int rows = min(TK, k1 - j0);
-    if (has_new && pos >= j0 && pos < j0 + rows) {
-      const int jr = pos - j0;
-      if (tid < D) {
-        reinterpret_cast<KVT*>(stg + jr * ROWB)[tid] = newkv[0][tid];
-        reinterpret_cast<KVT*>(stg + KV_TILE + jr * ROWB)[tid] = newkv[1][tid];
-      }
-      if constexpr (I8) {
-        if (tid == 0) {
-          reinterpret_cast<__half*>(stg + 2 * KV_TILE)[jr] = newsc[0];
-          reinterpret_cast<__half*>(stg + 2 * KV_TILE + TK * 2)[jr] = newsc[1];
+    const bool ok = mbar_wait(&full[warp], static_cast<uint32_t>(it) & 1u);
+    if (__any_sync(0xffffffffu, !ok)) {
+      bad = true;
+      break;
+    }
+    const __half* ksc = reinterpret_cast<const __half*>(slot + 2 * KVB);
+    const __half* vsc = ksc + TK;
+    // ---- the new token's K/V: stored format to the cache and into the slot
+    const int jr = pos - j0;
+    if (k1 == L && jr >= 0 && jr < rows) {
+      for (int kv = 0; kv < 2; ++kv) {
+        const float* src = qkv + (kv == 0 ? a.nq * D : (a.nq + a.nkv) * D) + g * D;
+        KVT* dst = reinterpret_cast<KVT*>(kv == 0 ? a.kc_w : a.vc_w) + (head_row + pos) * D;
+        KVT* row = reinterpret_cast<KVT*>(slot + kv * KVB + jr * ROWB);
+        if constexpr (I8) {
+          float amax = 0.f;
+          for (int i = lane; i < D; i += 32) amax = fmaxf(amax, fabsf(src[i]));
+          amax = warp_max(amax);
+          const __half sh = __float2half_rn(fminf(amax / 127.0f, 65504.0f));
+          const float sf = __half2float(sh);
+          for (int i = lane; i < D; i += 32) {
+            float cq = sf > 0.f ? rintf(src[i] / sf) : 0.f;
+            cq = fminf(fmaxf(cq, -127.f), 127.f);
+            const int8_t ci = static_cast<int8_t>(cq);
+            dst[i] = ci;
+            row[i] = ci;
+          }
+          if (lane == 0) {
+            (kv == 0 ? reinterpret_cast<__half*>(a.ks) : reinterpret_cast<__half*>(a.vs))[head_row + pos] = sh;
+            reinterpret_cast<__half*>(slot + 2 * KVB + kv * TK * 2)[jr] = sh;
+          }
+        } else if constexpr (std::is_same<KVT, __half>::value) {
+          for (int i = lane; i < D; i += 32) {
+            const __half hv = __float2half_rn(src[i]);
+            dst[i] = hv;
+            row[i] = hv;
+          }
+        } else {
+          for (int i = lane; i < D; i += 32) {
+            dst[i] = src[i];
+            row[i] = src[i];
+          }
         }
       }
-      __syncthreads();
+      __syncwarp();
     }
-    // scores
+    // ---- scores: LPK lanes per key, KPS keys per step
 #pragma unroll
-    for (int pass = 0; pass < NPASS; ++pass) {
-      const int jj = pass * KPP + warp * KPW + lane / LPK;
+    for (int st = 0; st < TK / KPS; ++st) {
+      const int jj = st * KPS + lane / LPK;
       float dot[REP];
 #pragma unroll
       for (int h = 0; h < REP; ++h) dot[h] = 0.f;
       if (jj < rows) {
-        const uint4 v = *reinterpret_cast<const uint4*>(stg + jj * ROWB + kl * 16);
-        float kf[EPL];
-        Unpack<KVT>::run(v, kf);
+        const uint8_t* kr = slot + jj * ROWB + kl * VPL * 16;
 #pragma unroll
-        for (int h = 0; h < REP; ++h)
+        for (int v = 0; v < VPL; ++v) {
+          float kf[EPL];
+          Unpack<KVT>::run(*reinterpret_cast<const uint4*>(kr + v * 16), kf);
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) dot[h] = fmaf(q[h][e], kf[e], dot[h]);
+          for (int h = 0; h < REP; ++h)
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) dot[h] = fmaf(q[h][v * EPL + e], kf[e], dot[h]);
+        }
       }
 #pragma unroll
       for (int h = 0; h < REP; ++h)
@@ -243,113 +271,116 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
       if (kl == 0 && jj < rows) {
         const float sc = I8 ? __half2float(ksc[jj]) : 1.f;
 #pragma unroll
-        for (int h = 0; h < REP; ++h) S[h][jj] = dot[h] * sc;
+        for (int h = 0; h < REP; ++h) Sw[warp][h][jj] = dot[h] * sc;
       }
     }
-    __syncthreads();
-    // online softmax, one warp per query head
-    if (warp < REP) {
-      const int h = warp;
-      float mt = -INFINITY;
-      for (int j = lane; j < rows; j += 32) mt = fmaxf(mt, S[h][j]);
-      mt = warp_max(mt);
-      const float mo = m_sh[h];
-      const float mn = fmaxf(mo, mt);
-      float sum = 0.f;
-      for (int j = lane; j < rows; j += 32) {
-        const float p = expf(S[h][j] - mn);
-        sum += p;
-        P[h][j] = I8 ? p * __half2float(vsc[j]) : p;
-      }
-      sum = warp_sum(sum);
-      if (lane == 0) {
-        const float al = expf(mo - mn);
-        al_sh[h] = al;
-        l_sh[h] = l_sh[h] * al + sum;
-        m_sh[h] = mn;
-      }
+    __syncwarp();
+    // ---- online softmax: lane j holds key j; every lane keeps the running (m, l)
+    float al[REP];
+#pragma unroll
+    for (int h = 0; h < REP; ++h) {
+      const float sv = lane < rows ? Sw[warp][h][lane] : -INFINITY;
+      const float mn = fmaxf(m[h], warp_max(sv));
+      al[h] = expf(m[h] - mn);  // m = -inf on the first tile: 0, and acc is 0 anyway
+      const float p = lane < rows ? expf(sv - mn) : 0.f;
+      l[h] = l[h] * al[h] + warp_sum(p);
+      m[h] = mn;
+      if (lane < rows) Pw[warp][lane][h] = I8 ? p * __half2float(vsc[lane]) : p;
     }
-    __syncthreads();
-    // o = alpha * o + P . V
-    {
-      const KVT* vt = reinterpret_cast<const KVT*>(stg + KV_TILE);
+    __syncwarp();
+    // ---- o = alpha * o + P . V
+    if (lane < DL) {
 #pragma unroll
-      for (int h = 0; h < REP; ++h) {
-        acc[h][0] *= al_sh[h];
-        acc[h][1] *= al_sh[h];
-      }
-      for (int j = kg; j < rows; j += KG) {
-        const float2 v = load2(vt + j * D + 2 * dp);
+      for (int h = 0; h < REP; ++h)
 #pragma unroll
-        for (int h = 0; h < REP; ++h) {
-          const float p = P[h][j];
-          acc[h][0] = fmaf(p, v.x, acc[h][0]);
-          acc[h][1] = fmaf(p, v.y, acc[h][1]);
+        for (int d = 0; d < DPL; ++d) acc[h][d] *= al[h];
+      const KVT* vt = reinterpret_cast<const KVT*>(slot + KVB) + lane * DPL;
+      for (int j = 0; j < rows; ++j) {
+        float vf[DPL];
+        load_dims<DPL>(vt + j * D, vf);
+        float p[REP];
+        if constexpr (REP == 4) {
+          const float4 p4 = *reinterpret_cast<const float4*>(&Pw[warp][j][0]);
+          p[0] = p4.x; p[1] = p4.y; p[2] = p4.z; p[3] = p4.w;
+        } else {
+#pragma unroll
+          for (int h = 0; h < REP; ++h) p[h] = Pw[warp][j][h];
         }
+#pragma unroll
+        for (int h = 0; h < REP; ++h)
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(p[h], vf[d], acc[h][d]);
       }
     }
-    __syncthreads();
-    if (tid == 0 && t + a.nstage < ntile) {
+    __syncwarp();
+    if (lane == 0 && it + 1 < nmine) {
       fence_proxy_async();
-      issue(t + a.nstage);
+      issue(t + kWarps);
     }
   }
-
-  if (timed_out) {
-    if (tid == 0) {
-      atomicOr(a.guard, GUARD_TIMEOUT);
-      const int issued = min(ntile, t + a.nstage);
-      for (int t2 = t; t2 < issued; ++t2)
-        (void)mbar_wait(&full[t2 % a.nstage], static_cast<uint32_t>(t2 / a.nstage) & 1u);
-    }
-    __syncthreads();
+  if (bad && lane == 0) {
+    atomicOr(a.guard, GUARD_TIMEOUT);
+    (void)mbar_wait(&full[warp], static_cast<uint32_t>(it) & 1u);  // the copy in flight, bounded
   }
 
-  // ---- this split's (m, l, o) ---------------------------------------------------------------
+  // ---- this warp's state into its (now idle) slot; then the CTA's state -------------
+  float* wst = reinterpret_cast<float*>(slot);
+  if (lane == 0) {
 #pragma unroll
-  for (int h = 0; h < REP; ++h) {
-    red[(kg * REP + h) * D + 2 * dp] = acc[h][0];
-    red[(kg * REP + h) * D + 2 * dp + 1] = acc[h][1];
+    for (int h = 0; h < REP; ++h) {
+      wst[h] = m[h];
+      wst[REP + h] = l[h];
+    }
+  }
+  if (lane < DL) {
+#pragma unroll
+    for (int h = 0; h < REP; ++h)
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) wst[2 * REP + h * D + lane * DPL + d] = acc[h][d];
   }
   __syncthreads();
-  constexpr int PSTRIDE = REP * (D + 2);
-  float* pp = a.part + ((static_cast<size_t>(b) * a.nkv + g) * ns + sp) * PSTRIDE;
-  for (int idx = tid; idx < REP * D; idx += kAttnThreads) {
-    const int h = idx / D, dim = idx - h * D;
-    float o = 0.f;
-    for (int q2 = 0; q2 < KG; ++q2) o += red[(q2 * REP + h) * D + dim];
-    pp[2 * REP + idx] = o;
-  }
-  if (tid < REP) {
-    pp[tid] = m_sh[tid];
-    pp[REP + tid] = l_sh[tid];
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned prev = atomicAdd(&a.counter[b * a.nkv + g], 1u);
-    last_sh = (prev == static_cast<unsigned>(ns - 1));
-  }
-  __syncthreads();
-  if (!last_sh) return;
-
-  // ---- last CTA of this KV head: log-sum-exp merge of the splits -------------------------------
-  __threadfence();
-  const float* base = a.part + (static_cast<size_t>(b) * a.nkv + g) * ns * PSTRIDE;
   for (int idx = tid; idx < REP * D; idx += kAttnThreads) {
     const int h = idx / D;
     float M = -INFINITY;
-    for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(base + s2 * PSTRIDE + h));
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, reinterpret_cast<const float*>(smem + w * a.slot_bytes)[h]);
+    float O = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float* ws = reinterpret_cast<const float*>(smem + w * a.slot_bytes);
+      if (ws[h] != -INFINITY) O = fmaf(ws[2 * REP + idx], expf(ws[h] - M), O);
+    }
+    cpart[2 * REP + idx] = O;
+  }
+  if (tid < REP) {
+    float M = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, reinterpret_cast<const float*>(smem + w * a.slot_bytes)[tid]);
+    float Ls = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float* ws = reinterpret_cast<const float*>(smem + w * a.slot_bytes);
+      if (ws[tid] != -INFINITY) Ls = fmaf(ws[REP + tid], expf(ws[tid] - M), Ls);
+    }
+    cpart[tid] = M;
+    cpart[REP + tid] = Ls;
+  }
+
+  // ---- merge of the cluster's splits through distributed shared memory -------------
+  cluster_sync_all();
+  const int rank = static_cast<int>(cluster_rank());
+  const int chunk = (REP * D + ns - 1) / ns;
+  const int lo = rank * chunk, hi = min(REP * D, lo + chunk);
+  for (int idx = lo + tid; idx < hi; idx += kAttnThreads) {
+    const int h = idx / D;
+    float M = -INFINITY;
+    for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, ld_peer(peer_addr(&cpart[h], s2)));
     float Ls = 0.f, O = 0.f;
     for (int s2 = 0; s2 < ns; ++s2) {
-      const float ms = __ldcg(base + s2 * PSTRIDE + h);
+      const float ms = ld_peer(peer_addr(&cpart[h], s2));
       const float w = ms == -INFINITY ? 0.f : expf(ms - M);
-      Ls = fmaf(__ldcg(base + s2 * PSTRIDE + REP + h), w, Ls);
-      O = fmaf(__ldcg(base + s2 * PSTRIDE + 2 * REP + idx), w, O);
+      Ls = fmaf(ld_peer(peer_addr(&cpart[REP + h], s2)), w, Ls);
+      O = fmaf(ld_peer(peer_addr(&cpart[2 * REP + idx], s2)), w, O);
     }
     a.out[static_cast<size_t>(b) * a.nq * D + (g * REP + h) * D + (idx - h * D)] = O / Ls;
   }
-  if (tid == 0) a.counter[b * a.nkv + g] = 0u;
+  cluster_sync_all();  // peers read this CTA's cpart until here
 }
 
 template <int D, int REP>
@@ -362,23 +393,46 @@ cudaError_t launch_dr(const AttnArgs& a, int kv_dtype, const cudaLaunchConfig_t&
   return cudaErrorInvalidValue;
 }
 
+template <typename K>
+cudaError_t attr_one(K kernel, int bytes) {
+  cudaError_t e = set_kernel_smem(kernel, bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
 template <int D, int REP>
 cudaError_t attr_dr(int bytes) {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(attn_decode_kernel<D, REP, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
-    return e;
-  if ((e = cudaFuncSetAttribute(attn_decode_kernel<D, REP, __half>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
-    return e;
-  return cudaFuncSetAttribute(attn_decode_kernel<D, REP, int8_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if ((e = attr_one(attn_decode_kernel<D, REP, float>, bytes))) return e;
+  if ((e = attr_one(attn_decode_kernel<D, REP, __half>, bytes))) return e;
+  return attr_one(attn_decode_kernel<D, REP, int8_t>, bytes);
+}
+
+template <int D, int REP>
+const void* kernel_ptr(int kv_dtype) {
+  switch (kv_dtype) {
+    case 0: return reinterpret_cast<const void*>(attn_decode_kernel<D, REP, float>);
+    case 2: return reinterpret_cast<const void*>(attn_decode_kernel<D, REP, __half>);
+    case 3: return reinterpret_cast<const void*>(attn_decode_kernel<D, REP, int8_t>);
+  }
+  return nullptr;
 }
 
 #define K2_ATTN_SHAPES(X) \
   X(16, 1) X(16, 2) X(16, 4) X(64, 1) X(64, 2) X(64, 4) X(128, 1) X(128, 2) X(128, 4)
 
+constexpr size_t kAttnMaxDyn = 200 * 1024;
+
 }  // namespace
+
+size_t attn_slot_bytes(int head_dim, int kv_dtype) {
+  const size_t elt = kv_dtype == 0 ? 4 : (kv_dtype == 2 ? 2 : 1);
+  return 2 * kAttnTK * head_dim * elt + (kv_dtype == 3 ? 2 * kAttnTK * 2 : 0);
+}
 
 bool attn_supported(int head_dim, int rep, int kv_dtype) {
   if (kv_dtype != 0 && kv_dtype != 2 && kv_dtype != 3) return false;
+  if (attn_slot_bytes(head_dim, kv_dtype) * kWarps > kAttnMaxDyn) return false;
 #define K2_ATTN_SUP(D, R) \
   if (head_dim == D && rep == R) return true;
   K2_ATTN_SHAPES(K2_ATTN_SUP)
@@ -386,18 +440,39 @@ bool attn_supported(int head_dim, int rep, int kv_dtype) {
   return false;
 }
 
-size_t attn_stage_bytes(int head_dim, int kv_dtype) {
-  const size_t elt = kv_dtype == 0 ? 4 : (kv_dtype == 2 ? 2 : 1);
-  return 2 * kAttnTK * head_dim * elt + (kv_dtype == 3 ? 2 * kAttnTK * 2 : 0);
-}
-
 cudaError_t attn_init_attrs() {
   cudaError_t e = cudaSuccess;
 #define K2_ATTN_ATTR(D, R) \
-  if (e == cudaSuccess) e = attr_dr<D, R>(160 * 1024);
+  if (e == cudaSuccess) e = attr_dr<D, R>(static_cast<int>(kAttnMaxDyn));
   K2_ATTN_SHAPES(K2_ATTN_ATTR)
 #undef K2_ATTN_ATTR
   return e;
+}
+
+int attn_max_cluster(int head_dim, int rep, int kv_dtype, int limit) {
+  const void* fn = nullptr;
+#define K2_ATTN_PTR(D, R) \
+  if (head_dim == D && rep == R) fn = kernel_ptr<D, R>(kv_dtype);
+  K2_ATTN_SHAPES(K2_ATTN_PTR)
+#undef K2_ATTN_PTR
+  if (!fn) return 0;
+  for (int c = limit; c >= 1; --c) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c, 1, 1);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = attn_slot_bytes(head_dim, kv_dtype) * kWarps;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n >= 1) return c;
+    (void)cudaGetLastError();
+  }
+  return 0;
 }
 
 cudaError_t launch_attn(const AttnArgs& a, int head_dim, int rep, int kv_dtype, int nsplit, int batch,
@@ -405,13 +480,17 @@ cudaError_t launch_attn(const AttnArgs& a, int head_dim, int rep, int kv_dtype, 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nsplit, a.nkv, batch);
   cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(a.nstage) * a.stage_bytes;
+  cfg.dynamicSmemBytes = static_cast<size_t>(a.slot_bytes) * kWarps;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = pdl ? 2 : 1;
 #define K2_ATTN_LAUNCH(D, R) \
   if (head_dim == D && rep == R) return launch_dr<D, R>(a, kv_dtype, cfg);
   K2_ATTN_SHAPES(K2_ATTN_LAUNCH)

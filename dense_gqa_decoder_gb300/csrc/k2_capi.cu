@@ -20,8 +20,8 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr size_t kGemvSmem = 104 * 1024;  // per-CTA budget: CTAs of two consecutive kernels share one SM
-constexpr size_t kAttnSmem = 96 * 1024;
-constexpr int kSplitMax = 64;
+constexpr size_t kAttnSmem = 128 * 1024;
+constexpr size_t kLmHeadSmem = 176 * 1024;
 constexpr int kArgmaxPartsMax = 1024;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -32,7 +32,7 @@ int elt_bytes(int dt) { return dt == K2_F32 ? 4 : (dt == K2_BF16 || dt == K2_F16
 // workspace layout
 // ---------------------------------------------------------------------------
 struct Layout {
-  size_t seq_len, guard, attn_counter, am_counter, rope, resid, qkv, attn_out, act, attn_part, am_val, am_idx;
+  size_t seq_len, guard, am_counter, rope, resid, qkv, attn_out, act, am_val, am_idx;
   size_t wqkv, wo, wgu, wdown, wlm;  // packed weights; per-layer strides below
   size_t wqkv_layer, wo_layer, wgu_layer, wdown_layer;
   size_t kc, vc, ks, vs;  // first layer; per-layer stride kv_layer / sc_layer
@@ -71,14 +71,12 @@ Layout layout_of(const k2_config& c) {
   };
   l.seq_len = take(sizeof(int) * s.B);
   l.guard = take(sizeof(unsigned));
-  l.attn_counter = take(sizeof(unsigned) * s.B * s.nkv);
   l.am_counter = take(sizeof(unsigned) * s.B);
   l.rope = take(sizeof(float2) * static_cast<size_t>(l.cap) * (s.d / 2));
   l.resid = take(sizeof(float) * static_cast<size_t>(s.B) * s.H);
   l.qkv = take(sizeof(float) * static_cast<size_t>(s.B) * s.qkv_n);
   l.attn_out = take(sizeof(float) * static_cast<size_t>(s.B) * s.nq * s.d);
   l.act = take(sizeof(float) * static_cast<size_t>(s.B) * s.I);
-  l.attn_part = take(sizeof(float) * static_cast<size_t>(s.B) * s.nkv * kSplitMax * s.rep * (s.d + 2));
   l.am_val = take(sizeof(float) * static_cast<size_t>(s.B) * kArgmaxPartsMax);
   l.am_idx = take(sizeof(int) * static_cast<size_t>(s.B) * kArgmaxPartsMax);
   const size_t scratch_end = o;
@@ -149,17 +147,16 @@ struct k2_ctx {
   // workspace pointers
   int* seq_len = nullptr;
   unsigned* guard = nullptr;
-  unsigned* attn_counter = nullptr;
   unsigned* am_counter = nullptr;
   float2* rope = nullptr;
-  float *resid = nullptr, *qkv = nullptr, *attn_out = nullptr, *act = nullptr, *attn_part = nullptr,
+  float *resid = nullptr, *qkv = nullptr, *attn_out = nullptr, *act = nullptr,
         *am_val = nullptr;
   int* am_idx = nullptr;
   // plans
   PackedGemvArgs p_qkv = {}, p_o = {}, p_gu = {}, p_down = {}, p_lm = {};
   int grid_qkv = 0, grid_o = 0, grid_gu = 0, grid_down = 0, grid_lm = 0;
   AttnArgs p_attn = {};
-  int attn_splits_b1 = 1;
+  int attn_cluster_max = 1;  // largest launchable attention cluster
   int force_splits = 0;
   // state
   std::vector<int> len;
@@ -167,8 +164,8 @@ struct k2_ctx {
   bool graph = false;
   std::map<std::tuple<int, const void*, const void*, const void*, void*>, cudaGraphExec_t> graphs;
   std::string err;
-  // profiling
-  cudaEvent_t ev[2] = {nullptr, nullptr};
+  // profiling: event pairs around the kernels of one step
+  std::vector<cudaEvent_t> pev;
 
   void* wqkv(int l) const { return ws + lay.wqkv + lay.wqkv_layer * l; }
   void* wop(int l) const { return ws + lay.wo + lay.wo_layer * l; }
@@ -197,38 +194,55 @@ struct k2_ctx {
 namespace {
 
 int attn_splits(const k2_ctx* c, int batch) {
-  if (c->force_splits > 0) return c->force_splits < kSplitMax ? c->force_splits : kSplitMax;
+  if (c->force_splits > 0) return c->force_splits < c->attn_cluster_max ? c->force_splits : c->attn_cluster_max;
   int n = (c->sms + c->s.nkv * batch - 1) / (c->s.nkv * batch);
   const int cap_splits = c->lay.cap / 8;
   if (n > cap_splits) n = cap_splits;
-  if (n > kSplitMax) n = kSplitMax;
+  if (n > c->attn_cluster_max) n = c->attn_cluster_max;
   return n < 1 ? 1 : n;
 }
 
-// Kernel launch recorder: plain launches, or with a CUDA event pair per kernel.
+// Kernel launch recorder: plain launches, or (profiling) each launch between
+// a pair of CUDA events; the events are read after the whole step has been
+// queued, so the timings are device time, not host launch latency.
 struct Launcher {
   k2_ctx* c;
   cudaStream_t s;
   bool pdl;
-  float* ms = nullptr;      // profiling output (null = not profiling)
-  int* launches = nullptr;
+  bool profile = false;
+  std::vector<int> classes;  // kernel class of each profiled launch
   cudaError_t err = cudaSuccess;
 
   template <typename F>
   void run(int cls, F&& f) {
     if (err != cudaSuccess) return;
-    if (ms) {
-      if ((err = cudaEventRecord(c->ev[0], s))) return;
+    if (profile) {
+      const size_t i = classes.size();
+      while (c->pev.size() < 2 * (i + 1)) {
+        cudaEvent_t e;
+        if ((err = cudaEventCreate(&e))) return;
+        c->pev.push_back(e);
+      }
+      if ((err = cudaEventRecord(c->pev[2 * i], s))) return;
       if ((err = f())) return;
-      if ((err = cudaEventRecord(c->ev[1], s))) return;
-      if ((err = cudaEventSynchronize(c->ev[1]))) return;
-      float t = 0.f;
-      if ((err = cudaEventElapsedTime(&t, c->ev[0], c->ev[1]))) return;
-      ms[cls] += t;
-      launches[cls] += 1;
+      if ((err = cudaEventRecord(c->pev[2 * i + 1], s))) return;
+      classes.push_back(cls);
     } else {
       err = f();
     }
+  }
+  // waits for the profiled launches and adds their device times per class
+  cudaError_t collect(float* ms, int* launches) {
+    if (err != cudaSuccess) return err;
+    if (classes.empty()) return cudaSuccess;
+    if ((err = cudaEventSynchronize(c->pev[2 * classes.size() - 1]))) return err;
+    for (size_t i = 0; i < classes.size(); ++i) {
+      float t = 0.f;
+      if ((err = cudaEventElapsedTime(&t, c->pev[2 * i], c->pev[2 * i + 1]))) return err;
+      ms[classes[i]] += t;
+      launches[classes[i]] += 1;
+    }
+    return cudaSuccess;
   }
 };
 
@@ -326,9 +340,10 @@ bool plan_all(k2_ctx* c) {
   c->p_down = base; c->p_down.N = s.H; c->p_down.K = s.I;
   c->p_lm = base; c->p_lm.N = s.V; c->p_lm.K = s.H; c->p_lm.Wp = c->wlm(); c->p_lm.gain = c->final_norm;
   if (s.qkv_n % 2 || (2 * s.I) % 2) return false;  // pair epilogues
-  if (!packed_plan(c->p_qkv, wb, kGemvSmem) || !packed_plan(c->p_o, wb, kGemvSmem) ||
-      !packed_plan(c->p_gu, wb, kGemvSmem) || !packed_plan(c->p_down, wb, kGemvSmem) ||
-      !packed_plan(c->p_lm, wb, kGemvSmem))
+  // lm_head ends the step and no kernel overlaps it, so it takes a deeper ring
+  if (!packed_plan(c->p_qkv, wb, kGemvSmem, 3) || !packed_plan(c->p_o, wb, kGemvSmem, 3) ||
+      !packed_plan(c->p_gu, wb, kGemvSmem, 3) || !packed_plan(c->p_down, wb, kGemvSmem, 3) ||
+      !packed_plan(c->p_lm, wb, kLmHeadSmem, kPackedMaxSlots))
     return false;
   c->p_o.gain = nullptr;
   c->p_down.gain = nullptr;
@@ -346,18 +361,11 @@ bool plan_all(k2_ctx* c) {
   at.nq = s.nq;
   at.nkv = s.nkv;
   at.seq_len = c->seq_len;
-  at.part = c->attn_part;
-  at.counter = c->attn_counter;
   at.out = c->attn_out;
   at.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(s.d)));
   const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
-  at.stage_bytes = static_cast<uint32_t>(attn_stage_bytes(s.d, kvdt));
-  int nst = static_cast<int>(kAttnSmem / at.stage_bytes);
-  if (nst > 4) nst = 4;
-  if (nst < 2) return false;
-  at.nstage = nst;
+  at.slot_bytes = static_cast<uint32_t>(attn_slot_bytes(s.d, kvdt));
   at.guard = c->guard;
-  c->attn_splits_b1 = attn_splits(c, 1);
   return true;
 }
 
@@ -436,14 +444,12 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   c->ws = ws;
   c->seq_len = reinterpret_cast<int*>(ws + c->lay.seq_len);
   c->guard = reinterpret_cast<unsigned*>(ws + c->lay.guard);
-  c->attn_counter = reinterpret_cast<unsigned*>(ws + c->lay.attn_counter);
   c->am_counter = reinterpret_cast<unsigned*>(ws + c->lay.am_counter);
   c->rope = reinterpret_cast<float2*>(ws + c->lay.rope);
   c->resid = reinterpret_cast<float*>(ws + c->lay.resid);
   c->qkv = reinterpret_cast<float*>(ws + c->lay.qkv);
   c->attn_out = reinterpret_cast<float*>(ws + c->lay.attn_out);
   c->act = reinterpret_cast<float*>(ws + c->lay.act);
-  c->attn_part = reinterpret_cast<float*>(ws + c->lay.attn_part);
   c->am_val = reinterpret_cast<float*>(ws + c->lay.am_val);
   c->am_idx = reinterpret_cast<int*>(ws + c->lay.am_idx);
   c->embed = w->embed;
@@ -461,10 +467,17 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if ((e = packed_init_attrs()) || (e = attn_init_attrs())) {
+  if ((e = packed_init_attrs()) || (e = attn_init_attrs()) || (e = misc_init_attrs())) {
     g_init_error = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     delete c;
     return K2_ERR_CUDA;
+  }
+  c->attn_cluster_max = attn_max_cluster(c->s.d, c->s.rep, cfg->kv_dtype == K2_F32 ? 0 : cfg->kv_dtype,
+                                         kAttnMaxCluster);
+  if (c->attn_cluster_max < 1) {
+    g_init_error = "no thread-block cluster of the attention kernel fits this GPU";
+    delete c;
+    return K2_ERR_UNSUPPORTED;
   }
   // zero the state words (lengths, guard, counters) and build the rope table
   if ((e = cudaMemsetAsync(ws, 0, c->lay.rope, s)) ||
@@ -485,8 +498,6 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   }
   if (e == cudaSuccess)
     e = launch_pack(c->wlm(), w->lm_head, nullptr, nullptr, PACK_PLAIN, z.V, z.H, z.wb, 0, 0, 1, s);
-  if (e == cudaSuccess) e = cudaEventCreate(&c->ev[0]);
-  if (e == cudaSuccess) e = cudaEventCreate(&c->ev[1]);
   if (e != cudaSuccess) {
     g_init_error = std::string("repack: ") + cudaGetErrorString(e);
     delete c;
@@ -499,8 +510,7 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
 void k2_free(k2_ctx* c) {
   if (!c) return;
   for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
-  if (c->ev[0]) cudaEventDestroy(c->ev[0]);
-  if (c->ev[1]) cudaEventDestroy(c->ev[1]);
+  for (cudaEvent_t e : c->pev) cudaEventDestroy(e);
   delete c;
 }
 
@@ -679,7 +689,8 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
     case K2_OPT_PDL: c->pdl = value != 0; break;
     case K2_OPT_GRAPH: c->graph = value != 0; break;
     case K2_OPT_ATTN_SPLITS:
-      if (value < 0 || value > kSplitMax) return c->fail(K2_ERR_ARG, "splits %lld outside [0, %d]", (long long)value, kSplitMax);
+      if (value < 0 || value > kAttnMaxCluster)
+        return c->fail(K2_ERR_ARG, "splits %lld outside [0, %d]", (long long)value, kAttnMaxCluster);
       c->force_splits = static_cast<int>(value);
       break;
     default: return c->fail(K2_ERR_ARG, "unknown option %d", option);
@@ -697,9 +708,10 @@ k2_status k2_profile_decode(k2_ctx* c, const int32_t* d_tokens, int32_t batch, i
   for (int b = 0; b < batch; ++b)
     if (c->len[b] >= c->s.ctx)
       return c->fail(K2_ERR_CONTEXT_FULL, "sequence %d is at max_context %d", b, c->s.ctx);
-  Launcher ln{c, static_cast<cudaStream_t>(stream), false, ms, launches};
+  Launcher ln{c, static_cast<cudaStream_t>(stream), false};
+  ln.profile = true;
   enqueue_decode(c, ln, d_tokens, batch, d_next, nullptr);
-  if (ln.err) return c->cuda_fail(ln.err, "profile launch");
+  if (ln.collect(ms, launches) != cudaSuccess) return c->cuda_fail(ln.err, "profile launch");
   for (int b = 0; b < batch; ++b) c->len[b] += 1;
   return K2_OK;
 }

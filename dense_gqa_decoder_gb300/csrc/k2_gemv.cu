@@ -296,11 +296,11 @@ template <typename WT>
 cudaError_t set_smem_attr(size_t bytes) {
   cudaError_t e = cudaSuccess;
   const int b = static_cast<int>(bytes);
-  if ((e = cudaFuncSetAttribute(gemv_kernel<WT, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, b))) return e;
-  if ((e = cudaFuncSetAttribute(gemv_kernel<WT, EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, b))) return e;
-  if ((e = cudaFuncSetAttribute(gemv_kernel<WT, EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, b))) return e;
-  if ((e = cudaFuncSetAttribute(gemv_kernel<WT, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, b))) return e;
-  return cudaFuncSetAttribute(gemv_kernel<WT, EPI_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+  if ((e = set_kernel_smem(gemv_kernel<WT, EPI_STORE>, b))) return e;
+  if ((e = set_kernel_smem(gemv_kernel<WT, EPI_RESID>, b))) return e;
+  if ((e = set_kernel_smem(gemv_kernel<WT, EPI_QKV>, b))) return e;
+  if ((e = set_kernel_smem(gemv_kernel<WT, EPI_SWIGLU>, b))) return e;
+  return set_kernel_smem(gemv_kernel<WT, EPI_ARGMAX>, b);
 }
 
 }  // namespace

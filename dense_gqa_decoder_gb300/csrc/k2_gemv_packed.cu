@@ -112,25 +112,47 @@ __global__ void __launch_bounds__(kPackedThreads, 1) packed_gemv_kernel(const Pa
     for (int k = 0; k < NS && k < nslots; ++k) issue(k);
     rec_n[warp] = 0;
   }
+  // norm gains are weights: fetch them before waiting for the previous kernel
+  constexpr int PG = 4;   // float4s of the gain per thread kept in registers (K <= 4096)
+  constexpr int PX = 10;  // float4s of x per thread loaded at once (K <= 10240)
+  const int KP = CT * CH;
+  const int gsz = a.gain ? K / a.groups : K;
+  float4 gq[PG];
+#pragma unroll
+  for (int i = 0; i < PG; ++i) {
+    const int e = tid * 4 + i * kPackedThreads * 4;
+    gq[i] = (a.gain != nullptr && e < K) ? load_gain4<WT>(a.gain, e) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   __syncwarp();
   pdl_wait();
-  pdl_trigger();
 
   // ---- normalised x, lane-interleaved per chunk, zero past K ---------------------
+  // All loads of x are issued before any is used: one L2 round trip.
   {
-    const int gsz = a.gain ? K / a.groups : K;
-    float ssq[4] = {0.f, 0.f, 0.f, 0.f};
-    const int KP = CT * CH;
-    for (int e = tid * 4; e < KP; e += kPackedThreads * 4) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e < K) v = __ldcg(reinterpret_cast<const float4*>(a.x + e));
+    auto xidx = [&](int e) {
       const int c = e / CH, r = e - c * CH, l = r / EPL, j = r - l * EPL;
-      *reinterpret_cast<float4*>(xs + ((c * NPL + j / 4) * 32 + l) * 4) = v;
+      return ((c * NPL + j / 4) * 32 + l) * 4;
+    };
+    float ssq[4] = {0.f, 0.f, 0.f, 0.f};
+    auto add_ssq = [&](int e, float4 v) {
       const float t = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
       const int grp = e < K ? e / gsz : 4;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if (q == grp) ssq[q] += t;
+    };
+    float4 xq[PX];
+#pragma unroll
+    for (int i = 0; i < PX; ++i) {
+      const int e = tid * 4 + i * kPackedThreads * 4;
+      xq[i] = e < K ? __ldcg(reinterpret_cast<const float4*>(a.x + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < PX; ++i) add_ssq(tid * 4 + i * kPackedThreads * 4, xq[i]);
+    for (int e = tid * 4 + PX * kPackedThreads * 4; e < KP; e += kPackedThreads * 4) {
+      const float4 v = e < K ? __ldcg(reinterpret_cast<const float4*>(a.x + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(xs + xidx(e)) = v;
+      add_ssq(e, v);
     }
     if (a.gain != nullptr) {
 #pragma unroll
@@ -144,18 +166,39 @@ __global__ void __launch_bounds__(kPackedThreads, 1) packed_gemv_kernel(const Pa
         rs_sh[tid] = 1.0f / sqrtf(t / static_cast<float>(gsz) + a.eps);
       }
       __syncthreads();
-      for (int e = tid * 4; e < K; e += kPackedThreads * 4) {
-        const int c = e / CH, r = e - c * CH, l = r / EPL, j = r - l * EPL;
-        float4* p = reinterpret_cast<float4*>(xs + ((c * NPL + j / 4) * 32 + l) * 4);
+#pragma unroll
+      for (int i = 0; i < PX; ++i) {
+        const int e = tid * 4 + i * kPackedThreads * 4;
+        if (e < KP) {
+          float4 v = xq[i];
+          if (e < K) {
+            const float rs = rs_sh[e / gsz];
+            const float4 gn = i < PG ? gq[i < PG ? i : 0] : load_gain4<WT>(a.gain, e);
+            v.x = v.x * rs * gn.x; v.y = v.y * rs * gn.y; v.z = v.z * rs * gn.z; v.w = v.w * rs * gn.w;
+          }
+          *reinterpret_cast<float4*>(xs + xidx(e)) = v;
+        }
+      }
+      for (int e = tid * 4 + PX * kPackedThreads * 4; e < K; e += kPackedThreads * 4) {
+        float4* p = reinterpret_cast<float4*>(xs + xidx(e));
         const float rs = rs_sh[e / gsz];
         const float4 gn = load_gain4<WT>(a.gain, e);
         float4 v = *p;
         v.x = v.x * rs * gn.x; v.y = v.y * rs * gn.y; v.z = v.z * rs * gn.z; v.w = v.w * rs * gn.w;
         *p = v;
       }
+    } else {
+#pragma unroll
+      for (int i = 0; i < PX; ++i) {
+        const int e = tid * 4 + i * kPackedThreads * 4;
+        if (e < KP) *reinterpret_cast<float4*>(xs + xidx(e)) = xq[i];
+      }
     }
     __syncthreads();
   }
+  // the next kernel may start its weight prefetch now that this one's reads
+  // of the previous kernel's output are done
+  pdl_trigger();
 
   // ---- epilogue of one finished pair (lane 0 / thread 0) ----------------------------
   Best best{-INFINITY, 0x7fffffff};
@@ -375,15 +418,15 @@ cudaError_t launch_typed(const PackedGemvArgs& a, int epi, const cudaLaunchConfi
 template <typename WT>
 cudaError_t set_attr(int bytes) {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(packed_gemv_kernel<WT, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+  if ((e = set_kernel_smem(packed_gemv_kernel<WT, EPI_STORE>, bytes)))
     return e;
-  if ((e = cudaFuncSetAttribute(packed_gemv_kernel<WT, EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+  if ((e = set_kernel_smem(packed_gemv_kernel<WT, EPI_RESID>, bytes)))
     return e;
-  if ((e = cudaFuncSetAttribute(packed_gemv_kernel<WT, EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+  if ((e = set_kernel_smem(packed_gemv_kernel<WT, EPI_QKV>, bytes)))
     return e;
-  if ((e = cudaFuncSetAttribute(packed_gemv_kernel<WT, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+  if ((e = set_kernel_smem(packed_gemv_kernel<WT, EPI_SWIGLU>, bytes)))
     return e;
-  return cudaFuncSetAttribute(packed_gemv_kernel<WT, EPI_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return set_kernel_smem(packed_gemv_kernel<WT, EPI_ARGMAX>, bytes);
 }
 
 }  // namespace
@@ -402,7 +445,7 @@ int packed_grid(int N, int sms) {
   return g < 1 ? 1 : g;
 }
 
-bool packed_plan(PackedGemvArgs& a, int wbytes, size_t smem_budget) {
+bool packed_plan(PackedGemvArgs& a, int wbytes, size_t smem_budget, int max_slots) {
   if (wbytes != 2 && wbytes != 4) return false;
   const int EPL = 16 / wbytes;
   const int CH = 32 * EPL;
@@ -417,7 +460,7 @@ bool packed_plan(PackedGemvArgs& a, int wbytes, size_t smem_budget) {
     const size_t ns = ring / (static_cast<size_t>(kPackedWarps) * su * kUnitB);
     if (ns >= 2) {
       a.SU = su;
-      a.NS = static_cast<int>(ns > 3 ? 3 : ns);
+      a.NS = static_cast<int>(ns > static_cast<size_t>(max_slots) ? max_slots : ns);
       return true;
     }
   }

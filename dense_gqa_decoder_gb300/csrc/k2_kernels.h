@@ -58,6 +58,18 @@ struct GemvArgs {
   unsigned* guard;
 };
 constexpr int kGemvKcMax = 10;
+
+// Every kernel of the step asks for the largest shared-memory carveout, so
+// consecutive kernels never make an SM reconfigure its L1/shared split (which
+// needs the SM drained) and can be resident together under programmatic
+// dependent launch.
+template <typename Kernel>
+inline cudaError_t set_kernel_smem(Kernel kernel, int dyn_bytes) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
+}
 constexpr int kGemvThreads = 256;
 
 // chooses R / nslice / kc / stages for a weight shape; false if unsupported
@@ -104,7 +116,7 @@ constexpr int kPackedMaxSlots = 8;
 
 // bytes of the packed copy of an [N, K] matrix
 size_t packed_bytes(int N, int K, int wbytes);
-bool packed_plan(PackedGemvArgs& a, int wbytes, size_t smem_budget);
+bool packed_plan(PackedGemvArgs& a, int wbytes, size_t smem_budget, int max_slots);
 int packed_grid(int N, int sms);
 cudaError_t packed_init_attrs();
 cudaError_t launch_packed_gemv(const PackedGemvArgs& a, int wbytes, int epi, int grid, cudaStream_t s, bool pdl);
@@ -134,21 +146,21 @@ struct AttnArgs {
   int qkv_stride;
   int nq, nkv;
   const int* seq_len;
-  int seq0;          // sequences seq0 .. seq0 + gridDim.z - 1
-  float* part;       // [batch][nkv][nsplit][REP*(D+2)]
-  unsigned* counter; // [batch][nkv]
-  float* out;        // [batch][nq*D]
-  float scale;       // 1/sqrt(D)
-  int nstage;
-  uint32_t stage_bytes;
+  int seq0;             // sequences seq0 .. seq0 + gridDim.z - 1
+  float* out;           // [batch][nq*D]
+  float scale;          // 1/sqrt(D)
+  uint32_t slot_bytes;  // one warp's tile slot
   unsigned* guard;
 };
 constexpr int kAttnThreads = 256;
-constexpr int kAttnTK = 64;  // keys per tile
+constexpr int kAttnTK = 32;          // keys per tile; a warp reads one tile at a time
+constexpr int kAttnMaxCluster = 16;  // key-range splits of one KV head = one thread-block cluster
 
 bool attn_supported(int head_dim, int rep, int kv_dtype);
-size_t attn_stage_bytes(int head_dim, int kv_dtype);
+size_t attn_slot_bytes(int head_dim, int kv_dtype);
 cudaError_t attn_init_attrs();
+// largest cluster (<= limit) of this attention kernel that fits the GPU; 0 on error
+int attn_max_cluster(int head_dim, int rep, int kv_dtype, int limit);
 cudaError_t launch_attn(const AttnArgs& a, int head_dim, int rep, int kv_dtype, int nsplit, int batch,
                         cudaStream_t s, bool pdl);
 
@@ -163,5 +175,6 @@ cudaError_t launch_repack_qkv(void* dst, const void* wq, const void* wk, const v
 cudaError_t launch_repack_gateup(void* dst, const void* wg, const void* wu, int wbytes, int inter, int hidden,
                                  cudaStream_t s);
 cudaError_t launch_advance(int* seq_len, int seq0, int batch, cudaStream_t s, bool pdl);
+cudaError_t misc_init_attrs();
 
 }  // namespace k2

@@ -137,6 +137,13 @@ cudaError_t launch_repack_gateup(void* dst, const void* wg, const void* wu, int 
   return cudaGetLastError();
 }
 
+cudaError_t misc_init_attrs() {
+  cudaError_t e = set_kernel_smem(embed_kernel<__nv_bfloat16>, 0);
+  if (e == cudaSuccess) e = set_kernel_smem(embed_kernel<float>, 0);
+  if (e == cudaSuccess) e = set_kernel_smem(advance_kernel, 0);
+  return e;
+}
+
 cudaError_t launch_advance(int* seq_len, int seq0, int batch, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32 * ((batch + 31) / 32)), s, pdl, attr);

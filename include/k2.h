@@ -202,9 +202,10 @@ k2_status k2_set_option(k2_ctx* ctx, int32_t option, int64_t value);
 enum { K2_K_EMBED = 0, K2_K_QKV, K2_K_ATTN, K2_K_OPROJ, K2_K_GATEUP, K2_K_DOWN, K2_K_LMHEAD, K2_K_COUNT };
 
 /* One decode step (as k2_decode_step) launched without graph or PDL, with a
- * CUDA event pair around every kernel; waits for the stream and adds the
- * measured milliseconds of each kernel class to ms[K2_K_COUNT] and the number
- * of launches to launches[K2_K_COUNT]. */
+ * CUDA event pair around every kernel; all launches are queued first, then the
+ * call waits for the last event and adds the device milliseconds of each
+ * kernel class to ms[K2_K_COUNT] and the number of launches to
+ * launches[K2_K_COUNT]. */
 k2_status k2_profile_decode(k2_ctx* ctx, const int32_t* d_tokens, int32_t batch, int32_t* d_next, float* ms,
                             int32_t* launches, void* stream);
 
