@@ -23,6 +23,7 @@ constexpr size_t kGemvSmem = 104 * 1024;  // per-CTA budget: CTAs of two consecu
 constexpr size_t kAttnSmem = 128 * 1024;
 constexpr size_t kLmHeadSmem = 176 * 1024;
 constexpr int kArgmaxPartsMax = 1024;
+constexpr int kMegaSplitMax = 64;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -32,7 +33,7 @@ int elt_bytes(int dt) { return dt == K2_F32 ? 4 : (dt == K2_BF16 || dt == K2_F16
 // workspace layout
 // ---------------------------------------------------------------------------
 struct Layout {
-  size_t seq_len, guard, am_counter, rope, resid, qkv, attn_out, act, am_val, am_idx;
+  size_t seq_len, guard, am_counter, bar, rope, resid, qkv, attn_out, act, am_val, am_idx, attn_part, ltab;
   size_t wqkv, wo, wgu, wdown, wlm;  // packed weights; per-layer strides below
   size_t wqkv_layer, wo_layer, wgu_layer, wdown_layer;
   size_t kc, vc, ks, vs;  // first layer; per-layer stride kv_layer / sc_layer
@@ -72,6 +73,7 @@ Layout layout_of(const k2_config& c) {
   l.seq_len = take(sizeof(int) * s.B);
   l.guard = take(sizeof(unsigned));
   l.am_counter = take(sizeof(unsigned) * s.B);
+  l.bar = take(2 * sizeof(unsigned));  // persistent step: grid barrier arrivals, finished CTAs
   l.rope = take(sizeof(float2) * static_cast<size_t>(l.cap) * (s.d / 2));
   l.resid = take(sizeof(float) * static_cast<size_t>(s.B) * s.H);
   l.qkv = take(sizeof(float) * static_cast<size_t>(s.B) * s.qkv_n);
@@ -79,6 +81,8 @@ Layout layout_of(const k2_config& c) {
   l.act = take(sizeof(float) * static_cast<size_t>(s.B) * s.I);
   l.am_val = take(sizeof(float) * static_cast<size_t>(s.B) * kArgmaxPartsMax);
   l.am_idx = take(sizeof(int) * static_cast<size_t>(s.B) * kArgmaxPartsMax);
+  l.attn_part = take(sizeof(float) * static_cast<size_t>(s.nkv) * kMegaSplitMax * s.rep * (s.d + 2));
+  l.ltab = take(sizeof(LayerPtrs) * static_cast<size_t>(s.L));
   const size_t scratch_end = o;
   l.wqkv_layer = align_up(packed_bytes(s.qkv_n, s.H, s.wb), kAlign);
   l.wo_layer = align_up(packed_bytes(s.H, s.nq * s.d, s.wb), kAlign);
@@ -149,7 +153,7 @@ struct k2_ctx {
   unsigned* guard = nullptr;
   unsigned* am_counter = nullptr;
   float2* rope = nullptr;
-  float *resid = nullptr, *qkv = nullptr, *attn_out = nullptr, *act = nullptr,
+  float *resid = nullptr, *qkv = nullptr, *attn_out = nullptr, *act = nullptr, *attn_part = nullptr,
         *am_val = nullptr;
   int* am_idx = nullptr;
   // plans
@@ -162,6 +166,12 @@ struct k2_ctx {
   std::vector<int> len;
   bool pdl = true;
   bool graph = false;
+  // persistent batch-1 step
+  bool mega_ok = false;
+  bool use_mega = true;
+  int mega_grid = 0;
+  MegaArgs mega = {};
+  std::vector<LayerPtrs> ltab;
   std::map<std::tuple<int, const void*, const void*, const void*, void*>, cudaGraphExec_t> graphs;
   std::string err;
   // profiling: event pairs around the kernels of one step
@@ -312,10 +322,30 @@ void chain_b1(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in, int
   }
 }
 
+// One token of sequence seq: the persistent kernel when it can run, else the
+// kernel chain.
+void enqueue_token(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in, int* next, float* logits,
+                   bool head) {
+  if (c->mega_ok && c->use_mega) {
+    MegaArgs m = c->mega;
+    m.seq = seq;
+    m.token_in = tok;
+    m.token_out = next;
+    m.logits = logits;
+    m.x_ext = x_in;
+    m.head = head ? 1 : 0;
+    const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
+    cudaStream_t st = ln.s;
+    ln.run(K2_K_STEP, [&] { return launch_mega(m, c->s.wb, c->s.d, c->s.rep, kvdt, c->mega_grid, st); });
+  } else {
+    chain_b1(c, ln, seq, tok, x_in, next, logits, head);
+  }
+}
+
 void enqueue_decode(k2_ctx* c, Launcher& ln, const int* d_tokens, int batch, int* d_next, float* d_logits) {
   for (int b = 0; b < batch; ++b)
-    chain_b1(c, ln, b, d_tokens + b, nullptr, d_next + b,
-             d_logits ? d_logits + static_cast<size_t>(b) * c->s.V : nullptr, true);
+    enqueue_token(c, ln, b, d_tokens + b, nullptr, d_next + b,
+                  d_logits ? d_logits + static_cast<size_t>(b) * c->s.V : nullptr, true);
 }
 
 bool plan_all(k2_ctx* c) {
@@ -367,6 +397,89 @@ bool plan_all(k2_ctx* c) {
   at.slot_bytes = static_cast<uint32_t>(attn_slot_bytes(s.d, kvdt));
   at.guard = c->guard;
   return true;
+}
+
+// The persistent batch-1 step: supported shape, one CTA per SM, a device
+// table of per-layer pointers.  Leaves mega_ok false when it cannot run.
+cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
+  const Sizes& s = c->s;
+  const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
+  c->mega_ok = false;
+  if (!mega_supported(s.wb, s.d, s.rep, kvdt)) return cudaSuccess;
+  const PackedGemvArgs* plans[5] = {&c->p_qkv, &c->p_o, &c->p_gu, &c->p_down, &c->p_lm};
+  for (const PackedGemvArgs* p : plans)
+    if (p->x_bytes > static_cast<uint32_t>(kMegaXBytes)) return cudaSuccess;
+  cudaError_t e = mega_init_attrs(s.wb, s.d, s.rep, kvdt);
+  if (e != cudaSuccess) return e;
+  const int grid = mega_max_grid(s.wb, s.d, s.rep, kvdt);
+  if (grid < s.nkv) return cudaSuccess;
+  // the QKV and residual epilogues keep their CTA's pairs in shared memory
+  if ((s.qkv_n / 2 + grid - 1) / grid > kMegaPairsMax || ((s.H + 1) / 2 + grid - 1) / grid > kMegaPairsMax)
+    return cudaSuccess;
+  int nsplit = grid / s.nkv;
+  if (nsplit > kMegaSplitMax) nsplit = kMegaSplitMax;
+  if (nsplit > c->lay.cap / 8) nsplit = c->lay.cap / 8;
+  if (nsplit < 1) nsplit = 1;
+  c->ltab.resize(s.L);
+  for (int l = 0; l < s.L; ++l) {
+    LayerPtrs& t = c->ltab[l];
+    t.wqkv = c->wqkv(l);
+    t.wo = c->wop(l);
+    t.wgu = c->wgu(l);
+    t.wdown = c->wdown(l);
+    t.attn_norm = c->attn_norm[l];
+    t.mlp_norm = c->mlp_norm[l];
+    t.kc = c->kc(l);
+    t.vc = c->vc(l);
+    t.ks = c->ks(l);
+    t.vs = c->vs(l);
+  }
+  LayerPtrs* dtab = reinterpret_cast<LayerPtrs*>(c->ws + c->lay.ltab);
+  e = cudaMemcpyAsync(dtab, c->ltab.data(), sizeof(LayerPtrs) * s.L, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return e;
+  auto gplan = [&](const PackedGemvArgs& p) {
+    MegaGemv g;
+    g.CT = p.CT;
+    return g;
+  };
+  MegaArgs& m = c->mega;
+  m = {};
+  m.layers = dtab;
+  m.n_layers = s.L;
+  m.embed = c->embed;
+  m.lm_head = c->wlm();
+  m.final_norm = c->final_norm;
+  m.hidden = s.H;
+  m.vocab = s.V;
+  m.nq = s.nq;
+  m.nkv = s.nkv;
+  m.groups = s.G;
+  m.inter = s.I;
+  m.eps = c->cfg.eps;
+  m.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(s.d)));
+  m.g_qkv = gplan(c->p_qkv);
+  m.g_o = gplan(c->p_o);
+  m.g_gu = gplan(c->p_gu);
+  m.g_down = gplan(c->p_down);
+  m.g_lm = gplan(c->p_lm);
+  m.cap = c->lay.cap;
+  m.nsplit = nsplit;
+  m.rope = c->rope;
+  m.seq_len = c->seq_len;
+  m.resid = c->resid;
+  m.qkv = c->qkv;
+  m.attn_out = c->attn_out;
+  m.act = c->act;
+  m.part = c->attn_part;
+  m.am_val = c->am_val;
+  m.am_idx = c->am_idx;
+  m.am_counter = c->am_counter;
+  m.bar_count = reinterpret_cast<unsigned*>(c->ws + c->lay.bar);
+  m.end_count = m.bar_count + 1;
+  m.guard = c->guard;
+  c->mega_grid = grid;
+  c->mega_ok = true;
+  return cudaSuccess;
 }
 
 k2_status validate_weights(k2_ctx* c, const k2_weights* w) {
@@ -452,6 +565,7 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   c->act = reinterpret_cast<float*>(ws + c->lay.act);
   c->am_val = reinterpret_cast<float*>(ws + c->lay.am_val);
   c->am_idx = reinterpret_cast<int*>(ws + c->lay.am_idx);
+  c->attn_part = reinterpret_cast<float*>(ws + c->lay.attn_part);
   c->embed = w->embed;
   c->lm_head = w->lm_head;
   c->final_norm = w->final_norm;
@@ -503,6 +617,11 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     delete c;
     return K2_ERR_CUDA;
   }
+  if ((e = plan_mega(c, s)) != cudaSuccess) {
+    g_init_error = std::string("persistent step set-up: ") + cudaGetErrorString(e);
+    delete c;
+    return K2_ERR_CUDA;
+  }
   *out = c;
   return K2_OK;
 }
@@ -522,6 +641,8 @@ k2_status k2_get_info(const k2_ctx* c, k2_info* info) {
   info->num_sms = c->sms;
   info->attn_splits = attn_splits(c, 1);
   info->gemv_grid = c->grid_gu;
+  info->persistent_grid = c->mega_ok ? c->mega_grid : 0;
+  info->persistent_splits = c->mega_ok ? c->mega.nsplit : 0;
   info->kv_bytes = static_cast<int64_t>(c->lay.kv_bytes);
   info->repack_bytes = static_cast<int64_t>(c->lay.repack_bytes);
   info->scratch_bytes = static_cast<int64_t>(c->lay.total - c->lay.kv_bytes - c->lay.repack_bytes);
@@ -540,7 +661,7 @@ k2_status k2_prefill(k2_ctx* c, int32_t seq, const int32_t* d_tokens, int32_t n,
   Launcher ln{c, static_cast<cudaStream_t>(stream), c->pdl};
   for (int i = 0; i < n; ++i) {
     const bool last = i == n - 1;
-    chain_b1(c, ln, seq, d_tokens + i, nullptr, d_next_token, last ? d_logits : nullptr, last);
+    enqueue_token(c, ln, seq, d_tokens + i, nullptr, d_next_token, last ? d_logits : nullptr, last);
   }
   if (ln.err != cudaSuccess) return c->cuda_fail(ln.err, "prefill launch");
   c->len[seq] += n;
@@ -599,7 +720,7 @@ k2_status k2_decode_layers(k2_ctx* c, float* d_x, int32_t batch, void* stream) {
       return c->fail(K2_ERR_CONTEXT_FULL, "sequence %d is at max_context %d", b, c->s.ctx);
   Launcher ln{c, static_cast<cudaStream_t>(stream), c->pdl};
   for (int b = 0; b < batch; ++b)
-    chain_b1(c, ln, b, nullptr, d_x + static_cast<size_t>(b) * c->s.H, nullptr, nullptr, false);
+    enqueue_token(c, ln, b, nullptr, d_x + static_cast<size_t>(b) * c->s.H, nullptr, nullptr, false);
   if (ln.err) return c->cuda_fail(ln.err, "layers launch");
   for (int b = 0; b < batch; ++b) c->len[b] += 1;
   return K2_OK;
@@ -679,6 +800,8 @@ k2_status k2_sync_status(k2_ctx* c, void* stream) {
 k2_status k2_clear_status(k2_ctx* c, void* stream) {
   if (!c) return K2_ERR_ARG;
   cudaError_t e = cudaMemsetAsync(c->guard, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream));
+  // a step cut short by a timeout may have left the grid barrier half counted
+  if (!e) e = cudaMemsetAsync(c->ws + c->lay.bar, 0, 2 * sizeof(unsigned), static_cast<cudaStream_t>(stream));
   if (e) return c->cuda_fail(e, "clear_status");
   return K2_OK;
 }
@@ -688,6 +811,7 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
   switch (option) {
     case K2_OPT_PDL: c->pdl = value != 0; break;
     case K2_OPT_GRAPH: c->graph = value != 0; break;
+    case K2_OPT_PERSISTENT: c->use_mega = value != 0; break;
     case K2_OPT_ATTN_SPLITS:
       if (value < 0 || value > kAttnMaxCluster)
         return c->fail(K2_ERR_ARG, "splits %lld outside [0, %d]", (long long)value, kAttnMaxCluster);

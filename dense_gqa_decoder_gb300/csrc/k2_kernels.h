@@ -165,6 +165,69 @@ cudaError_t launch_attn(const AttnArgs& a, int head_dim, int rep, int kv_dtype, 
                         cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------------------
+// persistent batch-1 decode step (one cooperative launch per token)
+// ---------------------------------------------------------------------------
+struct LayerPtrs {
+  const void* wqkv;  // packed
+  const void* wo;
+  const void* wgu;
+  const void* wdown;
+  const void* attn_norm;
+  const void* mlp_norm;
+  void* kc;  // K/V cache of the layer [batch][nkv][cap][D] and int8 scales
+  void* vc;
+  void* ks;
+  void* vs;
+};
+struct MegaGemv {
+  int CT;  // 512-byte chunks per row (the packed layout)
+};
+struct MegaArgs {
+  const LayerPtrs* layers;  // device table [n_layers]
+  int n_layers;
+  const void* embed;
+  const void* lm_head;  // packed
+  const void* final_norm;
+  int hidden, vocab, nq, nkv, groups, inter;
+  float eps, scale;
+  MegaGemv g_qkv, g_o, g_gu, g_down, g_lm;
+  int cap, nsplit;
+  const float2* rope;
+  int* seq_len;
+  int seq;
+  const int* token_in;
+  int* token_out;
+  float* logits;
+  float* x_ext;  // caller's residual stream (layers only), else null
+  int head;      // 1: final norm + lm_head + argmax
+  float* resid;
+  float* qkv;
+  float* attn_out;
+  float* act;
+  float* part;  // attention partials [nkv * nsplit][REP * (D + 2)]
+  float* am_val;
+  int* am_idx;
+  unsigned* am_counter;
+  unsigned* bar_count;  // grid barrier arrivals of the current launch (0 between launches)
+  unsigned* end_count;  // CTAs finished (0 between launches)
+  unsigned* guard;
+};
+constexpr int kMegaThreads = 256;
+constexpr int kMegaSlots = 2;                 // ring slots per warp
+constexpr int kMegaSlotBytes = 10 * 1024;     // one bulk copy: 10 packed units, or one 16-key K/V tile
+constexpr int kMegaRingBytes = 8 * kMegaSlots * kMegaSlotBytes;
+constexpr int kMegaXBytes = 40 * 1024;        // the normalised input vector (K <= 10240 at bf16)
+constexpr int kMegaSmemBytes = kMegaRingBytes + kMegaXBytes;
+constexpr int kMegaTK = 16;                   // keys per attention tile (at most)
+constexpr int kMegaPairsMax = 64;             // row pairs of one CTA in the QKV / residual phases
+
+bool mega_supported(int wbytes, int head_dim, int rep, int kv_dtype);
+cudaError_t mega_init_attrs(int wbytes, int head_dim, int rep, int kv_dtype);
+int mega_max_grid(int wbytes, int head_dim, int rep, int kv_dtype);  // 0: cannot run
+cudaError_t launch_mega(const MegaArgs& a, int wbytes, int head_dim, int rep, int kv_dtype, int grid,
+                        cudaStream_t s);
+
+// ---------------------------------------------------------------------------
 // small kernels
 // ---------------------------------------------------------------------------
 cudaError_t launch_embed(const void* E, int wbytes, int vocab, int hidden, const int* tokens, int batch,

@@ -106,6 +106,8 @@ typedef struct {
   int64_t kv_bytes;      /* bytes of the KV cache region */
   int64_t repack_bytes;  /* bytes of the packed projection weights */
   int64_t scratch_bytes; /* everything else in the workspace */
+  int32_t persistent_grid;   /* CTAs of the persistent batch-1 step (0: not available) */
+  int32_t persistent_splits; /* its key-range splits per KV head */
 } k2_info;
 
 /* ---- set-up -------------------------------------------------------------- */
@@ -194,12 +196,16 @@ typedef enum {
   K2_OPT_PDL = 0,         /* 1 (default): programmatic dependent launch between kernels */
   K2_OPT_GRAPH = 1,       /* 1: k2_decode_step records a CUDA graph per (batch, buffers,
                              stream) on first use and replays it (stream must not be NULL) */
-  K2_OPT_ATTN_SPLITS = 2  /* > 0: force the number of attention key splits (tests) */
+  K2_OPT_ATTN_SPLITS = 2, /* > 0: force the number of attention key splits of the kernel chain (tests) */
+  K2_OPT_PERSISTENT = 3   /* 1 (default): batch-1 tokens run as one persistent cooperative kernel
+                             (one CTA per SM, grid barriers between the phases of a layer) when the
+                             shape allows; 0: always the chain of per-step kernels */
 } k2_option;
 k2_status k2_set_option(k2_ctx* ctx, int32_t option, int64_t value);
 
 /* Kernel classes timed by k2_profile_decode. */
-enum { K2_K_EMBED = 0, K2_K_QKV, K2_K_ATTN, K2_K_OPROJ, K2_K_GATEUP, K2_K_DOWN, K2_K_LMHEAD, K2_K_COUNT };
+enum { K2_K_EMBED = 0, K2_K_QKV, K2_K_ATTN, K2_K_OPROJ, K2_K_GATEUP, K2_K_DOWN, K2_K_LMHEAD, K2_K_STEP, K2_K_COUNT };
+/* K2_K_STEP: a whole token run by the persistent kernel */
 
 /* One decode step (as k2_decode_step) launched without graph or PDL, with a
  * CUDA event pair around every kernel; all launches are queued first, then the
