@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <string>
 #include <tuple>
@@ -33,7 +34,8 @@ int elt_bytes(int dt) { return dt == K2_F32 ? 4 : (dt == K2_BF16 || dt == K2_F16
 // workspace layout
 // ---------------------------------------------------------------------------
 struct Layout {
-  size_t seq_len, guard, am_counter, bar, rope, resid, qkv, attn_out, act, am_val, am_idx, attn_part, ltab;
+  size_t seq_len, guard, am_counter, msync, rope, resid, qkv, attn_out, act, am_val, am_idx, attn_part, ltab;
+  size_t t_resid, t_qkv, t_attn, t_act;  // persistent step: (value, tag) activations
   size_t wqkv, wo, wgu, wdown, wlm;  // packed weights; per-layer strides below
   size_t wqkv_layer, wo_layer, wgu_layer, wdown_layer;
   size_t kc, vc, ks, vs;  // first layer; per-layer stride kv_layer / sc_layer
@@ -73,7 +75,8 @@ Layout layout_of(const k2_config& c) {
   l.seq_len = take(sizeof(int) * s.B);
   l.guard = take(sizeof(unsigned));
   l.am_counter = take(sizeof(unsigned) * s.B);
-  l.bar = take(2 * sizeof(unsigned));  // persistent step: grid barrier arrivals, finished CTAs
+  // persistent step: finished CTAs, launch epoch, per-KV-head finished splits
+  l.msync = take(sizeof(unsigned) * (2 + static_cast<size_t>(s.nkv)));
   l.rope = take(sizeof(float2) * static_cast<size_t>(l.cap) * (s.d / 2));
   l.resid = take(sizeof(float) * static_cast<size_t>(s.B) * s.H);
   l.qkv = take(sizeof(float) * static_cast<size_t>(s.B) * s.qkv_n);
@@ -83,6 +86,10 @@ Layout layout_of(const k2_config& c) {
   l.am_idx = take(sizeof(int) * static_cast<size_t>(s.B) * kArgmaxPartsMax);
   l.attn_part = take(sizeof(float) * static_cast<size_t>(s.nkv) * kMegaSplitMax * s.rep * (s.d + 2));
   l.ltab = take(sizeof(LayerPtrs) * static_cast<size_t>(s.L));
+  l.t_resid = take(8 * static_cast<size_t>(s.H));
+  l.t_qkv = take(8 * static_cast<size_t>(s.qkv_n));
+  l.t_attn = take(8 * static_cast<size_t>(s.nq) * s.d);
+  l.t_act = take(8 * static_cast<size_t>(s.I));
   const size_t scratch_end = o;
   l.wqkv_layer = align_up(packed_bytes(s.qkv_n, s.H, s.wb), kAlign);
   l.wo_layer = align_up(packed_bytes(s.H, s.nq * s.d, s.wb), kAlign);
@@ -333,6 +340,7 @@ void enqueue_token(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in
     m.token_out = next;
     m.logits = logits;
     m.x_ext = x_in;
+    m.x_out = x_in ? x_in : c->resid + static_cast<size_t>(seq) * c->s.H;
     m.head = head ? 1 : 0;
     const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
     cudaStream_t st = ln.s;
@@ -411,15 +419,24 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
     if (p->x_bytes > static_cast<uint32_t>(kMegaXBytes)) return cudaSuccess;
   cudaError_t e = mega_init_attrs(s.wb, s.d, s.rep, kvdt);
   if (e != cudaSuccess) return e;
-  const int grid = mega_max_grid(s.wb, s.d, s.rep, kvdt);
+  int grid = mega_max_grid(s.wb, s.d, s.rep, kvdt);
+  // every CTA must own rows of every layer GEMV (the dataflow waits rely on it)
+  grid = std::min(grid, std::min(s.qkv_n / 2, std::min((s.H + 1) / 2, s.I)));
   if (grid < s.nkv) return cudaSuccess;
   // the QKV and residual epilogues keep their CTA's pairs in shared memory
   if ((s.qkv_n / 2 + grid - 1) / grid > kMegaPairsMax || ((s.H + 1) / 2 + grid - 1) / grid > kMegaPairsMax)
     return cudaSuccess;
+  // inputs are polled in groups of four words
+  if (s.H % 4 || (s.nq * s.d) % 4 || s.I % 4) return cudaSuccess;
+  // tags carry the phase index in kMegaTagShift bits
+  if (5 * s.L + 1 >= (1 << kMegaTagShift)) return cudaSuccess;
+  // the merging CTA stages every split's partial in the 40 KB input buffer
+  const size_t part_bytes = sizeof(float) * static_cast<size_t>(s.rep) * (s.d + 2);
   int nsplit = grid / s.nkv;
+  nsplit = std::min(nsplit, static_cast<int>(kMegaXBytes / part_bytes));
   if (nsplit > kMegaSplitMax) nsplit = kMegaSplitMax;
   if (nsplit > c->lay.cap / 8) nsplit = c->lay.cap / 8;
-  if (nsplit < 1) nsplit = 1;
+  if (nsplit < 1) return cudaSuccess;
   c->ltab.resize(s.L);
   for (int l = 0; l < s.L; ++l) {
     LayerPtrs& t = c->ltab[l];
@@ -466,16 +483,17 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   m.nsplit = nsplit;
   m.rope = c->rope;
   m.seq_len = c->seq_len;
-  m.resid = c->resid;
-  m.qkv = c->qkv;
-  m.attn_out = c->attn_out;
-  m.act = c->act;
+  m.x_out = c->resid;
+  m.t_resid = reinterpret_cast<unsigned long long*>(c->ws + c->lay.t_resid);
+  m.t_qkv = reinterpret_cast<unsigned long long*>(c->ws + c->lay.t_qkv);
+  m.t_attn = reinterpret_cast<unsigned long long*>(c->ws + c->lay.t_attn);
+  m.t_act = reinterpret_cast<unsigned long long*>(c->ws + c->lay.t_act);
   m.part = c->attn_part;
   m.am_val = c->am_val;
   m.am_idx = c->am_idx;
-  m.am_counter = c->am_counter;
-  m.bar_count = reinterpret_cast<unsigned*>(c->ws + c->lay.bar);
-  m.end_count = m.bar_count + 1;
+  m.end_count = reinterpret_cast<unsigned*>(c->ws + c->lay.msync);
+  m.epoch = m.end_count + 1;
+  m.hcnt = m.end_count + 2;
   m.guard = c->guard;
   c->mega_grid = grid;
   c->mega_ok = true;
@@ -594,7 +612,10 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     return K2_ERR_UNSUPPORTED;
   }
   // zero the state words (lengths, guard, counters) and build the rope table
+  // and the tagged activations (a fresh context must not see an old tag)
   if ((e = cudaMemsetAsync(ws, 0, c->lay.rope, s)) ||
+      (e = cudaMemsetAsync(ws + c->lay.t_resid, 0, c->lay.t_act + 8 * static_cast<size_t>(c->s.I) - c->lay.t_resid,
+                           s)) ||
       (e = launch_rope_table(c->rope, c->lay.cap, c->s.d, static_cast<double>(cfg->rope_theta), s))) {
     g_init_error = std::string("init: ") + cudaGetErrorString(e);
     delete c;
@@ -801,7 +822,11 @@ k2_status k2_clear_status(k2_ctx* c, void* stream) {
   if (!c) return K2_ERR_ARG;
   cudaError_t e = cudaMemsetAsync(c->guard, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream));
   // a step cut short by a timeout may have left the grid barrier half counted
-  if (!e) e = cudaMemsetAsync(c->ws + c->lay.bar, 0, 2 * sizeof(unsigned), static_cast<cudaStream_t>(stream));
+  // finished-CTA and per-head split counters (not the epoch: tags must stay fresh)
+  if (!e) e = cudaMemsetAsync(c->ws + c->lay.msync, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream));
+  if (!e)
+    e = cudaMemsetAsync(c->ws + c->lay.msync + 2 * sizeof(unsigned), 0, sizeof(unsigned) * c->s.nkv,
+                        static_cast<cudaStream_t>(stream));
   if (e) return c->cuda_fail(e, "clear_status");
   return K2_OK;
 }

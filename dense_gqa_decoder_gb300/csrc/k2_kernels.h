@@ -183,7 +183,7 @@ struct MegaGemv {
   int CT;  // 512-byte chunks per row (the packed layout)
 };
 struct MegaArgs {
-  const LayerPtrs* layers;  // device table [n_layers]
+  const LayerPtrs* layers;  // device table, n_layers entries
   int n_layers;
   const void* embed;
   const void* lm_head;  // packed
@@ -197,19 +197,22 @@ struct MegaArgs {
   int seq;
   const int* token_in;
   int* token_out;
-  float* logits;
-  float* x_ext;  // caller's residual stream (layers only), else null
-  int head;      // 1: final norm + lm_head + argmax
-  float* resid;
-  float* qkv;
-  float* attn_out;
-  float* act;
-  float* part;  // attention partials [nkv * nsplit][REP * (D + 2)]
-  float* am_val;
+  float* logits;     // optional
+  float* x_ext;      // layers-only step: the hidden vector in and out; else null
+  float* x_out;      // plain fp32 copy of the residual leaving the last layer
+  int head;          // 1: final norm + lm_head + argmax after the layers
+  // activations as (value, tag) words: a consumer waits for the tag of the
+  // phase that writes them
+  unsigned long long* t_resid;
+  unsigned long long* t_qkv;
+  unsigned long long* t_attn;
+  unsigned long long* t_act;
+  float* part;       // attention partials [nkv * nsplit][rep * (d + 2)]
+  float* am_val;     // per-CTA argmax partials
   int* am_idx;
-  unsigned* am_counter;
-  unsigned* bar_count;  // grid barrier arrivals of the current launch (0 between launches)
-  unsigned* end_count;  // CTAs finished (0 between launches)
+  unsigned* hcnt;    // per KV head: splits finished in this launch
+  unsigned* end_count;
+  unsigned* epoch;   // launches so far (tags are derived from it)
   unsigned* guard;
 };
 constexpr int kMegaThreads = 256;
@@ -220,6 +223,7 @@ constexpr int kMegaXBytes = 40 * 1024;        // the normalised input vector (K 
 constexpr int kMegaSmemBytes = kMegaRingBytes + kMegaXBytes;
 constexpr int kMegaTK = 16;                   // keys per attention tile (at most)
 constexpr int kMegaPairsMax = 64;             // row pairs of one CTA in the QKV / residual phases
+constexpr int kMegaTagShift = 10;             // tag = (epoch + 1) << 10 | phase: at most 1023 phases
 
 bool mega_supported(int wbytes, int head_dim, int rep, int kv_dtype);
 cudaError_t mega_init_attrs(int wbytes, int head_dim, int rep, int kv_dtype);

@@ -8,30 +8,35 @@
 // their time to ramp-up and tails, and under programmatic dependent launch
 // the CTAs of a new kernel land on whatever SMs have room (measured: GEMV
 // CTAs doubled up on 64-74 SMs while others idled).  Here every phase uses
-// all SMs once and phases are separated by a grid barrier.
+// all SMs once.
 //
-// The weights and cached K/V rows never depend on the activations, so each
-// warp streams them continuously: its producer lane walks one fixed sequence
-// of 10 KB slots spanning every phase of the step (its share of the QKV
-// weights, then its K/V tiles, then its o_proj, gate/up, down weights, then
-// the next layer's ...) and refills a ring slot as soon as it is consumed.
-// The next phase's data is therefore already in flight while the CTAs meet
-// at a barrier and rebuild the input vector.  Each refill is one bulk TMA
-// copy (cp.async.bulk, mbarrier complete_tx) of a contiguous run of the
-// packed weights (pairs of rows in 512-byte chunks) or of one 16-key K/V
-// tile; a probe on this GPU streamed 6.9-7.4 TB/s with this consumer and
-// 5-10 KB copies.
+// Streaming: the weights and cached K/V rows never depend on the
+// activations, so each warp streams them continuously: its producer lane
+// walks one fixed sequence of 10 KB slots spanning every phase of the step
+// (its share of the QKV weights, then its K/V tiles, then its o_proj,
+// gate/up, down weights, then the next layer's ...) and refills a ring slot
+// as soon as it is consumed.  Each refill is one bulk copy (cp.async.bulk,
+// mbarrier complete_tx) of a contiguous run of the packed weights (pairs of
+// rows in 512-byte chunks) or of one K/V tile.
+//
+// Synchronisation is dataflow, not grid barriers: every activation element
+// is stored as one 64-bit word (fp32 value, 32-bit tag) with a relaxed
+// gpu-scope store, the tag naming the launch and the phase that wrote it.
+// A consumer loads the words it needs and retries those whose tag is not yet
+// the producer phase's; a 64-bit access is single-copy atomic, so a matching
+// tag carries its value.  This folds "wait for the phase" and "load the
+// input" into one L2 round trip.  Reuse of a buffer is safe because every
+// CTA owns rows of every GEMV output (the grid is never larger than the
+// smallest pair count): a CTA can only overwrite a buffer after it has seen
+// outputs that every CTA wrote after its last read of that buffer.
 //
 // Phases of a layer: QKV GEMV (+ GroupedRMSNorm, + split-half RoPE) | GQA
-// attention partials per (KV head, key split) with the KV append | split merge
-// | o_proj GEMV + residual | gate/up GEMV + SwiGLU | down GEMV + residual.
-// Then final norm + lm_head GEMV + first-index argmax (kimi-k3-in-c k3_run.c,
-// `argmax_`).
-//
-// Memory model: a phase's outputs are written with ordinary stores; the grid
-// barrier (CTA barrier, gpu-scope fence, release add, acquire poll) orders
-// them before every read in later phases, and those reads go to L2 (ld.cg or
-// TMA), never to a possibly stale L1 line.  Every wait is bounded.
+// attention partials per (KV head, key split) with the KV append, merged by
+// the last split of each KV head | o_proj GEMV + residual | gate/up GEMV +
+// SwiGLU | down GEMV + residual.  Then final norm + lm_head GEMV +
+// first-index argmax (kimi-k3-in-c k3_run.c, `argmax_`).  The residual rows
+// of a CTA stay in its shared memory from one residual phase to the next.
+// Every wait is bounded (GUARD_TIMEOUT).
 #include <math.h>
 
 #include <type_traits>
@@ -49,6 +54,7 @@ constexpr int NS = kMegaSlots;
 constexpr int SB = kMegaSlotBytes;
 constexpr int kUnit = 1024;      // one packed unit: a 512-byte chunk of both rows of a pair
 constexpr int SU = SB / kUnit;   // packed units per slot
+constexpr int PX = 10;           // float4 groups of the input vector per thread (K <= 10240)
 // keys per attention tile: the K and V rows (plus int8 scales) fit one slot
 template <int D, typename KVT>
 constexpr int tile_keys() {
@@ -56,8 +62,8 @@ constexpr int tile_keys() {
          : (2 * (kMegaTK / 2) * D * static_cast<int>(sizeof(KVT)) + 4 * (kMegaTK / 2) <= SB) ? kMegaTK / 2
                                                                                                : 0;
 }
-constexpr int kPhases = 6;       // per layer: QKV, ATTN, MERGE, O, GU, DOWN
-enum { PH_QKV = 0, PH_ATTN = 1, PH_MERGE = 2, PH_O = 3, PH_GU = 4, PH_DOWN = 5 };
+constexpr int kPhases = 5;       // per layer: QKV, ATTN, O, GU, DOWN
+enum { PH_QKV = 0, PH_ATTN = 1, PH_O = 2, PH_GU = 3, PH_DOWN = 4 };
 
 struct Best {
   float v;
@@ -78,13 +84,69 @@ __device__ __forceinline__ Best warp_best(Best p) {
   return p;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
+// ---- tagged activations ----------------------------------------------------------------------
+typedef unsigned long long u64;
+__device__ __forceinline__ void st_tagged(u64* p, float v, uint32_t tag) {
+  const u64 w = (static_cast<u64>(tag) << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
-__device__ __forceinline__ void red_release_add_u32(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void ld_tagged2(const u64* p, u64& w0, u64& w1) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(p) : "memory");
+}
+__device__ __forceinline__ u64 ld_tagged(const u64* p) {
+  u64 w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+__device__ __forceinline__ bool tag_is(u64 w, uint32_t tag) { return static_cast<uint32_t>(w >> 32) == tag; }
+__device__ __forceinline__ float tag_val(u64 w) { return __uint_as_float(static_cast<uint32_t>(w)); }
+
+// Bounded retry loop: false (and GUARD_TIMEOUT) once the wait has run out.
+struct Patience {
+  uint64_t t0 = 0;
+  __device__ __forceinline__ bool more(unsigned* guard) {
+    const uint64_t t = globaltimer();
+    if (t0 == 0) t0 = t;
+    if (t - t0 > kWaitLimitNs) {
+      atomicOr(guard, GUARD_TIMEOUT);
+      return false;
+    }
+    return true;
+  }
+};
+
+// x[e .. e+3] for e = tid * 4 + i * MT * 4 (i < PX, e < K) from tagged words.
+__device__ bool poll_x(const u64* tv, int K, uint32_t tag, float4* xq, unsigned* guard) {
+  const int tid = threadIdx.x;
+  unsigned pend = 0;
+#pragma unroll
+  for (int i = 0; i < PX; ++i) {
+    xq[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid * 4 + i * MT * 4 < K) pend |= 1u << i;
+  }
+  Patience wait;
+  while (pend) {
+    u64 w[PX][4];
+#pragma unroll
+    for (int i = 0; i < PX; ++i) {  // every load first, then the checks
+      w[i][0] = w[i][1] = w[i][2] = w[i][3] = 0;
+      if (pend & (1u << i)) {
+        const u64* p = tv + tid * 4 + i * MT * 4;
+        ld_tagged2(p, w[i][0], w[i][1]);
+        ld_tagged2(p + 2, w[i][2], w[i][3]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < PX; ++i) {
+      if ((pend & (1u << i)) && tag_is(w[i][0], tag) && tag_is(w[i][1], tag) && tag_is(w[i][2], tag) &&
+          tag_is(w[i][3], tag)) {
+        xq[i] = make_float4(tag_val(w[i][0]), tag_val(w[i][1]), tag_val(w[i][2]), tag_val(w[i][3]));
+        pend &= ~(1u << i);
+      }
+    }
+    if (pend && !wait.more(guard)) return false;
+  }
+  return true;
 }
 
 struct MegaShared {
@@ -96,37 +158,11 @@ struct MegaShared {
   int rec_n[MW];
   Best best[MW];
   int flag;
-  int ok;
-  float rsd[2 * kMegaPairsMax];     // residual rows of this CTA (RESID phases)
+  float rsd[2 * kMegaPairsMax];     // this CTA's residual rows, kept from one residual phase to the next
   float2 rope[kMegaPairsMax];       // (cos, sin) of this CTA's pairs (QKV phase)
-  float newkv[2][128];              // the new token's K and V rows (attention, head_dim <= 128)
+  float qs[512];                    // the query heads of one KV head, scaled (rep * head_dim <= 512)
+  float newkv[2][128];              // the new token's K and V rows (head_dim <= 128)
 };
-
-// Grid barrier number bi of this launch: every CTA adds one to the arrival
-// counter and waits until it reaches (bi + 1) * gridDim.x.  The counter is
-// set back to 0 by the last CTA of the launch.  False if the wait ran out.
-__device__ bool grid_sync(const MegaArgs& a, MegaShared& sh, int bi) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned target = static_cast<unsigned>(bi + 1) * gridDim.x;
-    __threadfence();
-    red_release_add_u32(a.bar_count, 1u);
-    int ok = 1;
-    if (ld_acquire_u32(a.bar_count) < target) {
-      const uint64_t t0 = globaltimer();
-      while (ld_acquire_u32(a.bar_count) < target) {
-        if (globaltimer() - t0 > kWaitLimitNs) {
-          atomicOr(a.guard, GUARD_TIMEOUT);
-          ok = 0;
-          break;
-        }
-      }
-    }
-    sh.ok = ok;
-  }
-  __syncthreads();
-  return sh.ok != 0;
-}
 
 // ---- static description of the step ------------------------------------------------
 struct GDesc {
@@ -220,7 +256,6 @@ struct Stream {
     attn = false;
     if (q > lastq) return;
     const int l = q / kPhases, j = q - (q / kPhases) * kPhases;
-    if (l < a.n_layers && j == PH_MERGE) return;
     if (l < a.n_layers && j == PH_ATTN) {
       if (cta >= a.nkv * a.nsplit) return;
       const AItem it = a_item<TKM>(a, cta, pos + 1);
@@ -303,15 +338,16 @@ struct Stream {
 };
 
 struct GEpi {
-  int epi;  // EPI_QKV, EPI_RESID, EPI_SWIGLU or EPI_ARGMAX
-  float* out;
+  int epi;          // EPI_QKV, EPI_RESID, EPI_SWIGLU or EPI_ARGMAX
+  u64* out;         // tagged output
+  float* plain;     // RESID: also a plain fp32 copy (the residual leaving the last layer)
   const float2* rope;
   int pos;
   int head_dim;
   int n_rot;
   float* logits;
-  float* resid_init;  // layer 0: CTA 0 stores the raw embedding row here
   unsigned* guard;
+  uint32_t tag;     // written with this tag
 };
 
 template <typename WT>
@@ -325,18 +361,24 @@ template <>
 __device__ __forceinline__ float4 load4_weight<float>(const float* p, int e) {
   return __ldg(reinterpret_cast<const float4*>(p + e));
 }
+template <typename WT>
+__device__ __forceinline__ float load1(const WT* p, size_t e) {
+  return to_f32(p[e]);
+}
 
-// One GEMV phase: rebuild x in shared memory, then consume this warp's slots
-// (already in flight) and refill the ring from the stream.  x comes from xg
-// (fp32, written by an earlier phase) or from xe (an embedding row).
+// One GEMV phase: build x in shared memory (waiting for its tags), then
+// consume this warp's slots (already in flight) and refill the ring from the
+// stream.  x comes from xt (tagged, written by the previous phase with tag
+// tag_in) or, in the first phase, from x0f (fp32) or x0w (an embedding row).
+// rsd0f / rsd0w: where the first residual phase takes its old residual rows.
 template <typename WT, int D, typename KVT>
-__device__ bool g_phase(const MegaArgs& a, const GDesc& d, const float* xg, const WT* xe, const GEpi& ep,
-                        uint8_t* smem, MegaShared& sh, Stream<D, KVT>& st, int& consumed, Best& best, int cta, int G,
-                        int pos, int qkv_n) {
+__device__ bool g_phase(const MegaArgs& a, const GDesc& d, const u64* xt, uint32_t tag_in, const float* x0f,
+                        const WT* x0w, const float* rsd0f, const WT* rsd0w, const GEpi& ep, uint8_t* smem,
+                        MegaShared& sh, Stream<D, KVT>& st, int& consumed, Best& best, int cta, int G, int pos,
+                        int qkv_n) {
   constexpr int EPL = Unpack<WT>::N;
   constexpr int CH = 32 * EPL;
   constexpr int NPL = EPL / 4;
-  constexpr int PX = 10;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = d.K, CT = d.CT;
   float* xs = reinterpret_cast<float*>(smem + kMegaRingBytes);
@@ -345,38 +387,27 @@ __device__ bool g_phase(const MegaArgs& a, const GDesc& d, const float* xg, cons
   if (lane == 0) sh.rec_n[warp] = 0;
 
   // ---- x, normalised if the phase has a gain, lane-interleaved per chunk
+  bool bad = false;
   {
-    const int KP = CT * CH;
+    const int KP = CT * CH;  // <= PX * MT * 4
     const int gsz = d.gain ? K / a.groups : K;
     auto xidx = [&](int e) {
       const int c = e / CH, rr = e - c * CH, l = rr / EPL, j = rr - l * EPL;
       return ((c * NPL + j / 4) * 32 + l) * 4;
     };
-    auto load4 = [&](int e) -> float4 {
-      if (e >= K) return make_float4(0.f, 0.f, 0.f, 0.f);
-      if (xg) return __ldcg(reinterpret_cast<const float4*>(xg + e));
-      return load4_weight<WT>(xe, e);
-    };
-    float ssq[4] = {0.f, 0.f, 0.f, 0.f};
-    auto add_ssq = [&](int e, float4 v) {
-      const float t = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-      const int grp = e < K ? e / gsz : 4;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (q == grp) ssq[q] += t;
-    };
-    // everything this phase reads from L2 is requested at once: x, the gain,
-    // and the epilogue's residual rows or RoPE factors
+    // side inputs (weights and tables) are requested before the wait
     constexpr int PG = 4;  // float4s of the gain per thread held in registers (K <= 4096)
     const WT* gw = static_cast<const WT*>(d.gain);
     float side = 0.f;
     float2 side2 = make_float2(1.f, 0.f);
-    if (ep.epi == EPI_RESID) {
-      if (tid < min(2 * r.p1, d.N) - 2 * r.p0) side = __ldcg(ep.out + 2 * r.p0 + tid);
-    } else if (ep.epi == EPI_QKV) {
+    const int nrows = min(2 * r.p1, d.N) - 2 * r.p0;
+    if (ep.epi == EPI_RESID && (rsd0f || rsd0w) && tid < nrows)
+      side = rsd0f ? __ldcg(rsd0f + 2 * r.p0 + tid) : load1(rsd0w, 2 * r.p0 + tid);
+    if (ep.epi == EPI_QKV) {
       const int half = ep.head_dim / 2;
       const int g = r.p0 + tid;
-      if (g < r.p1 && g / half < ep.n_rot) side2 = ep.rope[static_cast<size_t>(ep.pos) * half + (g - (g / half) * half)];
+      if (g < r.p1 && g / half < ep.n_rot)
+        side2 = ep.rope[static_cast<size_t>(ep.pos) * half + (g - (g / half) * half)];
     }
     float4 gq[PG];
 #pragma unroll
@@ -385,30 +416,30 @@ __device__ bool g_phase(const MegaArgs& a, const GDesc& d, const float* xg, cons
       gq[i] = (gw != nullptr && e < K) ? load4_weight<WT>(gw, e) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float4 xq[PX];
-#pragma unroll
-    for (int i = 0; i < PX; ++i) xq[i] = load4(tid * 4 + i * MT * 4);
-    if (ep.epi == EPI_RESID) {
-      if (tid < 2 * kMegaPairsMax) sh.rsd[tid] = side;
-    } else if (ep.epi == EPI_QKV) {
-      if (tid < kMegaPairsMax) sh.rope[tid] = side2;
-    }
-#pragma unroll
-    for (int i = 0; i < PX; ++i) add_ssq(tid * 4 + i * MT * 4, xq[i]);
-    for (int e = tid * 4 + PX * MT * 4; e < KP; e += MT * 4) {
-      const float4 v = load4(e);
-      *reinterpret_cast<float4*>(xs + xidx(e)) = v;
-      add_ssq(e, v);
-    }
-    if (ep.resid_init && cta == 0) {
+    if (xt) {
+      bad = !poll_x(xt, K, tag_in, xq, a.guard);
+    } else {
 #pragma unroll
       for (int i = 0; i < PX; ++i) {
         const int e = tid * 4 + i * MT * 4;
-        if (e < K) __stcg(reinterpret_cast<float4*>(ep.resid_init + e), xq[i]);
+        xq[i] = e >= K ? make_float4(0.f, 0.f, 0.f, 0.f)
+                       : (x0f ? __ldcg(reinterpret_cast<const float4*>(x0f + e)) : load4_weight<WT>(x0w, e));
       }
-      for (int e = tid * 4 + PX * MT * 4; e < K; e += MT * 4)
-        __stcg(reinterpret_cast<float4*>(ep.resid_init + e), load4(e));
     }
+    if (ep.epi == EPI_RESID && (rsd0f || rsd0w) && tid < 2 * kMegaPairsMax) sh.rsd[tid] = side;
+    if (ep.epi == EPI_QKV && tid < kMegaPairsMax) sh.rope[tid] = side2;
     if (d.gain != nullptr) {
+      float ssq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < PX; ++i) {
+        const int e = tid * 4 + i * MT * 4;
+        const float4 v = xq[i];
+        const float t = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        const int grp = e < K ? e / gsz : 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q == grp) ssq[q] += t;
+      }
 #pragma unroll
       for (int q = 0; q < 4; ++q) ssq[q] = warp_sum(ssq[q]);
       if (lane == 0)
@@ -433,14 +464,6 @@ __device__ bool g_phase(const MegaArgs& a, const GDesc& d, const float* xg, cons
           *reinterpret_cast<float4*>(xs + xidx(e)) = v;
         }
       }
-      for (int e = tid * 4 + PX * MT * 4; e < K; e += MT * 4) {
-        float4* q = reinterpret_cast<float4*>(xs + xidx(e));
-        const float rs = sh.rs[e / gsz];
-        const float4 gn = load4_weight<WT>(gw, e);
-        float4 v = *q;
-        v.x = v.x * rs * gn.x; v.y = v.y * rs * gn.y; v.z = v.z * rs * gn.z; v.w = v.w * rs * gn.w;
-        *q = v;
-      }
     } else {
 #pragma unroll
       for (int i = 0; i < PX; ++i) {
@@ -448,13 +471,13 @@ __device__ bool g_phase(const MegaArgs& a, const GDesc& d, const float* xg, cons
         if (e < KP) *reinterpret_cast<float4*>(xs + xidx(e)) = xq[i];
       }
     }
-    __syncthreads();
+    if (__syncthreads_or(bad)) return false;
   }
 
   auto finish = [&](int g, float v0, float v1) {
     const int row = 2 * g;
     if (ep.epi == EPI_SWIGLU) {
-      __stcg(ep.out + g, v0 / (1.0f + expf(-v0)) * v1);
+      st_tagged(ep.out + g, v0 / (1.0f + expf(-v0)) * v1, ep.tag);
     } else if (ep.epi == EPI_QKV) {
       const int half = ep.head_dim / 2;
       const int head = g / half, i = g - head * half;
@@ -464,14 +487,17 @@ __device__ bool g_phase(const MegaArgs& a, const GDesc& d, const float* xg, cons
         o0 = v0 * cs.x - v1 * cs.y;
         o1 = v1 * cs.x + v0 * cs.y;
       }
-      __stcg(ep.out + head * ep.head_dim + i, o0);
-      __stcg(ep.out + head * ep.head_dim + i + half, o1);
+      st_tagged(ep.out + head * ep.head_dim + i, o0, ep.tag);
+      st_tagged(ep.out + head * ep.head_dim + i + half, o1, ep.tag);
     } else {
       const int rows = min(2, d.N - row);
       const float v[2] = {v0, v1};
       for (int rr = 0; rr < rows; ++rr) {
         if (ep.epi == EPI_RESID) {
-          __stcg(ep.out + row + rr, sh.rsd[row + rr - 2 * r.p0] + v[rr]);
+          const float nv = sh.rsd[row + rr - 2 * r.p0] + v[rr];
+          sh.rsd[row + rr - 2 * r.p0] = nv;
+          st_tagged(ep.out + row + rr, nv, ep.tag);
+          if (ep.plain) ep.plain[row + rr] = nv;
         } else {
           if (ep.logits) ep.logits[row + rr] = v[rr];
           if (v[rr] != v[rr]) atomicOr(ep.guard, GUARD_NAN);
@@ -484,7 +510,6 @@ __device__ bool g_phase(const MegaArgs& a, const GDesc& d, const float* xg, cons
   int pl = r.ua / CT, c = r.ua - (r.ua / CT) * CT;
   bool pair_whole = (c == 0);
   float acc0 = 0.f, acc1 = 0.f;
-  bool bad = false;
   for (int k = 0; k < r.nslots; ++k) {
     const int s = consumed % NS;
     const bool ok = mbar_wait(&sh.full[warp][s], static_cast<uint32_t>(consumed / NS) & 1u);
@@ -549,7 +574,7 @@ __device__ bool g_phase(const MegaArgs& a, const GDesc& d, const float* xg, cons
     ++consumed;
     if (lane == 0) {
       fence_proxy_async();
-      st.issue_next(a, smem + static_cast<size_t>(warp) * NS * SB, sh.full[warp], cta, G, warp, pos, qkv_n);
+      st.issue_next(a, ring, sh.full[warp], cta, G, warp, pos, qkv_n);
     }
   }
   if (bad && lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
@@ -599,9 +624,12 @@ __device__ __forceinline__ void vload(const int8_t* p, float* f) {
   for (int i = 0; i < DPL; ++i) f[i] = static_cast<float>(p[i]);
 }
 
+// One attention item (KV head g, key split sp) per CTA: the partial
+// (max, sum, unnormalised output) of its REP query heads over its keys; the
+// last split of head g to finish merges all splits into attn_out.
 template <typename WT, int D, int REP, typename KVT>
-__device__ bool a_phase(const MegaArgs& a, int l, int pos, uint8_t* smem, MegaShared& sh, Stream<D, KVT>& st,
-                        int& consumed, int cta, int G, int qkv_n) {
+__device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint32_t tag_out, uint8_t* smem,
+                        MegaShared& sh, Stream<D, KVT>& st, int& consumed, int cta, int G, int qkv_n) {
   constexpr int ELT = sizeof(KVT);
   constexpr int EPL = 16 / ELT;
   constexpr int ROWB = D * ELT;
@@ -616,8 +644,9 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint8_t* smem, MegaSh
   constexpr int TKM = tile_keys<D, KVT>();
   constexpr uint32_t KVB = TKM * ROWB;
   constexpr int PSTR = REP * (D + 2);
+  constexpr int NQ4 = ((REP + 2) * D + MT - 1) / MT;  // tagged words per thread to stage
   static_assert(TKM > 0 && 2 * KVB + 2 * TKM * 2 <= SB, "an attention tile must fit one slot");
-  static_assert(D <= 128, "the new K/V rows are staged in a 128-float buffer");
+  static_assert(D <= 128 && REP * D <= 512, "staging buffers");
   __shared__ float Sw[MW][REP][TKM];
   __shared__ __align__(16) float Pw[MW][TKM][REP];
   __shared__ float wstate[MW][PSTR];
@@ -629,22 +658,55 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint8_t* smem, MegaSh
   const LayerPtrs& lp = a.layers[l];
   const size_t head_row = (static_cast<size_t>(a.seq) * a.nkv + it.g) * a.cap;
   uint8_t* ring = smem + static_cast<size_t>(warp) * NS * SB;
-  const float* qkv = a.qkv;
+  const bool appends = (it.k1 == L);  // this split holds the new token's key
+
+  // ---- stage the query heads (and the new K/V rows) once their tags arrive
+  {
+    const int total = REP * D + (appends ? 2 * D : 0);
+    const u64* src[NQ4];
+    unsigned pend = 0;
+#pragma unroll
+    for (int i = 0; i < NQ4; ++i) {
+      const int idx = tid + i * MT;
+      src[i] = a.t_qkv;
+      if (idx < total) {
+        pend |= 1u << i;
+        if (idx < REP * D) {
+          src[i] = a.t_qkv + static_cast<size_t>(it.g) * REP * D + idx;
+        } else {
+          const int kv = (idx - REP * D) / D, e = (idx - REP * D) - kv * D;
+          src[i] = a.t_qkv + (kv == 0 ? a.nq * D : (a.nq + a.nkv) * D) + it.g * D + e;
+        }
+      }
+    }
+    Patience wait;
+    bool bad = false;
+    while (pend) {
+      u64 w[NQ4];
+#pragma unroll
+      for (int i = 0; i < NQ4; ++i) w[i] = (pend & (1u << i)) ? ld_tagged(src[i]) : 0ull;
+#pragma unroll
+      for (int i = 0; i < NQ4; ++i) {
+        if ((pend & (1u << i)) && tag_is(w[i], tag_in)) {
+          const int idx = tid + i * MT;
+          if (idx < REP * D) sh.qs[idx] = tag_val(w[i]) * a.scale;
+          else sh.newkv[(idx - REP * D) / D][(idx - REP * D) % D] = tag_val(w[i]);
+          pend &= ~(1u << i);
+        }
+      }
+      if (pend && !wait.more(a.guard)) {
+        bad = true;
+        break;
+      }
+    }
+    if (__syncthreads_or(bad)) return false;
+  }
   const int kl = lane % LPK;
   float q[REP][QD];
 #pragma unroll
   for (int h = 0; h < REP; ++h)
 #pragma unroll
-    for (int e = 0; e < QD; ++e) q[h][e] = __ldcg(qkv + (it.g * REP + h) * D + kl * QD + e) * a.scale;
-  // the CTA holding the last keys appends the new token: stage its K and V
-  // rows now, in the same round trip as q
-  if (it.k1 == L) {
-    for (int idx = tid; idx < 2 * D; idx += MT) {
-      const int kv = idx / D, e = idx - (idx / D) * D;
-      sh.newkv[kv][e] = __ldcg(qkv + (kv == 0 ? a.nq * D : (a.nq + a.nkv) * D) + it.g * D + e);
-    }
-  }
-  __syncthreads();
+    for (int e = 0; e < QD; ++e) q[h][e] = sh.qs[h * D + kl * QD + e];
 
   float m[REP], lsum[REP], acc[REP][DPL];
 #pragma unroll
@@ -669,7 +731,7 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint8_t* smem, MegaSh
     const __half* ksc = reinterpret_cast<const __half*>(slot + 2 * KVB);
     const __half* vsc = ksc + TKM;
     const int jr = pos - j0;
-    if (it.k1 == L && jr >= 0 && jr < rows) {  // the new token: cache format, to global and into the slot
+    if (appends && jr >= 0 && jr < rows) {  // the new token: cache format, to global and into the slot
       for (int kv = 0; kv < 2; ++kv) {
         const float* src = sh.newkv[kv];
         KVT* dst = static_cast<KVT*>(kv == 0 ? lp.kc : lp.vc) + (head_row + pos) * D;
@@ -792,7 +854,8 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint8_t* smem, MegaSh
 #pragma unroll
       for (int dd = 0; dd < DPL; ++dd) wstate[warp][2 * REP + h * D + lane * DPL + dd] = acc[h][dd];
   }
-  __syncthreads();
+  if (__syncthreads_or(bad)) return false;
+  // ---- this split's partial: combine the warps
   float* pp = a.part + static_cast<size_t>(cta) * PSTR;
   for (int idx = tid; idx < REP * D; idx += MT) {
     const int h = idx / D;
@@ -812,37 +875,49 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint8_t* smem, MegaSh
     __stcg(pp + tid, M);
     __stcg(pp + REP + tid, Ls);
   }
-  return __syncthreads_and(!bad) != 0;
-}
-
-// outputs [cta * chunk, ...) of all query heads: log-sum-exp merge of the splits
-template <int D, int REP>
-__device__ void merge_phase(const MegaArgs& a, int cta, int G) {
-  constexpr int PSTR = REP * (D + 2);
-  const int total = a.nq * D;
-  const int chunk = (total + G - 1) / G;
-  const int lo = cta * chunk, hi = min(total, lo + chunk);
-  const int ns = a.nsplit;
-  for (int idx = lo + static_cast<int>(threadIdx.x); idx < hi; idx += MT) {
-    const int qh = idx / D, dd = idx - qh * D;
-    const int g = qh / REP, h = qh - g * REP;
-    const float* base = a.part + static_cast<size_t>(g) * ns * PSTR;
-    // one pass over the splits, rescaling as the running maximum grows
-    float M = -INFINITY, Ls = 0.f, O = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) {
-      const float ms = __ldcg(base + s * PSTR + h);
-      const float ls = __ldcg(base + s * PSTR + REP + h);
-      const float os = __ldcg(base + s * PSTR + 2 * REP + h * D + dd);
-      if (ms == -INFINITY) continue;
-      const float mn = fmaxf(M, ms);
-      const float wo = expf(M - mn), ws = expf(ms - mn);
-      Ls = Ls * wo + ls * ws;
-      O = O * wo + os * ws;
-      M = mn;
-    }
-    __stcg(a.attn_out + idx, O / Ls);
+  // ---- the last split of this KV head merges them all
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned done = atomicAdd(a.hcnt + it.g, 1u);
+    sh.flag = (done == static_cast<unsigned>((l + 1) * a.nsplit - 1));
   }
+  __syncthreads();
+  if (!sh.flag) return true;
+  __threadfence();
+  const int ns = a.nsplit;
+  float* stage = reinterpret_cast<float*>(smem + kMegaRingBytes);  // the x buffer is free here
+  const float* src = a.part + static_cast<size_t>(it.g) * ns * PSTR;
+  if constexpr (PSTR % 4 == 0) {
+    for (int i = tid; i < ns * PSTR / 4; i += MT)
+      reinterpret_cast<float4*>(stage)[i] = __ldcg(reinterpret_cast<const float4*>(src) + i);
+  } else {
+    for (int i = tid; i < ns * PSTR; i += MT) stage[i] = __ldcg(src + i);
+  }
+  float* wts = &wstate[0][0];  // MW * PSTR >= nsplit * REP floats
+  __syncthreads();
+  if (tid < REP) {  // per query head: the weight of each split, exp(M_s - M) / sum
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, stage[s * PSTR + tid]);
+    float Ls = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float ms = stage[s * PSTR + tid];
+      if (ms != -INFINITY) Ls = fmaf(stage[s * PSTR + REP + tid], expf(ms - M), Ls);
+    }
+    for (int s = 0; s < ns; ++s) {
+      const float ms = stage[s * PSTR + tid];
+      wts[s * REP + tid] = ms == -INFINITY ? 0.f : expf(ms - M) / Ls;
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < REP * D; idx += MT) {
+    const int h = idx / D;
+    float O = 0.f;
+    for (int s = 0; s < ns; ++s) O = fmaf(stage[s * PSTR + 2 * REP + idx], wts[s * REP + h], O);
+    st_tagged(a.t_attn + static_cast<size_t>(it.g) * REP * D + idx, O, tag_out);
+  }
+  __syncthreads();  // the stage is the next phase's x buffer
+  return true;
 }
 
 // ---- the step -------------------------------------------------------------------------------
@@ -855,8 +930,9 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
   const int pos = a.seq_len[a.seq];
   if (pos < 0 || pos >= a.cap) {
     if (tid == 0) atomicOr(a.guard, GUARD_POS);
-    return;  // every CTA sees the same pos and leaves before any grid barrier
+    return;  // every CTA sees the same pos and leaves before any wait
   }
+  const uint32_t tagbase = (*a.epoch + 1u) << kMegaTagShift;
   const int qkv_n = (a.nq + 2 * a.nkv) * D;
   Stream<D, KVT> st;
   if (lane == 0) {
@@ -878,50 +954,52 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
       xe = static_cast<const WT*>(a.embed) + static_cast<size_t>(tok) * a.hidden;
     }
   }
-  float* resid = a.x_ext ? a.x_ext : a.resid;
 
   // One loop over the phases, so that each phase body exists once in the
   // code: the instruction cache stays warm from one phase to the next.
+  // Phase q reads what phase q - 1 wrote.
   const int lastq = a.n_layers * kPhases - 1 + (a.head ? 1 : 0);
   bool ok = true;
-  for (int q = 0; q <= lastq; ++q) {
+  for (int q = 0; q <= lastq && ok; ++q) {
     const int l = q / kPhases, j = q - (q / kPhases) * kPhases;
+    const uint32_t tag_in = tagbase | static_cast<uint32_t>(q - 1), tag_out = tagbase | static_cast<uint32_t>(q);
     if (l < a.n_layers && j == PH_ATTN) {
-      ok = a_phase<WT, D, REP>(a, l, pos, smem, sh, st, consumed, cta, G, qkv_n);
-    } else if (l < a.n_layers && j == PH_MERGE) {
-      merge_phase<D, REP>(a, cta, G);
-    } else {
-      GEpi ep{EPI_RESID, resid, a.rope, pos, D, a.nq + a.nkv, nullptr, nullptr, a.guard};
-      const float* xg = resid;
-      const WT* xr = nullptr;
-      if (l >= a.n_layers) {
-        ep.epi = EPI_ARGMAX;
-        ep.out = nullptr;
-        ep.logits = a.logits;
-      } else if (j == PH_QKV) {
-        ep.epi = EPI_QKV;
-        ep.out = a.qkv;
-        if (l == 0) {
-          xg = a.x_ext;
-          xr = xe;
-          if (!a.x_ext) ep.resid_init = resid;
-        }
-      } else if (j == PH_O) {
-        xg = a.attn_out;
-      } else if (j == PH_GU) {
-        ep.epi = EPI_SWIGLU;
-        ep.out = a.act;
-      } else {
-        xg = a.act;
+      ok = a_phase<WT, D, REP>(a, l, pos, tag_in, tag_out, smem, sh, st, consumed, cta, G, qkv_n);
+      continue;
+    }
+    GEpi ep{EPI_RESID, a.t_resid, nullptr, a.rope, pos, D, a.nq + a.nkv, nullptr, a.guard, tag_out};
+    const u64* xt = a.t_resid;
+    const float* x0f = nullptr;
+    const WT* x0w = nullptr;
+    const float* r0f = nullptr;
+    const WT* r0w = nullptr;
+    if (l >= a.n_layers) {
+      ep.epi = EPI_ARGMAX;
+      ep.out = nullptr;
+      ep.logits = a.logits;
+    } else if (j == PH_QKV) {
+      ep.epi = EPI_QKV;
+      ep.out = a.t_qkv;
+      if (l == 0) {
+        xt = nullptr;
+        x0f = a.x_ext;
+        x0w = xe;
       }
-      ok = g_phase<WT, D, KVT>(a, gdesc(a, q, qkv_n, D), xg, xr, ep, smem, sh, st, consumed, best, cta, G, pos,
-                               qkv_n);
+    } else if (j == PH_O) {
+      xt = a.t_attn;
+      if (l == 0) {  // the residual rows start as the layer input
+        r0f = a.x_ext;
+        r0w = xe;
+      }
+    } else if (j == PH_GU) {
+      ep.epi = EPI_SWIGLU;
+      ep.out = a.t_act;
+    } else {
+      xt = a.t_act;
+      if (l == a.n_layers - 1) ep.plain = a.x_out;
     }
-    if (!ok) break;
-    if (q < lastq && !grid_sync(a, sh, q)) {
-      ok = false;
-      break;
-    }
+    ok = g_phase<WT, D, KVT>(a, gdesc(a, q, qkv_n, D), xt, tag_in, x0f, x0w, r0f, r0w, ep, smem, sh, st, consumed,
+                             best, cta, G, pos, qkv_n);
   }
   if (ok && a.head) {
     best = warp_best(best);
@@ -940,8 +1018,7 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
     for (; consumed < st.issued; ++consumed)
       if (!mbar_wait(&sh.full[warp][consumed % NS], static_cast<uint32_t>(consumed / NS) & 1u)) break;
   }
-  // the last CTA to get here finishes the step and re-arms the barrier
-  // counters (every CTA is past its last grid barrier by then)
+  // the last CTA to get here finishes the step and re-arms the counters
   __syncthreads();
   if (tid == 0) {
     __threadfence();
@@ -968,10 +1045,11 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
       *a.token_out = f.i;
     }
   }
+  for (int g = tid; g < a.nkv; g += MT) a.hcnt[g] = 0u;
   if (tid == 0) {
     if (!failed) a.seq_len[a.seq] = pos + 1;
-    *a.bar_count = 0u;
     *a.end_count = 0u;
+    *a.epoch = *a.epoch + 1u;  // the next launch writes fresh tags
   }
 }
 
