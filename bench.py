@@ -68,6 +68,8 @@ def algorithmic_bytes(s, ctx_len: int) -> dict:
         "total": weights + kv,
         # the gate/up GEMV: W [2I, H] + x [H] fp32 + gain [H] + act [I] fp32
         "gate_up_launch": 2 * I * H * wb + H * 4 + H * wb + I * 4,
+        # the persistent step kernel: weights, the KV history, the new K/V rows
+        "step_launch": weights + kv + s.n_layers * kv_row,
     }
 
 
@@ -81,9 +83,9 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_from_profiles(kernel_sources):
-    """dram bytes per launch of the gate/up GEMV from the committed ncu summary,
-    only if the kernel source is unchanged since the capture."""
+def traffic_from_profiles(kernel_sources, kernel):
+    """dram bytes per launch of `kernel` from the committed ncu summary, only
+    if the kernel sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     h = hashlib.sha256()
     for src in kernel_sources:
@@ -93,7 +95,7 @@ def traffic_from_profiles(kernel_sources):
     try:
         for line in open(path):
             kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
-            if kv.get("kernel") == "gemv_gate_up" and kv.get("source_sha") == sha:
+            if kv.get("kernel") == kernel and kv.get("source_sha") == sha:
                 return float(kv["dram_bytes_per_launch"]), sha
     except OSError:
         pass
@@ -336,11 +338,22 @@ def run_ours(args, world, rank, local, pg):
         for k in ms_k:
             ms_k[k] += a[k]
             n_k[k] += b[k]
-    gu_ms = ms_k["gate_up"] / max(1, n_k["gate_up"])
+    persistent = n_k["step"] > 0
     peak, peak_src = measured_peaks()
-    achieved = by["gate_up_launch"] / (gu_ms * 1e-3) / 1e9
-    src = [os.path.join(ROOT, "dense_gqa_decoder_gb300", "csrc", f) for f in ("k2_gemv.cu", "k2_common.cuh")]
-    traffic, sha = traffic_from_profiles(src)
+    csrc = os.path.join(ROOT, "dense_gqa_decoder_gb300", "csrc")
+    if persistent:
+        # the whole token is one kernel: it is the dominant (only) kernel
+        k_name, k_desc, k_bytes = "mega_decode", "mega_decode_kernel (whole decode step)", by["step_launch"]
+        k_ms = ms_k["step"] / n_k["step"]
+        src = [os.path.join(csrc, f) for f in ("k2_mega.cu", "k2_common.cuh", "k2_kernels.h")]
+        launches_per_step = 1
+    else:
+        k_name, k_desc, k_bytes = "gemv_gate_up", "gemv_gate_up (norm + gate/up GEMV + SwiGLU)", by["gate_up_launch"]
+        k_ms = ms_k["gate_up"] / max(1, n_k["gate_up"])
+        src = [os.path.join(csrc, f) for f in ("k2_gemv_packed.cu", "k2_common.cuh", "k2_kernels.h")]
+        launches_per_step = 1 + 5 * s.n_layers + 1
+    achieved = k_bytes / (k_ms * 1e-3) / 1e9
+    traffic, sha = traffic_from_profiles(src, k_name)
 
     # end to end through the C ABI with host buffers: token H2D, step, token D2H
     host_in = torch.zeros(1, dtype=torch.int32).pin_memory()
@@ -363,22 +376,22 @@ def run_ours(args, world, rank, local, pg):
         per_token, desc, _ = oracle_decode_sample(2, 1.0, args.ctx)
         cpu = {"value": 1.0 / per_token, "unit": "tok/s", "cores": blas_threads(), "kind": "oracle", "sample": desc}
 
-    launches_per_step = 1 + 5 * s.n_layers + 1
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": 1, "context": args.ctx, "layers": s.n_layers,
-                   "kv_dtype": "f16", "activations": "fp32", "cuda_graph": True, "pdl": True,
+                   "kv_dtype": "f16", "activations": "fp32", "cuda_graph": True,
+                   "persistent_kernel": persistent, "pdl": not persistent,
                    "l2": "no flush: every step streams 8.8 GB of weights, far above the 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "hbm": {"bytes_per_step": by["total"], "achieved_gbs": by["total"] / (ms_per_step * 1e-3) / 1e9,
                 "peak_gbs": peak, "frac": by["total"] / (ms_per_step * 1e-3) / 1e9 / peak,
                 "frac_of_8tbs_nominal": by["total"] / (ms_per_step * 1e-3) / 1e9 / 7900.0},
-        "roofline": {"bound": "hbm", "kernel": "gemv_gate_up (norm + gate/up GEMV + SwiGLU)",
+        "roofline": {"bound": "hbm", "kernel": k_desc,
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_source": peak_src, "algorithmic_bytes": by["gate_up_launch"],
-                     "launch_ms": gu_ms, "source_sha": sha},
+                     "traffic": traffic, "peak_source": peak_src, "algorithmic_bytes": k_bytes,
+                     "launch_ms": k_ms, "source_sha": sha},
         "kernel_ms_per_step": {k: ms_k[k] / args.profile_steps for k in ms_k},
         "gpu_launches": launches_per_step * args.steps,
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
