@@ -35,7 +35,7 @@ int elt_bytes(int dt) { return dt == K2_F32 ? 4 : (dt == K2_BF16 || dt == K2_F16
 // ---------------------------------------------------------------------------
 struct Layout {
   size_t seq_len, guard, am_counter, msync, rope, resid, qkv, attn_out, act, am_val, am_idx, attn_part, ltab;
-  size_t t_resid, t_qkv, t_attn, t_act;  // persistent step: (value, tag) activations
+  size_t t_resid, t_qkv, t_attn, t_act, t_part;  // persistent step: (value, tag) activations
   size_t wqkv, wo, wgu, wdown, wlm;  // packed weights; per-layer strides below
   size_t wqkv_layer, wo_layer, wgu_layer, wdown_layer;
   size_t kc, vc, ks, vs;  // first layer; per-layer stride kv_layer / sc_layer
@@ -75,8 +75,8 @@ Layout layout_of(const k2_config& c) {
   l.seq_len = take(sizeof(int) * s.B);
   l.guard = take(sizeof(unsigned));
   l.am_counter = take(sizeof(unsigned) * s.B);
-  // persistent step: finished CTAs, launch epoch, per-KV-head finished splits
-  l.msync = take(sizeof(unsigned) * (2 + static_cast<size_t>(s.nkv)));
+  // persistent step: finished CTAs, launch epoch
+  l.msync = take(sizeof(unsigned) * 2);
   l.rope = take(sizeof(float2) * static_cast<size_t>(l.cap) * (s.d / 2));
   l.resid = take(sizeof(float) * static_cast<size_t>(s.B) * s.H);
   l.qkv = take(sizeof(float) * static_cast<size_t>(s.B) * s.qkv_n);
@@ -90,6 +90,7 @@ Layout layout_of(const k2_config& c) {
   l.t_qkv = take(8 * static_cast<size_t>(s.qkv_n));
   l.t_attn = take(8 * static_cast<size_t>(s.nq) * s.d);
   l.t_act = take(8 * static_cast<size_t>(s.I));
+  l.t_part = take(8 * static_cast<size_t>(s.nkv) * kMegaSplitMax * s.rep * (s.d + 2));
   const size_t scratch_end = o;
   l.wqkv_layer = align_up(packed_bytes(s.qkv_n, s.H, s.wb), kAlign);
   l.wo_layer = align_up(packed_bytes(s.H, s.nq * s.d, s.wb), kAlign);
@@ -426,8 +427,11 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   // the QKV and residual epilogues keep their CTA's pairs in shared memory
   if ((s.qkv_n / 2 + grid - 1) / grid > kMegaPairsMax || ((s.H + 1) / 2 + grid - 1) / grid > kMegaPairsMax)
     return cudaSuccess;
-  // inputs are polled in groups of four words
-  if (s.H % 4 || (s.nq * s.d) % 4 || s.I % 4) return cudaSuccess;
+  // inputs are polled in groups of four words; the gains are copied in 16-byte
+  // pieces into the x buffer above a 16 KB input
+  if (s.H % 8 || (s.nq * s.d) % 4 || s.I % 4) return cudaSuccess;
+  if (static_cast<size_t>(s.H) * s.wb > static_cast<size_t>(kMegaGainBytes)) return cudaSuccess;
+  if (s.d / 2 > 64) return cudaSuccess;  // the RoPE row of the position is kept in shared memory
   // tags carry the phase index in kMegaTagShift bits
   if (5 * s.L + 1 >= (1 << kMegaTagShift)) return cudaSuccess;
   // the merging CTA stages every split's partial in the 40 KB input buffer
@@ -488,12 +492,11 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   m.t_qkv = reinterpret_cast<unsigned long long*>(c->ws + c->lay.t_qkv);
   m.t_attn = reinterpret_cast<unsigned long long*>(c->ws + c->lay.t_attn);
   m.t_act = reinterpret_cast<unsigned long long*>(c->ws + c->lay.t_act);
-  m.part = c->attn_part;
+  m.t_part = reinterpret_cast<unsigned long long*>(c->ws + c->lay.t_part);
   m.am_val = c->am_val;
   m.am_idx = c->am_idx;
   m.end_count = reinterpret_cast<unsigned*>(c->ws + c->lay.msync);
   m.epoch = m.end_count + 1;
-  m.hcnt = m.end_count + 2;
   m.guard = c->guard;
   c->mega_grid = grid;
   c->mega_ok = true;
@@ -614,7 +617,9 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   // zero the state words (lengths, guard, counters) and build the rope table
   // and the tagged activations (a fresh context must not see an old tag)
   if ((e = cudaMemsetAsync(ws, 0, c->lay.rope, s)) ||
-      (e = cudaMemsetAsync(ws + c->lay.t_resid, 0, c->lay.t_act + 8 * static_cast<size_t>(c->s.I) - c->lay.t_resid,
+      (e = cudaMemsetAsync(ws + c->lay.t_resid, 0,
+                           c->lay.t_part + 8 * static_cast<size_t>(c->s.nkv) * kMegaSplitMax * c->s.rep *
+                                               (c->s.d + 2) - c->lay.t_resid,
                            s)) ||
       (e = launch_rope_table(c->rope, c->lay.cap, c->s.d, static_cast<double>(cfg->rope_theta), s))) {
     g_init_error = std::string("init: ") + cudaGetErrorString(e);
@@ -822,11 +827,8 @@ k2_status k2_clear_status(k2_ctx* c, void* stream) {
   if (!c) return K2_ERR_ARG;
   cudaError_t e = cudaMemsetAsync(c->guard, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream));
   // a step cut short by a timeout may have left the grid barrier half counted
-  // finished-CTA and per-head split counters (not the epoch: tags must stay fresh)
+  // the finished-CTA counter (not the epoch: tags must stay fresh)
   if (!e) e = cudaMemsetAsync(c->ws + c->lay.msync, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream));
-  if (!e)
-    e = cudaMemsetAsync(c->ws + c->lay.msync + 2 * sizeof(unsigned), 0, sizeof(unsigned) * c->s.nkv,
-                        static_cast<cudaStream_t>(stream));
   if (e) return c->cuda_fail(e, "clear_status");
   return K2_OK;
 }

@@ -207,20 +207,20 @@ struct MegaArgs {
   unsigned long long* t_qkv;
   unsigned long long* t_attn;
   unsigned long long* t_act;
-  float* part;       // attention partials [nkv * nsplit][rep * (d + 2)]
+  unsigned long long* t_part;  // attention partials [nkv * nsplit][rep * (d + 2)], tagged
   float* am_val;     // per-CTA argmax partials
   int* am_idx;
-  unsigned* hcnt;    // per KV head: splits finished in this launch
   unsigned* end_count;
   unsigned* epoch;   // launches so far (tags are derived from it)
   unsigned* guard;
 };
 constexpr int kMegaThreads = 256;
 constexpr int kMegaSlots = 2;                 // ring slots per warp
-constexpr int kMegaSlotBytes = 10 * 1024;     // one bulk copy: 10 packed units, or one 16-key K/V tile
+constexpr int kMegaSlotBytes = 9 * 1024;      // one bulk copy: 9 packed units, or one 16-key K/V tile
 constexpr int kMegaRingBytes = 8 * kMegaSlots * kMegaSlotBytes;
 constexpr int kMegaXBytes = 40 * 1024;        // the normalised input vector (K <= 10240 at bf16)
-constexpr int kMegaSmemBytes = kMegaRingBytes + kMegaXBytes;
+constexpr int kMegaGainBytes = 8 * 1024;      // one norm gain (hidden x weight bytes); two buffers
+constexpr int kMegaSmemBytes = kMegaRingBytes + kMegaXBytes + 2 * kMegaGainBytes;
 constexpr int kMegaTK = 16;                   // keys per attention tile (at most)
 constexpr int kMegaPairsMax = 64;             // row pairs of one CTA in the QKV / residual phases
 constexpr int kMegaTagShift = 10;             // tag = (epoch + 1) << 10 | phase: at most 1023 phases

@@ -149,6 +149,36 @@ __device__ bool poll_x(const u64* tv, int K, uint32_t tag, float4* xq, unsigned*
   return true;
 }
 
+// n tagged words (n even, src 16-byte aligned) into dst[0 .. n), at most
+// 2 * kPollPairs * MT words, waiting until every tag equals `tag`.
+constexpr int kPollPairs = 20;
+__device__ bool poll_words(const u64* src, int n, uint32_t tag, float* dst, unsigned* guard) {
+  const int tid = threadIdx.x;
+  unsigned pend = 0;
+#pragma unroll
+  for (int i = 0; i < kPollPairs; ++i)
+    if (2 * (tid + i * MT) < n) pend |= 1u << i;
+  Patience wait;
+  while (pend) {
+    u64 w[kPollPairs][2];
+#pragma unroll
+    for (int i = 0; i < kPollPairs; ++i) {  // every load first, then the checks
+      w[i][0] = w[i][1] = 0;
+      if (pend & (1u << i)) ld_tagged2(src + 2 * (tid + i * MT), w[i][0], w[i][1]);
+    }
+#pragma unroll
+    for (int i = 0; i < kPollPairs; ++i) {
+      if ((pend & (1u << i)) && tag_is(w[i][0], tag) && tag_is(w[i][1], tag)) {
+        dst[2 * (tid + i * MT)] = tag_val(w[i][0]);
+        dst[2 * (tid + i * MT) + 1] = tag_val(w[i][1]);
+        pend &= ~(1u << i);
+      }
+    }
+    if (pend && !wait.more(guard)) return false;
+  }
+  return true;
+}
+
 struct MegaShared {
   uint64_t full[MW][NS];
   float ss[MW][4];
@@ -159,7 +189,8 @@ struct MegaShared {
   Best best[MW];
   int flag;
   float rsd[2 * kMegaPairsMax];     // this CTA's residual rows, kept from one residual phase to the next
-  float2 rope[kMegaPairsMax];       // (cos, sin) of this CTA's pairs (QKV phase)
+  uint64_t gbar[2];                 // the two norm-gain buffers
+  float2 rope_pos[64];              // (cos, sin) at this step's position, i < head_dim / 2
   float qs[512];                    // the query heads of one KV head, scaled (rep * head_dim <= 512)
   float newkv[2][128];              // the new token's K and V rows (head_dim <= 128)
 };
@@ -249,6 +280,7 @@ struct Stream {
   const __half* ksb = nullptr;
   const __half* vsb = nullptr;
   int j0 = 0, k1 = 0;
+  uint64_t policy = 0;  // L2 evict-first: weights and K/V history are read once per step
 
   __device__ void enter(const MegaArgs& a, int cta, int G, int warp, int pos, int qkv_n) {
     k = 0;
@@ -292,6 +324,7 @@ struct Stream {
   __device__ void start(const MegaArgs& a, uint8_t* ring, uint64_t* full, int cta, int G, int warp, int pos,
                         int qkv_n) {
     lastq = a.n_layers * kPhases - 1 + (a.head ? 1 : 0);
+    policy = l2_evict_first_policy();
     q = 0;
     issued = 0;
     enter(a, cta, G, warp, pos, qkv_n);
@@ -314,8 +347,8 @@ struct Stream {
         mbar_arrive(bar);
       } else {
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(dst, kb + static_cast<size_t>(j0) * ROWB, crow * ROWB, bar);
-        bulk_g2s(dst + TKM * ROWB, vb + static_cast<size_t>(j0) * ROWB, crow * ROWB, bar);
+        bulk_g2s_hint(dst, kb + static_cast<size_t>(j0) * ROWB, crow * ROWB, bar, policy);
+        bulk_g2s_hint(dst + TKM * ROWB, vb + static_cast<size_t>(j0) * ROWB, crow * ROWB, bar, policy);
         if constexpr (I8) {
           bulk_g2s(dst + 2 * TKM * ROWB, ksb + j0, srow * 2u, bar);
           bulk_g2s(dst + 2 * TKM * ROWB + TKM * 2, vsb + j0, srow * 2u, bar);
@@ -325,7 +358,7 @@ struct Stream {
     } else {
       const int nu = min(SU, left);
       mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nu) * kUnit);
-      bulk_g2s(dst, src, static_cast<uint32_t>(nu) * kUnit, bar);
+      bulk_g2s_hint(dst, src, static_cast<uint32_t>(nu) * kUnit, bar, policy);
       src += static_cast<size_t>(nu) * kUnit;
       left -= nu;
     }
@@ -336,6 +369,33 @@ struct Stream {
     }
   }
 };
+
+// The norm gains reach shared memory by bulk copies issued one gain phase
+// ahead (a DRAM read under the full weight stream waits several
+// microseconds): gain phase number `used` reads buffer used & 1.
+struct GainQ {
+  int used = 0;    // gain phases entered
+  int issued = 0;  // gain copies issued (thread 0)
+};
+__device__ __forceinline__ uint8_t* gain_buf(uint8_t* smem, int b) {
+  return smem + kMegaRingBytes + kMegaXBytes + b * kMegaGainBytes;
+}
+// the gain of the first gain phase after phase q (null if none)
+__device__ __forceinline__ const void* next_gain(const MegaArgs& a, int q) {
+  const int l = q / kPhases, j = q - (q / kPhases) * kPhases;
+  if (l >= a.n_layers) return nullptr;
+  if (j < PH_GU) return a.layers[l].mlp_norm;
+  if (l + 1 < a.n_layers) return a.layers[l + 1].attn_norm;
+  return a.head ? a.final_norm : nullptr;
+}
+__device__ __forceinline__ void issue_gain(const MegaArgs& a, uint8_t* smem, MegaShared& sh, GainQ& gq,
+                                           const void* g, int bytes) {
+  const int b = gq.issued & 1;
+  fence_proxy_async();
+  mbar_arrive_expect_tx(&sh.gbar[b], static_cast<uint32_t>(bytes));
+  bulk_g2s(gain_buf(smem, b), g, static_cast<uint32_t>(bytes), &sh.gbar[b]);
+  ++gq.issued;
+}
 
 struct GEpi {
   int epi;          // EPI_QKV, EPI_RESID, EPI_SWIGLU or EPI_ARGMAX
@@ -362,6 +422,17 @@ __device__ __forceinline__ float4 load4_weight<float>(const float* p, int e) {
   return __ldg(reinterpret_cast<const float4*>(p + e));
 }
 template <typename WT>
+__device__ __forceinline__ float4 load4_shared(const WT* p, int e);
+template <>
+__device__ __forceinline__ float4 load4_shared<__nv_bfloat16>(const __nv_bfloat16* p, int e) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p + e);
+  return make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+}
+template <>
+__device__ __forceinline__ float4 load4_shared<float>(const float* p, int e) {
+  return *reinterpret_cast<const float4*>(p + e);
+}
+template <typename WT>
 __device__ __forceinline__ float load1(const WT* p, size_t e) {
   return to_f32(p[e]);
 }
@@ -372,10 +443,10 @@ __device__ __forceinline__ float load1(const WT* p, size_t e) {
 // tag_in) or, in the first phase, from x0f (fp32) or x0w (an embedding row).
 // rsd0f / rsd0w: where the first residual phase takes its old residual rows.
 template <typename WT, int D, typename KVT>
-__device__ bool g_phase(const MegaArgs& a, const GDesc& d, const u64* xt, uint32_t tag_in, const float* x0f,
+__device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt, uint32_t tag_in, const float* x0f,
                         const WT* x0w, const float* rsd0f, const WT* rsd0w, const GEpi& ep, uint8_t* smem,
-                        MegaShared& sh, Stream<D, KVT>& st, int& consumed, Best& best, int cta, int G, int pos,
-                        int qkv_n) {
+                        MegaShared& sh, Stream<D, KVT>& st, GainQ& gq, int& consumed, Best& best, int cta, int G,
+                        int pos, int qkv_n) {
   constexpr int EPL = Unpack<WT>::N;
   constexpr int CH = 32 * EPL;
   constexpr int NPL = EPL / 4;
@@ -395,26 +466,21 @@ __device__ bool g_phase(const MegaArgs& a, const GDesc& d, const u64* xt, uint32
       const int c = e / CH, rr = e - c * CH, l = rr / EPL, j = rr - l * EPL;
       return ((c * NPL + j / 4) * 32 + l) * 4;
     };
-    // side inputs (weights and tables) are requested before the wait
-    constexpr int PG = 4;  // float4s of the gain per thread held in registers (K <= 4096)
-    const WT* gw = static_cast<const WT*>(d.gain);
+    // a gain phase: its gain was copied one gain phase ago; start the next one
+    const WT* gsm = nullptr;
+    int gb = 0, guse = 0;
+    if (d.gain != nullptr) {
+      gb = gq.used & 1;
+      guse = gq.used >> 1;
+      gsm = reinterpret_cast<const WT*>(gain_buf(smem, gb));
+      ++gq.used;
+      const void* ng = next_gain(a, q);
+      if (tid == 0 && ng != nullptr) issue_gain(a, smem, sh, gq, ng, K * static_cast<int>(sizeof(WT)));
+    }
     float side = 0.f;
-    float2 side2 = make_float2(1.f, 0.f);
     const int nrows = min(2 * r.p1, d.N) - 2 * r.p0;
     if (ep.epi == EPI_RESID && (rsd0f || rsd0w) && tid < nrows)
       side = rsd0f ? __ldcg(rsd0f + 2 * r.p0 + tid) : load1(rsd0w, 2 * r.p0 + tid);
-    if (ep.epi == EPI_QKV) {
-      const int half = ep.head_dim / 2;
-      const int g = r.p0 + tid;
-      if (g < r.p1 && g / half < ep.n_rot)
-        side2 = ep.rope[static_cast<size_t>(ep.pos) * half + (g - (g / half) * half)];
-    }
-    float4 gq[PG];
-#pragma unroll
-    for (int i = 0; i < PG; ++i) {
-      const int e = tid * 4 + i * MT * 4;
-      gq[i] = (gw != nullptr && e < K) ? load4_weight<WT>(gw, e) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
     float4 xq[PX];
     if (xt) {
       bad = !poll_x(xt, K, tag_in, xq, a.guard);
@@ -427,7 +493,10 @@ __device__ bool g_phase(const MegaArgs& a, const GDesc& d, const u64* xt, uint32
       }
     }
     if (ep.epi == EPI_RESID && (rsd0f || rsd0w) && tid < 2 * kMegaPairsMax) sh.rsd[tid] = side;
-    if (ep.epi == EPI_QKV && tid < kMegaPairsMax) sh.rope[tid] = side2;
+    if (gsm != nullptr && !mbar_wait(&sh.gbar[gb], static_cast<uint32_t>(guse) & 1u)) {
+      atomicOr(a.guard, GUARD_TIMEOUT);
+      bad = true;
+    }
     if (d.gain != nullptr) {
       float ssq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -458,7 +527,7 @@ __device__ bool g_phase(const MegaArgs& a, const GDesc& d, const u64* xt, uint32
           float4 v = xq[i];
           if (e < K) {
             const float rs = sh.rs[e / gsz];
-            const float4 gn = i < PG ? gq[i < PG ? i : 0] : load4_weight<WT>(gw, e);
+            const float4 gn = load4_shared<WT>(gsm, e);
             v.x = v.x * rs * gn.x; v.y = v.y * rs * gn.y; v.z = v.z * rs * gn.z; v.w = v.w * rs * gn.w;
           }
           *reinterpret_cast<float4*>(xs + xidx(e)) = v;
@@ -483,7 +552,7 @@ __device__ bool g_phase(const MegaArgs& a, const GDesc& d, const u64* xt, uint32
       const int head = g / half, i = g - head * half;
       float o0 = v0, o1 = v1;
       if (head < ep.n_rot) {
-        const float2 cs = sh.rope[g - r.p0];
+        const float2 cs = sh.rope_pos[i];
         o0 = v0 * cs.x - v1 * cs.y;
         o1 = v1 * cs.x + v0 * cs.y;
       }
@@ -833,12 +902,16 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
           for (int dd = 0; dd < DPL; ++dd) acc[h][dd] = fmaf(pr[h], vf[dd], acc[h][dd]);
       }
     }
-    // the slot may have been written here (the new row): order those generic
-    // writes, and every lane's reads, before the next bulk copy into it
-    fence_proxy_async();
+    // order this slot's generic accesses before the next bulk copy into it:
+    // every lane fences where the slot was written (the new row), else lane 0
+    const bool wrote = appends && jr >= 0 && jr < rows;
+    if (wrote) fence_proxy_async();
     __syncwarp();
     ++consumed;
-    if (lane == 0) st.issue_next(a, ring, sh.full[warp], cta, G, warp, pos, qkv_n);
+    if (lane == 0) {
+      if (!wrote) fence_proxy_async();
+      st.issue_next(a, ring, sh.full[warp], cta, G, warp, pos, qkv_n);
+    }
   }
   if (bad && lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
   if (lane == 0) {
@@ -855,8 +928,13 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
       for (int dd = 0; dd < DPL; ++dd) wstate[warp][2 * REP + h * D + lane * DPL + dd] = acc[h][dd];
   }
   if (__syncthreads_or(bad)) return false;
-  // ---- this split's partial: combine the warps
-  float* pp = a.part + static_cast<size_t>(cta) * PSTR;
+  // ---- this split's partial (max, sum, unnormalised output per query head):
+  // combine the warps.  Split 0 of each KV head keeps its own in the stage
+  // buffer and merges; the others publish theirs as tagged words.
+  const int ns = a.nsplit;
+  const bool merger = (it.sp == 0);
+  float* stage = reinterpret_cast<float*>(smem + kMegaRingBytes);  // the x buffer is free here
+  u64* pub = a.t_part + static_cast<size_t>(cta) * PSTR;
   for (int idx = tid; idx < REP * D; idx += MT) {
     const int h = idx / D;
     float M = -INFINITY;
@@ -864,7 +942,8 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
     float O = 0.f;
     for (int w = 0; w < MW; ++w)
       if (wstate[w][h] != -INFINITY) O = fmaf(wstate[w][2 * REP + idx], expf(wstate[w][h] - M), O);
-    __stcg(pp + 2 * REP + idx, O);
+    if (merger) stage[2 * REP + idx] = O;
+    else st_tagged(pub + 2 * REP + idx, O, tag_out);
   }
   if (tid < REP) {
     float M = -INFINITY;
@@ -872,27 +951,20 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
     float Ls = 0.f;
     for (int w = 0; w < MW; ++w)
       if (wstate[w][tid] != -INFINITY) Ls = fmaf(wstate[w][REP + tid], expf(wstate[w][tid] - M), Ls);
-    __stcg(pp + tid, M);
-    __stcg(pp + REP + tid, Ls);
+    if (merger) {
+      stage[tid] = M;
+      stage[REP + tid] = Ls;
+    } else {
+      st_tagged(pub + tid, M, tag_out);
+      st_tagged(pub + REP + tid, Ls, tag_out);
+    }
   }
-  // ---- the last split of this KV head merges them all
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const unsigned done = atomicAdd(a.hcnt + it.g, 1u);
-    sh.flag = (done == static_cast<unsigned>((l + 1) * a.nsplit - 1));
-  }
-  __syncthreads();
-  if (!sh.flag) return true;
-  __threadfence();
-  const int ns = a.nsplit;
-  float* stage = reinterpret_cast<float*>(smem + kMegaRingBytes);  // the x buffer is free here
-  const float* src = a.part + static_cast<size_t>(it.g) * ns * PSTR;
-  if constexpr (PSTR % 4 == 0) {
-    for (int i = tid; i < ns * PSTR / 4; i += MT)
-      reinterpret_cast<float4*>(stage)[i] = __ldcg(reinterpret_cast<const float4*>(src) + i);
-  } else {
-    for (int i = tid; i < ns * PSTR; i += MT) stage[i] = __ldcg(src + i);
+  if (!merger) return true;
+  // ---- split 0 waits for the other splits' partials and merges them all
+  {
+    const u64* src = a.t_part + static_cast<size_t>(cta + 1) * PSTR;  // splits 1 .. ns-1 follow
+    const bool ok = poll_words(src, (ns - 1) * PSTR, tag_out, stage + PSTR, a.guard);
+    if (__syncthreads_or(!ok)) return false;
   }
   float* wts = &wstate[0][0];  // MW * PSTR >= nsplit * REP floats
   __syncthreads();
@@ -935,12 +1007,19 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
   const uint32_t tagbase = (*a.epoch + 1u) << kMegaTagShift;
   const int qkv_n = (a.nq + 2 * a.nkv) * D;
   Stream<D, KVT> st;
+  GainQ gq;
+  if (tid == 0) {
+    mbar_init(&sh.gbar[0], 1);
+    mbar_init(&sh.gbar[1], 1);
+  }
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(&sh.full[warp][s], 1);
     fence_mbar_init();
     st.start(a, smem + static_cast<size_t>(warp) * NS * SB, sh.full[warp], cta, G, warp, pos, qkv_n);
   }
-  __syncwarp();
+  __syncthreads();  // barriers initialised
+  if (tid == 0) issue_gain(a, smem, sh, gq, a.layers[0].attn_norm, a.hidden * static_cast<int>(sizeof(WT)));
+  if (tid < D / 2) sh.rope_pos[tid] = a.rope[static_cast<size_t>(pos) * (D / 2) + tid];
   int consumed = 0;
   Best best{-INFINITY, 0x7fffffff};
 
@@ -998,8 +1077,8 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
       xt = a.t_act;
       if (l == a.n_layers - 1) ep.plain = a.x_out;
     }
-    ok = g_phase<WT, D, KVT>(a, gdesc(a, q, qkv_n, D), xt, tag_in, x0f, x0w, r0f, r0w, ep, smem, sh, st, consumed,
-                             best, cta, G, pos, qkv_n);
+    ok = g_phase<WT, D, KVT>(a, q, gdesc(a, q, qkv_n, D), xt, tag_in, x0f, x0w, r0f, r0w, ep, smem, sh, st, gq,
+                             consumed, best, cta, G, pos, qkv_n);
   }
   if (ok && a.head) {
     best = warp_best(best);
@@ -1017,6 +1096,10 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
   if (lane == 0) {
     for (; consumed < st.issued; ++consumed)
       if (!mbar_wait(&sh.full[warp][consumed % NS], static_cast<uint32_t>(consumed / NS) & 1u)) break;
+  }
+  if (tid == 0) {
+    for (int k = gq.used; k < gq.issued; ++k)
+      if (!mbar_wait(&sh.gbar[k & 1], static_cast<uint32_t>(k >> 1) & 1u)) break;
   }
   // the last CTA to get here finishes the step and re-arms the counters
   __syncthreads();
@@ -1045,7 +1128,6 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
       *a.token_out = f.i;
     }
   }
-  for (int g = tid; g < a.nkv; g += MT) a.hcnt[g] = 0u;
   if (tid == 0) {
     if (!failed) a.seq_len[a.seq] = pos + 1;
     *a.end_count = 0u;
