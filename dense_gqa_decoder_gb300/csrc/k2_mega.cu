@@ -390,8 +390,7 @@ __device__ __forceinline__ const void* next_gain(const MegaArgs& a, int q) {
 }
 __device__ __forceinline__ void issue_gain(const MegaArgs& a, uint8_t* smem, MegaShared& sh, GainQ& gq,
                                            const void* g, int bytes) {
-  const int b = gq.issued & 1;
-  fence_proxy_async();
+  const int b = gq.issued & 1;  // last read (generic loads, completed) two gain phases ago
   mbar_arrive_expect_tx(&sh.gbar[b], static_cast<uint32_t>(bytes));
   bulk_g2s(gain_buf(smem, b), g, static_cast<uint32_t>(bytes), &sh.gbar[b]);
   ++gq.issued;
@@ -639,12 +638,9 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
         }
       }
     }
-    __syncwarp();
+    __syncwarp();  // the slot was only read: no proxy fence needed before refilling it
     ++consumed;
-    if (lane == 0) {
-      fence_proxy_async();
-      st.issue_next(a, ring, sh.full[warp], cta, G, warp, pos, qkv_n);
-    }
+    if (lane == 0) st.issue_next(a, ring, sh.full[warp], cta, G, warp, pos, qkv_n);
   }
   if (bad && lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
   __syncthreads();
@@ -867,16 +863,26 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
       }
     }
     __syncwarp();
-    float al[REP];
+    // online softmax over the tile, lane = key, the REP heads interleaved
+    float al[REP], pr[REP], ps[REP];
 #pragma unroll
     for (int h = 0; h < REP; ++h) {
       const float sv = lane < rows ? Sw[warp][h][lane] : -INFINITY;
-      const float mn = fmaxf(m[h], warp_max(sv));
+      const float mn = fmaxf(m[h], warp_max_redux(sv));
       al[h] = expf(m[h] - mn);
-      const float pr = lane < rows ? expf(sv - mn) : 0.f;
-      lsum[h] = lsum[h] * al[h] + warp_sum(pr);
+      pr[h] = lane < rows ? expf(sv - mn) : 0.f;
+      ps[h] = pr[h];
       m[h] = mn;
-      if (lane < rows) Pw[warp][lane][h] = I8 ? pr * __half2float(vsc[lane]) : pr;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int h = 0; h < REP; ++h) ps[h] += __shfl_xor_sync(0xffffffffu, ps[h], o);
+    const float vs_l = I8 && lane < rows ? __half2float(vsc[lane]) : 1.f;
+#pragma unroll
+    for (int h = 0; h < REP; ++h) {
+      lsum[h] = lsum[h] * al[h] + ps[h];
+      if (lane < rows) Pw[warp][lane][h] = pr[h] * vs_l;
     }
     __syncwarp();
     if (lane < DL) {
@@ -885,6 +891,7 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
 #pragma unroll
         for (int dd = 0; dd < DPL; ++dd) acc[h][dd] *= al[h];
       const KVT* vt = reinterpret_cast<const KVT*>(slot + KVB) + lane * DPL;
+#pragma unroll 4
       for (int jj = 0; jj < rows; ++jj) {
         float vf[DPL];
         vload<DPL>(vt + jj * D, vf);
@@ -902,16 +909,14 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
           for (int dd = 0; dd < DPL; ++dd) acc[h][dd] = fmaf(pr[h], vf[dd], acc[h][dd]);
       }
     }
-    // order this slot's generic accesses before the next bulk copy into it:
-    // every lane fences where the slot was written (the new row), else lane 0
-    const bool wrote = appends && jr >= 0 && jr < rows;
-    if (wrote) fence_proxy_async();
+    // Where this slot was written by generic stores (the new row), order
+    // those writes before the next bulk copy into it.  Slots that were only
+    // read need no proxy fence: every load has completed (its value was used)
+    // before the warp barrier, as with a consumer-release mbarrier.
+    if (appends && jr >= 0 && jr < rows) fence_proxy_async();
     __syncwarp();
     ++consumed;
-    if (lane == 0) {
-      if (!wrote) fence_proxy_async();
-      st.issue_next(a, ring, sh.full[warp], cta, G, warp, pos, qkv_n);
-    }
+    if (lane == 0) st.issue_next(a, ring, sh.full[warp], cta, G, warp, pos, qkv_n);
   }
   if (bad && lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
   if (lane == 0) {
