@@ -432,6 +432,7 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   if (s.H % 8 || (s.nq * s.d) % 4 || s.I % 4) return cudaSuccess;
   if (static_cast<size_t>(s.H) * s.wb > static_cast<size_t>(kMegaGainBytes)) return cudaSuccess;
   if (s.d / 2 > 64) return cudaSuccess;  // the RoPE row of the position is kept in shared memory
+  if (s.L > kMegaMaxLayers) return cudaSuccess;
   // tags carry the phase index in kMegaTagShift bits
   if (5 * s.L + 1 >= (1 << kMegaTagShift)) return cudaSuccess;
   // the merging CTA stages every split's partial in the 40 KB input buffer
@@ -467,6 +468,20 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   m = {};
   m.layers = dtab;
   m.n_layers = s.L;
+  m.w_qkv = static_cast<const uint8_t*>(c->wqkv(0));
+  m.w_o = static_cast<const uint8_t*>(c->wop(0));
+  m.w_gu = static_cast<const uint8_t*>(c->wgu(0));
+  m.w_down = static_cast<const uint8_t*>(c->wdown(0));
+  m.ws_qkv = c->lay.wqkv_layer;
+  m.ws_o = c->lay.wo_layer;
+  m.ws_gu = c->lay.wgu_layer;
+  m.ws_down = c->lay.wdown_layer;
+  m.kc = static_cast<uint8_t*>(c->kc(0));
+  m.vc = static_cast<uint8_t*>(c->vc(0));
+  m.ks = static_cast<uint8_t*>(c->ks(0));
+  m.vs = static_cast<uint8_t*>(c->vs(0));
+  m.s_kv = c->lay.kv_layer;
+  m.s_sc = c->lay.sc_layer;
   m.embed = c->embed;
   m.lm_head = c->wlm();
   m.final_norm = c->final_norm;

@@ -183,8 +183,19 @@ struct MegaGemv {
   int CT;  // 512-byte chunks per row (the packed layout)
 };
 struct MegaArgs {
-  const LayerPtrs* layers;  // device table, n_layers entries
+  const LayerPtrs* layers;  // device table, n_layers entries (read once per launch: the norm gains)
   int n_layers;
+  // packed weights and KV cache of layer l = base + l * stride (bytes)
+  const uint8_t* w_qkv;
+  const uint8_t* w_o;
+  const uint8_t* w_gu;
+  const uint8_t* w_down;
+  unsigned long long ws_qkv, ws_o, ws_gu, ws_down;
+  uint8_t* kc;
+  uint8_t* vc;
+  uint8_t* ks;  // int8 KV scales (null otherwise)
+  uint8_t* vs;
+  unsigned long long s_kv, s_sc;
   const void* embed;
   const void* lm_head;  // packed
   const void* final_norm;
@@ -223,7 +234,8 @@ constexpr int kMegaGainBytes = 8 * 1024;      // one norm gain (hidden x weight 
 constexpr int kMegaSmemBytes = kMegaRingBytes + kMegaXBytes + 2 * kMegaGainBytes;
 constexpr int kMegaTK = 16;                   // keys per attention tile (at most)
 constexpr int kMegaPairsMax = 64;             // row pairs of one CTA in the QKV / residual phases
-constexpr int kMegaTagShift = 10;             // tag = (epoch + 1) << 10 | phase: at most 1023 phases
+constexpr int kMegaTagShift = 10;
+constexpr int kMegaMaxLayers = 64;            // norm-gain pointers kept in shared memory             // tag = (epoch + 1) << 10 | phase: at most 1023 phases
 
 bool mega_supported(int wbytes, int head_dim, int rep, int kv_dtype);
 cudaError_t mega_init_attrs(int wbytes, int head_dim, int rep, int kv_dtype);

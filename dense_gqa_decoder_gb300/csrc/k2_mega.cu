@@ -192,36 +192,40 @@ struct MegaShared {
   uint64_t gbar[2];                 // the two norm-gain buffers
   float2 rope_pos[64];              // (cos, sin) at this step's position, i < head_dim / 2
   float qs[512];                    // the query heads of one KV head, scaled (rep * head_dim <= 512)
+  int4 wr[5][MW];                   // per GEMV kind: this CTA's pairs [x, y), this warp's units [z, w)
+  int4 item;                        // this CTA's attention item: KV head, split, first key, end key
+  const void* gains[2 * kMegaMaxLayers + 1];  // attn_norm[l] at 2l, mlp_norm[l] at 2l + 1, final last
   float newkv[2][128];              // the new token's K and V rows (head_dim <= 128)
 };
 
 // ---- static description of the step ------------------------------------------------
+// GEMV kinds: 0 QKV, 1 o_proj, 2 gate/up, 3 down, 4 lm_head.  Row ranges do not
+// depend on the layer, so they are computed once per launch (shared memory).
 struct GDesc {
   const uint8_t* W;
-  int N, K, CT;
+  int N, K, CT, kind;
   const void* gain;
 };
 
-__device__ __forceinline__ GDesc gdesc(const MegaArgs& a, int q, int qkv_n, int head_dim) {
+__device__ __forceinline__ GDesc gdesc(const MegaArgs& a, const MegaShared& sh, int q, int qkv_n, int head_dim) {
   GDesc d;
   const int l = q / kPhases, j = q - (q / kPhases) * kPhases;
   if (l >= a.n_layers) {  // the lm_head phase
-    d.W = static_cast<const uint8_t*>(a.lm_head);
-    d.N = a.vocab;
-    d.K = a.hidden;
-    d.CT = a.g_lm.CT;
+    d.W = static_cast<const uint8_t*>(a.lm_head); d.N = a.vocab; d.K = a.hidden; d.CT = a.g_lm.CT; d.kind = 4;
     d.gain = a.final_norm;
     return d;
   }
-  const LayerPtrs& lp = a.layers[l];
+  const size_t ul = static_cast<size_t>(l);
   if (j == PH_QKV) {
-    d.W = static_cast<const uint8_t*>(lp.wqkv); d.N = qkv_n; d.K = a.hidden; d.CT = a.g_qkv.CT; d.gain = lp.attn_norm;
+    d.W = a.w_qkv + ul * a.ws_qkv; d.N = qkv_n; d.K = a.hidden; d.CT = a.g_qkv.CT; d.kind = 0;
+    d.gain = sh.gains[2 * l];
   } else if (j == PH_O) {
-    d.W = static_cast<const uint8_t*>(lp.wo); d.N = a.hidden; d.K = a.nq * head_dim; d.CT = a.g_o.CT; d.gain = nullptr;
+    d.W = a.w_o + ul * a.ws_o; d.N = a.hidden; d.K = a.nq * head_dim; d.CT = a.g_o.CT; d.kind = 1; d.gain = nullptr;
   } else if (j == PH_GU) {
-    d.W = static_cast<const uint8_t*>(lp.wgu); d.N = 2 * a.inter; d.K = a.hidden; d.CT = a.g_gu.CT; d.gain = lp.mlp_norm;
+    d.W = a.w_gu + ul * a.ws_gu; d.N = 2 * a.inter; d.K = a.hidden; d.CT = a.g_gu.CT; d.kind = 2;
+    d.gain = sh.gains[2 * l + 1];
   } else {
-    d.W = static_cast<const uint8_t*>(lp.wdown); d.N = a.hidden; d.K = a.inter; d.CT = a.g_down.CT; d.gain = nullptr;
+    d.W = a.w_down + ul * a.ws_down; d.N = a.hidden; d.K = a.inter; d.CT = a.g_down.CT; d.kind = 3; d.gain = nullptr;
   }
   return d;
 }
@@ -230,14 +234,22 @@ struct GRange {
   int p0, p1, ua, ub, nslots;  // the CTA's pairs [p0, p1); the warp's units [ua, ub)
 };
 
-__device__ __forceinline__ GRange g_range(const GDesc& d, int cta, int G, int warp) {
-  const int npairs = (d.N + 1) / 2;
+// the split of kind k's rows over CTAs and of a CTA's units over warps
+__device__ __forceinline__ int4 g_split(int N, int CT, int cta, int G, int warp) {
+  const int npairs = (N + 1) / 2;
+  const int p0 = static_cast<int>((static_cast<long long>(npairs) * cta) / G);
+  const int p1 = static_cast<int>((static_cast<long long>(npairs) * (cta + 1)) / G);
+  const long long U = static_cast<long long>(p1 - p0) * CT;
+  return make_int4(p0, p1, static_cast<int>((U * warp) / MW), static_cast<int>((U * (warp + 1)) / MW));
+}
+
+__device__ __forceinline__ GRange g_range(const GDesc& d, const MegaShared& sh, int warp) {
+  const int4 w = sh.wr[d.kind][warp];
   GRange r;
-  r.p0 = static_cast<int>((static_cast<long long>(npairs) * cta) / G);
-  r.p1 = static_cast<int>((static_cast<long long>(npairs) * (cta + 1)) / G);
-  const long long U = static_cast<long long>(r.p1 - r.p0) * d.CT;
-  r.ua = static_cast<int>((U * warp) / MW);
-  r.ub = static_cast<int>((U * (warp + 1)) / MW);
+  r.p0 = w.x;
+  r.p1 = w.y;
+  r.ua = w.z;
+  r.ub = w.w;
   r.nslots = (r.ub - r.ua + SU - 1) / SU;
   return r;
 }
@@ -246,14 +258,22 @@ struct AItem {
   int g, sp, k0, k1, ntile;
 };
 
-template <int TKM>
-__device__ __forceinline__ AItem a_item(const MegaArgs& a, int item, int L) {
-  AItem it;
-  it.g = item / a.nsplit;
-  it.sp = item - it.g * a.nsplit;
+// keys [k0, k1) of split sp of L keys (k0 a multiple of 8: 16-byte int8-scale copies)
+__device__ __forceinline__ int4 a_split(const MegaArgs& a, int item, int L) {
   const int ns = a.nsplit;
-  it.k0 = min(L, static_cast<int>((static_cast<long long>(L) * it.sp) / ns) & ~7);
-  it.k1 = (it.sp == ns - 1) ? L : min(L, static_cast<int>((static_cast<long long>(L) * (it.sp + 1)) / ns) & ~7);
+  const int g = item / ns, sp = item - (item / ns) * ns;
+  const int k0 = min(L, static_cast<int>((static_cast<long long>(L) * sp) / ns) & ~7);
+  const int k1 = (sp == ns - 1) ? L : min(L, static_cast<int>((static_cast<long long>(L) * (sp + 1)) / ns) & ~7);
+  return make_int4(g, sp, k0, k1);
+}
+
+template <int TKM>
+__device__ __forceinline__ AItem a_item(const MegaShared& sh) {
+  AItem it;
+  it.g = sh.item.x;
+  it.sp = sh.item.y;
+  it.k0 = sh.item.z;
+  it.k1 = sh.item.w;
   it.ntile = it.k1 > it.k0 ? (it.k1 - it.k0 + TKM - 1) / TKM : 0;
   return it;
 }
@@ -281,6 +301,7 @@ struct Stream {
   const __half* vsb = nullptr;
   int j0 = 0, k1 = 0;
   uint64_t policy = 0;  // L2 evict-first: weights and K/V history are read once per step
+  const MegaShared* shp = nullptr;
 
   __device__ void enter(const MegaArgs& a, int cta, int G, int warp, int pos, int qkv_n) {
     k = 0;
@@ -290,23 +311,22 @@ struct Stream {
     const int l = q / kPhases, j = q - (q / kPhases) * kPhases;
     if (l < a.n_layers && j == PH_ATTN) {
       if (cta >= a.nkv * a.nsplit) return;
-      const AItem it = a_item<TKM>(a, cta, pos + 1);
-      const LayerPtrs& lp = a.layers[l];
+      const AItem it = a_item<TKM>(*shp);
       const size_t head_row = (static_cast<size_t>(a.seq) * a.nkv + it.g) * a.cap;
       attn = true;
       n = a_mine<TKM>(it, warp);
-      kb = static_cast<const uint8_t*>(lp.kc) + head_row * ROWB;
-      vb = static_cast<const uint8_t*>(lp.vc) + head_row * ROWB;
+      kb = a.kc + static_cast<size_t>(l) * a.s_kv + head_row * ROWB;
+      vb = a.vc + static_cast<size_t>(l) * a.s_kv + head_row * ROWB;
       if constexpr (I8) {
-        ksb = static_cast<const __half*>(lp.ks) + head_row;
-        vsb = static_cast<const __half*>(lp.vs) + head_row;
+        ksb = reinterpret_cast<const __half*>(a.ks + static_cast<size_t>(l) * a.s_sc) + head_row;
+        vsb = reinterpret_cast<const __half*>(a.vs + static_cast<size_t>(l) * a.s_sc) + head_row;
       }
       j0 = it.k0 + warp * TKM;
       k1 = it.k1;
       return;
     }
-    const GDesc d = gdesc(a, q, qkv_n, D);
-    const GRange r = g_range(d, cta, G, warp);
+    const GDesc d = gdesc(a, *shp, q, qkv_n, D);
+    const GRange r = g_range(d, *shp, warp);
     n = r.nslots;
     src = d.W + (static_cast<size_t>(r.p0) * d.CT + r.ua) * kUnit;
     left = r.ub - r.ua;
@@ -321,8 +341,9 @@ struct Stream {
     done = q > lastq;
   }
 
-  __device__ void start(const MegaArgs& a, uint8_t* ring, uint64_t* full, int cta, int G, int warp, int pos,
-                        int qkv_n) {
+  __device__ void start(const MegaArgs& a, const MegaShared& sh, uint8_t* ring, uint64_t* full, int cta, int G,
+                        int warp, int pos, int qkv_n) {
+    shp = &sh;
     lastq = a.n_layers * kPhases - 1 + (a.head ? 1 : 0);
     policy = l2_evict_first_policy();
     q = 0;
@@ -381,11 +402,11 @@ __device__ __forceinline__ uint8_t* gain_buf(uint8_t* smem, int b) {
   return smem + kMegaRingBytes + kMegaXBytes + b * kMegaGainBytes;
 }
 // the gain of the first gain phase after phase q (null if none)
-__device__ __forceinline__ const void* next_gain(const MegaArgs& a, int q) {
+__device__ __forceinline__ const void* next_gain(const MegaArgs& a, const MegaShared& sh, int q) {
   const int l = q / kPhases, j = q - (q / kPhases) * kPhases;
   if (l >= a.n_layers) return nullptr;
-  if (j < PH_GU) return a.layers[l].mlp_norm;
-  if (l + 1 < a.n_layers) return a.layers[l + 1].attn_norm;
+  if (j < PH_GU) return sh.gains[2 * l + 1];
+  if (l + 1 < a.n_layers) return sh.gains[2 * l + 2];
   return a.head ? a.final_norm : nullptr;
 }
 __device__ __forceinline__ void issue_gain(const MegaArgs& a, uint8_t* smem, MegaShared& sh, GainQ& gq,
@@ -453,7 +474,7 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
   const int K = d.K, CT = d.CT;
   float* xs = reinterpret_cast<float*>(smem + kMegaRingBytes);
   uint8_t* ring = smem + static_cast<size_t>(warp) * NS * SB;
-  const GRange r = g_range(d, cta, G, warp);
+  const GRange r = g_range(d, sh, warp);
   if (lane == 0) sh.rec_n[warp] = 0;
 
   // ---- x, normalised if the phase has a gain, lane-interleaved per chunk
@@ -473,7 +494,7 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
       guse = gq.used >> 1;
       gsm = reinterpret_cast<const WT*>(gain_buf(smem, gb));
       ++gq.used;
-      const void* ng = next_gain(a, q);
+      const void* ng = next_gain(a, sh, q);
       if (tid == 0 && ng != nullptr) issue_gain(a, smem, sh, gq, ng, K * static_cast<int>(sizeof(WT)));
     }
     float side = 0.f;
@@ -718,9 +739,8 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (cta >= a.nkv * a.nsplit) return true;
   const int L = pos + 1;
-  const AItem it = a_item<TKM>(a, cta, L);
+  const AItem it = a_item<TKM>(sh);
   const int nmine = a_mine<TKM>(it, warp);
-  const LayerPtrs& lp = a.layers[l];
   const size_t head_row = (static_cast<size_t>(a.seq) * a.nkv + it.g) * a.cap;
   uint8_t* ring = smem + static_cast<size_t>(warp) * NS * SB;
   const bool appends = (it.k1 == L);  // this split holds the new token's key
@@ -799,7 +819,8 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
     if (appends && jr >= 0 && jr < rows) {  // the new token: cache format, to global and into the slot
       for (int kv = 0; kv < 2; ++kv) {
         const float* src = sh.newkv[kv];
-        KVT* dst = static_cast<KVT*>(kv == 0 ? lp.kc : lp.vc) + (head_row + pos) * D;
+        KVT* dst = reinterpret_cast<KVT*>((kv == 0 ? a.kc : a.vc) + static_cast<size_t>(l) * a.s_kv) +
+                   (head_row + pos) * D;
         KVT* row = reinterpret_cast<KVT*>(slot + kv * KVB + jr * ROWB);
         if constexpr (I8) {
           float amax = 0.f;
@@ -815,7 +836,7 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
             row[e] = ci;
           }
           if (lane == 0) {
-            static_cast<__half*>(kv == 0 ? lp.ks : lp.vs)[head_row + pos] = sh16;
+            reinterpret_cast<__half*>((kv == 0 ? a.ks : a.vs) + static_cast<size_t>(l) * a.s_sc)[head_row + pos] = sh16;
             reinterpret_cast<__half*>(slot + 2 * KVB + kv * TKM * 2)[jr] = sh16;
           }
         } else if constexpr (std::is_same<KVT, __half>::value) {
@@ -1020,10 +1041,22 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(&sh.full[warp][s], 1);
     fence_mbar_init();
-    st.start(a, smem + static_cast<size_t>(warp) * NS * SB, sh.full[warp], cta, G, warp, pos, qkv_n);
   }
-  __syncthreads();  // barriers initialised
-  if (tid == 0) issue_gain(a, smem, sh, gq, a.layers[0].attn_norm, a.hidden * static_cast<int>(sizeof(WT)));
+  // per-launch tables: row splits of the five GEMV kinds, the attention item,
+  // the norm-gain pointers
+  if (tid < 5 * MW) {
+    const int kind = tid / MW, w = tid - (tid / MW) * MW;
+    const int N = kind == 0 ? qkv_n : kind == 2 ? 2 * a.inter : kind == 4 ? a.vocab : a.hidden;
+    const int CT = kind == 0 ? a.g_qkv.CT : kind == 1 ? a.g_o.CT : kind == 2 ? a.g_gu.CT
+                 : kind == 3 ? a.g_down.CT : a.g_lm.CT;
+    sh.wr[kind][w] = g_split(N, CT, cta, G, w);
+  }
+  if (tid == 5 * MW) sh.item = a_split(a, min(cta, a.nkv * a.nsplit - 1), pos + 1);
+  for (int i = tid; i < 2 * a.n_layers; i += MT)
+    sh.gains[i] = (i & 1) ? a.layers[i >> 1].mlp_norm : a.layers[i >> 1].attn_norm;
+  __syncthreads();  // barriers initialised, tables written
+  if (lane == 0) st.start(a, sh, smem + static_cast<size_t>(warp) * NS * SB, sh.full[warp], cta, G, warp, pos, qkv_n);
+  if (tid == 0) issue_gain(a, smem, sh, gq, sh.gains[0], a.hidden * static_cast<int>(sizeof(WT)));
   if (tid < D / 2) sh.rope_pos[tid] = a.rope[static_cast<size_t>(pos) * (D / 2) + tid];
   int consumed = 0;
   Best best{-INFINITY, 0x7fffffff};
@@ -1082,7 +1115,7 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
       xt = a.t_act;
       if (l == a.n_layers - 1) ep.plain = a.x_out;
     }
-    ok = g_phase<WT, D, KVT>(a, q, gdesc(a, q, qkv_n, D), xt, tag_in, x0f, x0w, r0f, r0w, ep, smem, sh, st, gq,
+    ok = g_phase<WT, D, KVT>(a, q, gdesc(a, sh, q, qkv_n, D), xt, tag_in, x0f, x0w, r0f, r0w, ep, smem, sh, st, gq,
                              consumed, best, cta, G, pos, qkv_n);
   }
   if (ok && a.head) {
