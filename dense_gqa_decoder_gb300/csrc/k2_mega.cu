@@ -855,14 +855,17 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
       }
       __syncwarp();
     }
+    // scores: 8 lanes per key, every step computed (rows past the end hold
+    // stale bytes of the slot; their scores are never stored), so the
+    // compiler can overlap the steps
 #pragma unroll
     for (int stp = 0; stp < (TKM + KPS - 1) / KPS; ++stp) {
       const int jj = stp * KPS + lane / LPK;
       float dot[REP];
 #pragma unroll
       for (int h = 0; h < REP; ++h) dot[h] = 0.f;
-      if (jj < rows) {
-        const uint8_t* kr = slot + jj * ROWB + kl * VPL * 16;
+      {
+        const uint8_t* kr = slot + min(jj, TKM - 1) * ROWB + kl * VPL * 16;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
           float kf[EPL];
@@ -912,22 +915,27 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
 #pragma unroll
         for (int dd = 0; dd < DPL; ++dd) acc[h][dd] *= al[h];
       const KVT* vt = reinterpret_cast<const KVT*>(slot + KVB) + lane * DPL;
-#pragma unroll 4
-      for (int jj = 0; jj < rows; ++jj) {
+      auto pv_row = [&](int jj) {
         float vf[DPL];
         vload<DPL>(vt + jj * D, vf);
-        float pr[REP];
+        float pw[REP];
         if constexpr (REP == 4) {
           const float4 p4 = *reinterpret_cast<const float4*>(&Pw[warp][jj][0]);
-          pr[0] = p4.x; pr[1] = p4.y; pr[2] = p4.z; pr[3] = p4.w;
+          pw[0] = p4.x; pw[1] = p4.y; pw[2] = p4.z; pw[3] = p4.w;
         } else {
 #pragma unroll
-          for (int h = 0; h < REP; ++h) pr[h] = Pw[warp][jj][h];
+          for (int h = 0; h < REP; ++h) pw[h] = Pw[warp][jj][h];
         }
 #pragma unroll
         for (int h = 0; h < REP; ++h)
 #pragma unroll
-          for (int dd = 0; dd < DPL; ++dd) acc[h][dd] = fmaf(pr[h], vf[dd], acc[h][dd]);
+          for (int dd = 0; dd < DPL; ++dd) acc[h][dd] = fmaf(pw[h], vf[dd], acc[h][dd]);
+      };
+      if (rows == TKM) {  // a full tile: every row, unrolled
+#pragma unroll
+        for (int jj = 0; jj < TKM; ++jj) pv_row(jj);
+      } else {
+        for (int jj = 0; jj < rows; ++jj) pv_row(jj);
       }
     }
     // Where this slot was written by generic stores (the new row), order
