@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <array>
 #include <map>
 #include <string>
 #include <tuple>
@@ -25,6 +26,8 @@ constexpr size_t kAttnSmem = 128 * 1024;
 constexpr size_t kLmHeadSmem = 176 * 1024;
 constexpr int kArgmaxPartsMax = 1024;
 constexpr int kMegaSplitMax = 64;
+constexpr int kPrefillChunk = 2048;  // prompt tokens per tensor-core prefill pass
+constexpr int kTcPrefillMin = 8;     // shorter prompts are appended one decode step per token
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -36,6 +39,9 @@ int elt_bytes(int dt) { return dt == K2_F32 ? 4 : (dt == K2_BF16 || dt == K2_F16
 struct Layout {
   size_t seq_len, guard, am_counter, msync, rope, resid, qkv, attn_out, act, am_val, am_idx, attn_part, ltab;
   size_t t_resid, t_qkv, t_attn, t_act, t_part;  // persistent step: (value, tag) activations
+  // tensor-core prefill of up to `pchunk` tokens at a time (bf16 weights)
+  int pchunk;
+  size_t px, pxh, pxl, pah, pal, pqkv, pq;
   size_t wqkv, wo, wgu, wdown, wlm;  // packed weights; per-layer strides below
   size_t wqkv_layer, wo_layer, wgu_layer, wdown_layer;
   size_t kc, vc, ks, vs;  // first layer; per-layer stride kv_layer / sc_layer
@@ -91,6 +97,18 @@ Layout layout_of(const k2_config& c) {
   l.t_attn = take(8 * static_cast<size_t>(s.nq) * s.d);
   l.t_act = take(8 * static_cast<size_t>(s.I));
   l.t_part = take(8 * static_cast<size_t>(s.nkv) * kMegaSplitMax * s.rep * (s.d + 2));
+  l.pchunk = c.weight_dtype == K2_BF16 ? static_cast<int>(align_up(std::min(kPrefillChunk, s.ctx), 128)) : 0;
+  {
+    const size_t P = static_cast<size_t>(l.pchunk);
+    const size_t kx = std::max(s.H, s.nq * s.d);
+    l.px = take(P * s.H * 4);
+    l.pxh = take(P * kx * 2);
+    l.pxl = take(P * kx * 2);
+    l.pah = take(P * s.I * 2);
+    l.pal = take(P * s.I * 2);
+    l.pqkv = take(P * s.qkv_n * 4);
+    l.pq = take(P * s.nq * s.d * 4);
+  }
   const size_t scratch_end = o;
   l.wqkv_layer = align_up(packed_bytes(s.qkv_n, s.H, s.wb), kAlign);
   l.wo_layer = align_up(packed_bytes(s.H, s.nq * s.d, s.wb), kAlign);
@@ -180,6 +198,12 @@ struct k2_ctx {
   int mega_grid = 0;
   MegaArgs mega = {};
   std::vector<LayerPtrs> ltab;
+  // tensor-core prefill: TMA tensor maps (weights per layer: qkv, o, gate/up,
+  // down; activations: normed input, attention output, SwiGLU output, hi/lo)
+  bool tc_ok = false;
+  bool use_tc = true;
+  std::vector<std::array<uint8_t, kTcMapBytes>> tmw;  // 4 per layer
+  std::array<uint8_t, kTcMapBytes> tm_xh{}, tm_xl{}, tm_oh{}, tm_ol{}, tm_ah{}, tm_al{};
   std::map<std::tuple<int, const void*, const void*, const void*, void*>, cudaGraphExec_t> graphs;
   std::string err;
   // profiling: event pairs around the kernels of one step
@@ -518,6 +542,118 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   return cudaSuccess;
 }
 
+// Tensor maps of the tensor-core prefill (bf16 weights, a supported attention
+// shape).  Leaves tc_ok false when it cannot run.
+cudaError_t plan_tc_prefill(k2_ctx* c) {
+  const Sizes& s = c->s;
+  c->tc_ok = false;
+  if (c->lay.pchunk <= 0 || s.wb != 2 || !prefill_attn_supported(s.d, s.rep)) return cudaSuccess;
+  if (s.H % 8 || (s.nq * s.d) % 8 || s.I % 8) return cudaSuccess;
+  cudaError_t e = prefill_init_attrs();
+  if (e != cudaSuccess) return e;
+  c->tmw.resize(4 * static_cast<size_t>(s.L));
+  for (int l = 0; l < s.L; ++l) {
+    if (!tc_encode_weight(c->tmw[4 * l].data(), c->wqkv(l), s.qkv_n, s.H) ||
+        !tc_encode_weight(c->tmw[4 * l + 1].data(), c->wop(l), s.H, s.nq * s.d) ||
+        !tc_encode_weight(c->tmw[4 * l + 2].data(), c->wgu(l), 2 * s.I, s.H) ||
+        !tc_encode_weight(c->tmw[4 * l + 3].data(), c->wdown(l), s.H, s.I))
+      return cudaSuccess;
+  }
+  const int P = c->lay.pchunk;
+  if (!tc_encode_act(c->tm_xh.data(), c->ws + c->lay.pxh, P, s.H) ||
+      !tc_encode_act(c->tm_xl.data(), c->ws + c->lay.pxl, P, s.H) ||
+      !tc_encode_act(c->tm_oh.data(), c->ws + c->lay.pxh, P, s.nq * s.d) ||
+      !tc_encode_act(c->tm_ol.data(), c->ws + c->lay.pxl, P, s.nq * s.d) ||
+      !tc_encode_act(c->tm_ah.data(), c->ws + c->lay.pah, P, s.I) ||
+      !tc_encode_act(c->tm_al.data(), c->ws + c->lay.pal, P, s.I))
+    return cudaSuccess;
+  c->tc_ok = true;
+  return cudaSuccess;
+}
+
+// One block of n <= pchunk prompt tokens of sequence seq at positions
+// pos0 .. pos0+n-1 through every layer; the residual of its last token is left
+// in pX[n-1].
+cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int pos0, cudaStream_t st) {
+  const Sizes& s = c->s;
+  float* X = reinterpret_cast<float*>(c->ws + c->lay.px);
+  auto* xh = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxh);
+  auto* xl = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxl);
+  auto* ah = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pah);
+  auto* al = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pal);
+  float* qkv = reinterpret_cast<float*>(c->ws + c->lay.pqkv);
+  float* Q = reinterpret_cast<float*>(c->ws + c->lay.pq);
+  const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
+  const size_t head_row0 = static_cast<size_t>(seq) * s.nkv * c->lay.cap;
+  const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(s.d)));
+  auto gemm = [&](const void* mw, const void* mh, const void* ml, int N, int K, int mode, float* out,
+                  __nv_bfloat16* oh, __nv_bfloat16* ol, int ldo) {
+    TcGemmArgs g = {};
+    g.N = N;
+    g.K = K;
+    g.T = n;
+    g.ksteps = 4 * ((K + 255) / 256);
+    g.mode = mode;
+    g.ldo = ldo;
+    g.out = out;
+    g.out_hi = oh;
+    g.out_lo = ol;
+    g.guard = c->guard;
+    return launch_tc_gemm(mw, mh, ml, g, st);
+  };
+  cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.wb, X, s.H, s.V, c->guard, st);
+  for (int l = 0; l < s.L && !e; ++l) {
+    if (!e) e = launch_norm_rows(X, n, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
+    if (!e) e = gemm(c->tmw[4 * l].data(), c->tm_xh.data(), c->tm_xl.data(), s.qkv_n, s.H, TC_STORE, qkv, nullptr,
+                     nullptr, s.qkv_n);
+    if (!e)
+      e = launch_rope_append(qkv, Q, c->rope, kvdt, c->kc(l), c->vc(l), c->ks(l), c->vs(l), n, s.nq, s.nkv, s.d,
+                             pos0, head_row0, c->lay.cap, st);
+    if (!e)
+      e = launch_prefill_attn(Q, kvdt, c->kc(l), c->vc(l), c->ks(l), c->vs(l), xh, xl, n, s.nq, s.nkv, s.d, pos0,
+                              head_row0, c->lay.cap, scale, st);
+    if (!e) e = gemm(c->tmw[4 * l + 1].data(), c->tm_oh.data(), c->tm_ol.data(), s.H, s.nq * s.d, TC_RESID, X,
+                     nullptr, nullptr, s.H);
+    if (!e) e = launch_norm_rows(X, n, c->mlp_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
+    if (!e) e = gemm(c->tmw[4 * l + 2].data(), c->tm_xh.data(), c->tm_xl.data(), 2 * s.I, s.H, TC_SWIGLU, nullptr,
+                     ah, al, s.I);
+    if (!e) e = gemm(c->tmw[4 * l + 3].data(), c->tm_ah.data(), c->tm_al.data(), s.H, s.I, TC_RESID, X, nullptr,
+                     nullptr, s.H);
+  }
+  return e;
+}
+
+// The whole prompt through tensor-core blocks, then the greedy head on the
+// last token's residual (which is also left in the hidden view of seq).
+cudaError_t prefill_tc(k2_ctx* c, int seq, const int* d_tokens, int n, int* d_next, float* d_logits,
+                       cudaStream_t st) {
+  const Sizes& s = c->s;
+  const int P = c->lay.pchunk;
+  cudaError_t e = cudaSuccess;
+  int last = 0;
+  for (int b0 = 0; b0 < n && !e; b0 += P) {
+    last = std::min(P, n - b0);
+    e = prefill_block(c, seq, d_tokens + b0, last, c->len[seq] + b0, st);
+  }
+  if (e) return e;
+  float* xrow = c->resid + static_cast<size_t>(seq) * s.H;
+  e = cudaMemcpyAsync(xrow, c->ws + c->lay.px + static_cast<size_t>(last - 1) * s.H * 4, sizeof(float) * s.H,
+                      cudaMemcpyDeviceToDevice, st);
+  if (e) return e;
+  PackedGemvArgs lm = c->p_lm;
+  lm.x = xrow;
+  lm.logits = d_logits;
+  lm.next_token = d_next;
+  lm.counter = c->am_counter + seq;
+  lm.part_val = c->am_val + static_cast<size_t>(seq) * kArgmaxPartsMax;
+  lm.part_idx = c->am_idx + static_cast<size_t>(seq) * kArgmaxPartsMax;
+  lm.seq = seq;
+  lm.advance = 0;
+  e = launch_packed_gemv(lm, s.wb, EPI_ARGMAX, c->grid_lm, st, false);
+  if (e) return e;
+  return launch_advance_by(c->seq_len, seq, n, st);
+}
+
 k2_status validate_weights(k2_ctx* c, const k2_weights* w) {
   auto ok = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % 16) == 0; };
   if (!w) return c->fail(K2_ERR_ARG, "weights is NULL");
@@ -663,6 +799,11 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     delete c;
     return K2_ERR_CUDA;
   }
+  if ((e = plan_tc_prefill(c)) != cudaSuccess) {
+    g_init_error = std::string("tensor-core prefill set-up: ") + cudaGetErrorString(e);
+    delete c;
+    return K2_ERR_CUDA;
+  }
   *out = c;
   return K2_OK;
 }
@@ -699,6 +840,12 @@ k2_status k2_prefill(k2_ctx* c, int32_t seq, const int32_t* d_tokens, int32_t n,
   if (static_cast<long long>(c->len[seq]) + n > c->s.ctx)
     return c->fail(K2_ERR_CONTEXT_FULL, "prompt of %d tokens does not fit: sequence %d holds %d of %d", n, seq,
                    c->len[seq], c->s.ctx);
+  if (c->tc_ok && c->use_tc && n >= kTcPrefillMin) {
+    const cudaError_t e = prefill_tc(c, seq, d_tokens, n, d_next_token, d_logits, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return c->cuda_fail(e, "tensor-core prefill");
+    c->len[seq] += n;
+    return K2_OK;
+  }
   Launcher ln{c, static_cast<cudaStream_t>(stream), c->pdl};
   for (int i = 0; i < n; ++i) {
     const bool last = i == n - 1;
@@ -854,6 +1001,7 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
     case K2_OPT_PDL: c->pdl = value != 0; break;
     case K2_OPT_GRAPH: c->graph = value != 0; break;
     case K2_OPT_PERSISTENT: c->use_mega = value != 0; break;
+    case K2_OPT_TC_PREFILL: c->use_tc = value != 0; break;
     case K2_OPT_ATTN_SPLITS:
       if (value < 0 || value > kAttnMaxCluster)
         return c->fail(K2_ERR_ARG, "splits %lld outside [0, %d]", (long long)value, kAttnMaxCluster);

@@ -172,6 +172,8 @@ template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 template <>
 __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <>
+__device__ __forceinline__ float to_f32<int8_t>(int8_t v) { return static_cast<float>(v); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -1,6 +1,7 @@
 // Argument blocks and launchers of the sm_103a kernels (internal to libk2).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -254,6 +255,41 @@ cudaError_t launch_repack_qkv(void* dst, const void* wq, const void* wk, const v
 cudaError_t launch_repack_gateup(void* dst, const void* wg, const void* wu, int wbytes, int inter, int hidden,
                                  cudaStream_t s);
 cudaError_t launch_advance(int* seq_len, int seq0, int batch, cudaStream_t s, bool pdl);
+
+// ---- prefill: tensor-core GEMMs (k2_tcgemm.cu) and the row-wise kernels (k2_prefill.cu)
+enum { TC_STORE = 0, TC_RESID = 1, TC_SWIGLU = 2 };
+struct TcGemmArgs {
+  int N;       // weight rows (packed order)
+  int K;       // reduction length
+  int T;       // tokens
+  int ksteps;  // 64-element K steps over the packed chunks: 4 * ceil(K / 256)
+  int mode;    // TC_STORE: out[t][row] = acc; TC_RESID: out[t][row] += acc;
+               // TC_SWIGLU: rows (2p, 2p+1) -> silu(gate) * up -> out_hi/out_lo[t][p]
+  int ldo;     // row stride of the output (elements)
+  float* out;
+  __nv_bfloat16* out_hi;
+  __nv_bfloat16* out_lo;
+  unsigned* guard;
+};
+constexpr int kTcMapBytes = 128;  // one CUtensorMap
+bool tc_encode_weight(void* map, const void* packed, int N, int K);  // bf16 packed weights
+bool tc_encode_act(void* map, const void* buf, int rows, int K);     // bf16 [rows][K]
+cudaError_t tc_gemm_init_attrs();
+cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a,
+                           cudaStream_t s);
+bool prefill_attn_supported(int head_dim, int rep);
+cudaError_t prefill_init_attrs();
+cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbytes, float* X, int H, int vocab,
+                              unsigned* guard, cudaStream_t s);
+cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes, __nv_bfloat16* oh,
+                             __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s);
+cudaError_t launch_rope_append(const float* qkv, float* Q, const float2* rope, int kv_dtype, void* kc, void* vc,
+                               void* ks, void* vs, int n, int nq, int nkv, int D, int pos0, size_t head_row0, int cap,
+                               cudaStream_t s);
+cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, const void* vc, const void* ks,
+                                const void* vs, __nv_bfloat16* oh, __nv_bfloat16* ol, int n, int nq, int nkv, int D,
+                                int pos0, size_t head_row0, int cap, float scale, cudaStream_t s);
+cudaError_t launch_advance_by(int* seq_len, int seq, int n, cudaStream_t s);
 cudaError_t misc_init_attrs();
 
 }  // namespace k2

@@ -1,0 +1,377 @@
+// Prefill of a block of prompt tokens (k2-burn README, "Status: v0": prefill
+// then single-token decode; only the last position's logits are needed).
+//
+// The projections run as tensor-core GEMMs (k2_tcgemm.cu) over the whole
+// block; the kernels here do the row-wise work between them:
+//   embed rows -> [GroupedRMSNorm -> QKV GEMM -> split-half RoPE + KV append ->
+//   causal GQA attention -> o_proj GEMM (+residual) -> GroupedRMSNorm ->
+//   gate/up GEMM (+SwiGLU) -> down GEMM (+residual)] x layers.
+// Inputs of a GEMM are written as bf16 (hi, lo) pairs whose sum is the fp32
+// value (see k2_tcgemm.cu); the residual stream stays fp32.
+#include <math.h>
+
+#include <type_traits>
+
+#include "k2_kernels.h"
+#include "k2_common.cuh"
+
+namespace k2 {
+
+namespace {
+
+__device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+template <typename WT>
+__global__ void embed_rows_kernel(const int* __restrict__ tokens, const WT* __restrict__ E, float* __restrict__ X,
+                                  int H, int vocab, unsigned* guard) {
+  const int t = blockIdx.x;
+  int tok = tokens[t];
+  if (tok < 0 || tok >= vocab) {
+    if (threadIdx.x == 0) atomicOr(guard, GUARD_TOKEN);
+    tok = 0;
+  }
+  const WT* e = E + static_cast<size_t>(tok) * H;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) X[static_cast<size_t>(t) * H + i] = to_f32(e[i]);
+}
+
+// GroupedRMSNorm of one row (k2-burn README, "Model shape": layernorm groups),
+// written as bf16 hi/lo
+template <typename WT>
+__global__ void norm_rows_kernel(const float* __restrict__ X, const WT* __restrict__ gain, __nv_bfloat16* __restrict__ oh,
+                                 __nv_bfloat16* __restrict__ ol, int H, int groups, float eps) {
+  __shared__ float part[32][4];
+  __shared__ float rs[4];
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* x = X + static_cast<size_t>(t) * H;
+  const int gsz = H / groups;
+  float ss[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int i = tid; i < H; i += blockDim.x) {
+    const float v = x[i];
+    const int g = i / gsz;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (q == g) ss[q] += v * v;
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) ss[q] = warp_sum(ss[q]);
+  if (lane == 0)
+    for (int q = 0; q < 4; ++q) part[warp][q] = ss[q];
+  __syncthreads();
+  if (tid < groups) {
+    float s = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x / 32); ++w) s += part[w][tid];
+    rs[tid] = 1.0f / sqrtf(s / static_cast<float>(gsz) + eps);
+  }
+  __syncthreads();
+  for (int i = tid; i < H; i += blockDim.x) {
+    const float y = x[i] * rs[i / gsz] * to_f32(gain[i]);
+    __nv_bfloat16 hi, lo;
+    split_bf16(y, hi, lo);
+    oh[static_cast<size_t>(t) * H + i] = hi;
+    ol[static_cast<size_t>(t) * H + i] = lo;
+  }
+}
+
+// split-half RoPE on the QKV GEMM output (rows of every head in the packed
+// order (i, i + d/2) adjacent) and the KV append of every token of the block
+template <typename KVT>
+__global__ void rope_append_kernel(const float* __restrict__ qkv, float* __restrict__ Q, const float2* __restrict__ rope,
+                                   KVT* __restrict__ kc, KVT* __restrict__ vc, __half* __restrict__ ks,
+                                   __half* __restrict__ vs, int nq, int nkv, int D, int pos0, size_t head_row0,
+                                   int cap) {
+  extern __shared__ float rows[];  // [2 * nkv][D]: this token's K and V rows
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int qkv_n = (nq + 2 * nkv) * D, half = D / 2, pos = pos0 + t;
+  const float* src = qkv + static_cast<size_t>(t) * qkv_n;
+  for (int idx = tid; idx < (nq + 2 * nkv) * half; idx += blockDim.x) {
+    const int h = idx / half, i = idx - h * half;
+    float a = src[h * D + 2 * i], b = src[h * D + 2 * i + 1];
+    if (h < nq + nkv) {
+      const float2 cs = rope[static_cast<size_t>(pos) * half + i];
+      const float ra = a * cs.x - b * cs.y, rb = b * cs.x + a * cs.y;
+      a = ra;
+      b = rb;
+    }
+    if (h < nq) {
+      Q[static_cast<size_t>(t) * nq * D + h * D + i] = a;
+      Q[static_cast<size_t>(t) * nq * D + h * D + i + half] = b;
+    } else {
+      const int r = h - nq;  // K rows 0 .. nkv-1, then V rows
+      rows[r * D + i] = a;
+      rows[r * D + i + half] = b;
+    }
+  }
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int r = warp; r < 2 * nkv; r += blockDim.x / 32) {  // one warp per K or V row
+    const int g = r < nkv ? r : r - nkv;
+    const size_t row = (head_row0 + static_cast<size_t>(g) * cap + pos);
+    KVT* dst = (r < nkv ? kc : vc) + row * D;
+    const float* v = rows + r * D;
+    if constexpr (std::is_same<KVT, int8_t>::value) {
+      float amax = 0.f;
+      for (int e = lane; e < D; e += 32) amax = fmaxf(amax, fabsf(v[e]));
+      amax = warp_max(amax);
+      const __half s16 = __float2half_rn(fminf(amax / 127.0f, 65504.0f));
+      const float sf = __half2float(s16);
+      for (int e = lane; e < D; e += 32) {
+        float cq = sf > 0.f ? rintf(v[e] / sf) : 0.f;
+        cq = fminf(fmaxf(cq, -127.f), 127.f);
+        dst[e] = static_cast<int8_t>(cq);
+      }
+      if (lane == 0) (r < nkv ? ks : vs)[row] = s16;
+    } else if constexpr (std::is_same<KVT, __half>::value) {
+      for (int e = lane; e < D; e += 32) dst[e] = __float2half_rn(v[e]);
+    } else {
+      for (int e = lane; e < D; e += 32) dst[e] = v[e];
+    }
+  }
+}
+
+// Causal GQA attention of a block of query tokens against the cache (which
+// already holds the block's own rows).  One CTA per (16 query tokens, KV head):
+// the 16 x REP query rows share every 64-key K/V tile; fp32 scores, online
+// softmax per row, output written as bf16 hi/lo for the o_proj GEMM.
+constexpr int kPaQT = 16, kPaKT = 64, kPaThreads = 256;
+
+template <int D, int REP, typename KVT>
+__global__ void __launch_bounds__(kPaThreads) prefill_attn_kernel(const float* __restrict__ Q, const KVT* __restrict__ kc,
+                                                                  const KVT* __restrict__ vc, const __half* __restrict__ ks,
+                                                                  const __half* __restrict__ vs, __nv_bfloat16* __restrict__ oh,
+                                                                  __nv_bfloat16* __restrict__ ol, int n, int nq, int pos0,
+                                                                  size_t head_row0, int cap, float scale) {
+  constexpr int QR = kPaQT * REP;   // query rows of the CTA (64 for REP 4)
+  constexpr int DP = D + 1;         // padded row (bank spread)
+  constexpr int RPT = QR / 16;      // rows per thread (threads as 16 x 16)
+  constexpr int KPT = kPaKT / 16;   // keys per thread in the score tile
+  constexpr int DPT = D / 16;       // output dims per thread
+  extern __shared__ float sm[];
+  float* Qs = sm;                    // [QR][DP]
+  float* Ks = Qs + QR * DP;          // [KT][DP]
+  float* Vs = Ks + kPaKT * DP;       // [KT][D]
+  float* Ps = Vs + kPaKT * D;        // [QR][KT + 1]
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int t0 = blockIdx.x * kPaQT, g = blockIdx.y;
+  const int nt = min(kPaQT, n - t0);
+  const size_t hr = head_row0 + static_cast<size_t>(g) * cap;
+  // query rows: r = tq * REP + h  ->  token t0 + tq, head g * REP + h
+  for (int idx = tid; idx < QR * D; idx += kPaThreads) {
+    const int r = idx / D, d = idx - r * D, tq = r / REP, h = r - tq * REP;
+    Qs[r * DP + d] = tq < nt ? Q[static_cast<size_t>(t0 + tq) * nq * D + (g * REP + h) * D + d] * scale : 0.f;
+  }
+  float m[RPT], l[RPT], o[RPT][DPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < DPT; ++j) o[i][j] = 0.f;
+  }
+  const int kend = pos0 + t0 + nt;  // keys [0, kend) can be visible to some row of the CTA
+  for (int k0 = 0; k0 < kend; k0 += kPaKT) {
+    __syncthreads();  // the previous tile is consumed
+    for (int idx = tid; idx < kPaKT * D; idx += kPaThreads) {
+      const int j = idx / D, d = idx - j * D, key = k0 + j;
+      float kv = 0.f, vv = 0.f;
+      if (key < kend) {
+        kv = to_f32(kc[(hr + key) * D + d]);
+        vv = to_f32(vc[(hr + key) * D + d]);
+        if constexpr (std::is_same<KVT, int8_t>::value) {
+          kv *= __half2float(ks[hr + key]);
+          vv *= __half2float(vs[hr + key]);
+        }
+      }
+      Ks[j * DP + d] = kv;
+      Vs[j * D + d] = vv;
+    }
+    __syncthreads();
+    // scores of rows ty * RPT + i, keys tx + 16 * c
+    float s[RPT][KPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i)
+#pragma unroll
+      for (int c = 0; c < KPT; ++c) s[i][c] = 0.f;
+#pragma unroll 4
+    for (int d = 0; d < D; ++d) {
+      float qv[RPT], kv[KPT];
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) qv[i] = Qs[(ty * RPT + i) * DP + d];
+#pragma unroll
+      for (int c = 0; c < KPT; ++c) kv[c] = Ks[(tx + 16 * c) * DP + d];
+#pragma unroll
+      for (int i = 0; i < RPT; ++i)
+#pragma unroll
+        for (int c = 0; c < KPT; ++c) s[i][c] = fmaf(qv[i], kv[c], s[i][c]);
+    }
+    // causal mask, online softmax (the 16 threads of a row group share a row)
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int r = ty * RPT + i, tq = r / REP;
+      const int qpos = pos0 + t0 + tq;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < KPT; ++c) {
+        const int key = k0 + tx + 16 * c;
+        if (key > qpos || tq >= nt) s[i][c] = -INFINITY;
+        mx = fmaxf(mx, s[i][c]);
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m[i], mx);
+      const float al = mn == -INFINITY ? 1.f : expf(m[i] - mn);
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < KPT; ++c) {
+        const float p = s[i][c] == -INFINITY ? 0.f : expf(s[i][c] - mn);
+        Ps[r * (kPaKT + 1) + tx + 16 * c] = p;
+        sum += p;
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      l[i] = l[i] * al + sum;
+      m[i] = mn;
+#pragma unroll
+      for (int j = 0; j < DPT; ++j) o[i][j] *= al;
+    }
+    __syncthreads();
+    // o[rows][dims tx * DPT ..] += P . V
+#pragma unroll 4
+    for (int j = 0; j < kPaKT; ++j) {
+      float vv[DPT];
+#pragma unroll
+      for (int e = 0; e < DPT; ++e) vv[e] = Vs[j * D + tx * DPT + e];
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const float p = Ps[(ty * RPT + i) * (kPaKT + 1) + j];
+#pragma unroll
+        for (int e = 0; e < DPT; ++e) o[i][e] = fmaf(p, vv[e], o[i][e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = ty * RPT + i, tq = r / REP, h = r - tq * REP;
+    if (tq >= nt) continue;
+    const float inv = 1.0f / l[i];
+    const size_t base = static_cast<size_t>(t0 + tq) * nq * D + (g * REP + h) * D + tx * DPT;
+#pragma unroll
+    for (int e = 0; e < DPT; ++e) {
+      __nv_bfloat16 hi, lo;
+      split_bf16(o[i][e] * inv, hi, lo);
+      oh[base + e] = hi;
+      ol[base + e] = lo;
+    }
+  }
+}
+
+template <int D, int REP>
+constexpr size_t attn_smem() {
+  return sizeof(float) * (static_cast<size_t>(kPaQT * REP) * (D + 1) + kPaKT * (D + 1) + kPaKT * D +
+                          kPaQT * REP * (kPaKT + 1));
+}
+
+__global__ void advance_by_kernel(int* seq_len, int seq, int n) { seq_len[seq] += n; }
+
+#define K2_PREFILL_ATTN_SHAPES(X) X(128, 4) X(64, 4)
+
+}  // namespace
+
+bool prefill_attn_supported(int head_dim, int rep) {
+#define K2_PA_SUP(D, R) \
+  if (head_dim == D && rep == R) return true;
+  K2_PREFILL_ATTN_SHAPES(K2_PA_SUP)
+#undef K2_PA_SUP
+  return false;
+}
+
+cudaError_t prefill_init_attrs() {
+  cudaError_t e = cudaSuccess;
+#define K2_PA_ATTR(D, R)                                                                                     \
+  if (!e) e = cudaFuncSetAttribute(prefill_attn_kernel<D, R, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                   static_cast<int>(attn_smem<D, R>()));                                    \
+  if (!e) e = cudaFuncSetAttribute(prefill_attn_kernel<D, R, __half>,                                        \
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(attn_smem<D, R>())); \
+  if (!e) e = cudaFuncSetAttribute(prefill_attn_kernel<D, R, int8_t>,                                        \
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(attn_smem<D, R>()));
+  K2_PREFILL_ATTN_SHAPES(K2_PA_ATTR)
+#undef K2_PA_ATTR
+  if (!e) e = tc_gemm_init_attrs();
+  return e;
+}
+
+cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbytes, float* X, int H, int vocab,
+                              unsigned* guard, cudaStream_t s) {
+  if (wbytes == 2)
+    embed_rows_kernel<<<n, 256, 0, s>>>(tokens, static_cast<const __nv_bfloat16*>(E), X, H, vocab, guard);
+  else
+    embed_rows_kernel<<<n, 256, 0, s>>>(tokens, static_cast<const float*>(E), X, H, vocab, guard);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes, __nv_bfloat16* oh,
+                             __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s) {
+  if (wbytes == 2)
+    norm_rows_kernel<<<n, 256, 0, s>>>(X, static_cast<const __nv_bfloat16*>(gain), oh, ol, H, groups, eps);
+  else
+    norm_rows_kernel<<<n, 256, 0, s>>>(X, static_cast<const float*>(gain), oh, ol, H, groups, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_append(const float* qkv, float* Q, const float2* rope, int kv_dtype, void* kc, void* vc,
+                               void* ks, void* vs, int n, int nq, int nkv, int D, int pos0, size_t head_row0, int cap,
+                               cudaStream_t s) {
+  const size_t smem = sizeof(float) * 2 * nkv * D;
+  switch (kv_dtype) {
+    case 0:
+      rope_append_kernel<float><<<n, 256, smem, s>>>(qkv, Q, rope, static_cast<float*>(kc), static_cast<float*>(vc),
+                                                     nullptr, nullptr, nq, nkv, D, pos0, head_row0, cap);
+      break;
+    case 2:
+      rope_append_kernel<__half><<<n, 256, smem, s>>>(qkv, Q, rope, static_cast<__half*>(kc),
+                                                      static_cast<__half*>(vc), nullptr, nullptr, nq, nkv, D, pos0,
+                                                      head_row0, cap);
+      break;
+    default:
+      rope_append_kernel<int8_t><<<n, 256, smem, s>>>(qkv, Q, rope, static_cast<int8_t*>(kc),
+                                                      static_cast<int8_t*>(vc), static_cast<__half*>(ks),
+                                                      static_cast<__half*>(vs), nq, nkv, D, pos0, head_row0, cap);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, const void* vc, const void* ks,
+                                const void* vs, __nv_bfloat16* oh, __nv_bfloat16* ol, int n, int nq, int nkv, int D,
+                                int pos0, size_t head_row0, int cap, float scale, cudaStream_t s) {
+  const int rep = nq / nkv;
+  dim3 grid((n + kPaQT - 1) / kPaQT, nkv);
+#define K2_PA_LAUNCH(DD, R)                                                                                       \
+  if (D == DD && rep == R) {                                                                                      \
+    const size_t sm = attn_smem<DD, R>();                                                                         \
+    if (kv_dtype == 0)                                                                                            \
+      prefill_attn_kernel<DD, R, float><<<grid, kPaThreads, sm, s>>>(                                             \
+          Q, static_cast<const float*>(kc), static_cast<const float*>(vc), nullptr, nullptr, oh, ol, n, nq, pos0, \
+          head_row0, cap, scale);                                                                                 \
+    else if (kv_dtype == 2)                                                                                       \
+      prefill_attn_kernel<DD, R, __half><<<grid, kPaThreads, sm, s>>>(                                            \
+          Q, static_cast<const __half*>(kc), static_cast<const __half*>(vc), nullptr, nullptr, oh, ol, n, nq,     \
+          pos0, head_row0, cap, scale);                                                                           \
+    else                                                                                                          \
+      prefill_attn_kernel<DD, R, int8_t><<<grid, kPaThreads, sm, s>>>(                                            \
+          Q, static_cast<const int8_t*>(kc), static_cast<const int8_t*>(vc), static_cast<const __half*>(ks),      \
+          static_cast<const __half*>(vs), oh, ol, n, nq, pos0, head_row0, cap, scale);                            \
+    return cudaGetLastError();                                                                                    \
+  }
+  K2_PREFILL_ATTN_SHAPES(K2_PA_LAUNCH)
+#undef K2_PA_LAUNCH
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_advance_by(int* seq_len, int seq, int n, cudaStream_t s) {
+  advance_by_kernel<<<1, 1, 0, s>>>(seq_len, seq, n);
+  return cudaGetLastError();
+}
+
+}  // namespace k2

@@ -1,0 +1,248 @@
+// Tensor-core GEMM for prefill: D[rows x tokens] = W[rows x K] . X[tokens x K]^T
+// on the 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM).
+//
+// Prefill runs the decoder over a block of T prompt tokens at once (k2-burn
+// README, "Status: v0": prefill then single-token decode), so its projections
+// are dense contractions.  W is a packed projection matrix (pairs of rows in
+// 512-byte chunks, the same copy the decode step streams); a 4-D TMA tensor
+// map (element, row-in-pair, chunk, pair) reads it as ordinary 128-row K-major
+// tiles.  X is kept as two bf16 matrices whose sum is the fp32 activation
+// (x_hi = bf16(x), x_lo = bf16(x - x_hi)); each K step issues one MMA per
+// half, so the product keeps ~16 mantissa bits of the activation, the
+// precision the decode step's fp32 activations have, while W stays the model's
+// bf16.
+//
+// One CTA per 128-row x 128-token tile, 128 threads: thread 0 issues the TMA
+// loads into a 4-stage ring (mbarrier complete_tx), thread 32 issues the MMAs
+// (128x128x16, bf16 in, fp32 accumulate) and frees each stage with
+// tcgen05.commit, then all four warps read the accumulator tile out of TMEM
+// (warp w owns TMEM lanes 32w..32w+31 = rows) and apply the epilogue.  Every
+// wait is bounded; a timeout sets the guard word and skips the accumulator.
+#include <cuda.h>
+
+#include "k2_kernels.h"
+#include "k2_common.cuh"
+
+namespace k2 {
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + 2 * B_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment of the ring to 1024 B
+
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* m, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(m), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_4d(void* dst, const CUtensorMap* m, int c0, int c1, int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row core
+// groups 1024 B apart (the layout a 128-byte-swizzled TMA box leaves)
+__device__ __forceinline__ uint64_t smem_desc(const void* p) {
+  const uint64_t addr = (smem_u32(p) & 0x3FFFFu) >> 4;
+  return addr | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+// instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+__global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                         const __grid_constant__ CUtensorMap tmXh,
+                                                         const __grid_constant__ CUtensorMap tmXl, const TcGemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], done;
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BN;  // first token
+  const int m0 = blockIdx.y * BM;  // first (packed) weight row
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(BN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  const uint32_t tmem = tmem_slot;
+  const int nk = a.ksteps;
+  if (threadIdx.x == 0) {  // TMA producer
+    int k = 0;
+    for (; k < nk; ++k) {
+      const int s = k % STAGES;
+      if (k >= STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>((k / STAGES) - 1) & 1u)) {
+        atomicOr(a.guard, GUARD_TIMEOUT);
+        break;
+      }
+      mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+      uint8_t* st = smem + s * STAGE_BYTES;
+      const int kk = k * BK;
+      tma_4d(st, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
+      tma_2d(st + A_BYTES, &tmXh, kk, n0, &full[s]);
+      tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[s]);
+    }
+    // copies still in flight must land before the CTA ends: wait for the
+    // last ones the MMA thread may not have consumed (bounded)
+    for (int j = max(0, k - STAGES); j < k; ++j) mbar_wait(&full[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u);
+  } else if (threadIdx.x == 32) {  // MMA issuer
+    for (int k = 0; k < nk; ++k) {
+      const int s = k % STAGES;
+      if (!mbar_wait(&full[s], static_cast<uint32_t>(k / STAGES) & 1u)) {
+        atomicOr(a.guard, GUARD_TIMEOUT);
+        break;
+      }
+      tc_after();
+      uint8_t* st = smem + s * STAGE_BYTES;
+#pragma unroll
+      for (int j = 0; j < BK / 16; ++j) {
+        const uint64_t ad = smem_desc(st + j * 32);
+        mma(tmem, ad, smem_desc(st + A_BYTES + j * 32), (k | j) != 0);
+        mma(tmem, ad, smem_desc(st + A_BYTES + B_BYTES + j * 32), 1u);
+      }
+      mma_commit(&empty[s]);
+    }
+    mma_commit(&done);
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(&done, 0);
+  tc_after();
+  if (ok && (__ldcg(a.guard) & GUARD_TIMEOUT) == 0u) {
+    const int row = m0 + warp * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int t = n0 + c + j;
+        const float acc = __uint_as_float(v[j]);
+        if (a.mode == TC_SWIGLU) {  // rows (2p, 2p+1) = (gate_p, up_p): adjacent lanes
+          const float up = __shfl_xor_sync(0xffffffffu, acc, 1);
+          if (!(lane & 1) && t < a.T && row < a.N) {
+            const float y = acc / (1.0f + expf(-acc)) * up;
+            __nv_bfloat16 hi, lo;
+            split_bf16(y, hi, lo);
+            a.out_hi[static_cast<size_t>(t) * a.ldo + (row >> 1)] = hi;
+            a.out_lo[static_cast<size_t>(t) * a.ldo + (row >> 1)] = lo;
+          }
+        } else if (t < a.T && row < a.N) {
+          float* o = a.out + static_cast<size_t>(t) * a.ldo + row;
+          if (a.mode == TC_RESID) *o += acc;
+          else *o = acc;
+        }
+      }
+    }
+  } else if (threadIdx.x == 64 && !ok) {
+    atomicOr(a.guard, GUARD_TIMEOUT);
+  }
+  tc_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN) : "memory");
+}
+
+typedef CUresult (*EncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool tc_encode_weight(void* map, const void* packed, int N, int K) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  const int CT = (K + 255) / 256, npairs = (N + 1) / 2;
+  cuuint64_t dims[4] = {256, 2, static_cast<cuuint64_t>(CT), static_cast<cuuint64_t>(npairs)};
+  cuuint64_t strides[3] = {512, 1024, static_cast<cuuint64_t>(CT) * 1024};
+  cuuint32_t box[4] = {BK, 2, 1, BM / 2}, es[4] = {1, 1, 1, 1};
+  return enc(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(packed), dims,
+             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_encode_act(void* map, const void* buf, int rows, int K) {
+  EncodeTiled enc = encode_fn();
+  if (!enc || K % 8 != 0) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box[2] = {BK, BN}, es[2] = {1, 1};
+  return enc(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(buf), dims,
+             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t tc_gemm_init_attrs() {
+  return cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+}
+
+cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a,
+                           cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  dim3 grid((a.T + BN - 1) / BN, (2 * ((a.N + 1) / 2) + BM - 1) / BM);
+  tc_gemm_kernel<<<grid, 128, SMEM_BYTES, s>>>(*static_cast<const CUtensorMap*>(mapW),
+                                                *static_cast<const CUtensorMap*>(mapXh),
+                                                *static_cast<const CUtensorMap*>(mapXl), a);
+  return cudaGetLastError();
+}
+
+}  // namespace k2

@@ -144,6 +144,10 @@ k2_status k2_get_info(const k2_ctx* ctx, k2_info* info);
  * position's fp32 logits [vocab] are written there (kimi-k3-in-c k3_run.c:
  * `forward` returns last-position logits).  K2_ERR_CONTEXT_FULL if
  * length + n > max_context: the prompt is rejected, not truncated. */
+/* With bf16 weights (and option K2_OPT_TC_PREFILL) a prompt of 8 or more tokens is
+ * processed in blocks of up to 2048 tokens: the projections as tcgen05 tensor-core
+ * GEMMs (activations split into two bf16 halves, fp32 accumulation), causal
+ * attention over the cache, the residual stream in fp32. */
 k2_status k2_prefill(k2_ctx* ctx, int32_t seq, const int32_t* d_tokens, int32_t n, int32_t* d_next_token,
                      float* d_logits, void* stream);
 
@@ -197,9 +201,11 @@ typedef enum {
   K2_OPT_GRAPH = 1,       /* 1: k2_decode_step records a CUDA graph per (batch, buffers,
                              stream) on first use and replays it (stream must not be NULL) */
   K2_OPT_ATTN_SPLITS = 2, /* > 0: force the number of attention key splits of the kernel chain (tests) */
-  K2_OPT_PERSISTENT = 3   /* 1 (default): batch-1 tokens run as one persistent cooperative kernel
-                             (one CTA per SM, grid barriers between the phases of a layer) when the
+  K2_OPT_PERSISTENT = 3,  /* 1 (default): batch-1 tokens run as one persistent cooperative kernel
+                             (one CTA per SM, dataflow waits between the phases of a layer) when the
                              shape allows; 0: always the chain of per-step kernels */
+  K2_OPT_TC_PREFILL = 4   /* 1 (default): bf16 models prefill prompts of >= 8 tokens with tensor-core
+                             GEMMs over blocks of up to 2048 tokens; 0: one decode step per token */
 } k2_option;
 k2_status k2_set_option(k2_ctx* ctx, int32_t option, int64_t value);
 

@@ -1,0 +1,125 @@
+"""Tensor-core prefill (k2_prefill with bf16 weights) against the oracle and
+against the same library appending the prompt one decode step per token.
+
+Both GPU paths keep fp32 activations (the GEMM splits each activation into two
+bf16 halves), so they agree far more tightly than the bf16 parity bars; the
+oracle comparisons use the bars of tests/test_gpu_decode.py."""
+import numpy as np
+import pytest
+import torch
+
+import k2_inputs as ki
+from oracle import k2_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def k2():
+    from dense_gqa_decoder_gb300 import k2 as mod
+    return mod
+
+
+@pytest.fixture(scope="module")
+def mio():
+    from dense_gqa_decoder_gb300 import model_io
+    return model_io
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def prefill(k2, ctx, prompt, vocab, tc):
+    ctx.set_option(k2.K2_OPT_TC_PREFILL, 1 if tc else 0)
+    nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    logits = torch.empty(vocab, dtype=torch.float32, device="cuda")
+    ctx.prefill(0, torch.tensor(prompt, dtype=torch.int32, device="cuda"), nxt, logits)
+    torch.cuda.synchronize()
+    return int(nxt.item()), logits.cpu().numpy()
+
+
+def cache_rows(k2, ctx, s, kv, n):
+    """K and V rows 0..n-1 of every layer, dequantised, as float64."""
+    cap = ctx.info().kv_capacity
+    nkv, d = s.n_kv_heads, s.head_dim
+    out = []
+    for layer in range(s.n_layers):
+        kp, vp, ksp, vsp, _ = ctx.kv_view(layer, 0)
+        for ptr, sptr in ((kp, ksp), (vp, vsp)):
+            if kv == "i8":
+                codes = k2.device_view(ptr, nkv * cap * d, torch.int8).view(nkv, cap, d)[:, :n].float()
+                sc = k2.device_view(sptr, nkv * cap, torch.float16).view(nkv, cap)[:, :n].float()
+                out.append((codes * sc[..., None]).cpu().numpy())
+            else:
+                dt = torch.float16 if kv == "f16" else torch.float32
+                out.append(k2.device_view(ptr, nkv * cap * d, dt).view(nkv, cap, d)[:, :n].float().cpu().numpy())
+    return np.stack(out).astype(np.float64)
+
+
+@pytest.mark.parametrize("kv", ["f16", "i8", "f32"])
+def test_tc_prefill_matches_stepwise_and_oracle(k2, mio, kv):
+    s = ki.MEDIUM
+    n = 200  # two 128-token tiles, the second ragged
+    prompt = ki.prompt_ids(s.vocab, n, seed=31)
+    res = {}
+    for tc in (True, False):
+        ctx, host = mio.build_context(s, max_context=256, kv_dtype=kv, gain_scale=0.1, keep_host=True)
+        tok, lg = prefill(k2, ctx, prompt, s.vocab, tc)
+        hid = k2.device_view(ctx.hidden_view(0), s.hidden, torch.float32).cpu().numpy().copy()
+        res[tc] = (tok, lg, hid, cache_rows(k2, ctx, s, kv, n))
+        assert ctx.info().kv_capacity >= n
+        assert ctx.sync_status() == k2.K2_OK
+        if tc:
+            ref = O.OracleModel(s, lambda nm, l: host[(nm, l)], kv).forward_full(prompt)
+    (t1, l1, h1, c1), (t0, l0, h0, c0) = res[True], res[False]
+    assert t1 == t0 == O.argmax_first(ref)
+    assert rel_l2(l1, ref) <= (2e-4 if kv != "i8" else 5e-2)
+    # int8: the two paths' fp32 values (~1e-6 apart) pick different codes where
+    # a value sits on a rounding boundary; one code step is 1/127 of the row max
+    close = 1e-4 if kv != "i8" else 5e-3
+    assert rel_l2(l1, l0) <= close
+    assert rel_l2(h1, h0) <= close
+    if kv == "i8":
+        # codes may differ by one step where a value sits on a rounding boundary
+        assert rel_l2(c1, c0) <= 2e-2
+    elif kv == "f16":
+        # fp16 storage: values ~1e-6 apart round to neighbouring halves now and
+        # then; one ulp is 2^-11 relative, so even all of them flipping stays below
+        assert rel_l2(c1, c0) <= 2.0 ** -11
+    else:
+        assert rel_l2(c1, c0) <= 1e-5
+
+
+def test_tc_prefill_in_blocks_after_existing_rows(k2, mio):
+    """A second prompt appended to a non-empty cache, longer than one 2048-token
+    block, against the step-by-step path."""
+    s = ki.MEDIUM
+    first = ki.prompt_ids(s.vocab, 37, seed=41)
+    second = ki.prompt_ids(s.vocab, 2100, seed=42)
+    out = {}
+    for tc in (True, False):
+        ctx, _ = mio.build_context(s, max_context=2200, kv_dtype="f16", gain_scale=0.1)
+        prefill(k2, ctx, first, s.vocab, tc)
+        tok, lg = prefill(k2, ctx, second, s.vocab, tc)
+        out[tc] = (tok, lg)
+        assert ctx.kv_view(0, 0)[4] == len(first) + len(second)
+        assert ctx.sync_status() == k2.K2_OK
+    assert out[True][0] == out[False][0]
+    assert rel_l2(out[True][1], out[False][1]) <= 2e-4
+
+
+def test_tc_prefill_3p7b_layer_against_oracle(k2, mio):
+    """One decoder layer of the 3.7B shape: a 300-token prompt through the
+    tensor-core path against the oracle's full recompute."""
+    s = ki.K2_LAYER
+    n = 300
+    prompt = ki.prompt_ids(s.vocab, n, seed=51)
+    ctx, host = mio.build_context(s, max_context=512, kv_dtype="f16", keep_host=True)
+    tok, lg = prefill(k2, ctx, prompt, s.vocab, True)
+    ref = O.OracleModel(s, lambda nm, l: host[(nm, l)], "f16").forward_full(prompt)
+    assert rel_l2(lg, ref) <= 2e-4
+    assert tok == O.argmax_first(ref)
+    assert ctx.sync_status() == k2.K2_OK
