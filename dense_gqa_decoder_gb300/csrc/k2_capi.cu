@@ -41,7 +41,7 @@ struct Layout {
   size_t t_resid, t_qkv, t_attn, t_act, t_part;  // persistent step: (value, tag) activations
   // tensor-core prefill of up to `pchunk` tokens at a time (bf16 weights)
   int pchunk;
-  size_t px, pxh, pxl, pah, pal, pqkv, pq;
+  size_t px, pxh, pxl, pah, pal, pqkv, pq, plog;
   size_t wqkv, wo, wgu, wdown, wlm;  // packed weights; per-layer strides below
   size_t wqkv_layer, wo_layer, wgu_layer, wdown_layer;
   size_t kc, vc, ks, vs;  // first layer; per-layer stride kv_layer / sc_layer
@@ -108,6 +108,7 @@ Layout layout_of(const k2_config& c) {
     l.pal = take(P * s.I * 2);
     l.pqkv = take(P * s.qkv_n * 4);
     l.pq = take(P * s.nq * s.d * 4);
+    l.plog = take(P > 0 ? static_cast<size_t>(s.B) * s.V * 4 : 0);  // batched-decode logits
   }
   const size_t scratch_end = o;
   l.wqkv_layer = align_up(packed_bytes(s.qkv_n, s.H, s.wb), kAlign);
@@ -201,9 +202,10 @@ struct k2_ctx {
   // tensor-core prefill: TMA tensor maps (weights per layer: qkv, o, gate/up,
   // down; activations: normed input, attention output, SwiGLU output, hi/lo)
   bool tc_ok = false;
-  bool use_tc = true;
+  bool use_tc = true;        // prefill
+  bool use_tc_decode = true; // batched decode (batch >= 2)
   std::vector<std::array<uint8_t, kTcMapBytes>> tmw;  // 4 per layer
-  std::array<uint8_t, kTcMapBytes> tm_xh{}, tm_xl{}, tm_oh{}, tm_ol{}, tm_ah{}, tm_al{};
+  std::array<uint8_t, kTcMapBytes> tm_xh{}, tm_xl{}, tm_oh{}, tm_ol{}, tm_ah{}, tm_al{}, tm_lm{};
   std::map<std::tuple<int, const void*, const void*, const void*, void*>, cudaGraphExec_t> graphs;
   std::string err;
   // profiling: event pairs around the kernels of one step
@@ -375,7 +377,13 @@ void enqueue_token(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in
   }
 }
 
+cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int B, int* d_next, float* d_logits);
+
 void enqueue_decode(k2_ctx* c, Launcher& ln, const int* d_tokens, int batch, int* d_next, float* d_logits) {
+  if (batch >= 2 && c->tc_ok && c->use_tc_decode && batch <= c->lay.pchunk) {
+    ln.run(K2_K_STEP, [&] { return decode_batched(c, ln.s, d_tokens, batch, d_next, d_logits); });
+    return;
+  }
   for (int b = 0; b < batch; ++b)
     enqueue_token(c, ln, b, d_tokens + b, nullptr, d_next + b,
                   d_logits ? d_logits + static_cast<size_t>(b) * c->s.V : nullptr, true);
@@ -565,7 +573,8 @@ cudaError_t plan_tc_prefill(k2_ctx* c) {
       !tc_encode_act(c->tm_oh.data(), c->ws + c->lay.pxh, P, s.nq * s.d) ||
       !tc_encode_act(c->tm_ol.data(), c->ws + c->lay.pxl, P, s.nq * s.d) ||
       !tc_encode_act(c->tm_ah.data(), c->ws + c->lay.pah, P, s.I) ||
-      !tc_encode_act(c->tm_al.data(), c->ws + c->lay.pal, P, s.I))
+      !tc_encode_act(c->tm_al.data(), c->ws + c->lay.pal, P, s.I) ||
+      !tc_encode_weight(c->tm_lm.data(), c->wlm(), s.V, s.H))
     return cudaSuccess;
   c->tc_ok = true;
   return cudaSuccess;
@@ -595,6 +604,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.ksteps = 4 * ((K + 255) / 256);
     g.mode = mode;
     g.ldo = ldo;
+    g.splits = 1;
     g.out = out;
     g.out_hi = oh;
     g.out_lo = ol;
@@ -620,6 +630,82 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     if (!e) e = gemm(c->tmw[4 * l + 3].data(), c->tm_ah.data(), c->tm_al.data(), s.H, s.I, TC_RESID, X, nullptr,
                      nullptr, s.H);
   }
+  return e;
+}
+
+// K steps per CTA of a split-K GEMM: enough CTAs to cover the SMs twice,
+// at least 4 K steps each
+int tc_splits(const k2_ctx* c, int N, int K) {
+  const int tiles = (2 * ((N + 1) / 2) + 127) / 128;
+  const int ksteps = 4 * ((K + 255) / 256);
+  int sp = (2 * c->sms + tiles - 1) / tiles;
+  sp = std::min(sp, ksteps / 4);
+  return std::max(sp, 1);
+}
+
+// Decode of tokens d_tokens[0..B) of sequences 0..B-1 (B >= 2) with the
+// weights read once for all of them: tensor-core GEMMs with N = B tokens
+// (split-K where a GEMM has few row tiles), the batched attention kernel, and
+// a row-wise argmax.  Leaves each sequence's residual in its hidden view.
+cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int B, int* d_next, float* d_logits) {
+  const Sizes& s = c->s;
+  float* X = reinterpret_cast<float*>(c->ws + c->lay.px);
+  auto* xh = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxh);
+  auto* xl = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxl);
+  auto* ah = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pah);
+  auto* al = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pal);
+  float* qkvp = reinterpret_cast<float*>(c->ws + c->lay.pqkv);
+  float* logits = d_logits ? d_logits : reinterpret_cast<float*>(c->ws + c->lay.plog);
+  const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
+  auto gemm = [&](const void* mw, const void* mh, const void* ml, int N, int K, int mode, float* out,
+                  __nv_bfloat16* oh, __nv_bfloat16* ol, int ldo, int splits) {
+    TcGemmArgs g = {};
+    g.N = N;
+    g.K = K;
+    g.T = B;
+    g.ksteps = 4 * ((K + 255) / 256);
+    g.mode = mode;
+    g.ldo = ldo;
+    g.splits = splits;
+    g.out = out;
+    g.out_hi = oh;
+    g.out_lo = ol;
+    g.guard = c->guard;
+    return launch_tc_gemm(mw, mh, ml, g, st);
+  };
+  const int sq = tc_splits(c, s.qkv_n, s.H), so = tc_splits(c, s.H, s.nq * s.d), sd = tc_splits(c, s.H, s.I);
+  const int asplits = attn_splits(c, B);
+  cudaError_t e = launch_embed_rows(d_tokens, B, c->embed, s.wb, X, s.H, s.V, c->guard, st);
+  for (int l = 0; l < s.L && !e; ++l) {
+    if (!e) e = launch_norm_rows(X, B, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
+    if (!e && sq > 1) e = cudaMemsetAsync(qkvp, 0, sizeof(float) * B * s.qkv_n, st);
+    if (!e) e = gemm(c->tmw[4 * l].data(), c->tm_xh.data(), c->tm_xl.data(), s.qkv_n, s.H, TC_STORE, qkvp, nullptr,
+                     nullptr, s.qkv_n, sq);
+    if (!e) e = launch_rope_batch(qkvp, c->qkv, c->rope, c->seq_len, B, s.nq, s.nkv, s.d, c->lay.cap, c->guard, st);
+    if (!e) {
+      AttnArgs at = c->p_attn;
+      at.kc = at.kc_w = c->kc(l);
+      at.vc = at.vc_w = c->vc(l);
+      at.ks = c->ks(l);
+      at.vs = c->vs(l);
+      at.seq0 = 0;
+      e = launch_attn(at, s.d, s.rep, kvdt, asplits, B, st, false);
+    }
+    if (!e) e = launch_rows_hilo(c->attn_out, xh, xl, B, s.nq * s.d, st);
+    if (!e) e = gemm(c->tmw[4 * l + 1].data(), c->tm_oh.data(), c->tm_ol.data(), s.H, s.nq * s.d, TC_RESID, X,
+                     nullptr, nullptr, s.H, so);
+    if (!e) e = launch_norm_rows(X, B, c->mlp_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
+    if (!e) e = gemm(c->tmw[4 * l + 2].data(), c->tm_xh.data(), c->tm_xl.data(), 2 * s.I, s.H, TC_SWIGLU, nullptr,
+                     ah, al, s.I, 1);
+    if (!e) e = gemm(c->tmw[4 * l + 3].data(), c->tm_ah.data(), c->tm_al.data(), s.H, s.I, TC_RESID, X, nullptr,
+                     nullptr, s.H, sd);
+  }
+  if (!e) e = cudaMemcpyAsync(c->resid, X, sizeof(float) * B * s.H, cudaMemcpyDeviceToDevice, st);
+  if (!e) e = launch_norm_rows(X, B, c->final_norm, s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
+  if (!e) e = gemm(c->tm_lm.data(), c->tm_xh.data(), c->tm_xl.data(), s.V, s.H, TC_STORE, logits, nullptr, nullptr,
+                   s.V, 1);
+  if (!e) e = launch_argmax_rows(logits, B, s.V, d_next, c->guard, st);
+  if (!e) e = launch_advance(c->seq_len, 0, B, st, false);
   return e;
 }
 
@@ -1002,6 +1088,7 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
     case K2_OPT_GRAPH: c->graph = value != 0; break;
     case K2_OPT_PERSISTENT: c->use_mega = value != 0; break;
     case K2_OPT_TC_PREFILL: c->use_tc = value != 0; break;
+    case K2_OPT_TC_DECODE: c->use_tc_decode = value != 0; break;
     case K2_OPT_ATTN_SPLITS:
       if (value < 0 || value > kAttnMaxCluster)
         return c->fail(K2_ERR_ARG, "splits %lld outside [0, %d]", (long long)value, kAttnMaxCluster);

@@ -266,6 +266,8 @@ struct TcGemmArgs {
   int mode;    // TC_STORE: out[t][row] = acc; TC_RESID: out[t][row] += acc;
                // TC_SWIGLU: rows (2p, 2p+1) -> silu(gate) * up -> out_hi/out_lo[t][p]
   int ldo;     // row stride of the output (elements)
+  int splits;  // split-K: blockIdx.z takes K steps [ksteps*z/splits, ksteps*(z+1)/splits) and
+               // adds its partial with atomicAdd (TC_STORE / TC_RESID only; 1 = no split)
   float* out;
   __nv_bfloat16* out_hi;
   __nv_bfloat16* out_lo;
@@ -290,6 +292,10 @@ cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, co
                                 const void* vs, __nv_bfloat16* oh, __nv_bfloat16* ol, int n, int nq, int nkv, int D,
                                 int pos0, size_t head_row0, int cap, float scale, cudaStream_t s);
 cudaError_t launch_advance_by(int* seq_len, int seq, int n, cudaStream_t s);
+cudaError_t launch_rope_batch(const float* packed, float* nat, const float2* rope, const int* seq_len, int B, int nq,
+                              int nkv, int D, int cap, unsigned* guard, cudaStream_t s);
+cudaError_t launch_rows_hilo(const float* x, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int K, cudaStream_t s);
+cudaError_t launch_argmax_rows(const float* logits, int rows, int V, int* next, unsigned* guard, cudaStream_t s);
 cudaError_t misc_init_attrs();
 
 }  // namespace k2

@@ -275,6 +275,95 @@ constexpr size_t attn_smem() {
 
 __global__ void advance_by_kernel(int* seq_len, int seq, int n) { seq_len[seq] += n; }
 
+// Batched decode: token b belongs to sequence b at position seq_len[b].  The
+// QKV GEMM output (rows of every head in the packed order (i, i + d/2)) becomes
+// q | k | v in natural order with split-half RoPE at each token's position.
+__global__ void rope_batch_kernel(const float* __restrict__ packed, float* __restrict__ nat,
+                                  const float2* __restrict__ rope, const int* __restrict__ seq_len, int nq, int nkv,
+                                  int D, int cap, unsigned* guard) {
+  const int b = blockIdx.x;
+  const int qkv_n = (nq + 2 * nkv) * D, half = D / 2;
+  int pos = seq_len[b];
+  if (pos < 0 || pos >= cap) {
+    if (threadIdx.x == 0) atomicOr(guard, GUARD_POS);
+    pos = 0;
+  }
+  const float* src = packed + static_cast<size_t>(b) * qkv_n;
+  float* dst = nat + static_cast<size_t>(b) * qkv_n;
+  for (int idx = threadIdx.x; idx < (nq + 2 * nkv) * half; idx += blockDim.x) {
+    const int h = idx / half, i = idx - h * half;
+    float a = src[h * D + 2 * i], c = src[h * D + 2 * i + 1];
+    if (h < nq + nkv) {
+      const float2 cs = rope[static_cast<size_t>(pos) * half + i];
+      const float ra = a * cs.x - c * cs.y, rc = c * cs.x + a * cs.y;
+      a = ra;
+      c = rc;
+    }
+    dst[h * D + i] = a;
+    dst[h * D + i + half] = c;
+  }
+}
+
+// fp32 rows -> bf16 (hi, lo) rows
+__global__ void rows_hilo_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ oh,
+                                 __nv_bfloat16* __restrict__ ol, int K) {
+  const size_t base = static_cast<size_t>(blockIdx.x) * K;
+  for (int i = threadIdx.x; i < K; i += blockDim.x) {
+    __nv_bfloat16 hi, lo;
+    split_bf16(x[base + i], hi, lo);
+    oh[base + i] = hi;
+    ol[base + i] = lo;
+  }
+}
+
+// first index of the maximum of each logits row (kimi-k3-in-c k3_run.c,
+// `argmax_`); a NaN sets the guard and token 0 is written
+__global__ void argmax_rows_kernel(const float* __restrict__ logits, int V, int* __restrict__ next, unsigned* guard) {
+  __shared__ float bv[32];
+  __shared__ int bi[32];
+  const float* row = logits + static_cast<size_t>(blockIdx.x) * V;
+  float v = -INFINITY;
+  int idx = 0x7fffffff;
+  bool nan = false;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    const float x = row[i];
+    if (x != x) nan = true;
+    else if (x > v) {  // increasing i: the first maximum of this thread's elements is kept
+      v = x;
+      idx = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (ov > v || (ov == v && oi < idx)) {
+      v = ov;
+      idx = oi;
+    }
+  }
+  if (__syncthreads_or(nan)) {
+    if (threadIdx.x == 0) {
+      atomicOr(guard, GUARD_NAN);
+      next[blockIdx.x] = 0;
+    }
+    return;
+  }
+  if ((threadIdx.x & 31) == 0) {
+    bv[threadIdx.x >> 5] = v;
+    bi[threadIdx.x >> 5] = idx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w)
+      if (bv[w] > v || (bv[w] == v && bi[w] < idx)) {
+        v = bv[w];
+        idx = bi[w];
+      }
+    next[blockIdx.x] = idx == 0x7fffffff ? 0 : idx;
+  }
+}
+
 #define K2_PREFILL_ATTN_SHAPES(X) X(128, 4) X(64, 4)
 
 }  // namespace
@@ -367,6 +456,22 @@ cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, co
   K2_PREFILL_ATTN_SHAPES(K2_PA_LAUNCH)
 #undef K2_PA_LAUNCH
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_rope_batch(const float* packed, float* nat, const float2* rope, const int* seq_len, int B, int nq,
+                              int nkv, int D, int cap, unsigned* guard, cudaStream_t s) {
+  rope_batch_kernel<<<B, 256, 0, s>>>(packed, nat, rope, seq_len, nq, nkv, D, cap, guard);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rows_hilo(const float* x, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int K, cudaStream_t s) {
+  rows_hilo_kernel<<<rows, 256, 0, s>>>(x, oh, ol, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_argmax_rows(const float* logits, int rows, int V, int* next, unsigned* guard, cudaStream_t s) {
+  argmax_rows_kernel<<<rows, 1024, 0, s>>>(logits, V, next, guard);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_advance_by(int* seq_len, int seq, int n, cudaStream_t s) {

@@ -113,7 +113,10 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
   __syncthreads();
   tc_after();
   const uint32_t tmem = tmem_slot;
-  const int nk = a.ksteps;
+  // this CTA's K steps (split-K over blockIdx.z)
+  const int kb = static_cast<int>((static_cast<long long>(a.ksteps) * blockIdx.z) / a.splits);
+  const int ke = static_cast<int>((static_cast<long long>(a.ksteps) * (blockIdx.z + 1)) / a.splits);
+  const int nk = ke - kb;
   if (threadIdx.x == 0) {  // TMA producer
     int k = 0;
     for (; k < nk; ++k) {
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
       }
       mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
       uint8_t* st = smem + s * STAGE_BYTES;
-      const int kk = k * BK;
+      const int kk = (kb + k) * BK;
       tma_4d(st, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
       tma_2d(st + A_BYTES, &tmXh, kk, n0, &full[s]);
       tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[s]);
@@ -149,12 +152,12 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
       }
       mma_commit(&empty[s]);
     }
-    mma_commit(&done);
+    mma_commit(&done);  // with no K step at all it completes at once
   }
   __syncwarp();
   const bool ok = mbar_wait(&done, 0);
   tc_after();
-  if (ok && (__ldcg(a.guard) & GUARD_TIMEOUT) == 0u) {
+  if (ok && nk > 0 && (__ldcg(a.guard) & GUARD_TIMEOUT) == 0u) {
     const int row = m0 + warp * 32 + lane;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
@@ -175,7 +178,8 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
           }
         } else if (t < a.T && row < a.N) {
           float* o = a.out + static_cast<size_t>(t) * a.ldo + row;
-          if (a.mode == TC_RESID) *o += acc;
+          if (a.splits > 1) atomicAdd(o, acc);  // partial sums of a split K (the STORE target is zeroed)
+          else if (a.mode == TC_RESID) *o += acc;
           else *o = acc;
         }
       }
@@ -238,7 +242,8 @@ cudaError_t tc_gemm_init_attrs() {
 cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a,
                            cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
-  dim3 grid((a.T + BN - 1) / BN, (2 * ((a.N + 1) / 2) + BM - 1) / BM);
+  if (a.splits < 1 || (a.splits > 1 && a.mode == TC_SWIGLU)) return cudaErrorInvalidValue;
+  dim3 grid((a.T + BN - 1) / BN, (2 * ((a.N + 1) / 2) + BM - 1) / BM, a.splits);
   tc_gemm_kernel<<<grid, 128, SMEM_BYTES, s>>>(*static_cast<const CUtensorMap*>(mapW),
                                                 *static_cast<const CUtensorMap*>(mapXh),
                                                 *static_cast<const CUtensorMap*>(mapXl), a);

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libk2.so")
 K2_OK, K2_ERR_ARG, K2_ERR_SHAPE, K2_ERR_UNSUPPORTED, K2_ERR_TOKEN_RANGE, K2_ERR_CONTEXT_FULL, \
     K2_ERR_WORKSPACE, K2_ERR_CUDA, K2_ERR_DEVICE_GUARD = range(9)
 K2_F32, K2_BF16, K2_F16, K2_I8 = range(4)
-K2_OPT_PDL, K2_OPT_GRAPH, K2_OPT_ATTN_SPLITS, K2_OPT_PERSISTENT, K2_OPT_TC_PREFILL = range(5)
+K2_OPT_PDL, K2_OPT_GRAPH, K2_OPT_ATTN_SPLITS, K2_OPT_PERSISTENT, K2_OPT_TC_PREFILL, K2_OPT_TC_DECODE = range(6)
 KERNEL_CLASSES = ("embed", "qkv", "attn", "o_proj", "gate_up", "down", "lm_head", "step")
 DTYPES = {"f32": K2_F32, "bf16": K2_BF16, "f16": K2_F16, "i8": K2_I8}
 

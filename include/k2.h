@@ -204,8 +204,10 @@ typedef enum {
   K2_OPT_PERSISTENT = 3,  /* 1 (default): batch-1 tokens run as one persistent cooperative kernel
                              (one CTA per SM, dataflow waits between the phases of a layer) when the
                              shape allows; 0: always the chain of per-step kernels */
-  K2_OPT_TC_PREFILL = 4   /* 1 (default): bf16 models prefill prompts of >= 8 tokens with tensor-core
+  K2_OPT_TC_PREFILL = 4,  /* 1 (default): bf16 models prefill prompts of >= 8 tokens with tensor-core
                              GEMMs over blocks of up to 2048 tokens; 0: one decode step per token */
+  K2_OPT_TC_DECODE = 5    /* 1 (default): a bf16 decode step of batch >= 2 reads the weights once for
+                             all sequences (tensor-core GEMMs, N = batch); 0: one token at a time */
 } k2_option;
 k2_status k2_set_option(k2_ctx* ctx, int32_t option, int64_t value);
 

@@ -123,3 +123,37 @@ def test_tc_prefill_3p7b_layer_against_oracle(k2, mio):
     assert rel_l2(lg, ref) <= 2e-4
     assert tok == O.argmax_first(ref)
     assert ctx.sync_status() == k2.K2_OK
+
+
+@pytest.mark.parametrize("kv", ["f16", "i8"])
+def test_batched_decode_matches_one_token_at_a_time_and_oracle(k2, mio, kv):
+    """Batch-4 decode (weights read once per step for all four sequences)
+    against the same steps taken one sequence at a time, and sequences 0 and 3
+    against the oracle teacher-forced."""
+    s = ki.MEDIUM
+    B, steps = 4, 10
+    prompts = [ki.prompt_ids(s.vocab, n, seed=60 + b) for b, n in enumerate((23, 40, 9, 71))]
+    runs = {}
+    for batched in (True, False):
+        ctx, host = mio.build_context(s, max_context=128, max_batch=B, kv_dtype=kv, gain_scale=0.1, keep_host=True)
+        ctx.set_option(k2.K2_OPT_TC_DECODE, 1 if batched else 0)
+        nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
+        logits = torch.empty(B * s.vocab, dtype=torch.float32, device="cuda")
+        for b, p in enumerate(prompts):
+            ctx.prefill(b, torch.tensor(p, dtype=torch.int32, device="cuda"), nxt[b:b + 1])
+        toks, lgs = [nxt.cpu().numpy().copy()], []
+        for _ in range(steps):
+            ctx.decode_step(nxt, B, nxt, logits)
+            toks.append(nxt.cpu().numpy().copy())
+            lgs.append(logits.view(B, s.vocab).cpu().numpy().copy())
+        assert ctx.sync_status() == k2.K2_OK
+        runs[batched] = (np.stack(toks), np.stack(lgs))
+    (t1, l1), (t0, l0) = runs[True], runs[False]
+    assert np.array_equal(t1, t0)
+    assert rel_l2(l1, l0) <= (1e-4 if kv == "f16" else 5e-3)
+    model = O.OracleModel(s, lambda nm, l: host[(nm, l)], kv)
+    for b in (0, 3):
+        seq = np.concatenate([prompts[b], t1[:-1, b]])
+        am, ref, _ = model.teacher_forced(seq, len(prompts[b]))
+        assert rel_l2(l1[:, b], ref) <= (2e-4 if kv == "f16" else 5e-2)
+        assert np.mean(am == t1[1:, b]) >= (0.99 if kv == "f16" else 0.9)
