@@ -206,6 +206,8 @@ struct k2_ctx {
   bool use_tc_decode = true; // batched decode (batch >= 2)
   std::vector<std::array<uint8_t, kTcMapBytes>> tmw;  // 4 per layer
   std::array<uint8_t, kTcMapBytes> tm_xh{}, tm_xl{}, tm_oh{}, tm_ol{}, tm_ah{}, tm_al{}, tm_lm{};
+  // the same activation buffers in 16-token tiles (batched decode)
+  std::array<uint8_t, kTcMapBytes> tb_xh{}, tb_xl{}, tb_oh{}, tb_ol{}, tb_ah{}, tb_al{};
   std::map<std::tuple<int, const void*, const void*, const void*, void*>, cudaGraphExec_t> graphs;
   std::string err;
   // profiling: event pairs around the kernels of one step
@@ -380,7 +382,7 @@ void enqueue_token(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in
 cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int B, int* d_next, float* d_logits);
 
 void enqueue_decode(k2_ctx* c, Launcher& ln, const int* d_tokens, int batch, int* d_next, float* d_logits) {
-  if (batch >= 2 && c->tc_ok && c->use_tc_decode && batch <= c->lay.pchunk) {
+  if (batch >= 2 && batch <= 16 && c->tc_ok && c->use_tc_decode) {
     ln.run(K2_K_STEP, [&] { return decode_batched(c, ln.s, d_tokens, batch, d_next, d_logits); });
     return;
   }
@@ -568,12 +570,18 @@ cudaError_t plan_tc_prefill(k2_ctx* c) {
       return cudaSuccess;
   }
   const int P = c->lay.pchunk;
-  if (!tc_encode_act(c->tm_xh.data(), c->ws + c->lay.pxh, P, s.H) ||
-      !tc_encode_act(c->tm_xl.data(), c->ws + c->lay.pxl, P, s.H) ||
-      !tc_encode_act(c->tm_oh.data(), c->ws + c->lay.pxh, P, s.nq * s.d) ||
-      !tc_encode_act(c->tm_ol.data(), c->ws + c->lay.pxl, P, s.nq * s.d) ||
-      !tc_encode_act(c->tm_ah.data(), c->ws + c->lay.pah, P, s.I) ||
-      !tc_encode_act(c->tm_al.data(), c->ws + c->lay.pal, P, s.I) ||
+  bool ok = true;
+  for (int tt : {128, 16}) {
+    ok = ok && tc_encode_act((tt == 128 ? c->tm_xh : c->tb_xh).data(), c->ws + c->lay.pxh, P, s.H, tt) &&
+         tc_encode_act((tt == 128 ? c->tm_xl : c->tb_xl).data(), c->ws + c->lay.pxl, P, s.H, tt) &&
+         tc_encode_act((tt == 128 ? c->tm_oh : c->tb_oh).data(), c->ws + c->lay.pxh, P, s.nq * s.d, tt) &&
+         tc_encode_act((tt == 128 ? c->tm_ol : c->tb_ol).data(), c->ws + c->lay.pxl, P, s.nq * s.d, tt) &&
+         tc_encode_act((tt == 128 ? c->tm_ah : c->tb_ah).data(), c->ws + c->lay.pah, P, s.I, tt) &&
+         tc_encode_act((tt == 128 ? c->tm_al : c->tb_al).data(), c->ws + c->lay.pal, P, s.I, tt);
+  }
+  // the batched decode keeps the gate/up output of 16 tokens in the QKV buffer
+  if (16 * 2 * static_cast<size_t>(s.I) > static_cast<size_t>(P) * s.qkv_n) return cudaSuccess;
+  if (!ok ||
       !tc_encode_weight(c->tm_lm.data(), c->wlm(), s.V, s.H))
     return cudaSuccess;
   c->tc_ok = true;
@@ -604,6 +612,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.ksteps = 4 * ((K + 255) / 256);
     g.mode = mode;
     g.ldo = ldo;
+    g.tile_tokens = 128;
     g.splits = 1;
     g.out = out;
     g.out_hi = oh;
@@ -633,16 +642,6 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   return e;
 }
 
-// K steps per CTA of a split-K GEMM: enough CTAs to cover the SMs twice,
-// at least 4 K steps each
-int tc_splits(const k2_ctx* c, int N, int K) {
-  const int tiles = (2 * ((N + 1) / 2) + 127) / 128;
-  const int ksteps = 4 * ((K + 255) / 256);
-  int sp = (2 * c->sms + tiles - 1) / tiles;
-  sp = std::min(sp, ksteps / 4);
-  return std::max(sp, 1);
-}
-
 // Decode of tokens d_tokens[0..B) of sequences 0..B-1 (B >= 2) with the
 // weights read once for all of them: tensor-core GEMMs with N = B tokens
 // (split-K where a GEMM has few row tiles), the batched attention kernel, and
@@ -654,11 +653,12 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
   auto* xl = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxl);
   auto* ah = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pah);
   auto* al = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pal);
-  float* qkvp = reinterpret_cast<float*>(c->ws + c->lay.pqkv);
+  float* gout = reinterpret_cast<float*>(c->ws + c->lay.pqkv);  // QKV, then gate/up GEMM output
   float* logits = d_logits ? d_logits : reinterpret_cast<float*>(c->ws + c->lay.plog);
   const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
-  auto gemm = [&](const void* mw, const void* mh, const void* ml, int N, int K, int mode, float* out,
-                  __nv_bfloat16* oh, __nv_bfloat16* ol, int ldo, int splits) {
+  // stream-K GEMMs over 16-token tiles: one CTA per SM, fp32 atomic adds into
+  // `out` (zeroed first unless it is the residual stream)
+  auto gemm = [&](const void* mw, const void* mh, const void* ml, int N, int K, int mode, float* out, int ldo) {
     TcGemmArgs g = {};
     g.N = N;
     g.K = K;
@@ -666,22 +666,21 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
     g.ksteps = 4 * ((K + 255) / 256);
     g.mode = mode;
     g.ldo = ldo;
-    g.splits = splits;
+    g.tile_tokens = 16;
+    g.splits = 1;
     g.out = out;
-    g.out_hi = oh;
-    g.out_lo = ol;
     g.guard = c->guard;
-    return launch_tc_gemm(mw, mh, ml, g, st);
+    cudaError_t e = cudaSuccess;
+    if (mode == TC_STORE) e = cudaMemsetAsync(out, 0, sizeof(float) * static_cast<size_t>(B) * ldo, st);
+    if (!e) e = launch_tc_gemm_sk(mw, mh, ml, g, c->sms, st);
+    return e;
   };
-  const int sq = tc_splits(c, s.qkv_n, s.H), so = tc_splits(c, s.H, s.nq * s.d), sd = tc_splits(c, s.H, s.I);
   const int asplits = attn_splits(c, B);
   cudaError_t e = launch_embed_rows(d_tokens, B, c->embed, s.wb, X, s.H, s.V, c->guard, st);
   for (int l = 0; l < s.L && !e; ++l) {
     if (!e) e = launch_norm_rows(X, B, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
-    if (!e && sq > 1) e = cudaMemsetAsync(qkvp, 0, sizeof(float) * B * s.qkv_n, st);
-    if (!e) e = gemm(c->tmw[4 * l].data(), c->tm_xh.data(), c->tm_xl.data(), s.qkv_n, s.H, TC_STORE, qkvp, nullptr,
-                     nullptr, s.qkv_n, sq);
-    if (!e) e = launch_rope_batch(qkvp, c->qkv, c->rope, c->seq_len, B, s.nq, s.nkv, s.d, c->lay.cap, c->guard, st);
+    if (!e) e = gemm(c->tmw[4 * l].data(), c->tb_xh.data(), c->tb_xl.data(), s.qkv_n, s.H, TC_STORE, gout, s.qkv_n);
+    if (!e) e = launch_rope_batch(gout, c->qkv, c->rope, c->seq_len, B, s.nq, s.nkv, s.d, c->lay.cap, c->guard, st);
     if (!e) {
       AttnArgs at = c->p_attn;
       at.kc = at.kc_w = c->kc(l);
@@ -692,19 +691,17 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
       e = launch_attn(at, s.d, s.rep, kvdt, asplits, B, st, false);
     }
     if (!e) e = launch_rows_hilo(c->attn_out, xh, xl, B, s.nq * s.d, st);
-    if (!e) e = gemm(c->tmw[4 * l + 1].data(), c->tm_oh.data(), c->tm_ol.data(), s.H, s.nq * s.d, TC_RESID, X,
-                     nullptr, nullptr, s.H, so);
+    if (!e) e = gemm(c->tmw[4 * l + 1].data(), c->tb_oh.data(), c->tb_ol.data(), s.H, s.nq * s.d, TC_RESID, X, s.H);
     if (!e) e = launch_norm_rows(X, B, c->mlp_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
-    if (!e) e = gemm(c->tmw[4 * l + 2].data(), c->tm_xh.data(), c->tm_xl.data(), 2 * s.I, s.H, TC_SWIGLU, nullptr,
-                     ah, al, s.I, 1);
-    if (!e) e = gemm(c->tmw[4 * l + 3].data(), c->tm_ah.data(), c->tm_al.data(), s.H, s.I, TC_RESID, X, nullptr,
-                     nullptr, s.H, sd);
+    if (!e) e = gemm(c->tmw[4 * l + 2].data(), c->tb_xh.data(), c->tb_xl.data(), 2 * s.I, s.H, TC_STORE, gout,
+                     2 * s.I);
+    if (!e) e = launch_swiglu_rows(gout, ah, al, B, s.I, st);
+    if (!e) e = gemm(c->tmw[4 * l + 3].data(), c->tb_ah.data(), c->tb_al.data(), s.H, s.I, TC_RESID, X, s.H);
   }
   if (!e) e = cudaMemcpyAsync(c->resid, X, sizeof(float) * B * s.H, cudaMemcpyDeviceToDevice, st);
   if (!e) e = launch_norm_rows(X, B, c->final_norm, s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
-  if (!e) e = gemm(c->tm_lm.data(), c->tm_xh.data(), c->tm_xl.data(), s.V, s.H, TC_STORE, logits, nullptr, nullptr,
-                   s.V, 1);
-  if (!e) e = launch_argmax_rows(logits, B, s.V, d_next, c->guard, st);
+  if (!e) e = gemm(c->tm_lm.data(), c->tb_xh.data(), c->tb_xl.data(), s.V, s.H, TC_STORE, logits, s.V);
+  if (!e) e = launch_argmax_rows(logits, B, s.V, d_next, c->am_val, c->am_idx, kArgmaxPartsMax, c->guard, st);
   if (!e) e = launch_advance(c->seq_len, 0, B, st, false);
   return e;
 }

@@ -266,6 +266,7 @@ struct TcGemmArgs {
   int mode;    // TC_STORE: out[t][row] = acc; TC_RESID: out[t][row] += acc;
                // TC_SWIGLU: rows (2p, 2p+1) -> silu(gate) * up -> out_hi/out_lo[t][p]
   int ldo;     // row stride of the output (elements)
+  int tile_tokens;  // 128 (prefill) or 16 (batched decode): must match the activation maps
   int splits;  // split-K: blockIdx.z takes K steps [ksteps*z/splits, ksteps*(z+1)/splits) and
                // adds its partial with atomicAdd (TC_STORE / TC_RESID only; 1 = no split)
   float* out;
@@ -275,10 +276,13 @@ struct TcGemmArgs {
 };
 constexpr int kTcMapBytes = 128;  // one CUtensorMap
 bool tc_encode_weight(void* map, const void* packed, int N, int K);  // bf16 packed weights
-bool tc_encode_act(void* map, const void* buf, int rows, int K);     // bf16 [rows][K]
+bool tc_encode_act(void* map, const void* buf, int rows, int K, int tile_tokens);  // bf16 [rows][K]
 cudaError_t tc_gemm_init_attrs();
 cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a,
                            cudaStream_t s);
+// stream-K persistent variant (tile_tokens 16; TC_STORE into a zeroed target or TC_RESID), `ctas` CTAs
+cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a, int ctas,
+                              cudaStream_t s);
 bool prefill_attn_supported(int head_dim, int rep);
 cudaError_t prefill_init_attrs();
 cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbytes, float* X, int H, int vocab,
@@ -294,8 +298,10 @@ cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, co
 cudaError_t launch_advance_by(int* seq_len, int seq, int n, cudaStream_t s);
 cudaError_t launch_rope_batch(const float* packed, float* nat, const float2* rope, const int* seq_len, int B, int nq,
                               int nkv, int D, int cap, unsigned* guard, cudaStream_t s);
+cudaError_t launch_swiglu_rows(const float* gu, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int I, cudaStream_t s);
 cudaError_t launch_rows_hilo(const float* x, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int K, cudaStream_t s);
-cudaError_t launch_argmax_rows(const float* logits, int rows, int V, int* next, unsigned* guard, cudaStream_t s);
+cudaError_t launch_argmax_rows(const float* logits, int rows, int V, int* next, float* part_val, int* part_idx,
+                               int part_stride, unsigned* guard, cudaStream_t s);
 cudaError_t misc_init_attrs();
 
 }  // namespace k2

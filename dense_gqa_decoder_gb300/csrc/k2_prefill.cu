@@ -304,11 +304,25 @@ __global__ void rope_batch_kernel(const float* __restrict__ packed, float* __res
   }
 }
 
+// gate/up GEMM rows (2p, 2p+1) = (gate_p, up_p) -> silu(gate) * up as bf16 hi/lo
+__global__ void swiglu_rows_kernel(const float* __restrict__ gu, __nv_bfloat16* __restrict__ oh,
+                                   __nv_bfloat16* __restrict__ ol, int I) {
+  const float* r = gu + static_cast<size_t>(blockIdx.y) * 2 * I;
+  const size_t base = static_cast<size_t>(blockIdx.y) * I;
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < I; p += gridDim.x * blockDim.x) {
+    const float g = r[2 * p], u = r[2 * p + 1];
+    __nv_bfloat16 hi, lo;
+    split_bf16(g / (1.0f + expf(-g)) * u, hi, lo);
+    oh[base + p] = hi;
+    ol[base + p] = lo;
+  }
+}
+
 // fp32 rows -> bf16 (hi, lo) rows
 __global__ void rows_hilo_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ oh,
                                  __nv_bfloat16* __restrict__ ol, int K) {
-  const size_t base = static_cast<size_t>(blockIdx.x) * K;
-  for (int i = threadIdx.x; i < K; i += blockDim.x) {
+  const size_t base = static_cast<size_t>(blockIdx.y) * K;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < K; i += gridDim.x * blockDim.x) {
     __nv_bfloat16 hi, lo;
     split_bf16(x[base + i], hi, lo);
     oh[base + i] = hi;
@@ -317,52 +331,68 @@ __global__ void rows_hilo_kernel(const float* __restrict__ x, __nv_bfloat16* __r
 }
 
 // first index of the maximum of each logits row (kimi-k3-in-c k3_run.c,
-// `argmax_`); a NaN sets the guard and token 0 is written
-__global__ void argmax_rows_kernel(const float* __restrict__ logits, int V, int* __restrict__ next, unsigned* guard) {
-  __shared__ float bv[32];
-  __shared__ int bi[32];
-  const float* row = logits + static_cast<size_t>(blockIdx.x) * V;
+// `argmax_`), in two passes: kArgChunks partial maxima per row, then one per
+// row; a NaN sets the guard and token 0 is written
+constexpr int kArgChunks = 64;
+
+__device__ __forceinline__ void best_of(float& v, int& i, float ov, int oi) {
+  if (ov > v || (ov == v && oi < i)) {
+    v = ov;
+    i = oi;
+  }
+}
+
+__device__ __forceinline__ void block_best(float& v, int& i, float* sv, int* si) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) best_of(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
+  if ((threadIdx.x & 31) == 0) {
+    sv[threadIdx.x >> 5] = v;
+    si[threadIdx.x >> 5] = i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) best_of(v, i, sv[w], si[w]);
+}
+
+__global__ void argmax_part_kernel(const float* __restrict__ logits, int V, float* __restrict__ pv,
+                                   int* __restrict__ pi, int stride, unsigned* guard) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const int row = blockIdx.y, chunk = blockIdx.x;
+  const int lo = static_cast<int>((static_cast<long long>(V) * chunk) / gridDim.x);
+  const int hi = static_cast<int>((static_cast<long long>(V) * (chunk + 1)) / gridDim.x);
+  const float* r = logits + static_cast<size_t>(row) * V;
   float v = -INFINITY;
   int idx = 0x7fffffff;
   bool nan = false;
-  for (int i = threadIdx.x; i < V; i += blockDim.x) {
-    const float x = row[i];
+  for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    const float x = r[i];
     if (x != x) nan = true;
-    else if (x > v) {  // increasing i: the first maximum of this thread's elements is kept
+    else if (x > v) {  // increasing i per thread: its first maximum is kept
       v = x;
       idx = i;
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-    if (ov > v || (ov == v && oi < idx)) {
-      v = ov;
-      idx = oi;
-    }
-  }
-  if (__syncthreads_or(nan)) {
-    if (threadIdx.x == 0) {
-      atomicOr(guard, GUARD_NAN);
-      next[blockIdx.x] = 0;
-    }
-    return;
-  }
-  if ((threadIdx.x & 31) == 0) {
-    bv[threadIdx.x >> 5] = v;
-    bi[threadIdx.x >> 5] = idx;
-  }
-  __syncthreads();
+  if (__syncthreads_or(nan) && threadIdx.x == 0) atomicOr(guard, GUARD_NAN);
+  block_best(v, idx, sv, si);
   if (threadIdx.x == 0) {
-    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w)
-      if (bv[w] > v || (bv[w] == v && bi[w] < idx)) {
-        v = bv[w];
-        idx = bi[w];
-      }
-    next[blockIdx.x] = idx == 0x7fffffff ? 0 : idx;
+    pv[static_cast<size_t>(row) * stride + chunk] = v;
+    pi[static_cast<size_t>(row) * stride + chunk] = idx;
   }
 }
+
+__global__ void argmax_final_kernel(const float* __restrict__ pv, const int* __restrict__ pi, int chunks, int stride,
+                                    int* __restrict__ next) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  float v = -INFINITY;
+  int idx = 0x7fffffff;
+  for (int c = threadIdx.x; c < chunks; c += blockDim.x)
+    best_of(v, idx, pv[static_cast<size_t>(blockIdx.x) * stride + c], pi[static_cast<size_t>(blockIdx.x) * stride + c]);
+  block_best(v, idx, sv, si);
+  if (threadIdx.x == 0) next[blockIdx.x] = idx == 0x7fffffff ? 0 : idx;
+}
+
 
 #define K2_PREFILL_ATTN_SHAPES(X) X(128, 4) X(64, 4)
 
@@ -403,9 +433,9 @@ cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbyte
 cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes, __nv_bfloat16* oh,
                              __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s) {
   if (wbytes == 2)
-    norm_rows_kernel<<<n, 256, 0, s>>>(X, static_cast<const __nv_bfloat16*>(gain), oh, ol, H, groups, eps);
+    norm_rows_kernel<<<n, 512, 0, s>>>(X, static_cast<const __nv_bfloat16*>(gain), oh, ol, H, groups, eps);
   else
-    norm_rows_kernel<<<n, 256, 0, s>>>(X, static_cast<const float*>(gain), oh, ol, H, groups, eps);
+    norm_rows_kernel<<<n, 512, 0, s>>>(X, static_cast<const float*>(gain), oh, ol, H, groups, eps);
   return cudaGetLastError();
 }
 
@@ -460,17 +490,27 @@ cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, co
 
 cudaError_t launch_rope_batch(const float* packed, float* nat, const float2* rope, const int* seq_len, int B, int nq,
                               int nkv, int D, int cap, unsigned* guard, cudaStream_t s) {
-  rope_batch_kernel<<<B, 256, 0, s>>>(packed, nat, rope, seq_len, nq, nkv, D, cap, guard);
+  rope_batch_kernel<<<B, 1024, 0, s>>>(packed, nat, rope, seq_len, nq, nkv, D, cap, guard);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_rows(const float* gu, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int I, cudaStream_t s) {
+  swiglu_rows_kernel<<<dim3((I + 255) / 256, rows), 256, 0, s>>>(gu, oh, ol, I);
   return cudaGetLastError();
 }
 
 cudaError_t launch_rows_hilo(const float* x, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int K, cudaStream_t s) {
-  rows_hilo_kernel<<<rows, 256, 0, s>>>(x, oh, ol, K);
+  rows_hilo_kernel<<<dim3((K + 255) / 256, rows), 256, 0, s>>>(x, oh, ol, K);
   return cudaGetLastError();
 }
 
-cudaError_t launch_argmax_rows(const float* logits, int rows, int V, int* next, unsigned* guard, cudaStream_t s) {
-  argmax_rows_kernel<<<rows, 1024, 0, s>>>(logits, V, next, guard);
+cudaError_t launch_argmax_rows(const float* logits, int rows, int V, int* next, float* part_val, int* part_idx,
+                               int part_stride, unsigned* guard, cudaStream_t s) {
+  if (part_stride < kArgChunks) return cudaErrorInvalidValue;
+  argmax_part_kernel<<<dim3(kArgChunks, rows), 256, 0, s>>>(logits, V, part_val, part_idx, part_stride, guard);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  argmax_final_kernel<<<rows, 64, 0, s>>>(part_val, part_idx, kArgChunks, part_stride, next);
   return cudaGetLastError();
 }
 

@@ -20,6 +20,8 @@
 // wait is bounded; a timeout sets the guard word and skips the accumulator.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "k2_kernels.h"
 #include "k2_common.cuh"
 
@@ -27,9 +29,20 @@ namespace k2 {
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + 2 * B_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment of the ring to 1024 B
+constexpr int BM = 128, BK = 64;
+// tile shapes: 128 tokens for prefill, 16 for a batched decode step
+template <int BN_>
+struct Tile {
+  static constexpr int BN = BN_;
+  static constexpr int STAGES = BN_ >= 128 ? 4 : 8;
+  static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + 2 * B_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment of the ring to 1024 B
+  static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;             // allocation: a power of two >= 32
+  // instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major
+  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                    (static_cast<uint32_t>(BM >> 4) << 24);
+  static_assert(STAGE_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+};
 
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* m, int c0, int c1, uint64_t* bar) {
   asm volatile(
@@ -51,14 +64,11 @@ __device__ __forceinline__ uint64_t smem_desc(const void* p) {
   const uint64_t addr = (smem_u32(p) & 0x3FFFFu) >> 4;
   return addr | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
 }
-// instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
-__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -78,15 +88,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 
 __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(v);
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
+template <int BN_>
 __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                          const __grid_constant__ CUtensorMap tmXh,
                                                          const __grid_constant__ CUtensorMap tmXl, const TcGemmArgs a) {
+  using C = Tile<BN_>;
+  constexpr int BN = C::BN, STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -105,7 +127,7 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
-                 "r"(BN)
+                 "r"(C::TMEM_COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -147,8 +169,8 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
 #pragma unroll
       for (int j = 0; j < BK / 16; ++j) {
         const uint64_t ad = smem_desc(st + j * 32);
-        mma(tmem, ad, smem_desc(st + A_BYTES + j * 32), (k | j) != 0);
-        mma(tmem, ad, smem_desc(st + A_BYTES + B_BYTES + j * 32), 1u);
+        mma(tmem, ad, smem_desc(st + A_BYTES + j * 32), C::IDESC, (k | j) != 0);
+        mma(tmem, ad, smem_desc(st + A_BYTES + B_BYTES + j * 32), C::IDESC, 1u);
       }
       mma_commit(&empty[s]);
     }
@@ -159,12 +181,14 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
   tc_after();
   if (ok && nk > 0 && (__ldcg(a.guard) & GUARD_TIMEOUT) == 0u) {
     const int row = m0 + warp * 32 + lane;
+    constexpr int CW = BN < 32 ? BN : 32;  // accumulator columns read per tcgen05.ld
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+    for (int c = 0; c < BN; c += CW) {
+      uint32_t v[CW];
+      if constexpr (CW == 32) tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+      else tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < CW; ++j) {
         const int t = n0 + c + j;
         const float acc = __uint_as_float(v[j]);
         if (a.mode == TC_SWIGLU) {  // rows (2p, 2p+1) = (gate_p, up_p): adjacent lanes
@@ -190,7 +214,149 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
   tc_before();
   __syncthreads();
   if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+}
+
+// Stream-K variant for small token counts (batched decode): one persistent
+// CTA per SM takes an equal share of all (row tile, K step) pairs, so every SM
+// streams the same number of weight bytes; a tile cut by a share boundary is
+// finished with fp32 atomicAdd from both sides.  Warp 0 loads, warp 1 issues
+// the MMAs into one of two TMEM accumulators, warps 2-5 drain the other (warp
+// w reads TMEM lanes 32 (w % 4) ..), so accumulation and write-back overlap.
+// Output: atomicAdd into out (TC_RESID adds to the residual; TC_STORE expects
+// a zeroed target).
+template <int BN_>
+__global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                            const __grid_constant__ CUtensorMap tmXh,
+                                                            const __grid_constant__ CUtensorMap tmXl,
+                                                            const TcGemmArgs a) {
+  using C = Tile<BN_>;
+  constexpr int BN = C::BN, STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES, COLS = C::TMEM_COLS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], accf[2], acce[2];
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tok_tiles = (a.T + BN - 1) / BN;
+  const int row_tiles = (2 * ((a.N + 1) / 2) + BM - 1) / BM;
+  const int kpt = a.ksteps;
+  const long long total = static_cast<long long>(row_tiles) * tok_tiles * kpt;
+  const long long g0 = total * blockIdx.x / gridDim.x, g1 = total * (blockIdx.x + 1) / gridDim.x;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 4);  // one arrival per epilogue warp
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(2 * COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  const uint32_t tmem = tmem_slot;
+  if (threadIdx.x == 0) {  // TMA producer
+    long long g = g0;
+    int i = 0;
+    for (; g < g1; ++g, ++i) {
+      const int s = i % STAGES;
+      if (i >= STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>((i / STAGES) - 1) & 1u)) {
+        atomicOr(a.guard, GUARD_TIMEOUT);
+        break;
+      }
+      const long long tile = g / kpt;
+      const int k = static_cast<int>(g - tile * kpt);
+      const int m0 = static_cast<int>(tile / tok_tiles) * BM, n0 = static_cast<int>(tile % tok_tiles) * BN;
+      mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+      uint8_t* st = smem + s * STAGE_BYTES;
+      const int kk = k * BK;
+      tma_4d(st, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
+      tma_2d(st + A_BYTES, &tmXh, kk, n0, &full[s]);
+      tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[s]);
+    }
+    for (int j = max(0, i - STAGES); j < i; ++j) mbar_wait(&full[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u);
+  } else if (threadIdx.x == 32) {  // MMA issuer
+    int i = 0, piece = 0;
+    bool first = true;
+    for (long long g = g0; g < g1; ++g, ++i) {
+      const long long tile = g / kpt;
+      const int k = static_cast<int>(g - tile * kpt);
+      const int b = piece & 1;
+      if (first && piece >= 2 && !mbar_wait(&acce[b], static_cast<uint32_t>((piece >> 1) - 1) & 1u)) {
+        atomicOr(a.guard, GUARD_TIMEOUT);
+        break;
+      }
+      const int s = i % STAGES;
+      if (!mbar_wait(&full[s], static_cast<uint32_t>(i / STAGES) & 1u)) {
+        atomicOr(a.guard, GUARD_TIMEOUT);
+        break;
+      }
+      tc_after();
+      uint8_t* st = smem + s * STAGE_BYTES;
+      const uint32_t acc = tmem + b * COLS;
+#pragma unroll
+      for (int j = 0; j < BK / 16; ++j) {
+        const uint64_t ad = smem_desc(st + j * 32);
+        mma(acc, ad, smem_desc(st + A_BYTES + j * 32), C::IDESC, (!first || j != 0) ? 1u : 0u);
+        mma(acc, ad, smem_desc(st + A_BYTES + B_BYTES + j * 32), C::IDESC, 1u);
+      }
+      mma_commit(&empty[s]);
+      first = false;
+      if (k == kpt - 1 || g == g1 - 1) {  // this CTA's piece of the tile ends
+        mma_commit(&accf[b]);
+        ++piece;
+        first = true;
+      }
+    }
+  } else if (warp >= 2) {  // epilogue: drain each piece's accumulator
+    const int lg = (warp & 3) * 32;  // the TMEM lanes (tile rows) this warp may read
+    int piece = 0;
+    long long g = g0;
+    while (g < g1) {
+      const long long tile = g / kpt;
+      const long long end = min(g1, (tile + 1) * kpt);
+      const int b = piece & 1;
+      const bool ok = mbar_wait(&accf[b], static_cast<uint32_t>(piece >> 1) & 1u);
+      if (__any_sync(0xffffffffu, !ok)) {
+        if (lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
+        break;
+      }
+      tc_after();
+      uint32_t v[BN];
+      if constexpr (BN == 16) {
+        tmem_ld16(tmem + b * COLS + (static_cast<uint32_t>(lg) << 16), v);
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN; c += 32) tmem_ld32(tmem + b * COLS + (static_cast<uint32_t>(lg) << 16) + c, v + c);
+      }
+      tc_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[b]);
+      const int row = static_cast<int>(tile / tok_tiles) * BM + lg + lane;
+      const int n0 = static_cast<int>(tile % tok_tiles) * BN;
+      if (row < a.N) {
+#pragma unroll
+        for (int j = 0; j < BN; ++j)
+          if (n0 + j < a.T) atomicAdd(a.out + static_cast<size_t>(n0 + j) * a.ldo + row, __uint_as_float(v[j]));
+      }
+      g = end;
+      ++piece;
+    }
+  }
+  tc_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * COLS) : "memory");
 }
 
 typedef CUresult (*EncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -224,29 +390,54 @@ bool tc_encode_weight(void* map, const void* packed, int N, int K) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool tc_encode_act(void* map, const void* buf, int rows, int K) {
+bool tc_encode_act(void* map, const void* buf, int rows, int K, int tile_tokens) {
   EncodeTiled enc = encode_fn();
-  if (!enc || K % 8 != 0) return false;
+  if (!enc || K % 8 != 0 || (tile_tokens != 16 && tile_tokens != 128)) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  cuuint32_t box[2] = {BK, BN}, es[2] = {1, 1};
+  cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(tile_tokens)}, es[2] = {1, 1};
   return enc(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(buf), dims,
              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t tc_gemm_init_attrs() {
-  return cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Tile<128>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc_gemm_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<16>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tc_gemm_sk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Tile<16>::SMEM_BYTES);
+}
+
+cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a, int ctas,
+                              cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  if (a.tile_tokens != 16 || a.mode == TC_SWIGLU || ctas < 1) return cudaErrorInvalidValue;
+  const long long total = static_cast<long long>((2 * ((a.N + 1) / 2) + BM - 1) / BM) * ((a.T + 15) / 16) * a.ksteps;
+  const int grid = static_cast<int>(std::min<long long>(ctas, total));
+  tc_gemm_sk_kernel<16><<<grid, 192, Tile<16>::SMEM_BYTES, s>>>(*static_cast<const CUtensorMap*>(mapW),
+                                                               *static_cast<const CUtensorMap*>(mapXh),
+                                                               *static_cast<const CUtensorMap*>(mapXl), a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a,
                            cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   if (a.splits < 1 || (a.splits > 1 && a.mode == TC_SWIGLU)) return cudaErrorInvalidValue;
-  dim3 grid((a.T + BN - 1) / BN, (2 * ((a.N + 1) / 2) + BM - 1) / BM, a.splits);
-  tc_gemm_kernel<<<grid, 128, SMEM_BYTES, s>>>(*static_cast<const CUtensorMap*>(mapW),
-                                                *static_cast<const CUtensorMap*>(mapXh),
-                                                *static_cast<const CUtensorMap*>(mapXl), a);
+  const CUtensorMap& w = *static_cast<const CUtensorMap*>(mapW);
+  const CUtensorMap& xh = *static_cast<const CUtensorMap*>(mapXh);
+  const CUtensorMap& xl = *static_cast<const CUtensorMap*>(mapXl);
+  const int rows = (2 * ((a.N + 1) / 2) + BM - 1) / BM;
+  if (a.tile_tokens == 16) {
+    tc_gemm_kernel<16><<<dim3((a.T + 15) / 16, rows, a.splits), 128, Tile<16>::SMEM_BYTES, s>>>(w, xh, xl, a);
+  } else if (a.tile_tokens == 128) {
+    tc_gemm_kernel<128><<<dim3((a.T + 127) / 128, rows, a.splits), 128, Tile<128>::SMEM_BYTES, s>>>(w, xh, xl, a);
+  } else {
+    return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
