@@ -45,6 +45,9 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=32)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--layers", type=int, default=0, help="override layer count (debug)")
+    p.add_argument("--batch", type=int, default=1,
+                   help="> 1: aggregate decode throughput of that many sequences per step (each prefilled "
+                        "with --ctx random tokens); the default 1 is the batch-1 metric")
     return p.parse_args()
 
 
@@ -431,11 +434,86 @@ def run_ours(args, world, rank, local, pg):
         print(json.dumps(line), flush=True)
 
 
+def run_batched(args, world, rank, local, pg):
+    """Batched decode: --batch sequences, each prefilled with --ctx random ids,
+    advanced together by one k2_decode_step per step (weights read once per
+    step for all of them)."""
+    import torch
+
+    import k2_inputs as ki
+    from dense_gqa_decoder_gb300 import k2
+
+    torch.cuda.set_device(local)
+    s = ki.SHAPES[SHAPE_NAME]
+    if args.layers:
+        s = s.replace(n_layers=args.layers)
+    B = args.batch
+    cfg = k2.make_config(s, max_context=args.ctx + args.warmup + args.steps + 16, max_batch=B, kv_dtype="f16")
+    ctx = k2.Context(cfg, random_device_weights(s, seed=1234 + rank))
+    stream = torch.cuda.Stream()
+    tok = torch.zeros(B, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        for b in range(B):
+            prompt = torch.from_numpy(ki.prompt_ids(s.vocab, args.ctx, seed=1 + b + 100 * rank)).cuda()
+            ctx.prefill(b, prompt, tok[b:b + 1], stream=stream)
+    ctx.set_option(k2.K2_OPT_GRAPH, 1)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            ctx.decode_step(tok, B, tok, stream=stream)
+    stream.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        ctx.decode_step(tok, B, tok, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    if ctx.sync_status(stream) != k2.K2_OK:
+        raise RuntimeError("device guard after the timed steps: " + ctx.last_error())
+    ms_per_step = ms / args.steps
+    mean_ctx = args.ctx + args.warmup + (args.steps - 1) / 2 + 1
+    by = algorithmic_bytes(s, 1)
+    step_bytes = by["weights"] + B * (by["kv"] * mean_ctx)  # kv of one position x mean length, per sequence
+    peak, peak_src = measured_peaks()
+    achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": f"batch-{B} decode aggregate tok/s (3.7B dense GQA, bf16) and achieved HBM GB/s vs peak",
+        "value": world * B * args.steps / (ms / 1e3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"k2-horizon-3.7b-shape greedy decode, {B} sequences, context {args.ctx}, fp16 KV",
+                   "batch": B, "context": args.ctx, "layers": s.n_layers, "cuda_graph": True,
+                   "l2": "no flush: every step streams 8.8 GB of weights", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "decode_batched step (tensor-core GEMMs N = batch, attention, "
+                                               "row kernels)", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
+                     "algorithmic_bytes": step_bytes},
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local, pg = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank, pg)
+    elif args.batch > 1:
+        run_batched(args, world, rank, local, pg)
     else:
         run_ours(args, world, rank, local, pg)
     if pg:
