@@ -45,6 +45,7 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=32)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--layers", type=int, default=0, help="override layer count (debug)")
+    p.add_argument("--kv", default="f16", choices=["f16", "i8"], help="KV cache storage")
     p.add_argument("--batch", type=int, default=1,
                    help="> 1: aggregate decode throughput of that many sequences per step (each prefilled "
                         "with --ctx random tokens); the default 1 is the batch-1 metric")
@@ -55,7 +56,7 @@ def parse():
 # helpers
 # ---------------------------------------------------------------------------
 
-def algorithmic_bytes(s, ctx_len: int) -> dict:
+def algorithmic_bytes(s, ctx_len: int, kv: str = "f16") -> dict:
     """Bytes the decode step must move at context ctx_len (weights once, the
     KV history once, plus the small activations)."""
     H, d, I, V = s.hidden, s.head_dim, s.intermediate, s.vocab
@@ -63,7 +64,8 @@ def algorithmic_bytes(s, ctx_len: int) -> dict:
     wb = 2 if s.weight_dtype == "bf16" else 4
     per_layer = (qkv_n * H + H * s.n_heads * d + 2 * I * H + H * I + 2 * H) * wb
     weights = s.n_layers * per_layer + V * H * wb + H * wb
-    kv_row = 2 * s.n_kv_heads * d * 2  # fp16 K and V of one position, one layer
+    # K and V of one position, one layer: fp16, or int8 codes + one fp16 scale per head
+    kv_row = 2 * s.n_kv_heads * d * 2 if kv == "f16" else 2 * s.n_kv_heads * (d + 2)
     kv = s.n_layers * kv_row * ctx_len
     return {
         "weights": weights,
@@ -297,7 +299,7 @@ def run_ours(args, world, rank, local, pg):
     if args.layers:
         s = s.replace(n_layers=args.layers)
     budget = args.ctx + args.warmup + args.steps + args.profile_steps + args.e2e_steps + 16
-    cfg = k2.make_config(s, max_context=budget, max_batch=1, kv_dtype="f16")
+    cfg = k2.make_config(s, max_context=budget, max_batch=1, kv_dtype=args.kv)
     ctx = k2.Context(cfg, random_device_weights(s, seed=1234 + rank))
     stream = torch.cuda.Stream()
     tok = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -349,7 +351,7 @@ def run_ours(args, world, rank, local, pg):
     ms_per_step = ms / args.steps
     value = world * args.steps / (ms / 1e3)
     mean_ctx = ctx_start + (args.steps - 1) / 2 + 1
-    by = algorithmic_bytes(s, int(round(mean_ctx)))
+    by = algorithmic_bytes(s, int(round(mean_ctx)), args.kv)
 
     # per-kernel durations: one un-graphed step with an event pair per kernel
     ms_k = {k: 0.0 for k in k2.KERNEL_CLASSES}
@@ -407,8 +409,10 @@ def run_ours(args, world, rank, local, pg):
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": 1, "context": args.ctx, "layers": s.n_layers,
-                   "kv_dtype": "f16", "activations": "fp32", "cuda_graph": True,
+        "config": {"workload": WORKLOAD if (args.kv == "f16" and args.ctx == CTX) else
+                   f"k2-horizon-3.7b-shape greedy decode, batch 1, context {args.ctx}, {args.kv} KV, bf16 weights",
+                   "batch": 1, "context": args.ctx, "layers": s.n_layers,
+                   "kv_dtype": args.kv, "activations": "fp32", "cuda_graph": True,
                    "persistent_kernel": persistent, "pdl": not persistent,
                    "l2": "no flush: every step streams 8.8 GB of weights, far above the 129 MB L2",
                    "parallelism": f"replicas x{world}"},
@@ -448,7 +452,7 @@ def run_batched(args, world, rank, local, pg):
     if args.layers:
         s = s.replace(n_layers=args.layers)
     B = args.batch
-    cfg = k2.make_config(s, max_context=args.ctx + args.warmup + args.steps + 16, max_batch=B, kv_dtype="f16")
+    cfg = k2.make_config(s, max_context=args.ctx + args.warmup + args.steps + 16, max_batch=B, kv_dtype=args.kv)
     ctx = k2.Context(cfg, random_device_weights(s, seed=1234 + rank))
     stream = torch.cuda.Stream()
     tok = torch.zeros(B, dtype=torch.int32, device="cuda")
@@ -485,7 +489,7 @@ def run_batched(args, world, rank, local, pg):
         raise RuntimeError("device guard after the timed steps: " + ctx.last_error())
     ms_per_step = ms / args.steps
     mean_ctx = args.ctx + args.warmup + (args.steps - 1) / 2 + 1
-    by = algorithmic_bytes(s, 1)
+    by = algorithmic_bytes(s, 1, args.kv)
     step_bytes = by["weights"] + B * (by["kv"] * mean_ctx)  # kv of one position x mean length, per sequence
     peak, peak_src = measured_peaks()
     achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
@@ -494,7 +498,7 @@ def run_batched(args, world, rank, local, pg):
         "value": world * B * args.steps / (ms / 1e3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"k2-horizon-3.7b-shape greedy decode, {B} sequences, context {args.ctx}, fp16 KV",
+        "config": {"workload": f"k2-horizon-3.7b-shape greedy decode, {B} sequences, context {args.ctx}, {args.kv} KV",
                    "batch": B, "context": args.ctx, "layers": s.n_layers, "cuda_graph": True,
                    "l2": "no flush: every step streams 8.8 GB of weights", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "decode_batched step (tensor-core GEMMs N = batch, attention, "
