@@ -267,6 +267,240 @@ __global__ void __launch_bounds__(kPaThreads) prefill_attn_kernel(const float* _
   }
 }
 
+// The same causal attention on the tensor cores (mma.sync m16n8k16, fp16 in,
+// fp32 accumulate) for fp16 and int8 caches: a CTA of 4 warps takes 64 query
+// rows (64 / REP tokens x REP heads of one KV head), each warp 16 rows.  K/V
+// tiles of 64 keys sit in shared memory as fp16 (int8 codes are exact in fp16;
+// their scales multiply the scores' and probabilities' columns), with 16-byte
+// chunks XOR-swizzled by row so that ldmatrix reads are conflict-free.  The
+// query rows and the probabilities enter each MMA as two fp16 halves (hi + lo),
+// which keeps ~22 mantissa bits: the result matches fp32 CUDA-core arithmetic
+// to ~1e-6.  The score accumulators are reused as the probability fragments
+// of the P.V product (same register layout).
+constexpr int kMaRows = 64, kMaKT = 64, kMaThreads = 128;
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void split_half2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 f = __half22float2(h);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = pack_half2(a - f.x, b - f.y);
+}
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// byte offset of 16-byte chunk `c` of row `r` in a swizzled [rows][D] fp16 tile
+template <int D>
+__device__ __forceinline__ int swz(int r, int c) {
+  return r * (D * 2) + ((c ^ (r & 7)) << 4);
+}
+
+template <int D, int REP, typename KVT>
+__global__ void __launch_bounds__(kMaThreads) prefill_attn_mma_kernel(
+    const float* __restrict__ Q, const KVT* __restrict__ kc, const KVT* __restrict__ vc, const __half* __restrict__ ks,
+    const __half* __restrict__ vs, __nv_bfloat16* __restrict__ oh, __nv_bfloat16* __restrict__ ol, int n, int nq,
+    int pos0, size_t head_row0, int cap, float scale) {
+  constexpr bool I8 = std::is_same<KVT, int8_t>::value;
+  constexpr int QT = kMaRows / REP;  // tokens per CTA
+  constexpr int KS = D / 16;         // k-steps of Q.K
+  constexpr int NT = D / 8;          // n-tiles of P.V
+  constexpr int CH = D / 8;          // 16-byte chunks per fp16 row
+  __shared__ __align__(128) __half Ks[kMaKT * D];
+  __shared__ __align__(128) __half Vs[kMaKT * D];
+  __shared__ float ksc[kMaKT], vsc[kMaKT];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int t0 = blockIdx.x * QT, kvh = blockIdx.y;
+  const int nt = min(QT, n - t0);
+  const size_t hr = head_row0 + static_cast<size_t>(kvh) * cap;
+  // this thread's two query rows (r and r + 8 of the warp's 16)
+  const int r0 = warp * 16 + g, r1 = r0 + 8;
+  const int tq0 = r0 / REP, tq1 = r1 / REP;
+  const int qpos0 = pos0 + t0 + tq0, qpos1 = pos0 + t0 + tq1;
+  // query fragments (hi, lo): rows r0/r1, dims 16 kk + 2t (+1), + 8
+  uint32_t qh[KS][4], qlo[KS][4];
+  {
+    auto qv = [&](int r, int d) -> float {
+      const int tq = r / REP, h = r - tq * REP;
+      return tq < nt ? Q[static_cast<size_t>(t0 + tq) * nq * D + (kvh * REP + h) * D + d] * scale : 0.f;
+    };
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const int d0 = 16 * kk + 2 * t;
+      split_half2(qv(r0, d0), qv(r0, d0 + 1), qh[kk][0], qlo[kk][0]);
+      split_half2(qv(r1, d0), qv(r1, d0 + 1), qh[kk][1], qlo[kk][1]);
+      split_half2(qv(r0, d0 + 8), qv(r0, d0 + 9), qh[kk][2], qlo[kk][2]);
+      split_half2(qv(r1, d0 + 8), qv(r1, d0 + 9), qh[kk][3], qlo[kk][3]);
+    }
+  }
+  float o[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const uint32_t ks_base = smem_u32(Ks), vs_base = smem_u32(Vs);
+  const int kend = pos0 + t0 + nt;
+  for (int k0 = 0; k0 < kend; k0 += kMaKT) {
+    __syncthreads();  // the previous tile is consumed
+    for (int idx = tid; idx < kMaKT * CH; idx += kMaThreads) {
+      const int r = idx / CH, c = idx - r * CH, key = k0 + r;
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (key < kend) {
+        if constexpr (I8) {  // 8 codes -> 8 halves
+          const uint2 kq = *reinterpret_cast<const uint2*>(kc + (hr + key) * D + c * 8);
+          const uint2 vq = *reinterpret_cast<const uint2*>(vc + (hr + key) * D + c * 8);
+          auto cvt = [](uint2 q) {
+            uint32_t w[4];
+            const uint32_t x[2] = {q.x, q.y};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float a = static_cast<float>(static_cast<int8_t>((x[i >> 1] >> (16 * (i & 1))) & 0xFF));
+              const float b = static_cast<float>(static_cast<int8_t>((x[i >> 1] >> (16 * (i & 1) + 8)) & 0xFF));
+              w[i] = pack_half2(a, b);
+            }
+            return make_uint4(w[0], w[1], w[2], w[3]);
+          };
+          kv = cvt(kq);
+          vv = cvt(vq);
+        } else {
+          kv = *reinterpret_cast<const uint4*>(kc + (hr + key) * D + c * 8);
+          vv = *reinterpret_cast<const uint4*>(vc + (hr + key) * D + c * 8);
+        }
+      }
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(Ks) + swz<D>(r, c)) = kv;
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(Vs) + swz<D>(r, c)) = vv;
+    }
+    if (tid < kMaKT) {
+      const int key = k0 + tid;
+      ksc[tid] = I8 && key < kend ? __half2float(ks[hr + key]) : 1.f;
+      vsc[tid] = I8 && key < kend ? __half2float(vs[hr + key]) : 1.f;
+    }
+    __syncthreads();
+    // S = Q K^T over the 64 keys: 8 n-tiles of 8 keys
+    float sc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        const int m = lane >> 3, rr = lane & 7;
+        const int key = 8 * (j + (m >> 1)) + rr, chunk = 2 * kk + (m & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(ks_base + swz<D>(key, chunk), b0, b1, b2, b3);
+        mma16816(sc[j], qh[kk], b0, b1);
+        mma16816(sc[j], qlo[kk], b0, b1);
+        mma16816(sc[j + 1], qh[kk], b2, b3);
+        mma16816(sc[j + 1], qlo[kk], b2, b3);
+      }
+    }
+    // scales (int8), causal mask, online softmax of rows r0 (c0, c1) and r1 (c2, c3)
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int kl = 8 * j + 2 * t + e, key = k0 + kl;
+        const float ksf = I8 ? ksc[kl] : 1.f;
+        sc[j][e] = (key > qpos0 || tq0 >= nt) ? -INFINITY : sc[j][e] * ksf;
+        sc[j][2 + e] = (key > qpos1 || tq1 >= nt) ? -INFINITY : sc[j][2 + e] * ksf;
+        mx0 = fmaxf(mx0, sc[j][e]);
+        mx1 = fmaxf(mx1, sc[j][2 + e]);
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = mn0 == -INFINITY ? 1.f : expf(m0 - mn0), al1 = mn1 == -INFINITY ? 1.f : expf(m1 - mn1);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        sc[j][e] = sc[j][e] == -INFINITY ? 0.f : expf(sc[j][e] - mn0);
+        sc[j][2 + e] = sc[j][2 + e] == -INFINITY ? 0.f : expf(sc[j][2 + e] - mn1);
+        s0 += sc[j][e];
+        s1 += sc[j][2 + e];
+      }
+    }
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    l0 = l0 * al0 + s0;
+    l1 = l1 * al1 + s1;
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      o[j][0] *= al0;
+      o[j][1] *= al0;
+      o[j][2] *= al1;
+      o[j][3] *= al1;
+    }
+    // O += P V: k-steps of 16 keys (score n-tiles 2kk, 2kk+1), n-tiles of 8 dims
+#pragma unroll
+    for (int kk = 0; kk < kMaKT / 16; ++kk) {
+      uint32_t ph[4], pl[4];
+      {
+        const int ka = 16 * kk + 2 * t, kb = ka + 8;
+        const float va0 = I8 ? vsc[ka] : 1.f, va1 = I8 ? vsc[ka + 1] : 1.f;
+        const float vb0 = I8 ? vsc[kb] : 1.f, vb1 = I8 ? vsc[kb + 1] : 1.f;
+        split_half2(sc[2 * kk][0] * va0, sc[2 * kk][1] * va1, ph[0], pl[0]);
+        split_half2(sc[2 * kk][2] * va0, sc[2 * kk][3] * va1, ph[1], pl[1]);
+        split_half2(sc[2 * kk + 1][0] * vb0, sc[2 * kk + 1][1] * vb1, ph[2], pl[2]);
+        split_half2(sc[2 * kk + 1][2] * vb0, sc[2 * kk + 1][3] * vb1, ph[3], pl[3]);
+      }
+#pragma unroll
+      for (int j = 0; j < NT; j += 2) {
+        const int m = lane >> 3, rr = lane & 7;
+        const int key = 16 * kk + 8 * (m & 1) + rr, chunk = j + (m >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vs_base + swz<D>(key, chunk), b0, b1, b2, b3);
+        mma16816(o[j], ph, b0, b1);
+        mma16816(o[j], pl, b0, b1);
+        mma16816(o[j + 1], ph, b2, b3);
+        mma16816(o[j + 1], pl, b2, b3);
+      }
+    }
+  }
+  // normalise and write rows r0, r1 (dims 8j + 2t, +1) as bf16 hi/lo
+  const float inv0 = l0 > 0.f ? 1.0f / l0 : 0.f, inv1 = l1 > 0.f ? 1.0f / l1 : 0.f;
+#pragma unroll
+  for (int row = 0; row < 2; ++row) {
+    const int r = row ? r1 : r0, tq = r / REP, h = r - tq * REP;
+    if (tq >= nt) continue;
+    const float inv = row ? inv1 : inv0;
+    const size_t base = static_cast<size_t>(t0 + tq) * nq * D + (kvh * REP + h) * D;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        __nv_bfloat16 hi, lo;
+        split_bf16(o[j][2 * row + e] * inv, hi, lo);
+        oh[base + 8 * j + 2 * t + e] = hi;
+        ol[base + 8 * j + 2 * t + e] = lo;
+      }
+    }
+  }
+}
+
 template <int D, int REP>
 constexpr size_t attn_smem() {
   return sizeof(float) * (static_cast<size_t>(kPaQT * REP) * (D + 1) + kPaKT * (D + 1) + kPaKT * D +
@@ -469,16 +703,17 @@ cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, co
 #define K2_PA_LAUNCH(DD, R)                                                                                       \
   if (D == DD && rep == R) {                                                                                      \
     const size_t sm = attn_smem<DD, R>();                                                                         \
+    const dim3 mgrid((n + kMaRows / R - 1) / (kMaRows / R), nkv);                                              \
     if (kv_dtype == 0)                                                                                            \
       prefill_attn_kernel<DD, R, float><<<grid, kPaThreads, sm, s>>>(                                             \
           Q, static_cast<const float*>(kc), static_cast<const float*>(vc), nullptr, nullptr, oh, ol, n, nq, pos0, \
           head_row0, cap, scale);                                                                                 \
     else if (kv_dtype == 2)                                                                                       \
-      prefill_attn_kernel<DD, R, __half><<<grid, kPaThreads, sm, s>>>(                                            \
+      prefill_attn_mma_kernel<DD, R, __half><<<mgrid, kMaThreads, 0, s>>>(                                        \
           Q, static_cast<const __half*>(kc), static_cast<const __half*>(vc), nullptr, nullptr, oh, ol, n, nq,     \
           pos0, head_row0, cap, scale);                                                                           \
     else                                                                                                          \
-      prefill_attn_kernel<DD, R, int8_t><<<grid, kPaThreads, sm, s>>>(                                            \
+      prefill_attn_mma_kernel<DD, R, int8_t><<<mgrid, kMaThreads, 0, s>>>(                                        \
           Q, static_cast<const int8_t*>(kc), static_cast<const int8_t*>(vc), static_cast<const __half*>(ks),      \
           static_cast<const __half*>(vs), oh, ol, n, nq, pos0, head_row0, cap, scale);                            \
     return cudaGetLastError();                                                                                    \
