@@ -620,6 +620,20 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.guard = c->guard;
     return launch_tc_gemm(mw, mh, ml, g, st);
   };
+  auto gemm_sk = [&](const void* mw, const void* mh, const void* ml, int N, int K, float* resid) {
+    TcGemmArgs g = {};
+    g.N = N;
+    g.K = K;
+    g.T = n;
+    g.ksteps = 4 * ((K + 255) / 256);
+    g.mode = TC_RESID;
+    g.ldo = N;
+    g.tile_tokens = 128;
+    g.splits = 1;
+    g.out = resid;
+    g.guard = c->guard;
+    return launch_tc_gemm_sk(mw, mh, ml, g, c->sms, st);
+  };
   cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.wb, X, s.H, s.V, c->guard, st);
   for (int l = 0; l < s.L && !e; ++l) {
     if (!e) e = launch_norm_rows(X, n, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
@@ -631,13 +645,12 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     if (!e)
       e = launch_prefill_attn(Q, kvdt, c->kc(l), c->vc(l), c->ks(l), c->vs(l), xh, xl, n, s.nq, s.nkv, s.d, pos0,
                               head_row0, c->lay.cap, scale, st);
-    if (!e) e = gemm(c->tmw[4 * l + 1].data(), c->tm_oh.data(), c->tm_ol.data(), s.H, s.nq * s.d, TC_RESID, X,
-                     nullptr, nullptr, s.H);
+    // o_proj and down have few row tiles: stream-K over one CTA per SM
+    if (!e) e = gemm_sk(c->tmw[4 * l + 1].data(), c->tm_oh.data(), c->tm_ol.data(), s.H, s.nq * s.d, X);
     if (!e) e = launch_norm_rows(X, n, c->mlp_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
     if (!e) e = gemm(c->tmw[4 * l + 2].data(), c->tm_xh.data(), c->tm_xl.data(), 2 * s.I, s.H, TC_SWIGLU, nullptr,
                      ah, al, s.I);
-    if (!e) e = gemm(c->tmw[4 * l + 3].data(), c->tm_ah.data(), c->tm_al.data(), s.H, s.I, TC_RESID, X, nullptr,
-                     nullptr, s.H);
+    if (!e) e = gemm_sk(c->tmw[4 * l + 3].data(), c->tm_ah.data(), c->tm_al.data(), s.H, s.I, X);
   }
   return e;
 }

@@ -407,19 +407,25 @@ cudaError_t tc_gemm_init_attrs() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc_gemm_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<16>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tc_gemm_sk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Tile<16>::SMEM_BYTES);
+  e = cudaFuncSetAttribute(tc_gemm_sk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<16>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tc_gemm_sk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Tile<128>::SMEM_BYTES);
 }
 
 cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a, int ctas,
                               cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
-  if (a.tile_tokens != 16 || a.mode == TC_SWIGLU || ctas < 1) return cudaErrorInvalidValue;
-  const long long total = static_cast<long long>((2 * ((a.N + 1) / 2) + BM - 1) / BM) * ((a.T + 15) / 16) * a.ksteps;
+  if ((a.tile_tokens != 16 && a.tile_tokens != 128) || a.mode == TC_SWIGLU || ctas < 1) return cudaErrorInvalidValue;
+  const int tt = a.tile_tokens;
+  const long long total =
+      static_cast<long long>((2 * ((a.N + 1) / 2) + BM - 1) / BM) * ((a.T + tt - 1) / tt) * a.ksteps;
   const int grid = static_cast<int>(std::min<long long>(ctas, total));
-  tc_gemm_sk_kernel<16><<<grid, 192, Tile<16>::SMEM_BYTES, s>>>(*static_cast<const CUtensorMap*>(mapW),
-                                                               *static_cast<const CUtensorMap*>(mapXh),
-                                                               *static_cast<const CUtensorMap*>(mapXl), a);
+  const CUtensorMap& w = *static_cast<const CUtensorMap*>(mapW);
+  const CUtensorMap& xh = *static_cast<const CUtensorMap*>(mapXh);
+  const CUtensorMap& xl = *static_cast<const CUtensorMap*>(mapXl);
+  if (tt == 16) tc_gemm_sk_kernel<16><<<grid, 192, Tile<16>::SMEM_BYTES, s>>>(w, xh, xl, a);
+  else tc_gemm_sk_kernel<128><<<grid, 192, Tile<128>::SMEM_BYTES, s>>>(w, xh, xl, a);
   return cudaGetLastError();
 }
 
