@@ -518,19 +518,25 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
       bad = true;
     }
     if (d.gain != nullptr) {
+      // per-group sums of squares (groups <= 4, K <= 4096: the first 4
+      // float4 groups of a thread hold its part of x)
       float ssq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < PX; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int e = tid * 4 + i * MT * 4;
-        const float4 v = xq[i];
-        const float t = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        const int grp = e < K ? e / gsz : 4;
+        if (e < K) {
+          const float4 v = xq[i];
+          const float t = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+          const int grp = (e >= gsz) + (e >= 2 * gsz) + (e >= 3 * gsz);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (q == grp) ssq[q] += t;
+          for (int q = 0; q < 4; ++q)
+            if (q == grp) ssq[q] += t;
+        }
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) ssq[q] = warp_sum(ssq[q]);
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ssq[q] += __shfl_xor_sync(0xffffffffu, ssq[q], o);
       if (lane == 0)
         for (int q = 0; q < 4; ++q) sh.ss[warp][q] = ssq[q];
       __syncthreads();
@@ -541,12 +547,12 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
       }
       __syncthreads();
 #pragma unroll
-      for (int i = 0; i < PX; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int e = tid * 4 + i * MT * 4;
         if (e < KP) {
           float4 v = xq[i];
           if (e < K) {
-            const float rs = sh.rs[e / gsz];
+            const float rs = sh.rs[(e >= gsz) + (e >= 2 * gsz) + (e >= 3 * gsz)];
             const float4 gn = load4_shared<WT>(gsm, e);
             v.x = v.x * rs * gn.x; v.y = v.y * rs * gn.y; v.z = v.z * rs * gn.z; v.w = v.w * rs * gn.w;
           }
