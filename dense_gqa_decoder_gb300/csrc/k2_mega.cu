@@ -111,6 +111,7 @@ struct Patience {
       atomicOr(guard, GUARD_TIMEOUT);
       return false;
     }
+    if (kMegaPollSleepNs > 0) __nanosleep(kMegaPollSleepNs);
     return true;
   }
 };
@@ -671,21 +672,35 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
   }
   if (bad && lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
   __syncthreads();
-  if (tid == 0) {
-    int cur = -1;
-    float v0 = 0.f, v1 = 0.f;
-    for (int w = 0; w < MW; ++w) {
-      for (int rr = 0; rr < sh.rec_n[w]; ++rr) {
-        if (sh.rec_pair[w][rr] != cur) {
-          if (cur >= 0) finish(r.p0 + cur, v0, v1);
-          cur = sh.rec_pair[w][rr];
-          v0 = v1 = 0.f;
+  // Pairs split between warps (at most two records per warp, in pair order):
+  // the thread of a pair's first record sums its records in warp order and
+  // finishes it, all such pairs at once.
+  if (tid < 2 * MW) {
+    const int w = tid >> 1, rr = tid & 1;
+    if (rr < sh.rec_n[w]) {
+      const int pr = sh.rec_pair[w][rr];
+      int pw = w, prr = rr - 1;
+      if (prr < 0) {
+        for (pw = w - 1; pw >= 0 && sh.rec_n[pw] == 0; --pw) {
         }
-        v0 += sh.rec_val[w][rr][0];
-        v1 += sh.rec_val[w][rr][1];
+        prr = pw >= 0 ? sh.rec_n[pw] - 1 : 0;
+      }
+      if (pw < 0 || sh.rec_pair[pw][prr] != pr) {
+        float v0 = 0.f, v1 = 0.f;
+        for (int cw = w, cr = rr; cw < MW;) {
+          if (cr >= sh.rec_n[cw]) {
+            ++cw;
+            cr = 0;
+            continue;
+          }
+          if (sh.rec_pair[cw][cr] != pr) break;
+          v0 += sh.rec_val[cw][cr][0];
+          v1 += sh.rec_val[cw][cr][1];
+          ++cr;
+        }
+        finish(r.p0 + pr, v0, v1);
       }
     }
-    if (cur >= 0) finish(r.p0 + cur, v0, v1);
   }
   return __syncthreads_and(!bad) != 0;
 }
@@ -739,9 +754,11 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
   constexpr int NQ4 = ((REP + 2) * D + MT - 1) / MT;  // tagged words per thread to stage
   static_assert(TKM > 0 && 2 * KVB + 2 * TKM * 2 <= SB, "an attention tile must fit one slot");
   static_assert(D <= 128 && REP * D <= 512, "staging buffers");
+  static_assert(REP <= MW, "one warp per query head in the merge");
   __shared__ float Sw[MW][REP][TKM];
   __shared__ __align__(16) float Pw[MW][TKM][REP];
   __shared__ float wstate[MW][PSTR];
+  __shared__ float wfac[MW][REP];  // per warp and query head: exp(m_warp - m_split)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (cta >= a.nkv * a.nsplit) return true;
   const int L = pos + 1;
@@ -975,13 +992,17 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
   const bool merger = (it.sp == 0);
   float* stage = reinterpret_cast<float*>(smem + kMegaRingBytes);  // the x buffer is free here
   u64* pub = a.t_part + static_cast<size_t>(cta) * PSTR;
+  if (tid < MW * REP) {
+    const int w = tid / REP, h = tid - (tid / REP) * REP;
+    float M = -INFINITY;
+    for (int v = 0; v < MW; ++v) M = fmaxf(M, wstate[v][h]);
+    wfac[w][h] = wstate[w][h] == -INFINITY ? 0.f : expf(wstate[w][h] - M);
+  }
+  __syncthreads();
   for (int idx = tid; idx < REP * D; idx += MT) {
     const int h = idx / D;
-    float M = -INFINITY;
-    for (int w = 0; w < MW; ++w) M = fmaxf(M, wstate[w][h]);
     float O = 0.f;
-    for (int w = 0; w < MW; ++w)
-      if (wstate[w][h] != -INFINITY) O = fmaf(wstate[w][2 * REP + idx], expf(wstate[w][h] - M), O);
+    for (int w = 0; w < MW; ++w) O = fmaf(wstate[w][2 * REP + idx], wfac[w][h], O);
     if (merger) stage[2 * REP + idx] = O;
     else st_tagged(pub + 2 * REP + idx, O, tag_out);
   }
@@ -989,8 +1010,7 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
     float M = -INFINITY;
     for (int w = 0; w < MW; ++w) M = fmaxf(M, wstate[w][tid]);
     float Ls = 0.f;
-    for (int w = 0; w < MW; ++w)
-      if (wstate[w][tid] != -INFINITY) Ls = fmaf(wstate[w][REP + tid], expf(wstate[w][tid] - M), Ls);
+    for (int w = 0; w < MW; ++w) Ls = fmaf(wstate[w][REP + tid], wfac[w][tid], Ls);
     if (merger) {
       stage[tid] = M;
       stage[REP + tid] = Ls;
@@ -1008,17 +1028,20 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
   }
   float* wts = &wstate[0][0];  // MW * PSTR >= nsplit * REP floats
   __syncthreads();
-  if (tid < REP) {  // per query head: the weight of each split, exp(M_s - M) / sum
+  if (warp < REP) {  // warp h, lane per split: the weight of each split, exp(M_s - M) / sum
+    const int h = warp;
     float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, stage[s * PSTR + tid]);
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, stage[s * PSTR + h]);
+    M = warp_max(M);
     float Ls = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const float ms = stage[s * PSTR + tid];
-      if (ms != -INFINITY) Ls = fmaf(stage[s * PSTR + REP + tid], expf(ms - M), Ls);
+    for (int s = lane; s < ns; s += 32) {
+      const float ms = stage[s * PSTR + h];
+      if (ms != -INFINITY) Ls = fmaf(stage[s * PSTR + REP + h], expf(ms - M), Ls);
     }
-    for (int s = 0; s < ns; ++s) {
-      const float ms = stage[s * PSTR + tid];
-      wts[s * REP + tid] = ms == -INFINITY ? 0.f : expf(ms - M) / Ls;
+    Ls = warp_sum(Ls);
+    for (int s = lane; s < ns; s += 32) {
+      const float ms = stage[s * PSTR + h];
+      wts[s * REP + h] = ms == -INFINITY ? 0.f : expf(ms - M) / Ls;
     }
   }
   __syncthreads();
