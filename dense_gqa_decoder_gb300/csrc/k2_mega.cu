@@ -62,6 +62,7 @@ constexpr int tile_keys() {
          : (2 * (kMegaTK / 2) * D * static_cast<int>(sizeof(KVT)) + 4 * (kMegaTK / 2) <= SB) ? kMegaTK / 2
                                                                                                : 0;
 }
+static_assert(2 * MW <= 32, "the warp-split GEMV records fit one warp");
 constexpr int kPhases = 5;       // per layer: QKV, ATTN, O, GU, DOWN
 enum { PH_QKV = 0, PH_ATTN = 1, PH_O = 2, PH_GU = 3, PH_DOWN = 4 };
 
@@ -672,35 +673,30 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
   }
   if (bad && lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
   __syncthreads();
-  // Pairs split between warps (at most two records per warp, in pair order):
-  // the thread of a pair's first record sums its records in warp order and
-  // finishes it, all such pairs at once.
-  if (tid < 2 * MW) {
-    const int w = tid >> 1, rr = tid & 1;
-    if (rr < sh.rec_n[w]) {
-      const int pr = sh.rec_pair[w][rr];
-      int pw = w, prr = rr - 1;
-      if (prr < 0) {
-        for (pw = w - 1; pw >= 0 && sh.rec_n[pw] == 0; --pw) {
+  // Pairs split between warps: at most two records per warp, lane 2w + rr of
+  // warp 0 holding record rr of warp w.  Every record of a pair is summed in
+  // warp order by the lane of its first record, which finishes the pair; a
+  // fixed 16-step shuffle loop, so the lanes never diverge.
+  if (warp == 0) {
+    const int w = lane >> 1, rr = lane & 1;
+    const bool has = lane < 2 * MW && rr < sh.rec_n[w];
+    const int pr = has ? sh.rec_pair[w][rr] : -1 - lane;
+    const float a0 = has ? sh.rec_val[w][rr][0] : 0.f, a1 = has ? sh.rec_val[w][rr][1] : 0.f;
+    float v0 = 0.f, v1 = 0.f;
+    bool first = has;
+#pragma unroll
+    for (int j = 0; j < 2 * MW; ++j) {
+      const int pj = __shfl_sync(0xffffffffu, pr, j);
+      const float b0 = __shfl_sync(0xffffffffu, a0, j), b1 = __shfl_sync(0xffffffffu, a1, j);
+      if (pj == pr) {
+        if (j < lane) first = false;
+        if (j >= lane) {
+          v0 += b0;
+          v1 += b1;
         }
-        prr = pw >= 0 ? sh.rec_n[pw] - 1 : 0;
-      }
-      if (pw < 0 || sh.rec_pair[pw][prr] != pr) {
-        float v0 = 0.f, v1 = 0.f;
-        for (int cw = w, cr = rr; cw < MW;) {
-          if (cr >= sh.rec_n[cw]) {
-            ++cw;
-            cr = 0;
-            continue;
-          }
-          if (sh.rec_pair[cw][cr] != pr) break;
-          v0 += sh.rec_val[cw][cr][0];
-          v1 += sh.rec_val[cw][cr][1];
-          ++cr;
-        }
-        finish(r.p0 + pr, v0, v1);
       }
     }
+    if (first) finish(r.p0 + pr, v0, v1);
   }
   return __syncthreads_and(!bad) != 0;
 }
