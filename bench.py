@@ -429,7 +429,8 @@ def run_ours(args, world, rank, local, pg):
                     "algorithmic_tflop": (pf_linear + pf_attn) / 1e12,
                     "achieved_tflops": pf_tflops, "peak_tflops": tc_peak, "frac": pf_tflops / tc_peak,
                     "note": "useful FLOPs (2 per weight x token + causal attention); the GEMMs issue twice "
-                            "the linear MMAs (activations as bf16 hi + lo halves); attention runs on CUDA cores"},
+                            "the linear MMAs (activations as bf16 hi + lo halves); attention issues mma.sync "
+                            "on fp16 hi + lo halves of the queries and probabilities"},
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
         "clocks": clk,
         "cpu_baseline": cpu,
