@@ -22,10 +22,8 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr size_t kGemvSmem = 104 * 1024;  // per-CTA budget: CTAs of two consecutive kernels share one SM
-constexpr size_t kAttnSmem = 128 * 1024;
 constexpr size_t kLmHeadSmem = 176 * 1024;
 constexpr int kArgmaxPartsMax = 1024;
-constexpr int kMegaSplitMax = 64;
 constexpr int kPrefillChunk = 2048;  // prompt tokens per tensor-core prefill pass
 constexpr int kTcPrefillMin = 8;     // shorter prompts are appended one decode step per token
 
@@ -469,10 +467,7 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   if (s.L > kMegaMaxLayers) return cudaSuccess;
   // tags carry the phase index in kMegaTagShift bits
   if (5 * s.L + 1 >= (1 << kMegaTagShift)) return cudaSuccess;
-  // the merging CTA stages every split's partial in the 40 KB input buffer
-  const size_t part_bytes = sizeof(float) * static_cast<size_t>(s.rep) * (s.d + 2);
   int nsplit = grid / s.nkv;
-  nsplit = std::min(nsplit, static_cast<int>(kMegaXBytes / part_bytes));
   if (nsplit > kMegaSplitMax) nsplit = kMegaSplitMax;
   if (nsplit > c->lay.cap / 8) nsplit = c->lay.cap / 8;
   if (nsplit < 1) return cudaSuccess;

@@ -236,6 +236,7 @@ constexpr int kMegaSmemBytes = kMegaRingBytes + kMegaXBytes + 2 * kMegaGainBytes
 constexpr int kMegaTK = 16;                   // keys per attention tile (at most)
 constexpr unsigned kMegaPollSleepNs = 0;      // pause between rounds of a tag poll
 constexpr int kMegaPairsMax = 64;             // row pairs of one CTA in the QKV / residual phases
+constexpr int kMegaSplitMax = 64;             // key splits per KV head in the attention phase
 constexpr int kMegaTagShift = 10;
 constexpr int kMegaMaxLayers = 64;            // norm-gain pointers kept in shared memory             // tag = (epoch + 1) << 10 | phase: at most 1023 phases
 

@@ -151,36 +151,6 @@ __device__ bool poll_x(const u64* tv, int K, uint32_t tag, float4* xq, unsigned*
   return true;
 }
 
-// n tagged words (n even, src 16-byte aligned) into dst[0 .. n), at most
-// 2 * kPollPairs * MT words, waiting until every tag equals `tag`.
-constexpr int kPollPairs = 20;
-__device__ bool poll_words(const u64* src, int n, uint32_t tag, float* dst, unsigned* guard) {
-  const int tid = threadIdx.x;
-  unsigned pend = 0;
-#pragma unroll
-  for (int i = 0; i < kPollPairs; ++i)
-    if (2 * (tid + i * MT) < n) pend |= 1u << i;
-  Patience wait;
-  while (pend) {
-    u64 w[kPollPairs][2];
-#pragma unroll
-    for (int i = 0; i < kPollPairs; ++i) {  // every load first, then the checks
-      w[i][0] = w[i][1] = 0;
-      if (pend & (1u << i)) ld_tagged2(src + 2 * (tid + i * MT), w[i][0], w[i][1]);
-    }
-#pragma unroll
-    for (int i = 0; i < kPollPairs; ++i) {
-      if ((pend & (1u << i)) && tag_is(w[i][0], tag) && tag_is(w[i][1], tag)) {
-        dst[2 * (tid + i * MT)] = tag_val(w[i][0]);
-        dst[2 * (tid + i * MT) + 1] = tag_val(w[i][1]);
-        pend &= ~(1u << i);
-      }
-    }
-    if (pend && !wait.more(guard)) return false;
-  }
-  return true;
-}
-
 struct MegaShared {
   uint64_t full[MW][NS];
   float ss[MW][4];
@@ -982,10 +952,11 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
   }
   if (__syncthreads_or(bad)) return false;
   // ---- this split's partial (max, sum, unnormalised output per query head):
-  // combine the warps.  Split 0 of each KV head keeps its own in the stage
-  // buffer and merges; the others publish theirs as tagged words.
+  // combine the warps and publish it as tagged words.  Then every split of
+  // the KV head merges one slice of the REP * D outputs from all the splits'
+  // partials, so each CTA reads a few hundred words instead of one CTA
+  // reading them all.
   const int ns = a.nsplit;
-  const bool merger = (it.sp == 0);
   float* stage = reinterpret_cast<float*>(smem + kMegaRingBytes);  // the x buffer is free here
   u64* pub = a.t_part + static_cast<size_t>(cta) * PSTR;
   if (tid < MW * REP) {
@@ -999,52 +970,83 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
     const int h = idx / D;
     float O = 0.f;
     for (int w = 0; w < MW; ++w) O = fmaf(wstate[w][2 * REP + idx], wfac[w][h], O);
-    if (merger) stage[2 * REP + idx] = O;
-    else st_tagged(pub + 2 * REP + idx, O, tag_out);
+    st_tagged(pub + 2 * REP + idx, O, tag_out);
   }
   if (tid < REP) {
     float M = -INFINITY;
     for (int w = 0; w < MW; ++w) M = fmaxf(M, wstate[w][tid]);
     float Ls = 0.f;
     for (int w = 0; w < MW; ++w) Ls = fmaf(wstate[w][REP + tid], wfac[w][tid], Ls);
-    if (merger) {
-      stage[tid] = M;
-      stage[REP + tid] = Ls;
-    } else {
-      st_tagged(pub + tid, M, tag_out);
-      st_tagged(pub + REP + tid, Ls, tag_out);
-    }
+    st_tagged(pub + tid, M, tag_out);
+    st_tagged(pub + REP + tid, Ls, tag_out);
   }
-  if (!merger) return true;
-  // ---- split 0 waits for the other splits' partials and merges them all
+  // ---- this split's slice [o0, o1) of the merged outputs
+  const int o0 = (REP * D * it.sp) / ns, o1 = (REP * D * (it.sp + 1)) / ns, nsl = o1 - o0;
+  const u64* head_part = a.t_part + static_cast<size_t>(it.g) * ns * PSTR;  // split s at s * PSTR
+  float* mlv = stage;               // [s][2 * REP]: max, then sum, per query head
+  float* ov = stage + 2 * REP * ns;  // [s][nsl]: the slice of each split's output
   {
-    const u64* src = a.t_part + static_cast<size_t>(cta + 1) * PSTR;  // splits 1 .. ns-1 follow
-    const bool ok = poll_words(src, (ns - 1) * PSTR, tag_out, stage + PSTR, a.guard);
-    if (__syncthreads_or(!ok)) return false;
+    constexpr int NPW = (2 * REP * kMegaSplitMax + REP * D + kMegaSplitMax + MT - 1) / MT;
+    const int nml = 2 * REP * ns, nw = nml + nsl * ns;
+    const u64* src[NPW];
+    unsigned pend = 0;
+#pragma unroll
+    for (int i = 0; i < NPW; ++i) {
+      const int k = tid + i * MT;
+      src[i] = head_part;
+      if (k < nw) {
+        pend |= 1u << i;
+        if (k < nml) {
+          const int sp = k / (2 * REP);
+          src[i] = head_part + static_cast<size_t>(sp) * PSTR + (k - sp * 2 * REP);
+        } else {
+          const int kk = k - nml, sp = kk / nsl;
+          src[i] = head_part + static_cast<size_t>(sp) * PSTR + 2 * REP + o0 + (kk - sp * nsl);
+        }
+      }
+    }
+    Patience wait;
+    bool bad = false;
+    while (pend) {
+      u64 w[NPW];
+#pragma unroll
+      for (int i = 0; i < NPW; ++i) w[i] = (pend & (1u << i)) ? ld_tagged(src[i]) : 0ull;
+#pragma unroll
+      for (int i = 0; i < NPW; ++i) {
+        if ((pend & (1u << i)) && tag_is(w[i], tag_out)) {
+          stage[tid + i * MT] = tag_val(w[i]);  // mlv then ov: the word order above
+          pend &= ~(1u << i);
+        }
+      }
+      if (pend && !wait.more(a.guard)) {
+        bad = true;
+        break;
+      }
+    }
+    if (__syncthreads_or(bad)) return false;
   }
   float* wts = &wstate[0][0];  // MW * PSTR >= nsplit * REP floats
-  __syncthreads();
   if (warp < REP) {  // warp h, lane per split: the weight of each split, exp(M_s - M) / sum
     const int h = warp;
     float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, stage[s * PSTR + h]);
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, mlv[s * 2 * REP + h]);
     M = warp_max(M);
     float Ls = 0.f;
     for (int s = lane; s < ns; s += 32) {
-      const float ms = stage[s * PSTR + h];
-      if (ms != -INFINITY) Ls = fmaf(stage[s * PSTR + REP + h], expf(ms - M), Ls);
+      const float ms = mlv[s * 2 * REP + h];
+      if (ms != -INFINITY) Ls = fmaf(mlv[s * 2 * REP + REP + h], expf(ms - M), Ls);
     }
     Ls = warp_sum(Ls);
     for (int s = lane; s < ns; s += 32) {
-      const float ms = stage[s * PSTR + h];
+      const float ms = mlv[s * 2 * REP + h];
       wts[s * REP + h] = ms == -INFINITY ? 0.f : expf(ms - M) / Ls;
     }
   }
   __syncthreads();
-  for (int idx = tid; idx < REP * D; idx += MT) {
-    const int h = idx / D;
+  for (int t = tid; t < nsl; t += MT) {
+    const int idx = o0 + t, h = idx / D;
     float O = 0.f;
-    for (int s = 0; s < ns; ++s) O = fmaf(stage[s * PSTR + 2 * REP + idx], wts[s * REP + h], O);
+    for (int s = 0; s < ns; ++s) O = fmaf(ov[s * nsl + t], wts[s * REP + h], O);
     st_tagged(a.t_attn + static_cast<size_t>(it.g) * REP * D + idx, O, tag_out);
   }
   __syncthreads();  // the stage is the next phase's x buffer
