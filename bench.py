@@ -46,6 +46,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--layers", type=int, default=0, help="override layer count (debug)")
     p.add_argument("--kv", default="f16", choices=["f16", "i8"], help="KV cache storage")
+    p.add_argument("--kv-state", action="store_true",
+                   help="time saving and restoring the cache state of a --ctx-token sequence (k2_kv_save / "
+                        "k2_kv_load, pinned host memory) instead of decoding")
     p.add_argument("--batch", type=int, default=1,
                    help="> 1: aggregate decode throughput of that many sequences per step (each prefilled "
                         "with --ctx random tokens); the default 1 is the batch-1 metric")
@@ -439,6 +442,59 @@ def run_ours(args, world, rank, local, pg):
         print(json.dumps(line), flush=True)
 
 
+def run_kv_state(args, world, rank, local, pg):
+    """Save / restore of one sequence's cache: the state of a --ctx-token
+    prompt (K/V rows of every layer + header + the prompt's ids) written to
+    pinned host memory and read back, --steps times each after --warmup."""
+    import torch
+
+    import k2_inputs as ki
+    from dense_gqa_decoder_gb300 import k2
+
+    torch.cuda.set_device(local)
+    s = ki.SHAPES[SHAPE_NAME]
+    if args.layers:
+        s = s.replace(n_layers=args.layers)
+    cfg = k2.make_config(s, max_context=args.ctx + 16, max_batch=1, kv_dtype=args.kv)
+    ctx = k2.Context(cfg, random_device_weights(s, seed=1234 + rank))
+    stream = torch.cuda.Stream()
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ids = ki.prompt_ids(s.vocab, args.ctx, seed=1 + rank)
+    with torch.cuda.stream(stream):
+        ctx.prefill(0, torch.from_numpy(ids).cuda(), tok, stream=stream)
+    stream.synchronize()
+    n = ctx.kv_state_bytes(0, len(ids))
+    buf = torch.empty(n, dtype=torch.uint8).pin_memory()
+    save_s, load_s = [], []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        state = ctx.kv_save(0, ids, out=buf, stream=stream)
+        t1 = time.perf_counter()
+        back = ctx.kv_load(0, state, stream=stream)
+        t2 = time.perf_counter()
+        if i >= args.warmup:
+            save_s.append(t1 - t0)
+            load_s.append(t2 - t1)
+    assert back == [int(x) for x in ids]
+    with torch.cuda.stream(stream):
+        ctx.decode_step(tok, 1, tok, stream=stream)
+    if ctx.sync_status(stream) != k2.K2_OK:
+        raise RuntimeError("device guard after the restored step: " + ctx.last_error())
+    save_gbs = world * n / (sum(save_s) / len(save_s)) / 1e9
+    line = {
+        "metric": f"KV cache state save / restore, {args.ctx}-token sequence", "value": save_gbs, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": args.kv, "data": "synthetic",
+        "config": {"workload": f"k2-horizon-3.7b-shape cache of one sequence, context {args.ctx}, {args.kv} KV",
+                   "layers": s.n_layers, "host_buffer": "pinned"},
+        "state_bytes": n,
+        "save": {"ms": 1e3 * sum(save_s) / len(save_s), "gbs": save_gbs},
+        "load": {"ms": 1e3 * sum(load_s) / len(load_s), "gbs": world * n / (sum(load_s) / len(load_s)) / 1e9},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_batched(args, world, rank, local, pg):
     """Batched decode: --batch sequences, each prefilled with --ctx random ids,
     advanced together by one k2_decode_step per step (weights read once per
@@ -517,6 +573,8 @@ def main():
     world, rank, local, pg = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank, pg)
+    elif args.kv_state:
+        run_kv_state(args, world, rank, local, pg)
     elif args.batch > 1:
         run_batched(args, world, rank, local, pg)
     else:

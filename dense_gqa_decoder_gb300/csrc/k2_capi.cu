@@ -5,6 +5,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
+#include <stddef.h>
+#include <cstring>
 
 #include <algorithm>
 #include <array>
@@ -768,6 +770,82 @@ thread_local std::string g_init_error;
 // ---------------------------------------------------------------------------
 // C ABI
 // ---------------------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// saved cache state (layout documented in include/k2.h)
+// ---------------------------------------------------------------------------
+namespace {
+
+struct StateHeader {
+  char magic[4];
+  int32_t version;
+  int32_t fp[12];
+  int32_t cached, n_tokens;
+  int64_t row_bytes, scale_bytes, total_bytes;
+  int32_t reserved[2];
+};
+static_assert(sizeof(StateHeader) == K2_STATE_HEADER_BYTES, "state header size");
+static_assert(offsetof(StateHeader, fp) == 8 && offsetof(StateHeader, cached) == 56 &&
+                  offsetof(StateHeader, row_bytes) == 64 && offsetof(StateHeader, reserved) == 88,
+              "state header layout");
+constexpr char kStateMagic[4] = {'K', '2', 'S', 'T'};
+constexpr int32_t kStateVersion = 1;
+
+void state_fingerprint(const k2_config& c, int32_t* fp) {
+  fp[0] = c.hidden; fp[1] = c.n_layers; fp[2] = c.n_heads; fp[3] = c.n_kv_heads; fp[4] = c.head_dim;
+  fp[5] = c.intermediate; fp[6] = c.norm_groups; fp[7] = c.vocab; fp[8] = c.weight_dtype; fp[9] = c.kv_dtype;
+  std::memcpy(&fp[10], &c.eps, sizeof(float));
+  std::memcpy(&fp[11], &c.rope_theta, sizeof(float));
+}
+
+// Byte offsets of a state: tokens right after the header, then per layer
+// K rows, V rows and (int8) the K and V scales, each layer 16-byte aligned.
+struct StateGeom {
+  int64_t row, scale, kv_off, rows_bytes, scales_bytes, per_layer, total;
+};
+StateGeom state_geom(const k2_config& c, int64_t cached, int64_t n_tokens) {
+  StateGeom g;
+  g.row = static_cast<int64_t>(c.head_dim) * elt_bytes(c.kv_dtype);
+  g.scale = c.kv_dtype == K2_I8 ? 2 : 0;
+  g.kv_off = static_cast<int64_t>(align_up(K2_STATE_HEADER_BYTES + 4 * static_cast<size_t>(n_tokens), 16));
+  const int64_t rows = static_cast<int64_t>(c.n_kv_heads) * cached;
+  g.rows_bytes = rows * g.row;
+  g.scales_bytes = rows * g.scale;
+  g.per_layer = static_cast<int64_t>(align_up(static_cast<size_t>(2 * g.rows_bytes + 2 * g.scales_bytes), 16));
+  g.total = g.kv_off + c.n_layers * g.per_layer;
+  return g;
+}
+
+// The reason a state cannot be loaded for config c, or null.
+const char* state_problem(const k2_config& c, const void* buf, size_t bytes, StateHeader* out) {
+  if (!buf || bytes < sizeof(StateHeader)) return "shorter than the state header";
+  StateHeader h;
+  std::memcpy(&h, buf, sizeof h);
+  if (std::memcmp(h.magic, kStateMagic, 4) != 0) return "not a saved k2 cache state (magic)";
+  if (h.version != kStateVersion) return "a state version this library does not read";
+  int32_t fp[12];
+  state_fingerprint(c, fp);
+  if (std::memcmp(fp, h.fp, sizeof fp) != 0)
+    return "written for another model architecture or KV format (fingerprint differs)";
+  if (h.cached < 0 || h.n_tokens < 0 || h.reserved[0] != 0 || h.reserved[1] != 0) return "damaged header";
+  const StateGeom g = state_geom(c, h.cached, h.n_tokens);
+  if (h.row_bytes != g.row || h.scale_bytes != g.scale || h.total_bytes != g.total) return "damaged header (sizes)";
+  if (bytes < static_cast<size_t>(g.total)) return "truncated (shorter than its header says)";
+  if (out) *out = h;
+  return nullptr;
+}
+
+// One K or V (or scale) block of a layer: nkv runs of `run` bytes, cap
+// rows apart on the device, back to back in the state.
+cudaError_t state_copy(void* dst, const void* src, size_t run, size_t dev_pitch, int nkv, bool to_device,
+                       cudaStream_t st) {
+  if (run == 0) return cudaSuccess;
+  if (to_device)
+    return cudaMemcpy2DAsync(dst, dev_pitch, src, run, run, nkv, cudaMemcpyHostToDevice, st);
+  return cudaMemcpy2DAsync(dst, run, src, dev_pitch, run, nkv, cudaMemcpyDeviceToHost, st);
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t k2_workspace_bytes(const k2_config* cfg) {
@@ -1119,6 +1197,121 @@ k2_status k2_profile_decode(k2_ctx* c, const int32_t* d_tokens, int32_t batch, i
   enqueue_decode(c, ln, d_tokens, batch, d_next, nullptr);
   if (ln.collect(ms, launches) != cudaSuccess) return c->cuda_fail(ln.err, "profile launch");
   for (int b = 0; b < batch; ++b) c->len[b] += 1;
+  return K2_OK;
+}
+
+
+k2_status k2_kv_state_bytes(const k2_ctx* c, int32_t seq, int32_t n_tokens, size_t* bytes) {
+  if (!c || !bytes || seq < 0 || seq >= c->s.B || n_tokens < 0) return K2_ERR_ARG;
+  *bytes = static_cast<size_t>(state_geom(c->cfg, c->len[seq], n_tokens).total);
+  return K2_OK;
+}
+
+k2_status k2_kv_save(k2_ctx* c, int32_t seq, const int32_t* h_tokens, int32_t n_tokens, void* h_buf,
+                     size_t buf_bytes, size_t* written, void* stream) {
+  if (!c) return K2_ERR_ARG;
+  if (seq < 0 || seq >= c->s.B) return c->fail(K2_ERR_ARG, "seq %d outside [0, %d)", seq, c->s.B);
+  if (n_tokens < 0 || (n_tokens > 0 && !h_tokens) || !h_buf)
+    return c->fail(K2_ERR_ARG, "h_buf and (for n_tokens > 0) h_tokens must be non-null");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int cached = c->len[seq];
+  const StateGeom g = state_geom(c->cfg, cached, n_tokens);
+  if (buf_bytes < static_cast<size_t>(g.total))
+    return c->fail(K2_ERR_WORKSPACE, "the state needs %lld bytes, the buffer has %zu", (long long)g.total, buf_bytes);
+  // the cache must hold what the host believes: no pending fault, same length
+  unsigned guard = 0;
+  int dev_len = -1;
+  cudaError_t e = cudaMemcpyAsync(&guard, c->guard, sizeof guard, cudaMemcpyDeviceToHost, st);
+  if (!e) e = cudaMemcpyAsync(&dev_len, c->seq_len + seq, sizeof dev_len, cudaMemcpyDeviceToHost, st);
+  if (!e) e = cudaStreamSynchronize(st);
+  if (e) return c->cuda_fail(e, "kv_save");
+  if (guard) return c->fail(K2_ERR_DEVICE_GUARD, "the device guard is set (0x%x): not saving", guard);
+  if (dev_len != cached)
+    return c->fail(K2_ERR_DEVICE_GUARD, "sequence %d holds %d rows on the device, %d on the host", seq, dev_len, cached);
+  uint8_t* out = static_cast<uint8_t*>(h_buf);
+  StateHeader h = {};
+  std::memcpy(h.magic, kStateMagic, 4);
+  h.version = kStateVersion;
+  state_fingerprint(c->cfg, h.fp);
+  h.cached = cached;
+  h.n_tokens = n_tokens;
+  h.row_bytes = g.row;
+  h.scale_bytes = g.scale;
+  h.total_bytes = g.total;
+  std::memcpy(out, &h, sizeof h);
+  if (n_tokens) std::memcpy(out + sizeof h, h_tokens, 4 * static_cast<size_t>(n_tokens));
+  std::memset(out + sizeof h + 4 * static_cast<size_t>(n_tokens), 0,
+              static_cast<size_t>(g.kv_off) - sizeof h - 4 * static_cast<size_t>(n_tokens));
+  const size_t head0 = static_cast<size_t>(seq) * c->s.nkv * c->lay.cap;  // row of (seq, head 0)
+  const size_t run = static_cast<size_t>(cached) * g.row, srun = static_cast<size_t>(cached) * g.scale;
+  for (int l = 0; l < c->s.L && !e; ++l) {
+    uint8_t* o = out + g.kv_off + static_cast<size_t>(l) * g.per_layer;
+    const size_t pitch = static_cast<size_t>(c->lay.cap) * g.row;
+    e = state_copy(o, static_cast<uint8_t*>(c->kc(l)) + head0 * g.row, run, pitch, c->s.nkv, false, st);
+    if (!e) e = state_copy(o + g.rows_bytes, static_cast<uint8_t*>(c->vc(l)) + head0 * g.row, run, pitch, c->s.nkv, false, st);
+    if (!e && g.scale) {
+      const size_t sp = static_cast<size_t>(c->lay.cap) * 2;
+      e = state_copy(o + 2 * g.rows_bytes, static_cast<uint8_t*>(c->ks(l)) + head0 * 2, srun, sp, c->s.nkv, false, st);
+      if (!e)
+        e = state_copy(o + 2 * g.rows_bytes + g.scales_bytes, static_cast<uint8_t*>(c->vs(l)) + head0 * 2, srun, sp,
+                       c->s.nkv, false, st);
+    }
+    const size_t used = static_cast<size_t>(2 * g.rows_bytes + 2 * g.scales_bytes);
+    std::memset(o + used, 0, static_cast<size_t>(g.per_layer) - used);
+  }
+  if (!e) e = cudaStreamSynchronize(st);
+  if (e) return c->cuda_fail(e, "kv_save copies");
+  if (written) *written = static_cast<size_t>(g.total);
+  return K2_OK;
+}
+
+k2_status k2_kv_peek(const k2_config* cfg, const void* h_buf, size_t buf_bytes, int32_t* cached, int32_t* n_tokens) {
+  if (!cfg) return K2_ERR_ARG;
+  StateHeader h;
+  if (state_problem(*cfg, h_buf, buf_bytes, &h)) return K2_ERR_STATE;
+  if (cached) *cached = h.cached;
+  if (n_tokens) *n_tokens = h.n_tokens;
+  return K2_OK;
+}
+
+k2_status k2_kv_load(k2_ctx* c, int32_t seq, const void* h_buf, size_t buf_bytes, int32_t* h_tokens,
+                     int32_t max_tokens, void* stream) {
+  if (!c) return K2_ERR_ARG;
+  if (seq < 0 || seq >= c->s.B) return c->fail(K2_ERR_ARG, "seq %d outside [0, %d)", seq, c->s.B);
+  StateHeader h;
+  if (const char* why = state_problem(c->cfg, h_buf, buf_bytes, &h)) return c->fail(K2_ERR_STATE, "refusing the state: %s", why);
+  if (h.cached > c->s.ctx)
+    return c->fail(K2_ERR_CONTEXT_FULL, "the state holds %d rows, this context's max_context is %d", h.cached, c->s.ctx);
+  if (h.n_tokens > max_tokens || (h.n_tokens > 0 && !h_tokens))
+    return c->fail(K2_ERR_ARG, "the state holds %d token ids, h_tokens has room for %d", h.n_tokens,
+                   h_tokens ? max_tokens : 0);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const StateGeom g = state_geom(c->cfg, h.cached, h.n_tokens);
+  const uint8_t* in = static_cast<const uint8_t*>(h_buf);
+  const size_t head0 = static_cast<size_t>(seq) * c->s.nkv * c->lay.cap;
+  const size_t run = static_cast<size_t>(h.cached) * g.row, srun = static_cast<size_t>(h.cached) * g.scale;
+  cudaError_t e = cudaSuccess;
+  for (int l = 0; l < c->s.L && !e; ++l) {
+    const uint8_t* o = in + g.kv_off + static_cast<size_t>(l) * g.per_layer;
+    const size_t pitch = static_cast<size_t>(c->lay.cap) * g.row;
+    e = state_copy(static_cast<uint8_t*>(c->kc(l)) + head0 * g.row, o, run, pitch, c->s.nkv, true, st);
+    if (!e) e = state_copy(static_cast<uint8_t*>(c->vc(l)) + head0 * g.row, o + g.rows_bytes, run, pitch, c->s.nkv, true, st);
+    if (!e && g.scale) {
+      const size_t sp = static_cast<size_t>(c->lay.cap) * 2;
+      e = state_copy(static_cast<uint8_t*>(c->ks(l)) + head0 * 2, o + 2 * g.rows_bytes, srun, sp, c->s.nkv, true, st);
+      if (!e)
+        e = state_copy(static_cast<uint8_t*>(c->vs(l)) + head0 * 2, o + 2 * g.rows_bytes + g.scales_bytes, srun, sp,
+                       c->s.nkv, true, st);
+    }
+  }
+  // the length goes last, from a buffer that outlives the copy (synchronised below)
+  static thread_local int v;
+  v = h.cached;
+  if (!e) e = cudaMemcpyAsync(c->seq_len + seq, &v, sizeof(int), cudaMemcpyHostToDevice, st);
+  if (!e) e = cudaStreamSynchronize(st);
+  if (e) return c->cuda_fail(e, "kv_load copies");
+  c->len[seq] = h.cached;
+  if (h.n_tokens) std::memcpy(h_tokens, in + sizeof(StateHeader), 4 * static_cast<size_t>(h.n_tokens));
   return K2_OK;
 }
 

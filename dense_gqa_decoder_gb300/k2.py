@@ -15,7 +15,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libk2.so")
 
 K2_OK, K2_ERR_ARG, K2_ERR_SHAPE, K2_ERR_UNSUPPORTED, K2_ERR_TOKEN_RANGE, K2_ERR_CONTEXT_FULL, \
-    K2_ERR_WORKSPACE, K2_ERR_CUDA, K2_ERR_DEVICE_GUARD = range(9)
+    K2_ERR_WORKSPACE, K2_ERR_CUDA, K2_ERR_DEVICE_GUARD, K2_ERR_STATE = range(10)
+K2_STATE_HEADER_BYTES = 96
 K2_F32, K2_BF16, K2_F16, K2_I8 = range(4)
 K2_OPT_PDL, K2_OPT_GRAPH, K2_OPT_ATTN_SPLITS, K2_OPT_PERSISTENT, K2_OPT_TC_PREFILL, K2_OPT_TC_DECODE = range(6)
 KERNEL_CLASSES = ("embed", "qkv", "attn", "o_proj", "gate_up", "down", "lm_head", "step")
@@ -73,6 +74,10 @@ def _load():
         "k2_set_option": (C.c_int, [vp, i32, i64]),
         "k2_profile_decode": (C.c_int, [vp, vp, i32, vp, C.POINTER(C.c_float), C.POINTER(i32), vp]),
         "k2_greedy_head_noalloc": (C.c_int, [C.POINTER(Config), vp, vp, vp, vp, vp, vp]),
+        "k2_kv_state_bytes": (C.c_int, [vp, i32, i32, C.POINTER(C.c_size_t)]),
+        "k2_kv_save": (C.c_int, [vp, i32, vp, i32, vp, C.c_size_t, C.POINTER(C.c_size_t), vp]),
+        "k2_kv_peek": (C.c_int, [C.POINTER(Config), vp, C.c_size_t, C.POINTER(i32), C.POINTER(i32)]),
+        "k2_kv_load": (C.c_int, [vp, i32, vp, C.c_size_t, vp, i32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -84,7 +89,8 @@ def _load():
 LIB = _load()
 EXPORTED = ("k2_workspace_bytes", "k2_init_weights", "k2_free", "k2_last_error", "k2_get_info", "k2_prefill",
             "k2_decode_step", "k2_decode_layers", "k2_kv_reset", "k2_kv_set_len", "k2_kv_view", "k2_hidden_view",
-            "k2_sync_status", "k2_clear_status", "k2_set_option", "k2_profile_decode", "k2_greedy_head_noalloc")
+            "k2_sync_status", "k2_clear_status", "k2_set_option", "k2_profile_decode", "k2_greedy_head_noalloc",
+            "k2_kv_state_bytes", "k2_kv_save", "k2_kv_peek", "k2_kv_load")
 
 
 def _ptr(t):
@@ -194,6 +200,35 @@ class Context:
     def set_option(self, opt, value):
         self._check(LIB.k2_set_option(self.ctx, opt, value))
 
+    def kv_state_bytes(self, seq, n_tokens=0):
+        n = C.c_size_t()
+        st = LIB.k2_kv_state_bytes(self.ctx, seq, n_tokens, C.byref(n))
+        if st != K2_OK:
+            raise K2Error(st, "kv_state_bytes: bad seq or n_tokens")
+        return n.value
+
+    def kv_save(self, seq, tokens=(), out=None, stream=None):
+        """k2_kv_save into `out` (a uint8 CPU tensor, pinned copies fastest) or
+        a new pinned buffer; returns the uint8 tensor holding the state."""
+        ids = torch.as_tensor(list(tokens) if not torch.is_tensor(tokens) else tokens.cpu(),
+                              dtype=torch.int32).contiguous()
+        n = self.kv_state_bytes(seq, ids.numel())
+        if out is None:
+            out = torch.empty(n, dtype=torch.uint8).pin_memory()
+        wrote = C.c_size_t()
+        self._check(LIB.k2_kv_save(self.ctx, seq, ids.data_ptr() if ids.numel() else None, ids.numel(),
+                                   out.data_ptr(), out.numel(), C.byref(wrote), _stream(stream)))
+        return out[:wrote.value]
+
+    def kv_load(self, seq, state, stream=None):
+        """k2_kv_load from a uint8 CPU tensor; returns the saved token ids."""
+        state = state.contiguous()
+        cached, n_tok = peek_state(self.cfg, state)  # sizes the token buffer; the load re-checks
+        ids = torch.empty(max(n_tok, 0), dtype=torch.int32)
+        self._check(LIB.k2_kv_load(self.ctx, seq, state.data_ptr(), state.numel(),
+                                   ids.data_ptr() if n_tok > 0 else None, max(n_tok, 0), _stream(stream)))
+        return ids.tolist()
+
     def profile_decode(self, tokens, batch, next_tokens, stream=None):
         ms = (C.c_float * len(KERNEL_CLASSES))()
         n = (C.c_int32 * len(KERNEL_CLASSES))()
@@ -206,6 +241,27 @@ def greedy_head_noalloc(cfg: Config, lm_head, final_norm, x, logits, token, stre
     """k2_greedy_head_noalloc: returns the k2 status (no context, no workspace)."""
     return LIB.k2_greedy_head_noalloc(C.byref(cfg), _ptr(lm_head), _ptr(final_norm), _ptr(x), _ptr(logits),
                                       _ptr(token), _stream(stream))
+
+
+def peek_state(cfg: Config, state) -> tuple:
+    """k2_kv_peek: (cached rows, token ids) of a state in a uint8 CPU tensor,
+    or (-1, -1) if it cannot be loaded into a context of cfg's model."""
+    state = state.contiguous()
+    cached, n_tok = C.c_int32(-1), C.c_int32(-1)
+    if LIB.k2_kv_peek(C.byref(cfg), state.data_ptr(), state.numel(), C.byref(cached), C.byref(n_tok)) != K2_OK:
+        return -1, -1
+    return cached.value, n_tok.value
+
+
+def save_state_file(path: str, state) -> None:
+    with open(path, "wb") as f:
+        f.write(state.numpy().tobytes())
+
+
+def load_state_file(path: str) -> torch.Tensor:
+    with open(path, "rb") as f:
+        data = f.read()
+    return torch.frombuffer(bytearray(data), dtype=torch.uint8)
 
 
 def device_view(ptr: int, numel: int, dtype: torch.dtype) -> torch.Tensor:

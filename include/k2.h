@@ -57,7 +57,9 @@ typedef enum {
   K2_ERR_CONTEXT_FULL = 5, /* the tokens do not fit the remaining context */
   K2_ERR_WORKSPACE = 6,    /* workspace missing, misaligned or too small */
   K2_ERR_CUDA = 7,         /* a CUDA runtime call failed */
-  K2_ERR_DEVICE_GUARD = 8  /* the device guard word is set (k2_sync_status) */
+  K2_ERR_DEVICE_GUARD = 8, /* the device guard word is set (k2_sync_status) */
+  K2_ERR_STATE = 9         /* a saved cache state that is not this library's, is damaged, or was
+                              written for another model architecture or KV format */
 } k2_status;
 
 typedef enum { K2_F32 = 0, K2_BF16 = 1, K2_F16 = 2, K2_I8 = 3 } k2_dtype;
@@ -181,6 +183,58 @@ k2_status k2_kv_set_len(k2_ctx* ctx, int32_t seq, int32_t len, void* stream);
  * length (host view). */
 k2_status k2_kv_view(k2_ctx* ctx, int32_t layer, int32_t seq, void** k, void** v, void** k_scale, void** v_scale,
                      int32_t* len);
+
+/* ---- saved cache state ------------------------------------------------------
+ *
+ * A sequence's cache can be written to host memory and restored later, into
+ * this or another context, so that a resumed conversation pays only for its
+ * new tokens (kimi-k3-in-c k3_run.c, "conversation state").  The state holds
+ * only the occupied rows, so the restoring context may have a different
+ * max_context or max_batch.  Its header carries a fingerprint of the model
+ * architecture and KV format; a state written for anything else is refused,
+ * because restoring it would give fluent, wrong output.
+ *
+ * Layout (little-endian, all offsets from the start of the state):
+ *   0   char magic[4] = "K2ST"; int32 version = 1
+ *   8   int32 fp[12]: hidden, n_layers, n_heads, n_kv_heads, head_dim,
+ *       intermediate, norm_groups, vocab, weight_dtype, kv_dtype, and the bit
+ *       patterns of eps and rope_theta
+ *   56  int32 cached (rows per layer and KV head), int32 n_tokens
+ *   64  int64 row_bytes (one K or V row), int64 scale_bytes (2 for K2_I8, else 0),
+ *       int64 total_bytes
+ *   88  int32 reserved[2] = 0
+ *   96  int32 tokens[n_tokens] (the caller's token ids, e.g. the conversation so far)
+ *   then, 16-byte aligned, per layer: K [n_kv_heads][cached] rows, V the same,
+ *       and for K2_I8 the fp16 scales of K [n_kv_heads][cached], then of V. */
+#define K2_STATE_HEADER_BYTES 96
+
+/* Bytes of the state k2_kv_save writes for sequence seq with n_tokens ids. */
+k2_status k2_kv_state_bytes(const k2_ctx* ctx, int32_t seq, int32_t n_tokens, size_t* bytes);
+
+/* Writes sequence seq's state into h_buf (host memory of buf_bytes bytes;
+ * pinned memory copies fastest) with the n_tokens ids of h_tokens (host,
+ * nullable when n_tokens = 0); *written = its size.  Waits for `stream`
+ * first and returns when the copies are done.  K2_ERR_WORKSPACE if buf_bytes
+ * is too small; K2_ERR_DEVICE_GUARD if the device guard is set (the cache may
+ * not hold what the host expects). */
+k2_status k2_kv_save(k2_ctx* ctx, int32_t seq, const int32_t* h_tokens, int32_t n_tokens, void* h_buf,
+                     size_t buf_bytes, size_t* written, void* stream);
+
+/* Checks a state in host memory against a config without a context: magic,
+ * version, fingerprint and sizes.  K2_OK and *cached, *n_tokens (nullable) if
+ * it could be loaded into a context of cfg's architecture and KV format;
+ * K2_ERR_STATE otherwise (the reason is not kept: there is no context). */
+k2_status k2_kv_peek(const k2_config* cfg, const void* h_buf, size_t buf_bytes, int32_t* cached, int32_t* n_tokens);
+
+/* Restores a state into sequence seq (its previous rows are replaced), sets
+ * its length to the saved row count and copies the saved token ids into
+ * h_tokens (host, max_tokens entries; nullable when max_tokens = 0).
+ * Enqueued on `stream`, then waited for.  Before anything is changed:
+ * K2_ERR_STATE for a state of another architecture or KV format or a damaged
+ * one, K2_ERR_CONTEXT_FULL if its rows do not fit this context's
+ * max_context, K2_ERR_ARG if max_tokens is smaller than the saved count. */
+k2_status k2_kv_load(k2_ctx* ctx, int32_t seq, const void* h_buf, size_t buf_bytes, int32_t* h_tokens,
+                     int32_t max_tokens, void* stream);
 
 /* Device pointer of the fp32 residual stream of launch slot b ([hidden]); after
  * a decode step it holds the residual leaving the last layer for sequence b
