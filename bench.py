@@ -46,6 +46,14 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--layers", type=int, default=0, help="override layer count (debug)")
     p.add_argument("--kv", default="f16", choices=["f16", "i8"], help="KV cache storage")
+    p.add_argument("--temperature", type=float, default=0.0,
+                   help="> 0: sample each token (with --top-k / --top-p / --min-p / --repetition-penalty / "
+                        "--seed) instead of the greedy argmax")
+    p.add_argument("--top-k", type=int, default=0)
+    p.add_argument("--top-p", type=float, default=1.0)
+    p.add_argument("--min-p", type=float, default=0.0)
+    p.add_argument("--repetition-penalty", type=float, default=1.0)
+    p.add_argument("--seed", type=int, default=0)
     p.add_argument("--kv-state", action="store_true",
                    help="time saving and restoring the cache state of a --ctx-token sequence (k2_kv_save / "
                         "k2_kv_load, pinned host memory) instead of decoding")
@@ -305,6 +313,10 @@ def run_ours(args, world, rank, local, pg):
     cfg = k2.make_config(s, max_context=budget, max_batch=1, kv_dtype=args.kv)
     ctx = k2.Context(cfg, random_device_weights(s, seed=1234 + rank))
     stream = torch.cuda.Stream()
+    sampled = args.temperature > 0
+    if sampled:
+        ctx.set_sampling(k2.sampling(temperature=args.temperature, top_k=args.top_k, top_p=args.top_p,
+                                     min_p=args.min_p, repetition_penalty=args.repetition_penalty, seed=args.seed))
     tok = torch.zeros(1, dtype=torch.int32, device="cuda")
     prompt = torch.from_numpy(ki.prompt_ids(s.vocab, args.ctx, seed=1 + rank)).cuda()
     # prefill: one untimed warm-up on a short prompt, then the timed prompt
@@ -372,7 +384,7 @@ def run_ours(args, world, rank, local, pg):
         k_name, k_desc, k_bytes = "mega_decode", "mega_decode_kernel (whole decode step)", by["step_launch"]
         k_ms = ms_k["step"] / n_k["step"]
         src = [os.path.join(csrc, f) for f in ("k2_mega.cu", "k2_common.cuh", "k2_kernels.h")]
-        launches_per_step = 1
+        launches_per_step = 2 if sampled else 1  # the step, and the sampler when sampling
     else:
         k_name, k_desc, k_bytes = "gemv_gate_up", "gemv_gate_up (norm + gate/up GEMV + SwiGLU)", by["gate_up_launch"]
         k_ms = ms_k["gate_up"] / max(1, n_k["gate_up"])
@@ -412,8 +424,12 @@ def run_ours(args, world, rank, local, pg):
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD if (args.kv == "f16" and args.ctx == CTX) else
-                   f"k2-horizon-3.7b-shape greedy decode, batch 1, context {args.ctx}, {args.kv} KV, bf16 weights",
+        "config": {"workload": WORKLOAD if (args.kv == "f16" and args.ctx == CTX and not sampled) else
+                   f"k2-horizon-3.7b-shape {'sampled' if sampled else 'greedy'} decode, batch 1, context {args.ctx}, "
+                   f"{args.kv} KV, bf16 weights",
+                   "sampling": ({"temperature": args.temperature, "top_k": args.top_k, "top_p": args.top_p,
+                                 "min_p": args.min_p, "repetition_penalty": args.repetition_penalty,
+                                 "seed": args.seed} if sampled else None),
                    "batch": 1, "context": args.ctx, "layers": s.n_layers,
                    "kv_dtype": args.kv, "activations": "fp32", "cuda_graph": True,
                    "persistent_kernel": persistent, "pdl": not persistent,

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libk2.so")
-SOURCES = ["k2_capi.cu", "k2_gemv.cu", "k2_gemv_packed.cu", "k2_attn.cu", "k2_misc.cu", "k2_noalloc.cu", "k2_mega.cu",
+SOURCES = ["k2_capi.cu", "k2_sample.cu", "k2_gemv.cu", "k2_gemv_packed.cu", "k2_attn.cu", "k2_misc.cu", "k2_noalloc.cu", "k2_mega.cu",
            "k2_tcgemm.cu", "k2_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-cudart", "shared",

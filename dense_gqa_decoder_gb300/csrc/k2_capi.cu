@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 #include <stddef.h>
+#include <cmath>
 #include <cstring>
 
 #include <algorithm>
@@ -39,6 +40,7 @@ int elt_bytes(int dt) { return dt == K2_F32 ? 4 : (dt == K2_BF16 || dt == K2_F16
 struct Layout {
   size_t seq_len, guard, am_counter, msync, rope, resid, qkv, attn_out, act, am_val, am_idx, attn_part, ltab;
   size_t t_resid, t_qkv, t_attn, t_act, t_part;  // persistent step: (value, tag) activations
+  size_t hist, slog, sscr, sample_row;             // token history, sampling logits and scratch
   // tensor-core prefill of up to `pchunk` tokens at a time (bf16 weights)
   int pchunk;
   size_t px, pxh, pxl, pah, pal, pqkv, pq, plog;
@@ -97,6 +99,10 @@ Layout layout_of(const k2_config& c) {
   l.t_attn = take(8 * static_cast<size_t>(s.nq) * s.d);
   l.t_act = take(8 * static_cast<size_t>(s.I));
   l.t_part = take(8 * static_cast<size_t>(s.nkv) * kMegaSplitMax * s.rep * (s.d + 2));
+  l.hist = take(sizeof(int) * static_cast<size_t>(s.B) * l.cap);
+  l.slog = take(sizeof(float) * static_cast<size_t>(s.B) * s.V);
+  l.sample_row = sample_row_bytes(s.V);
+  l.sscr = take(kSampleBarBytes + static_cast<size_t>(s.B) * l.sample_row);
   l.pchunk = c.weight_dtype == K2_BF16 ? static_cast<int>(align_up(std::min(kPrefillChunk, s.ctx), 128)) : 0;
   {
     const size_t P = static_cast<size_t>(l.pchunk);
@@ -183,6 +189,12 @@ struct k2_ctx {
   float *resid = nullptr, *qkv = nullptr, *attn_out = nullptr, *act = nullptr, *attn_part = nullptr,
         *am_val = nullptr;
   int* am_idx = nullptr;
+  int* hist = nullptr;   // [max_batch][cap] token ids of each sequence's cache rows
+  float* slog = nullptr; // [max_batch][vocab] logits of a sampled step without caller logits
+  // sampling (temperature 0: greedy)
+  k2_sampling samp = {};
+  bool sampling = false;
+  std::vector<int> sample_cpr;  // CTAs per row of the sampler, by row count
   // plans
   PackedGemvArgs p_qkv = {}, p_o = {}, p_gu = {}, p_down = {}, p_lm = {};
   int grid_qkv = 0, grid_o = 0, grid_gu = 0, grid_down = 0, grid_lm = 0;
@@ -303,7 +315,10 @@ void chain_b1(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in, int
   cudaStream_t st = ln.s;
   const bool pdl = ln.pdl;
   if (!x_in)
-    ln.run(K2_K_EMBED, [&] { return launch_embed(c->embed, wb, s.V, s.H, tok, 1, x, c->guard, st, pdl); });
+    ln.run(K2_K_EMBED, [&] {
+      return launch_embed(c->embed, wb, s.V, s.H, tok, 1, x, c->guard, c->hist + static_cast<size_t>(seq) * c->lay.cap,
+                          c->lay.cap, c->seq_len + seq, st, pdl);
+    });
   const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
   const int splits = attn_splits(c, 1);
   for (int l = 0; l < s.L; ++l) {
@@ -381,14 +396,47 @@ void enqueue_token(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in
 
 cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int B, int* d_next, float* d_logits);
 
+// The sampler over `rows` rows of logits (k2_sample.cu), with the context's
+// sampling parameters and scratch.
+void enqueue_sample(k2_ctx* c, Launcher& ln, const float* logits, int rows, const int* seen, int seen_stride,
+                    const int* seen_len, const int* pos, int first_seq, int* next) {
+  SampleArgs a = {};
+  a.logits = logits;
+  a.ld = static_cast<size_t>(c->s.V);
+  a.vocab = c->s.V;
+  a.seen = c->samp.repetition_penalty != 1.0f ? seen : nullptr;
+  a.seen_stride = seen_stride;
+  a.seen_len = seen_len;
+  a.counter = pos;
+  a.first_seq = first_seq;
+  a.next = next;
+  a.temperature = c->samp.temperature;
+  a.top_p = c->samp.top_p;
+  a.min_p = c->samp.min_p;
+  a.penalty = c->samp.repetition_penalty;
+  a.top_k = c->samp.top_k;
+  a.key0 = static_cast<uint32_t>(c->samp.seed);
+  a.key1 = static_cast<uint32_t>(c->samp.seed >> 32);
+  a.scratch = c->ws + c->lay.sscr;
+  a.row_bytes = c->lay.sample_row;
+  a.ctas_per_row = c->sample_cpr[rows];
+  a.guard = c->guard;
+  cudaStream_t st = ln.s;
+  ln.run(K2_K_SAMPLE, [&] { return launch_sample(a, rows, st); });
+}
+
 void enqueue_decode(k2_ctx* c, Launcher& ln, const int* d_tokens, int batch, int* d_next, float* d_logits) {
+  // a sampled step needs the logits: the caller's, else scratch
+  float* lg = d_logits ? d_logits : (c->sampling ? c->slog : nullptr);
   if (batch >= 2 && batch <= 16 && c->tc_ok && c->use_tc_decode) {
-    ln.run(K2_K_STEP, [&] { return decode_batched(c, ln.s, d_tokens, batch, d_next, d_logits); });
-    return;
+    ln.run(K2_K_STEP, [&] { return decode_batched(c, ln.s, d_tokens, batch, d_next, lg); });
+  } else {
+    for (int b = 0; b < batch; ++b)
+      enqueue_token(c, ln, b, d_tokens + b, nullptr, d_next + b, lg ? lg + static_cast<size_t>(b) * c->s.V : nullptr,
+                    true);
   }
-  for (int b = 0; b < batch; ++b)
-    enqueue_token(c, ln, b, d_tokens + b, nullptr, d_next + b,
-                  d_logits ? d_logits + static_cast<size_t>(b) * c->s.V : nullptr, true);
+  // the step advanced every length: it is the position each drawn token takes
+  if (c->sampling) enqueue_sample(c, ln, lg, batch, c->hist, c->lay.cap, c->seq_len, c->seq_len, 0, d_next);
 }
 
 bool plan_all(k2_ctx* c) {
@@ -498,6 +546,7 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   MegaArgs& m = c->mega;
   m = {};
   m.layers = dtab;
+  m.hist = c->hist;
   m.n_layers = s.L;
   m.w_qkv = static_cast<const uint8_t*>(c->wqkv(0));
   m.w_o = static_cast<const uint8_t*>(c->wop(0));
@@ -631,7 +680,8 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.guard = c->guard;
     return launch_tc_gemm_sk(mw, mh, ml, g, c->sms, st);
   };
-  cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.wb, X, s.H, s.V, c->guard, st);
+  cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.wb, X, s.H, s.V, c->guard,
+                                    c->hist + static_cast<size_t>(seq) * c->lay.cap, 0, nullptr, pos0, st);
   for (int l = 0; l < s.L && !e; ++l) {
     if (!e) e = launch_norm_rows(X, n, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
     if (!e) e = gemm(c->tmw[4 * l].data(), c->tm_xh.data(), c->tm_xl.data(), s.qkv_n, s.H, TC_STORE, qkv, nullptr,
@@ -686,7 +736,8 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
     return e;
   };
   const int asplits = attn_splits(c, B);
-  cudaError_t e = launch_embed_rows(d_tokens, B, c->embed, s.wb, X, s.H, s.V, c->guard, st);
+  cudaError_t e = launch_embed_rows(d_tokens, B, c->embed, s.wb, X, s.H, s.V, c->guard, c->hist, c->lay.cap,
+                                    c->seq_len, 0, st);
   for (int l = 0; l < s.L && !e; ++l) {
     if (!e) e = launch_norm_rows(X, B, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
     if (!e) e = gemm(c->tmw[4 * l].data(), c->tb_xh.data(), c->tb_xl.data(), s.qkv_n, s.H, TC_STORE, gout, s.qkv_n);
@@ -907,6 +958,8 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   c->am_val = reinterpret_cast<float*>(ws + c->lay.am_val);
   c->am_idx = reinterpret_cast<int*>(ws + c->lay.am_idx);
   c->attn_part = reinterpret_cast<float*>(ws + c->lay.attn_part);
+  c->hist = reinterpret_cast<int*>(ws + c->lay.hist);
+  c->slog = reinterpret_cast<float*>(ws + c->lay.slog);
   c->embed = w->embed;
   c->lm_head = w->lm_head;
   c->final_norm = w->final_norm;
@@ -1009,16 +1062,21 @@ k2_status k2_prefill(k2_ctx* c, int32_t seq, const int32_t* d_tokens, int32_t n,
   if (static_cast<long long>(c->len[seq]) + n > c->s.ctx)
     return c->fail(K2_ERR_CONTEXT_FULL, "prompt of %d tokens does not fit: sequence %d holds %d of %d", n, seq,
                    c->len[seq], c->s.ctx);
-  if (c->tc_ok && c->use_tc && n >= kTcPrefillMin) {
-    const cudaError_t e = prefill_tc(c, seq, d_tokens, n, d_next_token, d_logits, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return c->cuda_fail(e, "tensor-core prefill");
-    c->len[seq] += n;
-    return K2_OK;
-  }
+  float* lg = d_logits ? d_logits : (c->sampling ? c->slog + static_cast<size_t>(seq) * c->s.V : nullptr);
   Launcher ln{c, static_cast<cudaStream_t>(stream), c->pdl};
-  for (int i = 0; i < n; ++i) {
-    const bool last = i == n - 1;
-    enqueue_token(c, ln, seq, d_tokens + i, nullptr, d_next_token, last ? d_logits : nullptr, last);
+  if (c->tc_ok && c->use_tc && n >= kTcPrefillMin) {
+    const cudaError_t e = prefill_tc(c, seq, d_tokens, n, d_next_token, lg, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return c->cuda_fail(e, "tensor-core prefill");
+  } else {
+    for (int i = 0; i < n; ++i) {
+      const bool last = i == n - 1;
+      enqueue_token(c, ln, seq, d_tokens + i, nullptr, d_next_token, last ? lg : nullptr, last);
+    }
+  }
+  if (c->sampling) {
+    ln.pdl = false;
+    enqueue_sample(c, ln, lg, 1, c->hist + static_cast<size_t>(seq) * c->lay.cap, c->lay.cap, c->seq_len + seq,
+                   c->seq_len + seq, seq, d_next_token);
   }
   if (ln.err != cudaSuccess) return c->cuda_fail(ln.err, "prefill launch");
   c->len[seq] += n;
@@ -1304,6 +1362,11 @@ k2_status k2_kv_load(k2_ctx* c, int32_t seq, const void* h_buf, size_t buf_bytes
                        c->s.nkv, true, st);
     }
   }
+  // the saved ids of the cached rows become the sequence's token history
+  const int nh = std::min(h.cached, h.n_tokens);
+  if (!e && nh > 0)
+    e = cudaMemcpyAsync(c->hist + static_cast<size_t>(seq) * c->lay.cap, in + sizeof(StateHeader),
+                        sizeof(int) * static_cast<size_t>(nh), cudaMemcpyHostToDevice, st);
   // the length goes last, from a buffer that outlives the copy (synchronised below)
   static thread_local int v;
   v = h.cached;
@@ -1315,4 +1378,51 @@ k2_status k2_kv_load(k2_ctx* c, int32_t seq, const void* h_buf, size_t buf_bytes
   return K2_OK;
 }
 
+
+k2_status k2_set_sampling(k2_ctx* c, const k2_sampling* p) {
+  if (!c) return K2_ERR_ARG;
+  if (p) {
+    if (!(p->temperature >= 0.f) || !(p->top_p > 0.f && p->top_p <= 1.f) || !(p->min_p >= 0.f && p->min_p <= 1.f) ||
+        !(p->repetition_penalty > 0.f) || p->top_k < 0 || !std::isfinite(p->temperature) ||
+        !std::isfinite(p->repetition_penalty))
+      return c->fail(K2_ERR_ARG,
+                     "sampling needs temperature >= 0, top_k >= 0, top_p in (0, 1], min_p in [0, 1], "
+                     "repetition_penalty > 0 (all finite)");
+  }
+  const bool on = p && p->temperature > 0.f;
+  if (on && c->sample_cpr.empty()) {
+    c->sample_cpr.assign(c->s.B + 1, 0);
+    for (int r = 1; r <= c->s.B; ++r) {
+      c->sample_cpr[r] = sample_ctas_per_row(r);
+      if (c->sample_cpr[r] < 1) return c->fail(K2_ERR_CUDA, "the sampler cannot be launched on this device");
+    }
+  }
+  c->samp = on ? *p : k2_sampling{};
+  c->sampling = on;
+  for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
+  c->graphs.clear();
+  return K2_OK;
+}
+
+k2_status k2_sample_logits(k2_ctx* c, const float* d_logits, int32_t rows, const int32_t* d_seen,
+                           int32_t seen_stride, const int32_t* d_seen_len, const int32_t* d_position,
+                           int32_t first_seq, int32_t* d_next, void* stream) {
+  if (!c) return K2_ERR_ARG;
+  if (!c->sampling) return c->fail(K2_ERR_ARG, "sampling is not set (temperature 0)");
+  if (rows < 1 || rows > c->s.B) return c->fail(K2_ERR_ARG, "rows %d outside [1, %d]", rows, c->s.B);
+  if (!d_logits || !d_position || !d_next || (d_seen && (!d_seen_len || seen_stride < 0)))
+    return c->fail(K2_ERR_ARG, "d_logits, d_position, d_next (and d_seen_len with d_seen) must be non-null");
+  Launcher ln{c, static_cast<cudaStream_t>(stream), false};
+  enqueue_sample(c, ln, d_logits, rows, d_seen, seen_stride, d_seen_len, d_position, first_seq, d_next);
+  if (ln.err != cudaSuccess) return c->cuda_fail(ln.err, "sample launch");
+  return K2_OK;
+}
+
+k2_status k2_philox(uint32_t first, int32_t n, uint32_t c1, uint32_t c2, uint32_t c3, uint64_t key, uint32_t* d_out,
+                    void* stream) {
+  if (n < 0 || (n > 0 && !d_out)) return K2_ERR_ARG;
+  const cudaError_t e = launch_philox(first, n, c1, c2, c3, static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32),
+                                      d_out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? K2_OK : K2_ERR_CUDA;
+}
 }  // extern "C"

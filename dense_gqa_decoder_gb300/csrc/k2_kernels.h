@@ -183,7 +183,38 @@ struct LayerPtrs {
 struct MegaGemv {
   int CT;  // 512-byte chunks per row (the packed layout)
 };
+// ---- sampling (k2_sample.cu) -------------------------------------------------
+constexpr int kSampleThreads = 256;
+constexpr int kSampleBins = 2048;     // radix digits of 11 bits
+constexpr int kSampleCtaMax = 64;     // CTAs per row
+constexpr int kSampleBarBytes = 256;  // the grid-barrier counter, before the rows' scratch
+struct SampleArgs {
+  const float* logits;  // row r at logits + r * ld
+  size_t ld;
+  int vocab;
+  const int* seen;      // row r's seen ids at seen + r * seen_stride (nullable: no penalty)
+  int seen_stride;
+  const int* seen_len;  // [rows]
+  const int* counter;   // [rows]: Philox counter word 0 (the position the token takes)
+  int first_seq;        // counter word 1 = first_seq + r
+  int* next;            // [rows]: the drawn ids
+  float temperature, top_p, min_p, penalty;
+  int top_k;
+  uint32_t key0, key1;  // the seed
+  uint8_t* scratch;     // kSampleBarBytes + rows * row_bytes, zeroed by launch_sample
+  size_t row_bytes;
+  int ctas_per_row;
+  unsigned* guard;
+};
+cudaError_t sample_init_attrs();
+int sample_ctas_per_row(int rows);
+size_t sample_row_bytes(int vocab);
+cudaError_t launch_sample(const SampleArgs& a, int rows, cudaStream_t s);
+cudaError_t launch_philox(uint32_t first, int n, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0, uint32_t k1,
+                          uint32_t* out, cudaStream_t s);
+
 struct MegaArgs {
+  int* hist;  // token history [seq][cap]: the step records its input token at its position (nullable)
   const LayerPtrs* layers;  // device table, n_layers entries (read once per launch: the norm gains)
   int n_layers;
   // packed weights and KV cache of layer l = base + l * stride (bytes)
@@ -249,8 +280,10 @@ cudaError_t launch_mega(const MegaArgs& a, int wbytes, int head_dim, int rep, in
 // ---------------------------------------------------------------------------
 // small kernels
 // ---------------------------------------------------------------------------
+// hist (nullable): the token of block b is recorded at hist[b * hist_stride + pos[b]]
 cudaError_t launch_embed(const void* E, int wbytes, int vocab, int hidden, const int* tokens, int batch,
-                         float* resid, unsigned* guard, cudaStream_t s, bool pdl);
+                         float* resid, unsigned* guard, int* hist, int hist_stride, const int* pos, cudaStream_t s,
+                         bool pdl);
 cudaError_t launch_rope_table(float2* tab, int cap, int head_dim, double theta, cudaStream_t s);
 cudaError_t launch_repack_qkv(void* dst, const void* wq, const void* wk, const void* wv, int wbytes, int nq,
                               int nkv, int d, int hidden, cudaStream_t s);
@@ -287,8 +320,10 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* m
                               cudaStream_t s);
 bool prefill_attn_supported(int head_dim, int rep);
 cudaError_t prefill_init_attrs();
+// hist (nullable): row t's token is recorded at hist[t * hist_stride + pos[t]], or at
+// hist[pos0 + t] when pos is null
 cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbytes, float* X, int H, int vocab,
-                              unsigned* guard, cudaStream_t s);
+                              unsigned* guard, int* hist, int hist_stride, const int* pos, int pos0, cudaStream_t s);
 cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes, __nv_bfloat16* oh,
                              __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s);
 cudaError_t launch_rope_append(const float* qkv, float* Q, const float2* rope, int kv_dtype, void* kc, void* vc,

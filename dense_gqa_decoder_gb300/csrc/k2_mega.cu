@@ -1099,6 +1099,7 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
   const WT* xe = nullptr;
   if (!a.x_ext) {
     const int tok = *a.token_in;
+    if (a.hist && cta == 0 && tid == 0) a.hist[static_cast<size_t>(a.seq) * a.cap + pos] = tok;
     if (tok < 0 || tok >= a.vocab) {
       if (tid == 0) atomicOr(a.guard, GUARD_TOKEN);
       xe = static_cast<const WT*>(a.embed);  // row 0 stands in; the guard reports the fault

@@ -14,11 +14,13 @@ namespace {
 // a zero row instead of an out-of-bounds read.
 template <typename WT>
 __global__ void embed_kernel(const WT* __restrict__ E, int vocab, int hidden, const int* __restrict__ tokens,
-                             float* __restrict__ resid, unsigned* guard) {
+                             float* __restrict__ resid, unsigned* guard, int* hist, int hist_stride,
+                             const int* pos) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
   const int tok = tokens[b];
+  if (hist && threadIdx.x == 0) hist[static_cast<size_t>(b) * hist_stride + pos[b]] = tok;
   float* dst = resid + static_cast<size_t>(b) * hidden;
   if (tok < 0 || tok >= vocab) {
     if (threadIdx.x == 0) atomicOr(guard, GUARD_TOKEN);
@@ -93,14 +95,15 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, bool pdl, cud
 }  // namespace
 
 cudaError_t launch_embed(const void* E, int wbytes, int vocab, int hidden, const int* tokens, int batch,
-                         float* resid, unsigned* guard, cudaStream_t s, bool pdl) {
+                         float* resid, unsigned* guard, int* hist, int hist_stride, const int* pos, cudaStream_t s,
+                         bool pdl) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(batch), dim3(256), s, pdl, attr);
   if (wbytes == 2)
     return cudaLaunchKernelEx(&cfg, embed_kernel<__nv_bfloat16>, static_cast<const __nv_bfloat16*>(E), vocab, hidden,
-                              tokens, resid, guard);
+                              tokens, resid, guard, hist, hist_stride, pos);
   return cudaLaunchKernelEx(&cfg, embed_kernel<float>, static_cast<const float*>(E), vocab, hidden, tokens, resid,
-                            guard);
+                            guard, hist, hist_stride, pos);
 }
 
 cudaError_t launch_rope_table(float2* tab, int cap, int head_dim, double theta, cudaStream_t s) {

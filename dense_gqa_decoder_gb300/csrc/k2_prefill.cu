@@ -26,9 +26,12 @@ __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bflo
 
 template <typename WT>
 __global__ void embed_rows_kernel(const int* __restrict__ tokens, const WT* __restrict__ E, float* __restrict__ X,
-                                  int H, int vocab, unsigned* guard) {
+                                  int H, int vocab, unsigned* guard, int* hist, int hist_stride, const int* pos,
+                                  int pos0) {
   const int t = blockIdx.x;
   int tok = tokens[t];
+  if (hist && threadIdx.x == 0)
+    hist[pos ? static_cast<size_t>(t) * hist_stride + pos[t] : static_cast<size_t>(pos0) + t] = tok;
   if (tok < 0 || tok >= vocab) {
     if (threadIdx.x == 0) atomicOr(guard, GUARD_TOKEN);
     tok = 0;
@@ -630,11 +633,13 @@ cudaError_t prefill_init_attrs() {
 }
 
 cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbytes, float* X, int H, int vocab,
-                              unsigned* guard, cudaStream_t s) {
+                              unsigned* guard, int* hist, int hist_stride, const int* pos, int pos0, cudaStream_t s) {
   if (wbytes == 2)
-    embed_rows_kernel<<<n, 256, 0, s>>>(tokens, static_cast<const __nv_bfloat16*>(E), X, H, vocab, guard);
+    embed_rows_kernel<<<n, 256, 0, s>>>(tokens, static_cast<const __nv_bfloat16*>(E), X, H, vocab, guard, hist,
+                                        hist_stride, pos, pos0);
   else
-    embed_rows_kernel<<<n, 256, 0, s>>>(tokens, static_cast<const float*>(E), X, H, vocab, guard);
+    embed_rows_kernel<<<n, 256, 0, s>>>(tokens, static_cast<const float*>(E), X, H, vocab, guard, hist, hist_stride,
+                                        pos, pos0);
   return cudaGetLastError();
 }
 

@@ -19,7 +19,7 @@ K2_OK, K2_ERR_ARG, K2_ERR_SHAPE, K2_ERR_UNSUPPORTED, K2_ERR_TOKEN_RANGE, K2_ERR_
 K2_STATE_HEADER_BYTES = 96
 K2_F32, K2_BF16, K2_F16, K2_I8 = range(4)
 K2_OPT_PDL, K2_OPT_GRAPH, K2_OPT_ATTN_SPLITS, K2_OPT_PERSISTENT, K2_OPT_TC_PREFILL, K2_OPT_TC_DECODE = range(6)
-KERNEL_CLASSES = ("embed", "qkv", "attn", "o_proj", "gate_up", "down", "lm_head", "step")
+KERNEL_CLASSES = ("embed", "qkv", "attn", "o_proj", "gate_up", "down", "lm_head", "step", "sample")
 DTYPES = {"f32": K2_F32, "bf16": K2_BF16, "f16": K2_F16, "i8": K2_I8}
 
 
@@ -50,6 +50,16 @@ class Info(C.Structure):
                 ("scratch_bytes", C.c_int64), ("persistent_grid", C.c_int32), ("persistent_splits", C.c_int32)]
 
 
+class Sampling(C.Structure):
+    _fields_ = [("temperature", C.c_float), ("top_k", C.c_int32), ("top_p", C.c_float), ("min_p", C.c_float),
+                ("repetition_penalty", C.c_float), ("seed", C.c_uint64)]
+
+
+def sampling(temperature=0.0, top_k=0, top_p=1.0, min_p=0.0, repetition_penalty=1.0, seed=0) -> Sampling:
+    return Sampling(temperature=temperature, top_k=top_k, top_p=top_p, min_p=min_p,
+                    repetition_penalty=repetition_penalty, seed=seed)
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libk2.so is not built ({LIB_PATH}); run dense_gqa_decoder_gb300.build")
@@ -78,6 +88,9 @@ def _load():
         "k2_kv_save": (C.c_int, [vp, i32, vp, i32, vp, C.c_size_t, C.POINTER(C.c_size_t), vp]),
         "k2_kv_peek": (C.c_int, [C.POINTER(Config), vp, C.c_size_t, C.POINTER(i32), C.POINTER(i32)]),
         "k2_kv_load": (C.c_int, [vp, i32, vp, C.c_size_t, vp, i32, vp]),
+        "k2_set_sampling": (C.c_int, [vp, C.POINTER(Sampling)]),
+        "k2_sample_logits": (C.c_int, [vp, vp, i32, vp, i32, vp, vp, i32, vp, vp]),
+        "k2_philox": (C.c_int, [C.c_uint32, i32, C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint64, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -90,7 +103,8 @@ LIB = _load()
 EXPORTED = ("k2_workspace_bytes", "k2_init_weights", "k2_free", "k2_last_error", "k2_get_info", "k2_prefill",
             "k2_decode_step", "k2_decode_layers", "k2_kv_reset", "k2_kv_set_len", "k2_kv_view", "k2_hidden_view",
             "k2_sync_status", "k2_clear_status", "k2_set_option", "k2_profile_decode", "k2_greedy_head_noalloc",
-            "k2_kv_state_bytes", "k2_kv_save", "k2_kv_peek", "k2_kv_load")
+            "k2_kv_state_bytes", "k2_kv_save", "k2_kv_peek", "k2_kv_load", "k2_set_sampling", "k2_sample_logits",
+            "k2_philox")
 
 
 def _ptr(t):
@@ -200,6 +214,18 @@ class Context:
     def set_option(self, opt, value):
         self._check(LIB.k2_set_option(self.ctx, opt, value))
 
+    def set_sampling(self, params=None):
+        """k2_set_sampling: a Sampling (see sampling()) or None for greedy."""
+        self._check(LIB.k2_set_sampling(self.ctx, C.byref(params) if params is not None else None))
+
+    def sample_logits(self, logits, rows, positions, next_tokens, seen=None, seen_len=None, first_seq=0,
+                      stream=None):
+        """k2_sample_logits on device tensors: logits [rows, vocab] fp32, positions
+        and next_tokens [rows] int32, seen [rows, stride] / seen_len [rows] int32."""
+        stride = seen.shape[-1] if seen is not None else 0
+        self._check(LIB.k2_sample_logits(self.ctx, _ptr(logits), rows, _ptr(seen), stride, _ptr(seen_len),
+                                         _ptr(positions), first_seq, _ptr(next_tokens), _stream(stream)))
+
     def kv_state_bytes(self, seq, n_tokens=0):
         n = C.c_size_t()
         st = LIB.k2_kv_state_bytes(self.ctx, seq, n_tokens, C.byref(n))
@@ -241,6 +267,16 @@ def greedy_head_noalloc(cfg: Config, lm_head, final_norm, x, logits, token, stre
     """k2_greedy_head_noalloc: returns the k2 status (no context, no workspace)."""
     return LIB.k2_greedy_head_noalloc(C.byref(cfg), _ptr(lm_head), _ptr(final_norm), _ptr(x), _ptr(logits),
                                       _ptr(token), _stream(stream))
+
+
+def philox(first: int, n: int, c1=0, c2=0, c3=0, key=0, stream=None) -> torch.Tensor:
+    """k2_philox: [n, 4] uint32 words (as int64) of Philox4x32-10 for counters
+    (first + i, c1, c2, c3) under the 64-bit key."""
+    out = torch.empty(4 * n, dtype=torch.int32, device="cuda")
+    st = LIB.k2_philox(first, n, c1, c2, c3, key, _ptr(out), _stream(stream))
+    if st != K2_OK:
+        raise K2Error(st, "k2_philox failed")
+    return out.view(n, 4).cpu().to(torch.int64) & 0xFFFFFFFF
 
 
 def peek_state(cfg: Config, state) -> tuple:

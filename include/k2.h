@@ -184,6 +184,61 @@ k2_status k2_kv_set_len(k2_ctx* ctx, int32_t seq, int32_t len, void* stream);
 k2_status k2_kv_view(k2_ctx* ctx, int32_t layer, int32_t seq, void** k, void** v, void** k_scale, void** v_scale,
                      int32_t* len);
 
+/* ---- sampling ------------------------------------------------------------------
+ *
+ * The pages' generation knobs (k2-burn README, "Sampling + greedy
+ * generation"): temperature 0 is the greedy argmax of k2_decode_step and
+ * k2_prefill, unchanged; temperature > 0 draws the next token instead, with
+ * top-k / top-p / min-p truncation, a repetition penalty and a seed.  For a
+ * row of logits l (fp32, one per vocabulary entry), in this order:
+ *   1. repetition penalty r (1 = off): each DISTINCT id among the sequence's
+ *      tokens so far (the prompt and every decode input, i.e. the rows of its
+ *      cache) has l -> l / r if l > 0, l * r otherwise;
+ *   2. z = l / temperature; z_max their maximum (NaN logits are excluded);
+ *   3. top-k (0 = off): keep z >= the k-th largest z (ties at it all kept);
+ *   4. weights w = exp(z - z_max) (fp32, computed by the library's own exp so
+ *      that it is reproducible), masses m = floor(w * 2^32) of the top-k
+ *      survivors, W their sum;
+ *   5. top-p (1 = off): keep the tokens whose strictly heavier survivors weigh
+ *      less than top_p * W (the smallest most-probable set reaching top_p;
+ *      tied weights are kept or dropped together);
+ *   6. min-p (0 = off): keep w >= min_p (the probability relative to the top one);
+ *   7. draw: x = Philox4x32-10(counter = (position the token will take,
+ *      sequence index, 0, 0), key = (seed low 32 bits, seed high 32 bits)),
+ *      u = (x[0] >> 8) / 2^24; the token is the first index, in vocabulary
+ *      order, whose running sum of kept masses exceeds floor(u * total).
+ * Draws depend only on (seed, sequence, position) and the logits, so a
+ * resumed sequence (k2_kv_load) continues with the same draws. */
+typedef struct {
+  float temperature;        /* 0 = greedy (the default) */
+  int32_t top_k;            /* 0 = off */
+  float top_p;              /* (0, 1]; 1 = off */
+  float min_p;              /* [0, 1]; 0 = off */
+  float repetition_penalty; /* > 0; 1 = off */
+  uint64_t seed;
+} k2_sampling;
+
+/* Sets the sampling of this context's decode steps and prefills (NULL or
+ * temperature 0: greedy).  The logits of a sampled step are written to d_logits
+ * when the call passes one, else to workspace scratch.  Recorded decode graphs
+ * are dropped. */
+k2_status k2_set_sampling(k2_ctx* ctx, const k2_sampling* params);
+
+/* The sampler alone, with this context's sampling parameters, on caller
+ * logits d_logits [rows][vocab] (rows <= max_batch): row r draws into
+ * d_next[r] with counter (d_position[r], first_seq + r); its repetition
+ * penalty covers d_seen[r * seen_stride .. + d_seen_len[r]) (d_seen NULL: no
+ * penalty).  All pointers are device memory.  K2_ERR_ARG if sampling is not
+ * set (temperature 0). */
+k2_status k2_sample_logits(k2_ctx* ctx, const float* d_logits, int32_t rows, const int32_t* d_seen,
+                           int32_t seen_stride, const int32_t* d_seen_len, const int32_t* d_position,
+                           int32_t first_seq, int32_t* d_next, void* stream);
+
+/* The sampler's generator: d_out[4 * i + w] = word w of Philox4x32-10 with
+ * counter (first + i, c1, c2, c3) and key (key low, key high), i < n. */
+k2_status k2_philox(uint32_t first, int32_t n, uint32_t c1, uint32_t c2, uint32_t c3, uint64_t key, uint32_t* d_out,
+                    void* stream);
+
 /* ---- saved cache state ------------------------------------------------------
  *
  * A sequence's cache can be written to host memory and restored later, into
@@ -227,8 +282,10 @@ k2_status k2_kv_save(k2_ctx* ctx, int32_t seq, const int32_t* h_tokens, int32_t 
 k2_status k2_kv_peek(const k2_config* cfg, const void* h_buf, size_t buf_bytes, int32_t* cached, int32_t* n_tokens);
 
 /* Restores a state into sequence seq (its previous rows are replaced), sets
- * its length to the saved row count and copies the saved token ids into
- * h_tokens (host, max_tokens entries; nullable when max_tokens = 0).
+ * its length to the saved row count, takes the first min(n_tokens, rows)
+ * saved ids as the sequence's token history (what the repetition penalty
+ * counts as seen), and copies the saved token ids into h_tokens (host,
+ * max_tokens entries; nullable when max_tokens = 0).
  * Enqueued on `stream`, then waited for.  Before anything is changed:
  * K2_ERR_STATE for a state of another architecture or KV format or a damaged
  * one, K2_ERR_CONTEXT_FULL if its rows do not fit this context's
@@ -266,8 +323,11 @@ typedef enum {
 k2_status k2_set_option(k2_ctx* ctx, int32_t option, int64_t value);
 
 /* Kernel classes timed by k2_profile_decode. */
-enum { K2_K_EMBED = 0, K2_K_QKV, K2_K_ATTN, K2_K_OPROJ, K2_K_GATEUP, K2_K_DOWN, K2_K_LMHEAD, K2_K_STEP, K2_K_COUNT };
-/* K2_K_STEP: a whole token run by the persistent kernel */
+enum {
+  K2_K_EMBED = 0, K2_K_QKV, K2_K_ATTN, K2_K_OPROJ, K2_K_GATEUP, K2_K_DOWN, K2_K_LMHEAD, K2_K_STEP, K2_K_SAMPLE,
+  K2_K_COUNT
+};
+/* K2_K_STEP: a whole token run by the persistent kernel; K2_K_SAMPLE: the sampler */
 
 /* One decode step (as k2_decode_step) launched without graph or PDL, with a
  * CUDA event pair around every kernel; all launches are queued first, then the

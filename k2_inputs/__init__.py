@@ -197,6 +197,21 @@ def weight(s: ModelShape, name: str, layer: int = -1, seed: int = 0,
     return Tensor(stored=stored.reshape(shape), values=values.reshape(shape))
 
 
+def logit_rows(rows: int, vocab: int, seed: int, scale: float = 3.0, ties: int = 0, neg_inf: int = 0,
+               nan: int = 0) -> np.ndarray:
+    """Synthetic fp32 logit rows [rows, vocab], N(0, scale^2) per entry; in each
+    row `ties` more entries copy the row's largest value and `neg_inf` / `nan`
+    entries are set to -inf / NaN (their positions drawn from the same seed)."""
+    out = normal_f32(seed, 9, rows * vocab).reshape(rows, vocab) * np.float32(scale)
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 10])))
+    for r in range(rows):
+        pick = g.permutation(vocab)[:ties + neg_inf + nan]
+        out[r, pick[:ties]] = out[r].max()
+        out[r, pick[ties:ties + neg_inf]] = -np.inf
+        out[r, pick[ties + neg_inf:]] = np.nan
+    return out.astype(np.float32)
+
+
 def prompt_ids(vocab: int, n: int, seed: int = 1) -> np.ndarray:
     g = np.random.Generator(np.random.PCG64(seed))
     return g.integers(0, vocab, size=n, dtype=np.int64).astype(np.int32)
