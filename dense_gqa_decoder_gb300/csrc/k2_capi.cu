@@ -1393,8 +1393,11 @@ k2_status k2_set_sampling(k2_ctx* c, const k2_sampling* p) {
   if (on && c->sample_cpr.empty()) {
     c->sample_cpr.assign(c->s.B + 1, 0);
     for (int r = 1; r <= c->s.B; ++r) {
-      c->sample_cpr[r] = sample_ctas_per_row(r);
-      if (c->sample_cpr[r] < 1) return c->fail(K2_ERR_CUDA, "the sampler cannot be launched on this device");
+      c->sample_cpr[r] = sample_ctas_per_row(r, c->s.V);
+      if (c->sample_cpr[r] < 1) {
+        c->sample_cpr.clear();
+        return c->fail(K2_ERR_UNSUPPORTED, "the sampler cannot hold %d rows of a %d-token vocabulary", r, c->s.V);
+      }
     }
   }
   c->samp = on ? *p : k2_sampling{};

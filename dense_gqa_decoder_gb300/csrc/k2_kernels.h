@@ -188,6 +188,7 @@ constexpr int kSampleThreads = 256;
 constexpr int kSampleBins = 2048;     // radix digits of 11 bits
 constexpr int kSampleCtaMax = 64;     // CTAs per row
 constexpr int kSampleBarBytes = 256;  // the grid-barrier counter, before the rows' scratch
+constexpr int kSampleSmemMax = 160 * 1024;  // z of one CTA's vocabulary slice
 struct SampleArgs {
   const float* logits;  // row r at logits + r * ld
   size_t ld;
@@ -206,8 +207,7 @@ struct SampleArgs {
   int ctas_per_row;
   unsigned* guard;
 };
-cudaError_t sample_init_attrs();
-int sample_ctas_per_row(int rows);
+int sample_ctas_per_row(int rows, int vocab);  // 0: the vocabulary does not fit
 size_t sample_row_bytes(int vocab);
 cudaError_t launch_sample(const SampleArgs& a, int rows, cudaStream_t s);
 cudaError_t launch_philox(uint32_t first, int n, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0, uint32_t k1,

@@ -136,46 +136,53 @@ __device__ bool grid_barrier(unsigned* bar, unsigned n, unsigned G, unsigned* gu
   return ok != 0;
 }
 
-// Warp 0 picks the digit: from the highest bin down, the first whose
-// cumulative value (plus `above`) reaches `need` by `reached`; returns the
-// digit and, in *above_out, the value of the bins above it.  Every CTA calls
-// it on the same merged bins and gets the same answer.
+// Warp 0 finds the digit: from the highest bin down, the first at which the
+// running value (plus `above`) satisfies `reached`; *above_out = the value of
+// the bins above it.  Three levels (groups of bins, sub-groups, bins), each a
+// suffix scan over the lanes; every CTA runs it on the same merged bins.
 template <typename T, typename Reached>
 __device__ int pick_digit(const T* bins, int nbins, T above, Reached reached, T* above_out) {
   __shared__ int dsel;
   __shared__ T asel;
-  const int lane = threadIdx.x & 31;
   if (threadIdx.x < 32) {
-    const int per = nbins / 32;  // bins lane * per .. lane * per + per - 1, lane 31 the highest
-    T own = 0;
-    for (int b = 0; b < per; ++b) own += bins[lane * per + b];
-    // inclusive suffix over lanes (lane 31 first)
-    T suf = own;
+    const int lane = threadIdx.x;
+    int lo = 0, n = nbins;
+    T acc = above;
+    int d = 0;
+    bool found = false;
+    while (true) {
+      const int q = n > 32 ? n / 32 : 1;  // bins per lane at this level
+      T own = 0;
+      if (n > 32) {
+        for (int b = 0; b < q; ++b) own += bins[lo + lane * q + (b + lane) % q];  // rotated: no bank conflicts
+      } else if (lane < n) {
+        own = bins[lo + lane];
+      }
+      T suf = own;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const T v = __shfl_down_sync(0xffffffffu, suf, o);
-      if (lane + o < 32) suf += v;
+      for (int o = 1; o < 32; o <<= 1) {
+        const T v = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += v;
+      }
+      const T excl = suf - own;  // the bins of higher lanes
+      const unsigned m = __ballot_sync(0xffffffffu, reached(acc + suf) && !reached(acc + excl));
+      if (m == 0) break;  // nothing reaches (not for consistent bins)
+      const int hl = 31 - __clz(m);
+      acc += __shfl_sync(0xffffffffu, excl, hl);
+      lo += hl * q;
+      if (q == 1) {
+        d = lo;
+        found = true;
+        break;
+      }
+      n = q;
     }
-    const T excl = suf - own;  // bins of higher lanes
-    const bool hit = reached(above + suf) && !reached(above + excl);
-    const unsigned m = __ballot_sync(0xffffffffu, hit);
-    const int hl = m ? 31 - __clz(m) : 0;  // the highest lane whose range crosses
-    if (lane == hl) {
-      T acc = above + excl;
-      int d = -1;
-      for (int b = per - 1; b >= 0; --b) {
-        const T v = bins[lane * per + b];
-        if (reached(acc + v)) {
-          d = lane * per + b;
-          break;
-        }
-        acc += v;
-      }
-      if (d < 0) {  // nothing reaches (not for consistent bins): the lowest bin, keep everything
-        d = 0;
-        acc = above;
-        for (int b = 1; b < nbins; ++b) acc += bins[b];
-      }
+    if (!found) {  // the lowest bin, keeping everything
+      d = 0;
+      acc = above;
+      for (int b = 1; b < nbins; ++b) acc += bins[b];
+    }
+    if (lane == 0) {
       dsel = d;
       asel = acc;
     }
@@ -186,7 +193,8 @@ __device__ int pick_digit(const T* bins, int nbins, T above, Reached reached, T*
 }
 
 __global__ void __launch_bounds__(ST) sample_kernel(const SampleArgs a) {
-  __shared__ unsigned hc[NB];  // this CTA's histogram, then the merged one
+  extern __shared__ float zs[];  // z of this CTA's slice of the vocabulary
+  __shared__ unsigned hc[NB];    // this CTA's histogram, then the merged one
   __shared__ u64 hm[NB];
   __shared__ float redf[ST / 32];
   __shared__ u64 redu[ST / 32];
@@ -202,8 +210,38 @@ __global__ void __launch_bounds__(ST) sample_kernel(const SampleArgs a) {
   unsigned* bar = reinterpret_cast<unsigned*>(a.scratch);
   const int s0 = static_cast<int>((static_cast<long long>(V) * j / cpr) & ~31LL);
   const int s1 = j == cpr - 1 ? V : static_cast<int>((static_cast<long long>(V) * (j + 1) / cpr) & ~31LL);
+  const int ns = s1 - s0;
   unsigned nbar = 0;
   const bool pen = a.seen != nullptr && a.penalty != 1.0f;
+  const bool topk = a.top_k > 0 && a.top_k < V;
+  const bool topp = a.top_p < 1.0f;
+
+  // merged bins of pass p into shared memory, after the barrier
+  auto merge_counts = [&](int p) -> bool {
+    unsigned* gc = rs.cnt + p * NB;
+    for (int b = tid; b < NB; b += ST)
+      if (hc[b]) atomicAdd(gc + b, hc[b]);
+    if (!grid_barrier(bar, ++nbar, G, a.guard)) return false;
+    for (int b = tid; b < NB; b += ST) hc[b] = __ldcg(gc + b);
+    __syncthreads();
+    return true;
+  };
+  auto merge_masses = [&](int p) -> bool {
+    u64* gm = rs.mass + p * NB;
+    for (int b = tid; b < NB; b += ST)
+      if (hm[b]) atomicAdd(gm + b, hm[b]);
+    if (!grid_barrier(bar, ++nbar, G, a.guard)) return false;
+    for (int b = tid; b < NB; b += ST) hm[b] = __ldcg(gm + b);
+    __syncthreads();
+    return true;
+  };
+  auto clear_bins = [&]() {
+    for (int b = tid; b < NB; b += ST) {
+      hc[b] = 0;
+      hm[b] = 0;
+    }
+    __syncthreads();
+  };
 
   // 1. the row's seen ids
   if (pen) {
@@ -215,17 +253,26 @@ __global__ void __launch_bounds__(ST) sample_kernel(const SampleArgs a) {
     }
     if (!grid_barrier(bar, ++nbar, G, a.guard)) return;
   }
-  auto zval = [&](int i) {
-    float l = __ldcg(lg + i);
-    if (!(l == l)) return -INFINITY;
-    if (pen && ((__ldcg(rs.bitmap + (i >> 5)) >> (i & 31)) & 1u)) l = l > 0.f ? l / a.penalty : l * a.penalty;
-    return l / a.temperature;
-  };
 
-  // 2. the maximum of z
+  // 2. z of the slice (kept in shared memory), its maximum, and the first
+  // top-k histogram (digit 0 of the order key)
+  clear_bins();
   {
     float mz = -INFINITY;
-    for (int i = s0 + tid; i < s1; i += ST) mz = fmaxf(mz, zval(i));
+    for (int t = tid; t < ns; t += ST) {
+      const int i = s0 + t;
+      float l = __ldcg(lg + i);
+      float z;
+      if (!(l == l)) {
+        z = -INFINITY;
+      } else {
+        if (pen && ((__ldcg(rs.bitmap + (i >> 5)) >> (i & 31)) & 1u)) l = l > 0.f ? l / a.penalty : l * a.penalty;
+        z = l / a.temperature;
+      }
+      zs[t] = z;
+      mz = fmaxf(mz, z);
+      if (topk) atomicAdd(&hc[(okey(z) >> dshift(0)) & dmask(0)], 1u);
+    }
     mz = warp_max(mz);
     if (lane == 0) redf[warp] = mz;
     __syncthreads();
@@ -234,32 +281,32 @@ __global__ void __launch_bounds__(ST) sample_kernel(const SampleArgs a) {
       for (int w = 1; w < ST / 32; ++w) t = fmaxf(t, redf[w]);
       atomicMax(rs.zmax, okey(t));
     }
-    if (!grid_barrier(bar, ++nbar, G, a.guard)) return;
+  }
+  if (topk) {
+    if (!merge_counts(0)) return;
+  } else if (!grid_barrier(bar, ++nbar, G, a.guard)) {
+    return;
   }
   const float zmax = okey_inv(__ldcg(rs.zmax));
 
   // 3. top-k: the key of the k-th largest z
   uint32_t kkey = 0;
-  if (a.top_k > 0 && a.top_k < V) {
+  if (topk) {
     uint32_t prefix = 0, mask = 0;
     unsigned need = static_cast<unsigned>(a.top_k);
     for (int p = 0; p < 3; ++p) {
-      for (int b = tid; b < NB; b += ST) hc[b] = 0;
-      __syncthreads();
-      for (int i = s0 + tid; i < s1; i += ST) {
-        const uint32_t k = okey(zval(i));
-        if ((k & mask) == prefix) atomicAdd(&hc[(k >> dshift(p)) & dmask(p)], 1u);
+      if (p > 0) {
+        clear_bins();
+        for (int t = tid; t < ns; t += ST) {
+          const uint32_t k = okey(zs[t]);
+          if ((k & mask) == prefix) atomicAdd(&hc[(k >> dshift(p)) & dmask(p)], 1u);
+        }
+        __syncthreads();
+        if (!merge_counts(p)) return;
       }
-      __syncthreads();
-      unsigned* gc = rs.cnt + p * NB;
-      for (int b = tid; b < NB; b += ST)
-        if (hc[b]) atomicAdd(gc + b, hc[b]);
-      if (!grid_barrier(bar, ++nbar, G, a.guard)) return;
-      for (int b = tid; b < NB; b += ST) hc[b] = __ldcg(gc + b);
-      __syncthreads();
       unsigned above = 0;
-      const int nb = static_cast<int>(dmask(p)) + 1;
-      const int d = pick_digit<unsigned>(hc, nb, 0u, [&](unsigned v) { return v >= need; }, &above);
+      const int d = pick_digit<unsigned>(hc, static_cast<int>(dmask(p)) + 1, 0u,
+                                         [&](unsigned v) { return v >= need; }, &above);
       need -= above;
       prefix |= static_cast<uint32_t>(d) << dshift(p);
       mask |= dmask(p) << dshift(p);
@@ -267,52 +314,37 @@ __global__ void __launch_bounds__(ST) sample_kernel(const SampleArgs a) {
     kkey = prefix;
   }
 
-  // 4. the total mass of the top-k survivors
-  u64 W = 0;
-  {
-    u64 acc = 0;
-    for (int i = s0 + tid; i < s1; i += ST) {
-      const float z = zval(i);
-      if (okey(z) >= kkey) acc += wmass(exp_neg(z - zmax));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) redu[warp] = acc;
-    __syncthreads();
-    if (tid == 0) {
-      u64 t = 0;
-      for (int w = 0; w < ST / 32; ++w) t += redu[w];
-      atomicAdd(rs.wsum, t);
-    }
-    if (!grid_barrier(bar, ++nbar, G, a.guard)) return;
-    W = __ldcg(rs.wsum);
-  }
-
-  // 5. top-p: the smallest weight key whose strictly heavier mass is below top_p * W
+  // 4./5. top-p over the weights of the top-k survivors; the first pass's
+  // merged bins also give their total W
   uint32_t pkey = 0;
-  if (a.top_p < 1.0f) {
-    const double target = static_cast<double>(a.top_p) * static_cast<double>(W);
+  if (topp) {
     uint32_t prefix = 0, mask = 0;
     u64 above = 0;
+    double target = 0.0;
     for (int p = 0; p < 3; ++p) {
-      for (int b = tid; b < NB; b += ST) hm[b] = 0;
-      __syncthreads();
-      for (int i = s0 + tid; i < s1; i += ST) {
-        const float z = zval(i);
+      clear_bins();
+      for (int t = tid; t < ns; t += ST) {
+        const float z = zs[t];
         if (okey(z) < kkey) continue;
         const float w = exp_neg(z - zmax);
         const uint32_t k = __float_as_uint(w);
         if ((k & mask) == prefix) atomicAdd(&hm[(k >> dshift(p)) & dmask(p)], wmass(w));
       }
       __syncthreads();
-      u64* gm = rs.mass + p * NB;
-      for (int b = tid; b < NB; b += ST)
-        if (hm[b]) atomicAdd(gm + b, hm[b]);
-      if (!grid_barrier(bar, ++nbar, G, a.guard)) return;
-      for (int b = tid; b < NB; b += ST) hm[b] = __ldcg(gm + b);
-      __syncthreads();
-      const int nb = static_cast<int>(dmask(p)) + 1;
-      const int d = pick_digit<u64>(hm, nb, above,
+      if (!merge_masses(p)) return;
+      if (p == 0) {
+        u64 t = 0;
+        for (int b = tid; b < NB; b += ST) t += hm[b];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) redu[warp] = t;
+        __syncthreads();
+        u64 W = 0;
+        for (int w = 0; w < ST / 32; ++w) W += redu[w];
+        target = static_cast<double>(a.top_p) * static_cast<double>(W);
+        __syncthreads();
+      }
+      const int d = pick_digit<u64>(hm, static_cast<int>(dmask(p)) + 1, above,
                                     [&](u64 v) { return static_cast<double>(v) >= target; }, &above);
       prefix |= static_cast<uint32_t>(d) << dshift(p);
       mask |= dmask(p) << dshift(p);
@@ -321,8 +353,8 @@ __global__ void __launch_bounds__(ST) sample_kernel(const SampleArgs a) {
   }
 
   // 6./7. the kept masses of this slice, then the draw
-  auto kept_mass = [&](int i) -> u64 {
-    const float z = zval(i);
+  auto kept_mass = [&](int t) -> u64 {
+    const float z = zs[t];
     if (okey(z) < kkey) return 0;
     const float w = exp_neg(z - zmax);
     if (__float_as_uint(w) < pkey || w < a.min_p) return 0;
@@ -330,7 +362,7 @@ __global__ void __launch_bounds__(ST) sample_kernel(const SampleArgs a) {
   };
   {
     u64 acc = 0;
-    for (int i = s0 + tid; i < s1; i += ST) acc += kept_mass(i);
+    for (int t = tid; t < ns; t += ST) acc += kept_mass(t);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) redu[warp] = acc;
@@ -343,9 +375,8 @@ __global__ void __launch_bounds__(ST) sample_kernel(const SampleArgs a) {
     if (!grid_barrier(bar, ++nbar, G, a.guard)) return;
   }
   // every CTA of the row: the total, the draw, the CTA whose slice holds it
-  u64 total = 0, base = 0;
+  u64 total = 0, base = 0, target = 0;
   int owner = -1;
-  u64 target = 0;
   {
     for (int c = 0; c < cpr; ++c) total += __ldcg(rs.part + c);
     const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(a.counter[row]),
@@ -371,33 +402,38 @@ __global__ void __launch_bounds__(ST) sample_kernel(const SampleArgs a) {
     return;
   }
   if (owner != j) return;
-  // tiles of ST indices: an inclusive block scan of the kept masses in order
-  if (tid == 0) found = -1;
-  __syncthreads();
-  for (int t0 = s0; t0 < s1; t0 += ST) {
-    const int i = t0 + tid;
-    const u64 m = i < s1 ? kept_mass(i) : 0;
-    u64 inc = m;
+  // each thread a contiguous run of the slice: one block scan of the runs'
+  // masses, then the thread whose run holds the target walks it
+  {
+    const int per = (ns + ST - 1) / ST;
+    const int t0 = tid * per, t1 = min(ns, t0 + per);
+    u64 own = 0;
+    for (int t = t0; t < t1; ++t) own += kept_mass(t);
+    u64 inc = own;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const u64 v = __shfl_up_sync(0xffffffffu, inc, o);
       if (lane >= o) inc += v;
     }
     if (lane == 31) scan_tot[warp] = inc;
+    if (tid == 0) found = -1;
     __syncthreads();
-    u64 wbase = base;
-    for (int w = 0; w < warp; ++w) wbase += scan_tot[w];
-    const bool hit = (wbase + inc > target) && (wbase + inc - m <= target) && m > 0;
-    if (hit) found = i;  // exactly one index crosses
-    u64 tile = 0;
-    for (int w = 0; w < ST / 32; ++w) tile += scan_tot[w];
+    u64 run = base + inc - own;
+    for (int w = 0; w < warp; ++w) run += scan_tot[w];
+    if (own > 0 && run <= target && target < run + own) {  // exactly one thread
+      for (int t = t0; t < t1; ++t) {
+        run += kept_mass(t);
+        if (run > target) {
+          found = s0 + t;
+          break;
+        }
+      }
+    }
     __syncthreads();
-    if (found >= 0) break;
-    base += tile;
   }
   if (tid == 0) {
     if (found < 0) {
-      atomicOr(a.guard, GUARD_NAN);  // no kept mass: cannot happen for finite logits
+      atomicOr(a.guard, GUARD_NAN);
       found = 0;
     }
     a.next[row] = found;
@@ -406,17 +442,25 @@ __global__ void __launch_bounds__(ST) sample_kernel(const SampleArgs a) {
 
 }  // namespace
 
-cudaError_t sample_init_attrs() { return cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 0); }
+// dynamic shared memory of one CTA: z of its slice (32-aligned bounds)
+size_t sample_smem_bytes(int vocab, int cpr) {
+  return 4 * (static_cast<size_t>((vocab + cpr - 1) / cpr) + 64);
+}
 
-int sample_ctas_per_row(int rows) {
-  int dev = 0, sms = 0, per_sm = 0;
+int sample_ctas_per_row(int rows, int vocab) {
+  int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_kernel, ST, 0) != cudaSuccess) return 0;
-  const int resident = sms * per_sm;
-  int cpr = resident / (rows > 0 ? rows : 1);
-  if (cpr > kSampleCtaMax) cpr = kSampleCtaMax;
-  return cpr;
+  if (cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSampleSmemMax) != cudaSuccess)
+    return 0;
+  for (int cpr = kSampleCtaMax; cpr >= 1; --cpr) {
+    const size_t smem = sample_smem_bytes(vocab, cpr);
+    if (smem > static_cast<size_t>(kSampleSmemMax)) break;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_kernel, ST, smem) != cudaSuccess) return 0;
+    if (per_sm >= 1 && static_cast<long long>(rows) * cpr <= static_cast<long long>(sms) * per_sm) return cpr;
+  }
+  return 0;
 }
 
 size_t sample_row_bytes(int vocab) {
@@ -431,6 +475,7 @@ cudaError_t launch_sample(const SampleArgs& a, int rows, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows * a.ctas_per_row);
   cfg.blockDim = dim3(ST);
+  cfg.dynamicSmemBytes = sample_smem_bytes(a.vocab, a.ctas_per_row);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -441,6 +486,7 @@ cudaError_t launch_sample(const SampleArgs& a, int rows, cudaStream_t s) {
   return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(sample_kernel), args);
 }
 
+namespace {
 // Philox4x32-10 outputs for counters (c, 0, 0, 0), c = first .. first + n - 1,
 // under key (k0, k1): out[4 * i + w] (the generator of the sampler, exposed
 // for its known-answer and cross-implementation checks).
@@ -454,6 +500,8 @@ __global__ void philox_kernel(uint32_t first, int n, uint32_t c1, uint32_t c2, u
   out[4 * i + 2] = x.z;
   out[4 * i + 3] = x.w;
 }
+
+}  // namespace
 
 cudaError_t launch_philox(uint32_t first, int n, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0, uint32_t k1,
                           uint32_t* out, cudaStream_t s) {

@@ -220,8 +220,10 @@ typedef struct {
 
 /* Sets the sampling of this context's decode steps and prefills (NULL or
  * temperature 0: greedy).  The logits of a sampled step are written to d_logits
- * when the call passes one, else to workspace scratch.  Recorded decode graphs
- * are dropped. */
+ * when the call passes one, else to workspace scratch; the sampler is one
+ * cooperative launch after the step.  Recorded decode graphs are dropped.
+ * K2_ERR_ARG for parameters outside the ranges below; K2_ERR_UNSUPPORTED if
+ * max_batch rows of this vocabulary do not fit the device's shared memory. */
 k2_status k2_set_sampling(k2_ctx* ctx, const k2_sampling* params);
 
 /* The sampler alone, with this context's sampling parameters, on caller
