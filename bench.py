@@ -54,6 +54,11 @@ def parse():
     p.add_argument("--min-p", type=float, default=0.0)
     p.add_argument("--repetition-penalty", type=float, default=1.0)
     p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--speculate", type=int, default=0,
+                   help="> 0: greedy decode by k2_decode_speculative with up to this many drafted ids per pass "
+                        "(wall clock; each pass waits for the device)")
+    p.add_argument("--spec-unit", type=int, default=0,
+                   help="with --speculate: the prompt repeats a random unit of this many ids (0: random ids)")
     p.add_argument("--kv-state", action="store_true",
                    help="time saving and restoring the cache state of a --ctx-token sequence (k2_kv_save / "
                         "k2_kv_load, pinned host memory) instead of decoding")
@@ -458,6 +463,61 @@ def run_ours(args, world, rank, local, pg):
         print(json.dumps(line), flush=True)
 
 
+def run_speculative(args, world, rank, local, pg):
+    """Greedy decoding with n-gram drafts verified in one pass: --steps
+    emitted tokens timed after --warmup, from a --ctx-token random prompt."""
+    import torch
+
+    import k2_inputs as ki
+    from dense_gqa_decoder_gb300 import k2
+
+    torch.cuda.set_device(local)
+    s = ki.SHAPES[SHAPE_NAME]
+    if args.layers:
+        s = s.replace(n_layers=args.layers)
+    cfg = k2.make_config(s, max_context=args.ctx + args.warmup + args.steps + 32, max_batch=1, kv_dtype=args.kv)
+    ctx = k2.Context(cfg, random_device_weights(s, seed=1234 + rank))
+    stream = torch.cuda.Stream()
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if args.spec_unit > 0:
+        unit = [int(x) for x in ki.prompt_ids(s.vocab, args.spec_unit, seed=1 + rank)]
+        ids = (unit * (args.ctx // args.spec_unit + 1))[:args.ctx]
+    else:
+        ids = [int(x) for x in ki.prompt_ids(s.vocab, args.ctx, seed=1 + rank)]
+    with torch.cuda.stream(stream):
+        ctx.prefill(0, torch.tensor(ids, dtype=torch.int32, device="cuda"), tok, stream=stream)
+    stream.synchronize()
+    seq = ids + [int(tok.item())]
+    emitted = 0
+    while emitted < args.warmup:
+        got = ctx.decode_speculative(0, seq, args.speculate, stream=stream)
+        seq += got
+        emitted += len(got)
+    t0 = time.perf_counter()
+    emitted, passes = 0, 0
+    while emitted < args.steps:
+        got = ctx.decode_speculative(0, seq, args.speculate, stream=stream)
+        seq += got
+        emitted += len(got)
+        passes += 1
+    dt = time.perf_counter() - t0
+    if ctx.sync_status(stream) != k2.K2_OK:
+        raise RuntimeError("device guard after speculative decoding: " + ctx.last_error())
+    line = {
+        "metric": "speculative greedy decode tok/s (3.7B dense GQA, bf16)", "value": world * emitted / dt,
+        "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"k2-horizon-3.7b-shape greedy decode with up to {args.speculate} n-gram drafts "
+                               f"per pass, batch 1, from a {args.ctx}-token "
+                               + (f"prompt repeating a {args.spec_unit}-id random unit" if args.spec_unit > 0
+                                  else "random prompt") + f", {args.kv} KV",
+                   "layers": s.n_layers, "timing": "wall clock (every pass waits for the device)"},
+        "passes": passes, "tokens_per_pass": emitted / passes, "ms_per_pass": 1e3 * dt / passes,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_kv_state(args, world, rank, local, pg):
     """Save / restore of one sequence's cache: the state of a --ctx-token
     prompt (K/V rows of every layer + header + the prompt's ids) written to
@@ -591,6 +651,8 @@ def main():
         run_reference(args, world, rank, pg)
     elif args.kv_state:
         run_kv_state(args, world, rank, local, pg)
+    elif args.speculate > 0:
+        run_speculative(args, world, rank, local, pg)
     elif args.batch > 1:
         run_batched(args, world, rank, local, pg)
     else:

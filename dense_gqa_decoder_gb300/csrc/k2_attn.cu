@@ -128,9 +128,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.z, g = blockIdx.y, sp = blockIdx.x, ns = gridDim.x;
-  const int seq = a.seq0 + b;
+  const int seq = a.block_mode ? a.block_seq : a.seq0 + b;
   // seq_len was written two or more launches back (see pdl_trigger placement)
-  const int pos = a.seq_len[seq];
+  const int pos = a.block_mode ? a.pos_base + b : a.seq_len[seq];
   if (pos < 0 || pos >= a.cap) {
     if (tid == 0) atomicOr(a.guard, GUARD_POS);
     return;  // every CTA of the launch sees the same pos and leaves before any cluster barrier
@@ -150,7 +150,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   auto issue = [&](int t) {  // lane 0: tile t of this CTA into this warp's slot
     const int j0 = k0 + t * TK;
     const int rows = min(TK, k1 - j0);
-    const int crow = max(0, min(rows, pos - j0));  // cached rows; row pos is the new one
+    // cached rows; row pos is the new one (in block mode it is cached too)
+    const int crow = max(0, min(rows, (a.block_mode ? pos + 1 : pos) - j0));
     const int srow = (crow + 7) & ~7;             // scale copies in 16-byte units
     const uint32_t bytes = 2u * crow * ROWB + (I8 && crow > 0 ? 2u * srow * 2u : 0u);
     if (bytes == 0) {
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
     const __half* vsc = ksc + TK;
     // ---- the new token's K/V: stored format to the cache and into the slot
     const int jr = pos - j0;
-    if (k1 == L && jr >= 0 && jr < rows) {
+    if (!a.block_mode && k1 == L && jr >= 0 && jr < rows) {
       for (int kv = 0; kv < 2; ++kv) {
         const float* src = qkv + (kv == 0 ? a.nq * D : (a.nq + a.nkv) * D) + g * D;
         KVT* dst = reinterpret_cast<KVT*>(kv == 0 ? a.kc_w : a.vc_w) + (head_row + pos) * D;

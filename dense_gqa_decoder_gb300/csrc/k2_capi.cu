@@ -29,6 +29,7 @@ constexpr size_t kLmHeadSmem = 176 * 1024;
 constexpr int kArgmaxPartsMax = 1024;
 constexpr int kPrefillChunk = 2048;  // prompt tokens per tensor-core prefill pass
 constexpr int kTcPrefillMin = 8;     // shorter prompts are appended one decode step per token
+constexpr int kSpecMax = 8;          // drafted ids verified in one pass
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -41,6 +42,7 @@ struct Layout {
   size_t seq_len, guard, am_counter, msync, rope, resid, qkv, attn_out, act, am_val, am_idx, attn_part, ltab;
   size_t t_resid, t_qkv, t_attn, t_act, t_part;  // persistent step: (value, tag) activations
   size_t hist, slog, sscr, sample_row;             // token history, sampling logits and scratch
+  size_t vlog, vids, varg, vpv, vpi;               // speculative verification: logits, ids, argmax
   // tensor-core prefill of up to `pchunk` tokens at a time (bf16 weights)
   int pchunk;
   size_t px, pxh, pxl, pah, pal, pqkv, pq, plog;
@@ -115,6 +117,12 @@ Layout layout_of(const k2_config& c) {
     l.pqkv = take(P * s.qkv_n * 4);
     l.pq = take(P * s.nq * s.d * 4);
     l.plog = take(P > 0 ? static_cast<size_t>(s.B) * s.V * 4 : 0);  // batched-decode logits
+    const size_t nv = P > 0 ? kSpecMax + 1 : 0;
+    l.vlog = take(nv * s.V * 4);
+    l.vids = take(sizeof(int) * (kSpecMax + 1));
+    l.varg = take(sizeof(int) * (kSpecMax + 1));
+    l.vpv = take(nv * kArgmaxPartsMax * 4);
+    l.vpi = take(nv * kArgmaxPartsMax * 4);
   }
   const size_t scratch_end = o;
   l.wqkv_layer = align_up(packed_bytes(s.qkv_n, s.H, s.wb), kAlign);
@@ -666,38 +674,78 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.guard = c->guard;
     return launch_tc_gemm(mw, mh, ml, g, st);
   };
-  auto gemm_sk = [&](const void* mw, const void* mh, const void* ml, int N, int K, float* resid) {
+  // a block of at most 16 tokens (a speculative verification) streams every
+  // weight matrix with the stream-K kernel over 16-token tiles, one CTA per
+  // SM: the 128-token tiles would leave most SMs idle
+  const bool small = n <= 16;
+  const int tt = small ? 16 : 128;
+  auto gemm_sk = [&](const void* mw, const void* mh, const void* ml, int N, int K, int mode, float* out, int ldo) {
     TcGemmArgs g = {};
     g.N = N;
     g.K = K;
     g.T = n;
     g.ksteps = 4 * ((K + 255) / 256);
-    g.mode = TC_RESID;
-    g.ldo = N;
-    g.tile_tokens = 128;
+    g.mode = mode;
+    g.ldo = ldo;
+    g.tile_tokens = tt;
     g.splits = 1;
-    g.out = resid;
+    g.out = out;
     g.guard = c->guard;
-    return launch_tc_gemm_sk(mw, mh, ml, g, c->sms, st);
+    cudaError_t e = cudaSuccess;
+    if (mode == TC_STORE) e = cudaMemsetAsync(out, 0, sizeof(float) * static_cast<size_t>(n) * ldo, st);
+    if (!e) e = launch_tc_gemm_sk(mw, mh, ml, g, c->sms, st);
+    return e;
   };
+  const void* m_xh = small ? c->tb_xh.data() : c->tm_xh.data();
+  const void* m_xl = small ? c->tb_xl.data() : c->tm_xl.data();
+  const void* m_oh = small ? c->tb_oh.data() : c->tm_oh.data();
+  const void* m_ol = small ? c->tb_ol.data() : c->tm_ol.data();
+  const void* m_ah = small ? c->tb_ah.data() : c->tm_ah.data();
+  const void* m_al = small ? c->tb_al.data() : c->tm_al.data();
+  float* O32 = Q + static_cast<size_t>(16) * s.nq * s.d;  // small blocks: the attention output after 16 query rows
   cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.wb, X, s.H, s.V, c->guard,
                                     c->hist + static_cast<size_t>(seq) * c->lay.cap, 0, nullptr, pos0, st);
   for (int l = 0; l < s.L && !e; ++l) {
     if (!e) e = launch_norm_rows(X, n, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
-    if (!e) e = gemm(c->tmw[4 * l].data(), c->tm_xh.data(), c->tm_xl.data(), s.qkv_n, s.H, TC_STORE, qkv, nullptr,
-                     nullptr, s.qkv_n);
+    if (!e)
+      e = small ? gemm_sk(c->tmw[4 * l].data(), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, s.qkv_n)
+                : gemm(c->tmw[4 * l].data(), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, nullptr, nullptr, s.qkv_n);
     if (!e)
       e = launch_rope_append(qkv, Q, c->rope, kvdt, c->kc(l), c->vc(l), c->ks(l), c->vs(l), n, s.nq, s.nkv, s.d,
                              pos0, head_row0, c->lay.cap, st);
-    if (!e)
+    if (!e && small) {
+      // few queries over a long history: the decode attention in block mode
+      // splits every query's keys over a cluster of CTAs
+      AttnArgs at = c->p_attn;
+      at.kc = at.kc_w = c->kc(l);
+      at.vc = at.vc_w = c->vc(l);
+      at.ks = c->ks(l);
+      at.vs = c->vs(l);
+      at.qkv = Q;
+      at.qkv_stride = s.nq * s.d;
+      at.seq0 = 0;
+      at.block_mode = 1;
+      at.block_seq = seq;
+      at.pos_base = pos0;
+      at.out = O32;
+      e = launch_attn(at, s.d, s.rep, kvdt, attn_splits(c, n), n, st, false);
+      if (!e) e = launch_rows_hilo(O32, xh, xl, n, s.nq * s.d, st);
+    } else if (!e) {
       e = launch_prefill_attn(Q, kvdt, c->kc(l), c->vc(l), c->ks(l), c->vs(l), xh, xl, n, s.nq, s.nkv, s.d, pos0,
                               head_row0, c->lay.cap, scale, st);
+    }
     // o_proj and down have few row tiles: stream-K over one CTA per SM
-    if (!e) e = gemm_sk(c->tmw[4 * l + 1].data(), c->tm_oh.data(), c->tm_ol.data(), s.H, s.nq * s.d, X);
+    if (!e) e = gemm_sk(c->tmw[4 * l + 1].data(), m_oh, m_ol, s.H, s.nq * s.d, TC_RESID, X, s.H);
     if (!e) e = launch_norm_rows(X, n, c->mlp_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
-    if (!e) e = gemm(c->tmw[4 * l + 2].data(), c->tm_xh.data(), c->tm_xl.data(), 2 * s.I, s.H, TC_SWIGLU, nullptr,
-                     ah, al, s.I);
-    if (!e) e = gemm_sk(c->tmw[4 * l + 3].data(), c->tm_ah.data(), c->tm_al.data(), s.H, s.I, X);
+    if (!e) {
+      if (small) {  // gate/up rows to fp32 (the QKV buffer is free by now), then SwiGLU rows
+        e = gemm_sk(c->tmw[4 * l + 2].data(), m_xh, m_xl, 2 * s.I, s.H, TC_STORE, qkv, 2 * s.I);
+        if (!e) e = launch_swiglu_rows(qkv, ah, al, n, s.I, st);
+      } else {
+        e = gemm(c->tmw[4 * l + 2].data(), m_xh, m_xl, 2 * s.I, s.H, TC_SWIGLU, nullptr, ah, al, s.I);
+      }
+    }
+    if (!e) e = gemm_sk(c->tmw[4 * l + 3].data(), m_ah, m_al, s.H, s.I, TC_RESID, X, s.H);
   }
   return e;
 }
@@ -796,6 +844,39 @@ cudaError_t prefill_tc(k2_ctx* c, int seq, const int* d_tokens, int n, int* d_ne
   e = launch_packed_gemv(lm, s.wb, EPI_ARGMAX, c->grid_lm, st, false);
   if (e) return e;
   return launch_advance_by(c->seq_len, seq, n, st);
+}
+
+// Appends the n ids at d_tokens (the next input and the drafts) to sequence
+// seq in one tensor-core pass and writes the greedy id after every one of
+// them (kimi-k3-in-c k3_run.c, --spec: batched greedy verification; the
+// logits of every position).  The device length is left to the caller.
+cudaError_t verify_block(k2_ctx* c, int seq, const int* d_tokens, int n, int* d_argmax, cudaStream_t st) {
+  const Sizes& s = c->s;
+  cudaError_t e = prefill_block(c, seq, d_tokens, n, c->len[seq], st);
+  float* X = reinterpret_cast<float*>(c->ws + c->lay.px);
+  auto* xh = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxh);
+  auto* xl = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxl);
+  float* logits = reinterpret_cast<float*>(c->ws + c->lay.vlog);
+  if (!e) e = launch_norm_rows(X, n, c->final_norm, s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
+  if (!e) e = cudaMemsetAsync(logits, 0, sizeof(float) * static_cast<size_t>(n) * s.V, st);
+  if (!e) {
+    TcGemmArgs g = {};
+    g.N = s.V;
+    g.K = s.H;
+    g.T = n;
+    g.ksteps = 4 * ((s.H + 255) / 256);
+    g.mode = TC_STORE;
+    g.ldo = s.V;
+    g.tile_tokens = 16;
+    g.splits = 1;
+    g.out = logits;
+    g.guard = c->guard;
+    e = launch_tc_gemm_sk(c->tm_lm.data(), c->tb_xh.data(), c->tb_xl.data(), g, c->sms, st);
+  }
+  if (!e)
+    e = launch_argmax_rows(logits, n, s.V, d_argmax, reinterpret_cast<float*>(c->ws + c->lay.vpv),
+                           reinterpret_cast<int*>(c->ws + c->lay.vpi), kArgmaxPartsMax, c->guard, st);
+  return e;
 }
 
 k2_status validate_weights(k2_ctx* c, const k2_weights* w) {
@@ -1427,5 +1508,84 @@ k2_status k2_philox(uint32_t first, int32_t n, uint32_t c1, uint32_t c2, uint32_
   const cudaError_t e = launch_philox(first, n, c1, c2, c3, static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32),
                                       d_out, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? K2_OK : K2_ERR_CUDA;
+}
+
+int32_t k2_spec_draft(const int32_t* h_tokens, int32_t n_tokens, int32_t max_draft, int32_t* h_out) {
+  if (!h_tokens || n_tokens < 0 || max_draft < 1 || !h_out) return 0;
+  const int cap = std::min<int>(max_draft, kSpecMax);
+  const int T = n_tokens;
+  for (int n = 4; n >= 3; --n) {  // the longer suffix first
+    if (T < n + 1) continue;
+    const int32_t* tail = h_tokens + T - n;
+    // the two latest earlier occurrences of the suffix
+    int latest = -1, second = -1;
+    for (int j = T - n - 1; j >= 0 && second < 0; --j) {
+      if (!std::equal(tail, tail + n, h_tokens + j)) continue;
+      if (latest < 0) latest = j;
+      else second = j;
+    }
+    if (latest < 0) continue;
+    int nd = 0;
+    while (nd < cap && latest + n + nd < T) {
+      const int32_t next = h_tokens[latest + n + nd];
+      // with two occurrences, draft only as far as their continuations agree
+      if (second >= 0 && (second + n + nd >= latest || h_tokens[second + n + nd] != next)) break;
+      h_out[nd++] = next;
+    }
+    if (nd > 0) return nd;
+  }
+  return 0;
+}
+
+k2_status k2_decode_speculative(k2_ctx* c, int32_t seq, const int32_t* h_tokens, int32_t n_tokens,
+                                int32_t max_draft, int32_t* h_out, int32_t* n_out, void* stream) {
+  if (!c) return K2_ERR_ARG;
+  if (seq < 0 || seq >= c->s.B) return c->fail(K2_ERR_ARG, "seq %d outside [0, %d)", seq, c->s.B);
+  if (!h_tokens || !h_out || !n_out || max_draft < 0)
+    return c->fail(K2_ERR_ARG, "h_tokens, h_out and n_out must be non-null, max_draft >= 0");
+  if (n_tokens != c->len[seq] + 1)
+    return c->fail(K2_ERR_ARG, "h_tokens must hold the %d cached ids and the next input (got %d ids)", c->len[seq],
+                   n_tokens);
+  if (c->sampling) return c->fail(K2_ERR_UNSUPPORTED, "speculative decoding verifies greedy ids only");
+  if (c->len[seq] >= c->s.ctx) return c->fail(K2_ERR_CONTEXT_FULL, "sequence %d is at max_context %d", seq, c->s.ctx);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int ids[kSpecMax + 1];
+  ids[0] = h_tokens[n_tokens - 1];
+  int nd = c->tc_ok ? k2_spec_draft(h_tokens, n_tokens, std::min<int>(max_draft, kSpecMax), ids + 1) : 0;
+  nd = std::min(nd, c->s.ctx - c->len[seq] - 1);  // every verified row must fit
+  if (nd < 0) nd = 0;
+  int* d_ids = reinterpret_cast<int*>(c->ws + c->lay.vids);
+  int* d_arg = reinterpret_cast<int*>(c->ws + c->lay.varg);
+  static thread_local int h_ids[kSpecMax + 1];
+  std::copy(ids, ids + nd + 1, h_ids);
+  cudaError_t e = cudaMemcpyAsync(d_ids, h_ids, sizeof(int) * (nd + 1), cudaMemcpyHostToDevice, st);
+  int out[kSpecMax + 1];
+  int accepted = 0;
+  if (nd == 0) {  // no draft: an ordinary decode step of this sequence
+    Launcher ln{c, st, false};
+    if (!e) enqueue_token(c, ln, seq, d_ids, nullptr, d_arg, nullptr, true);
+    if (!e) e = ln.err;
+    if (!e) e = cudaMemcpyAsync(out, d_arg, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (!e) e = cudaStreamSynchronize(st);
+    if (e) return c->cuda_fail(e, "speculative step");
+    c->len[seq] += 1;
+  } else {
+    if (!e) e = verify_block(c, seq, d_ids, nd + 1, d_arg, st);
+    if (!e) e = cudaMemcpyAsync(out, d_arg, sizeof(int) * (nd + 1), cudaMemcpyDeviceToHost, st);
+    if (!e) e = cudaStreamSynchronize(st);
+    if (e) return c->cuda_fail(e, "speculative verification");
+    // draft i is kept while it is the greedy id after the ids before it
+    while (accepted < nd && ids[1 + accepted] == out[accepted]) ++accepted;
+    const int len = c->len[seq] + 1 + accepted;  // the input row and the accepted drafts
+    static thread_local int v;
+    v = len;
+    e = cudaMemcpyAsync(c->seq_len + seq, &v, sizeof(int), cudaMemcpyHostToDevice, st);
+    if (!e) e = cudaStreamSynchronize(st);
+    if (e) return c->cuda_fail(e, "speculative length");
+    c->len[seq] = len;
+  }
+  std::copy(out, out + accepted + 1, h_out);
+  *n_out = accepted + 1;
+  return K2_OK;
 }
 }  // extern "C"

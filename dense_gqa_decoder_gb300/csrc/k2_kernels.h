@@ -152,6 +152,12 @@ struct AttnArgs {
   float scale;          // 1/sqrt(D)
   uint32_t slot_bytes;  // one warp's tile slot
   unsigned* guard;
+  // block mode (non-zero): every slot b is a query of sequence block_seq at
+  // position pos_base + b whose K/V row is already in the cache (a short
+  // causal block appended by the prefill path); nothing is written to the cache
+  int block_mode;
+  int block_seq;
+  int pos_base;
 };
 constexpr int kAttnThreads = 256;
 constexpr int kAttnTK = 32;          // keys per tile; a warp reads one tile at a time

@@ -91,6 +91,8 @@ def _load():
         "k2_set_sampling": (C.c_int, [vp, C.POINTER(Sampling)]),
         "k2_sample_logits": (C.c_int, [vp, vp, i32, vp, i32, vp, vp, i32, vp, vp]),
         "k2_philox": (C.c_int, [C.c_uint32, i32, C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint64, vp, vp]),
+        "k2_spec_draft": (i32, [vp, i32, i32, vp]),
+        "k2_decode_speculative": (C.c_int, [vp, i32, vp, i32, i32, vp, C.POINTER(i32), vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -104,7 +106,7 @@ EXPORTED = ("k2_workspace_bytes", "k2_init_weights", "k2_free", "k2_last_error",
             "k2_decode_step", "k2_decode_layers", "k2_kv_reset", "k2_kv_set_len", "k2_kv_view", "k2_hidden_view",
             "k2_sync_status", "k2_clear_status", "k2_set_option", "k2_profile_decode", "k2_greedy_head_noalloc",
             "k2_kv_state_bytes", "k2_kv_save", "k2_kv_peek", "k2_kv_load", "k2_set_sampling", "k2_sample_logits",
-            "k2_philox")
+            "k2_philox", "k2_spec_draft", "k2_decode_speculative")
 
 
 def _ptr(t):
@@ -226,6 +228,16 @@ class Context:
         self._check(LIB.k2_sample_logits(self.ctx, _ptr(logits), rows, _ptr(seen), stride, _ptr(seen_len),
                                          _ptr(positions), first_seq, _ptr(next_tokens), _stream(stream)))
 
+    def decode_speculative(self, seq, tokens, max_draft=8, stream=None):
+        """k2_decode_speculative: `tokens` = the cached ids + the next input;
+        returns the emitted greedy ids (the last one is the next input)."""
+        ids = (C.c_int32 * len(tokens))(*[int(t) for t in tokens])
+        out = (C.c_int32 * (max(max_draft, 0) + 1))()
+        n = C.c_int32(0)
+        self._check(LIB.k2_decode_speculative(self.ctx, seq, ids, len(tokens), max_draft, out, C.byref(n),
+                                              _stream(stream)))
+        return list(out[:n.value])
+
     def kv_state_bytes(self, seq, n_tokens=0):
         n = C.c_size_t()
         st = LIB.k2_kv_state_bytes(self.ctx, seq, n_tokens, C.byref(n))
@@ -277,6 +289,14 @@ def philox(first: int, n: int, c1=0, c2=0, c3=0, key=0, stream=None) -> torch.Te
     if st != K2_OK:
         raise K2Error(st, "k2_philox failed")
     return out.view(n, 4).cpu().to(torch.int64) & 0xFFFFFFFF
+
+
+def spec_draft(tokens, max_draft=8) -> list:
+    """k2_spec_draft (host only)."""
+    ids = (C.c_int32 * max(len(tokens), 1))(*[int(t) for t in tokens])
+    out = (C.c_int32 * 8)()
+    n = LIB.k2_spec_draft(ids, len(tokens), max_draft, out)
+    return list(out[:n])
 
 
 def peek_state(cfg: Config, state) -> tuple:

@@ -241,6 +241,39 @@ k2_status k2_sample_logits(k2_ctx* ctx, const float* d_logits, int32_t rows, con
 k2_status k2_philox(uint32_t first, int32_t n, uint32_t c1, uint32_t c2, uint32_t c3, uint64_t key, uint32_t* d_out,
                     void* stream);
 
+/* ---- speculative decoding ------------------------------------------------------
+ *
+ * kimi-k3-in-c k3_run.c, --spec: draft ids by n-gram lookup in the sequence
+ * itself and verify them in one batched pass; only the prefix the model
+ * itself would have emitted greedily is accepted.
+ *
+ * Drafting (the rule of the page's spec_draft): for n = 4, then 3, find the
+ * two latest earlier occurrences of the last n ids of h_tokens; propose the
+ * ids that followed the latest one (at most max_draft, at most 8, and not
+ * past the end of h_tokens); with a second occurrence, stop where the two
+ * continuations disagree or where the second one reaches the latest.  The
+ * first n giving a non-empty draft wins.  Returns the number of drafted ids
+ * written to h_out (host memory; 0 = no draft).  No context, no GPU. */
+int32_t k2_spec_draft(const int32_t* h_tokens, int32_t n_tokens, int32_t max_draft, int32_t* h_out);
+
+/* One speculative step of sequence seq.  h_tokens [n_tokens] (host) holds
+ * the sequence's cached ids followed by the next input id, so n_tokens =
+ * its cache length + 1.  The input and up to max_draft drafted ids (see
+ * k2_spec_draft, with max_draft capped so the rows fit max_context) are
+ * appended in one tensor-core pass that computes the greedy id after every
+ * one of them; draft i is accepted while it equals the greedy id after the
+ * ids before it.  The cache keeps the rows of the input and of the accepted
+ * drafts; h_out (room for max_draft + 1) receives the greedy ids after them
+ * (accepted + 1 ids, the last one the next input), *n_out their count.
+ * Without a draft (or without tensor-core prefill: fp32 weights) the step
+ * is an ordinary decode step of seq.  Greedy only: K2_ERR_UNSUPPORTED while
+ * sampling is set.  Waits for `stream`.  The verification pass runs the
+ * prefill arithmetic, so where the top two logits of a step lie within its
+ * ~1e-6 difference from the decode step's, the ids can differ from serial
+ * decoding. */
+k2_status k2_decode_speculative(k2_ctx* ctx, int32_t seq, const int32_t* h_tokens, int32_t n_tokens,
+                                int32_t max_draft, int32_t* h_out, int32_t* n_out, void* stream);
+
 /* ---- saved cache state ------------------------------------------------------
  *
  * A sequence's cache can be written to host memory and restored later, into

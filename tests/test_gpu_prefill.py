@@ -157,3 +157,18 @@ def test_batched_decode_matches_one_token_at_a_time_and_oracle(k2, mio, kv):
         am, ref, _ = model.teacher_forced(seq, len(prompts[b]))
         assert rel_l2(l1[:, b], ref) <= (2e-4 if kv == "f16" else 5e-2)
         assert np.mean(am == t1[1:, b]) >= (0.99 if kv == "f16" else 0.9)
+
+
+@pytest.mark.parametrize("n", [8, 12, 16, 17])
+def test_short_prompts_through_the_small_block_path(k2, mio, n):
+    """Prompts of 8..16 tokens stream the weights with the 16-token-tile GEMMs
+    (17 takes the 128-token tiles): against the step-by-step path."""
+    s = ki.MEDIUM
+    prompt = ki.prompt_ids(s.vocab, n, seed=70 + n)
+    out = {}
+    for tc in (True, False):
+        ctx, _ = mio.build_context(s, max_context=64, kv_dtype="f16", gain_scale=0.1)
+        out[tc] = prefill(k2, ctx, prompt, s.vocab, tc)
+        assert ctx.sync_status() == k2.K2_OK
+    assert out[True][0] == out[False][0]
+    assert rel_l2(out[True][1], out[False][1]) <= 1e-4
