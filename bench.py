@@ -466,6 +466,7 @@ def run_ours(args, world, rank, local, pg):
 def run_speculative(args, world, rank, local, pg):
     """Greedy decoding with n-gram drafts verified in one pass: --steps
     emitted tokens timed after --warmup, from a --ctx-token random prompt."""
+    import numpy as np
     import torch
 
     import k2_inputs as ki
@@ -487,18 +488,26 @@ def run_speculative(args, world, rank, local, pg):
     with torch.cuda.stream(stream):
         ctx.prefill(0, torch.tensor(ids, dtype=torch.int32, device="cuda"), tok, stream=stream)
     stream.synchronize()
-    seq = ids + [int(tok.item())]
+    ctx.set_option(k2.K2_OPT_GRAPH, 1)  # each (block size) is recorded once, then replayed
+    buf = np.zeros(args.ctx + args.warmup + args.steps + 32, dtype=np.int32)  # the sequence, passed without copies
+    buf[:len(ids)] = ids
+    buf[len(ids)] = int(tok.item())
+    n = len(ids) + 1
+
+    def step():
+        nonlocal n
+        got = ctx.decode_speculative(0, buf[:n], args.speculate, stream=stream)
+        buf[n:n + len(got)] = got
+        n += len(got)
+        return len(got)
+
     emitted = 0
     while emitted < args.warmup:
-        got = ctx.decode_speculative(0, seq, args.speculate, stream=stream)
-        seq += got
-        emitted += len(got)
+        emitted += step()
     t0 = time.perf_counter()
     emitted, passes = 0, 0
     while emitted < args.steps:
-        got = ctx.decode_speculative(0, seq, args.speculate, stream=stream)
-        seq += got
-        emitted += len(got)
+        emitted += step()
         passes += 1
     dt = time.perf_counter() - t0
     if ctx.sync_status(stream) != k2.K2_OK:

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   const int b = blockIdx.z, g = blockIdx.y, sp = blockIdx.x, ns = gridDim.x;
   const int seq = a.block_mode ? a.block_seq : a.seq0 + b;
   // seq_len was written two or more launches back (see pdl_trigger placement)
-  const int pos = a.block_mode ? a.pos_base + b : a.seq_len[seq];
+  const int pos = a.block_mode ? (a.pos_base_dev ? *a.pos_base_dev : a.pos_base) + b : a.seq_len[seq];
   if (pos < 0 || pos >= a.cap) {
     if (tid == 0) atomicOr(a.guard, GUARD_POS);
     return;  // every CTA of the launch sees the same pos and leaves before any cluster barrier

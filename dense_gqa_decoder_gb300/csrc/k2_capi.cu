@@ -229,6 +229,7 @@ struct k2_ctx {
   // the same activation buffers in 16-token tiles (batched decode)
   std::array<uint8_t, kTcMapBytes> tb_xh{}, tb_xl{}, tb_oh{}, tb_ol{}, tb_ah{}, tb_al{};
   std::map<std::tuple<int, const void*, const void*, const void*, void*>, cudaGraphExec_t> graphs;
+  std::map<std::tuple<int, int, void*>, cudaGraphExec_t> spec_graphs;  // (seq, ids verified (0: a plain step), stream)
   std::string err;
   // profiling: event pairs around the kernels of one step
   std::vector<cudaEvent_t> pev;
@@ -645,7 +646,10 @@ cudaError_t plan_tc_prefill(k2_ctx* c) {
 // One block of n <= pchunk prompt tokens of sequence seq at positions
 // pos0 .. pos0+n-1 through every layer; the residual of its last token is left
 // in pX[n-1].
-cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int pos0, cudaStream_t st) {
+// d_pos0 (nullable): the block's first position read on the device (a graph
+// replayed at any position), else pos0
+cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int pos0, cudaStream_t st,
+                          const int* d_pos0 = nullptr) {
   const Sizes& s = c->s;
   float* X = reinterpret_cast<float*>(c->ws + c->lay.px);
   auto* xh = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxh);
@@ -704,7 +708,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   const void* m_al = small ? c->tb_al.data() : c->tm_al.data();
   float* O32 = Q + static_cast<size_t>(16) * s.nq * s.d;  // small blocks: the attention output after 16 query rows
   cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.wb, X, s.H, s.V, c->guard,
-                                    c->hist + static_cast<size_t>(seq) * c->lay.cap, 0, nullptr, pos0, st);
+                                    c->hist + static_cast<size_t>(seq) * c->lay.cap, 0, nullptr, pos0, d_pos0, st);
   for (int l = 0; l < s.L && !e; ++l) {
     if (!e) e = launch_norm_rows(X, n, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
     if (!e)
@@ -712,7 +716,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
                 : gemm(c->tmw[4 * l].data(), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, nullptr, nullptr, s.qkv_n);
     if (!e)
       e = launch_rope_append(qkv, Q, c->rope, kvdt, c->kc(l), c->vc(l), c->ks(l), c->vs(l), n, s.nq, s.nkv, s.d,
-                             pos0, head_row0, c->lay.cap, st);
+                             pos0, d_pos0, head_row0, c->lay.cap, st);
     if (!e && small) {
       // few queries over a long history: the decode attention in block mode
       // splits every query's keys over a cluster of CTAs
@@ -727,6 +731,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
       at.block_mode = 1;
       at.block_seq = seq;
       at.pos_base = pos0;
+      at.pos_base_dev = d_pos0;
       at.out = O32;
       e = launch_attn(at, s.d, s.rep, kvdt, attn_splits(c, n), n, st, false);
       if (!e) e = launch_rows_hilo(O32, xh, xl, n, s.nq * s.d, st);
@@ -785,7 +790,7 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
   };
   const int asplits = attn_splits(c, B);
   cudaError_t e = launch_embed_rows(d_tokens, B, c->embed, s.wb, X, s.H, s.V, c->guard, c->hist, c->lay.cap,
-                                    c->seq_len, 0, st);
+                                    c->seq_len, 0, nullptr, st);
   for (int l = 0; l < s.L && !e; ++l) {
     if (!e) e = launch_norm_rows(X, B, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
     if (!e) e = gemm(c->tmw[4 * l].data(), c->tb_xh.data(), c->tb_xl.data(), s.qkv_n, s.H, TC_STORE, gout, s.qkv_n);
@@ -852,7 +857,7 @@ cudaError_t prefill_tc(k2_ctx* c, int seq, const int* d_tokens, int n, int* d_ne
 // logits of every position).  The device length is left to the caller.
 cudaError_t verify_block(k2_ctx* c, int seq, const int* d_tokens, int n, int* d_argmax, cudaStream_t st) {
   const Sizes& s = c->s;
-  cudaError_t e = prefill_block(c, seq, d_tokens, n, c->len[seq], st);
+  cudaError_t e = prefill_block(c, seq, d_tokens, n, c->len[seq], st, c->seq_len + seq);
   float* X = reinterpret_cast<float*>(c->ws + c->lay.px);
   auto* xh = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxh);
   auto* xl = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxl);
@@ -1114,6 +1119,7 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
 void k2_free(k2_ctx* c) {
   if (!c) return;
   for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : c->spec_graphs) cudaGraphExecDestroy(kv.second);
   for (cudaEvent_t e : c->pev) cudaEventDestroy(e);
   delete c;
 }
@@ -1319,7 +1325,9 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
     default: return c->fail(K2_ERR_ARG, "unknown option %d", option);
   }
   for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : c->spec_graphs) cudaGraphExecDestroy(kv.second);
   c->graphs.clear();
+  c->spec_graphs.clear();
   return K2_OK;
 }
 
@@ -1484,7 +1492,9 @@ k2_status k2_set_sampling(k2_ctx* c, const k2_sampling* p) {
   c->samp = on ? *p : k2_sampling{};
   c->sampling = on;
   for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : c->spec_graphs) cudaGraphExecDestroy(kv.second);
   c->graphs.clear();
+  c->spec_graphs.clear();
   return K2_OK;
 }
 
@@ -1561,16 +1571,43 @@ k2_status k2_decode_speculative(k2_ctx* c, int32_t seq, const int32_t* h_tokens,
   cudaError_t e = cudaMemcpyAsync(d_ids, h_ids, sizeof(int) * (nd + 1), cudaMemcpyHostToDevice, st);
   int out[kSpecMax + 1];
   int accepted = 0;
+  // The step's launches read every position on the device, so with
+  // K2_OPT_GRAPH they are recorded once per (sequence, block size) and replayed.
+  auto run = [&](int nblk, auto&& enqueue) -> cudaError_t {
+    if (!c->graph || !st) return enqueue();
+    const auto key = std::make_tuple(seq, nblk, stream);
+    auto it = c->spec_graphs.find(key);
+    if (it == c->spec_graphs.end()) {
+      cudaError_t ce = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
+      if (ce) return ce;
+      const cudaError_t le = enqueue();
+      cudaGraph_t g = nullptr;
+      ce = cudaStreamEndCapture(st, &g);
+      if (le || ce) {
+        if (g) cudaGraphDestroy(g);
+        return le ? le : ce;
+      }
+      cudaGraphExec_t ge = nullptr;
+      ce = cudaGraphInstantiate(&ge, g, 0);
+      cudaGraphDestroy(g);
+      if (ce) return ce;
+      it = c->spec_graphs.emplace(key, ge).first;
+    }
+    return cudaGraphLaunch(it->second, st);
+  };
   if (nd == 0) {  // no draft: an ordinary decode step of this sequence
-    Launcher ln{c, st, false};
-    if (!e) enqueue_token(c, ln, seq, d_ids, nullptr, d_arg, nullptr, true);
-    if (!e) e = ln.err;
+    if (!e)
+      e = run(0, [&] {
+        Launcher ln{c, st, false};
+        enqueue_token(c, ln, seq, d_ids, nullptr, d_arg, nullptr, true);
+        return ln.err;
+      });
     if (!e) e = cudaMemcpyAsync(out, d_arg, sizeof(int), cudaMemcpyDeviceToHost, st);
     if (!e) e = cudaStreamSynchronize(st);
     if (e) return c->cuda_fail(e, "speculative step");
     c->len[seq] += 1;
   } else {
-    if (!e) e = verify_block(c, seq, d_ids, nd + 1, d_arg, st);
+    if (!e) e = run(nd + 1, [&] { return verify_block(c, seq, d_ids, nd + 1, d_arg, st); });
     if (!e) e = cudaMemcpyAsync(out, d_arg, sizeof(int) * (nd + 1), cudaMemcpyDeviceToHost, st);
     if (!e) e = cudaStreamSynchronize(st);
     if (e) return c->cuda_fail(e, "speculative verification");

@@ -158,6 +158,7 @@ struct AttnArgs {
   int block_mode;
   int block_seq;
   int pos_base;
+  const int* pos_base_dev;  // block mode: read pos_base from device memory (nullable)
 };
 constexpr int kAttnThreads = 256;
 constexpr int kAttnTK = 32;          // keys per tile; a warp reads one tile at a time
@@ -327,14 +328,16 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* m
 bool prefill_attn_supported(int head_dim, int rep);
 cudaError_t prefill_init_attrs();
 // hist (nullable): row t's token is recorded at hist[t * hist_stride + pos[t]], or at
-// hist[pos0 + t] when pos is null
+// hist[pos0 + t] when pos is null (pos0 read from pos0_dev when that is not null)
 cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbytes, float* X, int H, int vocab,
-                              unsigned* guard, int* hist, int hist_stride, const int* pos, int pos0, cudaStream_t s);
+                              unsigned* guard, int* hist, int hist_stride, const int* pos, int pos0,
+                              const int* pos0_dev, cudaStream_t s);
 cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes, __nv_bfloat16* oh,
                              __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s);
+// pos0_dev (nullable): read the first position from device memory instead of pos0
 cudaError_t launch_rope_append(const float* qkv, float* Q, const float2* rope, int kv_dtype, void* kc, void* vc,
-                               void* ks, void* vs, int n, int nq, int nkv, int D, int pos0, size_t head_row0, int cap,
-                               cudaStream_t s);
+                               void* ks, void* vs, int n, int nq, int nkv, int D, int pos0, const int* pos0_dev,
+                               size_t head_row0, int cap, cudaStream_t s);
 cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, const void* vc, const void* ks,
                                 const void* vs, __nv_bfloat16* oh, __nv_bfloat16* ol, int n, int nq, int nkv, int D,
                                 int pos0, size_t head_row0, int cap, float scale, cudaStream_t s);

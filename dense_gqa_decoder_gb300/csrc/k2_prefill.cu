@@ -27,11 +27,12 @@ __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bflo
 template <typename WT>
 __global__ void embed_rows_kernel(const int* __restrict__ tokens, const WT* __restrict__ E, float* __restrict__ X,
                                   int H, int vocab, unsigned* guard, int* hist, int hist_stride, const int* pos,
-                                  int pos0) {
+                                  int pos0, const int* pos0_dev) {
   const int t = blockIdx.x;
   int tok = tokens[t];
   if (hist && threadIdx.x == 0)
-    hist[pos ? static_cast<size_t>(t) * hist_stride + pos[t] : static_cast<size_t>(pos0) + t] = tok;
+    hist[pos ? static_cast<size_t>(t) * hist_stride + pos[t]
+             : static_cast<size_t>(pos0_dev ? *pos0_dev : pos0) + t] = tok;
   if (tok < 0 || tok >= vocab) {
     if (threadIdx.x == 0) atomicOr(guard, GUARD_TOKEN);
     tok = 0;
@@ -83,11 +84,11 @@ __global__ void norm_rows_kernel(const float* __restrict__ X, const WT* __restri
 template <typename KVT>
 __global__ void rope_append_kernel(const float* __restrict__ qkv, float* __restrict__ Q, const float2* __restrict__ rope,
                                    KVT* __restrict__ kc, KVT* __restrict__ vc, __half* __restrict__ ks,
-                                   __half* __restrict__ vs, int nq, int nkv, int D, int pos0, size_t head_row0,
-                                   int cap) {
+                                   __half* __restrict__ vs, int nq, int nkv, int D, int pos0, const int* pos0_dev,
+                                   size_t head_row0, int cap) {
   extern __shared__ float rows[];  // [2 * nkv][D]: this token's K and V rows
   const int t = blockIdx.x, tid = threadIdx.x;
-  const int qkv_n = (nq + 2 * nkv) * D, half = D / 2, pos = pos0 + t;
+  const int qkv_n = (nq + 2 * nkv) * D, half = D / 2, pos = (pos0_dev ? *pos0_dev : pos0) + t;
   const float* src = qkv + static_cast<size_t>(t) * qkv_n;
   for (int idx = tid; idx < (nq + 2 * nkv) * half; idx += blockDim.x) {
     const int h = idx / half, i = idx - h * half;
@@ -633,13 +634,14 @@ cudaError_t prefill_init_attrs() {
 }
 
 cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbytes, float* X, int H, int vocab,
-                              unsigned* guard, int* hist, int hist_stride, const int* pos, int pos0, cudaStream_t s) {
+                              unsigned* guard, int* hist, int hist_stride, const int* pos, int pos0,
+                              const int* pos0_dev, cudaStream_t s) {
   if (wbytes == 2)
     embed_rows_kernel<<<n, 256, 0, s>>>(tokens, static_cast<const __nv_bfloat16*>(E), X, H, vocab, guard, hist,
-                                        hist_stride, pos, pos0);
+                                        hist_stride, pos, pos0, pos0_dev);
   else
     embed_rows_kernel<<<n, 256, 0, s>>>(tokens, static_cast<const float*>(E), X, H, vocab, guard, hist, hist_stride,
-                                        pos, pos0);
+                                        pos, pos0, pos0_dev);
   return cudaGetLastError();
 }
 
@@ -653,23 +655,23 @@ cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes
 }
 
 cudaError_t launch_rope_append(const float* qkv, float* Q, const float2* rope, int kv_dtype, void* kc, void* vc,
-                               void* ks, void* vs, int n, int nq, int nkv, int D, int pos0, size_t head_row0, int cap,
-                               cudaStream_t s) {
+                               void* ks, void* vs, int n, int nq, int nkv, int D, int pos0, const int* pos0_dev,
+                               size_t head_row0, int cap, cudaStream_t s) {
   const size_t smem = sizeof(float) * 2 * nkv * D;
   switch (kv_dtype) {
     case 0:
       rope_append_kernel<float><<<n, 256, smem, s>>>(qkv, Q, rope, static_cast<float*>(kc), static_cast<float*>(vc),
-                                                     nullptr, nullptr, nq, nkv, D, pos0, head_row0, cap);
+                                                     nullptr, nullptr, nq, nkv, D, pos0, pos0_dev, head_row0, cap);
       break;
     case 2:
       rope_append_kernel<__half><<<n, 256, smem, s>>>(qkv, Q, rope, static_cast<__half*>(kc),
                                                       static_cast<__half*>(vc), nullptr, nullptr, nq, nkv, D, pos0,
-                                                      head_row0, cap);
+                                                      pos0_dev, head_row0, cap);
       break;
     default:
       rope_append_kernel<int8_t><<<n, 256, smem, s>>>(qkv, Q, rope, static_cast<int8_t*>(kc),
                                                       static_cast<int8_t*>(vc), static_cast<__half*>(ks),
-                                                      static_cast<__half*>(vs), nq, nkv, D, pos0, head_row0, cap);
+                                                      static_cast<__half*>(vs), nq, nkv, D, pos0, pos0_dev, head_row0, cap);
   }
   return cudaGetLastError();
 }

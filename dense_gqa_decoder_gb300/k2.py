@@ -229,12 +229,18 @@ class Context:
                                          _ptr(positions), first_seq, _ptr(next_tokens), _stream(stream)))
 
     def decode_speculative(self, seq, tokens, max_draft=8, stream=None):
-        """k2_decode_speculative: `tokens` = the cached ids + the next input;
-        returns the emitted greedy ids (the last one is the next input)."""
-        ids = (C.c_int32 * len(tokens))(*[int(t) for t in tokens])
+        """k2_decode_speculative: `tokens` = the cached ids + the next input (a
+        contiguous numpy int32 array is passed without a copy); returns the
+        emitted greedy ids (the last one is the next input)."""
+        import numpy as np
+        if isinstance(tokens, np.ndarray) and tokens.dtype == np.int32 and tokens.flags.c_contiguous:
+            ids, n_ids = tokens.ctypes.data, tokens.size
+        else:
+            arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+            ids, n_ids = arr.ctypes.data, arr.size
         out = (C.c_int32 * (max(max_draft, 0) + 1))()
         n = C.c_int32(0)
-        self._check(LIB.k2_decode_speculative(self.ctx, seq, ids, len(tokens), max_draft, out, C.byref(n),
+        self._check(LIB.k2_decode_speculative(self.ctx, seq, ids, n_ids, max_draft, out, C.byref(n),
                                               _stream(stream)))
         return list(out[:n.value])
 

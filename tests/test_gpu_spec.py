@@ -39,14 +39,15 @@ def serial(ctx, prompt, n, vocab):
     return out
 
 
-def speculative(ctx, prompt, n, max_draft=8):
+def speculative(ctx, prompt, n, max_draft=8, stream=None):
     nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
     ctx.prefill(0, torch.tensor(prompt, dtype=torch.int32, device="cuda"), nxt)
+    torch.cuda.synchronize()
     seq = list(prompt) + [int(nxt.item())]
     out = [seq[-1]]
     passes = 0
     while len(out) < n:
-        got = ctx.decode_speculative(0, seq, max_draft)
+        got = ctx.decode_speculative(0, seq, max_draft, stream=stream)
         passes += 1
         out += got
         seq += got
@@ -54,16 +55,19 @@ def speculative(ctx, prompt, n, max_draft=8):
     return out[:n], passes
 
 
-@pytest.mark.parametrize("shape,kv,repeats", [("medium", "f16", True), ("medium", "i8", True),
-                                             ("k2_layer", "f16", False)])
-def test_speculative_stream_equals_serial_greedy(k2, mio, shape, kv, repeats):
+@pytest.mark.parametrize("shape,kv,repeats,graph", [("medium", "f16", True, 0), ("medium", "f16", True, 1),
+                                                   ("medium", "i8", True, 1), ("k2_layer", "f16", False, 1)])
+def test_speculative_stream_equals_serial_greedy(k2, mio, shape, kv, repeats, graph):
     s = ki.SHAPES[shape]
     n = 48
     prompt = repetitive_prompt(s.vocab, seed=40)
     ctx, _ = mio.build_context(s, max_context=160, kv_dtype=kv, gain_scale=0.1)
     ref = serial(ctx, prompt, n, s.vocab)
     ctx.kv_reset(0)
-    got, passes = speculative(ctx, prompt, n)
+    # graphs: every block size is recorded once and replayed at later positions
+    ctx.set_option(k2.K2_OPT_GRAPH, graph)
+    stream = torch.cuda.Stream() if graph else None
+    got, passes = speculative(ctx, prompt, n, stream=stream)
     assert got == ref
     assert ctx.sync_status() == k2.K2_OK
     # this medium model's greedy continuation repeats the prompt's pattern, so
