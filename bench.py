@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--layers", type=int, default=0, help="override layer count (debug)")
     p.add_argument("--kv", default="f16", choices=["f16", "i8"], help="KV cache storage")
+    p.add_argument("--weights", default="bf16", choices=["bf16", "f8"],
+                   help="stored projection weights: bf16, or fp8 E4M3 rows with per-row scales (quantized at init)")
     p.add_argument("--temperature", type=float, default=0.0,
                    help="> 0: sample each token (with --top-k / --top-p / --min-p / --repetition-penalty / "
                         "--seed) instead of the greedy argmax")
@@ -72,14 +74,21 @@ def parse():
 # helpers
 # ---------------------------------------------------------------------------
 
-def algorithmic_bytes(s, ctx_len: int, kv: str = "f16") -> dict:
+def algorithmic_bytes(s, ctx_len: int, kv: str = "f16", weights_store: str = "bf16") -> dict:
     """Bytes the decode step must move at context ctx_len (weights once, the
-    KV history once, plus the small activations)."""
+    KV history once, plus the small activations).  fp8 weights: one byte per
+    weight plus a 4-byte scale per row; gains and the embedding row stay bf16."""
     H, d, I, V = s.hidden, s.head_dim, s.intermediate, s.vocab
     qkv_n = (s.n_heads + 2 * s.n_kv_heads) * d
-    wb = 2 if s.weight_dtype == "bf16" else 4
-    per_layer = (qkv_n * H + H * s.n_heads * d + 2 * I * H + H * I + 2 * H) * wb
-    weights = s.n_layers * per_layer + V * H * wb + H * wb
+    gb = 2 if s.weight_dtype == "bf16" else 4
+    if weights_store == "f8":
+        wb = 1
+        per_layer = (qkv_n * H + H * s.n_heads * d + 2 * I * H + H * I) + 4 * (qkv_n + H + 2 * I + H) + 2 * H * gb
+        weights = s.n_layers * per_layer + V * H + 4 * V + H * gb
+    else:
+        wb = gb
+        per_layer = (qkv_n * H + H * s.n_heads * d + 2 * I * H + H * I + 2 * H) * wb
+        weights = s.n_layers * per_layer + V * H * wb + H * wb
     # K and V of one position, one layer: fp16, or int8 codes + one fp16 scale per head
     kv_row = 2 * s.n_kv_heads * d * 2 if kv == "f16" else 2 * s.n_kv_heads * (d + 2)
     kv = s.n_layers * kv_row * ctx_len
@@ -315,7 +324,8 @@ def run_ours(args, world, rank, local, pg):
     if args.layers:
         s = s.replace(n_layers=args.layers)
     budget = args.ctx + args.warmup + args.steps + args.profile_steps + args.e2e_steps + 16
-    cfg = k2.make_config(s, max_context=budget, max_batch=1, kv_dtype=args.kv)
+    cfg = k2.make_config(s, max_context=budget, max_batch=1, kv_dtype=args.kv,
+                         weights=args.weights if args.weights == "f8" else None)
     ctx = k2.Context(cfg, random_device_weights(s, seed=1234 + rank))
     stream = torch.cuda.Stream()
     sampled = args.temperature > 0
@@ -371,7 +381,7 @@ def run_ours(args, world, rank, local, pg):
     ms_per_step = ms / args.steps
     value = world * args.steps / (ms / 1e3)
     mean_ctx = ctx_start + (args.steps - 1) / 2 + 1
-    by = algorithmic_bytes(s, int(round(mean_ctx)), args.kv)
+    by = algorithmic_bytes(s, int(round(mean_ctx)), args.kv, args.weights)
 
     # per-kernel durations: one un-graphed step with an event pair per kernel
     ms_k = {k: 0.0 for k in k2.KERNEL_CLASSES}
@@ -397,6 +407,8 @@ def run_ours(args, world, rank, local, pg):
         launches_per_step = 1 + 5 * s.n_layers + 1
     achieved = k_bytes / (k_ms * 1e-3) / 1e9
     traffic, sha = traffic_from_profiles(src, k_name)
+    if not (args.kv == "f16" and args.ctx == CTX and args.weights == "bf16" and not sampled and not args.layers):
+        traffic = None  # the committed capture is of the default workload only
 
     # end to end through the C ABI with host buffers: token H2D, step, token D2H
     host_in = torch.zeros(1, dtype=torch.int32).pin_memory()
@@ -428,10 +440,11 @@ def run_ours(args, world, rank, local, pg):
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD if (args.kv == "f16" and args.ctx == CTX and not sampled) else
+        "vs_baseline": None, "dtype": "bf16" if args.weights == "bf16" else "f8e4m3", "data": "synthetic",
+        "config": {"workload": WORKLOAD if (args.kv == "f16" and args.ctx == CTX and not sampled and
+                                            args.weights == "bf16") else
                    f"k2-horizon-3.7b-shape {'sampled' if sampled else 'greedy'} decode, batch 1, context {args.ctx}, "
-                   f"{args.kv} KV, bf16 weights",
+                   f"{args.kv} KV, {'fp8 E4M3 (per-row scales)' if args.weights == 'f8' else 'bf16'} weights",
                    "sampling": ({"temperature": args.temperature, "top_k": args.top_k, "top_p": args.top_p,
                                  "min_p": args.min_p, "repetition_penalty": args.repetition_penalty,
                                  "seed": args.seed} if sampled else None),
@@ -452,9 +465,11 @@ def run_ours(args, world, rank, local, pg):
         "prefill": {"tokens": T, "ms": prefill_ms, "tok_per_s": T / (prefill_ms * 1e-3),
                     "algorithmic_tflop": (pf_linear + pf_attn) / 1e12,
                     "achieved_tflops": pf_tflops, "peak_tflops": tc_peak, "frac": pf_tflops / tc_peak,
-                    "note": "useful FLOPs (2 per weight x token + causal attention); the GEMMs issue twice "
-                            "the linear MMAs (activations as bf16 hi + lo halves); attention issues mma.sync "
-                            "on fp16 hi + lo halves of the queries and probabilities"},
+                    "note": ("useful FLOPs (2 per weight x token + causal attention); the GEMMs issue twice "
+                             "the linear MMAs (activations as bf16 hi + lo halves); attention issues mma.sync "
+                             "on fp16 hi + lo halves of the queries and probabilities") if args.weights == "bf16" else
+                            "fp8 weights have no tensor-core GEMM path: the prompt runs through the decode step, "
+                            "one token at a time"},
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
         "clocks": clk,
         "cpu_baseline": cpu,

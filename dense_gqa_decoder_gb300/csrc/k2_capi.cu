@@ -42,6 +42,8 @@ struct Layout {
   size_t seq_len, guard, am_counter, msync, rope, resid, qkv, attn_out, act, am_val, am_idx, attn_part, ltab;
   size_t t_resid, t_qkv, t_attn, t_act, t_part;  // persistent step: (value, tag) activations
   size_t hist, slog, sscr, sample_row;             // token history, sampling logits and scratch
+  size_t sqkv, so, sgu, sdown, slm;                // fp8 weights: per-row scales (first layer)
+  size_t sqkv_layer, so_layer, sgu_layer, sdown_layer;
   size_t vlog, vids, varg, vpv, vpi;               // speculative verification: logits, ids, argmax
   // tensor-core prefill of up to `pchunk` tokens at a time (bf16 weights)
   int pchunk;
@@ -57,6 +59,7 @@ struct Layout {
 
 struct Sizes {
   int H, L, nq, nkv, d, I, G, V, ctx, B, qkv_n, rep, wb, kvb;
+  int gb;  // bytes of an embedding / gain element (bf16 for fp8 weights); wb: of a packed weight
 };
 
 Sizes sizes_of(const k2_config& c) {
@@ -66,6 +69,7 @@ Sizes sizes_of(const k2_config& c) {
   s.qkv_n = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
   s.rep = c.n_kv_heads > 0 ? c.n_heads / c.n_kv_heads : 0;
   s.wb = elt_bytes(c.weight_dtype);
+  s.gb = c.weight_dtype == K2_F8 ? 2 : s.wb;
   s.kvb = elt_bytes(c.kv_dtype);
   return s;
 }
@@ -105,6 +109,19 @@ Layout layout_of(const k2_config& c) {
   l.slog = take(sizeof(float) * static_cast<size_t>(s.B) * s.V);
   l.sample_row = sample_row_bytes(s.V);
   l.sscr = take(kSampleBarBytes + static_cast<size_t>(s.B) * l.sample_row);
+  {  // one fp32 scale per packed (pair-padded) row of every fp8 matrix
+    const bool f8 = c.weight_dtype == K2_F8;
+    auto rows = [&](int N) { return f8 ? sizeof(float) * 2 * static_cast<size_t>((N + 1) / 2) : 0; };
+    l.sqkv_layer = rows(s.qkv_n);
+    l.so_layer = rows(s.H);
+    l.sgu_layer = rows(2 * s.I);
+    l.sdown_layer = rows(s.H);
+    l.sqkv = take(l.sqkv_layer * s.L);
+    l.so = take(l.so_layer * s.L);
+    l.sgu = take(l.sgu_layer * s.L);
+    l.sdown = take(l.sdown_layer * s.L);
+    l.slm = take(rows(s.V));
+  }
   l.pchunk = c.weight_dtype == K2_BF16 ? static_cast<int>(align_up(std::min(kPrefillChunk, s.ctx), 128)) : 0;
   {
     const size_t P = static_cast<size_t>(l.pchunk);
@@ -156,7 +173,8 @@ std::string check_config(const k2_config* c) {
   if (c->n_heads % c->n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
   if (c->head_dim % 2) return "head_dim must be even (split-half RoPE)";
   if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) return "eps must be >= 0 and rope_theta > 0";
-  if (c->weight_dtype != K2_F32 && c->weight_dtype != K2_BF16) return "weight_dtype must be K2_F32 or K2_BF16";
+  if (c->weight_dtype != K2_F32 && c->weight_dtype != K2_BF16 && c->weight_dtype != K2_F8)
+    return "weight_dtype must be K2_F32, K2_BF16 or K2_F8";
   if (c->kv_dtype != K2_F32 && c->kv_dtype != K2_F16 && c->kv_dtype != K2_I8)
     return "kv_dtype must be K2_F32, K2_F16 or K2_I8";
   if (c->max_batch > 64) return "max_batch above 64 is not supported";
@@ -450,7 +468,9 @@ void enqueue_decode(k2_ctx* c, Launcher& ln, const int* d_tokens, int batch, int
 
 bool plan_all(k2_ctx* c) {
   const Sizes& s = c->s;
-  const int wb = s.wb;
+  // the kernel chain streams bf16 / fp32 weights; fp8 models run the
+  // persistent step only (their chain plans, in bf16 terms, are never launched)
+  const int wb = s.gb;
   PackedGemvArgs base = {};
   base.groups = s.G;
   base.eps = c->cfg.eps;
@@ -521,7 +541,7 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   // inputs are polled in groups of four words; the gains are copied in 16-byte
   // pieces into the x buffer above a 16 KB input
   if (s.H % 8 || (s.nq * s.d) % 4 || s.I % 4) return cudaSuccess;
-  if (static_cast<size_t>(s.H) * s.wb > static_cast<size_t>(kMegaGainBytes)) return cudaSuccess;
+  if (static_cast<size_t>(s.H) * s.gb > static_cast<size_t>(kMegaGainBytes)) return cudaSuccess;
   if (s.d / 2 > 64) return cudaSuccess;  // the RoPE row of the position is kept in shared memory
   if (s.L > kMegaMaxLayers) return cudaSuccess;
   // tags carry the phase index in kMegaTagShift bits
@@ -547,15 +567,26 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   LayerPtrs* dtab = reinterpret_cast<LayerPtrs*>(c->ws + c->lay.ltab);
   e = cudaMemcpyAsync(dtab, c->ltab.data(), sizeof(LayerPtrs) * s.L, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return e;
-  auto gplan = [&](const PackedGemvArgs& p) {
+  auto gplan = [&](const PackedGemvArgs& p) {  // 512-byte chunks of packed (wb-byte) weights per row pair
     MegaGemv g;
-    g.CT = p.CT;
+    g.CT = (p.K * s.wb + 511) / 512;
     return g;
   };
   MegaArgs& m = c->mega;
   m = {};
   m.layers = dtab;
   m.hist = c->hist;
+  if (c->cfg.weight_dtype == K2_F8) {
+    m.sc_qkv = reinterpret_cast<const float*>(c->ws + c->lay.sqkv);
+    m.sc_o = reinterpret_cast<const float*>(c->ws + c->lay.so);
+    m.sc_gu = reinterpret_cast<const float*>(c->ws + c->lay.sgu);
+    m.sc_down = reinterpret_cast<const float*>(c->ws + c->lay.sdown);
+    m.sc_lm = reinterpret_cast<const float*>(c->ws + c->lay.slm);
+    m.ss_qkv = c->lay.sqkv_layer / sizeof(float);
+    m.ss_o = c->lay.so_layer / sizeof(float);
+    m.ss_gu = c->lay.sgu_layer / sizeof(float);
+    m.ss_down = c->lay.sdown_layer / sizeof(float);
+  }
   m.n_layers = s.L;
   m.w_qkv = static_cast<const uint8_t*>(c->wqkv(0));
   m.w_o = static_cast<const uint8_t*>(c->wop(0));
@@ -1086,7 +1117,27 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     return K2_ERR_CUDA;
   }
   const Sizes& z = c->s;
-  for (int l = 0; l < z.L && e == cudaSuccess; ++l) {
+  if (cfg->weight_dtype == K2_F8) {  // quantize the bf16 inputs into fp8 rows + scales
+    auto sc = [&](size_t base, size_t stride, int l) { return reinterpret_cast<float*>(ws + base + stride * l); };
+    const auto& L = c->lay;
+    for (int l = 0; l < z.L && e == cudaSuccess; ++l) {
+      e = launch_quant_pack(static_cast<uint8_t*>(c->wqkv(l)), sc(L.sqkv, L.sqkv_layer, l), w->wq[l], w->wk[l],
+                            w->wv[l], PACK_QKV, z.qkv_n, z.H, z.nq, z.nkv, z.d, true, s);
+      if (e == cudaSuccess)
+        e = launch_quant_pack(static_cast<uint8_t*>(c->wop(l)), sc(L.so, L.so_layer, l), w->wo[l], nullptr, nullptr,
+                              PACK_PLAIN, z.H, z.nq * z.d, 0, 0, 1, true, s);
+      if (e == cudaSuccess)
+        e = launch_quant_pack(static_cast<uint8_t*>(c->wgu(l)), sc(L.sgu, L.sgu_layer, l), w->w_gate[l], w->w_up[l],
+                              nullptr, PACK_GATEUP, 2 * z.I, z.H, 0, 0, 1, true, s);
+      if (e == cudaSuccess)
+        e = launch_quant_pack(static_cast<uint8_t*>(c->wdown(l)), sc(L.sdown, L.sdown_layer, l), w->w_down[l], nullptr,
+                              nullptr, PACK_PLAIN, z.H, z.I, 0, 0, 1, true, s);
+    }
+    if (e == cudaSuccess)
+      e = launch_quant_pack(static_cast<uint8_t*>(c->wlm()), reinterpret_cast<float*>(ws + L.slm), w->lm_head, nullptr,
+                            nullptr, PACK_PLAIN, z.V, z.H, 0, 0, 1, true, s);
+  }
+  for (int l = 0; l < z.L && e == cudaSuccess && cfg->weight_dtype != K2_F8; ++l) {
     e = launch_pack(c->wqkv(l), w->wq[l], w->wk[l], w->wv[l], PACK_QKV, z.qkv_n, z.H, z.wb, z.nq, z.nkv, z.d, s);
     if (e == cudaSuccess)
       e = launch_pack(c->wop(l), w->wo[l], nullptr, nullptr, PACK_PLAIN, z.H, z.nq * z.d, z.wb, 0, 0, 1, s);
@@ -1095,7 +1146,7 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     if (e == cudaSuccess)
       e = launch_pack(c->wdown(l), w->w_down[l], nullptr, nullptr, PACK_PLAIN, z.H, z.I, z.wb, 0, 0, 1, s);
   }
-  if (e == cudaSuccess)
+  if (e == cudaSuccess && cfg->weight_dtype != K2_F8)
     e = launch_pack(c->wlm(), w->lm_head, nullptr, nullptr, PACK_PLAIN, z.V, z.H, z.wb, 0, 0, 1, s);
   if (e != cudaSuccess) {
     g_init_error = std::string("repack: ") + cudaGetErrorString(e);
@@ -1106,6 +1157,11 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     g_init_error = std::string("persistent step set-up: ") + cudaGetErrorString(e);
     delete c;
     return K2_ERR_CUDA;
+  }
+  if (cfg->weight_dtype == K2_F8 && !c->mega_ok) {
+    g_init_error = "fp8 weights run on the persistent step only, which this shape / GPU does not support";
+    delete c;
+    return K2_ERR_UNSUPPORTED;
   }
   if ((e = plan_tc_prefill(c)) != cudaSuccess) {
     g_init_error = std::string("tensor-core prefill set-up: ") + cudaGetErrorString(e);
@@ -1314,7 +1370,11 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
   switch (option) {
     case K2_OPT_PDL: c->pdl = value != 0; break;
     case K2_OPT_GRAPH: c->graph = value != 0; break;
-    case K2_OPT_PERSISTENT: c->use_mega = value != 0; break;
+    case K2_OPT_PERSISTENT:
+      if (value == 0 && c->cfg.weight_dtype == K2_F8)
+        return c->fail(K2_ERR_UNSUPPORTED, "fp8 weights run on the persistent step only");
+      c->use_mega = value != 0;
+      break;
     case K2_OPT_TC_PREFILL: c->use_tc = value != 0; break;
     case K2_OPT_TC_DECODE: c->use_tc_decode = value != 0; break;
     case K2_OPT_ATTN_SPLITS:
@@ -1624,5 +1684,13 @@ k2_status k2_decode_speculative(k2_ctx* c, int32_t seq, const int32_t* h_tokens,
   std::copy(out, out + accepted + 1, h_out);
   *n_out = accepted + 1;
   return K2_OK;
+}
+
+k2_status k2_quantize_fp8(const void* d_src, int32_t rows, int32_t cols, uint8_t* d_codes, float* d_scales,
+                          void* stream) {
+  if (!d_src || !d_codes || !d_scales || rows < 0 || cols < 1) return K2_ERR_ARG;
+  const cudaError_t e = launch_quant_pack(d_codes, d_scales, d_src, nullptr, nullptr, PACK_PLAIN, rows, cols, 0, 0, 1,
+                                          false, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? K2_OK : K2_ERR_CUDA;
 }
 }  // extern "C"

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace k2 {
@@ -174,6 +175,24 @@ struct Unpack<__half> {
     for (int i = 0; i < 4; ++i) {
       float2 t = __half22float2(h[i]);
       f[2 * i] = t.x; f[2 * i + 1] = t.y;
+    }
+  }
+};
+// 16 bytes -> 16 floats (fp8 E4M3 codes; exact: every E4M3 value is an fp16 value)
+template <>
+struct Unpack<__nv_fp8_e4m3> {
+  static constexpr int N = 16;
+  __device__ __forceinline__ static void run(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> (16 * j)), __NV_E4M3);
+        const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&h));
+        f[4 * i + 2 * j] = t.x;
+        f[4 * i + 2 * j + 1] = t.y;
+      }
     }
   }
 };

@@ -403,6 +403,60 @@ __global__ void pack_kernel(WT* __restrict__ dst, const WT* __restrict__ s0, con
   }
 }
 
+// fp8 (E4M3) weight rows from bf16 (k2-burn README, "Post-training
+// quantization": fp8 checkpoints the engine runs directly): per packed row
+// (the row mapping of pack_kernel) s = max|w| / 448 and code = E4M3(w / s),
+// nearest with ties to even, saturating; a zero row gets s = 0 and codes 0.
+// packed != 0: codes in the packed pair/chunk layout; else row-major [N][K].
+__global__ void quant_pack_kernel(uint8_t* __restrict__ dst, float* __restrict__ scales,
+                                  const __nv_bfloat16* __restrict__ s0, const __nv_bfloat16* __restrict__ s1,
+                                  const __nv_bfloat16* __restrict__ s2, int mode, int N, int K, int CT, int nq,
+                                  int nkv, int d, int packed) {
+  constexpr int CH = 512;  // codes per row per chunk
+  __shared__ float red[32];
+  const int R = blockIdx.x, tid = threadIdx.x;
+  const __nv_bfloat16* src = nullptr;
+  if (R < N) {
+    if (mode == PACK_PLAIN) {
+      src = s0 + static_cast<size_t>(R) * K;
+    } else if (mode == PACK_GATEUP) {
+      src = ((R & 1) ? s1 : s0) + static_cast<size_t>(R >> 1) * K;
+    } else {
+      const int head = R / d, rr = R - head * d;
+      const int sr = (rr & 1) ? (rr >> 1) + d / 2 : (rr >> 1);
+      if (head < nq) src = s0 + (static_cast<size_t>(head) * d + sr) * K;
+      else if (head < nq + nkv) src = s1 + (static_cast<size_t>(head - nq) * d + sr) * K;
+      else src = s2 + (static_cast<size_t>(head - nq - nkv) * d + sr) * K;
+    }
+  }
+  float amax = 0.f;
+  if (src)
+    for (int e = tid; e < K; e += blockDim.x) amax = fmaxf(amax, fabsf(__bfloat162float(src[e])));
+  amax = warp_max(amax);
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+  if (tid < 32) {
+    float v = tid < static_cast<int>(blockDim.x >> 5) ? red[tid] : 0.f;
+    v = warp_max(v);
+    if (tid == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float scale = red[0] / 448.0f;
+  if (tid == 0) scales[R] = scale;
+  const int n = packed ? CT * CH : K;
+  for (int e = tid; e < n; e += blockDim.x) {
+    const float w = (src != nullptr && e < K) ? __bfloat162float(src[e]) : 0.f;
+    const uint8_t code = scale > 0.f ? static_cast<uint8_t>(__nv_cvt_float_to_fp8(w / scale, __NV_SATFINITE, __NV_E4M3))
+                                     : static_cast<uint8_t>(0);
+    if (packed) {
+      const int c = e / CH, i = e - c * CH;
+      dst[(static_cast<size_t>(R >> 1) * CT + c) * 2 * CH + (R & 1) * CH + i] = code;
+    } else {
+      dst[static_cast<size_t>(R) * K + e] = code;
+    }
+  }
+}
+
 template <typename WT>
 cudaError_t launch_typed(const PackedGemvArgs& a, int epi, const cudaLaunchConfig_t& cfg) {
   switch (epi) {
@@ -504,6 +558,18 @@ cudaError_t launch_pack(void* dst, const void* src0, const void* src1, const voi
     pack_kernel<float><<<rows, 256, 0, s>>>(static_cast<float*>(dst), static_cast<const float*>(src0),
                                             static_cast<const float*>(src1), static_cast<const float*>(src2), mode, N,
                                             K, CT, nq, nkv, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
+                              int mode, int N, int K, int nq, int nkv, int d, bool packed, cudaStream_t s) {
+  const int CT = (K + 511) / 512;
+  const int rows = packed ? 2 * ((N + 1) / 2) : N;
+  if (rows <= 0) return cudaSuccess;
+  quant_pack_kernel<<<rows, 256, 0, s>>>(dst, scales, static_cast<const __nv_bfloat16*>(src0),
+                                         static_cast<const __nv_bfloat16*>(src1),
+                                         static_cast<const __nv_bfloat16*>(src2), mode, N, K, CT, nq, nkv, d,
+                                         packed ? 1 : 0);
   return cudaGetLastError();
 }
 

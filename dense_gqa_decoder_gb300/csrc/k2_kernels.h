@@ -129,6 +129,11 @@ size_t packed_smem_bytes(const PackedGemvArgs& a);
 //                each head ordered (0, d/2), (1, d/2 + 1), ... (split-half RoPE pairs)
 //   PACK_GATEUP: row 2i = src0 row i, row 2i + 1 = src1 row i
 enum PackMode : int { PACK_PLAIN = 0, PACK_QKV = 1, PACK_GATEUP = 2 };
+// fp8 (E4M3) rows with one fp32 scale per row from bf16 sources (the row mapping
+// of launch_pack); packed: the pair/chunk layout with 512 codes per chunk,
+// else row-major codes [N][K].  scales get one entry per (padded) row.
+cudaError_t launch_quant_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
+                              int mode, int N, int K, int nq, int nkv, int d, bool packed, cudaStream_t s);
 cudaError_t launch_pack(void* dst, const void* src0, const void* src1, const void* src2, int mode, int N, int K,
                         int wbytes, int nq, int nkv, int d, cudaStream_t s);
 
@@ -221,6 +226,14 @@ cudaError_t launch_philox(uint32_t first, int n, uint32_t c1, uint32_t c2, uint3
                           uint32_t* out, cudaStream_t s);
 
 struct MegaArgs {
+  // fp8 weights: one fp32 scale per packed row of each matrix (null otherwise);
+  // layer l's scales at sc_* + l * ss_*
+  const float* sc_qkv;
+  const float* sc_o;
+  const float* sc_gu;
+  const float* sc_down;
+  const float* sc_lm;
+  size_t ss_qkv, ss_o, ss_gu, ss_down;
   int* hist;  // token history [seq][cap]: the step records its input token at its position (nullable)
   const LayerPtrs* layers;  // device table, n_layers entries (read once per launch: the norm gains)
   int n_layers;

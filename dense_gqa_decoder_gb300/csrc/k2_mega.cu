@@ -177,6 +177,7 @@ struct GDesc {
   const uint8_t* W;
   int N, K, CT, kind;
   const void* gain;
+  const float* scale;  // fp8 weights: the row scales (null otherwise)
 };
 
 __device__ __forceinline__ GDesc gdesc(const MegaArgs& a, const MegaShared& sh, int q, int qkv_n, int head_dim) {
@@ -185,19 +186,25 @@ __device__ __forceinline__ GDesc gdesc(const MegaArgs& a, const MegaShared& sh, 
   if (l >= a.n_layers) {  // the lm_head phase
     d.W = static_cast<const uint8_t*>(a.lm_head); d.N = a.vocab; d.K = a.hidden; d.CT = a.g_lm.CT; d.kind = 4;
     d.gain = a.final_norm;
+    d.scale = a.sc_lm;
     return d;
   }
   const size_t ul = static_cast<size_t>(l);
+  auto lsc = [&](const float* base, size_t stride) { return base ? base + ul * stride : nullptr; };
   if (j == PH_QKV) {
     d.W = a.w_qkv + ul * a.ws_qkv; d.N = qkv_n; d.K = a.hidden; d.CT = a.g_qkv.CT; d.kind = 0;
     d.gain = sh.gains[2 * l];
+    d.scale = lsc(a.sc_qkv, a.ss_qkv);
   } else if (j == PH_O) {
     d.W = a.w_o + ul * a.ws_o; d.N = a.hidden; d.K = a.nq * head_dim; d.CT = a.g_o.CT; d.kind = 1; d.gain = nullptr;
+    d.scale = lsc(a.sc_o, a.ss_o);
   } else if (j == PH_GU) {
     d.W = a.w_gu + ul * a.ws_gu; d.N = 2 * a.inter; d.K = a.hidden; d.CT = a.g_gu.CT; d.kind = 2;
     d.gain = sh.gains[2 * l + 1];
+    d.scale = lsc(a.sc_gu, a.ss_gu);
   } else {
     d.W = a.w_down + ul * a.ws_down; d.N = a.hidden; d.K = a.inter; d.CT = a.g_down.CT; d.kind = 3; d.gain = nullptr;
+    d.scale = lsc(a.sc_down, a.ss_down);
   }
   return d;
 }
@@ -434,12 +441,12 @@ __device__ __forceinline__ float load1(const WT* p, size_t e) {
 // stream.  x comes from xt (tagged, written by the previous phase with tag
 // tag_in) or, in the first phase, from x0f (fp32) or x0w (an embedding row).
 // rsd0f / rsd0w: where the first residual phase takes its old residual rows.
-template <typename WT, int D, typename KVT>
+template <typename WT, typename PT, int D, typename KVT>
 __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt, uint32_t tag_in, const float* x0f,
                         const WT* x0w, const float* rsd0f, const WT* rsd0w, const GEpi& ep, uint8_t* smem,
                         MegaShared& sh, Stream<D, KVT>& st, GainQ& gq, int& consumed, Best& best, int cta, int G,
                         int pos, int qkv_n) {
-  constexpr int EPL = Unpack<WT>::N;
+  constexpr int EPL = Unpack<PT>::N;  // packed weights per lane and row in a 512-byte chunk
   constexpr int CH = 32 * EPL;
   constexpr int NPL = EPL / 4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -577,6 +584,12 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
   int pl = r.ua / CT, c = r.ua - (r.ua / CT) * CT;
   bool pair_whole = (c == 0);
   float acc0 = 0.f, acc1 = 0.f;
+  // fp8: the current pair's row scales, loaded when the pair starts (used at its end)
+  float sc0 = 1.f, sc1 = 1.f;
+  if (d.scale && r.ub > r.ua) {
+    sc0 = __ldg(d.scale + 2 * (r.p0 + pl));
+    sc1 = __ldg(d.scale + 2 * (r.p0 + pl) + 1);
+  }
   for (int k = 0; k < r.nslots; ++k) {
     const int s = consumed % NS;
     const bool ok = mbar_wait(&sh.full[warp][s], static_cast<uint32_t>(consumed / NS) & 1u);
@@ -601,8 +614,8 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
         }
         const uint8_t* u8 = buf + (j + q) * kUnit + lane * 16;
         float w0[EPL], w1[EPL];
-        Unpack<WT>::run(*reinterpret_cast<const uint4*>(u8), w0);
-        Unpack<WT>::run(*reinterpret_cast<const uint4*>(u8 + 512), w1);
+        Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8), w0);
+        Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8 + 512), w1);
         float t0 = 0.f, t1 = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
@@ -617,7 +630,7 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
       const bool pair_end = (c == CT);
       const bool range_end = (u0 + j == r.ub);
       if (pair_end || range_end) {
-        const float s0 = warp_sum(acc0), s1 = warp_sum(acc1);
+        const float s0 = warp_sum(acc0) * sc0, s1 = warp_sum(acc1) * sc1;
         acc0 = acc1 = 0.f;
         if (lane == 0) {
           if (pair_whole && pair_end) {
@@ -634,6 +647,10 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
           ++pl;
           c = 0;
           pair_whole = true;
+          if (d.scale && r.ua + (u0 - r.ua) + j < r.ub) {
+            sc0 = __ldg(d.scale + 2 * (r.p0 + pl));
+            sc1 = __ldg(d.scale + 2 * (r.p0 + pl) + 1);
+          }
         }
       }
     }
@@ -1054,7 +1071,7 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
 }
 
 // ---- the step -------------------------------------------------------------------------------
-template <typename WT, int D, int REP, typename KVT>
+template <typename WT, typename PT, int D, int REP, typename KVT>
 __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ MegaShared sh;
@@ -1151,8 +1168,8 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
       xt = a.t_act;
       if (l == a.n_layers - 1) ep.plain = a.x_out;
     }
-    ok = g_phase<WT, D, KVT>(a, q, gdesc(a, sh, q, qkv_n, D), xt, tag_in, x0f, x0w, r0f, r0w, ep, smem, sh, st, gq,
-                             consumed, best, cta, G, pos, qkv_n);
+    ok = g_phase<WT, PT, D, KVT>(a, q, gdesc(a, sh, q, qkv_n, D), xt, tag_in, x0f, x0w, r0f, r0w, ep, smem, sh, st,
+                                 gq, consumed, best, cta, G, pos, qkv_n);
   }
   if (ok && a.head) {
     best = warp_best(best);
@@ -1214,24 +1231,28 @@ constexpr bool tile_fits() {
   return tile_keys<D, KVT>() > 0;
 }
 
-template <typename WT, int D, int REP, typename KVT>
+template <typename WT, typename PT, int D, int REP, typename KVT>
 const void* mega_fn() {
   if constexpr (tile_fits<D, KVT>())
-    return reinterpret_cast<const void*>(mega_decode_kernel<WT, D, REP, KVT>);
+    return reinterpret_cast<const void*>(mega_decode_kernel<WT, PT, D, REP, KVT>);
   else
     return nullptr;
 }
 
-// (weight type, head_dim, GQA ratio) combinations with a persistent kernel:
-// the 3.7B shape, the medium and the tiny test models
-#define K2_MEGA_SHAPES(X) X(__nv_bfloat16, 2, 128, 4) X(__nv_bfloat16, 2, 64, 4) X(float, 4, 16, 2)
+// (gain / embedding type, packed weight type and its bytes, head_dim, GQA
+// ratio) combinations with a persistent kernel: the 3.7B shape and the medium
+// model in bf16 and fp8 weights, the tiny fp32 model
+#define K2_MEGA_SHAPES(X)                                                                                         \
+  X(__nv_bfloat16, __nv_bfloat16, 2, 128, 4) X(__nv_bfloat16, __nv_bfloat16, 2, 64, 4) X(float, float, 4, 16, 2) \
+  X(__nv_bfloat16, __nv_fp8_e4m3, 1, 128, 4) X(__nv_bfloat16, __nv_fp8_e4m3, 1, 64, 4)
 
+// wbytes: bytes of one packed weight element (1 = fp8 E4M3)
 const void* mega_lookup(int wbytes, int head_dim, int rep, int kv_dtype) {
-#define K2_MEGA_LOOK(WT, WB, D, R)                                  \
-  if (wbytes == WB && head_dim == D && rep == R) {                  \
-    if (kv_dtype == 0) return mega_fn<WT, D, R, float>();           \
-    if (kv_dtype == 2) return mega_fn<WT, D, R, __half>();          \
-    if (kv_dtype == 3) return mega_fn<WT, D, R, int8_t>();          \
+#define K2_MEGA_LOOK(WT, PT, WB, D, R)                               \
+  if (wbytes == WB && head_dim == D && rep == R) {                   \
+    if (kv_dtype == 0) return mega_fn<WT, PT, D, R, float>();        \
+    if (kv_dtype == 2) return mega_fn<WT, PT, D, R, __half>();       \
+    if (kv_dtype == 3) return mega_fn<WT, PT, D, R, int8_t>();       \
   }
   K2_MEGA_SHAPES(K2_MEGA_LOOK)
 #undef K2_MEGA_LOOK

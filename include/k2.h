@@ -62,11 +62,16 @@ typedef enum {
                               written for another model architecture or KV format */
 } k2_status;
 
-typedef enum { K2_F32 = 0, K2_BF16 = 1, K2_F16 = 2, K2_I8 = 3 } k2_dtype;
+typedef enum { K2_F32 = 0, K2_BF16 = 1, K2_F16 = 2, K2_I8 = 3, K2_F8 = 4 } k2_dtype;
 
 /* Model shape and run limits (k2-burn README, "Model shape" and "KV cache
- * storage").  weight_dtype is K2_F32 or K2_BF16; kv_dtype is K2_F32, K2_F16
- * or K2_I8.  max_context = KV rows per sequence (prompt + generated tokens);
+ * storage").  weight_dtype is K2_F32, K2_BF16 or K2_F8; kv_dtype is K2_F32,
+ * K2_F16 or K2_I8.  K2_F8 (k2-burn README, "Post-training quantization"):
+ * the weights are given in bf16 and k2_init_weights stores every projection
+ * matrix and the lm_head as fp8 E4M3 rows with one fp32 scale per row (see
+ * k2_quantize_fp8); the embedding and the norm gains stay bf16.  Such a model
+ * runs on the persistent step only (prompts are appended one step per token)
+ * and is refused where that step is not available.  max_context = KV rows per sequence (prompt + generated tokens);
  * max_batch = number of independent sequences. */
 typedef struct {
   int32_t hidden, n_layers, n_heads, n_kv_heads, head_dim, intermediate, norm_groups, vocab;
@@ -371,6 +376,15 @@ enum {
  * launches[K2_K_COUNT]. */
 k2_status k2_profile_decode(k2_ctx* ctx, const int32_t* d_tokens, int32_t batch, int32_t* d_next, float* ms,
                             int32_t* launches, void* stream);
+
+/* The fp8 quantization of K2_F8 weights, on its own: each of `rows` bf16 rows
+ * of `cols` values at d_src (device, row-major) becomes d_scales[r] = max|w| /
+ * 448 (448: the largest finite E4M3 value) and d_codes[r * cols + c] =
+ * E4M3(w / scale), rounded to nearest with ties to even and saturating; a row
+ * of zeros gets scale 0 and codes 0.  The model computes with E4M3(code) *
+ * scale. */
+k2_status k2_quantize_fp8(const void* d_src, int32_t rows, int32_t cols, uint8_t* d_codes, float* d_scales,
+                          void* stream);
 
 /* ---- without a workspace ---------------------------------------------------- */
 

@@ -23,7 +23,7 @@ def k2():
 def declared_calls():
     text = open(os.path.join(ROOT, "include", "k2.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(k2_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(k2_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_every_declared_call_is_exported(k2):
