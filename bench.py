@@ -29,6 +29,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "batch-1 decode tok/s (3.7B dense GQA, bf16) and achieved HBM GB/s vs peak"
 WORKLOAD = "k2-horizon-3.7b-shape greedy decode, batch 1, context 4096, fp16 KV, bf16 weights"
+WEIGHT_DESC = {"bf16": "bf16", "f8": "fp8 E4M3 (per-row scales)", "q4": "int4 (one fp32 scale per 64 weights)"}
 CTX = 4096
 SHAPE_NAME = "k2_3p7b"
 FALLBACK_HBM_GBS = 6800.0
@@ -46,8 +47,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--layers", type=int, default=0, help="override layer count (debug)")
     p.add_argument("--kv", default="f16", choices=["f16", "i8"], help="KV cache storage")
-    p.add_argument("--weights", default="bf16", choices=["bf16", "f8"],
-                   help="stored projection weights: bf16, or fp8 E4M3 rows with per-row scales (quantized at init)")
+    p.add_argument("--weights", default="bf16", choices=["bf16", "f8", "q4"],
+                   help="stored projection weights: bf16, fp8 E4M3 rows with per-row scales, or int4 codes with "
+                        "one scale per 64 weights of a row (both quantized at init)")
     p.add_argument("--temperature", type=float, default=0.0,
                    help="> 0: sample each token (with --top-k / --top-p / --min-p / --repetition-penalty / "
                         "--seed) instead of the greedy argmax")
@@ -77,18 +79,20 @@ def parse():
 def algorithmic_bytes(s, ctx_len: int, kv: str = "f16", weights_store: str = "bf16") -> dict:
     """Bytes the decode step must move at context ctx_len (weights once, the
     KV history once, plus the small activations).  fp8 weights: one byte per
-    weight plus a 4-byte scale per row; gains and the embedding row stay bf16."""
+    weight plus a 4-byte scale per row; int4: half a byte per weight plus a
+    4-byte scale per 64 weights; gains and the embedding row stay bf16."""
     H, d, I, V = s.hidden, s.head_dim, s.intermediate, s.vocab
     qkv_n = (s.n_heads + 2 * s.n_kv_heads) * d
     gb = 2 if s.weight_dtype == "bf16" else 4
-    if weights_store == "f8":
-        wb = 1
-        per_layer = (qkv_n * H + H * s.n_heads * d + 2 * I * H + H * I) + 4 * (qkv_n + H + 2 * I + H) + 2 * H * gb
-        weights = s.n_layers * per_layer + V * H + 4 * V + H * gb
-    else:
-        wb = gb
-        per_layer = (qkv_n * H + H * s.n_heads * d + 2 * I * H + H * I + 2 * H) * wb
-        weights = s.n_layers * per_layer + V * H * wb + H * wb
+    def mat(N, K):  # bytes of one stored projection matrix [N, K]
+        if weights_store == "f8":  # one byte per weight, one fp32 scale per row
+            return N * K + 4 * N
+        if weights_store == "q4":  # half a byte per weight, one fp32 scale per 64 weights of a row
+            return N * K // 2 + 4 * N * ((K + 63) // 64)
+        return N * K * gb
+
+    per_layer = mat(qkv_n, H) + mat(H, s.n_heads * d) + mat(2 * I, H) + mat(H, I) + 2 * H * gb
+    weights = s.n_layers * per_layer + mat(V, H) + H * gb
     # K and V of one position, one layer: fp16, or int8 codes + one fp16 scale per head
     kv_row = 2 * s.n_kv_heads * d * 2 if kv == "f16" else 2 * s.n_kv_heads * (d + 2)
     kv = s.n_layers * kv_row * ctx_len
@@ -97,7 +101,7 @@ def algorithmic_bytes(s, ctx_len: int, kv: str = "f16", weights_store: str = "bf
         "kv": kv,
         "total": weights + kv,
         # the gate/up GEMV: W [2I, H] + x [H] fp32 + gain [H] + act [I] fp32
-        "gate_up_launch": 2 * I * H * wb + H * 4 + H * wb + I * 4,
+        "gate_up_launch": mat(2 * I, H) + H * 4 + H * gb + I * 4,
         # the persistent step kernel: weights, the KV history, the new K/V rows
         "step_launch": weights + kv + s.n_layers * kv_row,
     }
@@ -325,7 +329,7 @@ def run_ours(args, world, rank, local, pg):
         s = s.replace(n_layers=args.layers)
     budget = args.ctx + args.warmup + args.steps + args.profile_steps + args.e2e_steps + 16
     cfg = k2.make_config(s, max_context=budget, max_batch=1, kv_dtype=args.kv,
-                         weights=args.weights if args.weights == "f8" else None)
+                         weights=None if args.weights == "bf16" else args.weights)
     ctx = k2.Context(cfg, random_device_weights(s, seed=1234 + rank))
     stream = torch.cuda.Stream()
     sampled = args.temperature > 0
@@ -440,11 +444,11 @@ def run_ours(args, world, rank, local, pg):
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if args.weights == "bf16" else "f8e4m3", "data": "synthetic",
+        "vs_baseline": None, "dtype": {"bf16": "bf16", "f8": "f8e4m3", "q4": "i4"}[args.weights], "data": "synthetic",
         "config": {"workload": WORKLOAD if (args.kv == "f16" and args.ctx == CTX and not sampled and
                                             args.weights == "bf16") else
                    f"k2-horizon-3.7b-shape {'sampled' if sampled else 'greedy'} decode, batch 1, context {args.ctx}, "
-                   f"{args.kv} KV, {'fp8 E4M3 (per-row scales)' if args.weights == 'f8' else 'bf16'} weights",
+                   f"{args.kv} KV, {WEIGHT_DESC[args.weights]} weights",
                    "sampling": ({"temperature": args.temperature, "top_k": args.top_k, "top_p": args.top_p,
                                  "min_p": args.min_p, "repetition_penalty": args.repetition_penalty,
                                  "seed": args.seed} if sampled else None),
@@ -468,7 +472,7 @@ def run_ours(args, world, rank, local, pg):
                     "note": ("useful FLOPs (2 per weight x token + causal attention); the GEMMs issue twice "
                              "the linear MMAs (activations as bf16 hi + lo halves); attention issues mma.sync "
                              "on fp16 hi + lo halves of the queries and probabilities") if args.weights == "bf16" else
-                            "fp8 weights have no tensor-core GEMM path: the prompt runs through the decode step, "
+                            "quantized weights have no tensor-core GEMM path: the prompt runs through the decode step, "
                             "one token at a time"},
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
         "clocks": clk,

@@ -59,8 +59,11 @@ struct Layout {
 
 struct Sizes {
   int H, L, nq, nkv, d, I, G, V, ctx, B, qkv_n, rep, wb, kvb;
-  int gb;  // bytes of an embedding / gain element (bf16 for fp8 weights); wb: of a packed weight
+  int gb;  // bytes of an embedding / gain element (bf16 for fp8 / int4 weights); wb: of a packed weight
+  int wf;  // the packed weight format key of the persistent step (kWfmt*: weight bytes, or kWfmtQ4)
 };
+
+bool quantized(int weight_dtype) { return weight_dtype == K2_F8 || weight_dtype == K2_Q4; }
 
 Sizes sizes_of(const k2_config& c) {
   Sizes s;
@@ -69,7 +72,8 @@ Sizes sizes_of(const k2_config& c) {
   s.qkv_n = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
   s.rep = c.n_kv_heads > 0 ? c.n_heads / c.n_kv_heads : 0;
   s.wb = elt_bytes(c.weight_dtype);
-  s.gb = c.weight_dtype == K2_F8 ? 2 : s.wb;
+  s.gb = quantized(c.weight_dtype) ? 2 : s.wb;
+  s.wf = c.weight_dtype == K2_Q4 ? kWfmtQ4 : s.wb;
   s.kvb = elt_bytes(c.kv_dtype);
   return s;
 }
@@ -142,15 +146,17 @@ Layout layout_of(const k2_config& c) {
     l.vpi = take(nv * kArgmaxPartsMax * 4);
   }
   const size_t scratch_end = o;
-  l.wqkv_layer = align_up(packed_bytes(s.qkv_n, s.H, s.wb), kAlign);
-  l.wo_layer = align_up(packed_bytes(s.H, s.nq * s.d, s.wb), kAlign);
-  l.wgu_layer = align_up(packed_bytes(2 * s.I, s.H, s.wb), kAlign);
-  l.wdown_layer = align_up(packed_bytes(s.H, s.I, s.wb), kAlign);
+  // int4: codes and block scales in kQ4Unit units; else wb-byte weights in 1024-byte units
+  auto pbytes = [&](int N, int K) { return c.weight_dtype == K2_Q4 ? q4_packed_bytes(N, K) : packed_bytes(N, K, s.wb); };
+  l.wqkv_layer = align_up(pbytes(s.qkv_n, s.H), kAlign);
+  l.wo_layer = align_up(pbytes(s.H, s.nq * s.d), kAlign);
+  l.wgu_layer = align_up(pbytes(2 * s.I, s.H), kAlign);
+  l.wdown_layer = align_up(pbytes(s.H, s.I), kAlign);
   l.wqkv = take(l.wqkv_layer * s.L);
   l.wo = take(l.wo_layer * s.L);
   l.wgu = take(l.wgu_layer * s.L);
   l.wdown = take(l.wdown_layer * s.L);
-  l.wlm = take(packed_bytes(s.V, s.H, s.wb));
+  l.wlm = take(pbytes(s.V, s.H));
   l.repack_bytes = o - scratch_end;
   const size_t kv_start = o;
   l.kv_layer = align_up(static_cast<size_t>(s.B) * s.nkv * l.cap * s.d * s.kvb, kAlign);
@@ -173,8 +179,9 @@ std::string check_config(const k2_config* c) {
   if (c->n_heads % c->n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
   if (c->head_dim % 2) return "head_dim must be even (split-half RoPE)";
   if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) return "eps must be >= 0 and rope_theta > 0";
-  if (c->weight_dtype != K2_F32 && c->weight_dtype != K2_BF16 && c->weight_dtype != K2_F8)
-    return "weight_dtype must be K2_F32, K2_BF16 or K2_F8";
+  if (c->weight_dtype != K2_F32 && c->weight_dtype != K2_BF16 && c->weight_dtype != K2_F8 &&
+      c->weight_dtype != K2_Q4)
+    return "weight_dtype must be K2_F32, K2_BF16, K2_F8 or K2_Q4";
   if (c->kv_dtype != K2_F32 && c->kv_dtype != K2_F16 && c->kv_dtype != K2_I8)
     return "kv_dtype must be K2_F32, K2_F16 or K2_I8";
   if (c->max_batch > 64) return "max_batch above 64 is not supported";
@@ -415,7 +422,7 @@ void enqueue_token(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in
     m.head = head ? 1 : 0;
     const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
     cudaStream_t st = ln.s;
-    ln.run(K2_K_STEP, [&] { return launch_mega(m, c->s.wb, c->s.d, c->s.rep, kvdt, c->mega_grid, st); });
+    ln.run(K2_K_STEP, [&] { return launch_mega(m, c->s.wf, c->s.d, c->s.rep, kvdt, c->mega_grid, st); });
   } else {
     chain_b1(c, ln, seq, tok, x_in, next, logits, head);
   }
@@ -468,7 +475,7 @@ void enqueue_decode(k2_ctx* c, Launcher& ln, const int* d_tokens, int batch, int
 
 bool plan_all(k2_ctx* c) {
   const Sizes& s = c->s;
-  // the kernel chain streams bf16 / fp32 weights; fp8 models run the
+  // the kernel chain streams bf16 / fp32 weights; fp8 and int4 models run the
   // persistent step only (their chain plans, in bf16 terms, are never launched)
   const int wb = s.gb;
   PackedGemvArgs base = {};
@@ -525,13 +532,18 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   const Sizes& s = c->s;
   const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
   c->mega_ok = false;
-  if (!mega_supported(s.wb, s.d, s.rep, kvdt)) return cudaSuccess;
+  if (!mega_supported(s.wf, s.d, s.rep, kvdt)) return cudaSuccess;
+  const bool q4 = c->cfg.weight_dtype == K2_Q4;
   const PackedGemvArgs* plans[5] = {&c->p_qkv, &c->p_o, &c->p_gu, &c->p_down, &c->p_lm};
-  for (const PackedGemvArgs* p : plans)
-    if (p->x_bytes > static_cast<uint32_t>(kMegaXBytes)) return cudaSuccess;
-  cudaError_t e = mega_init_attrs(s.wb, s.d, s.rep, kvdt);
+  for (const PackedGemvArgs* p : plans) {
+    // the input vector, padded to whole chunks, fits its buffer (a gain phase: 4096 values)
+    const size_t kp = q4 ? static_cast<size_t>((p->K + kQ4Chunk - 1) / kQ4Chunk) * kQ4Chunk : p->x_bytes / 4;
+    if (p->x_bytes > static_cast<uint32_t>(kMegaXBytes) || kp * 4 > static_cast<size_t>(kMegaXBytes)) return cudaSuccess;
+    if (p->gain && kp > 4096) return cudaSuccess;
+  }
+  cudaError_t e = mega_init_attrs(s.wf, s.d, s.rep, kvdt);
   if (e != cudaSuccess) return e;
-  int grid = mega_max_grid(s.wb, s.d, s.rep, kvdt);
+  int grid = mega_max_grid(s.wf, s.d, s.rep, kvdt);
   // every CTA must own rows of every layer GEMV (the dataflow waits rely on it)
   grid = std::min(grid, std::min(s.qkv_n / 2, std::min((s.H + 1) / 2, s.I)));
   if (grid < s.nkv) return cudaSuccess;
@@ -567,9 +579,9 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   LayerPtrs* dtab = reinterpret_cast<LayerPtrs*>(c->ws + c->lay.ltab);
   e = cudaMemcpyAsync(dtab, c->ltab.data(), sizeof(LayerPtrs) * s.L, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return e;
-  auto gplan = [&](const PackedGemvArgs& p) {  // 512-byte chunks of packed (wb-byte) weights per row pair
+  auto gplan = [&](const PackedGemvArgs& p) {  // 512-byte chunks of packed weights per row
     MegaGemv g;
-    g.CT = (p.K * s.wb + 511) / 512;
+    g.CT = q4 ? (p.K + kQ4Chunk - 1) / kQ4Chunk : (p.K * s.wb + 511) / 512;
     return g;
   };
   MegaArgs& m = c->mega;
@@ -1117,6 +1129,24 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     return K2_ERR_CUDA;
   }
   const Sizes& z = c->s;
+  if (cfg->weight_dtype == K2_Q4) {  // quantize the bf16 inputs into int4 units (codes + block scales)
+    for (int l = 0; l < z.L && e == cudaSuccess; ++l) {
+      e = launch_q4_pack(static_cast<uint8_t*>(c->wqkv(l)), nullptr, w->wq[l], w->wk[l], w->wv[l], PACK_QKV, z.qkv_n,
+                         z.H, z.nq, z.nkv, z.d, true, s);
+      if (e == cudaSuccess)
+        e = launch_q4_pack(static_cast<uint8_t*>(c->wop(l)), nullptr, w->wo[l], nullptr, nullptr, PACK_PLAIN, z.H,
+                           z.nq * z.d, 0, 0, 1, true, s);
+      if (e == cudaSuccess)
+        e = launch_q4_pack(static_cast<uint8_t*>(c->wgu(l)), nullptr, w->w_gate[l], w->w_up[l], nullptr, PACK_GATEUP,
+                           2 * z.I, z.H, 0, 0, 1, true, s);
+      if (e == cudaSuccess)
+        e = launch_q4_pack(static_cast<uint8_t*>(c->wdown(l)), nullptr, w->w_down[l], nullptr, nullptr, PACK_PLAIN,
+                           z.H, z.I, 0, 0, 1, true, s);
+    }
+    if (e == cudaSuccess)
+      e = launch_q4_pack(static_cast<uint8_t*>(c->wlm()), nullptr, w->lm_head, nullptr, nullptr, PACK_PLAIN, z.V, z.H,
+                         0, 0, 1, true, s);
+  }
   if (cfg->weight_dtype == K2_F8) {  // quantize the bf16 inputs into fp8 rows + scales
     auto sc = [&](size_t base, size_t stride, int l) { return reinterpret_cast<float*>(ws + base + stride * l); };
     const auto& L = c->lay;
@@ -1137,7 +1167,7 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
       e = launch_quant_pack(static_cast<uint8_t*>(c->wlm()), reinterpret_cast<float*>(ws + L.slm), w->lm_head, nullptr,
                             nullptr, PACK_PLAIN, z.V, z.H, 0, 0, 1, true, s);
   }
-  for (int l = 0; l < z.L && e == cudaSuccess && cfg->weight_dtype != K2_F8; ++l) {
+  for (int l = 0; l < z.L && e == cudaSuccess && !quantized(cfg->weight_dtype); ++l) {
     e = launch_pack(c->wqkv(l), w->wq[l], w->wk[l], w->wv[l], PACK_QKV, z.qkv_n, z.H, z.wb, z.nq, z.nkv, z.d, s);
     if (e == cudaSuccess)
       e = launch_pack(c->wop(l), w->wo[l], nullptr, nullptr, PACK_PLAIN, z.H, z.nq * z.d, z.wb, 0, 0, 1, s);
@@ -1146,7 +1176,7 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     if (e == cudaSuccess)
       e = launch_pack(c->wdown(l), w->w_down[l], nullptr, nullptr, PACK_PLAIN, z.H, z.I, z.wb, 0, 0, 1, s);
   }
-  if (e == cudaSuccess && cfg->weight_dtype != K2_F8)
+  if (e == cudaSuccess && !quantized(cfg->weight_dtype))
     e = launch_pack(c->wlm(), w->lm_head, nullptr, nullptr, PACK_PLAIN, z.V, z.H, z.wb, 0, 0, 1, s);
   if (e != cudaSuccess) {
     g_init_error = std::string("repack: ") + cudaGetErrorString(e);
@@ -1158,8 +1188,8 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     delete c;
     return K2_ERR_CUDA;
   }
-  if (cfg->weight_dtype == K2_F8 && !c->mega_ok) {
-    g_init_error = "fp8 weights run on the persistent step only, which this shape / GPU does not support";
+  if (quantized(cfg->weight_dtype) && !c->mega_ok) {
+    g_init_error = "fp8 and int4 weights run on the persistent step only, which this shape / GPU does not support";
     delete c;
     return K2_ERR_UNSUPPORTED;
   }
@@ -1371,8 +1401,8 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
     case K2_OPT_PDL: c->pdl = value != 0; break;
     case K2_OPT_GRAPH: c->graph = value != 0; break;
     case K2_OPT_PERSISTENT:
-      if (value == 0 && c->cfg.weight_dtype == K2_F8)
-        return c->fail(K2_ERR_UNSUPPORTED, "fp8 weights run on the persistent step only");
+      if (value == 0 && quantized(c->cfg.weight_dtype))
+        return c->fail(K2_ERR_UNSUPPORTED, "fp8 and int4 weights run on the persistent step only");
       c->use_mega = value != 0;
       break;
     case K2_OPT_TC_PREFILL: c->use_tc = value != 0; break;
@@ -1691,6 +1721,14 @@ k2_status k2_quantize_fp8(const void* d_src, int32_t rows, int32_t cols, uint8_t
   if (!d_src || !d_codes || !d_scales || rows < 0 || cols < 1) return K2_ERR_ARG;
   const cudaError_t e = launch_quant_pack(d_codes, d_scales, d_src, nullptr, nullptr, PACK_PLAIN, rows, cols, 0, 0, 1,
                                           false, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? K2_OK : K2_ERR_CUDA;
+}
+
+k2_status k2_quantize_q4(const void* d_src, int32_t rows, int32_t cols, int8_t* d_codes, float* d_scales,
+                         void* stream) {
+  if (!d_src || !d_codes || !d_scales || rows < 0 || cols < 1) return K2_ERR_ARG;
+  const cudaError_t e = launch_q4_pack(reinterpret_cast<uint8_t*>(d_codes), d_scales, d_src, nullptr, nullptr,
+                                       PACK_PLAIN, rows, cols, 0, 0, 1, false, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? K2_OK : K2_ERR_CUDA;
 }
 }  // extern "C"

@@ -210,6 +210,45 @@ struct Unpack<int8_t> {
   }
 };
 
+// int4 weights, symmetric block quantization: codes c in [-7, 7] stored as
+// the nibble c + 8, one fp32 scale per 64 consecutive weights of a row.  A tag
+// type for the packed stream format, which carries each chunk's block scales
+// beside its codes.
+struct q4_block64 {};
+
+// The code of nibble K (0..4) of w as a float, exactly: the nibble v is OR-ed
+// into the mantissa of 2^23, which gives the float 2^23 + v 16^K; one fma by
+// 16^-K with -(2^23 16^-K + 8) leaves v - 8 (an integer: no rounding).
+template <int K>
+__device__ __forceinline__ float q4_code(uint32_t w) {
+  static_assert(K >= 0 && K <= 4, "the nibble must lie inside the 23-bit mantissa");
+  constexpr float inv = 1.0f / static_cast<float>(1u << (4 * K));
+  constexpr float off = -(8388608.0f * inv + 8.0f);
+  return fmaf(__uint_as_float((w & (0xFu << (4 * K))) | 0x4B000000u), inv, off);
+}
+
+// Partial dot products of two rows' words a, b (8 codes each, nibble k =
+// element k) with x[0..7]; nibbles 5..7 are shifted down to positions 2..4.
+__device__ __forceinline__ void q4_dot8(uint32_t a, uint32_t b, const float* x, float& ta, float& tb) {
+  const uint32_t a2 = a >> 12, b2 = b >> 12;
+  ta = fmaf(q4_code<0>(a), x[0], ta);
+  tb = fmaf(q4_code<0>(b), x[0], tb);
+  ta = fmaf(q4_code<1>(a), x[1], ta);
+  tb = fmaf(q4_code<1>(b), x[1], tb);
+  ta = fmaf(q4_code<2>(a), x[2], ta);
+  tb = fmaf(q4_code<2>(b), x[2], tb);
+  ta = fmaf(q4_code<3>(a), x[3], ta);
+  tb = fmaf(q4_code<3>(b), x[3], tb);
+  ta = fmaf(q4_code<4>(a), x[4], ta);
+  tb = fmaf(q4_code<4>(b), x[4], tb);
+  ta = fmaf(q4_code<2>(a2), x[5], ta);
+  tb = fmaf(q4_code<2>(b2), x[5], tb);
+  ta = fmaf(q4_code<3>(a2), x[6], ta);
+  tb = fmaf(q4_code<3>(b2), x[6], tb);
+  ta = fmaf(q4_code<4>(a2), x[7], ta);
+  tb = fmaf(q4_code<4>(b2), x[7], tb);
+}
+
 template <typename T>
 __device__ __forceinline__ float to_f32(T v);
 template <>

@@ -376,26 +376,27 @@ __global__ void __launch_bounds__(kPackedThreads, 1) packed_gemv_kernel(const Pa
 }
 
 // ---- packing (set-up) ----------------------------------------------------------------------
+// The source row of packed row R (null past N), per PackMode.
+template <typename WT>
+__device__ __forceinline__ const WT* pack_src_row(const WT* s0, const WT* s1, const WT* s2, int mode, int R, int N,
+                                                  int K, int nq, int nkv, int d) {
+  if (R >= N) return nullptr;
+  if (mode == PACK_PLAIN) return s0 + static_cast<size_t>(R) * K;
+  if (mode == PACK_GATEUP) return ((R & 1) ? s1 : s0) + static_cast<size_t>(R >> 1) * K;
+  const int head = R / d, rr = R - head * d;
+  const int sr = (rr & 1) ? (rr >> 1) + d / 2 : (rr >> 1);
+  if (head < nq) return s0 + (static_cast<size_t>(head) * d + sr) * K;
+  if (head < nq + nkv) return s1 + (static_cast<size_t>(head - nq) * d + sr) * K;
+  return s2 + (static_cast<size_t>(head - nq - nkv) * d + sr) * K;
+}
+
 template <typename WT>
 __global__ void pack_kernel(WT* __restrict__ dst, const WT* __restrict__ s0, const WT* __restrict__ s1,
                             const WT* __restrict__ s2, int mode, int N, int K, int CT, int nq, int nkv, int d) {
   constexpr int CH = 512 / sizeof(WT);
   const int R = blockIdx.x;  // packed row index (2 * pair + r)
   const int pair = R >> 1, r = R & 1;
-  const WT* src = nullptr;
-  if (R < N) {
-    if (mode == PACK_PLAIN) {
-      src = s0 + static_cast<size_t>(R) * K;
-    } else if (mode == PACK_GATEUP) {
-      src = ((R & 1) ? s1 : s0) + static_cast<size_t>(R >> 1) * K;
-    } else {
-      const int head = R / d, rr = R - head * d;
-      const int sr = (rr & 1) ? (rr >> 1) + d / 2 : (rr >> 1);
-      if (head < nq) src = s0 + (static_cast<size_t>(head) * d + sr) * K;
-      else if (head < nq + nkv) src = s1 + (static_cast<size_t>(head - nq) * d + sr) * K;
-      else src = s2 + (static_cast<size_t>(head - nq - nkv) * d + sr) * K;
-    }
-  }
+  const WT* src = pack_src_row(s0, s1, s2, mode, R, N, K, nq, nkv, d);
   WT* out = dst + static_cast<size_t>(pair) * CT * 2 * CH + r * CH;
   for (int e = threadIdx.x; e < CT * CH; e += blockDim.x) {
     const int c = e / CH, i = e - c * CH;
@@ -415,20 +416,7 @@ __global__ void quant_pack_kernel(uint8_t* __restrict__ dst, float* __restrict__
   constexpr int CH = 512;  // codes per row per chunk
   __shared__ float red[32];
   const int R = blockIdx.x, tid = threadIdx.x;
-  const __nv_bfloat16* src = nullptr;
-  if (R < N) {
-    if (mode == PACK_PLAIN) {
-      src = s0 + static_cast<size_t>(R) * K;
-    } else if (mode == PACK_GATEUP) {
-      src = ((R & 1) ? s1 : s0) + static_cast<size_t>(R >> 1) * K;
-    } else {
-      const int head = R / d, rr = R - head * d;
-      const int sr = (rr & 1) ? (rr >> 1) + d / 2 : (rr >> 1);
-      if (head < nq) src = s0 + (static_cast<size_t>(head) * d + sr) * K;
-      else if (head < nq + nkv) src = s1 + (static_cast<size_t>(head - nq) * d + sr) * K;
-      else src = s2 + (static_cast<size_t>(head - nq - nkv) * d + sr) * K;
-    }
-  }
+  const __nv_bfloat16* src = pack_src_row(s0, s1, s2, mode, R, N, K, nq, nkv, d);
   float amax = 0.f;
   if (src)
     for (int e = tid; e < K; e += blockDim.x) amax = fmaxf(amax, fabsf(__bfloat162float(src[e])));
@@ -454,6 +442,52 @@ __global__ void quant_pack_kernel(uint8_t* __restrict__ dst, float* __restrict__
     } else {
       dst[static_cast<size_t>(R) * K + e] = code;
     }
+  }
+}
+
+// int4 block quantization (k2-burn README, "Quantization": int4 checkpoints
+// with block size 64): one CTA of kQ4Chunk / 4 threads per (packed row R,
+// chunk c); thread t takes weights 4t .. 4t + 3 of the chunk, 16 threads one
+// 64-weight block.  s = max|w| / 7; code = w / s rounded to nearest, ties to
+// even, clamped to [-7, 7]; a zero block gets s = 0 and codes 0.  Packed:
+// nibble c + 8, element 2i in the low nibble of byte i, into the int4 unit
+// layout (kQ4Unit); plain: int8 codes [N][K], scales [N][ceil(K / 64)].
+__global__ void __launch_bounds__(kQ4Chunk / 4) q4_pack_kernel(uint8_t* __restrict__ dst, float* __restrict__ scales,
+                                                      const __nv_bfloat16* __restrict__ s0,
+                                                      const __nv_bfloat16* __restrict__ s1,
+                                                      const __nv_bfloat16* __restrict__ s2, int mode, int N, int K,
+                                                      int CT, int nq, int nkv, int d, int packed) {
+  const int R = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
+  const __nv_bfloat16* src = pack_src_row(s0, s1, s2, mode, R, N, K, nq, nkv, d);
+  const int e0 = c * kQ4Chunk + 4 * tid;  // the thread's first weight in the row
+  float w[4];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    w[i] = (src != nullptr && e0 + i < K) ? __bfloat162float(src[e0 + i]) : 0.f;
+    amax = fmaxf(amax, fabsf(w[i]));
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));  // the 16 threads
+  const float s = __fdiv_rn(amax, 7.0f);
+  int q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = s > 0.f ? max(-7, min(7, __float2int_rn(__fdiv_rn(w[i], s)))) : 0;
+  const int blk = tid >> 4;  // the block within the chunk
+  if (packed) {
+    uint8_t* unit = dst + (static_cast<size_t>(R >> 1) * CT + c) * kQ4Unit;
+    const uint32_t b0 = static_cast<uint32_t>(q[0] + 8) | (static_cast<uint32_t>(q[1] + 8) << 4);
+    const uint32_t b1 = static_cast<uint32_t>(q[2] + 8) | (static_cast<uint32_t>(q[3] + 8) << 4);
+    *reinterpret_cast<uint16_t*>(unit + (R & 1) * (kQ4Chunk / 2) + 2 * tid) = static_cast<uint16_t>(b0 | (b1 << 8));
+    if ((tid & 15) == 0)
+      *reinterpret_cast<float*>(unit + kQ4Chunk + (R & 1) * (kQ4Chunk / kQ4Block) * 4 + blk * 4) = s;
+  } else if (R < N) {
+    const int nb = (K + kQ4Block - 1) / kQ4Block;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (e0 + i < K) dst[static_cast<size_t>(R) * K + e0 + i] = static_cast<uint8_t>(static_cast<int8_t>(q[i]));
+    const int b = c * (kQ4Chunk / kQ4Block) + blk;
+    if ((tid & 15) == 0 && b < nb) scales[static_cast<size_t>(R) * nb + b] = s;
   }
 }
 
@@ -558,6 +592,23 @@ cudaError_t launch_pack(void* dst, const void* src0, const void* src1, const voi
     pack_kernel<float><<<rows, 256, 0, s>>>(static_cast<float*>(dst), static_cast<const float*>(src0),
                                             static_cast<const float*>(src1), static_cast<const float*>(src2), mode, N,
                                             K, CT, nq, nkv, d);
+  return cudaGetLastError();
+}
+
+size_t q4_packed_bytes(int N, int K) {
+  const size_t CT = (static_cast<size_t>(K) + kQ4Chunk - 1) / kQ4Chunk;
+  return (static_cast<size_t>(N) + 1) / 2 * CT * kQ4Unit;
+}
+
+cudaError_t launch_q4_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
+                           int mode, int N, int K, int nq, int nkv, int d, bool packed, cudaStream_t s) {
+  const int CT = (K + kQ4Chunk - 1) / kQ4Chunk;
+  const int rows = packed ? 2 * ((N + 1) / 2) : N;
+  if (rows <= 0 || CT <= 0) return cudaSuccess;
+  q4_pack_kernel<<<dim3(rows, CT), kQ4Chunk / 4, 0, s>>>(dst, scales, static_cast<const __nv_bfloat16*>(src0),
+                                                static_cast<const __nv_bfloat16*>(src1),
+                                                static_cast<const __nv_bfloat16*>(src2), mode, N, K, CT, nq, nkv, d,
+                                                packed ? 1 : 0);
   return cudaGetLastError();
 }
 

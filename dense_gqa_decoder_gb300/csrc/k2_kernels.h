@@ -134,6 +134,14 @@ enum PackMode : int { PACK_PLAIN = 0, PACK_QKV = 1, PACK_GATEUP = 2 };
 // else row-major codes [N][K].  scales get one entry per (padded) row.
 cudaError_t launch_quant_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
                               int mode, int N, int K, int nq, int nkv, int d, bool packed, cudaStream_t s);
+// int4 block quantization (symmetric, codes in [-7, 7], s = max|w| / 7 per 64
+// weights of a row, nearest with ties to even) of bf16 sources, with the row
+// mapping of launch_pack.  packed: the int4 unit layout (kQ4Unit bytes per
+// 1024-weight chunk of a row pair; dst only, scales unused); else plain
+// int8 codes [N][K] and scales [N][ceil(K / 64)].
+cudaError_t launch_q4_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
+                           int mode, int N, int K, int nq, int nkv, int d, bool packed, cudaStream_t s);
+size_t q4_packed_bytes(int N, int K);
 cudaError_t launch_pack(void* dst, const void* src0, const void* src1, const void* src2, int mode, int N, int K,
                         int wbytes, int nq, int nkv, int d, cudaStream_t s);
 
@@ -289,12 +297,23 @@ constexpr unsigned kMegaPollSleepNs = 0;      // pause between rounds of a tag p
 constexpr int kMegaPairsMax = 64;             // row pairs of one CTA in the QKV / residual phases
 constexpr int kMegaSplitMax = 64;             // key splits per KV head in the attention phase
 constexpr int kMegaTagShift = 10;
-constexpr int kMegaMaxLayers = 64;            // norm-gain pointers kept in shared memory             // tag = (epoch + 1) << 10 | phase: at most 1023 phases
+constexpr int kMegaMaxLayers = 64;            // norm-gain pointers kept in shared memory
+// tag = (epoch + 1) << kMegaTagShift | phase: at most 1023 phases
 
-bool mega_supported(int wbytes, int head_dim, int rep, int kv_dtype);
-cudaError_t mega_init_attrs(int wbytes, int head_dim, int rep, int kv_dtype);
-int mega_max_grid(int wbytes, int head_dim, int rep, int kv_dtype);  // 0: cannot run
-cudaError_t launch_mega(const MegaArgs& a, int wbytes, int head_dim, int rep, int kv_dtype, int grid,
+// Packed weight formats of the persistent step, the key that picks its
+// kernel: the bytes of one weight for fp32 (4), bf16 (2) and fp8 E4M3 (1), or
+// kWfmtQ4 for int4 codes with one fp32 scale per 64 weights of a row.  An
+// int4 unit is a 512-weight chunk of both rows of a pair: row 0's 256 bytes
+// of codes, row 1's, then row 0's 8 block scales and row 1's.
+constexpr int kWfmtQ4 = 5;
+constexpr int kQ4Block = 64;
+constexpr int kQ4Chunk = 512;  // weights per row in one unit
+constexpr int kQ4Unit = 576;
+
+bool mega_supported(int wfmt, int head_dim, int rep, int kv_dtype);
+cudaError_t mega_init_attrs(int wfmt, int head_dim, int rep, int kv_dtype);
+int mega_max_grid(int wfmt, int head_dim, int rep, int kv_dtype);  // 0: cannot run
+cudaError_t launch_mega(const MegaArgs& a, int wfmt, int head_dim, int rep, int kv_dtype, int grid,
                         cudaStream_t s);
 
 // ---------------------------------------------------------------------------

@@ -52,8 +52,18 @@ constexpr int MT = kMegaThreads;
 constexpr int MW = MT / 32;
 constexpr int NS = kMegaSlots;
 constexpr int SB = kMegaSlotBytes;
-constexpr int kUnit = 1024;      // one packed unit: a 512-byte chunk of both rows of a pair
-constexpr int SU = SB / kUnit;   // packed units per slot
+// Packed weight formats: one unit holds a 512-byte chunk of both rows of a
+// pair (UNIT bytes; int4: 256 bytes of codes per row and the two rows' 8
+// block scales of the chunk); EPL weights per lane and row in a chunk.
+template <typename PT>
+struct Fmt {
+  static constexpr int UNIT = 1024, EPL = Unpack<PT>::N;
+};
+template <>
+struct Fmt<q4_block64> {
+  static constexpr int UNIT = kQ4Unit, EPL = kQ4Chunk / 32;
+};
+static_assert(SB % Fmt<__nv_bfloat16>::UNIT == 0 && SB % Fmt<q4_block64>::UNIT == 0, "slots hold whole units");
 constexpr int PX = 10;           // float4 groups of the input vector per thread (K <= 10240)
 // keys per attention tile: the K and V rows (plus int8 scales) fit one slot
 template <int D, typename KVT>
@@ -222,6 +232,7 @@ __device__ __forceinline__ int4 g_split(int N, int CT, int cta, int G, int warp)
   return make_int4(p0, p1, static_cast<int>((U * warp) / MW), static_cast<int>((U * (warp + 1)) / MW));
 }
 
+template <int SU>  // packed units per slot
 __device__ __forceinline__ GRange g_range(const GDesc& d, const MegaShared& sh, int warp) {
   const int4 w = sh.wr[d.kind][warp];
   GRange r;
@@ -265,8 +276,9 @@ __device__ __forceinline__ int a_mine(const AItem& it, int warp) {
 // ---- the per-warp stream of slots (state kept in lane 0) -----------------------------------
 // The producer lane walks every phase q = layer * kPhases + j (then the lm_head
 // phase) in order; enter() caches where the current phase's copies come from.
-template <int D, typename KVT>
+template <int UB, int D, typename KVT>  // UB: bytes of a packed weight unit
 struct Stream {
+  static constexpr int SU = SB / UB;  // packed units per slot
   static constexpr int TKM = tile_keys<D, KVT>();
   static constexpr int ROWB = D * sizeof(KVT);
   static constexpr bool I8 = std::is_same<KVT, int8_t>::value;
@@ -305,9 +317,9 @@ struct Stream {
       return;
     }
     const GDesc d = gdesc(a, *shp, q, qkv_n, D);
-    const GRange r = g_range(d, *shp, warp);
+    const GRange r = g_range<SU>(d, *shp, warp);
     n = r.nslots;
-    src = d.W + (static_cast<size_t>(r.p0) * d.CT + r.ua) * kUnit;
+    src = d.W + (static_cast<size_t>(r.p0) * d.CT + r.ua) * UB;
     left = r.ub - r.ua;
   }
 
@@ -357,9 +369,9 @@ struct Stream {
       j0 += MW * TKM;
     } else {
       const int nu = min(SU, left);
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nu) * kUnit);
-      bulk_g2s_hint(dst, src, static_cast<uint32_t>(nu) * kUnit, bar, policy);
-      src += static_cast<size_t>(nu) * kUnit;
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nu) * UB);
+      bulk_g2s_hint(dst, src, static_cast<uint32_t>(nu) * UB, bar, policy);
+      src += static_cast<size_t>(nu) * UB;
       left -= nu;
     }
     ++issued;
@@ -444,16 +456,18 @@ __device__ __forceinline__ float load1(const WT* p, size_t e) {
 template <typename WT, typename PT, int D, typename KVT>
 __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt, uint32_t tag_in, const float* x0f,
                         const WT* x0w, const float* rsd0f, const WT* rsd0w, const GEpi& ep, uint8_t* smem,
-                        MegaShared& sh, Stream<D, KVT>& st, GainQ& gq, int& consumed, Best& best, int cta, int G,
-                        int pos, int qkv_n) {
-  constexpr int EPL = Unpack<PT>::N;  // packed weights per lane and row in a 512-byte chunk
+                        MegaShared& sh, Stream<Fmt<PT>::UNIT, D, KVT>& st, GainQ& gq, int& consumed, Best& best,
+                        int cta, int G, int pos, int qkv_n) {
+  constexpr bool Q4 = std::is_same<PT, q4_block64>::value;
+  constexpr int UNIT = Fmt<PT>::UNIT, SU = SB / UNIT;
+  constexpr int EPL = Fmt<PT>::EPL;  // packed weights per lane and row in a 512-byte chunk
   constexpr int CH = 32 * EPL;
   constexpr int NPL = EPL / 4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = d.K, CT = d.CT;
   float* xs = reinterpret_cast<float*>(smem + kMegaRingBytes);
   uint8_t* ring = smem + static_cast<size_t>(warp) * NS * SB;
-  const GRange r = g_range(d, sh, warp);
+  const GRange r = g_range<SU>(d, sh, warp);
   if (lane == 0) sh.rec_n[warp] = 0;
 
   // ---- x, normalised if the phase has a gain, lane-interleaved per chunk
@@ -612,18 +626,34 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
           const float4 t = *reinterpret_cast<const float4*>(xs + ((cc * NPL + pp) * 32 + lane) * 4);
           xv[4 * pp] = t.x; xv[4 * pp + 1] = t.y; xv[4 * pp + 2] = t.z; xv[4 * pp + 3] = t.w;
         }
-        const uint8_t* u8 = buf + (j + q) * kUnit + lane * 16;
-        float w0[EPL], w1[EPL];
-        Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8), w0);
-        Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8 + 512), w1);
-        float t0 = 0.f, t1 = 0.f;
+        const uint8_t* ub = buf + (j + q) * UNIT;
+        const uint8_t* u8 = ub + lane * 16;
+        if constexpr (Q4) {
+          // the lane's 16 weights are a quarter of one 64-weight block of each
+          // row: two partial sums per row, then the block scales
+          static_assert(EPL == 16 && UNIT == 576, "int4 unit: 256 code bytes and 8 scales per row");
+          const uint2 c0 = *reinterpret_cast<const uint2*>(ub + lane * 8);
+          const uint2 c1 = *reinterpret_cast<const uint2*>(ub + 256 + lane * 8);
+          const float bs0 = *reinterpret_cast<const float*>(ub + 512 + (lane >> 2) * 4);
+          const float bs1 = *reinterpret_cast<const float*>(ub + 544 + (lane >> 2) * 4);
+          float p0[2] = {0.f, 0.f}, p1[2] = {0.f, 0.f};
+          q4_dot8(c0.x, c1.x, xv, p0[0], p1[0]);
+          q4_dot8(c0.y, c1.y, xv + 8, p0[1], p1[1]);
+          acc0 = fmaf(p0[0] + p0[1], bs0, acc0);
+          acc1 = fmaf(p1[0] + p1[1], bs1, acc1);
+        } else {
+          float w0[EPL], w1[EPL];
+          Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8), w0);
+          Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8 + 512), w1);
+          float t0 = 0.f, t1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-          t0 = fmaf(w0[e], xv[e], t0);
-          t1 = fmaf(w1[e], xv[e], t1);
+          for (int e = 0; e < EPL; ++e) {
+            t0 = fmaf(w0[e], xv[e], t0);
+            t1 = fmaf(w1[e], xv[e], t1);
+          }
+          acc0 += t0;
+          acc1 += t1;
         }
-        acc0 += t0;
-        acc1 += t1;
       }
       j += seg;
       c += seg;
@@ -717,9 +747,9 @@ __device__ __forceinline__ void vload(const int8_t* p, float* f) {
 // One attention item (KV head g, key split sp) per CTA: the partial
 // (max, sum, unnormalised output) of its REP query heads over its keys; the
 // last split of head g to finish merges all splits into attn_out.
-template <typename WT, int D, int REP, typename KVT>
+template <typename WT, int D, int REP, int UB, typename KVT>
 __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint32_t tag_out, uint8_t* smem,
-                        MegaShared& sh, Stream<D, KVT>& st, int& consumed, int cta, int G, int qkv_n) {
+                        MegaShared& sh, Stream<UB, D, KVT>& st, int& consumed, int cta, int G, int qkv_n) {
   constexpr int ELT = sizeof(KVT);
   constexpr int EPL = 16 / ELT;
   constexpr int ROWB = D * ELT;
@@ -1084,7 +1114,7 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
   }
   const uint32_t tagbase = (*a.epoch + 1u) << kMegaTagShift;
   const int qkv_n = (a.nq + 2 * a.nkv) * D;
-  Stream<D, KVT> st;
+  Stream<Fmt<PT>::UNIT, D, KVT> st;
   GainQ gq;
   if (tid == 0) {
     mbar_init(&sh.gbar[0], 1);
@@ -1239,17 +1269,18 @@ const void* mega_fn() {
     return nullptr;
 }
 
-// (gain / embedding type, packed weight type and its bytes, head_dim, GQA
-// ratio) combinations with a persistent kernel: the 3.7B shape and the medium
-// model in bf16 and fp8 weights, the tiny fp32 model
+// (gain / embedding type, packed weight type and its format key, head_dim,
+// GQA ratio) combinations with a persistent kernel: the 3.7B shape and the
+// medium model in bf16, fp8 and int4 weights, the tiny fp32 model
 #define K2_MEGA_SHAPES(X)                                                                                         \
   X(__nv_bfloat16, __nv_bfloat16, 2, 128, 4) X(__nv_bfloat16, __nv_bfloat16, 2, 64, 4) X(float, float, 4, 16, 2) \
-  X(__nv_bfloat16, __nv_fp8_e4m3, 1, 128, 4) X(__nv_bfloat16, __nv_fp8_e4m3, 1, 64, 4)
+  X(__nv_bfloat16, __nv_fp8_e4m3, 1, 128, 4) X(__nv_bfloat16, __nv_fp8_e4m3, 1, 64, 4)                           \
+  X(__nv_bfloat16, q4_block64, kWfmtQ4, 128, 4) X(__nv_bfloat16, q4_block64, kWfmtQ4, 64, 4)
 
-// wbytes: bytes of one packed weight element (1 = fp8 E4M3)
-const void* mega_lookup(int wbytes, int head_dim, int rep, int kv_dtype) {
+// wfmt: the packed weight format (kWfmt* in k2_kernels.h)
+const void* mega_lookup(int wfmt, int head_dim, int rep, int kv_dtype) {
 #define K2_MEGA_LOOK(WT, PT, WB, D, R)                               \
-  if (wbytes == WB && head_dim == D && rep == R) {                   \
+  if (wfmt == WB && head_dim == D && rep == R) {                     \
     if (kv_dtype == 0) return mega_fn<WT, PT, D, R, float>();        \
     if (kv_dtype == 2) return mega_fn<WT, PT, D, R, __half>();       \
     if (kv_dtype == 3) return mega_fn<WT, PT, D, R, int8_t>();       \
@@ -1261,12 +1292,12 @@ const void* mega_lookup(int wbytes, int head_dim, int rep, int kv_dtype) {
 
 }  // namespace
 
-bool mega_supported(int wbytes, int head_dim, int rep, int kv_dtype) {
-  return mega_lookup(wbytes, head_dim, rep, kv_dtype) != nullptr;
+bool mega_supported(int wfmt, int head_dim, int rep, int kv_dtype) {
+  return mega_lookup(wfmt, head_dim, rep, kv_dtype) != nullptr;
 }
 
-cudaError_t mega_init_attrs(int wbytes, int head_dim, int rep, int kv_dtype) {
-  const void* fn = mega_lookup(wbytes, head_dim, rep, kv_dtype);
+cudaError_t mega_init_attrs(int wfmt, int head_dim, int rep, int kv_dtype) {
+  const void* fn = mega_lookup(wfmt, head_dim, rep, kv_dtype);
   if (!fn) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMegaSmemBytes);
   if (e != cudaSuccess) return e;
@@ -1274,8 +1305,8 @@ cudaError_t mega_init_attrs(int wbytes, int head_dim, int rep, int kv_dtype) {
                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
 }
 
-int mega_max_grid(int wbytes, int head_dim, int rep, int kv_dtype) {
-  const void* fn = mega_lookup(wbytes, head_dim, rep, kv_dtype);
+int mega_max_grid(int wfmt, int head_dim, int rep, int kv_dtype) {
+  const void* fn = mega_lookup(wfmt, head_dim, rep, kv_dtype);
   if (!fn) return 0;
   int per_sm = 0, dev = 0, sms = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, MT, kMegaSmemBytes) != cudaSuccess) return 0;
@@ -1284,8 +1315,8 @@ int mega_max_grid(int wbytes, int head_dim, int rep, int kv_dtype) {
   return per_sm >= 1 ? sms : 0;  // one CTA per SM
 }
 
-cudaError_t launch_mega(const MegaArgs& a, int wbytes, int head_dim, int rep, int kv_dtype, int grid, cudaStream_t s) {
-  const void* fn = mega_lookup(wbytes, head_dim, rep, kv_dtype);
+cudaError_t launch_mega(const MegaArgs& a, int wfmt, int head_dim, int rep, int kv_dtype, int grid, cudaStream_t s) {
+  const void* fn = mega_lookup(wfmt, head_dim, rep, kv_dtype);
   if (!fn) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -17,10 +17,10 @@ LIB_PATH = os.path.join(_HERE, "libk2.so")
 K2_OK, K2_ERR_ARG, K2_ERR_SHAPE, K2_ERR_UNSUPPORTED, K2_ERR_TOKEN_RANGE, K2_ERR_CONTEXT_FULL, \
     K2_ERR_WORKSPACE, K2_ERR_CUDA, K2_ERR_DEVICE_GUARD, K2_ERR_STATE = range(10)
 K2_STATE_HEADER_BYTES = 96
-K2_F32, K2_BF16, K2_F16, K2_I8, K2_F8 = range(5)
+K2_F32, K2_BF16, K2_F16, K2_I8, K2_F8, K2_Q4 = range(6)
 K2_OPT_PDL, K2_OPT_GRAPH, K2_OPT_ATTN_SPLITS, K2_OPT_PERSISTENT, K2_OPT_TC_PREFILL, K2_OPT_TC_DECODE = range(6)
 KERNEL_CLASSES = ("embed", "qkv", "attn", "o_proj", "gate_up", "down", "lm_head", "step", "sample")
-DTYPES = {"f32": K2_F32, "bf16": K2_BF16, "f16": K2_F16, "i8": K2_I8, "f8": K2_F8}
+DTYPES = {"f32": K2_F32, "bf16": K2_BF16, "f16": K2_F16, "i8": K2_I8, "f8": K2_F8, "q4": K2_Q4}
 
 
 class K2Error(RuntimeError):
@@ -93,6 +93,7 @@ def _load():
         "k2_philox": (C.c_int, [C.c_uint32, i32, C.c_uint32, C.c_uint32, C.c_uint32, C.c_uint64, vp, vp]),
         "k2_spec_draft": (i32, [vp, i32, i32, vp]),
         "k2_quantize_fp8": (C.c_int, [vp, i32, i32, vp, vp, vp]),
+        "k2_quantize_q4": (C.c_int, [vp, i32, i32, vp, vp, vp]),
         "k2_decode_speculative": (C.c_int, [vp, i32, vp, i32, i32, vp, C.POINTER(i32), vp]),
     }
     for name, (res, args) in sig.items():
@@ -107,7 +108,8 @@ EXPORTED = ("k2_workspace_bytes", "k2_init_weights", "k2_free", "k2_last_error",
             "k2_decode_step", "k2_decode_layers", "k2_kv_reset", "k2_kv_set_len", "k2_kv_view", "k2_hidden_view",
             "k2_sync_status", "k2_clear_status", "k2_set_option", "k2_profile_decode", "k2_greedy_head_noalloc",
             "k2_kv_state_bytes", "k2_kv_save", "k2_kv_peek", "k2_kv_load", "k2_set_sampling", "k2_sample_logits",
-            "k2_philox", "k2_spec_draft", "k2_decode_speculative", "k2_quantize_fp8")
+            "k2_philox", "k2_spec_draft", "k2_decode_speculative", "k2_quantize_fp8",
+            "k2_quantize_q4")
 
 
 def _ptr(t):
@@ -126,7 +128,8 @@ def _stream(stream):
 
 def make_config(shape, max_context: int, max_batch: int = 1, kv_dtype: str = "f16", weights: str = None) -> Config:
     """weights: the stored weight dtype, default the shape's; "f8" stores the
-    shape's bf16 weights as fp8 E4M3 rows with per-row scales."""
+    shape's bf16 weights as fp8 E4M3 rows with per-row scales, "q4" as int4
+    codes with one scale per 64 weights of a row."""
     return Config(hidden=shape.hidden, n_layers=shape.n_layers, n_heads=shape.n_heads, n_kv_heads=shape.n_kv_heads,
                   head_dim=shape.head_dim, intermediate=shape.intermediate, norm_groups=shape.norm_groups,
                   vocab=shape.vocab, max_context=max_context, max_batch=max_batch, eps=shape.eps,
@@ -309,6 +312,18 @@ def quantize_fp8(src, stream=None):
     st = LIB.k2_quantize_fp8(_ptr(src), rows, cols, _ptr(codes), _ptr(scales), _stream(stream))
     if st != K2_OK:
         raise K2Error(st, "k2_quantize_fp8 failed")
+    return codes, scales
+
+
+def quantize_q4(src, stream=None):
+    """k2_quantize_q4 on a [rows, cols] bf16 device tensor: (codes int8 [rows, cols],
+    scales fp32 [rows, ceil(cols / 64)])."""
+    rows, cols = src.shape
+    codes = torch.empty(rows, cols, dtype=torch.int8, device="cuda")
+    scales = torch.empty(rows, (cols + 63) // 64, dtype=torch.float32, device="cuda")
+    st = LIB.k2_quantize_q4(_ptr(src), rows, cols, _ptr(codes), _ptr(scales), _stream(stream))
+    if st != K2_OK:
+        raise K2Error(st, "k2_quantize_q4 failed")
     return codes, scales
 
 

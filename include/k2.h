@@ -62,14 +62,17 @@ typedef enum {
                               written for another model architecture or KV format */
 } k2_status;
 
-typedef enum { K2_F32 = 0, K2_BF16 = 1, K2_F16 = 2, K2_I8 = 3, K2_F8 = 4 } k2_dtype;
+typedef enum { K2_F32 = 0, K2_BF16 = 1, K2_F16 = 2, K2_I8 = 3, K2_F8 = 4, K2_Q4 = 5 } k2_dtype;
 
 /* Model shape and run limits (k2-burn README, "Model shape" and "KV cache
- * storage").  weight_dtype is K2_F32, K2_BF16 or K2_F8; kv_dtype is K2_F32,
- * K2_F16 or K2_I8.  K2_F8 (k2-burn README, "Post-training quantization"):
- * the weights are given in bf16 and k2_init_weights stores every projection
- * matrix and the lm_head as fp8 E4M3 rows with one fp32 scale per row (see
- * k2_quantize_fp8); the embedding and the norm gains stay bf16.  Such a model
+ * storage").  weight_dtype is K2_F32, K2_BF16, K2_F8 or K2_Q4; kv_dtype is
+ * K2_F32, K2_F16 or K2_I8.  K2_F8 and K2_Q4 (k2-burn README, "Post-training
+ * quantization" and "Quantization": fp8 E4M3 and int4 block-64 checkpoints;
+ * only the Linear weights are quantized): the weights are given in bf16 and
+ * k2_init_weights stores every projection matrix and the lm_head as fp8 E4M3
+ * rows with one fp32 scale per row (K2_F8, see k2_quantize_fp8), or as int4
+ * codes with one fp32 scale per 64 weights of a row (K2_Q4, see
+ * k2_quantize_q4); the embedding and the norm gains stay bf16.  Such a model
  * runs on the persistent step only (prompts are appended one step per token)
  * and is refused where that step is not available.  max_context = KV rows per sequence (prompt + generated tokens);
  * max_batch = number of independent sequences. */
@@ -385,6 +388,18 @@ k2_status k2_profile_decode(k2_ctx* ctx, const int32_t* d_tokens, int32_t batch,
  * scale. */
 k2_status k2_quantize_fp8(const void* d_src, int32_t rows, int32_t cols, uint8_t* d_codes, float* d_scales,
                           void* stream);
+
+/* The int4 block quantization of K2_Q4 weights, on its own (k2-burn README,
+ * "Quantization": int4 with block size 64; symmetric codes).  Each of `rows`
+ * bf16 rows of `cols` values at d_src (device, row-major) is cut into blocks
+ * of 64 consecutive values (the last block of a row may be shorter); block b
+ * of row r gets d_scales[r * ceil(cols / 64) + b] = max|w| / 7 and each value
+ * the code d_codes[r * cols + c] = w / scale rounded to the nearest integer,
+ * ties to even, clamped to [-7, 7]; a block of zeros gets scale 0 and codes 0.
+ * The model computes with code * scale.  All buffers are the caller's device
+ * memory; K2_ERR_ARG for null pointers, rows < 0 or cols < 1. */
+k2_status k2_quantize_q4(const void* d_src, int32_t rows, int32_t cols, int8_t* d_codes, float* d_scales,
+                         void* stream);
 
 /* ---- without a workspace ---------------------------------------------------- */
 
