@@ -216,37 +216,52 @@ struct Unpack<int8_t> {
 // beside its codes.
 struct q4_block64 {};
 
-// The code of nibble K (0..4) of w as a float, exactly: the nibble v is OR-ed
-// into the mantissa of 2^23, which gives the float 2^23 + v 16^K; one fma by
-// 16^-K with -(2^23 16^-K + 8) leaves v - 8 (an integer: no rounding).
-template <int K>
-__device__ __forceinline__ float q4_code(uint32_t w) {
-  static_assert(K >= 0 && K <= 4, "the nibble must lie inside the 23-bit mantissa");
-  constexpr float inv = 1.0f / static_cast<float>(1u << (4 * K));
-  constexpr float off = -(8388608.0f * inv + 8.0f);
-  return fmaf(__uint_as_float((w & (0xFu << (4 * K))) | 0x4B000000u), inv, off);
+// ---- packed fp32 pairs (fma.rn.f32x2): two IEEE fmas, each rounded as fmaf
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ float sum2(f32x2 v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
 }
 
-// Partial dot products of two rows' words a, b (8 codes each, nibble k =
-// element k) with x[0..7]; nibbles 5..7 are shifted down to positions 2..4.
-__device__ __forceinline__ void q4_dot8(uint32_t a, uint32_t b, const float* x, float& ta, float& tb) {
-  const uint32_t a2 = a >> 12, b2 = b >> 12;
-  ta = fmaf(q4_code<0>(a), x[0], ta);
-  tb = fmaf(q4_code<0>(b), x[0], tb);
-  ta = fmaf(q4_code<1>(a), x[1], ta);
-  tb = fmaf(q4_code<1>(b), x[1], tb);
-  ta = fmaf(q4_code<2>(a), x[2], ta);
-  tb = fmaf(q4_code<2>(b), x[2], tb);
-  ta = fmaf(q4_code<3>(a), x[3], ta);
-  tb = fmaf(q4_code<3>(b), x[3], tb);
-  ta = fmaf(q4_code<4>(a), x[4], ta);
-  tb = fmaf(q4_code<4>(b), x[4], tb);
-  ta = fmaf(q4_code<2>(a2), x[5], ta);
-  tb = fmaf(q4_code<2>(b2), x[5], tb);
-  ta = fmaf(q4_code<3>(a2), x[6], ta);
-  tb = fmaf(q4_code<3>(b2), x[6], tb);
-  ta = fmaf(q4_code<4>(a2), x[7], ta);
-  tb = fmaf(q4_code<4>(b2), x[7], tb);
+// Nibble K (0..4) of w OR-ed into the mantissa of 2^23: the float
+// 2^23 + v 16^K (v the nibble's value).
+template <int K>
+__device__ __forceinline__ float q4_raw(uint32_t w) {
+  static_assert(K >= 0 && K <= 4, "the nibble must lie inside the 23-bit mantissa");
+  return __uint_as_float((w & (0xFu << (4 * K))) | 0x4B000000u);
+}
+// The fma that turns q4_raw<K> into the code v - 8, exactly (every value on
+// the way is an integer below 2^24): multiplier 16^-K, addend -(2^23 16^-K + 8).
+template <int K>
+__device__ __forceinline__ constexpr float q4_mul() { return 1.0f / static_cast<float>(1u << (4 * K)); }
+template <int K>
+__device__ __forceinline__ constexpr float q4_add() { return -(8388608.0f * q4_mul<K>() + 8.0f); }
+template <int KA, int KB>
+__device__ __forceinline__ f32x2 q4_codes2(uint32_t wa, uint32_t wb) {
+  return fma2(pk2(q4_raw<KA>(wa), q4_raw<KB>(wb)), pk2(q4_mul<KA>(), q4_mul<KB>()),
+              pk2(q4_add<KA>(), q4_add<KB>()));
+}
+
+// acc += the 8 codes of word w (nibble k = element k) times x[0..7], as two
+// interleaved sums (even and odd elements); nibbles 5..7 are shifted down to
+// positions 2..4 first.
+__device__ __forceinline__ void q4_dot8(uint32_t w, const float* x, f32x2& acc) {
+  const uint32_t w2 = w >> 12;
+  acc = fma2(q4_codes2<0, 1>(w, w), pk2(x[0], x[1]), acc);
+  acc = fma2(q4_codes2<2, 3>(w, w), pk2(x[2], x[3]), acc);
+  acc = fma2(q4_codes2<4, 2>(w, w2), pk2(x[4], x[5]), acc);
+  acc = fma2(q4_codes2<3, 4>(w2, w2), pk2(x[6], x[7]), acc);
 }
 
 template <typename T>

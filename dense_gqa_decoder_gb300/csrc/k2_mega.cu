@@ -636,23 +636,26 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
           const uint2 c1 = *reinterpret_cast<const uint2*>(ub + 256 + lane * 8);
           const float bs0 = *reinterpret_cast<const float*>(ub + 512 + (lane >> 2) * 4);
           const float bs1 = *reinterpret_cast<const float*>(ub + 544 + (lane >> 2) * 4);
-          float p0[2] = {0.f, 0.f}, p1[2] = {0.f, 0.f};
-          q4_dot8(c0.x, c1.x, xv, p0[0], p1[0]);
-          q4_dot8(c0.y, c1.y, xv + 8, p0[1], p1[1]);
-          acc0 = fmaf(p0[0] + p0[1], bs0, acc0);
-          acc1 = fmaf(p1[0] + p1[1], bs1, acc1);
+          f32x2 p00 = 0ull, p01 = 0ull, p10 = 0ull, p11 = 0ull;  // (row, word) sums of element pairs
+          q4_dot8(c0.x, xv, p00);
+          q4_dot8(c0.y, xv + 8, p01);
+          q4_dot8(c1.x, xv, p10);
+          q4_dot8(c1.y, xv + 8, p11);
+          acc0 = fmaf(sum2(p00) + sum2(p01), bs0, acc0);
+          acc1 = fmaf(sum2(p10) + sum2(p11), bs1, acc1);
         } else {
           float w0[EPL], w1[EPL];
           Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8), w0);
           Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8 + 512), w1);
-          float t0 = 0.f, t1 = 0.f;
+          f32x2 t0 = 0ull, t1 = 0ull;  // sums of element pairs
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) {
-            t0 = fmaf(w0[e], xv[e], t0);
-            t1 = fmaf(w1[e], xv[e], t1);
+          for (int e = 0; e < EPL; e += 2) {
+            const f32x2 xe = pk2(xv[e], xv[e + 1]);
+            t0 = fma2(pk2(w0[e], w0[e + 1]), xe, t0);
+            t1 = fma2(pk2(w1[e], w1[e + 1]), xe, t1);
           }
-          acc0 += t0;
-          acc1 += t1;
+          acc0 += sum2(t0);
+          acc1 += sum2(t1);
         }
       }
       j += seg;
