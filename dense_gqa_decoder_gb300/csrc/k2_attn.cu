@@ -11,10 +11,12 @@
 //     KV head) form one thread-block cluster; a CTA owns a contiguous key
 //     range, so every K/V byte is read from HBM once per step and shared by
 //     the REP query heads of the group;
-//   * the range is cut into 32-key tiles dealt round-robin to the 8 warps;
+//   * the range is cut into 32-key tiles dealt round-robin to the 4 warps;
 //     each warp streams its tiles through its own shared-memory slot with
 //     bulk TMA copies (K rows, V rows), the first one requested before
 //     griddepcontrol.wait (cached rows never depend on the previous kernel);
+//     three CTAs (12 warps) share an SM, so one warp's copy and its
+//     latency-bound tile steps overlap the others';
 //   * per tile a warp computes the 32 scores (8 lanes per key), one fp32
 //     online-softmax update (one lane per key) and the P.V product (lanes own
 //     output dims), keeping its own (m, l, o) per head: no CTA barrier inside
@@ -24,7 +26,7 @@
 //     per row, k2-burn README "KV cache storage") by the warp whose tile holds
 //     position pos, which also uses the stored values itself;
 //   * int8 rows are dequantised inside the kernel (code * row scale);
-//   * the 8 warp states are merged in shared memory, then the splits of the
+//   * the warp states are merged in shared memory, then the splits of the
 //     cluster merge through distributed shared memory: after a cluster
 //     barrier each CTA finalises a slice of the head outputs from its peers'
 //     (m, l, o) with log-sum-exp weights -- no partials in global memory, no
@@ -103,7 +105,7 @@ __device__ __forceinline__ float ld_peer(uint32_t addr) {
 constexpr int kWarps = kAttnThreads / 32;
 
 template <int D, int REP, typename KVT>
-__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const AttnArgs a) {
   constexpr int TK = kAttnTK;
   constexpr int ELT = sizeof(KVT);
   constexpr int EPL = 16 / ELT;              // elements per 16-byte load
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   constexpr bool I8 = KVTraits<KVT>::kI8;
   constexpr uint32_t KVB = TK * ROWB;        // bytes of the K (or V) rows of a tile
   constexpr int PSTR = REP * (D + 2);        // a partial state: m[REP], l[REP], o[REP][D]
-  static_assert(NV % LPK == 0 && 32 % LPK == 0 && TK == 32, "head_dim / dtype");
+  static_assert(NV % LPK == 0 && 32 % LPK == 0 && TK <= 32, "head_dim / dtype");
 
   extern __shared__ __align__(128) uint8_t smem[];  // kWarps slots of a.slot_bytes
   __shared__ uint64_t full[kWarps];
@@ -246,9 +248,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
       }
       __syncwarp();
     }
-    // ---- scores: LPK lanes per key, KPS keys per step
+    // ---- scores: LPK lanes per key, KPS keys per step (keys past the tile: no load, no store)
 #pragma unroll
-    for (int st = 0; st < TK / KPS; ++st) {
+    for (int st = 0; st < (TK + KPS - 1) / KPS; ++st) {
       const int jj = st * KPS + lane / LPK;
       float dot[REP];
 #pragma unroll
@@ -448,6 +450,19 @@ cudaError_t attn_init_attrs() {
   K2_ATTN_SHAPES(K2_ATTN_ATTR)
 #undef K2_ATTN_ATTR
   return e;
+}
+
+int attn_ctas_per_sm(int head_dim, int rep, int kv_dtype) {
+  const void* fn = nullptr;
+#define K2_ATTN_PTR(D, R) \
+  if (head_dim == D && rep == R) fn = kernel_ptr<D, R>(kv_dtype);
+  K2_ATTN_SHAPES(K2_ATTN_PTR)
+#undef K2_ATTN_PTR
+  int n = 0;
+  if (!fn || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kAttnThreads,
+                                                           attn_slot_bytes(head_dim, kv_dtype) * kWarps) != cudaSuccess)
+    return 1;
+  return n < 1 ? 1 : n;
 }
 
 int attn_max_cluster(int head_dim, int rep, int kv_dtype, int limit) {

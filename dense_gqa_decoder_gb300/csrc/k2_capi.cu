@@ -233,6 +233,7 @@ struct k2_ctx {
   int grid_qkv = 0, grid_o = 0, grid_gu = 0, grid_down = 0, grid_lm = 0;
   AttnArgs p_attn = {};
   int attn_cluster_max = 1;  // largest launchable attention cluster
+  int attn_resident = 1;     // attention CTAs resident on the whole GPU at once
   int force_splits = 0;
   // state
   std::vector<int> len;
@@ -285,13 +286,24 @@ struct k2_ctx {
 
 namespace {
 
+// Key splits per (sequence, KV head): the count whose CTAs fill the last wave
+// of resident CTAs best (a clearly fuller last wave wins; on a tie the fewer
+// splits, which merge less), within the cluster limit and >= 8 keys per split.
 int attn_splits(const k2_ctx* c, int batch) {
   if (c->force_splits > 0) return c->force_splits < c->attn_cluster_max ? c->force_splits : c->attn_cluster_max;
-  int n = (c->sms + c->s.nkv * batch - 1) / (c->s.nkv * batch);
-  const int cap_splits = c->lay.cap / 8;
-  if (n > cap_splits) n = cap_splits;
-  if (n > c->attn_cluster_max) n = c->attn_cluster_max;
-  return n < 1 ? 1 : n;
+  const int items = c->s.nkv * batch;
+  const int max_splits = std::max(1, std::min(c->attn_cluster_max, c->lay.cap / 8));
+  int best = 1;
+  double best_fill = -1.0;
+  for (int n = 1; n <= max_splits; ++n) {
+    const double waves = static_cast<double>(items) * n / c->attn_resident;
+    const double fill = waves / std::ceil(waves);
+    if (fill > best_fill + 0.02) {
+      best = n;
+      best_fill = fill;
+    }
+  }
+  return best;
 }
 
 // Kernel launch recorder: plain launches, or (profiling) each launch between
@@ -1109,6 +1121,7 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     delete c;
     return K2_ERR_CUDA;
   }
+  c->attn_resident = c->sms * attn_ctas_per_sm(c->s.d, c->s.rep, cfg->kv_dtype == K2_F32 ? 0 : cfg->kv_dtype);
   c->attn_cluster_max = attn_max_cluster(c->s.d, c->s.rep, cfg->kv_dtype == K2_F32 ? 0 : cfg->kv_dtype,
                                          kAttnMaxCluster);
   if (c->attn_cluster_max < 1) {

@@ -173,7 +173,7 @@ struct AttnArgs {
   int pos_base;
   const int* pos_base_dev;  // block mode: read pos_base from device memory (nullable)
 };
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 128;     // 4 warps: three CTAs (12 warps) share an SM
 constexpr int kAttnTK = 32;          // keys per tile; a warp reads one tile at a time
 constexpr int kAttnMaxCluster = 16;  // key-range splits of one KV head = one thread-block cluster
 
@@ -182,6 +182,7 @@ size_t attn_slot_bytes(int head_dim, int kv_dtype);
 cudaError_t attn_init_attrs();
 // largest cluster (<= limit) of this attention kernel that fits the GPU; 0 on error
 int attn_max_cluster(int head_dim, int rep, int kv_dtype, int limit);
+int attn_ctas_per_sm(int head_dim, int rep, int kv_dtype);  // resident CTAs of the attention kernel per SM
 cudaError_t launch_attn(const AttnArgs& a, int head_dim, int rep, int kv_dtype, int nsplit, int batch,
                         cudaStream_t s, bool pdl);
 
