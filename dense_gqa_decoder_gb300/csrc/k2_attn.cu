@@ -16,7 +16,9 @@
 //     bulk TMA copies (K rows, V rows), the first one requested before
 //     griddepcontrol.wait (cached rows never depend on the previous kernel);
 //     three CTAs (12 warps) share an SM, so one warp's copy and its
-//     latency-bound tile steps overlap the others';
+//     latency-bound tile steps overlap the others'; the K and V halves of a
+//     slot have their own barriers, so the next tile's K rows are copied
+//     while the warp still works on the current tile's softmax and P.V;
 //   * per tile a warp computes the 32 scores (8 lanes per key), one fp32
 //     online-softmax update (one lane per key) and the P.V product (lanes own
 //     output dims), keeping its own (m, l, o) per head: no CTA barrier inside
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const Attn
   static_assert(NV % LPK == 0 && 32 % LPK == 0 && TK <= 32, "head_dim / dtype");
 
   extern __shared__ __align__(128) uint8_t smem[];  // kWarps slots of a.slot_bytes
-  __shared__ uint64_t full[kWarps];
+  __shared__ uint64_t fullk[kWarps], fullv[kWarps];  // the K half (+ K scales), the V half (+ V scales)
   __shared__ float Sw[kWarps][REP][TK];
   __shared__ __align__(16) float Pw[kWarps][TK][REP];
   __shared__ float cpart[PSTR];  // this CTA's (m, l, o), read by the cluster peers
@@ -149,30 +151,32 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const Attn
   const __half* VSg = I8 ? reinterpret_cast<const __half*>(a.vs) + head_row : nullptr;
   uint8_t* slot = smem + static_cast<size_t>(warp) * a.slot_bytes;
 
-  auto issue = [&](int t) {  // lane 0: tile t of this CTA into this warp's slot
+  // lane 0: one half (kv = 0: K, 1: V) of tile t of this CTA into this warp's slot
+  auto issue = [&](int t, int kv) {
     const int j0 = k0 + t * TK;
     const int rows = min(TK, k1 - j0);
     // cached rows; row pos is the new one (in block mode it is cached too)
     const int crow = max(0, min(rows, (a.block_mode ? pos + 1 : pos) - j0));
     const int srow = (crow + 7) & ~7;             // scale copies in 16-byte units
-    const uint32_t bytes = 2u * crow * ROWB + (I8 && crow > 0 ? 2u * srow * 2u : 0u);
+    uint64_t* bar = kv == 0 ? &fullk[warp] : &fullv[warp];
+    const uint32_t bytes = crow * ROWB + (I8 && crow > 0 ? srow * 2u : 0u);
     if (bytes == 0) {
-      mbar_arrive(&full[warp]);
+      mbar_arrive(bar);
       return;
     }
-    mbar_arrive_expect_tx(&full[warp], bytes);
-    bulk_g2s(slot, Kg + static_cast<size_t>(j0) * ROWB, crow * ROWB, &full[warp]);
-    bulk_g2s(slot + KVB, Vg + static_cast<size_t>(j0) * ROWB, crow * ROWB, &full[warp]);
-    if constexpr (I8) {
-      bulk_g2s(slot + 2 * KVB, KSg + j0, srow * 2u, &full[warp]);
-      bulk_g2s(slot + 2 * KVB + TK * 2, VSg + j0, srow * 2u, &full[warp]);
-    }
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(slot + kv * KVB, (kv == 0 ? Kg : Vg) + static_cast<size_t>(j0) * ROWB, crow * ROWB, bar);
+    if constexpr (I8) bulk_g2s(slot + 2 * KVB + kv * TK * 2, (kv == 0 ? KSg : VSg) + j0, srow * 2u, bar);
   };
 
   if (lane == 0) {
-    mbar_init(&full[warp], 1);
+    mbar_init(&fullk[warp], 1);
+    mbar_init(&fullv[warp], 1);
     fence_mbar_init();
-    if (nmine > 0) issue(warp);
+    if (nmine > 0) {
+      issue(warp, 0);
+      issue(warp, 1);
+    }
   }
   __syncwarp();
   pdl_wait();
@@ -198,20 +202,29 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const Attn
 
   bool bad = false;
   int it = 0;
+  bool kdone = false, knext = false;  // lane 0: this tile's K half landed; the next tile's K copy issued
   for (; it < nmine; ++it) {
+    kdone = knext = false;
     const int t = warp + it * kWarps;
     const int j0 = k0 + t * TK;
     const int rows = min(TK, k1 - j0);
-    const bool ok = mbar_wait(&full[warp], static_cast<uint32_t>(it) & 1u);
-    if (__any_sync(0xffffffffu, !ok)) {
+    const uint32_t par = static_cast<uint32_t>(it) & 1u;
+    if (__any_sync(0xffffffffu, !mbar_wait(&fullk[warp], par))) {
       bad = true;
       break;
     }
+    kdone = true;
     const __half* ksc = reinterpret_cast<const __half*>(slot + 2 * KVB);
     const __half* vsc = ksc + TK;
     // ---- the new token's K/V: stored format to the cache and into the slot
+    // (the V half only once its copy has landed)
     const int jr = pos - j0;
-    if (!a.block_mode && k1 == L && jr >= 0 && jr < rows) {
+    const bool newrow = !a.block_mode && k1 == L && jr >= 0 && jr < rows;
+    if (newrow) {
+      if (__any_sync(0xffffffffu, !mbar_wait(&fullv[warp], par))) {
+        bad = true;
+        break;
+      }
       for (int kv = 0; kv < 2; ++kv) {
         const float* src = qkv + (kv == 0 ? a.nq * D : (a.nq + a.nkv) * D) + g * D;
         KVT* dst = reinterpret_cast<KVT*>(kv == 0 ? a.kc_w : a.vc_w) + (head_row + pos) * D;
@@ -278,6 +291,12 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const Attn
       }
     }
     __syncwarp();
+    // the K half (and K scales) is read: copy the next tile's K rows now
+    if (lane == 0 && it + 1 < nmine) {
+      if (newrow) fence_proxy_async();  // generic stores into the slot before the bulk copy over them
+      issue(t + kWarps, 0);
+      knext = true;
+    }
     // ---- online softmax: lane j holds key j; every lane keeps the running (m, l)
     float al[REP];
 #pragma unroll
@@ -291,6 +310,10 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const Attn
       if (lane < rows) Pw[warp][lane][h] = I8 ? p * __half2float(vsc[lane]) : p;
     }
     __syncwarp();
+    if (!newrow && __any_sync(0xffffffffu, !mbar_wait(&fullv[warp], par))) {
+      bad = true;
+      break;
+    }
     // ---- o = alpha * o + P . V
     if (lane < DL) {
 #pragma unroll
@@ -317,13 +340,21 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const Attn
     }
     __syncwarp();
     if (lane == 0 && it + 1 < nmine) {
-      fence_proxy_async();
-      issue(t + kWarps);
+      if (newrow) fence_proxy_async();
+      issue(t + kWarps, 1);
     }
   }
   if (bad && lane == 0) {
     atomicOr(a.guard, GUARD_TIMEOUT);
-    (void)mbar_wait(&full[warp], static_cast<uint32_t>(it) & 1u);  // the copy in flight, bounded
+    // the copies that may still be in flight into this slot, bounded: this
+    // tile's K half (unless it landed), the next tile's K half (if issued),
+    // this tile's V half (a wait that returns at once if it landed)
+    const uint32_t par = static_cast<uint32_t>(it) & 1u;
+    if (it < nmine) {
+      if (!kdone) (void)mbar_wait(&fullk[warp], par);
+      if (knext) (void)mbar_wait(&fullk[warp], par ^ 1u);
+      (void)mbar_wait(&fullv[warp], par);
+    }
   }
 
   // ---- this warp's state into its (now idle) slot; then the CTA's state -------------
