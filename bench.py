@@ -472,8 +472,11 @@ def run_ours(args, world, rank, local, pg):
                     "note": ("useful FLOPs (2 per weight x token + causal attention); the GEMMs issue twice "
                              "the linear MMAs (activations as bf16 hi + lo halves); attention issues mma.sync "
                              "on fp16 hi + lo halves of the queries and probabilities") if args.weights == "bf16" else
-                            "quantized weights have no tensor-core GEMM path: the prompt runs through the decode step, "
-                            "one token at a time"},
+                            ("fp8: the same tensor-core GEMMs over bf16 copies of the E4M3 codes, each row's scale "
+                             "applied in the GEMM epilogue; the last prompt token takes the fp8 decode step")
+                            if args.weights == "f8" else
+                            "int4: no tensor-core GEMM path (block scales along K): the prompt runs through the "
+                            "decode step, one token at a time"},
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
         "clocks": clk,
         "cpu_baseline": cpu,

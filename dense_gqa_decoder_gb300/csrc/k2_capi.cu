@@ -50,6 +50,9 @@ struct Layout {
   size_t px, pxh, pxl, pah, pal, pqkv, pq, plog;
   size_t wqkv, wo, wgu, wdown, wlm;  // packed weights; per-layer strides below
   size_t wqkv_layer, wo_layer, wgu_layer, wdown_layer;
+  // fp8 weights with a tensor-core prefill: the codes as bf16 in the bf16 packed layout
+  size_t tqkv, to, tgu, tdown;
+  size_t tqkv_layer, to_layer, tgu_layer, tdown_layer;
   size_t kc, vc, ks, vs;  // first layer; per-layer stride kv_layer / sc_layer
   size_t kv_layer, sc_layer;
   size_t total;
@@ -126,7 +129,9 @@ Layout layout_of(const k2_config& c) {
     l.sdown = take(l.sdown_layer * s.L);
     l.slm = take(rows(s.V));
   }
-  l.pchunk = c.weight_dtype == K2_BF16 ? static_cast<int>(align_up(std::min(kPrefillChunk, s.ctx), 128)) : 0;
+  l.pchunk = (c.weight_dtype == K2_BF16 || c.weight_dtype == K2_F8)
+                 ? static_cast<int>(align_up(std::min(kPrefillChunk, s.ctx), 128))
+                 : 0;
   {
     const size_t P = static_cast<size_t>(l.pchunk);
     const size_t kx = std::max(s.H, s.nq * s.d);
@@ -157,6 +162,16 @@ Layout layout_of(const k2_config& c) {
   l.wgu = take(l.wgu_layer * s.L);
   l.wdown = take(l.wdown_layer * s.L);
   l.wlm = take(pbytes(s.V, s.H));
+  if (c.weight_dtype == K2_F8 && l.pchunk > 0) {  // bf16 copies of the fp8 codes for the prefill GEMMs
+    l.tqkv_layer = align_up(packed_bytes(s.qkv_n, s.H, 2), kAlign);
+    l.to_layer = align_up(packed_bytes(s.H, s.nq * s.d, 2), kAlign);
+    l.tgu_layer = align_up(packed_bytes(2 * s.I, s.H, 2), kAlign);
+    l.tdown_layer = align_up(packed_bytes(s.H, s.I, 2), kAlign);
+    l.tqkv = take(l.tqkv_layer * s.L);
+    l.to = take(l.to_layer * s.L);
+    l.tgu = take(l.tgu_layer * s.L);
+    l.tdown = take(l.tdown_layer * s.L);
+  }
   l.repack_bytes = o - scratch_end;
   const size_t kv_start = o;
   l.kv_layer = align_up(static_cast<size_t>(s.B) * s.nkv * l.cap * s.d * s.kvb, kAlign);
@@ -247,7 +262,8 @@ struct k2_ctx {
   std::vector<LayerPtrs> ltab;
   // tensor-core prefill: TMA tensor maps (weights per layer: qkv, o, gate/up,
   // down; activations: normed input, attention output, SwiGLU output, hi/lo)
-  bool tc_ok = false;
+  bool tc_ok = false;    // tensor-core prefill
+  bool tc_full = false;  // and the paths that also need a bf16 lm_head (batched decode, speculation)
   bool use_tc = true;        // prefill
   bool use_tc_decode = true; // batched decode (batch >= 2)
   std::vector<std::array<uint8_t, kTcMapBytes>> tmw;  // 4 per layer
@@ -265,6 +281,21 @@ struct k2_ctx {
   void* wgu(int l) const { return ws + lay.wgu + lay.wgu_layer * l; }
   void* wdown(int l) const { return ws + lay.wdown + lay.wdown_layer * l; }
   void* wlm() const { return ws + lay.wlm; }
+  // the bf16 weights of the prefill GEMMs (m: 0 QKV, 1 o_proj, 2 gate/up, 3 down) and,
+  // for fp8 weights, their row scales
+  bool f8() const { return cfg.weight_dtype == K2_F8; }
+  void* tcw(int l, int m) const {
+    if (!f8()) return m == 0 ? wqkv(l) : m == 1 ? wop(l) : m == 2 ? wgu(l) : wdown(l);
+    const size_t base[4] = {lay.tqkv, lay.to, lay.tgu, lay.tdown};
+    const size_t stride[4] = {lay.tqkv_layer, lay.to_layer, lay.tgu_layer, lay.tdown_layer};
+    return ws + base[m] + stride[m] * l;
+  }
+  const float* tcs(int l, int m) const {
+    if (!f8()) return nullptr;
+    const size_t base[4] = {lay.sqkv, lay.so, lay.sgu, lay.sdown};
+    const size_t stride[4] = {lay.sqkv_layer, lay.so_layer, lay.sgu_layer, lay.sdown_layer};
+    return reinterpret_cast<const float*>(ws + base[m] + stride[m] * l);
+  }
   void* kc(int l) const { return ws + lay.kc + lay.kv_layer * l; }
   void* vc(int l) const { return ws + lay.vc + lay.kv_layer * l; }
   void* ks(int l) const { return lay.sc_layer ? ws + lay.ks + lay.sc_layer * l : nullptr; }
@@ -474,7 +505,7 @@ void enqueue_sample(k2_ctx* c, Launcher& ln, const float* logits, int rows, cons
 void enqueue_decode(k2_ctx* c, Launcher& ln, const int* d_tokens, int batch, int* d_next, float* d_logits) {
   // a sampled step needs the logits: the caller's, else scratch
   float* lg = d_logits ? d_logits : (c->sampling ? c->slog : nullptr);
-  if (batch >= 2 && batch <= 16 && c->tc_ok && c->use_tc_decode) {
+  if (batch >= 2 && batch <= 16 && c->tc_full && c->use_tc_decode) {
     ln.run(K2_K_STEP, [&] { return decode_batched(c, ln.s, d_tokens, batch, d_next, lg); });
   } else {
     for (int b = 0; b < batch; ++b)
@@ -662,21 +693,23 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   return cudaSuccess;
 }
 
-// Tensor maps of the tensor-core prefill (bf16 weights, a supported attention
-// shape).  Leaves tc_ok false when it cannot run.
+// Tensor maps of the tensor-core prefill (bf16 weights, or fp8 weights through
+// bf16 copies of their codes; a supported attention shape).  Leaves tc_ok
+// false when it cannot run; tc_full (batched decode, speculation: a bf16
+// lm_head) only for bf16 weights.
 cudaError_t plan_tc_prefill(k2_ctx* c) {
   const Sizes& s = c->s;
-  c->tc_ok = false;
-  if (c->lay.pchunk <= 0 || s.wb != 2 || !prefill_attn_supported(s.d, s.rep)) return cudaSuccess;
+  c->tc_ok = c->tc_full = false;
+  if (c->lay.pchunk <= 0 || s.gb != 2 || !prefill_attn_supported(s.d, s.rep)) return cudaSuccess;
   if (s.H % 8 || (s.nq * s.d) % 8 || s.I % 8) return cudaSuccess;
   cudaError_t e = prefill_init_attrs();
   if (e != cudaSuccess) return e;
   c->tmw.resize(4 * static_cast<size_t>(s.L));
   for (int l = 0; l < s.L; ++l) {
-    if (!tc_encode_weight(c->tmw[4 * l].data(), c->wqkv(l), s.qkv_n, s.H) ||
-        !tc_encode_weight(c->tmw[4 * l + 1].data(), c->wop(l), s.H, s.nq * s.d) ||
-        !tc_encode_weight(c->tmw[4 * l + 2].data(), c->wgu(l), 2 * s.I, s.H) ||
-        !tc_encode_weight(c->tmw[4 * l + 3].data(), c->wdown(l), s.H, s.I))
+    if (!tc_encode_weight(c->tmw[4 * l].data(), c->tcw(l, 0), s.qkv_n, s.H) ||
+        !tc_encode_weight(c->tmw[4 * l + 1].data(), c->tcw(l, 1), s.H, s.nq * s.d) ||
+        !tc_encode_weight(c->tmw[4 * l + 2].data(), c->tcw(l, 2), 2 * s.I, s.H) ||
+        !tc_encode_weight(c->tmw[4 * l + 3].data(), c->tcw(l, 3), s.H, s.I))
       return cudaSuccess;
   }
   const int P = c->lay.pchunk;
@@ -691,10 +724,9 @@ cudaError_t plan_tc_prefill(k2_ctx* c) {
   }
   // the batched decode keeps the gate/up output of 16 tokens in the QKV buffer
   if (16 * 2 * static_cast<size_t>(s.I) > static_cast<size_t>(P) * s.qkv_n) return cudaSuccess;
-  if (!ok ||
-      !tc_encode_weight(c->tm_lm.data(), c->wlm(), s.V, s.H))
-    return cudaSuccess;
+  if (!ok) return cudaSuccess;
   c->tc_ok = true;
+  c->tc_full = !c->f8() && tc_encode_weight(c->tm_lm.data(), c->wlm(), s.V, s.H);
   return cudaSuccess;
 }
 
@@ -716,7 +748,8 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
   const size_t head_row0 = static_cast<size_t>(seq) * s.nkv * c->lay.cap;
   const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(s.d)));
-  auto gemm = [&](const void* mw, const void* mh, const void* ml, int N, int K, int mode, float* out,
+  // rs: the weight rows' scales (fp8 codes), else null
+  auto gemm = [&](const void* mw, const float* rs, const void* mh, const void* ml, int N, int K, int mode, float* out,
                   __nv_bfloat16* oh, __nv_bfloat16* ol, int ldo) {
     TcGemmArgs g = {};
     g.N = N;
@@ -731,6 +764,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.out_hi = oh;
     g.out_lo = ol;
     g.guard = c->guard;
+    g.row_scale = rs;
     return launch_tc_gemm(mw, mh, ml, g, st);
   };
   // a block of at most 16 tokens (a speculative verification) streams every
@@ -738,7 +772,8 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   // SM: the 128-token tiles would leave most SMs idle
   const bool small = n <= 16;
   const int tt = small ? 16 : 128;
-  auto gemm_sk = [&](const void* mw, const void* mh, const void* ml, int N, int K, int mode, float* out, int ldo) {
+  auto gemm_sk = [&](const void* mw, const float* rs, const void* mh, const void* ml, int N, int K, int mode, float* out,
+                     int ldo) {
     TcGemmArgs g = {};
     g.N = N;
     g.K = K;
@@ -750,6 +785,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.splits = 1;
     g.out = out;
     g.guard = c->guard;
+    g.row_scale = rs;
     cudaError_t e = cudaSuccess;
     if (mode == TC_STORE) e = cudaMemsetAsync(out, 0, sizeof(float) * static_cast<size_t>(n) * ldo, st);
     if (!e) e = launch_tc_gemm_sk(mw, mh, ml, g, c->sms, st);
@@ -762,13 +798,14 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   const void* m_ah = small ? c->tb_ah.data() : c->tm_ah.data();
   const void* m_al = small ? c->tb_al.data() : c->tm_al.data();
   float* O32 = Q + static_cast<size_t>(16) * s.nq * s.d;  // small blocks: the attention output after 16 query rows
-  cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.wb, X, s.H, s.V, c->guard,
+  cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.gb, X, s.H, s.V, c->guard,
                                     c->hist + static_cast<size_t>(seq) * c->lay.cap, 0, nullptr, pos0, d_pos0, st);
   for (int l = 0; l < s.L && !e; ++l) {
-    if (!e) e = launch_norm_rows(X, n, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
+    if (!e) e = launch_norm_rows(X, n, c->attn_norm[l], s.gb, xh, xl, s.H, s.G, c->cfg.eps, st);
     if (!e)
-      e = small ? gemm_sk(c->tmw[4 * l].data(), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, s.qkv_n)
-                : gemm(c->tmw[4 * l].data(), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, nullptr, nullptr, s.qkv_n);
+      e = small ? gemm_sk(c->tmw[4 * l].data(), c->tcs(l, 0), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, s.qkv_n)
+                : gemm(c->tmw[4 * l].data(), c->tcs(l, 0), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, nullptr, nullptr,
+                       s.qkv_n);
     if (!e)
       e = launch_rope_append(qkv, Q, c->rope, kvdt, c->kc(l), c->vc(l), c->ks(l), c->vs(l), n, s.nq, s.nkv, s.d,
                              pos0, d_pos0, head_row0, c->lay.cap, st);
@@ -795,17 +832,17 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
                               head_row0, c->lay.cap, scale, st);
     }
     // o_proj and down have few row tiles: stream-K over one CTA per SM
-    if (!e) e = gemm_sk(c->tmw[4 * l + 1].data(), m_oh, m_ol, s.H, s.nq * s.d, TC_RESID, X, s.H);
-    if (!e) e = launch_norm_rows(X, n, c->mlp_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
+    if (!e) e = gemm_sk(c->tmw[4 * l + 1].data(), c->tcs(l, 1), m_oh, m_ol, s.H, s.nq * s.d, TC_RESID, X, s.H);
+    if (!e) e = launch_norm_rows(X, n, c->mlp_norm[l], s.gb, xh, xl, s.H, s.G, c->cfg.eps, st);
     if (!e) {
       if (small) {  // gate/up rows to fp32 (the QKV buffer is free by now), then SwiGLU rows
-        e = gemm_sk(c->tmw[4 * l + 2].data(), m_xh, m_xl, 2 * s.I, s.H, TC_STORE, qkv, 2 * s.I);
+        e = gemm_sk(c->tmw[4 * l + 2].data(), c->tcs(l, 2), m_xh, m_xl, 2 * s.I, s.H, TC_STORE, qkv, 2 * s.I);
         if (!e) e = launch_swiglu_rows(qkv, ah, al, n, s.I, st);
       } else {
-        e = gemm(c->tmw[4 * l + 2].data(), m_xh, m_xl, 2 * s.I, s.H, TC_SWIGLU, nullptr, ah, al, s.I);
+        e = gemm(c->tmw[4 * l + 2].data(), c->tcs(l, 2), m_xh, m_xl, 2 * s.I, s.H, TC_SWIGLU, nullptr, ah, al, s.I);
       }
     }
-    if (!e) e = gemm_sk(c->tmw[4 * l + 3].data(), m_ah, m_al, s.H, s.I, TC_RESID, X, s.H);
+    if (!e) e = gemm_sk(c->tmw[4 * l + 3].data(), c->tcs(l, 3), m_ah, m_al, s.H, s.I, TC_RESID, X, s.H);
   }
   return e;
 }
@@ -883,11 +920,20 @@ cudaError_t prefill_tc(k2_ctx* c, int seq, const int* d_tokens, int n, int* d_ne
   const int P = c->lay.pchunk;
   cudaError_t e = cudaSuccess;
   int last = 0;
-  for (int b0 = 0; b0 < n && !e; b0 += P) {
-    last = std::min(P, n - b0);
+  // fp8 weights: the lm_head exists only as fp8 rows, so the last token takes
+  // the persistent step (which ends in the lm_head and argmax)
+  const int nb = c->f8() ? n - 1 : n;
+  for (int b0 = 0; b0 < nb && !e; b0 += P) {
+    last = std::min(P, nb - b0);
     e = prefill_block(c, seq, d_tokens + b0, last, c->len[seq] + b0, st);
   }
   if (e) return e;
+  if (c->f8()) {
+    if ((e = launch_advance_by(c->seq_len, seq, nb, st)) != cudaSuccess) return e;
+    Launcher ln{c, st, false};
+    enqueue_token(c, ln, seq, d_tokens + nb, nullptr, d_next, d_logits, true);
+    return ln.err;
+  }
   float* xrow = c->resid + static_cast<size_t>(seq) * s.H;
   e = cudaMemcpyAsync(xrow, c->ws + c->lay.px + static_cast<size_t>(last - 1) * s.H * 4, sizeof(float) * s.H,
                       cudaMemcpyDeviceToDevice, st);
@@ -917,7 +963,7 @@ cudaError_t verify_block(k2_ctx* c, int seq, const int* d_tokens, int n, int* d_
   auto* xh = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxh);
   auto* xl = reinterpret_cast<__nv_bfloat16*>(c->ws + c->lay.pxl);
   float* logits = reinterpret_cast<float*>(c->ws + c->lay.vlog);
-  if (!e) e = launch_norm_rows(X, n, c->final_norm, s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
+  if (!e) e = launch_norm_rows(X, n, c->final_norm, s.gb, xh, xl, s.H, s.G, c->cfg.eps, st);
   if (!e) e = cudaMemsetAsync(logits, 0, sizeof(float) * static_cast<size_t>(n) * s.V, st);
   if (!e) {
     TcGemmArgs g = {};
@@ -1191,6 +1237,12 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   }
   if (e == cudaSuccess && !quantized(cfg->weight_dtype))
     e = launch_pack(c->wlm(), w->lm_head, nullptr, nullptr, PACK_PLAIN, z.V, z.H, z.wb, 0, 0, 1, s);
+  for (int l = 0; l < z.L && e == cudaSuccess && cfg->weight_dtype == K2_F8 && c->lay.pchunk > 0; ++l) {
+    e = launch_f8_expand(c->tcw(l, 0), static_cast<const uint8_t*>(c->wqkv(l)), z.qkv_n, z.H, s);
+    if (e == cudaSuccess) e = launch_f8_expand(c->tcw(l, 1), static_cast<const uint8_t*>(c->wop(l)), z.H, z.nq * z.d, s);
+    if (e == cudaSuccess) e = launch_f8_expand(c->tcw(l, 2), static_cast<const uint8_t*>(c->wgu(l)), 2 * z.I, z.H, s);
+    if (e == cudaSuccess) e = launch_f8_expand(c->tcw(l, 3), static_cast<const uint8_t*>(c->wdown(l)), z.H, z.I, s);
+  }
   if (e != cudaSuccess) {
     g_init_error = std::string("repack: ") + cudaGetErrorString(e);
     delete c;
@@ -1233,6 +1285,8 @@ k2_status k2_get_info(const k2_ctx* c, k2_info* info) {
   info->gemv_grid = c->grid_gu;
   info->persistent_grid = c->mega_ok ? c->mega_grid : 0;
   info->persistent_splits = c->mega_ok ? c->mega.nsplit : 0;
+  info->tc_prefill = c->tc_ok ? 1 : 0;
+  info->tc_batched = c->tc_full ? 1 : 0;
   info->kv_bytes = static_cast<int64_t>(c->lay.kv_bytes);
   info->repack_bytes = static_cast<int64_t>(c->lay.repack_bytes);
   info->scratch_bytes = static_cast<int64_t>(c->lay.total - c->lay.kv_bytes - c->lay.repack_bytes);
@@ -1664,7 +1718,7 @@ k2_status k2_decode_speculative(k2_ctx* c, int32_t seq, const int32_t* h_tokens,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int ids[kSpecMax + 1];
   ids[0] = h_tokens[n_tokens - 1];
-  int nd = c->tc_ok ? k2_spec_draft(h_tokens, n_tokens, std::min<int>(max_draft, kSpecMax), ids + 1) : 0;
+  int nd = c->tc_full ? k2_spec_draft(h_tokens, n_tokens, std::min<int>(max_draft, kSpecMax), ids + 1) : 0;
   nd = std::min(nd, c->s.ctx - c->len[seq] - 1);  // every verified row must fit
   if (nd < 0) nd = 0;
   int* d_ids = reinterpret_cast<int*>(c->ws + c->lay.vids);

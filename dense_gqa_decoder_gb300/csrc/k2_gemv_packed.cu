@@ -595,6 +595,24 @@ cudaError_t launch_pack(void* dst, const void* src0, const void* src1, const voi
   return cudaGetLastError();
 }
 
+// One CTA of 256 threads per (packed row R, bf16 chunk c): weight k = 256 c + t.
+__global__ void __launch_bounds__(256) f8_expand_kernel(__nv_bfloat16* __restrict__ dst,
+                                                        const uint8_t* __restrict__ src, int CT8, int CT16) {
+  const int R = blockIdx.x, c = blockIdx.y, k = c * 256 + threadIdx.x;
+  const int c8 = k >> 9, i8 = k & 511;
+  const uint8_t code = src[(static_cast<size_t>(R >> 1) * CT8 + c8) * 1024 + (R & 1) * 512 + i8];
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);
+  dst[(static_cast<size_t>(R >> 1) * CT16 + c) * 512 + (R & 1) * 256 + threadIdx.x] =
+      __float2bfloat16_rn(__half2float(__half(h)));
+}
+
+cudaError_t launch_f8_expand(void* dst, const uint8_t* src, int N, int K, cudaStream_t s) {
+  const int CT8 = (K + 511) / 512, CT16 = (K + 255) / 256, rows = 2 * ((N + 1) / 2);
+  if (rows <= 0 || CT16 <= 0) return cudaSuccess;
+  f8_expand_kernel<<<dim3(rows, CT16), 256, 0, s>>>(static_cast<__nv_bfloat16*>(dst), src, CT8, CT16);
+  return cudaGetLastError();
+}
+
 size_t q4_packed_bytes(int N, int K) {
   const size_t CT = (static_cast<size_t>(K) + kQ4Chunk - 1) / kQ4Chunk;
   return (static_cast<size_t>(N) + 1) / 2 * CT * kQ4Unit;

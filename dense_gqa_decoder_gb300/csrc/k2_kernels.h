@@ -142,6 +142,9 @@ cudaError_t launch_quant_pack(uint8_t* dst, float* scales, const void* src0, con
 cudaError_t launch_q4_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
                            int mode, int N, int K, int nq, int nkv, int d, bool packed, cudaStream_t s);
 size_t q4_packed_bytes(int N, int K);
+// The fp8 codes of a packed matrix (512 per chunk and row) as bf16 values (exact:
+// every E4M3 value is a bf16 value) in the bf16 packed layout (256 per chunk and row).
+cudaError_t launch_f8_expand(void* dst, const uint8_t* src, int N, int K, cudaStream_t s);
 cudaError_t launch_pack(void* dst, const void* src0, const void* src1, const void* src2, int mode, int N, int K,
                         int wbytes, int nq, int nkv, int d, cudaStream_t s);
 
@@ -348,6 +351,7 @@ struct TcGemmArgs {
   __nv_bfloat16* out_hi;
   __nv_bfloat16* out_lo;
   unsigned* guard;
+  const float* row_scale;  // non-null: each row's accumulator is multiplied by row_scale[row] first
 };
 constexpr int kTcMapBytes = 128;  // one CUtensorMap
 bool tc_encode_weight(void* map, const void* packed, int N, int K);  // bf16 packed weights

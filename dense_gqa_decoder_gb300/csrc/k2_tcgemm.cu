@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
   tc_after();
   if (ok && nk > 0 && (__ldcg(a.guard) & GUARD_TIMEOUT) == 0u) {
     const int row = m0 + warp * 32 + lane;
+    const float rs = (a.row_scale != nullptr && row < a.N) ? __ldg(a.row_scale + row) : 1.f;
     constexpr int CW = BN < 32 ? BN : 32;  // accumulator columns read per tcgen05.ld
 #pragma unroll 1
     for (int c = 0; c < BN; c += CW) {
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
 #pragma unroll
       for (int j = 0; j < CW; ++j) {
         const int t = n0 + c + j;
-        const float acc = __uint_as_float(v[j]);
+        const float acc = a.row_scale != nullptr ? __uint_as_float(v[j]) * rs : __uint_as_float(v[j]);
         if (a.mode == TC_SWIGLU) {  // rows (2p, 2p+1) = (gate_p, up_p): adjacent lanes
           const float up = __shfl_xor_sync(0xffffffffu, acc, 1);
           if (!(lane & 1) && t < a.T && row < a.N) {
@@ -345,9 +346,12 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
       const int row = static_cast<int>(tile / tok_tiles) * BM + lg + lane;
       const int n0 = static_cast<int>(tile % tok_tiles) * BN;
       if (row < a.N) {
+        const float rs = a.row_scale != nullptr ? __ldg(a.row_scale + row) : 1.f;
 #pragma unroll
         for (int j = 0; j < BN; ++j)
-          if (n0 + j < a.T) atomicAdd(a.out + static_cast<size_t>(n0 + j) * a.ldo + row, __uint_as_float(v[j]));
+          if (n0 + j < a.T)
+            atomicAdd(a.out + static_cast<size_t>(n0 + j) * a.ldo + row,
+                      a.row_scale != nullptr ? __uint_as_float(v[j]) * rs : __uint_as_float(v[j]));
       }
       g = end;
       ++piece;

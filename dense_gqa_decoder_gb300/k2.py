@@ -47,7 +47,8 @@ class Weights(C.Structure):
 class Info(C.Structure):
     _fields_ = [("kv_capacity", C.c_int32), ("num_sms", C.c_int32), ("attn_splits", C.c_int32),
                 ("gemv_grid", C.c_int32), ("kv_bytes", C.c_int64), ("repack_bytes", C.c_int64),
-                ("scratch_bytes", C.c_int64), ("persistent_grid", C.c_int32), ("persistent_splits", C.c_int32)]
+                ("scratch_bytes", C.c_int64), ("persistent_grid", C.c_int32), ("persistent_splits", C.c_int32),
+                ("tc_prefill", C.c_int32), ("tc_batched", C.c_int32)]
 
 
 class Sampling(C.Structure):

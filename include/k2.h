@@ -118,6 +118,10 @@ typedef struct {
   int64_t scratch_bytes; /* everything else in the workspace */
   int32_t persistent_grid;   /* CTAs of the persistent batch-1 step (0: not available) */
   int32_t persistent_splits; /* its key-range splits per KV head */
+  int32_t tc_prefill;        /* 1: prompts of >= 8 tokens run through the tensor-core GEMMs
+                                (bf16 weights, or fp8 weights through bf16 copies of their codes) */
+  int32_t tc_batched;        /* 1: batched decode and speculative verification on the tensor
+                                cores (bf16 weights only) */
 } k2_info;
 
 /* ---- set-up -------------------------------------------------------------- */

@@ -79,3 +79,42 @@ def test_fp8_refuses_the_kernel_chain(k2, mio):
     with pytest.raises(k2.K2Error) as e:
         ctx.set_option(k2.K2_OPT_PERSISTENT, 0)
     assert e.value.status == k2.K2_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("shape,kv,n", [("medium", "f16", 40), ("medium", "i8", 9), ("k2_layer", "f16", 300)])
+def test_fp8_tensor_core_prefill_matches_stepwise(k2, mio, shape, kv, n):
+    """A prompt of fp8 weights on the tensor cores (bf16 copies of the codes, the
+    row scales in the GEMM epilogue, the last token on the persistent step)
+    against the same prompt appended one persistent step per token, and against
+    the oracle's full recompute over the same quantized weights.  The bar is the
+    bf16 tensor-core prefill's: its activations enter the MMAs as bf16 hi + lo
+    halves (~16 significant bits), 2e-4 relative on the logits."""
+    s = ki.SHAPES[shape]
+    ids = ki.prompt_ids(s.vocab, n, seed=94)
+    prompt = torch.tensor(ids, dtype=torch.int32, device="cuda")
+    runs = []
+    for tc in (1, 0):
+        ctx, host = mio.build_context(s, max_context=n + 16, kv_dtype=kv, gain_scale=0.1, keep_host=True,
+                                      weights="f8")
+        info = ctx.info()
+        assert info.tc_prefill == 1 and info.tc_batched == 0
+        ctx.set_option(k2.K2_OPT_TC_PREFILL, tc)
+        nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+        logits = torch.empty(s.vocab, dtype=torch.float32, device="cuda")
+        ctx.prefill(0, prompt, nxt, logits)
+        toks, lgs = [int(nxt.item())], [logits.cpu().numpy().copy()]
+        for _ in range(4):
+            ctx.decode_step(nxt, 1, nxt, logits)
+            toks.append(int(nxt.item()))
+            lgs.append(logits.cpu().numpy().copy())
+        assert ctx.sync_status() == k2.K2_OK
+        runs.append((toks, np.stack(lgs).astype(np.float64)))
+    (t_tc, l_tc), (t_st, l_st) = runs
+    rel = float(np.linalg.norm(l_tc - l_st) / np.linalg.norm(l_st))
+    assert rel <= (2e-4 if kv == "f16" else 2e-2), rel
+    ref = O.OracleModel(s, Q8.fp8_weights(lambda nm, l: host[(nm, l)]), kv).forward_full(ids)
+    rel_o = float(np.linalg.norm(l_tc[0] - ref) / np.linalg.norm(ref))
+    assert rel_o <= (2e-4 if kv == "f16" else 5e-2), rel_o
+    if kv == "f16":
+        assert t_tc == t_st
+        assert t_tc[0] == O.argmax_first(ref)
