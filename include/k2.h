@@ -73,8 +73,11 @@ typedef enum { K2_F32 = 0, K2_BF16 = 1, K2_F16 = 2, K2_I8 = 3, K2_F8 = 4, K2_Q4 
  * rows with one fp32 scale per row (K2_F8, see k2_quantize_fp8), or as int4
  * codes with one fp32 scale per 64 weights of a row (K2_Q4, see
  * k2_quantize_q4); the embedding and the norm gains stay bf16.  Such a model
- * runs on the persistent step only (prompts are appended one step per token)
- * and is refused where that step is not available.  max_context = KV rows per sequence (prompt + generated tokens);
+ * decodes on the persistent step only and is refused where that step is not
+ * available.  Prompts of >= 8 tokens with K2_F8 weights run through the
+ * tensor-core GEMMs over bf16 copies of the codes (exact), each row's scale
+ * applied to its outputs, the last token through the persistent step; K2_Q4
+ * prompts are appended one persistent step per token.  max_context = KV rows per sequence (prompt + generated tokens);
  * max_batch = number of independent sequences. */
 typedef struct {
   int32_t hidden, n_layers, n_heads, n_kv_heads, head_dim, intermediate, norm_groups, vocab;
@@ -158,10 +161,12 @@ k2_status k2_get_info(const k2_ctx* ctx, k2_info* info);
  * position's fp32 logits [vocab] are written there (kimi-k3-in-c k3_run.c:
  * `forward` returns last-position logits).  K2_ERR_CONTEXT_FULL if
  * length + n > max_context: the prompt is rejected, not truncated. */
-/* With bf16 weights (and option K2_OPT_TC_PREFILL) a prompt of 8 or more tokens is
- * processed in blocks of up to 2048 tokens: the projections as tcgen05 tensor-core
- * GEMMs (activations split into two bf16 halves, fp32 accumulation), causal
- * attention over the cache, the residual stream in fp32. */
+/* With bf16 or fp8 weights (and option K2_OPT_TC_PREFILL) a prompt of 8 or more
+ * tokens is processed in blocks of up to 2048 tokens: the projections as tcgen05
+ * tensor-core GEMMs (activations split into two bf16 halves, fp32 accumulation;
+ * fp8: the codes as bf16, each output row times its scale), causal attention over
+ * the cache, the residual stream in fp32.  With fp8 weights the last token takes
+ * the persistent step, which ends in the fp8 lm_head. */
 k2_status k2_prefill(k2_ctx* ctx, int32_t seq, const int32_t* d_tokens, int32_t n, int32_t* d_next_token,
                      float* d_logits, void* stream);
 
@@ -362,8 +367,8 @@ typedef enum {
   K2_OPT_PERSISTENT = 3,  /* 1 (default): batch-1 tokens run as one persistent cooperative kernel
                              (one CTA per SM, dataflow waits between the phases of a layer) when the
                              shape allows; 0: always the chain of per-step kernels */
-  K2_OPT_TC_PREFILL = 4,  /* 1 (default): bf16 models prefill prompts of >= 8 tokens with tensor-core
-                             GEMMs over blocks of up to 2048 tokens; 0: one decode step per token */
+  K2_OPT_TC_PREFILL = 4,  /* 1 (default): bf16 and fp8 models prefill prompts of >= 8 tokens with
+                             tensor-core GEMMs over blocks of up to 2048 tokens; 0: one decode step per token */
   K2_OPT_TC_DECODE = 5    /* 1 (default): a bf16 decode step of batch >= 2 reads the weights once for
                              all sequences (tensor-core GEMMs, N = batch); 0: one token at a time */
 } k2_option;
