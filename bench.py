@@ -208,6 +208,24 @@ def dist_setup(n_gpus):
     return world, rank, local, pg
 
 
+def max_over_ranks(pg, value: float) -> float:
+    """The largest of a per-rank number over all ranks (the slowest rank's
+    time); the number itself on a single rank."""
+    if pg is None:
+        return value
+    import torch
+    dev = "cuda" if pg.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: float, seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (every rank does the same fixed work: weak scaling)."""
+    return world * units_per_rank / seconds
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle legs (the oracle as it stands, on this host's cores)
 # ---------------------------------------------------------------------------
@@ -375,15 +393,11 @@ def run_ours(args, world, rank, local, pg):
     if pg:
         pg.barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(pg, e0.elapsed_time(e1))
     if ctx.sync_status(stream) != k2.K2_OK:
         raise RuntimeError("device guard after the timed steps: " + ctx.last_error())
     ms_per_step = ms / args.steps
-    value = world * args.steps / (ms / 1e3)
+    value = job_throughput(world, args.steps, ms / 1e3)
     mean_ctx = ctx_start + (args.steps - 1) / 2 + 1
     by = algorithmic_bytes(s, int(round(mean_ctx)), args.kv, args.weights)
 
@@ -644,11 +658,7 @@ def run_batched(args, world, rank, local, pg):
     if pg:
         pg.barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(pg, e0.elapsed_time(e1))
     if ctx.sync_status(stream) != k2.K2_OK:
         raise RuntimeError("device guard after the timed steps: " + ctx.last_error())
     ms_per_step = ms / args.steps
@@ -659,7 +669,8 @@ def run_batched(args, world, rank, local, pg):
     achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
     line = {
         "metric": f"batch-{B} decode aggregate tok/s (3.7B dense GQA, bf16) and achieved HBM GB/s vs peak",
-        "value": world * B * args.steps / (ms / 1e3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "value": job_throughput(world, B * args.steps, ms / 1e3), "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"k2-horizon-3.7b-shape greedy decode, {B} sequences, context {args.ctx}, {args.kv} KV",
