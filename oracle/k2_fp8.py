@@ -5,7 +5,7 @@ the library.
 
 k2-burn README, "Post-training quantization": a quantize step produces fp8
 (E4M3) checkpoints that the engine runs directly.  The page names the format
-only; the reading taken (listed in the design doc): one fp32 scale per weight row
+only; the reading taken: one fp32 scale per weight row
 (output feature), s = max|w| / 448 (448 = the largest finite E4M3 value),
 code = E4M3(w / s) rounded to nearest, ties to even, saturating at +-448; a
 row of zeros gets s = 0 and codes 0.  The weight the model computes with is

@@ -29,7 +29,7 @@ inputs) and K/V rows stored as fp32, fp16 or int8+fp16 scale (``store_kv``).
 The int8 quantiser takes its rounding decisions in float32, the precision the
 CUDA kernels use for the same decision.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
   * GroupedRMSNorm: the hidden vector is split into ``groups`` contiguous
     equal groups; each group is divided by sqrt(mean(x_g^2) + eps); the result
     is multiplied by one full-length gain.  No mean subtraction, no bias.  All

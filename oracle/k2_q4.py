@@ -6,8 +6,7 @@ the library.
 k2-burn README, "Post-training quantization" / "Quantization": the quantize
 step produces int4 "Q4S" checkpoints with block size 64, and only the Linear
 weights (the projections and the lm_head) are quantized.  The page names the
-scheme, the bit width and the block size only; the reading taken (listed in
-DESIGN.md):
+scheme, the bit width and the block size only; the reading taken:
 
   * a block is 64 consecutive weights of one row (one output feature) along
     the input dimension; a row whose length is not a multiple of 64 ends in a

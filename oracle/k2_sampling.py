@@ -10,7 +10,7 @@ flags): temperature 0 is the greedy argmax; temperature > 0 draws the next
 token from the logits after a repetition penalty on already-seen tokens and
 the top-k / top-p / min-p truncation filters, with a seeded generator.
 
-Readings where the page only names the knobs (each listed in the design doc):
+Readings where the page only names the knobs:
   * repetition penalty r: each distinct already-seen id has its logit l
     replaced by l / r if l > 0, else l * r (r = 1: off);
   * order: penalty, z = l / temperature, top-k, top-p, min-p, draw;

@@ -1,6 +1,6 @@
 """Parity of the CUDA decode path (through the C ABI) with the CPU oracle.
 
-Tolerances (written here, derived in the design doc):
+Tolerances (each written in its test):
   * fp32 tiny model: greedy tokens identical, logits max-abs <= 1e-4;
   * bf16 weights + fp16 KV: hidden-state relative L2 <= 2e-2 and teacher-forced
     argmax agreement >= 99%; the kernels keep fp32 activations, so the tests
