@@ -65,6 +65,8 @@ MUTANTS = (
     "no_attn_scale",        # the 1/sqrt(d) is dropped
     "attend_excludes_self", # the newly appended KV row is not attended to
     "k_pos_shift",          # K rotated one position ahead of Q
+    "swiglu_swapped",       # silu applied to the up branch instead of the gate
+    "no_silu",              # the gate branch enters the product without silu
 )
 
 
@@ -284,7 +286,11 @@ class OracleModel:
             exclude_self=self.mutant == "attend_excludes_self")
         x = x + attn.reshape(T, s.n_heads * d) @ self._w("wo", l).T
         xn = self._norm(x, self._w("mlp_norm", l))
-        a = silu(xn @ self._w("w_gate", l).T) * (xn @ self._w("w_up", l).T)
+        g = xn @ self._w("w_gate", l).T
+        u = xn @ self._w("w_up", l).T
+        if self.mutant == "swiglu_swapped":
+            g, u = u, g
+        a = (g if self.mutant == "no_silu" else silu(g)) * u
         return x + a @ self._w("w_down", l).T
 
     def embed(self, tokens):

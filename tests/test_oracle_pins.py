@@ -305,6 +305,52 @@ def test_uniform_attention_closed_form():
         np.testing.assert_allclose(x[p], expect, rtol=1e-12, atol=1e-13)
 
 
+def test_swiglu_branch_closed_form():
+    # With Wq = 0 and Wo = 0 the attention adds nothing, so the layer's update
+    # is Wd . (silu(Wg . xn) * (Wu . xn)) with xn the post-attention norm of
+    # the embedding row.  Wg picks xn[0] * 3 / xn[0], Wu picks -xn[0] / xn[0],
+    # i.e. gate g = 3 and up u = -1 in channel 0 (zero elsewhere), and Wd
+    # copies channel 0 into hidden element 5.  The update is silu(3) * (-1) =
+    # -3 / (1 + e^-3) = -2.857722..., while silu on the up branch gives
+    # silu(-1) * 3 = -0.806824... and no silu at all gives -3.
+    s = ki.TINY.replace(n_layers=1)
+    H, I = s.hidden, s.intermediate
+    base = {}
+
+    def w(n, l):
+        if (n, l) not in base:
+            base[(n, l)] = ki.weight(s, n, l).values
+        return base[(n, l)]
+    tok = ki.prompt_ids(s.vocab, 1, seed=5)
+    e = w("embed", -1)[tok[0]].astype(np.float64)
+    xn = O.grouped_rms_norm(e, np.ones(H), 2, s.eps)
+    wg = np.zeros((I, H))
+    wg[0, 0] = 3.0 / xn[0]
+    wu = np.zeros((I, H))
+    wu[0, 0] = -1.0 / xn[0]
+    wd = np.zeros((H, I))
+    wd[5, 0] = 1.0
+
+    def get(n, l):
+        if n in ("wq", "wo"):
+            return np.zeros(ki.tensor_shape(s, n))
+        if n in ("attn_norm", "mlp_norm", "final_norm"):
+            return np.ones(H)
+        mlp = {"w_gate": wg, "w_up": wu, "w_down": wd}
+        return mlp[n] if n in mlp else w(n, l)
+    expect = e.copy()
+    expect[5] += -3.0 / (1.0 + math.exp(-3.0))
+    assert abs(expect[5] - e[5] - (-2.8577223804673)) < 1e-12
+    got = {}
+    for m in (None, "swiglu_swapped", "no_silu"):
+        x, _ = O.OracleModel(s, get, "f32", mutant=m).run(tok, O.KVCache(1, 1, s.n_kv_heads, s.head_dim), logits_rows=None)
+        got[m] = x[0]
+    np.testing.assert_allclose(got[None], expect, rtol=0, atol=1e-12)
+    # the two plausible mistakes give the hand-computed wrong values
+    assert abs(got["swiglu_swapped"][5] - e[5] - (-1.0 / (1.0 + math.exp(1.0))) * 3.0) < 1e-12
+    assert abs(got["no_silu"][5] - e[5] - (-3.0)) < 1e-12
+
+
 @pytest.mark.parametrize("mutant", [m for m in O.MUTANTS if m is not None])
 def test_planted_mutants_break_parity(mutant):
     # cpu_weights.rs, `Ablation`: a known-bad graph must move the output by far
