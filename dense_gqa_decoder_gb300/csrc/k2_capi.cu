@@ -1677,29 +1677,53 @@ k2_status k2_philox(uint32_t first, int32_t n, uint32_t c1, uint32_t c2, uint32_
   return e == cudaSuccess ? K2_OK : K2_ERR_CUDA;
 }
 
+// Drafting works on the history read backwards, r[k] = h_tokens[T - 1 - k].
+// The Z-algorithm gives, for every shift i >= 1, z[i] = the length of the
+// longest common prefix of r and r[i..]: the number of ids that the earlier
+// stretch of the history ending at position T - 1 - i shares with the end of
+// the history.  A suffix of n ids occurred earlier, ending at T - 1 - i,
+// exactly when z[i] >= n, and the smallest such shifts are its most recent
+// occurrences; one pass serves n = 4 and n = 3 alike.
 int32_t k2_spec_draft(const int32_t* h_tokens, int32_t n_tokens, int32_t max_draft, int32_t* h_out) {
   if (!h_tokens || n_tokens < 0 || max_draft < 1 || !h_out) return 0;
-  const int cap = std::min<int>(max_draft, kSpecMax);
+  constexpr int kLongest = 4, kShortest = 3;
   const int T = n_tokens;
-  for (int n = 4; n >= 3; --n) {  // the longer suffix first
-    if (T < n + 1) continue;
-    const int32_t* tail = h_tokens + T - n;
-    // the two latest earlier occurrences of the suffix
-    int latest = -1, second = -1;
-    for (int j = T - n - 1; j >= 0 && second < 0; --j) {
-      if (!std::equal(tail, tail + n, h_tokens + j)) continue;
-      if (latest < 0) latest = j;
-      else second = j;
+  if (T < kShortest + 1) return 0;
+  const int cap = std::min<int>(max_draft, kSpecMax);
+  auto r = [&](int k) { return h_tokens[T - 1 - k]; };
+  static thread_local std::vector<int> z;
+  z.assign(T, 0);
+  // shifts of the two most recent occurrences per suffix length n (0 = none)
+  int near[kLongest + 1][2] = {};
+  for (int i = 1, lo = 0, hi = 0; i + kShortest <= T; ++i) {
+    int m = i < hi ? std::min(hi - i, z[i - lo]) : 0;
+    while (i + m < T && r(m) == r(i + m)) ++m;
+    z[i] = m;
+    if (i + m > hi) lo = i, hi = i + m;
+    for (int n = kShortest; n <= std::min(m, kLongest); ++n)
+      if (i + n <= T) {
+        if (!near[n][0]) near[n][0] = i;
+        else if (!near[n][1]) near[n][1] = i;
+      }
+    if (near[kLongest][1]) break;  // both lengths have their two latest occurrences
+  }
+  for (int n = kLongest; n >= kShortest; --n) {
+    const int a = near[n][0], b = near[n][1];
+    if (!a) continue;
+    // the ids after the newest occurrence run from T - a to the end (a of them)
+    int len = std::min(cap, a);
+    if (b) {
+      // the older occurrence must agree, and its continuation (from T - b)
+      // must stay short of the newest occurrence, which starts at T - a - n
+      len = std::min(len, b - a - n);
+      int agree = 0;
+      while (agree < len && h_tokens[T - a + agree] == h_tokens[T - b + agree]) ++agree;
+      len = agree;
     }
-    if (latest < 0) continue;
-    int nd = 0;
-    while (nd < cap && latest + n + nd < T) {
-      const int32_t next = h_tokens[latest + n + nd];
-      // with two occurrences, draft only as far as their continuations agree
-      if (second >= 0 && (second + n + nd >= latest || h_tokens[second + n + nd] != next)) break;
-      h_out[nd++] = next;
+    if (len > 0) {
+      std::copy(h_tokens + T - a, h_tokens + T - a + len, h_out);
+      return len;
     }
-    if (nd > 0) return nd;
   }
   return 0;
 }

@@ -48,3 +48,17 @@ def test_the_library_drafts_like_the_oracle(k2):
         cap = int(rng.integers(1, 10))
         assert k2.spec_draft(seq, cap) == SP.spec_draft(seq, cap), (seq, cap)
     assert k2.spec_draft([], 8) == []
+
+
+def test_the_library_drafts_like_the_oracle_on_structured_sequences(k2):
+    # repeated units with sparse edits (long matches, overlapping and
+    # periodic occurrences, disagreeing continuations), up to 3000 ids
+    rng = np.random.default_rng(13)
+    for case in range(300):
+        unit = rng.integers(0, int(rng.integers(2, 40)), size=int(rng.integers(1, 24))).tolist()
+        T = int(rng.integers(4, 3000 if case % 10 == 0 else 200))
+        seq = (unit * (T // len(unit) + 1))[:T]
+        for _ in range(int(rng.integers(0, 6))):
+            seq[int(rng.integers(0, T))] = int(rng.integers(0, 50))
+        cap = int(rng.integers(1, 10))
+        assert k2.spec_draft(seq, cap) == SP.spec_draft(seq, cap), (case, cap)
