@@ -260,6 +260,11 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
     __syncthreads();
     if (last_sh) {
       __threadfence();
+      // every CTA raised its guard bits before it counted itself, so the
+      // last one sees them all; a timed-out CTA's partial maximum covers only
+      // the rows that arrived, so no token comes out of such a launch
+      const unsigned g = __ldcg(a.guard);
+      const bool timed = (g & GUARD_TIMEOUT) != 0u;
       BestPair b{-INFINITY, 0x7fffffff};
       for (int i = tid; i < G; i += kGemvThreads) b = better(b, BestPair{__ldcg(a.part_val + i), __ldcg(a.part_idx + i)});
       b = warp_best(b);
@@ -268,12 +273,18 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
       if (tid == 0) {
         BestPair f = best_sh[0];
         for (int w = 1; w < kGemvThreads / 32; ++w) f = better(f, best_sh[w]);
+        bool nan = (g & GUARD_NAN) != 0u;
         if (f.i == 0x7fffffff) {  // every logit was NaN
           atomicOr(a.guard, GUARD_NAN);
           f.i = 0;
+          nan = true;
         }
-        *a.next_token = f.i;
-        if (a.advance) a.seq_len[a.seq] += 1;
+        if (a.fail_token) {
+          *a.next_token = (nan || timed) ? -1 : f.i;
+        } else if (!timed) {
+          *a.next_token = f.i;
+          if (a.advance) a.seq_len[a.seq] += 1;
+        }
         *a.counter = 0u;
       }
     }

@@ -355,6 +355,9 @@ __global__ void __launch_bounds__(kPackedThreads, 1) packed_gemv_kernel(const Pa
     __syncthreads();
     if (last_sh) {
       __threadfence();
+      // a timed-out CTA's partial maximum covers only the rows that arrived:
+      // such a launch writes no token and leaves the sequence where it was
+      const bool timed = (__ldcg(a.guard) & GUARD_TIMEOUT) != 0u;
       Best b{-INFINITY, 0x7fffffff};
       for (int i = tid; i < G; i += kPackedThreads) b = better(b, Best{__ldcg(a.part_val + i), __ldcg(a.part_idx + i)});
       b = warp_best(b);
@@ -367,8 +370,10 @@ __global__ void __launch_bounds__(kPackedThreads, 1) packed_gemv_kernel(const Pa
           atomicOr(a.guard, GUARD_NAN);
           f.i = 0;
         }
-        *a.next_token = f.i;
-        if (a.advance) a.seq_len[a.seq] += 1;
+        if (!timed) {
+          *a.next_token = f.i;
+          if (a.advance) a.seq_len[a.seq] += 1;
+        }
         *a.counter = 0u;
       }
     }

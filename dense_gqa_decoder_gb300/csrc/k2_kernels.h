@@ -57,6 +57,7 @@ struct GemvArgs {
   int* next_token;    // where the token goes
   int advance;        // last CTA does seq_len[seq] += 1
   unsigned* guard;
+  int fail_token;     // nonzero: a NaN logit or a timed-out wait makes the token -1
 };
 constexpr int kGemvKcMax = 10;
 

@@ -13,7 +13,12 @@
 // size that every GPU loading this library keeps until the process exits.
 // All calls share it, so calls whose kernels overlap on the GPU (two streams,
 // or two host threads) race on it; serialise them.  Each call clears the
-// counter it relies on before its kernel runs.
+// counter and the guard bits it relies on before its kernel runs.
+//
+// A caller without a context has no k2_sync_status to ask, so a call whose
+// logits hold a NaN, or whose kernel gave up on a bounded wait, writes -1 as
+// its token instead of an index; every other call writes the first index of
+// the maximum logit.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -30,7 +35,7 @@ struct HeadScratch {
   float val[kMaxCtas];  // per-CTA best logit
   int idx[kMaxCtas];    // per-CTA index of that logit
   unsigned counter;     // CTAs finished; the kernel's last CTA resets it to 0
-  unsigned guard;       // device guard bits (NaN logits) of the last call
+  unsigned guard;       // device guard bits (NaN logits, a wait that ran out) of this call
 };
 
 static __device__ __align__(256) unsigned char g_head_scratch[sizeof(HeadScratch)];
@@ -90,6 +95,7 @@ extern "C" k2_status k2_greedy_head_noalloc(const k2_config* cfg, const void* lm
   a.next_token = d_token;
   a.advance = 0;  // no sequence state is touched
   a.guard = &scr->guard;
+  a.fail_token = 1;  // the caller has no status word to read: a failed call says so in d_token (-1)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the counter and guard must start at zero (a call cut short could have left them set)
   if (cudaMemsetAsync(&scr->counter, 0, 2 * sizeof(unsigned), s) != cudaSuccess) return K2_ERR_CUDA;

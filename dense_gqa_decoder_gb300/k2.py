@@ -290,7 +290,29 @@ class Context:
 
 
 def greedy_head_noalloc(cfg: Config, lm_head, final_norm, x, logits, token, stream=None) -> int:
-    """k2_greedy_head_noalloc: returns the k2 status (no context, no workspace)."""
+    """k2_greedy_head_noalloc: returns the k2 status (no context, no workspace).
+
+    The tensors are checked here, since the C call reads raw pointers: x
+    float32 [hidden], logits float32 [vocab] or None, token int32 [1],
+    lm_head [vocab, hidden] and final_norm [hidden] in the config's weight
+    dtype, all contiguous CUDA tensors.  A token of -1 after the call means a
+    NaN logit or a bounded wait that ran out on the device.  ``x = None``
+    passes a null pointer through (the call refuses it)."""
+    wdt = {K2_F32: torch.float32, K2_BF16: torch.bfloat16}.get(cfg.weight_dtype)
+
+    def want(t, name, dtype, numel):
+        if t is None:
+            return
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == dtype and t.numel() == numel):
+            raise ValueError(f"greedy_head_noalloc: {name} must be a contiguous CUDA {dtype} tensor "
+                             f"of {numel} elements, got {t.dtype} {tuple(t.shape)} on {t.device}")
+    if wdt is not None:
+        want(lm_head, "lm_head", wdt, cfg.vocab * cfg.hidden)
+        want(final_norm, "final_norm", wdt, cfg.hidden)
+    if cfg.hidden > 0 and cfg.vocab > 0:
+        want(x, "x", torch.float32, cfg.hidden)
+        want(logits, "logits", torch.float32, cfg.vocab)
+    want(token, "token", torch.int32, 1)
     return LIB.k2_greedy_head_noalloc(C.byref(cfg), _ptr(lm_head), _ptr(final_norm), _ptr(x), _ptr(logits),
                                       _ptr(token), _stream(stream))
 

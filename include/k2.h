@@ -264,13 +264,15 @@ k2_status k2_philox(uint32_t first, int32_t n, uint32_t c1, uint32_t c2, uint32_
  * itself and verify them in one batched pass; only the prefix the model
  * itself would have emitted greedily is accepted.
  *
- * Drafting (the rule of the page's spec_draft): for n = 4, then 3, find the
- * two latest earlier occurrences of the last n ids of h_tokens; propose the
- * ids that followed the latest one (at most max_draft, at most 8, and not
- * past the end of h_tokens); with a second occurrence, stop where the two
- * continuations disagree or where the second one reaches the latest.  The
- * first n giving a non-empty draft wins.  Returns the number of drafted ids
- * written to h_out (host memory; 0 = no draft).  No context, no GPU. */
+ * Drafting (the rule stated for the page's spec_draft): for n = 4, then 3,
+ * take the two latest earlier occurrences of the last n ids of h_tokens;
+ * propose the ids that followed the latest one (at most max_draft, at most
+ * 8, and not past the end of h_tokens); with a second occurrence, only as
+ * far as the two continuations agree and the older one stays short of the
+ * latest occurrence.  The first n giving a non-empty draft wins.  All
+ * occurrences come from one linear pass (the Z-algorithm over the history
+ * read backwards).  Returns the number of drafted ids written to h_out (host
+ * memory; 0 = no draft).  No context, no GPU. */
 int32_t k2_spec_draft(const int32_t* h_tokens, int32_t n_tokens, int32_t max_draft, int32_t* h_out);
 
 /* One speculative step of sequence seq.  h_tokens [n_tokens] (host) holds
@@ -429,9 +431,19 @@ k2_status k2_quantize_q4(const void* d_src, int32_t rows, int32_t cols, int8_t* 
  * K2_NOALLOC_MAX_CTAS entries that every device loading the library holds
  * until exit; K2_ERR_WORKSPACE if the launch would need more CTAs than that.
  * The first call on a device looks up that array's address and sets kernel
- * attributes; make it before any stream capture.  All calls share the array
- * and each clears its counter before launching, so calls that overlap on the
- * GPU race: serialise them (one stream, one thread). */
+ * attributes; make it before any stream capture.  That look-up is kept for
+ * the life of the process: do not call this across a cudaDeviceReset of the
+ * device.  All calls share the array and each clears its counter and guard
+ * bits before launching, so calls that overlap on the GPU race: serialise
+ * them (one stream, one thread).
+ *
+ * Failure on the device: with no context there is no k2_sync_status to read,
+ * so the token itself carries it.  If any logit is NaN, or a bounded wait in
+ * the kernel ran out, *d_token is written as -1 (d_logits, when given, still
+ * holds the logits computed); otherwise it is the first index of the largest
+ * logit.  The return value covers only what the host can check (K2_OK,
+ * K2_ERR_ARG, K2_ERR_SHAPE, K2_ERR_UNSUPPORTED, K2_ERR_WORKSPACE,
+ * K2_ERR_CUDA). */
 #define K2_NOALLOC_MAX_CTAS 1024
 k2_status k2_greedy_head_noalloc(const k2_config* cfg, const void* lm_head, const void* final_norm, const float* d_x,
                                  float* d_logits, int32_t* d_token, void* stream);
