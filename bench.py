@@ -69,6 +69,9 @@ def parse():
     p.add_argument("--batch", type=int, default=1,
                    help="> 1: aggregate decode throughput of that many sequences per step (each prefilled "
                         "with --ctx random tokens); the default 1 is the batch-1 metric")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the sub-records of the int8-KV context-8192 and batch-16 context-8192 workloads "
+                        "that the default run adds to its line")
     return p.parse_args()
 
 
@@ -226,6 +229,39 @@ def job_throughput(world: int, units_per_rank: float, seconds: float) -> float:
     return world * units_per_rank / seconds
 
 
+def step_stats(per_step_ms) -> dict:
+    """Median and 90th percentile (nearest rank) of the per-step times."""
+    v = sorted(per_step_ms)
+    if not v:
+        return {"p50_ms": None, "p90_ms": None}
+    k = max(0, -(-9 * len(v) // 10) - 1)
+    return {"p50_ms": statistics.median(v), "p90_ms": v[k]}
+
+
+def timed_decode(ctx, tok, batch, steps, stream, local, pg):
+    """`steps` decode steps (CUDA graph replays) on `stream`, an event before
+    the first and after every step, between a barrier and a synchronize on
+    both sides, with the SM clocks sampled meanwhile.  Returns (ms of all
+    steps, max over ranks; per-step ms on this rank; clock summary)."""
+    import torch
+    clocks = ClockSampler(local)
+    clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        ctx.decode_step(tok, batch, tok, stream=stream)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clk = clocks.stop()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return max_over_ranks(pg, ev[0].elapsed_time(ev[-1])), per, clk
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle legs (the oracle as it stands, on this host's cores)
 # ---------------------------------------------------------------------------
@@ -348,7 +384,8 @@ def run_ours(args, world, rank, local, pg):
     budget = args.ctx + args.warmup + args.steps + args.profile_steps + args.e2e_steps + 16
     cfg = k2.make_config(s, max_context=budget, max_batch=1, kv_dtype=args.kv,
                          weights=None if args.weights == "bf16" else args.weights)
-    ctx = k2.Context(cfg, random_device_weights(s, seed=1234 + rank))
+    wdev = random_device_weights(s, seed=1234 + rank)
+    ctx = k2.Context(cfg, wdev)
     stream = torch.cuda.Stream()
     sampled = args.temperature > 0
     if sampled:
@@ -377,23 +414,8 @@ def run_ours(args, world, rank, local, pg):
     if ctx.sync_status(stream) != k2.K2_OK:
         raise RuntimeError("device guard after warm-up: " + ctx.last_error())
 
-    clocks = ClockSampler(local)
-    clocks.start()
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     ctx_start = ctx.kv_view(0, 0)[4]
-    e0.record(stream)
-    for _ in range(args.steps):
-        ctx.decode_step(tok, 1, tok, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if pg:
-        pg.barrier()
-    clk = clocks.stop()
-    ms = max_over_ranks(pg, e0.elapsed_time(e1))
+    ms, per_step, clk = timed_decode(ctx, tok, 1, args.steps, stream, local, pg)
     if ctx.sync_status(stream) != k2.K2_OK:
         raise RuntimeError("device guard after the timed steps: " + ctx.last_error())
     ms_per_step = ms / args.steps
@@ -473,7 +495,8 @@ def run_ours(args, world, rank, local, pg):
                    "parallelism": f"replicas x{world}"},
         "hbm": {"bytes_per_step": by["total"], "achieved_gbs": by["total"] / (ms_per_step * 1e-3) / 1e9,
                 "peak_gbs": peak, "frac": by["total"] / (ms_per_step * 1e-3) / 1e9 / peak,
-                "frac_of_8tbs_nominal": by["total"] / (ms_per_step * 1e-3) / 1e9 / 7900.0},
+                "frac_of_8tbs_nominal": by["total"] / (ms_per_step * 1e-3) / 1e9 / 8000.0},
+        "step_ms": step_stats(per_step),
         "roofline": {"bound": "hbm", "kernel": k_desc,
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": peak_src, "algorithmic_bytes": k_bytes,
@@ -495,8 +518,102 @@ def run_ours(args, world, rank, local, pg):
         "clocks": clk,
         "cpu_baseline": cpu,
     }
+    default = (args.kv == "f16" and args.ctx == CTX and args.weights == "bf16" and not sampled and not args.layers)
+    if default and not args.no_configs:
+        # the two larger workloads, each on a fresh context over the same weights
+        del ctx
+        torch.cuda.empty_cache()
+        line["configs"] = {
+            "int8_kv_ctx8192": sub_int8_ctx8192(args, s, wdev, world, local, pg),
+            "batch16_ctx8192": sub_batch16_ctx8192(args, s, wdev, world, local, pg),
+        }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def sub_int8_ctx8192(args, s, wdev, world, local, pg):
+    """The int8-KV workload: allocation 32768 positions, prefill of 8192
+    random ids, then 512 greedy decode steps (after the warm-up), batch 1."""
+    import torch
+
+    import k2_inputs as ki
+    from dense_gqa_decoder_gb300 import k2
+    T, steps = 8192, 512
+    ctx = k2.Context(k2.make_config(s, max_context=32768, max_batch=1, kv_dtype="i8"), wdev)
+    stream = torch.cuda.Stream()
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    with torch.cuda.stream(stream):
+        ctx.prefill(0, torch.from_numpy(ki.prompt_ids(s.vocab, T, seed=1)).cuda(), tok, stream=stream)
+    p1.record(stream)
+    stream.synchronize()
+    ctx.set_option(k2.K2_OPT_GRAPH, 1)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            ctx.decode_step(tok, 1, tok, stream=stream)
+    stream.synchronize()
+    c0 = ctx.kv_view(0, 0)[4]
+    ms, per, clk = timed_decode(ctx, tok, 1, steps, stream, local, pg)
+    if ctx.sync_status(stream) != k2.K2_OK:
+        raise RuntimeError("device guard (int8 KV workload): " + ctx.last_error())
+    by = algorithmic_bytes(s, int(round(c0 + (steps - 1) / 2 + 1)), "i8")
+    peak, peak_src = measured_peaks()
+    mps = ms / steps
+    achieved = by["step_launch"] / (mps * 1e-3) / 1e9
+    del ctx
+    torch.cuda.empty_cache()
+    return {"workload": f"k2-horizon-3.7b-shape greedy decode, batch 1, int8 KV (allocation 32768), prefill {T} "
+                        f"random ids, then {steps} timed steps (context {c0} -> {c0 + steps})",
+            "value": job_throughput(world, steps, ms / 1e3), "unit": "tok/s", "ms_per_step": mps,
+            "step_ms": step_stats(per), "prefill_ms": p0.elapsed_time(p1),
+            "roofline": {"bound": "hbm", "kernel": "mega_decode_kernel (whole decode step, graph replay)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": None, "peak_source": peak_src, "algorithmic_bytes": by["step_launch"]},
+            "clocks": clk}
+
+
+def sub_batch16_ctx8192(args, s, wdev, world, local, pg):
+    """The batch-16 workload: 16 independent sequences, each prefilled with
+    8192 random ids (distinct seeds), then 128 greedy decode steps of all 16
+    (after the warm-up)."""
+    import torch
+
+    import k2_inputs as ki
+    from dense_gqa_decoder_gb300 import k2
+    B, T, steps = 16, 8192, 128
+    ctx = k2.Context(k2.make_config(s, max_context=T + args.warmup + steps + 16, max_batch=B, kv_dtype="f16"), wdev)
+    stream = torch.cuda.Stream()
+    tok = torch.zeros(B, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        for b in range(B):
+            ctx.prefill(b, torch.from_numpy(ki.prompt_ids(s.vocab, T, seed=1 + b)).cuda(), tok[b:b + 1],
+                        stream=stream)
+    ctx.set_option(k2.K2_OPT_GRAPH, 1)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            ctx.decode_step(tok, B, tok, stream=stream)
+    stream.synchronize()
+    c0 = ctx.kv_view(0, 0)[4]
+    ms, per, clk = timed_decode(ctx, tok, B, steps, stream, local, pg)
+    if ctx.sync_status(stream) != k2.K2_OK:
+        raise RuntimeError("device guard (batch-16 workload): " + ctx.last_error())
+    one = algorithmic_bytes(s, 1, "f16")
+    step_bytes = one["weights"] + B * one["kv"] * (c0 + (steps - 1) / 2 + 1)
+    peak, peak_src = measured_peaks()
+    mps = ms / steps
+    achieved = step_bytes / (mps * 1e-3) / 1e9
+    del ctx
+    torch.cuda.empty_cache()
+    return {"workload": f"k2-horizon-3.7b-shape greedy decode, {B} sequences, fp16 KV, each prefilled with {T} "
+                        f"random ids, then {steps} timed steps (context {c0} -> {c0 + steps})",
+            "value": job_throughput(world, B * steps, ms / 1e3), "unit": "tok/s", "ms_per_step": mps,
+            "step_ms": step_stats(per),
+            "roofline": {"bound": "hbm", "kernel": "batched decode step (tensor-core GEMMs with N = 16, decode "
+                                                   "attention, row kernels; graph replay)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": None, "peak_source": peak_src, "algorithmic_bytes": step_bytes},
+            "clocks": clk}
 
 
 def run_speculative(args, world, rank, local, pg):
@@ -643,22 +760,7 @@ def run_batched(args, world, rank, local, pg):
         for _ in range(args.warmup):
             ctx.decode_step(tok, B, tok, stream=stream)
     stream.synchronize()
-    clocks = ClockSampler(local)
-    clocks.start()
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        ctx.decode_step(tok, B, tok, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if pg:
-        pg.barrier()
-    clk = clocks.stop()
-    ms = max_over_ranks(pg, e0.elapsed_time(e1))
+    ms, per, clk = timed_decode(ctx, tok, B, args.steps, stream, local, pg)
     if ctx.sync_status(stream) != k2.K2_OK:
         raise RuntimeError("device guard after the timed steps: " + ctx.last_error())
     ms_per_step = ms / args.steps
@@ -680,6 +782,7 @@ def run_batched(args, world, rank, local, pg):
                                                "row kernels)", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
                      "algorithmic_bytes": step_bytes},
+        "step_ms": step_stats(per),
         "clocks": clk,
     }
     if rank == 0:

@@ -272,6 +272,9 @@ struct k2_ctx {
   std::array<uint8_t, kTcMapBytes> tb_xh{}, tb_xl{}, tb_oh{}, tb_ol{}, tb_ah{}, tb_al{};
   std::map<std::tuple<int, const void*, const void*, const void*, void*>, cudaGraphExec_t> graphs;
   std::map<std::tuple<int, int, void*>, cudaGraphExec_t> spec_graphs;  // (seq, ids verified (0: a plain step), stream)
+  int spec_rows = 0;  // rows of logits the last speculative step left in the verification buffer
+  unsigned long long poll_limit_ns = 1000000000ull;  // persistent step: waits for other CTAs' words (1 s)
+  int stall_phase = -1;                              // persistent step: test option K2_OPT_STALL_PHASE
   std::string err;
   // profiling: event pairs around the kernels of one step
   std::vector<cudaEvent_t> pev;
@@ -463,6 +466,8 @@ void enqueue_token(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in
     m.x_ext = x_in;
     m.x_out = x_in ? x_in : c->resid + static_cast<size_t>(seq) * c->s.H;
     m.head = head ? 1 : 0;
+    m.poll_limit_ns = c->poll_limit_ns;
+    m.stall_phase = c->stall_phase;
     const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
     cudaStream_t st = ln.s;
     ln.run(K2_K_STEP, [&] { return launch_mega(m, c->s.wf, c->s.d, c->s.rep, kvdt, c->mega_grid, st); });
@@ -1437,6 +1442,13 @@ k2_status k2_hidden_view(k2_ctx* c, int32_t b, float** d_x) {
   return K2_OK;
 }
 
+k2_status k2_spec_logits_view(k2_ctx* c, float** d_logits, int32_t* rows) {
+  if (!c || !d_logits || !rows) return K2_ERR_ARG;
+  *d_logits = c->lay.pchunk > 0 ? reinterpret_cast<float*>(c->ws + c->lay.vlog) : nullptr;
+  *rows = c->spec_rows;
+  return K2_OK;
+}
+
 k2_status k2_sync_status(k2_ctx* c, void* stream) {
   if (!c) return K2_ERR_ARG;
   unsigned g = 0;
@@ -1458,7 +1470,16 @@ k2_status k2_clear_status(k2_ctx* c, void* stream) {
   // a step cut short by a timeout may have left the grid barrier half counted
   // the finished-CTA counter (not the epoch: tags must stay fresh)
   if (!e) e = cudaMemsetAsync(c->ws + c->lay.msync, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream));
+  // a step that failed on the device left its sequences' lengths where they
+  // were, while the host copy advanced when the step was enqueued: take the
+  // device's word for it
+  std::vector<int> dlen(c->s.B, 0);
+  if (!e)
+    e = cudaMemcpyAsync(dlen.data(), c->seq_len, sizeof(int) * c->s.B, cudaMemcpyDeviceToHost,
+                        static_cast<cudaStream_t>(stream));
+  if (!e) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e) return c->cuda_fail(e, "clear_status");
+  for (int b = 0; b < c->s.B; ++b) c->len[b] = dlen[b];
   return K2_OK;
 }
 
@@ -1478,6 +1499,16 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
       if (value < 0 || value > kAttnMaxCluster)
         return c->fail(K2_ERR_ARG, "splits %lld outside [0, %d]", (long long)value, kAttnMaxCluster);
       c->force_splits = static_cast<int>(value);
+      break;
+    case K2_OPT_WAIT_LIMIT_US:
+      if (value < 1 || value > 1000000)
+        return c->fail(K2_ERR_ARG, "wait limit %lld us outside [1, 1000000]", (long long)value);
+      c->poll_limit_ns = static_cast<unsigned long long>(value) * 1000ull;
+      break;
+    case K2_OPT_STALL_PHASE:
+      if (value < -1 || value == 0 || value > 5LL * c->s.L)
+        return c->fail(K2_ERR_ARG, "stall phase %lld outside -1 or [1, %d]", (long long)value, 5 * c->s.L);
+      c->stall_phase = static_cast<int>(value);
       break;
     default: return c->fail(K2_ERR_ARG, "unknown option %d", option);
   }
@@ -1776,17 +1807,22 @@ k2_status k2_decode_speculative(k2_ctx* c, int32_t seq, const int32_t* h_tokens,
     }
     return cudaGraphLaunch(it->second, st);
   };
+  // the logits of every verified position stay in the verification buffer
+  // (k2_spec_logits_view); a plain step leaves its one row there too
+  float* vlog = c->lay.pchunk > 0 ? reinterpret_cast<float*>(c->ws + c->lay.vlog) : nullptr;
+  c->spec_rows = 0;
   if (nd == 0) {  // no draft: an ordinary decode step of this sequence
     if (!e)
       e = run(0, [&] {
         Launcher ln{c, st, false};
-        enqueue_token(c, ln, seq, d_ids, nullptr, d_arg, nullptr, true);
+        enqueue_token(c, ln, seq, d_ids, nullptr, d_arg, vlog, true);
         return ln.err;
       });
     if (!e) e = cudaMemcpyAsync(out, d_arg, sizeof(int), cudaMemcpyDeviceToHost, st);
     if (!e) e = cudaStreamSynchronize(st);
     if (e) return c->cuda_fail(e, "speculative step");
     c->len[seq] += 1;
+    c->spec_rows = vlog ? 1 : 0;
   } else {
     if (!e) e = run(nd + 1, [&] { return verify_block(c, seq, d_ids, nd + 1, d_arg, st); });
     if (!e) e = cudaMemcpyAsync(out, d_arg, sizeof(int) * (nd + 1), cudaMemcpyDeviceToHost, st);
@@ -1801,6 +1837,7 @@ k2_status k2_decode_speculative(k2_ctx* c, int32_t seq, const int32_t* h_tokens,
     if (!e) e = cudaStreamSynchronize(st);
     if (e) return c->cuda_fail(e, "speculative length");
     c->len[seq] = len;
+    c->spec_rows = nd + 1;
   }
   std::copy(out, out + accepted + 1, h_out);
   *n_out = accepted + 1;

@@ -289,6 +289,12 @@ struct MegaArgs {
   unsigned* end_count;
   unsigned* epoch;   // launches so far (tags are derived from it)
   unsigned* guard;
+  // how long a wait for another CTA's tagged words may last (waits for this
+  // CTA's own bulk copies keep kWaitLimitNs: a copy must land before its CTA exits)
+  unsigned long long poll_limit_ns;
+  // >= 0: phase stall_phase waits for a tag that no phase writes, so its
+  // waits run out (tests of the timeout path); -1 otherwise
+  int stall_phase;
 };
 constexpr int kMegaThreads = 256;
 constexpr int kMegaSlots = 2;                 // ring slots per warp

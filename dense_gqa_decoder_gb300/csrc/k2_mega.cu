@@ -114,11 +114,13 @@ __device__ __forceinline__ float tag_val(u64 w) { return __uint_as_float(static_
 
 // Bounded retry loop: false (and GUARD_TIMEOUT) once the wait has run out.
 struct Patience {
+  uint64_t limit;
   uint64_t t0 = 0;
+  __device__ __forceinline__ explicit Patience(uint64_t limit_ns) : limit(limit_ns) {}
   __device__ __forceinline__ bool more(unsigned* guard) {
     const uint64_t t = globaltimer();
     if (t0 == 0) t0 = t;
-    if (t - t0 > kWaitLimitNs) {
+    if (t - t0 > limit) {
       atomicOr(guard, GUARD_TIMEOUT);
       return false;
     }
@@ -128,7 +130,7 @@ struct Patience {
 };
 
 // x[e .. e+3] for e = tid * 4 + i * MT * 4 (i < PX, e < K) from tagged words.
-__device__ bool poll_x(const u64* tv, int K, uint32_t tag, float4* xq, unsigned* guard) {
+__device__ bool poll_x(const u64* tv, int K, uint32_t tag, float4* xq, unsigned* guard, uint64_t limit_ns) {
   const int tid = threadIdx.x;
   unsigned pend = 0;
 #pragma unroll
@@ -136,7 +138,7 @@ __device__ bool poll_x(const u64* tv, int K, uint32_t tag, float4* xq, unsigned*
     xq[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid * 4 + i * MT * 4 < K) pend |= 1u << i;
   }
-  Patience wait;
+  Patience wait(limit_ns);
   while (pend) {
     u64 w[PX][4];
 #pragma unroll
@@ -496,7 +498,7 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
       side = rsd0f ? __ldcg(rsd0f + 2 * r.p0 + tid) : load1(rsd0w, 2 * r.p0 + tid);
     float4 xq[PX];
     if (xt) {
-      bad = !poll_x(xt, K, tag_in, xq, a.guard);
+      bad = !poll_x(xt, K, tag_in, xq, a.guard, a.poll_limit_ns);
     } else {
 #pragma unroll
       for (int i = 0; i < PX; ++i) {
@@ -803,7 +805,7 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
         }
       }
     }
-    Patience wait;
+    Patience wait(a.poll_limit_ns);
     bool bad = false;
     while (pend) {
       u64 w[NQ4];
@@ -1055,7 +1057,7 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
         }
       }
     }
-    Patience wait;
+    Patience wait(a.poll_limit_ns);
     bool bad = false;
     while (pend) {
       u64 w[NPW];
@@ -1165,7 +1167,9 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
   bool ok = true;
   for (int q = 0; q <= lastq && ok; ++q) {
     const int l = q / kPhases, j = q - (q / kPhases) * kPhases;
-    const uint32_t tag_in = tagbase | static_cast<uint32_t>(q - 1), tag_out = tagbase | static_cast<uint32_t>(q);
+    uint32_t tag_in = tagbase | static_cast<uint32_t>(q - 1);
+    const uint32_t tag_out = tagbase | static_cast<uint32_t>(q);
+    if (q == a.stall_phase) tag_in = tagbase | ((1u << kMegaTagShift) - 1u);  // no phase has this number
     if (l < a.n_layers && j == PH_ATTN) {
       ok = a_phase<WT, D, REP>(a, l, pos, tag_in, tag_out, smem, sh, st, consumed, cta, G, qkv_n);
       continue;

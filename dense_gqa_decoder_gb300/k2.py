@@ -18,7 +18,8 @@ K2_OK, K2_ERR_ARG, K2_ERR_SHAPE, K2_ERR_UNSUPPORTED, K2_ERR_TOKEN_RANGE, K2_ERR_
     K2_ERR_WORKSPACE, K2_ERR_CUDA, K2_ERR_DEVICE_GUARD, K2_ERR_STATE = range(10)
 K2_STATE_HEADER_BYTES = 96
 K2_F32, K2_BF16, K2_F16, K2_I8, K2_F8, K2_Q4 = range(6)
-K2_OPT_PDL, K2_OPT_GRAPH, K2_OPT_ATTN_SPLITS, K2_OPT_PERSISTENT, K2_OPT_TC_PREFILL, K2_OPT_TC_DECODE = range(6)
+(K2_OPT_PDL, K2_OPT_GRAPH, K2_OPT_ATTN_SPLITS, K2_OPT_PERSISTENT, K2_OPT_TC_PREFILL, K2_OPT_TC_DECODE,
+ K2_OPT_WAIT_LIMIT_US, K2_OPT_STALL_PHASE) = range(8)
 KERNEL_CLASSES = ("embed", "qkv", "attn", "o_proj", "gate_up", "down", "lm_head", "step", "sample")
 DTYPES = {"f32": K2_F32, "bf16": K2_BF16, "f16": K2_F16, "i8": K2_I8, "f8": K2_F8, "q4": K2_Q4}
 
@@ -96,6 +97,7 @@ def _load():
         "k2_quantize_fp8": (C.c_int, [vp, i32, i32, vp, vp, vp]),
         "k2_quantize_q4": (C.c_int, [vp, i32, i32, vp, vp, vp]),
         "k2_decode_speculative": (C.c_int, [vp, i32, vp, i32, i32, vp, C.POINTER(i32), vp]),
+        "k2_spec_logits_view": (C.c_int, [vp, C.POINTER(vp), C.POINTER(i32)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -110,7 +112,7 @@ EXPORTED = ("k2_workspace_bytes", "k2_init_weights", "k2_free", "k2_last_error",
             "k2_sync_status", "k2_clear_status", "k2_set_option", "k2_profile_decode", "k2_greedy_head_noalloc",
             "k2_kv_state_bytes", "k2_kv_save", "k2_kv_peek", "k2_kv_load", "k2_set_sampling", "k2_sample_logits",
             "k2_philox", "k2_spec_draft", "k2_decode_speculative", "k2_quantize_fp8",
-            "k2_quantize_q4")
+            "k2_quantize_q4", "k2_spec_logits_view")
 
 
 def _ptr(t):
@@ -214,6 +216,15 @@ class Context:
         p = C.c_void_p()
         self._check(LIB.k2_hidden_view(self.ctx, b, C.byref(p)))
         return p.value
+
+    def spec_logits(self):
+        """k2_spec_logits_view: the logits of the last speculative step as a
+        [rows, vocab] float32 CUDA tensor view (not a copy)."""
+        p, rows = C.c_void_p(), C.c_int32(0)
+        self._check(LIB.k2_spec_logits_view(self.ctx, C.byref(p), C.byref(rows)))
+        if rows.value == 0:
+            return torch.empty(0, self.cfg.vocab, dtype=torch.float32, device="cuda")
+        return device_view(p.value, rows.value * self.cfg.vocab, torch.float32).view(rows.value, self.cfg.vocab)
 
     def sync_status(self, stream=None):
         return LIB.k2_sync_status(self.ctx, _stream(stream))

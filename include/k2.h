@@ -293,6 +293,14 @@ int32_t k2_spec_draft(const int32_t* h_tokens, int32_t n_tokens, int32_t max_dra
 k2_status k2_decode_speculative(k2_ctx* ctx, int32_t seq, const int32_t* h_tokens, int32_t n_tokens,
                                 int32_t max_draft, int32_t* h_out, int32_t* n_out, void* stream);
 
+/* Test hook: the fp32 logits [*rows][vocab] (device memory owned by the
+ * context) of the last k2_decode_speculative call.  Row i holds the logits
+ * after the input and drafts 0..i-1, for every position the pass verified
+ * (the input and all drafts, accepted or not); a step without a draft leaves
+ * one row.  *rows = 0 (and *d_logits NULL) for models without a tensor-core
+ * path.  Valid until the next call on the context. */
+k2_status k2_spec_logits_view(k2_ctx* ctx, float** d_logits, int32_t* rows);
+
 /* ---- saved cache state ------------------------------------------------------
  *
  * A sequence's cache can be written to host memory and restored later, into
@@ -358,7 +366,9 @@ k2_status k2_hidden_view(k2_ctx* ctx, int32_t b, float** d_x);
  * K2_ERR_DEVICE_GUARD (with the reasons in k2_last_error) otherwise. */
 k2_status k2_sync_status(k2_ctx* ctx, void* stream);
 
-/* Clears the device guard word (enqueued on stream). */
+/* Clears the device guard word and re-reads every sequence's length from the
+ * device (a step that failed on the device did not advance its sequences);
+ * waits for `stream`. */
 k2_status k2_clear_status(k2_ctx* ctx, void* stream);
 
 typedef enum {
@@ -371,8 +381,17 @@ typedef enum {
                              shape allows; 0: always the chain of per-step kernels */
   K2_OPT_TC_PREFILL = 4,  /* 1 (default): bf16 and fp8 models prefill prompts of >= 8 tokens with
                              tensor-core GEMMs over blocks of up to 2048 tokens; 0: one decode step per token */
-  K2_OPT_TC_DECODE = 5    /* 1 (default): a bf16 decode step of batch >= 2 reads the weights once for
+  K2_OPT_TC_DECODE = 5,   /* 1 (default): a bf16 decode step of batch >= 2 reads the weights once for
                              all sequences (tensor-core GEMMs, N = batch); 0: one token at a time */
+  K2_OPT_WAIT_LIMIT_US = 6, /* how long (microseconds, 1 .. 1000000; default 1000000) a CTA of the
+                             persistent step waits for words another CTA publishes before it gives up:
+                             the step then ends early, raises the guard (K2_ERR_DEVICE_GUARD,
+                             "bounded-wait-timeout"), writes no token and does not advance the
+                             sequence.  Waits for the CTA's own copies keep their 1 s limit. */
+  K2_OPT_STALL_PHASE = 7  /* test of that path: phase p (1 .. 5 * n_layers; layer l's phases are
+                             5l + 0 QKV, 1 attention, 2 o_proj, 3 gate/up, 4 down, and 5 * n_layers
+                             is the lm_head) of the persistent step waits for words that no phase
+                             writes, so its waits run out; -1 (default) turns it off */
 } k2_option;
 k2_status k2_set_option(k2_ctx* ctx, int32_t option, int64_t value);
 

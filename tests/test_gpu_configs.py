@@ -1,0 +1,199 @@
+"""Parity at the head shape of the larger workloads, against the oracle.
+
+* Batch-16 decode (16 independent sequences, each with its own fp16 or int8
+  KV cache of up to 8192 N(0,1) rows): one decode step of one 3.7B-shape
+  layer (head_dim 128, 32 query heads over 8 KV heads) through the batched
+  path, the same launch configuration as the batch-16 x 8192 measurement
+  (tensor-core GEMMs over 16-token tiles, the decode attention kernel with
+  its key splits sized for 16 x 8 KV heads).  Every sequence is checked
+  against the oracle's single-layer step over the same stored rows.
+* int8 KV prefill of more than one 2048-token block at head_dim 128, after
+  rows already in the cache, against the oracle's full recompute.
+* Speculative decoding against the oracle: the emitted ids and the logits of
+  every verified position, teacher-forced over the emitted sequence
+  (kimi-k3-in-c k3_run.c, --spec: batched greedy verification accepts exactly
+  the prefix the model itself would have emitted).
+
+Bars (spec tolerances): bf16 weights with fp16 KV relative L2 <= 2e-2
+and argmax agreement >= 99 %, int8 KV relative L2 <= 5e-2; the kernels keep
+fp32 activations, so each test also holds the layer update to a far tighter
+bound that catches real bugs."""
+import numpy as np
+import pytest
+import torch
+
+import k2_inputs as ki
+from oracle import k2_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def k2():
+    from dense_gqa_decoder_gb300 import k2 as mod
+    return mod
+
+
+@pytest.fixture(scope="module")
+def mio():
+    from dense_gqa_decoder_gb300 import model_io
+    return model_io
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def fill_kv(k2, ctx, layer, seq, kv, vals, cap):
+    """Writes K and V rows vals [2, nkv, n, d] (float32) into (layer, seq) in
+    the cache format; returns the stored values as float64 [2, n, nkv, d]."""
+    nkv, n, d = vals.shape[1:]
+    kp, vp, ksp, vsp, _ = ctx.kv_view(layer, seq)
+    out = []
+    for ptr, sptr, arr in ((kp, ksp, vals[0]), (vp, vsp, vals[1])):
+        if kv == "f16":
+            k2.device_view(ptr, nkv * cap * d, torch.float16).view(nkv, cap, d)[:, :n].copy_(
+                torch.from_numpy(arr.astype(np.float16)))
+            out.append(arr.astype(np.float16).astype(np.float64))
+        else:
+            codes, scales = O.int8_quantize(arr)
+            k2.device_view(ptr, nkv * cap * d, torch.int8).view(nkv, cap, d)[:, :n].copy_(torch.from_numpy(codes))
+            k2.device_view(sptr, nkv * cap, torch.float16).view(nkv, cap)[:, :n].copy_(torch.from_numpy(scales))
+            out.append(O.int8_dequantize(codes, scales))
+    return np.stack(out).transpose(0, 2, 1, 3)
+
+
+def read_row(k2, ctx, layer, seq, kv, cap, s, row):
+    """Stored K and V of one cache row, dequantised: [2, nkv, d]."""
+    nkv, d = s.n_kv_heads, s.head_dim
+    kp, vp, ksp, vsp, _ = ctx.kv_view(layer, seq)
+    out = []
+    for ptr, sptr in ((kp, ksp), (vp, vsp)):
+        if kv == "f16":
+            out.append(k2.device_view(ptr, nkv * cap * d, torch.float16).view(nkv, cap, d)[:, row].float().cpu().numpy())
+        else:
+            c = k2.device_view(ptr, nkv * cap * d, torch.int8).view(nkv, cap, d)[:, row].float()
+            sc = k2.device_view(sptr, nkv * cap, torch.float16).view(nkv, cap)[:, row].float()
+            out.append((c * sc[:, None]).cpu().numpy())
+    return np.stack(out).astype(np.float64)
+
+
+# 16 distinct lengths up to 8192: full, one short, a ragged split, tiny, and
+# an empty cache (the new token attends to itself alone)
+LENS = [8192, 8191, 4097, 33, 0, 2048, 6000, 7777, 100, 4096, 8000, 3000, 511, 512, 5000, 1]
+
+
+@pytest.mark.parametrize("kv", ["f16", "i8"])
+def test_batch16_3p7b_layer_ctx8192_against_oracle(k2, mio, kv):
+    s = ki.K2_LAYER
+    B = len(LENS)
+    ctx, host = mio.build_context(s, max_context=max(LENS) + 1, max_batch=B, kv_dtype=kv, keep_host=True)
+    info = ctx.info()
+    assert info.tc_batched == 1  # the weights-once-per-step path
+    cap = info.kv_capacity
+    stored = []
+    for b, n in enumerate(LENS):
+        vals = ki.kv_fill_f16((2, s.n_kv_heads, n, s.head_dim), seed=200 + b).astype(np.float32)
+        stored.append(fill_kv(k2, ctx, 0, b, kv, vals, cap))
+        ctx.kv_set_len(b, n)
+    toks = ki.prompt_ids(s.vocab, B, seed=9)
+    d_tok = torch.tensor(toks, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
+    logits = torch.empty(B * s.vocab, dtype=torch.float32, device="cuda")
+    ctx.decode_step(d_tok, B, nxt, logits)
+    assert ctx.sync_status() == k2.K2_OK
+    lg = logits.view(B, s.vocab).cpu().numpy()
+    nx = nxt.cpu().numpy()
+    model = O.OracleModel(s, lambda nm, l: host[(nm, l)], kv)
+    E = host[("embed", -1)].astype(np.float64)
+    upd_tol = 1e-3 if kv == "f16" else 2e-2
+    for b, n in enumerate(LENS):
+        assert ctx.kv_view(0, b)[4] == n + 1
+        hid = k2.device_view(ctx.hidden_view(b), s.hidden, torch.float32).cpu().numpy().astype(np.float64)
+        cache = model.new_cache(n + 1)
+        cache.k[0][:n] = stored[b][0]
+        cache.v[0][:n] = stored[b][1]
+        cache.length = n
+        x, ref = model.run([toks[b]], cache)
+        e = E[toks[b]]
+        # the layer's update (hidden state minus the embedding row), the harder comparison
+        assert rel_l2(hid - e, x[0] - e) <= upd_tol, (b, n)
+        assert rel_l2(lg[b], ref[0]) <= (2e-2 if kv == "f16" else 5e-2), (b, n)
+        if kv == "f16":
+            assert nx[b] == O.argmax_first(ref[0]), (b, n)
+        # the appended row, read back from the cache
+        row = read_row(k2, ctx, 0, b, kv, cap, s, n)
+        want = np.stack([cache.k[0][n], cache.v[0][n]])
+        assert rel_l2(row, want) <= (1e-3 if kv == "f16" else 2e-2), (b, n)
+
+
+def test_int8_tc_prefill_3p7b_layer_two_blocks_against_oracle(k2, mio):
+    """int8 KV: 37 rows, then a 2100-token prompt (a 2048-token block and a
+    52-token block) through the tensor-core prefill at head_dim 128."""
+    s = ki.K2_LAYER
+    first = ki.prompt_ids(s.vocab, 37, seed=81)
+    second = ki.prompt_ids(s.vocab, 2100, seed=82)
+    ctx, host = mio.build_context(s, max_context=2200, kv_dtype="i8", keep_host=True)
+    assert ctx.info().tc_prefill == 1
+    nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ctx.prefill(0, torch.tensor(first, dtype=torch.int32, device="cuda"), nxt)
+    logits = torch.empty(s.vocab, dtype=torch.float32, device="cuda")
+    ctx.prefill(0, torch.tensor(second, dtype=torch.int32, device="cuda"), nxt, logits)
+    assert ctx.sync_status() == k2.K2_OK
+    n = len(first) + len(second)
+    assert ctx.kv_view(0, 0)[4] == n
+    model = O.OracleModel(s, lambda nm, l: host[(nm, l)], "i8")
+    cache = model.new_cache(n)
+    _, ref = model.run(np.concatenate([first, second]), cache)
+    lg = logits.cpu().numpy()
+    assert rel_l2(lg, ref[0]) <= 5e-2
+    assert rel_l2(lg, ref[0]) <= 1e-2  # fp32 activations: only int8 code flips remain
+    # every cached row (codes may differ by one step where a value sits on a
+    # rounding boundary: the two sides' fp32 / fp64 values differ by ~1e-6)
+    cap = ctx.info().kv_capacity
+    nkv, d = s.n_kv_heads, s.head_dim
+    kp, vp, ksp, vsp, _ = ctx.kv_view(0, 0)
+    for ptr, sptr, want in ((kp, ksp, cache.k[0][:n]), (vp, vsp, cache.v[0][:n])):
+        c = k2.device_view(ptr, nkv * cap * d, torch.int8).view(nkv, cap, d)[:, :n].float()
+        sc = k2.device_view(sptr, nkv * cap, torch.float16).view(nkv, cap)[:, :n].float()
+        got = (c * sc[..., None]).cpu().numpy().transpose(1, 0, 2)
+        assert rel_l2(got, want) <= 2e-2
+
+
+def repetitive_prompt(vocab, seed):
+    unit = list(ki.prompt_ids(vocab, 7, seed=seed))
+    return unit * 4 + unit[:3]
+
+
+@pytest.mark.parametrize("kv,tol,agree", [("f16", 2e-4, 0.99), ("i8", 5e-2, 0.9)])
+def test_speculative_matches_oracle_teacher_forced(k2, mio, kv, tol, agree):
+    s = ki.MEDIUM
+    prompt = repetitive_prompt(s.vocab, seed=40)
+    ctx, host = mio.build_context(s, max_context=160, kv_dtype=kv, gain_scale=0.1, keep_host=True)
+    nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ctx.prefill(0, torch.tensor(prompt, dtype=torch.int32, device="cuda"), nxt)
+    seq = list(prompt) + [int(nxt.item())]
+    rows = {}  # position of the last id seen -> logits after it
+    verified = 0
+    while len(seq) - len(prompt) < 48:
+        p0 = len(seq) - 1  # the input id's position (the cache length before the call)
+        got = ctx.decode_speculative(0, seq, 8)
+        lg = ctx.spec_logits().cpu().numpy()
+        assert lg.shape[0] >= len(got)
+        verified += lg.shape[0] > 1
+        for i in range(len(got)):  # rows of accepted positions: their prefix is the emitted one
+            rows[p0 + i] = lg[i]
+        seq += got
+    assert ctx.sync_status() == k2.K2_OK
+    assert verified > 0  # drafts were verified in blocks
+    model = O.OracleModel(s, lambda nm, l: host[(nm, l)], kv)
+    first = len(prompt)
+    am, ref, _ = model.teacher_forced(np.array(seq[:-1]), first)
+    pos = sorted(rows)
+    assert pos == list(range(first, len(seq) - 1))
+    got = np.stack([rows[p] for p in pos])
+    assert rel_l2(got, ref) <= tol
+    emitted = np.array(seq[first + 1:])  # the id after each position
+    assert np.mean(am == emitted) >= agree
