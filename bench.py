@@ -300,6 +300,20 @@ def oracle_decode_sample(n_layers_sample: int = 2, vocab_fraction: float = 1.0, 
     return per_token, desc, t_layers + t_head
 
 
+def host_cpu() -> dict:
+    """The host the oracle ran on: logical CPUs and the model name."""
+    name = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                name = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"nproc": os.cpu_count(), "model": name}
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -334,7 +348,7 @@ def run_reference(args, world, rank, pg):
         "impl": "reference",
         "config": {"workload": WORKLOAD, "batch": 1, "context": args.ctx},
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
-                         "sample": desc + "; each step is 1/36 of a token"},
+                         "sample": desc + "; each step is 1/36 of a token", "host": host_cpu()},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -469,7 +483,8 @@ def run_ours(args, world, rank, local, pg):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         per_token, desc, _ = oracle_decode_sample(2, 1.0, args.ctx)
-        cpu = {"value": 1.0 / per_token, "unit": "tok/s", "cores": blas_threads(), "kind": "oracle", "sample": desc}
+        cpu = {"value": 1.0 / per_token, "unit": "tok/s", "cores": blas_threads(), "kind": "oracle", "sample": desc,
+               "host": host_cpu()}
 
     T = args.ctx
     pf_linear = 2.0 * s.n_layers * ((s.n_heads + 2 * s.n_kv_heads) * s.head_dim * s.hidden

@@ -295,6 +295,12 @@ struct MegaArgs {
   // >= 0: phase stall_phase waits for a tag that no phase writes, so its
   // waits run out (tests of the timeout path); -1 otherwise
   int stall_phase;
+  // at the start of every phase whose kind j (0 QKV .. 4 down, 5 lm_head) has
+  // bit j set in l2_mask, each warp asks L2 for its next l2_ahead slots beyond
+  // those already in flight, so that they stream while the phase waits for
+  // its input
+  int l2_ahead;
+  int l2_mask;
 };
 constexpr int kMegaThreads = 256;
 constexpr int kMegaSlots = 2;                 // ring slots per warp

@@ -382,7 +382,40 @@ struct Stream {
       next_phase(a, cta, G, warp, pos, qkv_n);
     }
   }
+
+  // what issue_next would copy next, asked of L2 instead (on a copy of the
+  // stream: the real one is not advanced)
+  __device__ void prefetch_next(const MegaArgs& a, int cta, int G, int warp, int pos, int qkv_n) {
+    if (done) return;
+    if (attn) {
+      const int rows = min(TKM, k1 - j0);
+      const int crow = max(0, min(rows, pos - j0));
+      if (crow > 0) {
+        bulk_prefetch_l2(kb + static_cast<size_t>(j0) * ROWB, crow * ROWB);
+        bulk_prefetch_l2(vb + static_cast<size_t>(j0) * ROWB, crow * ROWB);
+      }
+      j0 += MW * TKM;
+    } else {
+      const int nu = min(SU, left);
+      bulk_prefetch_l2(src, static_cast<uint32_t>(nu) * UB);
+      src += static_cast<size_t>(nu) * UB;
+      left -= nu;
+    }
+    ++issued;
+    if (++k >= n) {
+      n = 0;
+      next_phase(a, cta, G, warp, pos, qkv_n);
+    }
+  }
 };
+
+// The next `count` slots of a warp's stream beyond those in flight, fetched
+// into L2 (called by the producer lane once per phase, off the hot loop).
+template <int UB, int D, typename KVT>
+__device__ __noinline__ void stream_prefetch(Stream<UB, D, KVT> s, const MegaArgs& a, int cta, int G, int warp,
+                                             int pos, int qkv_n, int count) {
+  for (int i = 0; i < count && !s.done; ++i) s.prefetch_next(a, cta, G, warp, pos, qkv_n);
+}
 
 // The norm gains reach shared memory by bulk copies issued one gain phase
 // ahead (a DRAM read under the full weight stream waits several
@@ -1170,6 +1203,8 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
     uint32_t tag_in = tagbase | static_cast<uint32_t>(q - 1);
     const uint32_t tag_out = tagbase | static_cast<uint32_t>(q);
     if (q == a.stall_phase) tag_in = tagbase | ((1u << kMegaTagShift) - 1u);  // no phase has this number
+    if (lane == 0 && a.l2_ahead > 0 && ((a.l2_mask >> (l < a.n_layers ? j : 5)) & 1))
+      stream_prefetch(st, a, cta, G, warp, pos, qkv_n, a.l2_ahead);
     if (l < a.n_layers && j == PH_ATTN) {
       ok = a_phase<WT, D, REP>(a, l, pos, tag_in, tag_out, smem, sh, st, consumed, cta, G, qkv_n);
       continue;

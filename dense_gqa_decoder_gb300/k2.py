@@ -19,7 +19,7 @@ K2_OK, K2_ERR_ARG, K2_ERR_SHAPE, K2_ERR_UNSUPPORTED, K2_ERR_TOKEN_RANGE, K2_ERR_
 K2_STATE_HEADER_BYTES = 96
 K2_F32, K2_BF16, K2_F16, K2_I8, K2_F8, K2_Q4 = range(6)
 (K2_OPT_PDL, K2_OPT_GRAPH, K2_OPT_ATTN_SPLITS, K2_OPT_PERSISTENT, K2_OPT_TC_PREFILL, K2_OPT_TC_DECODE,
- K2_OPT_WAIT_LIMIT_US, K2_OPT_STALL_PHASE) = range(8)
+ K2_OPT_WAIT_LIMIT_US, K2_OPT_STALL_PHASE, K2_OPT_L2_AHEAD, K2_OPT_L2_AHEAD_PHASES) = range(10)
 KERNEL_CLASSES = ("embed", "qkv", "attn", "o_proj", "gate_up", "down", "lm_head", "step", "sample")
 DTYPES = {"f32": K2_F32, "bf16": K2_BF16, "f16": K2_F16, "i8": K2_I8, "f8": K2_F8, "q4": K2_Q4}
 
@@ -304,19 +304,21 @@ def greedy_head_noalloc(cfg: Config, lm_head, final_norm, x, logits, token, stre
     """k2_greedy_head_noalloc: returns the k2 status (no context, no workspace).
 
     The tensors are checked here, since the C call reads raw pointers: x
-    float32 [hidden], logits float32 [vocab] or None, token int32 [1],
-    lm_head [vocab, hidden] and final_norm [hidden] in the config's weight
-    dtype, all contiguous CUDA tensors.  A token of -1 after the call means a
-    NaN logit or a bounded wait that ran out on the device.  ``x = None``
-    passes a null pointer through (the call refuses it)."""
+    float32, logits float32 or None, token int32, lm_head and final_norm in
+    the config's weight dtype, all contiguous CUDA tensors holding at least
+    the elements the call touches (x and final_norm: hidden, lm_head:
+    vocab * hidden, logits: vocab, token: 1); the call itself checks the
+    config's shape.  A token of -1 after the call means a NaN logit or a
+    bounded wait that ran out on the device.  ``x = None`` passes a null
+    pointer through (the call refuses it)."""
     wdt = {K2_F32: torch.float32, K2_BF16: torch.bfloat16}.get(cfg.weight_dtype)
 
     def want(t, name, dtype, numel):
         if t is None:
             return
-        if not (t.is_cuda and t.is_contiguous() and t.dtype == dtype and t.numel() == numel):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == dtype and t.numel() >= numel):
             raise ValueError(f"greedy_head_noalloc: {name} must be a contiguous CUDA {dtype} tensor "
-                             f"of {numel} elements, got {t.dtype} {tuple(t.shape)} on {t.device}")
+                             f"of at least {numel} elements, got {t.dtype} {tuple(t.shape)} on {t.device}")
     if wdt is not None:
         want(lm_head, "lm_head", wdt, cfg.vocab * cfg.hidden)
         want(final_norm, "final_norm", wdt, cfg.hidden)

@@ -392,6 +392,10 @@ typedef enum {
                              5l + 0 QKV, 1 attention, 2 o_proj, 3 gate/up, 4 down, and 5 * n_layers
                              is the lm_head) of the persistent step waits for words that no phase
                              writes, so its waits run out; -1 (default) turns it off */
+  K2_OPT_L2_AHEAD = 8,    /* persistent step: at the start of a phase, each warp fetches into L2 this many
+                             of its next weight / K-V slots beyond those in flight (0 .. 64) */
+  K2_OPT_L2_AHEAD_PHASES = 9 /* the phase kinds that do so, bit j for kind j (0 QKV, 1 attention, 2 o_proj,
+                             3 gate/up, 4 down, 5 lm_head) */
 } k2_option;
 k2_status k2_set_option(k2_ctx* ctx, int32_t option, int64_t value);
 
