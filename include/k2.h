@@ -388,7 +388,7 @@ typedef enum {
                              the step then ends early, raises the guard (K2_ERR_DEVICE_GUARD,
                              "bounded-wait-timeout"), writes no token and does not advance the
                              sequence.  Waits for the CTA's own copies keep their 1 s limit. */
-  K2_OPT_STALL_PHASE = 7  /* test of that path: phase p (1 .. 5 * n_layers; layer l's phases are
+  K2_OPT_STALL_PHASE = 7, /* test of that path: phase p (1 .. 5 * n_layers; layer l's phases are
                              5l + 0 QKV, 1 attention, 2 o_proj, 3 gate/up, 4 down, and 5 * n_layers
                              is the lm_head) of the persistent step waits for words that no phase
                              writes, so its waits run out; -1 (default) turns it off */
