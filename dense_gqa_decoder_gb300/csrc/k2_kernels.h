@@ -301,6 +301,10 @@ struct MegaArgs {
   // its input
   int l2_ahead;
   int l2_mask;
+  // measurement: when set, thread 0 of every CTA stamps %globaltimer (ns) at
+  // trace[(q * gridDim + cta) * 4 + k] for phase q: k = 0 phase start, 1 input
+  // ready, 2 weight / K-V slots consumed, 3 phase end
+  unsigned long long* trace;
 };
 constexpr int kMegaThreads = 256;
 constexpr int kMegaSlots = 2;                 // ring slots per warp

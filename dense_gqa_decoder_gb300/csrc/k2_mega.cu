@@ -129,6 +129,11 @@ struct Patience {
   }
 };
 
+__device__ __forceinline__ void trace_mark(const MegaArgs& a, int q, int k) {
+  if (a.trace != nullptr && threadIdx.x == 0)
+    a.trace[(static_cast<size_t>(q) * gridDim.x + blockIdx.x) * 4 + k] = globaltimer();
+}
+
 // x[e .. e+3] for e = tid * 4 + i * MT * 4 (i < PX, e < K) from tagged words.
 __device__ bool poll_x(const u64* tv, int K, uint32_t tag, float4* xq, unsigned* guard, uint64_t limit_ns) {
   const int tid = threadIdx.x;
@@ -595,6 +600,7 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
       }
     }
     if (__syncthreads_or(bad)) return false;
+  trace_mark(a, q, 1);
   }
 
   auto finish = [&](int g, float v0, float v1) {
@@ -728,6 +734,7 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
   }
   if (bad && lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
   __syncthreads();
+  trace_mark(a, q, 2);
   // Pairs split between warps: at most two records per warp, lane 2w + rr of
   // warp 0 holding record rr of warp w.  Every record of a pair is summed in
   // warp order by the lane of its first record, which finishes the pair; a
@@ -860,6 +867,7 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
     }
     if (__syncthreads_or(bad)) return false;
   }
+  trace_mark(a, l * kPhases + PH_ATTN, 1);
   const int kl = lane % LPK;
   float q[REP][QD];
 #pragma unroll
@@ -1036,6 +1044,7 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
       for (int dd = 0; dd < DPL; ++dd) wstate[warp][2 * REP + h * D + lane * DPL + dd] = acc[h][dd];
   }
   if (__syncthreads_or(bad)) return false;
+  trace_mark(a, l * kPhases + PH_ATTN, 2);
   // ---- this split's partial (max, sum, unnormalised output per query head):
   // combine the warps and publish it as tagged words.  Then every split of
   // the KV head merges one slice of the REP * D outputs from all the splits'
@@ -1205,8 +1214,10 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
     if (q == a.stall_phase) tag_in = tagbase | ((1u << kMegaTagShift) - 1u);  // no phase has this number
     if (lane == 0 && a.l2_ahead > 0 && ((a.l2_mask >> (l < a.n_layers ? j : 5)) & 1))
       stream_prefetch(st, a, cta, G, warp, pos, qkv_n, a.l2_ahead);
+    trace_mark(a, q, 0);
     if (l < a.n_layers && j == PH_ATTN) {
       ok = a_phase<WT, D, REP>(a, l, pos, tag_in, tag_out, smem, sh, st, consumed, cta, G, qkv_n);
+      trace_mark(a, q, 3);
       continue;
     }
     GEpi ep{EPI_RESID, a.t_resid, nullptr, a.rope, pos, D, a.nq + a.nkv, nullptr, a.guard, tag_out};
@@ -1242,6 +1253,7 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
     }
     ok = g_phase<WT, PT, D, KVT>(a, q, gdesc(a, sh, q, qkv_n, D), xt, tag_in, x0f, x0w, r0f, r0w, ep, smem, sh, st,
                                  gq, consumed, best, cta, G, pos, qkv_n);
+    trace_mark(a, q, 3);
   }
   if (ok && a.head) {
     best = warp_best(best);
