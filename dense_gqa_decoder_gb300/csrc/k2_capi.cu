@@ -270,6 +270,8 @@ struct k2_ctx {
   std::array<uint8_t, kTcMapBytes> tm_xh{}, tm_xl{}, tm_oh{}, tm_ol{}, tm_ah{}, tm_al{}, tm_lm{};
   // the same activation buffers in 16-token tiles (batched decode)
   std::array<uint8_t, kTcMapBytes> tb_xh{}, tb_xl{}, tb_oh{}, tb_ol{}, tb_ah{}, tb_al{};
+  // fp16 caches: the tensor maps of each layer's K and V for the tensor-core decode attention
+  std::vector<std::array<uint8_t, kTcMapBytes>> tm_k, tm_v;
   std::map<std::tuple<int, const void*, const void*, const void*, void*>, cudaGraphExec_t> graphs;
   std::map<std::tuple<int, int, void*>, cudaGraphExec_t> spec_graphs;  // (seq, ids verified (0: a plain step), stream)
   int spec_rows = 0;  // rows of logits the last speculative step left in the verification buffer
@@ -392,6 +394,14 @@ struct Launcher {
 //   tok: device token (null when x_in is given); x_in: caller's residual
 //   stream (layers only); head: run final norm + lm_head + argmax (else only
 //   advance the length).
+// the decode attention of layer l reads an fp16 cache through its tensor maps
+void attn_maps(const k2_ctx* c, AttnArgs& at, int l) {
+  if (!c->tm_k.empty()) {
+    at.map_k = c->tm_k[l].data();
+    at.map_v = c->tm_v[l].data();
+  }
+}
+
 void chain_b1(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in, int* next, float* logits, bool head) {
   const Sizes& s = c->s;
   const int wb = s.wb;
@@ -420,6 +430,7 @@ void chain_b1(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in, int
     at.ks = c->ks(l);
     at.vs = c->vs(l);
     at.seq0 = seq;
+    attn_maps(c, at, l);
     ln.run(K2_K_ATTN, [&] { return launch_attn(at, s.d, s.rep, kvdt, splits, 1, st, pdl); });
 
     PackedGemvArgs o = c->p_o;
@@ -837,6 +848,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
       at.pos_base = pos0;
       at.pos_base_dev = d_pos0;
       at.out = O32;
+      attn_maps(c, at, l);
       e = launch_attn(at, s.d, s.rep, kvdt, attn_splits(c, n), n, st, false);
       if (!e) e = launch_rows_hilo(O32, xh, xl, n, s.nq * s.d, st);
     } else if (!e) {
@@ -906,6 +918,7 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
       at.ks = c->ks(l);
       at.vs = c->vs(l);
       at.seq0 = 0;
+      attn_maps(c, at, l);
       e = launch_attn(at, s.d, s.rep, kvdt, asplits, B, st, false);
     }
     if (!e) e = launch_rows_hilo(c->attn_out, xh, xl, B, s.nq * s.d, st);
@@ -1186,6 +1199,18 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     g_init_error = "no thread-block cluster of the attention kernel fits this GPU";
     delete c;
     return K2_ERR_UNSUPPORTED;
+  }
+  if (cfg->kv_dtype == K2_F16 && attn_tc_supported(c->s.d, c->s.rep)) {
+    c->tm_k.resize(c->s.L);
+    c->tm_v.resize(c->s.L);
+    const long long rows = static_cast<long long>(c->s.B) * c->s.nkv * c->lay.cap;
+    for (int l = 0; l < c->s.L; ++l)
+      if (!attn_encode_kv(c->tm_k[l].data(), c->kc(l), rows, c->s.d) ||
+          !attn_encode_kv(c->tm_v[l].data(), c->vc(l), rows, c->s.d)) {
+        g_init_error = "init: tensor maps of the KV cache";
+        delete c;
+        return K2_ERR_CUDA;
+      }
   }
   // zero the state words (lengths, guard, counters) and build the rope table
   // and the tagged activations (a fresh context must not see an old tag)

@@ -176,6 +176,10 @@ struct AttnArgs {
   int block_seq;
   int pos_base;
   const int* pos_base_dev;  // block mode: read pos_base from device memory (nullable)
+  // fp16 caches: host copies of the CUtensorMaps of this layer's K and V
+  // (attn_encode_kv); when both are set the tensor-core kernel runs
+  const void* map_k;
+  const void* map_v;
 };
 constexpr int kAttnThreads = 128;     // 4 warps: three CTAs (12 warps) share an SM
 constexpr int kAttnTK = 32;          // keys per tile; a warp reads one tile at a time
@@ -189,6 +193,10 @@ int attn_max_cluster(int head_dim, int rep, int kv_dtype, int limit);
 int attn_ctas_per_sm(int head_dim, int rep, int kv_dtype);  // resident CTAs of the attention kernel per SM
 cudaError_t launch_attn(const AttnArgs& a, int head_dim, int rep, int kv_dtype, int nsplit, int batch,
                         cudaStream_t s, bool pdl);
+// the tensor-core attention (fp16 caches): shapes it covers, and the tensor map of
+// one layer's K or V cache, [rows][head_dim] fp16 (rows = batch * n_kv_heads * cap)
+bool attn_tc_supported(int head_dim, int rep);
+bool attn_encode_kv(void* map, const void* base, long long rows, int head_dim);
 
 // ---------------------------------------------------------------------------
 // persistent batch-1 decode step (one cooperative launch per token)

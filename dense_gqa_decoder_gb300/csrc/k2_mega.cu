@@ -129,9 +129,14 @@ struct Patience {
   }
 };
 
+__device__ __forceinline__ unsigned long long sm_clock() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
+  return t;
+}
 __device__ __forceinline__ void trace_mark(const MegaArgs& a, int q, int k) {
   if (a.trace != nullptr && threadIdx.x == 0)
-    a.trace[(static_cast<size_t>(q) * gridDim.x + blockIdx.x) * 4 + k] = globaltimer();
+    a.trace[(static_cast<size_t>(q) * gridDim.x + blockIdx.x) * 4 + k] = sm_clock();
 }
 
 // x[e .. e+3] for e = tid * 4 + i * MT * 4 (i < PX, e < K) from tagged words.
@@ -1189,6 +1194,11 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
   if (tid < D / 2) sh.rope_pos[tid] = a.rope[static_cast<size_t>(pos) * (D / 2) + tid];
   int consumed = 0;
   Best best{-INFINITY, 0x7fffffff};
+  if (a.trace != nullptr && tid == 0) {  // aligns this SM's clock with the others
+    const size_t at = (static_cast<size_t>(a.n_layers * kPhases + 1) * G + cta) * 4;
+    a.trace[at] = globaltimer();
+    a.trace[at + 1] = sm_clock();
+  }
 
   const WT* xe = nullptr;
   if (!a.x_ext) {
