@@ -259,6 +259,7 @@ struct k2_ctx {
   bool use_mega = true;
   int mega_grid = 0;
   MegaArgs mega = {};
+  KvMaps mega_maps = {};  // the persistent step's tensor maps of the caches (tensor-core attention)
   std::vector<LayerPtrs> ltab;
   // tensor-core prefill: TMA tensor maps (weights per layer: qkv, o, gate/up,
   // down; activations: normed input, attention output, SwiGLU output, hi/lo)
@@ -488,7 +489,7 @@ void enqueue_token(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in
     m.trace = c->trace;
     const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
     cudaStream_t st = ln.s;
-    ln.run(K2_K_STEP, [&] { return launch_mega(m, c->s.wf, c->s.d, c->s.rep, kvdt, c->mega_grid, st); });
+    ln.run(K2_K_STEP, [&] { return launch_mega(m, c->mega_maps, c->s.wf, c->s.d, c->s.rep, kvdt, c->mega_grid, st); });
   } else {
     chain_b1(c, ln, seq, tok, x_in, next, logits, head);
   }
@@ -711,6 +712,12 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   m.end_count = reinterpret_cast<unsigned*>(c->ws + c->lay.msync);
   m.epoch = m.end_count + 1;
   m.guard = c->guard;
+  if (mega_tc_attention(s.d, kvdt)) {
+    const long long rows = static_cast<long long>(s.B) * s.nkv * c->lay.cap;
+    if (!attn_encode_kv_layers(&c->mega_maps.k, c->kc(0), rows, s.d, s.L, c->lay.kv_layer, kMegaTK) ||
+        !attn_encode_kv_layers(&c->mega_maps.v, c->vc(0), rows, s.d, s.L, c->lay.kv_layer, kMegaTK))
+      return cudaSuccess;  // no tensor maps: the persistent step stays off (mega_ok false)
+  }
   c->mega_grid = grid;
   c->mega_ok = true;
   return cudaSuccess;

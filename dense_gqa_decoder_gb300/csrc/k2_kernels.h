@@ -1,6 +1,7 @@
 // Argument blocks and launchers of the sm_103a kernels (internal to libk2).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -314,6 +315,12 @@ struct MegaArgs {
   // ready, 2 weight / K-V slots consumed, 3 phase end
   unsigned long long* trace;
 };
+// fp16 caches of a head_dim that is a multiple of 64: the persistent step
+// reads K and V tiles through these tensor maps ([layer][rows][head_dim] fp16,
+// boxes of 64 dims x kMegaTK rows, 128-byte swizzle); zero otherwise
+struct alignas(64) KvMaps {
+  CUtensorMap k, v;
+};
 constexpr int kMegaThreads = 256;
 constexpr int kMegaSlots = 2;                 // ring slots per warp
 constexpr int kMegaSlotBytes = 9 * 1024;      // one bulk copy: 9 packed units, or one 16-key K/V tile
@@ -342,8 +349,14 @@ constexpr int kQ4Unit = 576;
 bool mega_supported(int wfmt, int head_dim, int rep, int kv_dtype);
 cudaError_t mega_init_attrs(int wfmt, int head_dim, int rep, int kv_dtype);
 int mega_max_grid(int wfmt, int head_dim, int rep, int kv_dtype);  // 0: cannot run
-cudaError_t launch_mega(const MegaArgs& a, int wfmt, int head_dim, int rep, int kv_dtype, int grid,
+cudaError_t launch_mega(const MegaArgs& a, const KvMaps& maps, int wfmt, int head_dim, int rep, int kv_dtype, int grid,
                         cudaStream_t s);
+// the persistent step runs its attention on the tensor cores (and needs KvMaps)
+bool mega_tc_attention(int head_dim, int kv_dtype);
+// tensor map of every layer's K or V cache: [layers][rows][head_dim] fp16, layer
+// l at base + l * layer_stride bytes, boxes of 64 dims x box_rows rows
+bool attn_encode_kv_layers(void* map, const void* base, long long rows, int head_dim, int layers,
+                           unsigned long long layer_stride, int box_rows);
 
 // ---------------------------------------------------------------------------
 // small kernels

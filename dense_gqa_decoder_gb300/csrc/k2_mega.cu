@@ -285,6 +285,27 @@ __device__ __forceinline__ int a_mine(const AItem& it, int warp) {
   return it.ntile > warp ? (it.ntile - warp + MW - 1) / MW : 0;
 }
 
+// fp16 caches with head_dim a multiple of 64: the attention phase runs on the
+// tensor cores, its K/V tiles copied by TMA tensor copies (128-byte swizzle)
+template <int D, typename KVT>
+constexpr bool tc_attn() {
+  return std::is_same<KVT, __half>::value && D % 64 == 0;
+}
+// a swizzled attention box: kMegaTK rows of 128 bytes (64 fp16 dims)
+constexpr int kTcBox = kMegaTK * 128;
+// byte offset of 16-byte chunk c (0..7) of row r inside a box (128-byte swizzle)
+__device__ __forceinline__ uint32_t swz128(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ void tma_3d_hint(void* dst, const CUtensorMap* m, int c0, int c1, int c2, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // ---- the per-warp stream of slots (state kept in lane 0) -----------------------------------
 // The producer lane walks every phase q = layer * kPhases + j (then the lm_head
 // phase) in order; enter() caches where the current phase's copies come from.
@@ -294,6 +315,7 @@ struct Stream {
   static constexpr int TKM = tile_keys<D, KVT>();
   static constexpr int ROWB = D * sizeof(KVT);
   static constexpr bool I8 = std::is_same<KVT, int8_t>::value;
+  static constexpr bool TC = tc_attn<D, KVT>();
   int q = 0, k = 0, n = 0, issued = 0, lastq = 0;
   bool done = false, attn = false;
   const uint8_t* src = nullptr;  // GEMV: next unit to copy
@@ -305,6 +327,8 @@ struct Stream {
   int j0 = 0, k1 = 0;
   uint64_t policy = 0;  // L2 evict-first: weights and K/V history are read once per step
   const MegaShared* shp = nullptr;
+  const KvMaps* maps = nullptr;  // TC: the tensor maps of the caches
+  int trow = 0, tlay = 0;        // TC: the tensor row of key 0 of this KV head, the layer
 
   __device__ void enter(const MegaArgs& a, int cta, int G, int warp, int pos, int qkv_n) {
     k = 0;
@@ -326,6 +350,8 @@ struct Stream {
       }
       j0 = it.k0 + warp * TKM;
       k1 = it.k1;
+      trow = static_cast<int>(head_row);
+      tlay = l;
       return;
     }
     const GDesc d = gdesc(a, *shp, q, qkv_n, D);
@@ -344,9 +370,10 @@ struct Stream {
     done = q > lastq;
   }
 
-  __device__ void start(const MegaArgs& a, const MegaShared& sh, uint8_t* ring, uint64_t* full, int cta, int G,
-                        int warp, int pos, int qkv_n) {
+  __device__ void start(const MegaArgs& a, const MegaShared& sh, const KvMaps* km, uint8_t* ring, uint64_t* full,
+                        int cta, int G, int warp, int pos, int qkv_n) {
     shp = &sh;
+    maps = km;
     lastq = a.n_layers * kPhases - 1 + (a.head ? 1 : 0);
     policy = l2_evict_first_policy();
     q = 0;
@@ -362,7 +389,17 @@ struct Stream {
     const int s = issued % NS;
     uint8_t* dst = ring + static_cast<size_t>(s) * SB;
     uint64_t* bar = &full[s];
-    if (attn) {
+    if (attn && TC) {
+      // whole boxes of kMegaTK rows (rows past the tile are masked by the consumer)
+      constexpr int NB = D / 64;
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * NB * kTcBox));
+#pragma unroll
+      for (int bx = 0; bx < NB; ++bx) {
+        tma_3d_hint(dst + bx * kTcBox, &maps->k, 64 * bx, trow + j0, tlay, bar, policy);
+        tma_3d_hint(dst + (NB + bx) * kTcBox, &maps->v, 64 * bx, trow + j0, tlay, bar, policy);
+      }
+      j0 += MW * TKM;
+    } else if (attn) {
       const int rows = min(TKM, k1 - j0);
       const int crow = max(0, min(rows, pos - j0));  // cached rows; row pos is written this step
       const int srow = (crow + 7) & ~7;
@@ -818,8 +855,7 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
   static_assert(TKM > 0 && 2 * KVB + 2 * TKM * 2 <= SB, "an attention tile must fit one slot");
   static_assert(D <= 128 && REP * D <= 512, "staging buffers");
   static_assert(REP <= MW, "one warp per query head in the merge");
-  __shared__ float Sw[MW][REP][TKM];
-  __shared__ __align__(16) float Pw[MW][TKM][REP];
+  constexpr bool TCA = tc_attn<D, KVT>();
   __shared__ float wstate[MW][PSTR];
   __shared__ float wfac[MW][REP];  // per warp and query head: exp(m_warp - m_split)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -873,6 +909,10 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
     if (__syncthreads_or(bad)) return false;
   }
   trace_mark(a, l * kPhases + PH_ATTN, 1);
+  bool bad = false;
+  if constexpr (!TCA) {
+  __shared__ float Sw[MW][REP][TKM];
+  __shared__ __align__(16) float Pw[MW][TKM][REP];
   const int kl = lane % LPK;
   float q[REP][QD];
 #pragma unroll
@@ -888,7 +928,6 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
 #pragma unroll
     for (int dd = 0; dd < DPL; ++dd) acc[h][dd] = 0.f;
   }
-  bool bad = false;
   for (int i = 0; i < nmine; ++i) {
     const int t = warp + i * MW;
     const int j0 = it.k0 + t * TKM;
@@ -1048,6 +1087,142 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
 #pragma unroll
       for (int dd = 0; dd < DPL; ++dd) wstate[warp][2 * REP + h * D + lane * DPL + dd] = acc[h][dd];
   }
+  } else {
+  // Q.K^T and P.V on the tensor cores (mma.sync m16n8k16, fp16 operands,
+  // fp32 accumulation).  M rows: row h < REP is fp16(q_h) (or fp16(p_h)), row
+  // REP + h the remainder q_h - fp16(q_h), so one MMA carries both halves; the
+  // fp16 K/V values are exact.  The tile's boxes are swizzled (chunk c of row r
+  // at c ^ (r & 7)), so the ldmatrix loads hit distinct banks.
+  constexpr int NB = D / 64, KS = D / 16, NT = D / 8, XR = 4 * REP;
+  static_assert(TKM == 16 && (REP == 1 || REP == 2 || REP == 4), "tensor-core tile shape");
+  const int gq = lane >> 2, tq = lane & 3, hq = gq % REP;
+  const bool live = gq < 2 * REP, rem = gq >= REP;
+  uint32_t qa[KS][2];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int d = 16 * ks + 8 * hf + 2 * tq;
+      uint32_t hi = 0u, lo = 0u;
+      if (live) split_half2(sh.qs[hq * D + d], sh.qs[hq * D + d + 1], hi, lo);
+      qa[ks][hf] = rem ? lo : hi;
+    }
+  float o[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;
+  for (int i = 0; i < nmine; ++i) {
+    const int t = warp + i * MW;
+    const int j0 = it.k0 + t * TKM;
+    const int rows = min(TKM, it.k1 - j0);
+    const int s = consumed % NS;
+    const bool ok = mbar_wait(&sh.full[warp][s], static_cast<uint32_t>(consumed / NS) & 1u);
+    if (__any_sync(0xffffffffu, !ok)) {
+      bad = true;
+      break;
+    }
+    uint8_t* ksl = ring + static_cast<size_t>(s) * SB;
+    uint8_t* vsl = ksl + NB * kTcBox;
+    const int jr = pos - j0;
+    const bool newrow = appends && jr >= 0 && jr < rows;
+    if (newrow) {  // the new token: fp16 to the cache and into the swizzled slot
+      for (int kv = 0; kv < 2; ++kv) {
+        const float* src = sh.newkv[kv];
+        __half* dst = reinterpret_cast<__half*>((kv == 0 ? a.kc : a.vc) + static_cast<size_t>(l) * a.s_kv) +
+                      (head_row + pos) * D;
+        uint8_t* base = kv == 0 ? ksl : vsl;
+        for (int e = lane; e < D; e += 32) {
+          const __half hv = __float2half_rn(src[e]);
+          dst[e] = hv;
+          *reinterpret_cast<__half*>(base + (e >> 6) * kTcBox + swz128(jr, (e & 63) >> 3) + (e & 7) * 2) = hv;
+        }
+      }
+    }
+    if (rows < TKM) {  // stale rows past the tile: P is 0 there, but 0 x NaN is NaN
+      for (int e = lane; e < (TKM - rows) * NB * 8; e += 32) {
+        const int r = rows + e / (NB * 8), bx = (e / 8) % NB, c = e & 7;
+        *reinterpret_cast<uint4*>(vsl + bx * kTcBox + r * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    __syncwarp();
+    float sacc[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint32_t af[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+      const int mi = lane >> 3, key = 8 * (mi >> 1) + (lane & 7), chunk = 2 * ks + (mi & 1);
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4(smem_u32(ksl + (chunk >> 3) * kTcBox + swz128(key, chunk & 7)), r0, r1, r2, r3);
+      mma16816(sacc[0], af, r0, r1);
+      mma16816(sacc[1], af, r2, r3);
+    }
+    // this lane's row: keys 8n + 2tq + e; the two halves of q add up
+    float sc[2][2];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float v = sacc[n][e] + __shfl_xor_sync(0xffffffffu, sacc[n][e], XR);
+        sc[n][e] = 8 * n + 2 * tq + e < rows ? v : -INFINITY;
+        mx = fmaxf(mx, sc[n][e]);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(m_run, mx);
+    const float al = expf(m_run - mn);
+    float ps = 0.f;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        sc[n][e] = expf(sc[n][e] - mn);
+        ps += sc[n][e];
+      }
+    ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+    l_run = l_run * al + ps;
+    m_run = mn;
+    uint32_t pa[2];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t hi = 0u, lo = 0u;
+      if (live) split_half2(sc[hf][0], sc[hf][1], hi, lo);
+      pa[hf] = rem ? lo : hi;
+    }
+    const uint32_t pf[4] = {pa[0], 0u, pa[1], 0u};
+#pragma unroll
+    for (int np = 0; np < NT / 2; ++np) {
+      const int mi = lane >> 3, key = 8 * (mi & 1) + (lane & 7), chunk = 2 * np + (mi >> 1);
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4_t(smem_u32(vsl + (chunk >> 3) * kTcBox + swz128(key, chunk & 7)), r0, r1, r2, r3);
+      o[2 * np][0] *= al;
+      o[2 * np][1] *= al;
+      o[2 * np + 1][0] *= al;
+      o[2 * np + 1][1] *= al;
+      mma16816(o[2 * np], pf, r0, r1);
+      mma16816(o[2 * np + 1], pf, r2, r3);
+    }
+    // generic stores into the slot (the new row, zeroed rows) before the next copy over them
+    if (newrow || rows < TKM) fence_proxy_async();
+    __syncwarp();
+    ++consumed;
+    if (lane == 0) st.issue_next(a, ring, sh.full[warp], cta, G, warp, pos, qkv_n);
+  }
+  if (bad && lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
+  if (live && !rem && tq == 0) {
+    wstate[warp][hq] = m_run;
+    wstate[warp][REP + hq] = l_run;
+  }
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float v = o[n][e] + __shfl_xor_sync(0xffffffffu, o[n][e], XR);
+      if (live && !rem) wstate[warp][2 * REP + hq * D + 8 * n + 2 * tq + e] = v;
+    }
+  }
   if (__syncthreads_or(bad)) return false;
   trace_mark(a, l * kPhases + PH_ATTN, 2);
   // ---- this split's partial (max, sum, unnormalised output per query head):
@@ -1154,8 +1329,12 @@ __device__ bool a_phase(const MegaArgs& a, int l, int pos, uint32_t tag_in, uint
 
 // ---- the step -------------------------------------------------------------------------------
 template <typename WT, typename PT, int D, int REP, typename KVT>
-__global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const __grid_constant__ KvMaps maps, const MegaArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // the tensor-core attention's swizzled boxes need 1024-byte aligned slots
+  uint8_t* const smem = tc_attn<D, KVT>() ? reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                                        ~static_cast<uintptr_t>(1023))
+                                          : smem_raw;
   __shared__ MegaShared sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x, G = gridDim.x;
@@ -1189,7 +1368,8 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const MegaArgs a) {
   for (int i = tid; i < 2 * a.n_layers; i += MT)
     sh.gains[i] = (i & 1) ? a.layers[i >> 1].mlp_norm : a.layers[i >> 1].attn_norm;
   __syncthreads();  // barriers initialised, tables written
-  if (lane == 0) st.start(a, sh, smem + static_cast<size_t>(warp) * NS * SB, sh.full[warp], cta, G, warp, pos, qkv_n);
+  if (lane == 0)
+    st.start(a, sh, &maps, smem + static_cast<size_t>(warp) * NS * SB, sh.full[warp], cta, G, warp, pos, qkv_n);
   if (tid == 0) issue_gain(a, smem, sh, gq, sh.gains[0], a.hidden * static_cast<int>(sizeof(WT)));
   if (tid < D / 2) sh.rope_pos[tid] = a.rope[static_cast<size_t>(pos) * (D / 2) + tid];
   int consumed = 0;
@@ -1360,10 +1540,18 @@ bool mega_supported(int wfmt, int head_dim, int rep, int kv_dtype) {
   return mega_lookup(wfmt, head_dim, rep, kv_dtype) != nullptr;
 }
 
+bool mega_tc_attention(int head_dim, int kv_dtype) { return kv_dtype == 2 && head_dim % 64 == 0; }
+
+namespace {
+// dynamic shared memory of an instance: the tensor-core attention aligns its ring to 1024 bytes
+size_t mega_smem(int head_dim, int kv_dtype) { return kMegaSmemBytes + (mega_tc_attention(head_dim, kv_dtype) ? 1024 : 0); }
+}  // namespace
+
 cudaError_t mega_init_attrs(int wfmt, int head_dim, int rep, int kv_dtype) {
   const void* fn = mega_lookup(wfmt, head_dim, rep, kv_dtype);
   if (!fn) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMegaSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(mega_smem(head_dim, kv_dtype)));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
@@ -1373,26 +1561,28 @@ int mega_max_grid(int wfmt, int head_dim, int rep, int kv_dtype) {
   const void* fn = mega_lookup(wfmt, head_dim, rep, kv_dtype);
   if (!fn) return 0;
   int per_sm = 0, dev = 0, sms = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, MT, kMegaSmemBytes) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, MT, mega_smem(head_dim, kv_dtype)) != cudaSuccess)
+    return 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   return per_sm >= 1 ? sms : 0;  // one CTA per SM
 }
 
-cudaError_t launch_mega(const MegaArgs& a, int wfmt, int head_dim, int rep, int kv_dtype, int grid, cudaStream_t s) {
+cudaError_t launch_mega(const MegaArgs& a, const KvMaps& maps, int wfmt, int head_dim, int rep, int kv_dtype, int grid,
+                        cudaStream_t s) {
   const void* fn = mega_lookup(wfmt, head_dim, rep, kv_dtype);
   if (!fn) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(MT);
-  cfg.dynamicSmemBytes = kMegaSmemBytes;
+  cfg.dynamicSmemBytes = mega_smem(head_dim, kv_dtype);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void* args[] = {const_cast<MegaArgs*>(&a)};
+  void* args[] = {const_cast<KvMaps*>(&maps), const_cast<MegaArgs*>(&a)};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

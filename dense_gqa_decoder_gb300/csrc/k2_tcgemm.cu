@@ -419,6 +419,21 @@ bool attn_encode_kv(void* map, const void* base, long long rows, int head_dim) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool attn_encode_kv_layers(void* map, const void* base, long long rows, int head_dim, int layers,
+                           unsigned long long layer_stride, int box_rows) {
+  EncodeTiled enc = encode_fn();
+  if (!enc || head_dim % 64 != 0 || rows <= 0 || layers <= 0 || layer_stride % 16 != 0 || box_rows < 1 ||
+      box_rows > 256)
+    return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(layers)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2, layer_stride};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1}, es[3] = {1, 1, 1};
+  return enc(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
+             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t tc_gemm_init_attrs() {
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Tile<128>::SMEM_BYTES);
