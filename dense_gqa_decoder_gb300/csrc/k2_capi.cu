@@ -278,9 +278,10 @@ struct k2_ctx {
   int spec_rows = 0;  // rows of logits the last speculative step left in the verification buffer
   unsigned long long poll_limit_ns = 1000000000ull;  // persistent step: waits for other CTAs' words (1 s)
   int stall_phase = -1;                              // persistent step: test option K2_OPT_STALL_PHASE
-  // persistent step: L2 look-ahead per phase kind (one slot at the QKV, gate/up
-  // and down phases measured fastest: 1.954 against 2.002 ms per token)
-  int l2_ahead = 1, l2_mask = 0x19;
+  // persistent step: L2 look-ahead per phase kind (two slots at the gate/up and
+  // down phases measured fastest at context 4096: 1.934 against 1.990 ms per
+  // token without; deeper look-ahead, or look-ahead at the attention phase, was slower)
+  int l2_ahead = 2, l2_mask = 0x18;
   unsigned long long* trace = nullptr;               // persistent step: K2_OPT_TRACE buffer
   std::string err;
   // profiling: event pairs around the kernels of one step
