@@ -424,22 +424,17 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const Attn
 // of the KV head as M rows.  Row h < REP holds fp16(q_h) (or fp16(p_h)), row
 // REP + h the remainder q_h - fp16(q_h), so one MMA carries both halves and the
 // sum of the two rows keeps about 22 bits of every q and p; the fp16 K/V values
-// themselves are exact.  Each warp streams 16-key tiles through two slots (the
-// tile after next is requested as soon as a slot is free, so one tile is always
-// in flight while the other is computed); a tile's K and V rows arrive by TMA
-// tensor copies in boxes of 64 dims x 16 rows with the 128-byte swizzle (16-byte
-// chunk c of row r stored at chunk c ^ (r & 7)), so the ldmatrix fragment loads
-// hit distinct banks.  A box always holds 16 rows: rows past the tile's end are
-// masked out of the scores and zeroed in V before P.V (stale rows may hold any
-// bit pattern).
+// themselves are exact.  K/V tiles of 32 keys arrive by TMA tensor copies in
+// boxes of 64 dims x 32 rows with the 128-byte swizzle (16-byte chunk c of row
+// r stored at chunk c ^ (r & 7)), so the ldmatrix fragment loads hit distinct
+// banks.  A box always holds 32 rows: rows past the tile's end are masked out of
+// the scores and zeroed in V before P.V (stale rows may hold any bit pattern).
 template <int D>
 struct TcTile {
-  static constexpr int TK = kAttnTcTK;      // keys per tile
-  static constexpr int NB = D / 64;         // 64-dim boxes per K (or V) tile
-  static constexpr int BOX = TK * 128;      // bytes of one box
-  static constexpr int KV = NB * BOX;       // bytes of the K (or V) rows of a tile
-  static constexpr int SLOT = 2 * KV;       // one tile
-  static constexpr int WARP = 2 * SLOT;     // a warp's two slots
+  static constexpr int NB = D / 64;          // 64-dim boxes per K (or V) tile
+  static constexpr int BOX = kAttnTK * 128;  // bytes of one box: 32 rows of 128 B
+  static constexpr int KV = NB * BOX;        // bytes of the K (or V) half of a slot
+  static constexpr int SLOT = 2 * KV;
 };
 // byte offset of 16-byte chunk c (0..7) of row r inside a swizzled box
 __device__ __forceinline__ uint32_t swz(int r, int c) { return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)); }
@@ -456,18 +451,17 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_tc_kernel(const _
                                                                         const __grid_constant__ CUtensorMap mv,
                                                                         const AttnArgs a) {
   using T = TcTile<D>;
-  constexpr int TK = T::TK;
+  constexpr int TK = kAttnTK;
   constexpr int KS = D / 16;  // k-steps of Q.K^T
   constexpr int NT = D / 8;   // n-tiles (8 dims) of P.V
   constexpr int PSTR = REP * (D + 2);
   constexpr int XR = 4 * REP;  // lane distance between a head's fp16 row and its remainder row
-  static_assert(TK == 16 && D % 64 == 0 && (REP == 1 || REP == 2 || REP == 4), "tile shape");
-  static_assert(2 * REP + REP * D <= T::WARP / 4, "a warp's state fits its slots");
+  static_assert(TK == 32 && D % 64 == 0 && (REP == 1 || REP == 2 || REP == 4), "tile shape");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t full[kWarps][2];
+  __shared__ uint64_t fullk[kWarps], fullv[kWarps];
   __shared__ float cpart[PSTR];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -487,27 +481,26 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_tc_kernel(const _
   const int ntile = k1 > k0 ? (k1 - k0 + TK - 1) / TK : 0;
   const int nmine = ntile > warp ? (ntile - warp + kWarps - 1) / kWarps : 0;
   const size_t head_row = (static_cast<size_t>(seq) * a.nkv + g) * a.cap;
-  uint8_t* wbase = smem + static_cast<size_t>(warp) * T::WARP;
+  uint8_t* ksl = smem + static_cast<size_t>(warp) * T::SLOT;
+  uint8_t* vsl = ksl + T::KV;
 
-  // lane 0: the K and V rows of this warp's tile number `it` into slot it & 1
-  auto issue = [&](int it) {
-    const int y = static_cast<int>(head_row) + k0 + (warp + it * kWarps) * TK;
-    uint8_t* sl = wbase + (it & 1) * T::SLOT;
-    uint64_t* bar = &full[warp][it & 1];
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(T::SLOT));
+  // lane 0: the K (kv = 0) or V half of tile t, all of its boxes
+  auto issue = [&](int t, int kv) {
+    const int y = static_cast<int>(head_row) + k0 + t * TK;
+    uint64_t* bar = kv == 0 ? &fullk[warp] : &fullv[warp];
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(T::KV));
 #pragma unroll
-    for (int bx = 0; bx < T::NB; ++bx) {
-      tma_2d_kv(sl + bx * T::BOX, &mk, 64 * bx, y, bar);
-      tma_2d_kv(sl + T::KV + bx * T::BOX, &mv, 64 * bx, y, bar);
-    }
+    for (int bx = 0; bx < T::NB; ++bx) tma_2d_kv((kv == 0 ? ksl : vsl) + bx * T::BOX, kv == 0 ? &mk : &mv, 64 * bx, y, bar);
   };
 
   if (lane == 0) {
-    mbar_init(&full[warp][0], 1);
-    mbar_init(&full[warp][1], 1);
+    mbar_init(&fullk[warp], 1);
+    mbar_init(&fullv[warp], 1);
     fence_mbar_init();
-    if (nmine > 0) issue(0);
-    if (nmine > 1) issue(1);
+    if (nmine > 0) {
+      issue(warp, 0);
+      issue(warp, 1);
+    }
   }
   __syncwarp();
   pdl_wait();
@@ -537,20 +530,26 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_tc_kernel(const _
 
   bool bad = false;
   int it = 0;
+  bool kdone = false, knext = false;
   for (; it < nmine; ++it) {
+    kdone = knext = false;
     const int t = warp + it * kWarps;
     const int j0 = k0 + t * TK;
     const int rows = min(TK, k1 - j0);
-    if (__any_sync(0xffffffffu, !mbar_wait(&full[warp][it & 1], static_cast<uint32_t>(it >> 1) & 1u))) {
+    const uint32_t par = static_cast<uint32_t>(it) & 1u;
+    if (__any_sync(0xffffffffu, !mbar_wait(&fullk[warp], par))) {
       bad = true;
       break;
     }
-    uint8_t* ksl = wbase + (it & 1) * T::SLOT;
-    uint8_t* vsl = ksl + T::KV;
+    kdone = true;
     // ---- the new token's K/V: fp16 to the cache and into the (swizzled) slot
     const int jr = pos - j0;
     const bool newrow = !a.block_mode && k1 == L && jr >= 0 && jr < rows;
     if (newrow) {
+      if (__any_sync(0xffffffffu, !mbar_wait(&fullv[warp], par))) {
+        bad = true;
+        break;
+      }
       for (int kv = 0; kv < 2; ++kv) {
         const float* src = qkv + (kv == 0 ? a.nq * D : (a.nq + a.nkv) * D) + g * D;
         __half* dst = reinterpret_cast<__half*>(kv == 0 ? a.kc_w : a.vc_w) + (head_row + pos) * D;
@@ -561,32 +560,36 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_tc_kernel(const _
           *reinterpret_cast<__half*>(base + (i >> 6) * T::BOX + swz(jr, (i & 63) >> 3) + (i & 7) * 2) = hv;
         }
       }
+      __syncwarp();
     }
-    if (rows < TK) {  // stale rows past the tile: P is 0 there, but 0 x NaN is NaN
-      for (int i = lane; i < (TK - rows) * T::NB * 8; i += 32) {
-        const int r = rows + i / (T::NB * 8), bx = (i / 8) % T::NB, c = i & 7;
-        *reinterpret_cast<uint4*>(vsl + bx * T::BOX + r * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    __syncwarp();
-    // ---- S = Q.K^T: two n-tiles of 8 keys
-    float s[2][4];
+    // ---- S = Q.K^T: four n-tiles of 8 keys
+    float s[4][4];
 #pragma unroll
-    for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+    for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       const uint32_t af[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-      const int mi = lane >> 3, key = 8 * (mi >> 1) + (lane & 7), chunk = 2 * ks + (mi & 1);
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4(smem_u32(ksl + (chunk >> 3) * T::BOX + swz(key, chunk & 7)), r0, r1, r2, r3);
-      mma16816(s[0], af, r0, r1);
-      mma16816(s[1], af, r2, r3);
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        const int mi = lane >> 3, key = 8 * (2 * pp + (mi >> 1)) + (lane & 7), chunk = 2 * ks + (mi & 1);
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(smem_u32(ksl + (chunk >> 3) * T::BOX + swz(key, chunk & 7)), r0, r1, r2, r3);
+        mma16816(s[2 * pp], af, r0, r1);
+        mma16816(s[2 * pp + 1], af, r2, r3);
+      }
+    }
+    __syncwarp();
+    // the K half is read: copy the next tile's K rows now
+    if (lane == 0 && it + 1 < nmine) {
+      if (newrow) fence_proxy_async();  // generic stores into the slot before the tensor copy over them
+      issue(t + kWarps, 0);
+      knext = true;
     }
     // ---- online softmax on this lane's row: keys 8n + 2tq + e; the two halves of q add up
-    float sc[2][2];
+    float sc[4][2];
     float mx = -INFINITY;
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float v = s[n][e] + __shfl_xor_sync(0xffffffffu, s[n][e], XR);
@@ -599,7 +602,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_tc_kernel(const _
     const float al = expf(m_run - mn);  // m_run = -inf on the first tile: 0 (o is 0 anyway)
     float ps = 0.f;
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         sc[n][e] = expf(sc[n][e] - mn);
@@ -609,43 +612,66 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_tc_kernel(const _
     ps += __shfl_xor_sync(0xffffffffu, ps, 2);
     l_run = l_run * al + ps;
     m_run = mn;
-    uint32_t pa[2];
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      uint32_t hi = 0u, lo = 0u;
-      if (live) split_half2(sc[hf][0], sc[hf][1], hi, lo);
-      pa[hf] = rem ? lo : hi;
+    for (int n = 0; n < NT; ++n) {
+      o[n][0] *= al;
+      o[n][1] *= al;
     }
-    const uint32_t pf[4] = {pa[0], 0u, pa[1], 0u};
-    // ---- O = alpha O + P.V: one k-step of 16 keys, n-tiles of 8 dims in pairs
+    // A fragments of P: k-step kk covers keys 16kk .. 16kk + 15 (n-tiles 2kk, 2kk + 1)
+    uint32_t pa[2][2];
 #pragma unroll
-    for (int np = 0; np < NT / 2; ++np) {
-      const int mi = lane >> 3, key = 8 * (mi & 1) + (lane & 7), chunk = 2 * np + (mi >> 1);
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4_t(smem_u32(vsl + (chunk >> 3) * T::BOX + swz(key, chunk & 7)), r0, r1, r2, r3);
-      o[2 * np][0] *= al;
-      o[2 * np][1] *= al;
-      o[2 * np + 1][0] *= al;
-      o[2 * np + 1][1] *= al;
-      mma16816(o[2 * np], pf, r0, r1);
-      mma16816(o[2 * np + 1], pf, r2, r3);
+    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t hi = 0u, lo = 0u;
+        if (live) split_half2(sc[2 * kk + hf][0], sc[2 * kk + hf][1], hi, lo);
+        pa[kk][hf] = rem ? lo : hi;
+      }
+    // ---- the V half: stale rows past the tile's end are zeroed (P is 0 there, but 0 x NaN is NaN)
+    if (!newrow && __any_sync(0xffffffffu, !mbar_wait(&fullv[warp], par))) {
+      bad = true;
+      break;
     }
-    // the slot is read: the tile after next goes into it (generic stores into
-    // the slot, the new row or zeroed rows, come before the tensor copy over them)
-    if (newrow || rows < TK) fence_proxy_async();
+    if (rows < TK) {
+      for (int i = lane; i < (TK - rows) * T::NB * 8; i += 32) {
+        const int r = rows + i / (T::NB * 8), bx = (i / 8) % T::NB, c = i & 7;
+        *reinterpret_cast<uint4*>(vsl + bx * T::BOX + r * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
+    // ---- O += P.V: two k-steps of 16 keys, n-tiles of 8 dims in pairs
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const uint32_t af[4] = {pa[kk][0], 0u, pa[kk][1], 0u};
+#pragma unroll
+      for (int np = 0; np < NT / 2; ++np) {
+        const int mi = lane >> 3, key = 16 * kk + 8 * (mi & 1) + (lane & 7), chunk = 2 * np + (mi >> 1);
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(smem_u32(vsl + (chunk >> 3) * T::BOX + swz(key, chunk & 7)), r0, r1, r2, r3);
+        mma16816(o[2 * np], af, r0, r1);
+        mma16816(o[2 * np + 1], af, r2, r3);
+      }
+    }
     __syncwarp();
-    if (lane == 0 && it + 2 < nmine) issue(it + 2);
+    if (lane == 0 && it + 1 < nmine) {
+      if (newrow || rows < TK) fence_proxy_async();
+      issue(t + kWarps, 1);
+    }
   }
   if (bad && lane == 0) {
     atomicOr(a.guard, GUARD_TIMEOUT);
-    // the copies that may still be in flight into this warp's slots, bounded:
-    // the tile whose wait gave up and the one after it (if issued)
-    for (int k = it; k < min(nmine, it + 2); ++k) (void)mbar_wait(&full[warp][k & 1], static_cast<uint32_t>(k >> 1) & 1u);
+    // the copies that may still be in flight into this slot, bounded (as in the scalar kernel)
+    const uint32_t par = static_cast<uint32_t>(it) & 1u;
+    if (it < nmine) {
+      if (!kdone) (void)mbar_wait(&fullk[warp], par);
+      if (knext) (void)mbar_wait(&fullk[warp], par ^ 1u);
+      (void)mbar_wait(&fullv[warp], par);
+    }
   }
   __syncwarp();
 
-  // ---- this warp's (m, l, o) per head into its idle slots: o = fp16 row + remainder row
-  float* wst = reinterpret_cast<float*>(wbase);
+  // ---- this warp's (m, l, o) per head into its idle slot: o = fp16 row + remainder row
+  float* wst = reinterpret_cast<float*>(ksl);
   if (live && !rem && tq == 0) {
     wst[hq] = m_run;
     wst[REP + hq] = l_run;
@@ -661,20 +687,20 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_tc_kernel(const _
   for (int idx = tid; idx < REP * D; idx += kAttnThreads) {
     const int h = idx / D;
     float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, reinterpret_cast<const float*>(smem + w * T::WARP)[h]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, reinterpret_cast<const float*>(smem + w * T::SLOT)[h]);
     float O = 0.f;
     for (int w = 0; w < kWarps; ++w) {
-      const float* ws = reinterpret_cast<const float*>(smem + w * T::WARP);
+      const float* ws = reinterpret_cast<const float*>(smem + w * T::SLOT);
       if (ws[h] != -INFINITY) O = fmaf(ws[2 * REP + idx], expf(ws[h] - M), O);
     }
     cpart[2 * REP + idx] = O;
   }
   if (tid < REP) {
     float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, reinterpret_cast<const float*>(smem + w * T::WARP)[tid]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, reinterpret_cast<const float*>(smem + w * T::SLOT)[tid]);
     float Ls = 0.f;
     for (int w = 0; w < kWarps; ++w) {
-      const float* ws = reinterpret_cast<const float*>(smem + w * T::WARP);
+      const float* ws = reinterpret_cast<const float*>(smem + w * T::SLOT);
       if (ws[tid] != -INFINITY) Ls = fmaf(ws[REP + tid], expf(ws[tid] - M), Ls);
     }
     cpart[tid] = M;
@@ -745,7 +771,7 @@ template <int D, int REP>
 cudaError_t launch_tc(const AttnArgs& a, const cudaLaunchConfig_t& cfg) {
   if constexpr (D % 64 == 0) {
     cudaLaunchConfig_t c2 = cfg;
-    c2.dynamicSmemBytes = static_cast<size_t>(TcTile<D>::WARP) * kWarps + 1024;
+    c2.dynamicSmemBytes = static_cast<size_t>(TcTile<D>::SLOT) * kWarps + 1024;
     return cudaLaunchKernelEx(&c2, attn_decode_tc_kernel<D, REP>, *static_cast<const CUtensorMap*>(a.map_k),
                               *static_cast<const CUtensorMap*>(a.map_v), a);
   }

@@ -184,7 +184,6 @@ struct AttnArgs {
 };
 constexpr int kAttnThreads = 128;     // 4 warps: three CTAs (12 warps) share an SM
 constexpr int kAttnTK = 32;          // keys per tile; a warp reads one tile at a time
-constexpr int kAttnTcTK = 16;        // tensor-core kernel (fp16 caches): keys per tile, two tiles per warp
 constexpr int kAttnMaxCluster = 16;  // key-range splits of one KV head = one thread-block cluster
 
 bool attn_supported(int head_dim, int rep, int kv_dtype);
@@ -319,7 +318,7 @@ struct MegaArgs {
 // fp16 caches of a head_dim that is a multiple of 64: the persistent step
 // reads K and V tiles through these tensor maps ([layer][rows][head_dim] fp16,
 // boxes of 64 dims x kMegaTK rows, 128-byte swizzle); zero otherwise
-struct KvMaps {
+struct alignas(64) KvMaps {
   CUtensorMap k, v;
 };
 constexpr int kMegaThreads = 256;

@@ -406,14 +406,14 @@ bool tc_encode_act(void* map, const void* buf, int rows, int K, int tile_tokens)
 }
 
 // One layer's K or V cache as a 2-D tensor [rows][head_dim] of fp16, read by
-// the tensor-core decode attention in boxes of 64 dims x 16 rows with the
+// the tensor-core decode attention in boxes of 64 dims x 32 rows with the
 // 128-byte swizzle (the layout its ldmatrix fragments expect).
 bool attn_encode_kv(void* map, const void* base, long long rows, int head_dim) {
   EncodeTiled enc = encode_fn();
   if (!enc || head_dim % 64 != 0 || rows <= 0) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kAttnTcTK)}, es[2] = {1, 1};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kAttnTK)}, es[2] = {1, 1};
   return enc(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
