@@ -318,7 +318,7 @@ struct MegaArgs {
 // fp16 caches of a head_dim that is a multiple of 64: the persistent step
 // reads K and V tiles through these tensor maps ([layer][rows][head_dim] fp16,
 // boxes of 64 dims x kMegaTK rows, 128-byte swizzle); zero otherwise
-struct alignas(64) KvMaps {
+struct KvMaps {
   CUtensorMap k, v;
 };
 constexpr int kMegaThreads = 256;
