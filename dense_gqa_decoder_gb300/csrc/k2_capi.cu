@@ -893,8 +893,12 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
   float* gout = reinterpret_cast<float*>(c->ws + c->lay.pqkv);  // QKV, then gate/up GEMM output
   float* logits = d_logits ? d_logits : reinterpret_cast<float*>(c->ws + c->lay.plog);
   const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
-  // stream-K GEMMs over 16-token tiles: one CTA per SM, fp32 atomic adds into
-  // `out` (zeroed first unless it is the residual stream)
+  // Every launch of the step uses programmatic dependent launch: a kernel may
+  // start while its predecessor drains and waits for it (griddepcontrol.wait)
+  // before reading its output; the stream-K GEMMs request their first weight
+  // stages before that wait.  The GEMMs add their partial sums with fp32 atomics
+  // into `out`: a target that is not the residual stream is cleared by the norm
+  // kernel in front of the GEMM (a memset node would break the chain).
   auto gemm = [&](const void* mw, const void* mh, const void* ml, int N, int K, int mode, float* out, int ldo) {
     TcGemmArgs g = {};
     g.N = N;
@@ -907,18 +911,20 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
     g.splits = 1;
     g.out = out;
     g.guard = c->guard;
-    cudaError_t e = cudaSuccess;
-    if (mode == TC_STORE) e = cudaMemsetAsync(out, 0, sizeof(float) * static_cast<size_t>(B) * ldo, st);
-    if (!e) e = launch_tc_gemm_sk(mw, mh, ml, g, c->sms, st);
-    return e;
+    return launch_tc_gemm_sk(mw, mh, ml, g, c->sms, st, true);
   };
+  // the final norm clears the logits unless the caller's buffer is not 16-byte aligned
+  const bool lg_aligned = reinterpret_cast<uintptr_t>(logits) % 16 == 0 && (static_cast<size_t>(B) * s.V) % 4 == 0;
   const int asplits = attn_splits(c, B);
   cudaError_t e = launch_embed_rows(d_tokens, B, c->embed, s.wb, X, s.H, s.V, c->guard, c->hist, c->lay.cap,
-                                    c->seq_len, 0, nullptr, st);
+                                    c->seq_len, 0, nullptr, st, true);
   for (int l = 0; l < s.L && !e; ++l) {
-    if (!e) e = launch_norm_rows(X, B, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
+    if (!e)
+      e = launch_norm_rows(X, B, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st, true, gout,
+                           static_cast<size_t>(B) * s.qkv_n);
     if (!e) e = gemm(c->tmw[4 * l].data(), c->tb_xh.data(), c->tb_xl.data(), s.qkv_n, s.H, TC_STORE, gout, s.qkv_n);
-    if (!e) e = launch_rope_batch(gout, c->qkv, c->rope, c->seq_len, B, s.nq, s.nkv, s.d, c->lay.cap, c->guard, st);
+    if (!e)
+      e = launch_rope_batch(gout, c->qkv, c->rope, c->seq_len, B, s.nq, s.nkv, s.d, c->lay.cap, c->guard, st, true);
     if (!e) {
       AttnArgs at = c->p_attn;
       at.kc = at.kc_w = c->kc(l);
@@ -927,21 +933,26 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
       at.vs = c->vs(l);
       at.seq0 = 0;
       attn_maps(c, at, l);
-      e = launch_attn(at, s.d, s.rep, kvdt, asplits, B, st, false);
+      e = launch_attn(at, s.d, s.rep, kvdt, asplits, B, st, true);
     }
-    if (!e) e = launch_rows_hilo(c->attn_out, xh, xl, B, s.nq * s.d, st);
+    if (!e) e = launch_rows_hilo(c->attn_out, xh, xl, B, s.nq * s.d, st, true);
     if (!e) e = gemm(c->tmw[4 * l + 1].data(), c->tb_oh.data(), c->tb_ol.data(), s.H, s.nq * s.d, TC_RESID, X, s.H);
-    if (!e) e = launch_norm_rows(X, B, c->mlp_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
-    if (!e) e = gemm(c->tmw[4 * l + 2].data(), c->tb_xh.data(), c->tb_xl.data(), 2 * s.I, s.H, TC_STORE, gout,
-                     2 * s.I);
-    if (!e) e = launch_swiglu_rows(gout, ah, al, B, s.I, st);
+    if (!e)
+      e = launch_norm_rows(X, B, c->mlp_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st, true, gout,
+                           static_cast<size_t>(B) * 2 * s.I);
+    if (!e)
+      e = gemm(c->tmw[4 * l + 2].data(), c->tb_xh.data(), c->tb_xl.data(), 2 * s.I, s.H, TC_STORE, gout, 2 * s.I);
+    if (!e) e = launch_swiglu_rows(gout, ah, al, B, s.I, st, true);
     if (!e) e = gemm(c->tmw[4 * l + 3].data(), c->tb_ah.data(), c->tb_al.data(), s.H, s.I, TC_RESID, X, s.H);
   }
-  if (!e) e = cudaMemcpyAsync(c->resid, X, sizeof(float) * B * s.H, cudaMemcpyDeviceToDevice, st);
-  if (!e) e = launch_norm_rows(X, B, c->final_norm, s.wb, xh, xl, s.H, s.G, c->cfg.eps, st);
+  // the final norm also leaves the residual in the hidden view
+  if (!e && !lg_aligned) e = cudaMemsetAsync(logits, 0, sizeof(float) * static_cast<size_t>(B) * s.V, st);
+  if (!e)
+    e = launch_norm_rows(X, B, c->final_norm, s.wb, xh, xl, s.H, s.G, c->cfg.eps, st, true,
+                         lg_aligned ? logits : nullptr, lg_aligned ? static_cast<size_t>(B) * s.V : 0, c->resid);
   if (!e) e = gemm(c->tm_lm.data(), c->tb_xh.data(), c->tb_xl.data(), s.V, s.H, TC_STORE, logits, s.V);
-  if (!e) e = launch_argmax_rows(logits, B, s.V, d_next, c->am_val, c->am_idx, kArgmaxPartsMax, c->guard, st);
-  if (!e) e = launch_advance(c->seq_len, 0, B, st, false);
+  if (!e) e = launch_argmax_rows(logits, B, s.V, d_next, c->am_val, c->am_idx, kArgmaxPartsMax, c->guard, st, true);
+  if (!e) e = launch_advance(c->seq_len, 0, B, st, true);
   return e;
 }
 

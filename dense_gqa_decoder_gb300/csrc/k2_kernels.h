@@ -397,18 +397,24 @@ bool tc_encode_act(void* map, const void* buf, int rows, int K, int tile_tokens)
 cudaError_t tc_gemm_init_attrs();
 cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a,
                            cudaStream_t s);
-// stream-K persistent variant (tile_tokens 16; TC_STORE into a zeroed target or TC_RESID), `ctas` CTAs
+// stream-K persistent variant (tile_tokens 16; TC_STORE into a zeroed target or TC_RESID), `ctas` CTAs.
+// pdl: programmatic dependent launch; the first weight stages are requested before
+// the kernel waits for its predecessor (weights never depend on an earlier kernel)
 cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a, int ctas,
-                              cudaStream_t s);
+                              cudaStream_t s, bool pdl = false);
 bool prefill_attn_supported(int head_dim, int rep);
 cudaError_t prefill_init_attrs();
 // hist (nullable): row t's token is recorded at hist[t * hist_stride + pos[t]], or at
 // hist[pos0 + t] when pos is null (pos0 read from pos0_dev when that is not null)
 cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbytes, float* X, int H, int vocab,
                               unsigned* guard, int* hist, int hist_stride, const int* pos, int pos0,
-                              const int* pos0_dev, cudaStream_t s);
+                              const int* pos0_dev, cudaStream_t s, bool pdl = false);
+// GroupedRMSNorm rows -> bf16 hi/lo; zero (nullable, zero_floats a multiple of 4,
+// 16-byte aligned): extra CTAs clear it (the output of the GEMM that follows);
+// copy (nullable): the rows of X are also copied there
 cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes, __nv_bfloat16* oh,
-                             __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s);
+                             __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s, bool pdl = false,
+                             float* zero = nullptr, size_t zero_floats = 0, float* copy = nullptr);
 // pos0_dev (nullable): read the first position from device memory instead of pos0
 cudaError_t launch_rope_append(const float* qkv, float* Q, const float2* rope, int kv_dtype, void* kc, void* vc,
                                void* ks, void* vs, int n, int nq, int nkv, int D, int pos0, const int* pos0_dev,
@@ -418,11 +424,13 @@ cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, co
                                 int pos0, size_t head_row0, int cap, float scale, cudaStream_t s);
 cudaError_t launch_advance_by(int* seq_len, int seq, int n, cudaStream_t s);
 cudaError_t launch_rope_batch(const float* packed, float* nat, const float2* rope, const int* seq_len, int B, int nq,
-                              int nkv, int D, int cap, unsigned* guard, cudaStream_t s);
-cudaError_t launch_swiglu_rows(const float* gu, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int I, cudaStream_t s);
-cudaError_t launch_rows_hilo(const float* x, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int K, cudaStream_t s);
+                              int nkv, int D, int cap, unsigned* guard, cudaStream_t s, bool pdl = false);
+cudaError_t launch_swiglu_rows(const float* gu, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int I, cudaStream_t s,
+                               bool pdl = false);
+cudaError_t launch_rows_hilo(const float* x, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int K, cudaStream_t s,
+                             bool pdl = false);
 cudaError_t launch_argmax_rows(const float* logits, int rows, int V, int* next, float* part_val, int* part_idx,
-                               int part_stride, unsigned* guard, cudaStream_t s);
+                               int part_stride, unsigned* guard, cudaStream_t s, bool pdl = false);
 cudaError_t misc_init_attrs();
 
 }  // namespace k2

@@ -12,6 +12,9 @@
 
 #include <type_traits>
 
+#include <algorithm>
+#include <utility>
+
 #include "k2_kernels.h"
 #include "k2_common.cuh"
 
@@ -29,6 +32,8 @@ __global__ void embed_rows_kernel(const int* __restrict__ tokens, const WT* __re
                                   int H, int vocab, unsigned* guard, int* hist, int hist_stride, const int* pos,
                                   int pos0, const int* pos0_dev) {
   const int t = blockIdx.x;
+  pdl_wait();  // tokens and lengths come from the previous kernel
+  pdl_trigger();
   int tok = tokens[t];
   if (hist && threadIdx.x == 0)
     hist[pos ? static_cast<size_t>(t) * hist_stride + pos[t]
@@ -45,10 +50,19 @@ __global__ void embed_rows_kernel(const int* __restrict__ tokens, const WT* __re
 // written as bf16 hi/lo
 template <typename WT>
 __global__ void norm_rows_kernel(const float* __restrict__ X, const WT* __restrict__ gain, __nv_bfloat16* __restrict__ oh,
-                                 __nv_bfloat16* __restrict__ ol, int H, int groups, float eps) {
+                                 __nv_bfloat16* __restrict__ ol, int H, int groups, float eps, int rows,
+                                 float4* __restrict__ zero, size_t zero_n4, float* __restrict__ copy) {
   __shared__ float part[32][4];
   __shared__ float rs[4];
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();  // X comes from the previous kernel
+  pdl_trigger();
+  if (t >= rows) {  // the CTAs past the rows clear the next GEMM's output (zero_n4 float4s)
+    for (size_t i = static_cast<size_t>(t - rows) * blockDim.x + tid; i < zero_n4;
+         i += static_cast<size_t>(gridDim.x - rows) * blockDim.x)
+      zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
   const float* x = X + static_cast<size_t>(t) * H;
   const int gsz = H / groups;
   float ss[4] = {0.f, 0.f, 0.f, 0.f};
@@ -76,6 +90,7 @@ __global__ void norm_rows_kernel(const float* __restrict__ X, const WT* __restri
     split_bf16(y, hi, lo);
     oh[static_cast<size_t>(t) * H + i] = hi;
     ol[static_cast<size_t>(t) * H + i] = lo;
+    if (copy) copy[static_cast<size_t>(t) * H + i] = x[i];
   }
 }
 
@@ -495,6 +510,8 @@ __global__ void rope_batch_kernel(const float* __restrict__ packed, float* __res
                                   int D, int cap, unsigned* guard) {
   const int b = blockIdx.x;
   const int qkv_n = (nq + 2 * nkv) * D, half = D / 2;
+  pdl_wait();
+  pdl_trigger();
   int pos = seq_len[b];
   if (pos < 0 || pos >= cap) {
     if (threadIdx.x == 0) atomicOr(guard, GUARD_POS);
@@ -521,6 +538,8 @@ __global__ void swiglu_rows_kernel(const float* __restrict__ gu, __nv_bfloat16* 
                                    __nv_bfloat16* __restrict__ ol, int I) {
   const float* r = gu + static_cast<size_t>(blockIdx.y) * 2 * I;
   const size_t base = static_cast<size_t>(blockIdx.y) * I;
+  pdl_wait();
+  pdl_trigger();
   for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < I; p += gridDim.x * blockDim.x) {
     const float g = r[2 * p], u = r[2 * p + 1];
     __nv_bfloat16 hi, lo;
@@ -534,6 +553,8 @@ __global__ void swiglu_rows_kernel(const float* __restrict__ gu, __nv_bfloat16* 
 __global__ void rows_hilo_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ oh,
                                  __nv_bfloat16* __restrict__ ol, int K) {
   const size_t base = static_cast<size_t>(blockIdx.y) * K;
+  pdl_wait();
+  pdl_trigger();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < K; i += gridDim.x * blockDim.x) {
     __nv_bfloat16 hi, lo;
     split_bf16(x[base + i], hi, lo);
@@ -574,6 +595,8 @@ __global__ void argmax_part_kernel(const float* __restrict__ logits, int V, floa
   const int lo = static_cast<int>((static_cast<long long>(V) * chunk) / gridDim.x);
   const int hi = static_cast<int>((static_cast<long long>(V) * (chunk + 1)) / gridDim.x);
   const float* r = logits + static_cast<size_t>(row) * V;
+  pdl_wait();
+  pdl_trigger();
   float v = -INFINITY;
   int idx = 0x7fffffff;
   bool nan = false;
@@ -597,6 +620,8 @@ __global__ void argmax_final_kernel(const float* __restrict__ pv, const int* __r
                                     int* __restrict__ next) {
   __shared__ float sv[32];
   __shared__ int si[32];
+  pdl_wait();
+  pdl_trigger();
   float v = -INFINITY;
   int idx = 0x7fffffff;
   for (int c = threadIdx.x; c < chunks; c += blockDim.x)
@@ -633,25 +658,49 @@ cudaError_t prefill_init_attrs() {
   return e;
 }
 
+namespace {
+// A launch with programmatic dependent launch when `pdl` (the kernel waits for
+// its predecessor with griddepcontrol.wait before reading what it wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+}  // namespace
+
 cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbytes, float* X, int H, int vocab,
                               unsigned* guard, int* hist, int hist_stride, const int* pos, int pos0,
-                              const int* pos0_dev, cudaStream_t s) {
+                              const int* pos0_dev, cudaStream_t s, bool pdl) {
   if (wbytes == 2)
-    embed_rows_kernel<<<n, 256, 0, s>>>(tokens, static_cast<const __nv_bfloat16*>(E), X, H, vocab, guard, hist,
-                                        hist_stride, pos, pos0, pos0_dev);
-  else
-    embed_rows_kernel<<<n, 256, 0, s>>>(tokens, static_cast<const float*>(E), X, H, vocab, guard, hist, hist_stride,
-                                        pos, pos0, pos0_dev);
-  return cudaGetLastError();
+    return launch_k(embed_rows_kernel<__nv_bfloat16>, dim3(n), dim3(256), 0, s, pdl, tokens,
+                    static_cast<const __nv_bfloat16*>(E), X, H, vocab, guard, hist, hist_stride, pos, pos0, pos0_dev);
+  return launch_k(embed_rows_kernel<float>, dim3(n), dim3(256), 0, s, pdl, tokens, static_cast<const float*>(E), X, H,
+                  vocab, guard, hist, hist_stride, pos, pos0, pos0_dev);
 }
 
 cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes, __nv_bfloat16* oh,
-                             __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s) {
+                             __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s, bool pdl, float* zero,
+                             size_t zero_floats, float* copy) {
+  if (zero_floats % 4 || (zero_floats && reinterpret_cast<uintptr_t>(zero) % 16)) return cudaErrorInvalidValue;
+  const size_t n4 = zero_floats / 4;
+  // extra CTAs (up to one per 8192 float4s, at most 64) clear the next GEMM's output
+  const int zc = n4 ? static_cast<int>(std::min<size_t>(64, (n4 + 8191) / 8192)) : 0;
   if (wbytes == 2)
-    norm_rows_kernel<<<n, 512, 0, s>>>(X, static_cast<const __nv_bfloat16*>(gain), oh, ol, H, groups, eps);
-  else
-    norm_rows_kernel<<<n, 512, 0, s>>>(X, static_cast<const float*>(gain), oh, ol, H, groups, eps);
-  return cudaGetLastError();
+    return launch_k(norm_rows_kernel<__nv_bfloat16>, dim3(n + zc), dim3(512), 0, s, pdl, X,
+                    static_cast<const __nv_bfloat16*>(gain), oh, ol, H, groups, eps, n,
+                    reinterpret_cast<float4*>(zero), n4, copy);
+  return launch_k(norm_rows_kernel<float>, dim3(n + zc), dim3(512), 0, s, pdl, X, static_cast<const float*>(gain), oh,
+                  ol, H, groups, eps, n, reinterpret_cast<float4*>(zero), n4, copy);
 }
 
 cudaError_t launch_rope_append(const float* qkv, float* Q, const float2* rope, int kv_dtype, void* kc, void* vc,
@@ -705,29 +754,28 @@ cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, co
 }
 
 cudaError_t launch_rope_batch(const float* packed, float* nat, const float2* rope, const int* seq_len, int B, int nq,
-                              int nkv, int D, int cap, unsigned* guard, cudaStream_t s) {
-  rope_batch_kernel<<<B, 1024, 0, s>>>(packed, nat, rope, seq_len, nq, nkv, D, cap, guard);
-  return cudaGetLastError();
+                              int nkv, int D, int cap, unsigned* guard, cudaStream_t s, bool pdl) {
+  return launch_k(rope_batch_kernel, dim3(B), dim3(1024), 0, s, pdl, packed, nat, rope, seq_len, nq, nkv, D, cap, guard);
 }
 
-cudaError_t launch_swiglu_rows(const float* gu, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int I, cudaStream_t s) {
-  swiglu_rows_kernel<<<dim3((I + 255) / 256, rows), 256, 0, s>>>(gu, oh, ol, I);
-  return cudaGetLastError();
+cudaError_t launch_swiglu_rows(const float* gu, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int I, cudaStream_t s,
+                               bool pdl) {
+  return launch_k(swiglu_rows_kernel, dim3((I + 255) / 256, rows), dim3(256), 0, s, pdl, gu, oh, ol, I);
 }
 
-cudaError_t launch_rows_hilo(const float* x, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int K, cudaStream_t s) {
-  rows_hilo_kernel<<<dim3((K + 255) / 256, rows), 256, 0, s>>>(x, oh, ol, K);
-  return cudaGetLastError();
+cudaError_t launch_rows_hilo(const float* x, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int K, cudaStream_t s,
+                             bool pdl) {
+  return launch_k(rows_hilo_kernel, dim3((K + 255) / 256, rows), dim3(256), 0, s, pdl, x, oh, ol, K);
 }
 
 cudaError_t launch_argmax_rows(const float* logits, int rows, int V, int* next, float* part_val, int* part_idx,
-                               int part_stride, unsigned* guard, cudaStream_t s) {
+                               int part_stride, unsigned* guard, cudaStream_t s, bool pdl) {
   if (part_stride < kArgChunks) return cudaErrorInvalidValue;
-  argmax_part_kernel<<<dim3(kArgChunks, rows), 256, 0, s>>>(logits, V, part_val, part_idx, part_stride, guard);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_k(argmax_part_kernel, dim3(kArgChunks, rows), dim3(256), 0, s, pdl, logits, V, part_val,
+                           part_idx, part_stride, guard);
   if (e != cudaSuccess) return e;
-  argmax_final_kernel<<<rows, 64, 0, s>>>(part_val, part_idx, kArgChunks, part_stride, next);
-  return cudaGetLastError();
+  return launch_k(argmax_final_kernel, dim3(rows), dim3(64), 0, s, pdl, static_cast<const float*>(part_val),
+                  static_cast<const int*>(part_idx), static_cast<int>(kArgChunks), part_stride, next);
 }
 
 cudaError_t launch_advance_by(int* seq_len, int seq, int n, cudaStream_t s) {

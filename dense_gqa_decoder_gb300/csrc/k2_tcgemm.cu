@@ -267,20 +267,44 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
   tc_after();
   const uint32_t tmem = tmem_slot;
   if (threadIdx.x == 0) {  // TMA producer
-    long long g = g0;
-    int i = 0;
+    // Under programmatic dependent launch the weights of the first stages are
+    // requested before waiting for the previous kernel (they never depend on
+    // it); the activations of those stages follow once it has completed.
+    auto where = [&](long long gg, int& m0, int& n0, int& kk) {
+      const long long tile = gg / kpt;
+      const int k = static_cast<int>(gg - tile * kpt);
+      m0 = static_cast<int>(tile / tok_tiles) * BM;
+      n0 = static_cast<int>(tile % tok_tiles) * BN;
+      kk = k * BK;
+    };
+    const int pre = static_cast<int>(min(static_cast<long long>(STAGES), g1 - g0));
+    for (int j = 0; j < pre; ++j) {
+      int m0, n0, kk;
+      where(g0 + j, m0, n0, kk);
+      mbar_arrive_expect_tx(&full[j], STAGE_BYTES);
+      tma_4d(smem + j * STAGE_BYTES, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[j]);
+    }
+    pdl_wait();
+    pdl_trigger();
+    for (int j = 0; j < pre; ++j) {
+      int m0, n0, kk;
+      where(g0 + j, m0, n0, kk);
+      uint8_t* st = smem + j * STAGE_BYTES;
+      tma_2d(st + A_BYTES, &tmXh, kk, n0, &full[j]);
+      tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[j]);
+    }
+    long long g = g0 + pre;
+    int i = pre;
     for (; g < g1; ++g, ++i) {
       const int s = i % STAGES;
       if (i >= STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>((i / STAGES) - 1) & 1u)) {
         atomicOr(a.guard, GUARD_TIMEOUT);
         break;
       }
-      const long long tile = g / kpt;
-      const int k = static_cast<int>(g - tile * kpt);
-      const int m0 = static_cast<int>(tile / tok_tiles) * BM, n0 = static_cast<int>(tile % tok_tiles) * BN;
+      int m0, n0, kk;
+      where(g, m0, n0, kk);
       mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
       uint8_t* st = smem + s * STAGE_BYTES;
-      const int kk = k * BK;
       tma_4d(st, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
       tma_2d(st + A_BYTES, &tmXh, kk, n0, &full[s]);
       tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[s]);
@@ -321,6 +345,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
     }
   } else if (warp >= 2) {  // epilogue: drain each piece's accumulator
     const int lg = (warp & 3) * 32;  // the TMEM lanes (tile rows) this warp may read
+    pdl_wait();  // the output (residual or zeroed target) is the previous kernels'
     int piece = 0;
     long long g = g0;
     while (g < g1) {
@@ -447,7 +472,7 @@ cudaError_t tc_gemm_init_attrs() {
 }
 
 cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a, int ctas,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool pdl) {
   if (a.T <= 0) return cudaSuccess;
   if ((a.tile_tokens != 16 && a.tile_tokens != 128) || a.mode == TC_SWIGLU || ctas < 1) return cudaErrorInvalidValue;
   const int tt = a.tile_tokens;
@@ -457,9 +482,18 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* m
   const CUtensorMap& w = *static_cast<const CUtensorMap*>(mapW);
   const CUtensorMap& xh = *static_cast<const CUtensorMap*>(mapXh);
   const CUtensorMap& xl = *static_cast<const CUtensorMap*>(mapXl);
-  if (tt == 16) tc_gemm_sk_kernel<16><<<grid, 192, Tile<16>::SMEM_BYTES, s>>>(w, xh, xl, a);
-  else tc_gemm_sk_kernel<128><<<grid, 192, Tile<128>::SMEM_BYTES, s>>>(w, xh, xl, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = tt == 16 ? Tile<16>::SMEM_BYTES : Tile<128>::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (tt == 16) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<16>, w, xh, xl, a);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128>, w, xh, xl, a);
 }
 
 cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a,
