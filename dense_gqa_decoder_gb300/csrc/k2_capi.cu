@@ -281,7 +281,7 @@ struct k2_ctx {
   // persistent step: L2 look-ahead per phase kind (two slots at the gate/up and
   // down phases measured fastest at context 4096: 1.934 against 1.990 ms per
   // token without; deeper look-ahead, or look-ahead at the attention phase, was slower)
-  int l2_ahead = 2, l2_mask = 0x18, l2_lines = 0;
+  int l2_ahead = 2, l2_mask = 0x18;
   unsigned long long* trace = nullptr;               // persistent step: K2_OPT_TRACE buffer
   std::string err;
   // profiling: event pairs around the kernels of one step
@@ -487,7 +487,6 @@ void enqueue_token(k2_ctx* c, Launcher& ln, int seq, const int* tok, float* x_in
     m.stall_phase = c->stall_phase;
     m.l2_ahead = c->l2_ahead;
     m.l2_mask = c->l2_mask;
-    m.l2_lines = c->l2_lines;
     m.trace = c->trace;
     const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
     cudaStream_t st = ln.s;
@@ -1558,15 +1557,8 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
       c->poll_limit_ns = static_cast<unsigned long long>(value) * 1000ull;
       break;
     case K2_OPT_L2_AHEAD:
-      if (value < 0 || value > (c->l2_lines ? kMegaLineAhead : 64))
-        return c->fail(K2_ERR_ARG, "L2 look-ahead %lld outside [0, %d]", (long long)value, c->l2_lines ? kMegaLineAhead : 64);
+      if (value < 0 || value > 64) return c->fail(K2_ERR_ARG, "L2 look-ahead %lld outside [0, 64]", (long long)value);
       c->l2_ahead = static_cast<int>(value);
-      break;
-    case K2_OPT_L2_AHEAD_LINES:
-      if (value != 0 && value != 1) return c->fail(K2_ERR_ARG, "L2 look-ahead mode %lld is not 0 or 1", (long long)value);
-      if (value == 1 && c->l2_ahead > kMegaLineAhead)
-        return c->fail(K2_ERR_ARG, "line look-ahead covers at most %d slots", kMegaLineAhead);
-      c->l2_lines = static_cast<int>(value);
       break;
     case K2_OPT_L2_AHEAD_PHASES:
       if (value < 0 || value > 63) return c->fail(K2_ERR_ARG, "phase mask %lld outside [0, 63]", (long long)value);

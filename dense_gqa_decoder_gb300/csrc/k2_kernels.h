@@ -310,7 +310,6 @@ struct MegaArgs {
   // its input
   int l2_ahead;
   int l2_mask;
-  int l2_lines;  // 0: the look-ahead goes through the copy engine (bulk prefetch); 1: line prefetches of the warp
   // measurement: when set, thread 0 of every CTA stamps %globaltimer (ns) at
   // trace[(q * gridDim + cta) * 4 + k] for phase q: k = 0 phase start, 1 input
   // ready, 2 weight / K-V slots consumed, 3 phase end
@@ -335,7 +334,6 @@ constexpr int kMegaPairsMax = 64;             // row pairs of one CTA in the QKV
 constexpr int kMegaSplitMax = 64;             // key splits per KV head in the attention phase
 constexpr int kMegaTagShift = 10;
 constexpr int kMegaMaxLayers = 64;            // norm-gain pointers kept in shared memory
-constexpr int kMegaLineAhead = 6;             // slots of the line-prefetch look-ahead, at most
 // tag = (epoch + 1) << kMegaTagShift | phase: at most 1023 phases
 
 // Packed weight formats of the persistent step, the key that picks its

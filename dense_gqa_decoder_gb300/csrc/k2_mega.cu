@@ -190,9 +190,6 @@ struct MegaShared {
   int4 item;                        // this CTA's attention item: KV head, split, first key, end key
   const void* gains[2 * kMegaMaxLayers + 1];  // attn_norm[l] at 2l, mlp_norm[l] at 2l + 1, final last
   float newkv[2][128];              // the new token's K and V rows (head_dim <= 128)
-  const uint8_t* pf_addr[MW][2 * kMegaLineAhead];  // line look-ahead: ranges a warp fetches into L2
-  uint32_t pf_bytes[MW][2 * kMegaLineAhead];
-  int pf_n[MW];
 };
 
 // ---- static description of the step ------------------------------------------------
@@ -433,36 +430,6 @@ struct Stream {
     }
   }
 
-  // the byte ranges issue_next would copy next, listed (on a copy of the
-  // stream: the real one is not advanced); returns the new count
-  __device__ int list_next(const MegaArgs& a, int cta, int G, int warp, int pos, int qkv_n, const uint8_t** addr,
-                           uint32_t* bytes, int n_have) {
-    if (done) return n_have;
-    if (attn) {
-      const int rows = min(TKM, k1 - j0);
-      const int crow = max(0, min(rows, pos - j0));
-      if (crow > 0) {
-        addr[n_have] = kb + static_cast<size_t>(j0) * ROWB;
-        bytes[n_have++] = crow * ROWB;
-        addr[n_have] = vb + static_cast<size_t>(j0) * ROWB;
-        bytes[n_have++] = crow * ROWB;
-      }
-      j0 += MW * TKM;
-    } else {
-      const int nu = min(SU, left);
-      addr[n_have] = src;
-      bytes[n_have++] = static_cast<uint32_t>(nu) * UB;
-      src += static_cast<size_t>(nu) * UB;
-      left -= nu;
-    }
-    ++issued;
-    if (++k >= n) {
-      n = 0;
-      next_phase(a, cta, G, warp, pos, qkv_n);
-    }
-    return n_have;
-  }
-
   // what issue_next would copy next, asked of L2 instead (on a copy of the
   // stream: the real one is not advanced)
   __device__ void prefetch_next(const MegaArgs& a, int cta, int G, int warp, int pos, int qkv_n) {
@@ -488,17 +455,6 @@ struct Stream {
     }
   }
 };
-
-// The byte ranges of the next `count` slots of a warp's stream beyond those in
-// flight (the producer lane, once per phase): the whole warp then fetches their
-// lines into L2.
-template <int UB, int D, typename KVT>
-__device__ __noinline__ int stream_list(Stream<UB, D, KVT> s, const MegaArgs& a, int cta, int G, int warp, int pos,
-                                        int qkv_n, int count, const uint8_t** addr, uint32_t* bytes) {
-  int n = 0;
-  for (int i = 0; i < count && !s.done; ++i) n = s.list_next(a, cta, G, warp, pos, qkv_n, addr, bytes, n);
-  return n;
-}
 
 // The next `count` slots of a warp's stream beyond those in flight, fetched
 // into L2 (called by the producer lane once per phase, off the hot loop).
@@ -1446,21 +1402,8 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const __grid_constan
     uint32_t tag_in = tagbase | static_cast<uint32_t>(q - 1);
     const uint32_t tag_out = tagbase | static_cast<uint32_t>(q);
     if (q == a.stall_phase) tag_in = tagbase | ((1u << kMegaTagShift) - 1u);  // no phase has this number
-    if (a.l2_ahead > 0 && ((a.l2_mask >> (l < a.n_layers ? j : 5)) & 1)) {
-      if (!a.l2_lines) {
-        if (lane == 0) stream_prefetch(st, a, cta, G, warp, pos, qkv_n, a.l2_ahead);
-      } else {
-        if (lane == 0)
-          sh.pf_n[warp] = stream_list(st, a, cta, G, warp, pos, qkv_n, min(a.l2_ahead, kMegaLineAhead),
-                                      sh.pf_addr[warp], sh.pf_bytes[warp]);
-        __syncwarp();
-        for (int e = 0; e < sh.pf_n[warp]; ++e) {
-          const uint8_t* p = sh.pf_addr[warp][e];
-          const uint32_t nb = sh.pf_bytes[warp][e];
-          for (uint32_t off = static_cast<uint32_t>(lane) * 128u; off < nb; off += 32u * 128u) prefetch_line_l2(p + off);
-        }
-      }
-    }
+    if (lane == 0 && a.l2_ahead > 0 && ((a.l2_mask >> (l < a.n_layers ? j : 5)) & 1))
+      stream_prefetch(st, a, cta, G, warp, pos, qkv_n, a.l2_ahead);
     trace_mark(a, q, 0);
     if (l < a.n_layers && j == PH_ATTN) {
       ok = a_phase<WT, D, REP>(a, l, pos, tag_in, tag_out, smem, sh, st, consumed, cta, G, qkv_n);
