@@ -260,6 +260,9 @@ struct k2_ctx {
   int mega_grid = 0;
   MegaArgs mega = {};
   KvMaps mega_maps = {};  // the persistent step's tensor maps of the caches (tensor-core attention)
+  KvMaps pf_maps = {};    // the tcgen05 prefill attention's tensor maps of the caches (64-row boxes)
+  bool pf_tc = false;     // fp16 cache of a supported shape: prefill attention on tcgen05
+  bool use_pf_tc = true;  // option K2_OPT_PREFILL_ATTN
   std::vector<LayerPtrs> ltab;
   // tensor-core prefill: TMA tensor maps (weights per layer: qkv, o, gate/up,
   // down; activations: normed input, attention output, SwiGLU output, hi/lo)
@@ -859,6 +862,21 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
       attn_maps(c, at, l);
       e = launch_attn(at, s.d, s.rep, kvdt, attn_splits(c, n), n, st, false);
       if (!e) e = launch_rows_hilo(O32, xh, xl, n, s.nq * s.d, st);
+    } else if (!e && c->pf_tc && c->use_pf_tc) {
+      PrefillAttnArgs pa = {};
+      pa.Q = Q;
+      pa.oh = xh;
+      pa.ol = xl;
+      pa.n = n;
+      pa.nq = s.nq;
+      pa.nkv = s.nkv;
+      pa.pos0 = pos0;
+      pa.head_row0 = static_cast<int>(head_row0);
+      pa.cap = c->lay.cap;
+      pa.layer = l;
+      pa.scale = scale;
+      pa.guard = c->guard;
+      e = launch_prefill_attn_tc(c->pf_maps, pa, s.d, s.rep, st);
     } else if (!e) {
       e = launch_prefill_attn(Q, kvdt, c->kc(l), c->vc(l), c->ks(l), c->vs(l), xh, xl, n, s.nq, s.nkv, s.d, pos0,
                               head_row0, c->lay.cap, scale, st);
@@ -1219,6 +1237,11 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     delete c;
     return K2_ERR_UNSUPPORTED;
   }
+  if (cfg->kv_dtype == K2_F16 && prefill_attn_tc_supported(c->s.d, c->s.rep)) {
+    const long long rows = static_cast<long long>(c->s.B) * c->s.nkv * c->lay.cap;
+    c->pf_tc = attn_encode_kv_layers(&c->pf_maps.k, c->kc(0), rows, c->s.d, c->s.L, c->lay.kv_layer, 64) &&
+               attn_encode_kv_layers(&c->pf_maps.v, c->vc(0), rows, c->s.d, c->s.L, c->lay.kv_layer, 64);
+  }
   if (cfg->kv_dtype == K2_F16 && attn_tc_supported(c->s.d, c->s.rep)) {
     c->tm_k.resize(c->s.L);
     c->tm_v.resize(c->s.L);
@@ -1564,6 +1587,7 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
       if (value < 0 || value > 63) return c->fail(K2_ERR_ARG, "phase mask %lld outside [0, 63]", (long long)value);
       c->l2_mask = static_cast<int>(value);
       break;
+    case K2_OPT_PREFILL_ATTN: c->use_pf_tc = value != 0; break;
     case K2_OPT_TRACE:
       if (value < 0 || value % 8) return c->fail(K2_ERR_ARG, "trace buffer must be 8-byte aligned (or 0)");
       c->trace = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));

@@ -402,6 +402,27 @@ cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapX
 // the kernel waits for its predecessor (weights never depend on an earlier kernel)
 cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a, int ctas,
                               cudaStream_t s, bool pdl = false);
+// Causal prefill attention on the tensor cores (tcgen05, fp16 caches): the n
+// query tokens of a block at positions pos0 .. pos0 + n - 1 (Q [n][nq * D] fp32,
+// rotated) against every cached key of their sequence up to their own position,
+// through `maps` (the K and V caches of every layer, boxes of 64 dims x 64 rows);
+// the attention output goes to oh / ol [n][nq * D] as bf16 hi / lo halves.
+struct PrefillAttnArgs {
+  const float* Q;
+  __nv_bfloat16* oh;
+  __nv_bfloat16* ol;
+  int n, nq, nkv;
+  int pos0;
+  int head_row0;  // cache row of key 0 of KV head 0 of the sequence (KV head g at + g * cap)
+  int cap;
+  int layer;
+  float scale;
+  unsigned* guard;
+};
+bool prefill_attn_tc_supported(int head_dim, int rep);
+cudaError_t prefill_attn_tc_init_attrs();
+cudaError_t launch_prefill_attn_tc(const KvMaps& maps, const PrefillAttnArgs& a, int head_dim, int rep,
+                                   cudaStream_t s);
 bool prefill_attn_supported(int head_dim, int rep);
 cudaError_t prefill_init_attrs();
 // hist (nullable): row t's token is recorded at hist[t * hist_stride + pos[t]], or at

@@ -655,6 +655,7 @@ cudaError_t prefill_init_attrs() {
   K2_PREFILL_ATTN_SHAPES(K2_PA_ATTR)
 #undef K2_PA_ATTR
   if (!e) e = tc_gemm_init_attrs();
+  if (!e) e = prefill_attn_tc_init_attrs();
   return e;
 }
 

@@ -405,6 +405,305 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
+// ---- causal prefill attention on the 5th-generation tensor cores -------------------------------
+// One CTA takes 128 query rows -- 128 / REP tokens x the REP query heads of one
+// KV head -- and walks the cached keys 0 .. (its last position) in tiles of 64:
+//   S = Q.K^T   (tcgen05.mma M=128 N=64, S in TMEM): Q as fp16 hi + lo halves
+//               (two MMAs per k-step: ~22 bits of every query), K the fp16 cache;
+//   softmax     thread r owns row r (TMEM lane r): tcgen05.ld of its 64 scores,
+//               causal mask, running maximum; P = exp(s - m) as fp16 hi + lo
+//               rows into shared memory;
+//   O += P.V^T  (tcgen05.mma M=128 N=D, O in TMEM).
+// Every operand is K-major with the 128-byte swizzle (the layout of the GEMMs'
+// descriptors): Q and P are written so by the threads, K arrives so by TMA, and
+// V (TMA rows [key][dim]) is transposed into [dim][key] with ldmatrix.trans /
+// stmatrix.  The running maximum of a row only moves when a tile's maximum
+// exceeds it by more than kRescaleLog (then O and the sum are rescaled in
+// TMEM); otherwise p = exp(s - m) may exceed 1 (at most e^kRescaleLog, exact in
+// fp16 range) and the final division by the sum makes the result exact anyway.
+// K/V tiles are double-buffered: the tile after next is requested as soon as a
+// stage is consumed.
+constexpr int kPaRows = 128, kPaKeys = 64, kPaThreads = 128;
+constexpr float kRescaleLog = 8.0f;
+
+template <int D>
+struct PaSmem {
+  static constexpr int NA = D / 64;                   // 64-dim swizzle atoms per row
+  static constexpr int Q = kPaRows * 128;             // one atom of the 128 query rows (16 KB)
+  static constexpr int KT = kPaKeys * 128;            // one atom of a 64-key K (or V) tile (8 KB)
+  static constexpr int STAGE = 2 * NA * KT;           // K and V of one tile
+  static constexpr int OFF_QH = 0, OFF_QL = OFF_QH + NA * Q;
+  static constexpr int OFF_ST = OFF_QL + NA * Q;      // two stages
+  static constexpr int OFF_VT = OFF_ST + 2 * STAGE;   // V^T [D][64 keys]
+  static constexpr int OFF_PH = OFF_VT + D * 128;     // P hi [128][64 keys]
+  static constexpr int OFF_PL = OFF_PH + kPaRows * 128;
+  static constexpr int BYTES = OFF_PL + kPaRows * 128;
+  static constexpr int DYN = BYTES + 1024;            // + alignment to 1024 B
+  static constexpr int TMEM_COLS = D + 64 <= 128 ? 128 : 256;  // O [D] then S [64]
+  // instruction descriptors (kind::f16): fp16 A and B, fp32 D, K-major, M = 128
+  static constexpr uint32_t IDESC_S = (1u << 4) | (static_cast<uint32_t>(kPaKeys >> 3) << 17) | (8u << 24);
+  static constexpr uint32_t IDESC_O = (1u << 4) | (static_cast<uint32_t>(D >> 3) << 17) | (8u << 24);
+};
+
+// byte offset of element (row r, column e) in a K-major 128-byte-swizzled block of 64 columns
+__device__ __forceinline__ uint32_t sw128(int r, int e) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((((e >> 3) ^ (r & 7)) & 7) << 4) + (e & 7) * 2);
+}
+__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* m, int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          smem_u32(dst)),
+      "l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int D, int REP>
+__global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __grid_constant__ KvMaps maps,
+                                                                        const PrefillAttnArgs a) {
+  using Sm = PaSmem<D>;
+  constexpr int NA = Sm::NA;
+  constexpr int QT = kPaRows / REP;  // tokens per CTA
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full[2], sbar, obar;
+  __shared__ uint32_t tmem_slot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * QT, g = blockIdx.y;
+  const int nt = min(QT, a.n - t0);
+  const int tq = tid / REP, hh = tid - tq * REP;  // this thread's row: token t0 + tq, query head g * REP + hh
+  const bool row_ok = tq < nt;
+  const int qpos = a.pos0 + t0 + tq;              // the row's position: it sees keys 0 .. qpos
+  const int kend = a.pos0 + t0 + nt;              // keys of the CTA: 0 .. kend - 1
+  const int nkt = (kend + kPaKeys - 1) / kPaKeys;
+  const int krow0 = a.head_row0 + g * a.cap;      // tensor row of key 0 of this KV head
+
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(&sbar, 1);
+    mbar_init(&obar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(Sm::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // this row of Q (pre-scaled by 1 / sqrt(D)) as fp16 hi + lo, swizzled
+  {
+    const float* q = a.Q + static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D;
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = row_ok ? q[8 * c + e] * a.scale : 0.f;
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split_half2(v[2 * e], v[2 * e + 1], hi[e], lo[e]);
+      const uint32_t off = (c >> 3) * Sm::Q + sw128(tid, 8 * (c & 7));
+      *reinterpret_cast<uint4*>(smem + Sm::OFF_QH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(smem + Sm::OFF_QL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+  }
+  fence_proxy_async();  // generic stores (Q) before the MMAs read them
+  auto issue_tile = [&](int kt) {
+    const int st = kt & 1;
+    uint8_t* base = smem + Sm::OFF_ST + st * Sm::STAGE;
+    mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(Sm::STAGE));
+#pragma unroll
+    for (int at = 0; at < NA; ++at) {
+      tma_3d(base + at * Sm::KT, &maps.k, 64 * at, krow0 + kt * kPaKeys, a.layer, &full[st]);
+      tma_3d(base + (NA + at) * Sm::KT, &maps.v, 64 * at, krow0 + kt * kPaKeys, a.layer, &full[st]);
+    }
+  };
+  if (tid == 0) {
+    if (nkt > 0) issue_tile(0);
+    if (nkt > 1) issue_tile(1);
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t t_o = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's lanes, O at column 0
+  const uint32_t t_s = t_o + D;                                            // S at column D
+
+  float m_ref = -INFINITY, l_sum = 0.f;
+  bool bad = false;
+  int kt = 0, s_issued = 0, o_issued = 0;
+  for (; kt < nkt; ++kt) {
+    const int st = kt & 1;
+    const uint8_t* kst = smem + Sm::OFF_ST + st * Sm::STAGE;
+    const uint8_t* vst = kst + NA * Sm::KT;
+    if (!mbar_wait(&full[st], static_cast<uint32_t>(kt >> 1) & 1u)) bad = true;
+    if (__syncthreads_or(bad)) break;
+    if (tid == 0) {  // S = Q.K^T (hi and lo halves of Q)
+      tc_after();
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        const uint64_t kd = smem_desc(kst + (j >> 2) * Sm::KT + (j & 3) * 32);
+        mma(t_s, smem_desc(smem + Sm::OFF_QH + (j >> 2) * Sm::Q + (j & 3) * 32), kd, Sm::IDESC_S, j > 0 ? 1u : 0u);
+        mma(t_s, smem_desc(smem + Sm::OFF_QL + (j >> 2) * Sm::Q + (j & 3) * 32), kd, Sm::IDESC_S, 1u);
+      }
+      mma_commit(&sbar);
+    }
+    ++s_issued;
+    // the previous tile's P.V must be done before V^T, P and O are touched
+    if (kt > 0 && !mbar_wait(&obar, static_cast<uint32_t>(kt - 1) & 1u)) bad = true;
+    // V^T [dim][key] from the V rows [key][dim]: 8x8 blocks, transposed on the
+    // way through registers; keys past the CTA's last one become zeros
+    {
+      const int kvalid = kend - kt * kPaKeys;
+      constexpr int NBLK = (kPaKeys / 8) * (D / 8);
+      for (int bi = warp * 4; bi < NBLK; bi += 4 * (kPaThreads / 32)) {
+        const int m = lane >> 3, r8 = lane & 7;
+        const int blk = bi + m, kb = blk / (D / 8), db = blk - kb * (D / 8);
+        const int key = 8 * kb + r8;
+        uint32_t r[4];
+        ldsm_x4_t(smem_u32(vst + (db >> 3) * Sm::KT + sw128(key, 8 * (db & 7))), r[0], r[1], r[2], r[3]);
+        // lane (gq, tq) holds keys 8kb' + 2tq, +1 of dim 8db' + gq for each of the 4 blocks
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int kbi = (bi + i) / (D / 8);
+          const int k0i = 8 * kbi + 2 * (lane & 3);
+          uint32_t w = r[i];
+          if (k0i >= kvalid) w &= 0u;
+          else if (k0i + 1 >= kvalid) w &= 0x0000FFFFu;
+          r[i] = w;
+        }
+        const int dim = 8 * db + r8;
+        stsm_x4(smem_u32(smem + Sm::OFF_VT + sw128(dim, 8 * kb)), r[0], r[1], r[2], r[3]);
+      }
+    }
+    // this row's scores
+    if (!mbar_wait(&sbar, static_cast<uint32_t>(kt) & 1u)) bad = true;
+    tc_after();
+    float sv[kPaKeys];
+    {
+      uint32_t raw[32];
+#pragma unroll
+      for (int h = 0; h < kPaKeys / 32; ++h) {
+        tmem_ld32(t_s + 32 * h, raw);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[32 * h + j] = __uint_as_float(raw[j]);
+      }
+    }
+    float mt = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kPaKeys; ++j) {
+      const bool vis = row_ok && kt * kPaKeys + j <= qpos;
+      sv[j] = vis ? sv[j] : -INFINITY;
+      mt = fmaxf(mt, sv[j]);
+    }
+    // the reference maximum moves only when a tile's maximum exceeds it by kRescaleLog
+    const bool move = row_ok && mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog);
+    const float alpha = move ? (m_ref == -INFINITY ? 0.f : expf(m_ref - mt)) : 1.f;
+    if (move) {
+      l_sum *= alpha;
+      m_ref = mt;
+    }
+    if (kt > 0 && __any_sync(0xffffffffu, move)) {  // O *= alpha in TMEM (a warp-wide access)
+      uint32_t ov[32];
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        tmem_ld32(t_o + c, ov);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+        tmem_st32(t_o + c, ov);
+      }
+    }
+    // P = exp(s - m_ref) as fp16 hi + lo rows
+    float ps = 0.f;
+#pragma unroll
+    for (int c = 0; c < kPaKeys / 8; ++c) {
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p0 = sv[8 * c + 2 * e] == -INFINITY ? 0.f : expf(sv[8 * c + 2 * e] - m_ref);
+        const float p1 = sv[8 * c + 2 * e + 1] == -INFINITY ? 0.f : expf(sv[8 * c + 2 * e + 1] - m_ref);
+        ps += p0 + p1;
+        split_half2(p0, p1, hi[e], lo[e]);
+      }
+      *reinterpret_cast<uint4*>(smem + Sm::OFF_PH + sw128(tid, 8 * c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(smem + Sm::OFF_PL + sw128(tid, 8 * c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    l_sum += ps;
+    fence_proxy_async();  // P and V^T (generic stores) before the MMAs read them
+    tc_before();
+    if (__syncthreads_or(bad)) break;
+    if (tid == 0) {  // O += P.V^T (hi and lo halves of P)
+      tc_after();
+#pragma unroll
+      for (int j = 0; j < kPaKeys / 16; ++j) {
+        const uint64_t vd = smem_desc(smem + Sm::OFF_VT + j * 32);
+        mma(t_o, smem_desc(smem + Sm::OFF_PH + j * 32), vd, Sm::IDESC_O, (kt > 0 || j > 0) ? 1u : 0u);
+        mma(t_o, smem_desc(smem + Sm::OFF_PL + j * 32), vd, Sm::IDESC_O, 1u);
+      }
+      mma_commit(&obar);
+      // this stage is consumed (S done, V transposed): the tile after next goes there
+      if (kt + 2 < nkt) issue_tile(kt + 2);
+    }
+    ++o_issued;
+  }
+  if (bad) {
+    if (tid == 0) atomicOr(a.guard, GUARD_TIMEOUT);
+    // copies and MMAs still in flight end before the CTA's memory goes away (bounded waits)
+    if (tid == 0)
+      for (int k = kt; k < min(nkt, kt + 2); ++k) (void)mbar_wait(&full[k & 1], static_cast<uint32_t>(k >> 1) & 1u);
+    if (s_issued > 0) (void)mbar_wait(&sbar, static_cast<uint32_t>(s_issued - 1) & 1u);
+  }
+  const bool have_o = o_issued > 0 && mbar_wait(&obar, static_cast<uint32_t>(o_issued - 1) & 1u);
+  tc_after();
+  if (!bad && have_o) {
+    // the row: O / sum, as bf16 hi + lo
+    const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+    __nv_bfloat16* oh = a.oh + static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D;
+    __nv_bfloat16* ol = a.ol + static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D;
+#pragma unroll 1
+    for (int c = 0; c < D; c += 32) {
+      uint32_t ov[32];
+      tmem_ld32(t_o + c, ov);
+      if (row_ok) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          __nv_bfloat16 h0, l0, h1, l1;
+          split_bf16(__uint_as_float(ov[j]) * inv, h0, l0);
+          split_bf16(__uint_as_float(ov[j + 1]) * inv, h1, l1);
+          *reinterpret_cast<__nv_bfloat162*>(oh + c + j) = __nv_bfloat162(h0, h1);
+          *reinterpret_cast<__nv_bfloat162*>(ol + c + j) = __nv_bfloat162(l0, l1);
+        }
+      }
+    }
+  } else if (tid == 0 && !bad && o_issued > 0) {
+    atomicOr(a.guard, GUARD_TIMEOUT);
+  }
+  tc_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Sm::TMEM_COLS) : "memory");
+}
+
 }  // namespace
 
 bool tc_encode_weight(void* map, const void* packed, int N, int K) {
@@ -457,6 +756,29 @@ bool attn_encode_kv_layers(void* map, const void* base, long long rows, int head
   return enc(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims,
              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool prefill_attn_tc_supported(int head_dim, int rep) { return (head_dim == 64 || head_dim == 128) && rep == 4; }
+
+cudaError_t prefill_attn_tc_init_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(prefill_attn_tc_kernel<128, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PaSmem<128>::DYN);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_attn_tc_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PaSmem<64>::DYN);
+  return e;
+}
+
+cudaError_t launch_prefill_attn_tc(const KvMaps& maps, const PrefillAttnArgs& a, int head_dim, int rep,
+                                   cudaStream_t s) {
+  if (a.n <= 0) return cudaSuccess;
+  if (!prefill_attn_tc_supported(head_dim, rep)) return cudaErrorInvalidValue;
+  const dim3 grid((a.n + kPaRows / rep - 1) / (kPaRows / rep), a.nkv);
+  if (head_dim == 128)
+    prefill_attn_tc_kernel<128, 4><<<grid, kPaThreads, PaSmem<128>::DYN, s>>>(maps, a);
+  else
+    prefill_attn_tc_kernel<64, 4><<<grid, kPaThreads, PaSmem<64>::DYN, s>>>(maps, a);
+  return cudaGetLastError();
 }
 
 cudaError_t tc_gemm_init_attrs() {

@@ -396,12 +396,15 @@ typedef enum {
                              of its next weight / K-V slots beyond those in flight (0 .. 64; default 2) */
   K2_OPT_L2_AHEAD_PHASES = 9, /* the phase kinds that do so, bit j for kind j (0 QKV, 1 attention, 2 o_proj,
                              3 gate/up, 4 down, 5 lm_head); default 0x18: gate/up, down */
-  K2_OPT_TRACE = 10       /* measurement: the device address (as an integer; 0 = off) of a caller's buffer of
+  K2_OPT_TRACE = 10,      /* measurement: the device address (as an integer; 0 = off) of a caller's buffer of
                              (5 * n_layers + 2) * persistent_grid * 4 uint64 words; each persistent step then
                              writes, per phase q and CTA c, the SM's %clock64 at [(q * grid + c) * 4 + k]:
                              k = 0 phase start, 1 input ready, 2 slots consumed, 3 phase end; and at
                              [((5 * n_layers + 1) * grid + c) * 4 + {0, 1}] the %globaltimer ns and the
                              %clock64 of the CTA's start, which align the SMs' clocks */
+  K2_OPT_PREFILL_ATTN = 11 /* prefill attention of fp16 caches (head_dim 64 / 128, 4 query heads per KV head):
+                             1 (default) on the 5th-generation tensor cores (tcgen05, S and O in tensor
+                             memory), 0 on mma.sync */
 } k2_option;
 k2_status k2_set_option(k2_ctx* ctx, int32_t option, int64_t value);
 

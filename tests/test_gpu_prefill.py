@@ -172,3 +172,29 @@ def test_short_prompts_through_the_small_block_path(k2, mio, n):
         assert ctx.sync_status() == k2.K2_OK
     assert out[True][0] == out[False][0]
     assert rel_l2(out[True][1], out[False][1]) <= 1e-4
+
+
+@pytest.mark.parametrize("shape,first,n", [("k2_layer", 50, 1000), ("medium", 0, 333), ("medium", 129, 64)])
+def test_tcgen05_prefill_attention_against_mma_sync_and_oracle(k2, mio, shape, first, n):
+    """The prefill attention on the 5th-generation tensor cores (option
+    K2_OPT_PREFILL_ATTN = 1, the default for fp16 caches) against the mma.sync
+    kernel (= 0) and the oracle's full recompute: a prompt after `first` cached
+    rows, so query blocks start mid-tile and the last key tile is partial."""
+    s = ki.SHAPES[shape]
+    pre = ki.prompt_ids(s.vocab, first, seed=91) if first else None
+    prompt = ki.prompt_ids(s.vocab, n, seed=92)
+    out = {}
+    for tc_attn in (1, 0):
+        ctx, host = mio.build_context(s, max_context=first + n + 8, kv_dtype="f16", gain_scale=0.1, keep_host=True)
+        ctx.set_option(k2.K2_OPT_PREFILL_ATTN, tc_attn)
+        if pre is not None:
+            prefill(k2, ctx, pre, s.vocab, True)
+        out[tc_attn] = prefill(k2, ctx, prompt, s.vocab, True)
+        assert ctx.sync_status() == k2.K2_OK
+    seq = prompt if pre is None else np.concatenate([pre, prompt])
+    ref = O.OracleModel(s, lambda nm, l: host[(nm, l)], "f16").forward_full(seq)
+    (t1, l1), (t0, l0) = out[1], out[0]
+    assert rel_l2(l1, ref) <= 2e-4
+    assert rel_l2(l0, ref) <= 2e-4
+    assert rel_l2(l1, l0) <= 1e-4
+    assert t1 == t0 == O.argmax_first(ref)
