@@ -410,20 +410,24 @@ EncodeTiled encode_fn() {
 // KV head -- and walks the cached keys 0 .. (its last position) in tiles of 64:
 //   S = Q.K^T   (tcgen05.mma M=128 N=64, S in TMEM): Q as fp16 hi + lo halves
 //               (two MMAs per k-step: ~22 bits of every query), K the fp16 cache;
-//   softmax     thread r owns row r (TMEM lane r): tcgen05.ld of its 64 scores,
-//               causal mask, running maximum; P = exp(s - m) as fp16 hi + lo
-//               rows into shared memory;
+//   softmax     row r (TMEM lane r) is shared by the two warps that may read
+//               lane group r / 32: each takes 32 of the tile's 64 scores
+//               (tcgen05.ld), the two exchange their maxima through shared
+//               memory, and write their halves of P = exp(s - m) as fp16 hi + lo;
 //   O += P.V^T  (tcgen05.mma M=128 N=D, O in TMEM).
 // Every operand is K-major with the 128-byte swizzle (the layout of the GEMMs'
 // descriptors): Q and P are written so by the threads, K arrives so by TMA, and
 // V (TMA rows [key][dim]) is transposed into [dim][key] with ldmatrix.trans /
-// stmatrix.  The running maximum of a row only moves when a tile's maximum
-// exceeds it by more than kRescaleLog (then O and the sum are rescaled in
-// TMEM); otherwise p = exp(s - m) may exceed 1 (at most e^kRescaleLog, exact in
-// fp16 range) and the final division by the sum makes the result exact anyway.
+// stmatrix.  The tensor pipe never waits for the softmax: S of the next tile is
+// issued (into the other of two S buffers) before this tile's softmax, and P,
+// V^T are double-buffered, so P.V of one tile overlaps the next one's softmax.
+// A row's reference maximum only moves when a tile's maximum exceeds it by
+// more than kRescaleLog (then O and the row's sums are rescaled in TMEM);
+// otherwise p = exp(s - m) may exceed 1 (at most e^kRescaleLog, well inside
+// fp16), and the final division by the sum makes the result exact anyway.
 // K/V tiles are double-buffered: the tile after next is requested as soon as a
 // stage is consumed.
-constexpr int kPaRows = 128, kPaKeys = 64, kPaThreads = 128;
+constexpr int kPaRows = 128, kPaKeys = 64, kPaThreads = 256;
 constexpr float kRescaleLog = 8.0f;
 
 template <int D>
@@ -432,14 +436,15 @@ struct PaSmem {
   static constexpr int Q = kPaRows * 128;             // one atom of the 128 query rows (16 KB)
   static constexpr int KT = kPaKeys * 128;            // one atom of a 64-key K (or V) tile (8 KB)
   static constexpr int STAGE = 2 * NA * KT;           // K and V of one tile
+  static constexpr int VT = D * 128;                  // V^T [D][64 keys]
+  static constexpr int P = kPaRows * 128;             // P [128][64 keys] (one half)
   static constexpr int OFF_QH = 0, OFF_QL = OFF_QH + NA * Q;
   static constexpr int OFF_ST = OFF_QL + NA * Q;      // two stages
-  static constexpr int OFF_VT = OFF_ST + 2 * STAGE;   // V^T [D][64 keys]
-  static constexpr int OFF_PH = OFF_VT + D * 128;     // P hi [128][64 keys]
-  static constexpr int OFF_PL = OFF_PH + kPaRows * 128;
-  static constexpr int BYTES = OFF_PL + kPaRows * 128;
+  static constexpr int OFF_VT = OFF_ST + 2 * STAGE;   // two V^T buffers
+  static constexpr int OFF_P = OFF_VT + 2 * VT;       // two buffers of P hi, P lo
+  static constexpr int BYTES = OFF_P + 4 * P;
   static constexpr int DYN = BYTES + 1024;            // + alignment to 1024 B
-  static constexpr int TMEM_COLS = D + 64 <= 128 ? 128 : 256;  // O [D] then S [64]
+  static constexpr int TMEM_COLS = D + 128 <= 128 ? 128 : 256;  // O [D], then S [64] x 2
   // instruction descriptors (kind::f16): fp16 A and B, fp32 D, K-major, M = 128
   static constexpr uint32_t IDESC_S = (1u << 4) | (static_cast<uint32_t>(kPaKeys >> 3) << 17) | (8u << 24);
   static constexpr uint32_t IDESC_O = (1u << 4) | (static_cast<uint32_t>(D >> 3) << 17) | (8u << 24);
@@ -472,10 +477,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
-  const __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
 
 template <int D, int REP>
 __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __grid_constant__ KvMaps maps,
@@ -483,15 +484,19 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   using Sm = PaSmem<D>;
   constexpr int NA = Sm::NA;
   constexpr int QT = kPaRows / REP;  // tokens per CTA
+  constexpr int DH = D / 2;          // O columns per half
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t full[2], sbar, obar;
+  __shared__ __align__(8) uint64_t full[2], sbar[2], obar[2];
   __shared__ uint32_t tmem_slot;
+  __shared__ float xmax[2][kPaRows];  // each half's tile maximum per row
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = (warp & 3) * 32 + lane;  // TMEM lane = query row
+  const int hf = warp >> 2;                // which 32 of the 64 scores (and half of O) this thread takes
   const int t0 = blockIdx.x * QT, g = blockIdx.y;
   const int nt = min(QT, a.n - t0);
-  const int tq = tid / REP, hh = tid - tq * REP;  // this thread's row: token t0 + tq, query head g * REP + hh
+  const int tq = row / REP, hh = row - tq * REP;  // token t0 + tq, query head g * REP + hh
   const bool row_ok = tq < nt;
   const int qpos = a.pos0 + t0 + tq;              // the row's position: it sees keys 0 .. qpos
   const int kend = a.pos0 + t0 + nt;              // keys of the CTA: 0 .. kend - 1
@@ -499,10 +504,11 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   const int krow0 = a.head_row0 + g * a.cap;      // tensor row of key 0 of this KV head
 
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
-    mbar_init(&sbar, 1);
-    mbar_init(&obar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&sbar[b], 1);
+      mbar_init(&obar[b], 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -511,18 +517,19 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // this row of Q (pre-scaled by 1 / sqrt(D)) as fp16 hi + lo, swizzled
+  // this row's half of Q (pre-scaled by 1 / sqrt(D)) as fp16 hi + lo, swizzled
   {
     const float* q = a.Q + static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D;
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
+    for (int cc = 0; cc < D / 16; ++cc) {
+      const int c = hf * (D / 16) + cc;  // 8-dim chunk
       float v[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = row_ok ? q[8 * c + e] * a.scale : 0.f;
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) split_half2(v[2 * e], v[2 * e + 1], hi[e], lo[e]);
-      const uint32_t off = (c >> 3) * Sm::Q + sw128(tid, 8 * (c & 7));
+      const uint32_t off = (c >> 3) * Sm::Q + sw128(row, 8 * (c & 7));
       *reinterpret_cast<uint4*>(smem + Sm::OFF_QH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(smem + Sm::OFF_QL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
@@ -546,34 +553,54 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   __syncthreads();
   tc_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t t_o = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's lanes, O at column 0
-  const uint32_t t_s = t_o + D;                                            // S at column D
+  // thread 0: S of tile kt = Q.K^T into S buffer kt & 1 (hi and lo halves of Q)
+  auto issue_s = [&](int kt) {
+    const uint8_t* kst = smem + Sm::OFF_ST + (kt & 1) * Sm::STAGE;
+    const uint32_t ts = tmem + D + 64 * (kt & 1);
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+      const uint64_t kd = smem_desc(kst + (j >> 2) * Sm::KT + (j & 3) * 32);
+      mma(ts, smem_desc(smem + Sm::OFF_QH + (j >> 2) * Sm::Q + (j & 3) * 32), kd, Sm::IDESC_S, j > 0 ? 1u : 0u);
+      mma(ts, smem_desc(smem + Sm::OFF_QL + (j >> 2) * Sm::Q + (j & 3) * 32), kd, Sm::IDESC_S, 1u);
+    }
+    mma_commit(&sbar[kt & 1]);
+  };
+  const uint32_t lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
+  const uint32_t t_o = tmem + lanes + hf * DH;                             // this thread's half of O
 
-  float m_ref = -INFINITY, l_sum = 0.f;
+  float m_ref = -INFINITY, l_part = 0.f;  // the row's reference maximum; this half's sum of p
   bool bad = false;
   int kt = 0, s_issued = 0, o_issued = 0;
-  for (; kt < nkt; ++kt) {
-    const int st = kt & 1;
-    const uint8_t* kst = smem + Sm::OFF_ST + st * Sm::STAGE;
-    const uint8_t* vst = kst + NA * Sm::KT;
-    if (!mbar_wait(&full[st], static_cast<uint32_t>(kt >> 1) & 1u)) bad = true;
-    if (__syncthreads_or(bad)) break;
-    if (tid == 0) {  // S = Q.K^T (hi and lo halves of Q)
+  if (tid == 0 && nkt > 0) {
+    if (mbar_wait(&full[0], 0)) {
       tc_after();
-#pragma unroll
-      for (int j = 0; j < D / 16; ++j) {
-        const uint64_t kd = smem_desc(kst + (j >> 2) * Sm::KT + (j & 3) * 32);
-        mma(t_s, smem_desc(smem + Sm::OFF_QH + (j >> 2) * Sm::Q + (j & 3) * 32), kd, Sm::IDESC_S, j > 0 ? 1u : 0u);
-        mma(t_s, smem_desc(smem + Sm::OFF_QL + (j >> 2) * Sm::Q + (j & 3) * 32), kd, Sm::IDESC_S, 1u);
-      }
-      mma_commit(&sbar);
+      issue_s(0);
+      s_issued = 1;
+    } else {
+      bad = true;
     }
-    ++s_issued;
-    // the previous tile's P.V must be done before V^T, P and O are touched
-    if (kt > 0 && !mbar_wait(&obar, static_cast<uint32_t>(kt - 1) & 1u)) bad = true;
+  }
+  for (; kt < nkt; ++kt) {
+    const int b = kt & 1;
+    // thread 0: S of the next tile goes to the tensor pipe before this tile's softmax
+    if (tid == 0 && !bad && kt + 1 < nkt) {
+      if (mbar_wait(&full[(kt + 1) & 1], static_cast<uint32_t>((kt + 1) >> 1) & 1u)) {
+        tc_after();
+        issue_s(kt + 1);
+        s_issued = kt + 2;
+      } else {
+        bad = true;
+      }
+    }
+    // this tile's K/V stage has landed (its S was issued only then); the P.V
+    // of two tiles ago, which read buffers b, is done
+    if (!mbar_wait(&full[b], static_cast<uint32_t>(kt >> 1) & 1u)) bad = true;
+    if (kt >= 2 && !mbar_wait(&obar[b], static_cast<uint32_t>((kt - 2) >> 1) & 1u)) bad = true;
     // V^T [dim][key] from the V rows [key][dim]: 8x8 blocks, transposed on the
     // way through registers; keys past the CTA's last one become zeros
     {
+      const uint8_t* vst = smem + Sm::OFF_ST + b * Sm::STAGE + NA * Sm::KT;
+      uint8_t* vt = smem + Sm::OFF_VT + b * Sm::VT;
       const int kvalid = kend - kt * kPaKeys;
       constexpr int NBLK = (kPaKeys / 8) * (D / 8);
       for (int bi = warp * 4; bi < NBLK; bi += 4 * (kPaThreads / 32)) {
@@ -582,106 +609,121 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
         const int key = 8 * kb + r8;
         uint32_t r[4];
         ldsm_x4_t(smem_u32(vst + (db >> 3) * Sm::KT + sw128(key, 8 * (db & 7))), r[0], r[1], r[2], r[3]);
-        // lane (gq, tq) holds keys 8kb' + 2tq, +1 of dim 8db' + gq for each of the 4 blocks
+        // lane (gq, tq) holds keys 8kb + 2tq, +1 of dim 8db + gq, for each of the 4 blocks
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int kbi = (bi + i) / (D / 8);
-          const int k0i = 8 * kbi + 2 * (lane & 3);
-          uint32_t w = r[i];
-          if (k0i >= kvalid) w &= 0u;
-          else if (k0i + 1 >= kvalid) w &= 0x0000FFFFu;
-          r[i] = w;
+          const int k0i = 8 * ((bi + i) / (D / 8)) + 2 * (lane & 3);
+          if (k0i >= kvalid) r[i] = 0u;
+          else if (k0i + 1 >= kvalid) r[i] &= 0x0000FFFFu;
         }
-        const int dim = 8 * db + r8;
-        stsm_x4(smem_u32(smem + Sm::OFF_VT + sw128(dim, 8 * kb)), r[0], r[1], r[2], r[3]);
+        stsm_x4(smem_u32(vt + sw128(8 * db + r8, 8 * kb)), r[0], r[1], r[2], r[3]);
       }
     }
-    // this row's scores
-    if (!mbar_wait(&sbar, static_cast<uint32_t>(kt) & 1u)) bad = true;
+    // this thread's 32 scores of the row
+    if (!mbar_wait(&sbar[b], static_cast<uint32_t>(kt >> 1) & 1u)) bad = true;
     tc_after();
-    float sv[kPaKeys];
+    float sv[32];
     {
       uint32_t raw[32];
+      tmem_ld32(tmem + lanes + D + 64 * b + 32 * hf, raw);
 #pragma unroll
-      for (int h = 0; h < kPaKeys / 32; ++h) {
-        tmem_ld32(t_s + 32 * h, raw);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[32 * h + j] = __uint_as_float(raw[j]);
-      }
+      for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(raw[j]);
     }
-    float mt = -INFINITY;
+    float mx = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kPaKeys; ++j) {
-      const bool vis = row_ok && kt * kPaKeys + j <= qpos;
+    for (int j = 0; j < 32; ++j) {
+      const bool vis = row_ok && kt * kPaKeys + 32 * hf + j <= qpos;
       sv[j] = vis ? sv[j] : -INFINITY;
-      mt = fmaxf(mt, sv[j]);
+      mx = fmaxf(mx, sv[j]);
     }
+    xmax[hf][row] = mx;
+    asm volatile("bar.sync 1, %0;" ::"r"(kPaThreads) : "memory");
+    const float mt = fmaxf(mx, xmax[hf ^ 1][row]);
     // the reference maximum moves only when a tile's maximum exceeds it by kRescaleLog
     const bool move = row_ok && mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog);
     const float alpha = move ? (m_ref == -INFINITY ? 0.f : expf(m_ref - mt)) : 1.f;
     if (move) {
-      l_sum *= alpha;
+      l_part *= alpha;
       m_ref = mt;
     }
-    if (kt > 0 && __any_sync(0xffffffffu, move)) {  // O *= alpha in TMEM (a warp-wide access)
+    if (kt > 0 && __any_sync(0xffffffffu, move)) {  // this half of O *= alpha (a warp-wide access)
+      // every earlier P.V must be done: the one of the previous tile may still run
+      if (!mbar_wait(&obar[b ^ 1], static_cast<uint32_t>((kt - 1) >> 1) & 1u)) bad = true;
+      tc_after();
       uint32_t ov[32];
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = 0; c < DH; c += 32) {
         tmem_ld32(t_o + c, ov);
 #pragma unroll
         for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
         tmem_st32(t_o + c, ov);
       }
     }
-    // P = exp(s - m_ref) as fp16 hi + lo rows
-    float ps = 0.f;
+    // P = exp(s - m_ref) as fp16 hi + lo, this half's 32 keys
+    {
+      uint8_t* ph = smem + Sm::OFF_P + (2 * b) * Sm::P;
+      uint8_t* pl = ph + Sm::P;
+      float ps = 0.f;
 #pragma unroll
-    for (int c = 0; c < kPaKeys / 8; ++c) {
-      uint32_t hi[4], lo[4];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p0 = sv[8 * c + 2 * e] == -INFINITY ? 0.f : expf(sv[8 * c + 2 * e] - m_ref);
-        const float p1 = sv[8 * c + 2 * e + 1] == -INFINITY ? 0.f : expf(sv[8 * c + 2 * e + 1] - m_ref);
-        ps += p0 + p1;
-        split_half2(p0, p1, hi[e], lo[e]);
+        for (int e = 0; e < 4; ++e) {
+          const float s0 = sv[8 * c + 2 * e], s1 = sv[8 * c + 2 * e + 1];
+          const float p0 = s0 == -INFINITY ? 0.f : expf(s0 - m_ref);
+          const float p1 = s1 == -INFINITY ? 0.f : expf(s1 - m_ref);
+          ps += p0 + p1;
+          split_half2(p0, p1, hi[e], lo[e]);
+        }
+        const uint32_t off = sw128(row, 32 * hf + 8 * c);
+        *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      *reinterpret_cast<uint4*>(smem + Sm::OFF_PH + sw128(tid, 8 * c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(smem + Sm::OFF_PL + sw128(tid, 8 * c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      l_part += ps;
     }
-    l_sum += ps;
     fence_proxy_async();  // P and V^T (generic stores) before the MMAs read them
     tc_before();
     if (__syncthreads_or(bad)) break;
     if (tid == 0) {  // O += P.V^T (hi and lo halves of P)
       tc_after();
+      const uint8_t* ph = smem + Sm::OFF_P + (2 * b) * Sm::P;
+      const uint8_t* vt = smem + Sm::OFF_VT + b * Sm::VT;
 #pragma unroll
       for (int j = 0; j < kPaKeys / 16; ++j) {
-        const uint64_t vd = smem_desc(smem + Sm::OFF_VT + j * 32);
-        mma(t_o, smem_desc(smem + Sm::OFF_PH + j * 32), vd, Sm::IDESC_O, (kt > 0 || j > 0) ? 1u : 0u);
-        mma(t_o, smem_desc(smem + Sm::OFF_PL + j * 32), vd, Sm::IDESC_O, 1u);
+        const uint64_t vd = smem_desc(vt + j * 32);
+        mma(tmem, smem_desc(ph + j * 32), vd, Sm::IDESC_O, (kt > 0 || j > 0) ? 1u : 0u);
+        mma(tmem, smem_desc(ph + Sm::P + j * 32), vd, Sm::IDESC_O, 1u);
       }
-      mma_commit(&obar);
+      mma_commit(&obar[b]);
       // this stage is consumed (S done, V transposed): the tile after next goes there
       if (kt + 2 < nkt) issue_tile(kt + 2);
     }
-    ++o_issued;
+    o_issued = kt + 1;
   }
+  bad = __syncthreads_or(bad) != 0;  // one verdict for the CTA
+  // copies and MMAs still in flight end before the CTA's memory goes away (bounded waits)
   if (bad) {
-    if (tid == 0) atomicOr(a.guard, GUARD_TIMEOUT);
-    // copies and MMAs still in flight end before the CTA's memory goes away (bounded waits)
-    if (tid == 0)
+    if (tid == 0) {
+      atomicOr(a.guard, GUARD_TIMEOUT);
       for (int k = kt; k < min(nkt, kt + 2); ++k) (void)mbar_wait(&full[k & 1], static_cast<uint32_t>(k >> 1) & 1u);
-    if (s_issued > 0) (void)mbar_wait(&sbar, static_cast<uint32_t>(s_issued - 1) & 1u);
+      if (s_issued > kt + 1) (void)mbar_wait(&sbar[(kt + 1) & 1], static_cast<uint32_t>((kt + 1) >> 1) & 1u);
+    }
   }
-  const bool have_o = o_issued > 0 && mbar_wait(&obar, static_cast<uint32_t>(o_issued - 1) & 1u);
+  bool have_o = o_issued > 0;
+  for (int k = max(0, o_issued - 2); k < o_issued; ++k)
+    if (!mbar_wait(&obar[k & 1], static_cast<uint32_t>(k >> 1) & 1u)) have_o = false;
+  have_o = __syncthreads_and(have_o) != 0;  // the tensor-memory reads below are warp-wide
   tc_after();
+  // the row's sum: both halves
+  xmax[hf][row] = l_part;
+  asm volatile("bar.sync 1, %0;" ::"r"(kPaThreads) : "memory");
+  const float l_sum = l_part + xmax[hf ^ 1][row];
   if (!bad && have_o) {
-    // the row: O / sum, as bf16 hi + lo
+    // this half of the row: O / sum, as bf16 hi + lo
     const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-    __nv_bfloat16* oh = a.oh + static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D;
-    __nv_bfloat16* ol = a.ol + static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D;
+    const size_t ob = static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D + hf * DH;
 #pragma unroll 1
-    for (int c = 0; c < D; c += 32) {
+    for (int c = 0; c < DH; c += 32) {
       uint32_t ov[32];
       tmem_ld32(t_o + c, ov);
       if (row_ok) {
@@ -690,8 +732,8 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
           __nv_bfloat16 h0, l0, h1, l1;
           split_bf16(__uint_as_float(ov[j]) * inv, h0, l0);
           split_bf16(__uint_as_float(ov[j + 1]) * inv, h1, l1);
-          *reinterpret_cast<__nv_bfloat162*>(oh + c + j) = __nv_bfloat162(h0, h1);
-          *reinterpret_cast<__nv_bfloat162*>(ol + c + j) = __nv_bfloat162(l0, l1);
+          *reinterpret_cast<__nv_bfloat162*>(a.oh + ob + c + j) = __nv_bfloat162(h0, h1);
+          *reinterpret_cast<__nv_bfloat162*>(a.ol + ob + c + j) = __nv_bfloat162(l0, l1);
         }
       }
     }
