@@ -630,14 +630,15 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
       for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(raw[j]);
     }
     float mx = -INFINITY;
+    const int last = row_ok ? qpos - kt * kPaKeys - 32 * hf : -1;  // this half's last visible column
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      const bool vis = row_ok && kt * kPaKeys + 32 * hf + j <= qpos;
-      sv[j] = vis ? sv[j] : -INFINITY;
+      sv[j] = j <= last ? sv[j] : -INFINITY;
       mx = fmaxf(mx, sv[j]);
     }
+    // the row's other half is taken by warp w ^ 4: a barrier of those two warps
     xmax[hf][row] = mx;
-    asm volatile("bar.sync 1, %0;" ::"r"(kPaThreads) : "memory");
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
     const float mt = fmaxf(mx, xmax[hf ^ 1][row]);
     // the reference maximum moves only when a tile's maximum exceeds it by kRescaleLog
     const bool move = row_ok && mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog);
@@ -663,15 +664,15 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
     {
       uint8_t* ph = smem + Sm::OFF_P + (2 * b) * Sm::P;
       uint8_t* pl = ph + Sm::P;
+      const float mr = m_ref == -INFINITY ? 0.f : m_ref;  // a row with no visible key yet: all p are 0
       float ps = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float s0 = sv[8 * c + 2 * e], s1 = sv[8 * c + 2 * e + 1];
-          const float p0 = s0 == -INFINITY ? 0.f : expf(s0 - m_ref);
-          const float p1 = s1 == -INFINITY ? 0.f : expf(s1 - m_ref);
+          // masked columns are -inf: __expf gives 0
+          const float p0 = __expf(sv[8 * c + 2 * e] - mr), p1 = __expf(sv[8 * c + 2 * e + 1] - mr);
           ps += p0 + p1;
           split_half2(p0, p1, hi[e], lo[e]);
         }
@@ -716,7 +717,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   tc_after();
   // the row's sum: both halves
   xmax[hf][row] = l_part;
-  asm volatile("bar.sync 1, %0;" ::"r"(kPaThreads) : "memory");
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
   const float l_sum = l_part + xmax[hf ^ 1][row];
   if (!bad && have_o) {
     // this half of the row: O / sum, as bf16 hi + lo
