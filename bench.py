@@ -522,8 +522,9 @@ def run_ours(args, world, rank, local, pg):
                     "algorithmic_tflop": (pf_linear + pf_attn) / 1e12,
                     "achieved_tflops": pf_tflops, "peak_tflops": tc_peak, "frac": pf_tflops / tc_peak,
                     "note": ("useful FLOPs (2 per weight x token + causal attention); the GEMMs issue twice "
-                             "the linear MMAs (activations as bf16 hi + lo halves); attention issues mma.sync "
-                             "on fp16 hi + lo halves of the queries and probabilities") if args.weights == "bf16" else
+                             "the linear MMAs (activations as bf16 hi + lo halves); attention (fp16 KV) issues "
+                             "tcgen05 MMAs on fp16 hi + lo halves of the queries and probabilities, S and O "
+                             "in tensor memory") if args.weights == "bf16" else
                             ("fp8: the same tensor-core GEMMs over bf16 copies of the E4M3 codes, each row's scale "
                              "applied in the GEMM epilogue; the last prompt token takes the fp8 decode step")
                             if args.weights == "f8" else
