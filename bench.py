@@ -69,6 +69,9 @@ def parse():
     p.add_argument("--batch", type=int, default=1,
                    help="> 1: aggregate decode throughput of that many sequences per step (each prefilled "
                         "with --ctx random tokens); the default 1 is the batch-1 metric")
+    p.add_argument("--prefill-split", type=int, default=1, choices=[0, 1],
+                   help="K2_OPT_PREFILL_SPLIT for the prefill: 1 = activations as bf16 hi + lo halves "
+                        "(the default), 0 = single bf16 activations")
     p.add_argument("--no-configs", action="store_true",
                    help="skip the sub-records of the int8-KV context-8192 and batch-16 context-8192 workloads "
                         "that the default run adds to its line")
@@ -78,6 +81,21 @@ def parse():
 # ---------------------------------------------------------------------------
 # helpers
 # ---------------------------------------------------------------------------
+def prefill_note(args):
+    if args.weights == "f8":
+        return ("fp8: the same tensor-core GEMMs over bf16 copies of the E4M3 codes, each row's scale applied in "
+                "the GEMM epilogue; the last prompt token takes the fp8 decode step")
+    if args.weights == "q4":
+        return ("int4: no tensor-core GEMM path (block scales along K): the prompt runs through the decode step, "
+                "one token at a time")
+    if args.prefill_split:
+        return ("useful FLOPs (2 per weight x token + causal attention); the GEMMs issue twice the linear MMAs "
+                "(activations as bf16 hi + lo halves); attention (fp16 KV) issues tcgen05 MMAs on fp16 hi + lo "
+                "halves of the queries and probabilities, S and O in tensor memory")
+    return ("useful FLOPs (2 per weight x token + causal attention); single bf16 activations into the GEMMs and "
+            "single fp16 queries and probabilities into the tcgen05 attention (fp16 KV), S and O in tensor memory")
+
+
 
 def algorithmic_bytes(s, ctx_len: int, kv: str = "f16", weights_store: str = "bf16") -> dict:
     """Bytes the decode step must move at context ctx_len (weights once, the
@@ -408,6 +426,7 @@ def run_ours(args, world, rank, local, pg):
     tok = torch.zeros(1, dtype=torch.int32, device="cuda")
     prompt = torch.from_numpy(ki.prompt_ids(s.vocab, args.ctx, seed=1 + rank)).cuda()
     # prefill: one untimed warm-up on a short prompt, then the timed prompt
+    ctx.set_option(k2.K2_OPT_PREFILL_SPLIT, args.prefill_split)
     with torch.cuda.stream(stream):
         ctx.prefill(0, prompt[:256], tok, stream=stream)
     stream.synchronize()
@@ -521,15 +540,8 @@ def run_ours(args, world, rank, local, pg):
         "prefill": {"tokens": T, "ms": prefill_ms, "tok_per_s": T / (prefill_ms * 1e-3),
                     "algorithmic_tflop": (pf_linear + pf_attn) / 1e12,
                     "achieved_tflops": pf_tflops, "peak_tflops": tc_peak, "frac": pf_tflops / tc_peak,
-                    "note": ("useful FLOPs (2 per weight x token + causal attention); the GEMMs issue twice "
-                             "the linear MMAs (activations as bf16 hi + lo halves); attention (fp16 KV) issues "
-                             "tcgen05 MMAs on fp16 hi + lo halves of the queries and probabilities, S and O "
-                             "in tensor memory") if args.weights == "bf16" else
-                            ("fp8: the same tensor-core GEMMs over bf16 copies of the E4M3 codes, each row's scale "
-                             "applied in the GEMM epilogue; the last prompt token takes the fp8 decode step")
-                            if args.weights == "f8" else
-                            "int4: no tensor-core GEMM path (block scales along K): the prompt runs through the "
-                            "decode step, one token at a time"},
+                    "split": bool(args.prefill_split),
+                    "note": prefill_note(args)},
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
         "clocks": clk,
         "cpu_baseline": cpu,

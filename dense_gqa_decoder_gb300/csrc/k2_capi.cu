@@ -263,6 +263,7 @@ struct k2_ctx {
   KvMaps pf_maps = {};    // the tcgen05 prefill attention's tensor maps of the caches (64-row boxes)
   bool pf_tc = false;     // fp16 cache of a supported shape: prefill attention on tcgen05
   bool use_pf_tc = true;  // option K2_OPT_PREFILL_ATTN
+  bool pf_split = true;   // option K2_OPT_PREFILL_SPLIT
   std::vector<LayerPtrs> ltab;
   // tensor-core prefill: TMA tensor maps (weights per layer: qkv, o, gate/up,
   // down; activations: normed input, attention output, SwiGLU output, hi/lo)
@@ -825,12 +826,15 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     if (!e) e = launch_tc_gemm_sk(mw, mh, ml, g, c->sms, st);
     return e;
   };
+  // without the split (blocks over 16 tokens only) the low-half maps are null:
+  // the GEMMs read the high halves alone
+  const bool split = small || c->pf_split;
   const void* m_xh = small ? c->tb_xh.data() : c->tm_xh.data();
-  const void* m_xl = small ? c->tb_xl.data() : c->tm_xl.data();
+  const void* m_xl = small ? c->tb_xl.data() : split ? c->tm_xl.data() : nullptr;
   const void* m_oh = small ? c->tb_oh.data() : c->tm_oh.data();
-  const void* m_ol = small ? c->tb_ol.data() : c->tm_ol.data();
+  const void* m_ol = small ? c->tb_ol.data() : split ? c->tm_ol.data() : nullptr;
   const void* m_ah = small ? c->tb_ah.data() : c->tm_ah.data();
-  const void* m_al = small ? c->tb_al.data() : c->tm_al.data();
+  const void* m_al = small ? c->tb_al.data() : split ? c->tm_al.data() : nullptr;
   float* O32 = Q + static_cast<size_t>(16) * s.nq * s.d;  // small blocks: the attention output after 16 query rows
   cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.gb, X, s.H, s.V, c->guard,
                                     c->hist + static_cast<size_t>(seq) * c->lay.cap, 0, nullptr, pos0, d_pos0, st);
@@ -866,7 +870,8 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
       PrefillAttnArgs pa = {};
       pa.Q = Q;
       pa.oh = xh;
-      pa.ol = xl;
+      pa.ol = split ? xl : nullptr;
+      pa.split = split ? 1 : 0;
       pa.n = n;
       pa.nq = s.nq;
       pa.nkv = s.nkv;
@@ -889,7 +894,8 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
         e = gemm_sk(c->tmw[4 * l + 2].data(), c->tcs(l, 2), m_xh, m_xl, 2 * s.I, s.H, TC_STORE, qkv, 2 * s.I);
         if (!e) e = launch_swiglu_rows(qkv, ah, al, n, s.I, st);
       } else {
-        e = gemm(c->tmw[4 * l + 2].data(), c->tcs(l, 2), m_xh, m_xl, 2 * s.I, s.H, TC_SWIGLU, nullptr, ah, al, s.I);
+        e = gemm(c->tmw[4 * l + 2].data(), c->tcs(l, 2), m_xh, m_xl, 2 * s.I, s.H, TC_SWIGLU, nullptr, ah,
+                 split ? al : nullptr, s.I);
       }
     }
     if (!e) e = gemm_sk(c->tmw[4 * l + 3].data(), c->tcs(l, 3), m_ah, m_al, s.H, s.I, TC_RESID, X, s.H);
@@ -1588,6 +1594,7 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
       c->l2_mask = static_cast<int>(value);
       break;
     case K2_OPT_PREFILL_ATTN: c->use_pf_tc = value != 0; break;
+    case K2_OPT_PREFILL_SPLIT: c->pf_split = value != 0; break;
     case K2_OPT_TRACE:
       if (value < 0 || value % 8) return c->fail(K2_ERR_ARG, "trace buffer must be 8-byte aligned (or 0)");
       c->trace = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));

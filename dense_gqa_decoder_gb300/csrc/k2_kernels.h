@@ -387,7 +387,7 @@ struct TcGemmArgs {
                // adds its partial with atomicAdd (TC_STORE / TC_RESID only; 1 = no split)
   float* out;
   __nv_bfloat16* out_hi;
-  __nv_bfloat16* out_lo;
+  __nv_bfloat16* out_lo;   // TC_SWIGLU: nullable (only the high half is written)
   unsigned* guard;
   const float* row_scale;  // non-null: each row's accumulator is multiplied by row_scale[row] first
 };
@@ -395,6 +395,8 @@ constexpr int kTcMapBytes = 128;  // one CUtensorMap
 bool tc_encode_weight(void* map, const void* packed, int N, int K);  // bf16 packed weights
 bool tc_encode_act(void* map, const void* buf, int rows, int K, int tile_tokens);  // bf16 [rows][K]
 cudaError_t tc_gemm_init_attrs();
+// mapXl (the activations' low halves) null: one MMA per K step on the high
+// halves alone (tile_tokens 128 only)
 cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a,
                            cudaStream_t s);
 // stream-K persistent variant (tile_tokens 16; TC_STORE into a zeroed target or TC_RESID), `ctas` CTAs.
@@ -407,6 +409,8 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* m
 // rotated) against every cached key of their sequence up to their own position,
 // through `maps` (the K and V caches of every layer, boxes of 64 dims x 64 rows);
 // the attention output goes to oh / ol [n][nq * D] as bf16 hi / lo halves.
+// split: queries and probabilities enter the MMAs as fp16 hi + lo halves (two
+// MMAs each), else as single fp16 values and only oh is written.
 struct PrefillAttnArgs {
   const float* Q;
   __nv_bfloat16* oh;
@@ -418,6 +422,7 @@ struct PrefillAttnArgs {
   int layer;
   float scale;
   unsigned* guard;
+  int split;
 };
 bool prefill_attn_tc_supported(int head_dim, int rep);
 cudaError_t prefill_attn_tc_init_attrs();

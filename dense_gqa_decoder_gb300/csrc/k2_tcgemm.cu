@@ -10,7 +10,9 @@
 // (x_hi = bf16(x), x_lo = bf16(x - x_hi)); each K step issues one MMA per
 // half, so the product keeps ~16 mantissa bits of the activation, the
 // precision the decode step's fp32 activations have, while W stays the model's
-// bf16.
+// bf16.  Without the low half (LO = false: no map for it) each K step issues
+// one MMA on x_hi alone -- activations in the model's dtype, half the MMAs and
+// half the activation bytes -- and the ring holds more stages.
 //
 // One CTA per 128-row x 128-token tile, 128 threads: thread 0 issues the TMA
 // loads into a 4-stage ring (mbarrier complete_tx), thread 32 issues the MMAs
@@ -31,11 +33,13 @@ namespace {
 
 constexpr int BM = 128, BK = 64;
 // tile shapes: 128 tokens for prefill, 16 for a batched decode step
-template <int BN_>
+template <int BN_, bool LO_ = true>
 struct Tile {
   static constexpr int BN = BN_;
-  static constexpr int STAGES = BN_ >= 128 ? 4 : 8;
-  static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + 2 * B_BYTES;
+  static constexpr bool LO = LO_;  // the activations' low half is a second B operand
+  static constexpr int STAGES = BN_ >= 128 ? (LO_ ? 4 : 6) : 8;
+  static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + (LO_ ? 2 : 1) * B_BYTES;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment of the ring to 1024 B
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;             // allocation: a power of two >= 32
   // instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major
@@ -102,11 +106,11 @@ __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
-template <int BN_>
+template <int BN_, bool LO>
 __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                          const __grid_constant__ CUtensorMap tmXh,
                                                          const __grid_constant__ CUtensorMap tmXl, const TcGemmArgs a) {
-  using C = Tile<BN_>;
+  using C = Tile<BN_, LO>;
   constexpr int BN = C::BN, STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -152,7 +156,7 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
       const int kk = (kb + k) * BK;
       tma_4d(st, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
       tma_2d(st + A_BYTES, &tmXh, kk, n0, &full[s]);
-      tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[s]);
+      if constexpr (LO) tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[s]);
     }
     // copies still in flight must land before the CTA ends: wait for the
     // last ones the MMA thread may not have consumed (bounded)
@@ -170,7 +174,7 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
       for (int j = 0; j < BK / 16; ++j) {
         const uint64_t ad = smem_desc(st + j * 32);
         mma(tmem, ad, smem_desc(st + A_BYTES + j * 32), C::IDESC, (k | j) != 0);
-        mma(tmem, ad, smem_desc(st + A_BYTES + B_BYTES + j * 32), C::IDESC, 1u);
+        if constexpr (LO) mma(tmem, ad, smem_desc(st + A_BYTES + B_BYTES + j * 32), C::IDESC, 1u);
       }
       mma_commit(&empty[s]);
     }
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
             __nv_bfloat16 hi, lo;
             split_bf16(y, hi, lo);
             a.out_hi[static_cast<size_t>(t) * a.ldo + (row >> 1)] = hi;
-            a.out_lo[static_cast<size_t>(t) * a.ldo + (row >> 1)] = lo;
+            if (a.out_lo != nullptr) a.out_lo[static_cast<size_t>(t) * a.ldo + (row >> 1)] = lo;
           }
         } else if (t < a.T && row < a.N) {
           float* o = a.out + static_cast<size_t>(t) * a.ldo + row;
@@ -226,12 +230,12 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
 // w reads TMEM lanes 32 (w % 4) ..), so accumulation and write-back overlap.
 // Output: atomicAdd into out (TC_RESID adds to the residual; TC_STORE expects
 // a zeroed target).
-template <int BN_>
+template <int BN_, bool LO>
 __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constant__ CUtensorMap tmW,
                                                             const __grid_constant__ CUtensorMap tmXh,
                                                             const __grid_constant__ CUtensorMap tmXl,
                                                             const TcGemmArgs a) {
-  using C = Tile<BN_>;
+  using C = Tile<BN_, LO>;
   constexpr int BN = C::BN, STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES, COLS = C::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
       where(g0 + j, m0, n0, kk);
       uint8_t* st = smem + j * STAGE_BYTES;
       tma_2d(st + A_BYTES, &tmXh, kk, n0, &full[j]);
-      tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[j]);
+      if constexpr (LO) tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[j]);
     }
     long long g = g0 + pre;
     int i = pre;
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
       uint8_t* st = smem + s * STAGE_BYTES;
       tma_4d(st, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
       tma_2d(st + A_BYTES, &tmXh, kk, n0, &full[s]);
-      tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[s]);
+      if constexpr (LO) tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[s]);
     }
     for (int j = max(0, i - STAGES); j < i; ++j) mbar_wait(&full[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u);
   } else if (threadIdx.x == 32) {  // MMA issuer
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
       for (int j = 0; j < BK / 16; ++j) {
         const uint64_t ad = smem_desc(st + j * 32);
         mma(acc, ad, smem_desc(st + A_BYTES + j * 32), C::IDESC, (!first || j != 0) ? 1u : 0u);
-        mma(acc, ad, smem_desc(st + A_BYTES + B_BYTES + j * 32), C::IDESC, 1u);
+        if constexpr (LO) mma(acc, ad, smem_desc(st + A_BYTES + B_BYTES + j * 32), C::IDESC, 1u);
       }
       mma_commit(&empty[s]);
       first = false;
@@ -409,11 +413,13 @@ EncodeTiled encode_fn() {
 // One CTA takes 128 query rows -- 128 / REP tokens x the REP query heads of one
 // KV head -- and walks the cached keys 0 .. (its last position) in tiles of 64:
 //   S = Q.K^T   (tcgen05.mma M=128 N=64, S in TMEM): Q as fp16 hi + lo halves
-//               (two MMAs per k-step: ~22 bits of every query), K the fp16 cache;
+//               (two MMAs per k-step: ~22 bits of every query; SPLIT = false:
+//               fp16 Q alone, one MMA), K the fp16 cache;
 //   softmax     row r (TMEM lane r) is shared by the two warps that may read
 //               lane group r / 32: each takes 32 of the tile's 64 scores
 //               (tcgen05.ld), the two exchange their maxima through shared
-//               memory, and write their halves of P = exp(s - m) as fp16 hi + lo;
+//               memory, and write their halves of P = exp(s - m) as fp16 hi + lo
+//               (SPLIT = false: fp16 P alone);
 //   O += P.V^T  (tcgen05.mma M=128 N=D, O in TMEM).
 // Every operand is K-major with the 128-byte swizzle (the layout of the GEMMs'
 // descriptors): Q and P are written so by the threads, K arrives so by TMA, and
@@ -478,7 +484,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-template <int D, int REP>
+template <int D, int REP, bool SPLIT>
 __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __grid_constant__ KvMaps maps,
                                                                         const PrefillAttnArgs a) {
   using Sm = PaSmem<D>;
@@ -531,7 +537,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
       for (int e = 0; e < 4; ++e) split_half2(v[2 * e], v[2 * e + 1], hi[e], lo[e]);
       const uint32_t off = (c >> 3) * Sm::Q + sw128(row, 8 * (c & 7));
       *reinterpret_cast<uint4*>(smem + Sm::OFF_QH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(smem + Sm::OFF_QL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      if constexpr (SPLIT) *reinterpret_cast<uint4*>(smem + Sm::OFF_QL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
   }
   fence_proxy_async();  // generic stores (Q) before the MMAs read them
@@ -561,7 +567,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
     for (int j = 0; j < D / 16; ++j) {
       const uint64_t kd = smem_desc(kst + (j >> 2) * Sm::KT + (j & 3) * 32);
       mma(ts, smem_desc(smem + Sm::OFF_QH + (j >> 2) * Sm::Q + (j & 3) * 32), kd, Sm::IDESC_S, j > 0 ? 1u : 0u);
-      mma(ts, smem_desc(smem + Sm::OFF_QL + (j >> 2) * Sm::Q + (j & 3) * 32), kd, Sm::IDESC_S, 1u);
+      if constexpr (SPLIT) mma(ts, smem_desc(smem + Sm::OFF_QL + (j >> 2) * Sm::Q + (j & 3) * 32), kd, Sm::IDESC_S, 1u);
     }
     mma_commit(&sbar[kt & 1]);
   };
@@ -678,7 +684,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
         }
         const uint32_t off = sw128(row, 32 * hf + 8 * c);
         *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if constexpr (SPLIT) *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       l_part += ps;
     }
@@ -693,7 +699,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
       for (int j = 0; j < kPaKeys / 16; ++j) {
         const uint64_t vd = smem_desc(vt + j * 32);
         mma(tmem, smem_desc(ph + j * 32), vd, Sm::IDESC_O, (kt > 0 || j > 0) ? 1u : 0u);
-        mma(tmem, smem_desc(ph + Sm::P + j * 32), vd, Sm::IDESC_O, 1u);
+        if constexpr (SPLIT) mma(tmem, smem_desc(ph + Sm::P + j * 32), vd, Sm::IDESC_O, 1u);
       }
       mma_commit(&obar[b]);
       // this stage is consumed (S done, V transposed): the tile after next goes there
@@ -734,7 +740,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
           split_bf16(__uint_as_float(ov[j]) * inv, h0, l0);
           split_bf16(__uint_as_float(ov[j + 1]) * inv, h1, l1);
           *reinterpret_cast<__nv_bfloat162*>(a.oh + ob + c + j) = __nv_bfloat162(h0, h1);
-          *reinterpret_cast<__nv_bfloat162*>(a.ol + ob + c + j) = __nv_bfloat162(l0, l1);
+          if constexpr (SPLIT) *reinterpret_cast<__nv_bfloat162*>(a.ol + ob + c + j) = __nv_bfloat162(l0, l1);
         }
       }
     }
@@ -804,36 +810,45 @@ bool attn_encode_kv_layers(void* map, const void* base, long long rows, int head
 bool prefill_attn_tc_supported(int head_dim, int rep) { return (head_dim == 64 || head_dim == 128) && rep == 4; }
 
 cudaError_t prefill_attn_tc_init_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(prefill_attn_tc_kernel<128, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       PaSmem<128>::DYN);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(prefill_attn_tc_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PaSmem<64>::DYN);
+  const auto set = [](const void* k, int bytes) {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  };
+  cudaError_t e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<128, 4, true>), PaSmem<128>::DYN);
+  if (e == cudaSuccess) e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<128, 4, false>), PaSmem<128>::DYN);
+  if (e == cudaSuccess) e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<64, 4, true>), PaSmem<64>::DYN);
+  if (e == cudaSuccess) e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<64, 4, false>), PaSmem<64>::DYN);
   return e;
 }
 
 cudaError_t launch_prefill_attn_tc(const KvMaps& maps, const PrefillAttnArgs& a, int head_dim, int rep,
                                    cudaStream_t s) {
   if (a.n <= 0) return cudaSuccess;
-  if (!prefill_attn_tc_supported(head_dim, rep)) return cudaErrorInvalidValue;
+  if (!prefill_attn_tc_supported(head_dim, rep) || (a.split && a.ol == nullptr)) return cudaErrorInvalidValue;
   const dim3 grid((a.n + kPaRows / rep - 1) / (kPaRows / rep), a.nkv);
-  if (head_dim == 128)
-    prefill_attn_tc_kernel<128, 4><<<grid, kPaThreads, PaSmem<128>::DYN, s>>>(maps, a);
+  if (head_dim == 128 && a.split)
+    prefill_attn_tc_kernel<128, 4, true><<<grid, kPaThreads, PaSmem<128>::DYN, s>>>(maps, a);
+  else if (head_dim == 128)
+    prefill_attn_tc_kernel<128, 4, false><<<grid, kPaThreads, PaSmem<128>::DYN, s>>>(maps, a);
+  else if (a.split)
+    prefill_attn_tc_kernel<64, 4, true><<<grid, kPaThreads, PaSmem<64>::DYN, s>>>(maps, a);
   else
-    prefill_attn_tc_kernel<64, 4><<<grid, kPaThreads, PaSmem<64>::DYN, s>>>(maps, a);
+    prefill_attn_tc_kernel<64, 4, false><<<grid, kPaThreads, PaSmem<64>::DYN, s>>>(maps, a);
   return cudaGetLastError();
 }
 
+template <typename K>
+cudaError_t smem_attr(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
 cudaError_t tc_gemm_init_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Tile<128>::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_gemm_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<16>::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_gemm_sk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<16>::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tc_gemm_sk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Tile<128>::SMEM_BYTES);
+  cudaError_t e = smem_attr(tc_gemm_kernel<128, true>, Tile<128, true>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<128, false>, Tile<128, false>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<16, true>, Tile<16, true>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<16, true>, Tile<16, true>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true>, Tile<128, true>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, false>, Tile<128, false>::SMEM_BYTES);
+  return e;
 }
 
 cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a, int ctas,
@@ -841,38 +856,48 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* m
   if (a.T <= 0) return cudaSuccess;
   if ((a.tile_tokens != 16 && a.tile_tokens != 128) || a.mode == TC_SWIGLU || ctas < 1) return cudaErrorInvalidValue;
   const int tt = a.tile_tokens;
+  const bool lo = mapXl != nullptr;
+  if (tt == 16 && !lo) return cudaErrorInvalidValue;
   const long long total =
       static_cast<long long>((2 * ((a.N + 1) / 2) + BM - 1) / BM) * ((a.T + tt - 1) / tt) * a.ksteps;
   const int grid = static_cast<int>(std::min<long long>(ctas, total));
   const CUtensorMap& w = *static_cast<const CUtensorMap*>(mapW);
   const CUtensorMap& xh = *static_cast<const CUtensorMap*>(mapXh);
-  const CUtensorMap& xl = *static_cast<const CUtensorMap*>(mapXl);
+  const CUtensorMap& xl = *static_cast<const CUtensorMap*>(lo ? mapXl : mapXh);  // unread without the low half
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = tt == 16 ? Tile<16>::SMEM_BYTES : Tile<128>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = tt == 16 ? Tile<16, true>::SMEM_BYTES
+                                  : (lo ? Tile<128, true>::SMEM_BYTES : Tile<128, false>::SMEM_BYTES);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (tt == 16) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<16>, w, xh, xl, a);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128>, w, xh, xl, a);
+  if (tt == 16) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<16, true>, w, xh, xl, a);
+  if (lo) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true>, w, xh, xl, a);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, false>, w, xh, xl, a);
 }
 
 cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a,
                            cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   if (a.splits < 1 || (a.splits > 1 && a.mode == TC_SWIGLU)) return cudaErrorInvalidValue;
+  const bool lo = mapXl != nullptr;
   const CUtensorMap& w = *static_cast<const CUtensorMap*>(mapW);
   const CUtensorMap& xh = *static_cast<const CUtensorMap*>(mapXh);
-  const CUtensorMap& xl = *static_cast<const CUtensorMap*>(mapXl);
+  const CUtensorMap& xl = *static_cast<const CUtensorMap*>(lo ? mapXl : mapXh);  // unread without the low half
   const int rows = (2 * ((a.N + 1) / 2) + BM - 1) / BM;
-  if (a.tile_tokens == 16) {
-    tc_gemm_kernel<16><<<dim3((a.T + 15) / 16, rows, a.splits), 128, Tile<16>::SMEM_BYTES, s>>>(w, xh, xl, a);
+  if (a.tile_tokens == 16 && lo) {
+    tc_gemm_kernel<16, true><<<dim3((a.T + 15) / 16, rows, a.splits), 128, Tile<16, true>::SMEM_BYTES, s>>>(w, xh, xl,
+                                                                                                            a);
+  } else if (a.tile_tokens == 128 && lo) {
+    tc_gemm_kernel<128, true>
+        <<<dim3((a.T + 127) / 128, rows, a.splits), 128, Tile<128, true>::SMEM_BYTES, s>>>(w, xh, xl, a);
   } else if (a.tile_tokens == 128) {
-    tc_gemm_kernel<128><<<dim3((a.T + 127) / 128, rows, a.splits), 128, Tile<128>::SMEM_BYTES, s>>>(w, xh, xl, a);
+    tc_gemm_kernel<128, false>
+        <<<dim3((a.T + 127) / 128, rows, a.splits), 128, Tile<128, false>::SMEM_BYTES, s>>>(w, xh, xl, a);
   } else {
     return cudaErrorInvalidValue;
   }

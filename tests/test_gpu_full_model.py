@@ -19,11 +19,31 @@ from oracle import k2_oracle as O
 pytestmark = pytest.mark.gpu
 
 
-def test_full_3p7b_prefill512_decode256_teacher_forced():
+_ORACLE = {}
+
+
+def _teacher_forced(s, host, seq, start):
+    key = tuple(int(t) for t in seq)
+    if key not in _ORACLE:
+        _ORACLE[key] = O.OracleModel(s, lambda n, l: host[(n, l)], "f16").teacher_forced(seq, start)
+    return _ORACLE[key]
+
+
+@pytest.mark.parametrize("split", [1, 0])
+def test_full_3p7b_prefill512_decode256_teacher_forced(split):
+    """split = 0 (K2_OPT_PREFILL_SPLIT off): the 512-token prefill feeds the
+    GEMMs single bf16 activations and the attention single fp16 queries and
+    probabilities; the decode steps keep fp32 activations.  That mode does not
+    hold the bf16 bars on this 36-layer model -- measured: agreement 0.965,
+    logits relative L2 1.1e-2 over the 257 predictions and 2.1e-2 on the
+    prefill's own logits -- which is why the split is the default.  The test
+    keeps the measured cost of dropping it bounded (agreement >= 0.95, relative
+    L2 <= 3e-2) and holds split = 1 to the bars and to 1e-3."""
     from dense_gqa_decoder_gb300 import k2, model_io
     s = ki.K2_3P7B
     n_prompt, n_new = 512, 256
     ctx, host = model_io.build_context(s, max_context=n_prompt + n_new + 8, kv_dtype="f16", keep_host=True)
+    ctx.set_option(k2.K2_OPT_PREFILL_SPLIT, split)
     prompt = ki.prompt_ids(s.vocab, n_prompt, seed=1)
     nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
     logits = torch.empty(s.vocab, dtype=torch.float32, device="cuda")
@@ -37,10 +57,16 @@ def test_full_3p7b_prefill512_decode256_teacher_forced():
     del ctx
     torch.cuda.empty_cache()
     seq = np.concatenate([prompt, toks[:-1]])
-    am, lg_ref, _ = O.OracleModel(s, lambda n, l: host[(n, l)], "f16").teacher_forced(seq, n_prompt - 1)
+    am, lg_ref, _ = _teacher_forced(s, host, seq, n_prompt - 1)
     got = np.stack(lgs).astype(np.float64)
     rel = float(np.linalg.norm(got - lg_ref) / np.linalg.norm(lg_ref))
+    rel_first = float(np.linalg.norm(got[0] - lg_ref[0]) / np.linalg.norm(lg_ref[0]))
     agree = float(np.mean(am == np.array(toks)))
-    assert agree >= 0.99, agree
-    assert rel <= 2e-2
-    assert rel <= 1e-3, rel
+    print(f"split={split} rel_l2={rel:.3e} rel_l2_prefill_logits={rel_first:.3e} agreement={agree:.4f}")
+    if split:
+        assert agree >= 0.99, agree
+        assert rel <= 2e-2
+        assert rel <= 1e-3, rel
+    else:
+        assert agree >= 0.95, agree
+        assert rel <= 3e-2, rel
