@@ -151,17 +151,20 @@ Layout layout_of(const k2_config& c) {
     l.vpi = take(nv * kArgmaxPartsMax * 4);
   }
   const size_t scratch_end = o;
-  // int4: codes and block scales in kQ4Unit units; else wb-byte weights in 1024-byte units
-  auto pbytes = [&](int N, int K) { return c.weight_dtype == K2_Q4 ? q4_packed_bytes(N, K) : packed_bytes(N, K, s.wb); };
-  l.wqkv_layer = align_up(pbytes(s.qkv_n, s.H), kAlign);
-  l.wo_layer = align_up(pbytes(s.H, s.nq * s.d), kAlign);
-  l.wgu_layer = align_up(pbytes(2 * s.I, s.H), kAlign);
-  l.wdown_layer = align_up(pbytes(s.H, s.I), kAlign);
+  // int4: codes and block scales in kQ4Unit units (pair or tile units by GEMV
+  // kind, q4_tiled); else wb-byte weights in 1024-byte units
+  auto pbytes = [&](int N, int K, int kind) {
+    return c.weight_dtype == K2_Q4 ? q4_packed_bytes(N, K, q4_tiled(kind)) : packed_bytes(N, K, s.wb);
+  };
+  l.wqkv_layer = align_up(pbytes(s.qkv_n, s.H, 0), kAlign);
+  l.wo_layer = align_up(pbytes(s.H, s.nq * s.d, 1), kAlign);
+  l.wgu_layer = align_up(pbytes(2 * s.I, s.H, 2), kAlign);
+  l.wdown_layer = align_up(pbytes(s.H, s.I, 3), kAlign);
   l.wqkv = take(l.wqkv_layer * s.L);
   l.wo = take(l.wo_layer * s.L);
   l.wgu = take(l.wgu_layer * s.L);
   l.wdown = take(l.wdown_layer * s.L);
-  l.wlm = take(pbytes(s.V, s.H));
+  l.wlm = take(pbytes(s.V, s.H, 4));
   if (c.weight_dtype == K2_F8 && l.pchunk > 0) {  // bf16 copies of the fp8 codes for the prefill GEMMs
     l.tqkv_layer = align_up(packed_bytes(s.qkv_n, s.H, 2), kAlign);
     l.to_layer = align_up(packed_bytes(s.H, s.nq * s.d, 2), kAlign);
@@ -284,7 +287,9 @@ struct k2_ctx {
   int stall_phase = -1;                              // persistent step: test option K2_OPT_STALL_PHASE
   // persistent step: L2 look-ahead per phase kind (two slots at the gate/up and
   // down phases measured fastest at context 4096: 1.934 against 1.990 ms per
-  // token without; deeper look-ahead, or look-ahead at the attention phase, was slower)
+  // token without; deeper look-ahead, or look-ahead at the attention phase, was
+  // slower; quantized weights measured faster without it -- int4 1.85 against
+  // 1.92 ms, fp8 1.66 against 1.71 ms -- so their default mask is 0)
   int l2_ahead = 2, l2_mask = 0x18;
   unsigned long long* trace = nullptr;               // persistent step: K2_OPT_TRACE buffer
   std::string err;
@@ -607,20 +612,27 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   if (!mega_supported(s.wf, s.d, s.rep, kvdt)) return cudaSuccess;
   const bool q4 = c->cfg.weight_dtype == K2_Q4;
   const PackedGemvArgs* plans[5] = {&c->p_qkv, &c->p_o, &c->p_gu, &c->p_down, &c->p_lm};
-  for (const PackedGemvArgs* p : plans) {
-    // the input vector, padded to whole chunks, fits its buffer (a gain phase: 4096 values)
-    const size_t kp = q4 ? static_cast<size_t>((p->K + kQ4Chunk - 1) / kQ4Chunk) * kQ4Chunk : p->x_bytes / 4;
+  for (int kind = 0; kind < 5; ++kind) {
+    const PackedGemvArgs* p = plans[kind];
+    // the input vector, padded to whole chunks (int4: 64-weight blocks for
+    // tiles, 512-weight chunks for pairs), fits its buffer (a gain phase: 4096 values)
+    const int q4c = q4_tiled(kind) ? kQ4Block : kQ4Chunk;
+    const size_t kp = q4 ? static_cast<size_t>((p->K + q4c - 1) / q4c) * q4c : p->x_bytes / 4;
     if (p->x_bytes > static_cast<uint32_t>(kMegaXBytes) || kp * 4 > static_cast<size_t>(kMegaXBytes)) return cudaSuccess;
     if (p->gain && kp > 4096) return cudaSuccess;
   }
   cudaError_t e = mega_init_attrs(s.wf, s.d, s.rep, kvdt);
   if (e != cudaSuccess) return e;
   int grid = mega_max_grid(s.wf, s.d, s.rep, kvdt);
-  // every CTA must own rows of every layer GEMV (the dataflow waits rely on it)
-  grid = std::min(grid, std::min(s.qkv_n / 2, std::min((s.H + 1) / 2, s.I)));
+  // every CTA must own rows of every layer GEMV (the dataflow waits rely on
+  // it); int4 rows of the tiled kinds are owned in 16-row tiles (8 pairs)
+  auto rb = [&](int kind) { return q4 && q4_tiled(kind) ? kQ4GroupRows / 2 : 1; };  // pairs per ownership unit
+  auto owned = [&](int N, int kind) { return ((N + 1) / 2 + rb(kind) - 1) / rb(kind); };
+  grid = std::min(grid, std::min(owned(s.qkv_n, 0), std::min(owned(s.H, 1), owned(2 * s.I, 2))));
   if (grid < s.nkv) return cudaSuccess;
   // the QKV and residual epilogues keep their CTA's pairs in shared memory
-  if ((s.qkv_n / 2 + grid - 1) / grid > kMegaPairsMax || ((s.H + 1) / 2 + grid - 1) / grid > kMegaPairsMax)
+  if ((owned(s.qkv_n, 0) + grid - 1) / grid * rb(0) > kMegaPairsMax ||
+      (owned(s.H, 1) + grid - 1) / grid * rb(1) > kMegaPairsMax)
     return cudaSuccess;
   // inputs are polled in groups of four words; the gains are copied in 16-byte
   // pieces into the x buffer above a 16 KB input
@@ -651,9 +663,10 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   LayerPtrs* dtab = reinterpret_cast<LayerPtrs*>(c->ws + c->lay.ltab);
   e = cudaMemcpyAsync(dtab, c->ltab.data(), sizeof(LayerPtrs) * s.L, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return e;
-  auto gplan = [&](const PackedGemvArgs& p) {  // 512-byte chunks of packed weights per row
+  auto gplan = [&](const PackedGemvArgs& p, int kind) {  // packed units per row pair (int4 tiles: per tile)
     MegaGemv g;
-    g.CT = q4 ? (p.K + kQ4Chunk - 1) / kQ4Chunk : (p.K * s.wb + 511) / 512;
+    g.CT = !q4 ? (p.K * s.wb + 511) / 512 : q4_tiled(kind) ? (p.K + kQ4Block - 1) / kQ4Block
+                                                           : (p.K + kQ4Chunk - 1) / kQ4Chunk;
     return g;
   };
   MegaArgs& m = c->mega;
@@ -697,11 +710,11 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   m.inter = s.I;
   m.eps = c->cfg.eps;
   m.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(s.d)));
-  m.g_qkv = gplan(c->p_qkv);
-  m.g_o = gplan(c->p_o);
-  m.g_gu = gplan(c->p_gu);
-  m.g_down = gplan(c->p_down);
-  m.g_lm = gplan(c->p_lm);
+  m.g_qkv = gplan(c->p_qkv, 0);
+  m.g_o = gplan(c->p_o, 1);
+  m.g_gu = gplan(c->p_gu, 2);
+  m.g_down = gplan(c->p_down, 3);
+  m.g_lm = gplan(c->p_lm, 4);
   m.cap = c->lay.cap;
   m.nsplit = nsplit;
   m.rope = c->rope;
@@ -1174,6 +1187,7 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   }
   k2_ctx* c = new k2_ctx();
   c->cfg = *cfg;
+  if (cfg->weight_dtype == K2_Q4 || cfg->weight_dtype == K2_F8) c->l2_mask = 0;
   c->s = sizes_of(*cfg);
   c->lay = layout_of(*cfg);
   k2_status st = validate_weights(c, w);
@@ -1275,21 +1289,22 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   const Sizes& z = c->s;
   if (cfg->weight_dtype == K2_Q4) {  // quantize the bf16 inputs into int4 units (codes + block scales)
     for (int l = 0; l < z.L && e == cudaSuccess; ++l) {
+      const auto lay = [](int kind) { return q4_tiled(kind) ? Q4_TILES : Q4_PAIRS; };
       e = launch_q4_pack(static_cast<uint8_t*>(c->wqkv(l)), nullptr, w->wq[l], w->wk[l], w->wv[l], PACK_QKV, z.qkv_n,
-                         z.H, z.nq, z.nkv, z.d, true, s);
+                         z.H, z.nq, z.nkv, z.d, lay(0), s);
       if (e == cudaSuccess)
         e = launch_q4_pack(static_cast<uint8_t*>(c->wop(l)), nullptr, w->wo[l], nullptr, nullptr, PACK_PLAIN, z.H,
-                           z.nq * z.d, 0, 0, 1, true, s);
+                           z.nq * z.d, 0, 0, 1, lay(1), s);
       if (e == cudaSuccess)
         e = launch_q4_pack(static_cast<uint8_t*>(c->wgu(l)), nullptr, w->w_gate[l], w->w_up[l], nullptr, PACK_GATEUP,
-                           2 * z.I, z.H, 0, 0, 1, true, s);
+                           2 * z.I, z.H, 0, 0, 1, lay(2), s);
       if (e == cudaSuccess)
         e = launch_q4_pack(static_cast<uint8_t*>(c->wdown(l)), nullptr, w->w_down[l], nullptr, nullptr, PACK_PLAIN,
-                           z.H, z.I, 0, 0, 1, true, s);
+                           z.H, z.I, 0, 0, 1, lay(3), s);
     }
     if (e == cudaSuccess)
       e = launch_q4_pack(static_cast<uint8_t*>(c->wlm()), nullptr, w->lm_head, nullptr, nullptr, PACK_PLAIN, z.V, z.H,
-                         0, 0, 1, true, s);
+                         0, 0, 1, q4_tiled(4) ? Q4_TILES : Q4_PAIRS, s);
   }
   if (cfg->weight_dtype == K2_F8) {  // quantize the bf16 inputs into fp8 rows + scales
     auto sc = [&](size_t base, size_t stride, int l) { return reinterpret_cast<float*>(ws + base + stride * l); };
@@ -1950,7 +1965,7 @@ k2_status k2_quantize_q4(const void* d_src, int32_t rows, int32_t cols, int8_t* 
                          void* stream) {
   if (!d_src || !d_codes || !d_scales || rows < 0 || cols < 1) return K2_ERR_ARG;
   const cudaError_t e = launch_q4_pack(reinterpret_cast<uint8_t*>(d_codes), d_scales, d_src, nullptr, nullptr,
-                                       PACK_PLAIN, rows, cols, 0, 0, 1, false, static_cast<cudaStream_t>(stream));
+                                       PACK_PLAIN, rows, cols, 0, 0, 1, Q4_PLAIN, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? K2_OK : K2_ERR_CUDA;
 }
 }  // extern "C"

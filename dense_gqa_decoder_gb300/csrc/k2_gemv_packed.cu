@@ -454,14 +454,17 @@ __global__ void quant_pack_kernel(uint8_t* __restrict__ dst, float* __restrict__
 // with block size 64): one CTA of kQ4Chunk / 4 threads per (packed row R,
 // chunk c); thread t takes weights 4t .. 4t + 3 of the chunk, 16 threads one
 // 64-weight block.  s = max|w| / 7; code = w / s rounded to nearest, ties to
-// even, clamped to [-7, 7]; a zero block gets s = 0 and codes 0.  Packed:
-// nibble c + 8, element 2i in the low nibble of byte i, into the int4 unit
-// layout (kQ4Unit); plain: int8 codes [N][K], scales [N][ceil(K / 64)].
+// even, clamped to [-7, 7]; a zero block gets s = 0 and codes 0.  Pairs:
+// nibble c + 8, element 2i in the low nibble of byte i, into the int4 pair
+// unit; tiles: nibble c + 8 OR-ed into the int4 tile unit (the rows of a tile
+// word come from two CTAs, hence the atomic OR into a cleared buffer); plain:
+// int8 codes [N][K], scales [N][ceil(K / 64)].  (Both unit layouts are
+// described with kWfmtQ4.)
 __global__ void __launch_bounds__(kQ4Chunk / 4) q4_pack_kernel(uint8_t* __restrict__ dst, float* __restrict__ scales,
                                                       const __nv_bfloat16* __restrict__ s0,
                                                       const __nv_bfloat16* __restrict__ s1,
                                                       const __nv_bfloat16* __restrict__ s2, int mode, int N, int K,
-                                                      int CT, int nq, int nkv, int d, int packed) {
+                                                      int CT, int nq, int nkv, int d, int layout) {
   const int R = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
   const __nv_bfloat16* src = pack_src_row(s0, s1, s2, mode, R, N, K, nq, nkv, d);
   const int e0 = c * kQ4Chunk + 4 * tid;  // the thread's first weight in the row
@@ -479,13 +482,29 @@ __global__ void __launch_bounds__(kQ4Chunk / 4) q4_pack_kernel(uint8_t* __restri
 #pragma unroll
   for (int i = 0; i < 4; ++i) q[i] = s > 0.f ? max(-7, min(7, __float2int_rn(__fdiv_rn(w[i], s)))) : 0;
   const int blk = tid >> 4;  // the block within the chunk
-  if (packed) {
+  if (layout == Q4_PAIRS) {
     uint8_t* unit = dst + (static_cast<size_t>(R >> 1) * CT + c) * kQ4Unit;
     const uint32_t b0 = static_cast<uint32_t>(q[0] + 8) | (static_cast<uint32_t>(q[1] + 8) << 4);
     const uint32_t b1 = static_cast<uint32_t>(q[2] + 8) | (static_cast<uint32_t>(q[3] + 8) << 4);
     *reinterpret_cast<uint16_t*>(unit + (R & 1) * (kQ4Chunk / 2) + 2 * tid) = static_cast<uint16_t>(b0 | (b1 << 8));
     if ((tid & 15) == 0)
       *reinterpret_cast<float*>(unit + kQ4Chunk + (R & 1) * (kQ4Chunk / kQ4Block) * 4 + blk * 4) = s;
+  } else if (layout == Q4_TILES) {
+    const int nb = (K + kQ4Block - 1) / kQ4Block;  // blocks (units) per tile
+    const int b = c * (kQ4Chunk / kQ4Block) + blk;
+    if (b < nb) {
+      const int rl = R % kQ4GroupRows, pair = rl >> 1, member = rl & 1;
+      uint8_t* unit = dst + (static_cast<size_t>(R / kQ4GroupRows) * nb + b) * kQ4Unit;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int kb = 4 * (tid & 15) + i;  // position in the block
+        const int j = kb >> 4, kk = kb & 15, t = (kk & 7) >> 1, hi8 = kk >> 3, odd = kk & 1;
+        const int shift = 4 * member + 8 * hi8 + 16 * odd;
+        atomicOr(reinterpret_cast<unsigned*>(unit + (pair * 4 + t) * 16 + j * 4),
+                 static_cast<unsigned>(q[i] + 8) << shift);
+      }
+      if ((tid & 15) == 0) *reinterpret_cast<float*>(unit + 512 + pair * 8 + member * 4) = s;
+    }
   } else if (R < N) {
     const int nb = (K + kQ4Block - 1) / kQ4Block;
 #pragma unroll
@@ -618,20 +637,31 @@ cudaError_t launch_f8_expand(void* dst, const uint8_t* src, int N, int K, cudaSt
   return cudaGetLastError();
 }
 
-size_t q4_packed_bytes(int N, int K) {
-  const size_t CT = (static_cast<size_t>(K) + kQ4Chunk - 1) / kQ4Chunk;
-  return (static_cast<size_t>(N) + 1) / 2 * CT * kQ4Unit;
+size_t q4_packed_bytes(int N, int K, bool tiles) {
+  if (!tiles) {
+    const size_t CT = (static_cast<size_t>(K) + kQ4Chunk - 1) / kQ4Chunk;
+    return (static_cast<size_t>(N) + 1) / 2 * CT * kQ4Unit;
+  }
+  const size_t nb = (static_cast<size_t>(K) + kQ4Block - 1) / kQ4Block;
+  const size_t groups = (static_cast<size_t>(N) + kQ4GroupRows - 1) / kQ4GroupRows;
+  return groups * nb * kQ4Unit;
 }
 
 cudaError_t launch_q4_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
-                           int mode, int N, int K, int nq, int nkv, int d, bool packed, cudaStream_t s) {
+                           int mode, int N, int K, int nq, int nkv, int d, int layout, cudaStream_t s) {
   const int CT = (K + kQ4Chunk - 1) / kQ4Chunk;
-  const int rows = packed ? 2 * ((N + 1) / 2) : N;
+  const int rows = layout == Q4_TILES   ? kQ4GroupRows * ((N + kQ4GroupRows - 1) / kQ4GroupRows)
+                   : layout == Q4_PAIRS ? 2 * ((N + 1) / 2)
+                                        : N;
   if (rows <= 0 || CT <= 0) return cudaSuccess;
+  if (layout == Q4_TILES) {
+    const cudaError_t e = cudaMemsetAsync(dst, 0, q4_packed_bytes(N, K, true), s);
+    if (e != cudaSuccess) return e;
+  }
   q4_pack_kernel<<<dim3(rows, CT), kQ4Chunk / 4, 0, s>>>(dst, scales, static_cast<const __nv_bfloat16*>(src0),
                                                 static_cast<const __nv_bfloat16*>(src1),
                                                 static_cast<const __nv_bfloat16*>(src2), mode, N, K, CT, nq, nkv, d,
-                                                packed ? 1 : 0);
+                                                layout);
   return cudaGetLastError();
 }
 

@@ -173,6 +173,7 @@ __device__ bool poll_x(const u64* tv, int K, uint32_t tag, float4* xq, unsigned*
   return true;
 }
 
+static_assert(MW * 2 * (kQ4GroupRows / 2) * 2 <= 512, "int4 split-tile records fit the query buffer");
 struct MegaShared {
   uint64_t full[MW][NS];
   float ss[MW][4];
@@ -191,6 +192,37 @@ struct MegaShared {
   const void* gains[2 * kMegaMaxLayers + 1];  // attn_norm[l] at 2l, mlp_norm[l] at 2l + 1, final last
   float newkv[2][128];              // the new token's K and V rows (head_dim <= 128)
 };
+
+// ---- int4 tiles on the tensor cores -------------------------------------------------
+// One mma.sync m16n8k16 (fp16 in, fp32 accumulate) over 16 weights of the 16
+// rows of an int4 tile.  A: the lane's tile word w (layout with kWfmtQ4): each
+// nibble pair OR-ed into the exponent of fp16 1024 gives 1024 + n (rows g) or
+// 1024 + 16 n (rows g + 8) exactly, and one fp16 add or fma turns that into
+// the code n - 8, exactly.  B: the input as fp16 high and low halves in
+// columns 0 and 1 (lanes 0..7 hold them; the other columns are zero), so D
+// column 0 + column 1 is the product with ~22 bits of the input.
+__device__ __forceinline__ void q4_tile_mma(uint32_t w, const uint32_t* xf, int lane, float* d) {
+  constexpr uint32_t kOne024 = 0x64006400u;  // fp16 1024 in both halves
+  const uint32_t w8 = w >> 8;
+  uint32_t a[4] = {(w & 0x000F000Fu) | kOne024, (w & 0x00F000F0u) | kOne024, (w8 & 0x000F000Fu) | kOne024,
+                   (w8 & 0x00F000F0u) | kOne024};
+  const __half2 lo_off = __float2half2_rn(-1032.f), hi_mul = __float2half2_rn(0.0625f),
+                hi_off = __float2half2_rn(-72.f);
+#pragma unroll
+  for (int i = 0; i < 4; i += 2) {
+    const __half2 r0 = __hadd2(*reinterpret_cast<const __half2*>(&a[i]), lo_off);
+    const __half2 r1 = __hfma2(*reinterpret_cast<const __half2*>(&a[i + 1]), hi_mul, hi_off);
+    a[i] = *reinterpret_cast<const uint32_t*>(&r0);
+    a[i + 1] = *reinterpret_cast<const uint32_t*>(&r1);
+  }
+  uint2 b = make_uint2(0u, 0u);
+  if (lane < 8) b = *reinterpret_cast<const uint2*>(xf + 2 * lane);
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y));
+}
 
 // ---- static description of the step ------------------------------------------------
 // GEMV kinds: 0 QKV, 1 o_proj, 2 gate/up, 3 down, 4 lm_head.  Row ranges do not
@@ -550,12 +582,18 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
   float* xs = reinterpret_cast<float*>(smem + kMegaRingBytes);
   uint8_t* ring = smem + static_cast<size_t>(warp) * NS * SB;
   const GRange r = g_range<SU>(d, sh, warp);
+  // int4 gate/up and lm_head: r.p0 / r.p1 count 16-row tiles (8 pairs each);
+  // P0 / P1 are pairs
+  const bool tiles = Q4 && q4_tiled(d.kind);
+  const int npairs = (d.N + 1) / 2;
+  const int P0 = tiles ? r.p0 * (kQ4GroupRows / 2) : r.p0;
+  const int P1 = tiles ? min(r.p1 * (kQ4GroupRows / 2), npairs) : r.p1;
   if (lane == 0) sh.rec_n[warp] = 0;
 
   // ---- x, normalised if the phase has a gain, lane-interleaved per chunk
   bool bad = false;
   {
-    const int KP = CT * CH;  // <= PX * MT * 4
+    const int KP = tiles ? CT * kQ4Block : CT * CH;  // <= PX * MT * 4
     const int gsz = d.gain ? K / a.groups : K;
     auto xidx = [&](int e) {
       const int c = e / CH, rr = e - c * CH, l = rr / EPL, j = rr - l * EPL;
@@ -573,9 +611,9 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
       if (tid == 0 && ng != nullptr) issue_gain(a, smem, sh, gq, ng, K * static_cast<int>(sizeof(WT)));
     }
     float side = 0.f;
-    const int nrows = min(2 * r.p1, d.N) - 2 * r.p0;
+    const int nrows = min(2 * P1, d.N) - 2 * P0;
     if (ep.epi == EPI_RESID && (rsd0f || rsd0w) && tid < nrows)
-      side = rsd0f ? __ldcg(rsd0f + 2 * r.p0 + tid) : load1(rsd0w, 2 * r.p0 + tid);
+      side = rsd0f ? __ldcg(rsd0f + 2 * P0 + tid) : load1(rsd0w, 2 * P0 + tid);
     float4 xq[PX];
     if (xt) {
       bad = !poll_x(xt, K, tag_in, xq, a.guard, a.poll_limit_ns);
@@ -624,14 +662,35 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int e = tid * 4 + i * MT * 4;
-        if (e < KP) {
+        if (e < K) {
           float4 v = xq[i];
-          if (e < K) {
-            const float rs = sh.rs[(e >= gsz) + (e >= 2 * gsz) + (e >= 3 * gsz)];
-            const float4 gn = load4_shared<WT>(gsm, e);
-            v.x = v.x * rs * gn.x; v.y = v.y * rs * gn.y; v.z = v.z * rs * gn.z; v.w = v.w * rs * gn.w;
-          }
-          *reinterpret_cast<float4*>(xs + xidx(e)) = v;
+          const float rs = sh.rs[(e >= gsz) + (e >= 2 * gsz) + (e >= 3 * gsz)];
+          const float4 gn = load4_shared<WT>(gsm, e);
+          v.x = v.x * rs * gn.x; v.y = v.y * rs * gn.y; v.z = v.z * rs * gn.z; v.w = v.w * rs * gn.w;
+          xq[i] = v;
+        }
+      }
+    }
+    if (tiles) {
+      // the B fragments of the int4 tile MMAs: per 16 inputs, word (4 h + t) * 2 + r
+      // of lane 4 h + t holds inputs 2t + 8r, 2t + 8r + 1 as fp16 (h = 0: high
+      // halves, h = 1: low halves)
+      uint32_t* xf = reinterpret_cast<uint32_t*>(xs);
+#pragma unroll
+      for (int i = 0; i < PX; ++i) {
+        const int e = tid * 4 + i * MT * 4;
+        if (e < KP) {
+          const float4 v = xq[i];
+          const __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
+          const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+          const __half2 l01 = __floats2half2_rn(v.x - f01.x, v.y - f01.y);
+          const __half2 l23 = __floats2half2_rn(v.z - f23.x, v.w - f23.y);
+          const int kk = e & 15, t = (kk & 7) >> 1, rr = kk >> 3;
+          uint32_t* base = xf + (e >> 4) * 16 + rr;
+          base[2 * t] = *reinterpret_cast<const uint32_t*>(&h01);
+          base[2 * (t + 1)] = *reinterpret_cast<const uint32_t*>(&h23);
+          base[2 * (4 + t)] = *reinterpret_cast<const uint32_t*>(&l01);
+          base[2 * (5 + t)] = *reinterpret_cast<const uint32_t*>(&l23);
         }
       }
     } else {
@@ -665,8 +724,8 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
       const float v[2] = {v0, v1};
       for (int rr = 0; rr < rows; ++rr) {
         if (ep.epi == EPI_RESID) {
-          const float nv = sh.rsd[row + rr - 2 * r.p0] + v[rr];
-          sh.rsd[row + rr - 2 * r.p0] = nv;
+          const float nv = sh.rsd[row + rr - 2 * P0] + v[rr];
+          sh.rsd[row + rr - 2 * P0] = nv;
           st_tagged(ep.out + row + rr, nv, ep.tag);
           if (ep.plain) ep.plain[row + rr] = nv;
         } else {
@@ -678,129 +737,224 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
     }
   };
 
-  int pl = r.ua / CT, c = r.ua - (r.ua / CT) * CT;
-  bool pair_whole = (c == 0);
-  float acc0 = 0.f, acc1 = 0.f;
-  // fp8: the current pair's row scales, loaded when the pair starts (used at its end)
-  float sc0 = 1.f, sc1 = 1.f;
-  if (d.scale && r.ub > r.ua) {
-    sc0 = __ldg(d.scale + 2 * (r.p0 + pl));
-    sc1 = __ldg(d.scale + 2 * (r.p0 + pl) + 1);
-  }
-  for (int k = 0; k < r.nslots; ++k) {
-    const int s = consumed % NS;
-    const bool ok = mbar_wait(&sh.full[warp][s], static_cast<uint32_t>(consumed / NS) & 1u);
-    if (__any_sync(0xffffffffu, !ok)) {
-      bad = true;
-      break;
-    }
-    const uint8_t* buf = ring + static_cast<size_t>(s) * SB;
-    const int u0 = r.ua + k * SU;
-    const int n = min(SU, r.ub - u0);
-    int j = 0;
-    while (j < n) {
-      const int seg = min(n - j, CT - c);
-#pragma unroll 2
-      for (int q = 0; q < seg; ++q) {
-        const int cc = c + q;
-        float xv[EPL];
-#pragma unroll
-        for (int pp = 0; pp < NPL; ++pp) {
-          const float4 t = *reinterpret_cast<const float4*>(xs + ((cc * NPL + pp) * 32 + lane) * 4);
-          xv[4 * pp] = t.x; xv[4 * pp + 1] = t.y; xv[4 * pp + 2] = t.z; xv[4 * pp + 3] = t.w;
-        }
-        const uint8_t* ub = buf + (j + q) * UNIT;
-        const uint8_t* u8 = ub + lane * 16;
-        if constexpr (Q4) {
-          // the lane's 16 weights are a quarter of one 64-weight block of each
-          // row: two partial sums per row, then the block scales
-          static_assert(EPL == 16 && UNIT == 576, "int4 unit: 256 code bytes and 8 scales per row");
-          const uint2 c0 = *reinterpret_cast<const uint2*>(ub + lane * 8);
-          const uint2 c1 = *reinterpret_cast<const uint2*>(ub + 256 + lane * 8);
-          const float bs0 = *reinterpret_cast<const float*>(ub + 512 + (lane >> 2) * 4);
-          const float bs1 = *reinterpret_cast<const float*>(ub + 544 + (lane >> 2) * 4);
-          f32x2 p00 = 0ull, p01 = 0ull, p10 = 0ull, p11 = 0ull;  // (row, word) sums of element pairs
-          q4_dot8(c0.x, xv, p00);
-          q4_dot8(c0.y, xv + 8, p01);
-          q4_dot8(c1.x, xv, p10);
-          q4_dot8(c1.y, xv + 8, p11);
-          acc0 = fmaf(sum2(p00) + sum2(p01), bs0, acc0);
-          acc1 = fmaf(sum2(p10) + sum2(p11), bs1, acc1);
-        } else {
-          float w0[EPL], w1[EPL];
-          Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8), w0);
-          Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8 + 512), w1);
-          f32x2 t0 = 0ull, t1 = 0ull;  // sums of element pairs
-#pragma unroll
-          for (int e = 0; e < EPL; e += 2) {
-            const f32x2 xe = pk2(xv[e], xv[e + 1]);
-            t0 = fma2(pk2(w0[e], w0[e + 1]), xe, t0);
-            t1 = fma2(pk2(w1[e], w1[e + 1]), xe, t1);
-          }
-          acc0 += sum2(t0);
-          acc1 += sum2(t1);
-        }
+  if (tiles) {
+    // int4 tiles: unit (tile gi of the CTA's range, block b); lane 4 g + t
+    // accumulates rows g and g + 8 of the tile -- pair 8 gi + g -- in acc0 / acc1
+    // (meaningful for t = 0); a tile split between warps leaves records of
+    // its 8 pairs, summed in warp order below
+    const uint32_t* xf = reinterpret_cast<const uint32_t*>(xs);
+    constexpr int TP = kQ4GroupRows / 2;  // pairs per tile
+    const int g8 = lane >> 2;
+    float(*recv)[2][TP][2] = reinterpret_cast<float(*)[2][TP][2]>(sh.qs);
+    int gi = r.ua / CT, b = r.ua - (r.ua / CT) * CT;
+    bool whole = (b == 0);
+    float acc0 = 0.f, acc1 = 0.f;
+    for (int k = 0; k < r.nslots; ++k) {
+      const int s = consumed % NS;
+      const bool ok = mbar_wait(&sh.full[warp][s], static_cast<uint32_t>(consumed / NS) & 1u);
+      if (__any_sync(0xffffffffu, !ok)) {
+        bad = true;
+        break;
       }
-      j += seg;
-      c += seg;
-      const bool pair_end = (c == CT);
-      const bool range_end = (u0 + j == r.ub);
-      if (pair_end || range_end) {
-        const float s0 = warp_sum(acc0) * sc0, s1 = warp_sum(acc1) * sc1;
-        acc0 = acc1 = 0.f;
-        if (lane == 0) {
-          if (pair_whole && pair_end) {
-            finish(r.p0 + pl, s0, s1);
+      const uint8_t* buf = ring + static_cast<size_t>(s) * SB;
+      const int u0 = r.ua + k * SU;
+      const int n = min(SU, r.ub - u0);
+#pragma unroll 2
+      for (int j = 0; j < n; ++j) {
+        const uint8_t* ub = buf + j * UNIT;
+        const uint4 cw = *reinterpret_cast<const uint4*>(ub + lane * 16);
+        const float2 sc = *reinterpret_cast<const float2*>(ub + 512 + g8 * 8);
+        const uint32_t* xb = xf + b * 64;  // the block's four 16-input B fragments
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};  // two MMA chains
+        q4_tile_mma(cw.x, xb, lane, d0);
+        q4_tile_mma(cw.y, xb + 16, lane, d1);
+        q4_tile_mma(cw.z, xb + 32, lane, d0);
+        q4_tile_mma(cw.w, xb + 48, lane, d1);
+        acc0 = fmaf(sc.x, (d0[0] + d0[1]) + (d1[0] + d1[1]), acc0);
+        acc1 = fmaf(sc.y, (d0[2] + d0[3]) + (d1[2] + d1[3]), acc1);
+        ++b;
+        const bool tile_end = (b == CT);
+        if (tile_end || u0 + j + 1 == r.ub) {
+          const int pl = gi * TP + g8;  // the pair within the CTA's pairs
+          if (whole && tile_end) {
+            if ((lane & 3) == 0 && P0 + pl < npairs) finish(P0 + pl, acc0, acc1);
           } else {
             const int rr = sh.rec_n[warp];
-            sh.rec_pair[warp][rr] = pl;
-            sh.rec_val[warp][rr][0] = s0;
-            sh.rec_val[warp][rr][1] = s1;
-            sh.rec_n[warp] = rr + 1;
+            if ((lane & 3) == 0) {
+              recv[warp][rr][g8][0] = acc0;
+              recv[warp][rr][g8][1] = acc1;
+            }
+            __syncwarp();
+            if (lane == 0) {
+              sh.rec_pair[warp][rr] = gi;
+              sh.rec_n[warp] = rr + 1;
+            }
+            __syncwarp();
           }
-        }
-        if (pair_end) {
-          ++pl;
-          c = 0;
-          pair_whole = true;
-          if (d.scale && r.ua + (u0 - r.ua) + j < r.ub) {
-            sc0 = __ldg(d.scale + 2 * (r.p0 + pl));
-            sc1 = __ldg(d.scale + 2 * (r.p0 + pl) + 1);
+          acc0 = acc1 = 0.f;
+          if (tile_end) {
+            ++gi;
+            b = 0;
+            whole = true;
           }
         }
       }
+      __syncwarp();  // the slot was only read: no proxy fence needed before refilling it
+      ++consumed;
+      if (lane == 0) st.issue_next(a, ring, sh.full[warp], cta, G, warp, pos, qkv_n);
     }
-    __syncwarp();  // the slot was only read: no proxy fence needed before refilling it
-    ++consumed;
-    if (lane == 0) st.issue_next(a, ring, sh.full[warp], cta, G, warp, pos, qkv_n);
-  }
-  if (bad && lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
-  __syncthreads();
-  trace_mark(a, q, 2);
-  // Pairs split between warps: at most two records per warp, lane 2w + rr of
-  // warp 0 holding record rr of warp w.  Every record of a pair is summed in
-  // warp order by the lane of its first record, which finishes the pair; a
-  // fixed 16-step shuffle loop, so the lanes never diverge.
-  if (warp == 0) {
-    const int w = lane >> 1, rr = lane & 1;
-    const bool has = lane < 2 * MW && rr < sh.rec_n[w];
-    const int pr = has ? sh.rec_pair[w][rr] : -1 - lane;
-    const float a0 = has ? sh.rec_val[w][rr][0] : 0.f, a1 = has ? sh.rec_val[w][rr][1] : 0.f;
-    float v0 = 0.f, v1 = 0.f;
-    bool first = has;
+    if (bad && lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
+    __syncthreads();
+    trace_mark(a, q, 2);
+    // split tiles: thread (w, rr, p) of the first record of a tile sums that
+    // tile's records of pair p in warp order and finishes the pair
+    if (tid < MW * 2 * TP) {
+      const int w = tid / (2 * TP), rr = (tid / TP) & 1, p = tid % TP;
+      if (rr < sh.rec_n[w]) {
+        const int gid = sh.rec_pair[w][rr];
+        bool first = true;
+        for (int w2 = 0; w2 <= w; ++w2)
+          for (int r2 = 0; r2 < sh.rec_n[w2]; ++r2)
+            if ((w2 < w || r2 < rr) && sh.rec_pair[w2][r2] == gid) first = false;
+        if (first) {
+          float v0 = 0.f, v1 = 0.f;
+          for (int w2 = w; w2 < MW; ++w2)
+            for (int r2 = (w2 == w ? rr : 0); r2 < sh.rec_n[w2]; ++r2)
+              if (sh.rec_pair[w2][r2] == gid) {
+                v0 += recv[w2][r2][p][0];
+                v1 += recv[w2][r2][p][1];
+              }
+          const int pl = gid * TP + p;
+          if (P0 + pl < npairs) finish(P0 + pl, v0, v1);
+        }
+      }
+    }
+  } else {
+    int pl = r.ua / CT, c = r.ua - (r.ua / CT) * CT;
+    bool pair_whole = (c == 0);
+    float acc0 = 0.f, acc1 = 0.f;
+    // fp8: the current pair's row scales, loaded when the pair starts (used at its end)
+    float sc0 = 1.f, sc1 = 1.f;
+    if (d.scale && r.ub > r.ua) {
+      sc0 = __ldg(d.scale + 2 * (r.p0 + pl));
+      sc1 = __ldg(d.scale + 2 * (r.p0 + pl) + 1);
+    }
+    for (int k = 0; k < r.nslots; ++k) {
+      const int s = consumed % NS;
+      const bool ok = mbar_wait(&sh.full[warp][s], static_cast<uint32_t>(consumed / NS) & 1u);
+      if (__any_sync(0xffffffffu, !ok)) {
+        bad = true;
+        break;
+      }
+      const uint8_t* buf = ring + static_cast<size_t>(s) * SB;
+      const int u0 = r.ua + k * SU;
+      const int n = min(SU, r.ub - u0);
+      int j = 0;
+      while (j < n) {
+        const int seg = min(n - j, CT - c);
+#pragma unroll 2
+        for (int q = 0; q < seg; ++q) {
+          const int cc = c + q;
+          float xv[EPL];
 #pragma unroll
-    for (int j = 0; j < 2 * MW; ++j) {
-      const int pj = __shfl_sync(0xffffffffu, pr, j);
-      const float b0 = __shfl_sync(0xffffffffu, a0, j), b1 = __shfl_sync(0xffffffffu, a1, j);
-      if (pj == pr) {
-        if (j < lane) first = false;
-        if (j >= lane) {
-          v0 += b0;
-          v1 += b1;
+          for (int pp = 0; pp < NPL; ++pp) {
+            const float4 t = *reinterpret_cast<const float4*>(xs + ((cc * NPL + pp) * 32 + lane) * 4);
+            xv[4 * pp] = t.x; xv[4 * pp + 1] = t.y; xv[4 * pp + 2] = t.z; xv[4 * pp + 3] = t.w;
+          }
+          const uint8_t* ub = buf + (j + q) * UNIT;
+          if constexpr (Q4) {
+            // int4 pair units: the lane's 16 weights are a quarter of one
+            // 64-weight block of each row: two partial sums per row, then the
+            // block scales
+            static_assert(EPL == 16 && UNIT == 576, "int4 unit: 256 code bytes and 8 scales per row");
+            const uint2 c0 = *reinterpret_cast<const uint2*>(ub + lane * 8);
+            const uint2 c1 = *reinterpret_cast<const uint2*>(ub + 256 + lane * 8);
+            const float bs0 = *reinterpret_cast<const float*>(ub + 512 + (lane >> 2) * 4);
+            const float bs1 = *reinterpret_cast<const float*>(ub + 544 + (lane >> 2) * 4);
+            f32x2 p00 = 0ull, p01 = 0ull, p10 = 0ull, p11 = 0ull;  // (row, word) sums of element pairs
+            q4_dot8(c0.x, xv, p00);
+            q4_dot8(c0.y, xv + 8, p01);
+            q4_dot8(c1.x, xv, p10);
+            q4_dot8(c1.y, xv + 8, p11);
+            acc0 = fmaf(sum2(p00) + sum2(p01), bs0, acc0);
+            acc1 = fmaf(sum2(p10) + sum2(p11), bs1, acc1);
+          } else {
+            const uint8_t* u8 = ub + lane * 16;
+            float w0[EPL], w1[EPL];
+            Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8), w0);
+            Unpack<PT>::run(*reinterpret_cast<const uint4*>(u8 + 512), w1);
+            f32x2 t0 = 0ull, t1 = 0ull;  // sums of element pairs
+#pragma unroll
+            for (int e = 0; e < EPL; e += 2) {
+              const f32x2 xe = pk2(xv[e], xv[e + 1]);
+              t0 = fma2(pk2(w0[e], w0[e + 1]), xe, t0);
+              t1 = fma2(pk2(w1[e], w1[e + 1]), xe, t1);
+            }
+            acc0 += sum2(t0);
+            acc1 += sum2(t1);
+          }
+        }
+        j += seg;
+        c += seg;
+        const bool pair_end = (c == CT);
+        const bool range_end = (u0 + j == r.ub);
+        if (pair_end || range_end) {
+          const float s0 = warp_sum(acc0) * sc0, s1 = warp_sum(acc1) * sc1;
+          acc0 = acc1 = 0.f;
+          if (lane == 0) {
+            if (pair_whole && pair_end) {
+              finish(P0 + pl, s0, s1);
+            } else {
+              const int rr = sh.rec_n[warp];
+              sh.rec_pair[warp][rr] = pl;
+              sh.rec_val[warp][rr][0] = s0;
+              sh.rec_val[warp][rr][1] = s1;
+              sh.rec_n[warp] = rr + 1;
+            }
+          }
+          if (pair_end) {
+            ++pl;
+            c = 0;
+            pair_whole = true;
+            if (d.scale && r.ua + (u0 - r.ua) + j < r.ub) {
+              sc0 = __ldg(d.scale + 2 * (r.p0 + pl));
+              sc1 = __ldg(d.scale + 2 * (r.p0 + pl) + 1);
+            }
+          }
         }
       }
+      __syncwarp();  // the slot was only read: no proxy fence needed before refilling it
+      ++consumed;
+      if (lane == 0) st.issue_next(a, ring, sh.full[warp], cta, G, warp, pos, qkv_n);
     }
-    if (first) finish(r.p0 + pr, v0, v1);
+    if (bad && lane == 0) atomicOr(a.guard, GUARD_TIMEOUT);
+    __syncthreads();
+    trace_mark(a, q, 2);
+    // Pairs split between warps: at most two records per warp, lane 2w + rr of
+    // warp 0 holding record rr of warp w.  Every record of a pair is summed in
+    // warp order by the lane of its first record, which finishes the pair; a
+    // fixed 16-step shuffle loop, so the lanes never diverge.
+    if (warp == 0) {
+      const int w = lane >> 1, rr = lane & 1;
+      const bool has = lane < 2 * MW && rr < sh.rec_n[w];
+      const int pr = has ? sh.rec_pair[w][rr] : -1 - lane;
+      const float a0 = has ? sh.rec_val[w][rr][0] : 0.f, a1 = has ? sh.rec_val[w][rr][1] : 0.f;
+      float v0 = 0.f, v1 = 0.f;
+      bool first = has;
+#pragma unroll
+      for (int j = 0; j < 2 * MW; ++j) {
+        const int pj = __shfl_sync(0xffffffffu, pr, j);
+        const float b0 = __shfl_sync(0xffffffffu, a0, j), b1 = __shfl_sync(0xffffffffu, a1, j);
+        if (pj == pr) {
+          if (j < lane) first = false;
+          if (j >= lane) {
+            v0 += b0;
+            v1 += b1;
+          }
+        }
+      }
+      if (first) finish(P0 + pr, v0, v1);
+    }
   }
   return __syncthreads_and(!bad) != 0;
 }
@@ -1362,7 +1516,9 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const __grid_constan
     const int N = kind == 0 ? qkv_n : kind == 2 ? 2 * a.inter : kind == 4 ? a.vocab : a.hidden;
     const int CT = kind == 0 ? a.g_qkv.CT : kind == 1 ? a.g_o.CT : kind == 2 ? a.g_gu.CT
                  : kind == 3 ? a.g_down.CT : a.g_lm.CT;
-    sh.wr[kind][w] = g_split(N, CT, cta, G, w);
+    // int4 tiled kinds own rows in tiles of 16: the split counts tiles as its "pairs"
+    const bool tl = std::is_same<PT, q4_block64>::value && q4_tiled(kind);
+    sh.wr[kind][w] = g_split(tl ? 2 * ((N + kQ4GroupRows - 1) / kQ4GroupRows) : N, CT, cta, G, w);
   }
   if (tid == 5 * MW) sh.item = a_split(a, min(cta, a.nkv * a.nsplit - 1), pos + 1);
   for (int i = tid; i < 2 * a.n_layers; i += MT)

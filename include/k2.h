@@ -395,7 +395,7 @@ typedef enum {
   K2_OPT_L2_AHEAD = 8,    /* persistent step: at the start of a phase, each warp fetches into L2 this many
                              of its next weight / K-V slots beyond those in flight (0 .. 64; default 2) */
   K2_OPT_L2_AHEAD_PHASES = 9, /* the phase kinds that do so, bit j for kind j (0 QKV, 1 attention, 2 o_proj,
-                             3 gate/up, 4 down, 5 lm_head); default 0x18: gate/up, down */
+                             3 gate/up, 4 down, 5 lm_head); default 0x18 (gate/up, down), 0 for fp8 and int4 weights */
   K2_OPT_TRACE = 10,      /* measurement: the device address (as an integer; 0 = off) of a caller's buffer of
                              (5 * n_layers + 2) * persistent_grid * 4 uint64 words; each persistent step then
                              writes, per phase q and CTA c, the SM's %clock64 at [(q * grid + c) * 4 + k]:
