@@ -116,18 +116,21 @@ Layout layout_of(const k2_config& c) {
   l.slog = take(sizeof(float) * static_cast<size_t>(s.B) * s.V);
   l.sample_row = sample_row_bytes(s.V);
   l.sscr = take(kSampleBarBytes + static_cast<size_t>(s.B) * l.sample_row);
-  {  // one fp32 scale per packed (pair-padded) row of every fp8 matrix
+  {  // one fp32 scale per packed (pair- or tile-padded) row of every fp8 matrix
     const bool f8 = c.weight_dtype == K2_F8;
-    auto rows = [&](int N) { return f8 ? sizeof(float) * 2 * static_cast<size_t>((N + 1) / 2) : 0; };
-    l.sqkv_layer = rows(s.qkv_n);
-    l.so_layer = rows(s.H);
-    l.sgu_layer = rows(2 * s.I);
-    l.sdown_layer = rows(s.H);
+    auto rows = [&](int N, int kind) {
+      const size_t pad = tiled_kind(kind) ? kQ4GroupRows : 2;
+      return f8 ? sizeof(float) * pad * ((static_cast<size_t>(N) + pad - 1) / pad) : 0;
+    };
+    l.sqkv_layer = rows(s.qkv_n, 0);
+    l.so_layer = rows(s.H, 1);
+    l.sgu_layer = rows(2 * s.I, 2);
+    l.sdown_layer = rows(s.H, 3);
     l.sqkv = take(l.sqkv_layer * s.L);
     l.so = take(l.so_layer * s.L);
     l.sgu = take(l.sgu_layer * s.L);
     l.sdown = take(l.sdown_layer * s.L);
-    l.slm = take(rows(s.V));
+    l.slm = take(rows(s.V, 4));
   }
   l.pchunk = (c.weight_dtype == K2_BF16 || c.weight_dtype == K2_F8)
                  ? static_cast<int>(align_up(std::min(kPrefillChunk, s.ctx), 128))
@@ -151,10 +154,12 @@ Layout layout_of(const k2_config& c) {
     l.vpi = take(nv * kArgmaxPartsMax * 4);
   }
   const size_t scratch_end = o;
-  // int4: codes and block scales in kQ4Unit units (pair or tile units by GEMV
-  // kind, q4_tiled); else wb-byte weights in 1024-byte units
+  // fp8 / int4: pair or tile units by GEMV kind (tiled_kind); else wb-byte
+  // weights in 1024-byte units
   auto pbytes = [&](int N, int K, int kind) {
-    return c.weight_dtype == K2_Q4 ? q4_packed_bytes(N, K, q4_tiled(kind)) : packed_bytes(N, K, s.wb);
+    return c.weight_dtype == K2_Q4   ? q4_packed_bytes(N, K, tiled_kind(kind))
+           : c.weight_dtype == K2_F8 ? f8_packed_bytes(N, K, tiled_kind(kind))
+                                     : packed_bytes(N, K, s.wb);
   };
   l.wqkv_layer = align_up(pbytes(s.qkv_n, s.H, 0), kAlign);
   l.wo_layer = align_up(pbytes(s.H, s.nq * s.d, 1), kAlign);
@@ -610,14 +615,15 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   const int kvdt = c->cfg.kv_dtype == K2_F32 ? 0 : c->cfg.kv_dtype;
   c->mega_ok = false;
   if (!mega_supported(s.wf, s.d, s.rep, kvdt)) return cudaSuccess;
-  const bool q4 = c->cfg.weight_dtype == K2_Q4;
+  const bool q4 = c->cfg.weight_dtype == K2_Q4, f8 = c->cfg.weight_dtype == K2_F8;
   const PackedGemvArgs* plans[5] = {&c->p_qkv, &c->p_o, &c->p_gu, &c->p_down, &c->p_lm};
   for (int kind = 0; kind < 5; ++kind) {
     const PackedGemvArgs* p = plans[kind];
     // the input vector, padded to whole chunks (int4: 64-weight blocks for
     // tiles, 512-weight chunks for pairs), fits its buffer (a gain phase: 4096 values)
-    const int q4c = q4_tiled(kind) ? kQ4Block : kQ4Chunk;
-    const size_t kp = q4 ? static_cast<size_t>((p->K + q4c - 1) / q4c) * q4c : p->x_bytes / 4;
+    const int q4c = tiled_kind(kind) ? kQ4Block : kQ4Chunk;
+    const size_t kp = q4 || (f8 && tiled_kind(kind)) ? static_cast<size_t>((p->K + q4c - 1) / q4c) * q4c
+                                                     : p->x_bytes / 4;
     if (p->x_bytes > static_cast<uint32_t>(kMegaXBytes) || kp * 4 > static_cast<size_t>(kMegaXBytes)) return cudaSuccess;
     if (p->gain && kp > 4096) return cudaSuccess;
   }
@@ -625,8 +631,8 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   int grid = mega_max_grid(s.wf, s.d, s.rep, kvdt);
   // every CTA must own rows of every layer GEMV (the dataflow waits rely on
-  // it); int4 rows of the tiled kinds are owned in 16-row tiles (8 pairs)
-  auto rb = [&](int kind) { return q4 && q4_tiled(kind) ? kQ4GroupRows / 2 : 1; };  // pairs per ownership unit
+  // it); fp8 and int4 rows of the tiled kinds are owned in 16-row tiles (8 pairs)
+  auto rb = [&](int kind) { return (q4 || f8) && tiled_kind(kind) ? kQ4GroupRows / 2 : 1; };  // pairs per owner unit
   auto owned = [&](int N, int kind) { return ((N + 1) / 2 + rb(kind) - 1) / rb(kind); };
   grid = std::min(grid, std::min(owned(s.qkv_n, 0), std::min(owned(s.H, 1), owned(2 * s.I, 2))));
   if (grid < s.nkv) return cudaSuccess;
@@ -665,8 +671,9 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   auto gplan = [&](const PackedGemvArgs& p, int kind) {  // packed units per row pair (int4 tiles: per tile)
     MegaGemv g;
-    g.CT = !q4 ? (p.K * s.wb + 511) / 512 : q4_tiled(kind) ? (p.K + kQ4Block - 1) / kQ4Block
-                                                           : (p.K + kQ4Chunk - 1) / kQ4Chunk;
+    g.CT = (q4 || f8) && tiled_kind(kind) ? (p.K + kQ4Block - 1) / kQ4Block
+           : q4                              ? (p.K + kQ4Chunk - 1) / kQ4Chunk
+                                             : (p.K * s.wb + 511) / 512;
     return g;
   };
   MegaArgs& m = c->mega;
@@ -1289,7 +1296,7 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   const Sizes& z = c->s;
   if (cfg->weight_dtype == K2_Q4) {  // quantize the bf16 inputs into int4 units (codes + block scales)
     for (int l = 0; l < z.L && e == cudaSuccess; ++l) {
-      const auto lay = [](int kind) { return q4_tiled(kind) ? Q4_TILES : Q4_PAIRS; };
+      const auto lay = [](int kind) { return tiled_kind(kind) ? LAYOUT_TILES : LAYOUT_PAIRS; };
       e = launch_q4_pack(static_cast<uint8_t*>(c->wqkv(l)), nullptr, w->wq[l], w->wk[l], w->wv[l], PACK_QKV, z.qkv_n,
                          z.H, z.nq, z.nkv, z.d, lay(0), s);
       if (e == cudaSuccess)
@@ -1304,27 +1311,28 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
     }
     if (e == cudaSuccess)
       e = launch_q4_pack(static_cast<uint8_t*>(c->wlm()), nullptr, w->lm_head, nullptr, nullptr, PACK_PLAIN, z.V, z.H,
-                         0, 0, 1, q4_tiled(4) ? Q4_TILES : Q4_PAIRS, s);
+                         0, 0, 1, tiled_kind(4) ? LAYOUT_TILES : LAYOUT_PAIRS, s);
   }
   if (cfg->weight_dtype == K2_F8) {  // quantize the bf16 inputs into fp8 rows + scales
     auto sc = [&](size_t base, size_t stride, int l) { return reinterpret_cast<float*>(ws + base + stride * l); };
+    const auto lay = [](int kind) { return tiled_kind(kind) ? LAYOUT_TILES : LAYOUT_PAIRS; };
     const auto& L = c->lay;
     for (int l = 0; l < z.L && e == cudaSuccess; ++l) {
       e = launch_quant_pack(static_cast<uint8_t*>(c->wqkv(l)), sc(L.sqkv, L.sqkv_layer, l), w->wq[l], w->wk[l],
-                            w->wv[l], PACK_QKV, z.qkv_n, z.H, z.nq, z.nkv, z.d, true, s);
+                            w->wv[l], PACK_QKV, z.qkv_n, z.H, z.nq, z.nkv, z.d, lay(0), s);
       if (e == cudaSuccess)
         e = launch_quant_pack(static_cast<uint8_t*>(c->wop(l)), sc(L.so, L.so_layer, l), w->wo[l], nullptr, nullptr,
-                              PACK_PLAIN, z.H, z.nq * z.d, 0, 0, 1, true, s);
+                              PACK_PLAIN, z.H, z.nq * z.d, 0, 0, 1, lay(1), s);
       if (e == cudaSuccess)
         e = launch_quant_pack(static_cast<uint8_t*>(c->wgu(l)), sc(L.sgu, L.sgu_layer, l), w->w_gate[l], w->w_up[l],
-                              nullptr, PACK_GATEUP, 2 * z.I, z.H, 0, 0, 1, true, s);
+                              nullptr, PACK_GATEUP, 2 * z.I, z.H, 0, 0, 1, lay(2), s);
       if (e == cudaSuccess)
         e = launch_quant_pack(static_cast<uint8_t*>(c->wdown(l)), sc(L.sdown, L.sdown_layer, l), w->w_down[l], nullptr,
-                              nullptr, PACK_PLAIN, z.H, z.I, 0, 0, 1, true, s);
+                              nullptr, PACK_PLAIN, z.H, z.I, 0, 0, 1, lay(3), s);
     }
     if (e == cudaSuccess)
       e = launch_quant_pack(static_cast<uint8_t*>(c->wlm()), reinterpret_cast<float*>(ws + L.slm), w->lm_head, nullptr,
-                            nullptr, PACK_PLAIN, z.V, z.H, 0, 0, 1, true, s);
+                            nullptr, PACK_PLAIN, z.V, z.H, 0, 0, 1, lay(4), s);
   }
   for (int l = 0; l < z.L && e == cudaSuccess && !quantized(cfg->weight_dtype); ++l) {
     e = launch_pack(c->wqkv(l), w->wq[l], w->wk[l], w->wv[l], PACK_QKV, z.qkv_n, z.H, z.wb, z.nq, z.nkv, z.d, s);
@@ -1338,10 +1346,13 @@ k2_status k2_init_weights(const k2_config* cfg, const k2_weights* w, void* d_wor
   if (e == cudaSuccess && !quantized(cfg->weight_dtype))
     e = launch_pack(c->wlm(), w->lm_head, nullptr, nullptr, PACK_PLAIN, z.V, z.H, z.wb, 0, 0, 1, s);
   for (int l = 0; l < z.L && e == cudaSuccess && cfg->weight_dtype == K2_F8 && c->lay.pchunk > 0; ++l) {
-    e = launch_f8_expand(c->tcw(l, 0), static_cast<const uint8_t*>(c->wqkv(l)), z.qkv_n, z.H, s);
-    if (e == cudaSuccess) e = launch_f8_expand(c->tcw(l, 1), static_cast<const uint8_t*>(c->wop(l)), z.H, z.nq * z.d, s);
-    if (e == cudaSuccess) e = launch_f8_expand(c->tcw(l, 2), static_cast<const uint8_t*>(c->wgu(l)), 2 * z.I, z.H, s);
-    if (e == cudaSuccess) e = launch_f8_expand(c->tcw(l, 3), static_cast<const uint8_t*>(c->wdown(l)), z.H, z.I, s);
+    e = launch_f8_expand(c->tcw(l, 0), static_cast<const uint8_t*>(c->wqkv(l)), z.qkv_n, z.H, tiled_kind(0), s);
+    if (e == cudaSuccess)
+      e = launch_f8_expand(c->tcw(l, 1), static_cast<const uint8_t*>(c->wop(l)), z.H, z.nq * z.d, tiled_kind(1), s);
+    if (e == cudaSuccess)
+      e = launch_f8_expand(c->tcw(l, 2), static_cast<const uint8_t*>(c->wgu(l)), 2 * z.I, z.H, tiled_kind(2), s);
+    if (e == cudaSuccess)
+      e = launch_f8_expand(c->tcw(l, 3), static_cast<const uint8_t*>(c->wdown(l)), z.H, z.I, tiled_kind(3), s);
   }
   if (e != cudaSuccess) {
     g_init_error = std::string("repack: ") + cudaGetErrorString(e);
@@ -1957,7 +1968,7 @@ k2_status k2_quantize_fp8(const void* d_src, int32_t rows, int32_t cols, uint8_t
                           void* stream) {
   if (!d_src || !d_codes || !d_scales || rows < 0 || cols < 1) return K2_ERR_ARG;
   const cudaError_t e = launch_quant_pack(d_codes, d_scales, d_src, nullptr, nullptr, PACK_PLAIN, rows, cols, 0, 0, 1,
-                                          false, static_cast<cudaStream_t>(stream));
+                                          LAYOUT_PLAIN, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? K2_OK : K2_ERR_CUDA;
 }
 
@@ -1965,7 +1976,7 @@ k2_status k2_quantize_q4(const void* d_src, int32_t rows, int32_t cols, int8_t* 
                          void* stream) {
   if (!d_src || !d_codes || !d_scales || rows < 0 || cols < 1) return K2_ERR_ARG;
   const cudaError_t e = launch_q4_pack(reinterpret_cast<uint8_t*>(d_codes), d_scales, d_src, nullptr, nullptr,
-                                       PACK_PLAIN, rows, cols, 0, 0, 1, Q4_PLAIN, static_cast<cudaStream_t>(stream));
+                                       PACK_PLAIN, rows, cols, 0, 0, 1, LAYOUT_PLAIN, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? K2_OK : K2_ERR_CUDA;
 }
 }  // extern "C"

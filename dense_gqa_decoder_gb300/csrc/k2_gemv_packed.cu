@@ -414,10 +414,19 @@ __global__ void pack_kernel(WT* __restrict__ dst, const WT* __restrict__ s0, con
 // (the row mapping of pack_kernel) s = max|w| / 448 and code = E4M3(w / s),
 // nearest with ties to even, saturating; a zero row gets s = 0 and codes 0.
 // packed != 0: codes in the packed pair/chunk layout; else row-major [N][K].
+// byte of packed row R, weight e in the fp8 tile layout (described with kWfmtQ4)
+__device__ __forceinline__ size_t f8_tile_offset(int R, int e, int nb) {
+  const int rl = R % kQ4GroupRows, pair = rl >> 1, member = rl & 1;
+  const int kb = e & 63, j = kb >> 4, kk = kb & 15, t = (kk & 7) >> 1, hi8 = kk >> 3, odd = kk & 1;
+  const int lane = pair * 4 + t;
+  return (static_cast<size_t>(R / kQ4GroupRows) * nb + (e >> 6)) * 1024 + (j >> 1) * 512 + lane * 16 + (j & 1) * 8 +
+         4 * hi8 + 2 * member + odd;
+}
+
 __global__ void quant_pack_kernel(uint8_t* __restrict__ dst, float* __restrict__ scales,
                                   const __nv_bfloat16* __restrict__ s0, const __nv_bfloat16* __restrict__ s1,
                                   const __nv_bfloat16* __restrict__ s2, int mode, int N, int K, int CT, int nq,
-                                  int nkv, int d, int packed) {
+                                  int nkv, int d, int layout) {
   constexpr int CH = 512;  // codes per row per chunk
   __shared__ float red[32];
   const int R = blockIdx.x, tid = threadIdx.x;
@@ -436,14 +445,17 @@ __global__ void quant_pack_kernel(uint8_t* __restrict__ dst, float* __restrict__
   __syncthreads();
   const float scale = red[0] / 448.0f;
   if (tid == 0) scales[R] = scale;
-  const int n = packed ? CT * CH : K;
+  const int nb = (K + 63) / 64;  // tile units per tile
+  const int n = layout == LAYOUT_PAIRS ? CT * CH : layout == LAYOUT_TILES ? nb * 64 : K;
   for (int e = tid; e < n; e += blockDim.x) {
     const float w = (src != nullptr && e < K) ? __bfloat162float(src[e]) : 0.f;
     const uint8_t code = scale > 0.f ? static_cast<uint8_t>(__nv_cvt_float_to_fp8(w / scale, __NV_SATFINITE, __NV_E4M3))
                                      : static_cast<uint8_t>(0);
-    if (packed) {
+    if (layout == LAYOUT_PAIRS) {
       const int c = e / CH, i = e - c * CH;
       dst[(static_cast<size_t>(R >> 1) * CT + c) * 2 * CH + (R & 1) * CH + i] = code;
+    } else if (layout == LAYOUT_TILES) {
+      dst[f8_tile_offset(R, e, nb)] = code;
     } else {
       dst[static_cast<size_t>(R) * K + e] = code;
     }
@@ -482,14 +494,14 @@ __global__ void __launch_bounds__(kQ4Chunk / 4) q4_pack_kernel(uint8_t* __restri
 #pragma unroll
   for (int i = 0; i < 4; ++i) q[i] = s > 0.f ? max(-7, min(7, __float2int_rn(__fdiv_rn(w[i], s)))) : 0;
   const int blk = tid >> 4;  // the block within the chunk
-  if (layout == Q4_PAIRS) {
+  if (layout == LAYOUT_PAIRS) {
     uint8_t* unit = dst + (static_cast<size_t>(R >> 1) * CT + c) * kQ4Unit;
     const uint32_t b0 = static_cast<uint32_t>(q[0] + 8) | (static_cast<uint32_t>(q[1] + 8) << 4);
     const uint32_t b1 = static_cast<uint32_t>(q[2] + 8) | (static_cast<uint32_t>(q[3] + 8) << 4);
     *reinterpret_cast<uint16_t*>(unit + (R & 1) * (kQ4Chunk / 2) + 2 * tid) = static_cast<uint16_t>(b0 | (b1 << 8));
     if ((tid & 15) == 0)
       *reinterpret_cast<float*>(unit + kQ4Chunk + (R & 1) * (kQ4Chunk / kQ4Block) * 4 + blk * 4) = s;
-  } else if (layout == Q4_TILES) {
+  } else if (layout == LAYOUT_TILES) {
     const int nb = (K + kQ4Block - 1) / kQ4Block;  // blocks (units) per tile
     const int b = c * (kQ4Chunk / kQ4Block) + blk;
     if (b < nb) {
@@ -621,20 +633,29 @@ cudaError_t launch_pack(void* dst, const void* src0, const void* src1, const voi
 
 // One CTA of 256 threads per (packed row R, bf16 chunk c): weight k = 256 c + t.
 __global__ void __launch_bounds__(256) f8_expand_kernel(__nv_bfloat16* __restrict__ dst,
-                                                        const uint8_t* __restrict__ src, int CT8, int CT16) {
+                                                        const uint8_t* __restrict__ src, int CT8, int CT16, int nb) {
   const int R = blockIdx.x, c = blockIdx.y, k = c * 256 + threadIdx.x;
   const int c8 = k >> 9, i8 = k & 511;
-  const uint8_t code = src[(static_cast<size_t>(R >> 1) * CT8 + c8) * 1024 + (R & 1) * 512 + i8];
+  // nb > 0: the source is in tile units (nb per tile); weights past the tile's
+  // blocks are zero
+  const uint8_t code = nb > 0 ? ((k >> 6) < nb ? src[f8_tile_offset(R, k, nb)] : static_cast<uint8_t>(0))
+                              : src[(static_cast<size_t>(R >> 1) * CT8 + c8) * 1024 + (R & 1) * 512 + i8];
   const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);
   dst[(static_cast<size_t>(R >> 1) * CT16 + c) * 512 + (R & 1) * 256 + threadIdx.x] =
       __float2bfloat16_rn(__half2float(__half(h)));
 }
 
-cudaError_t launch_f8_expand(void* dst, const uint8_t* src, int N, int K, cudaStream_t s) {
+cudaError_t launch_f8_expand(void* dst, const uint8_t* src, int N, int K, bool tiles, cudaStream_t s) {
   const int CT8 = (K + 511) / 512, CT16 = (K + 255) / 256, rows = 2 * ((N + 1) / 2);
   if (rows <= 0 || CT16 <= 0) return cudaSuccess;
-  f8_expand_kernel<<<dim3(rows, CT16), 256, 0, s>>>(static_cast<__nv_bfloat16*>(dst), src, CT8, CT16);
+  f8_expand_kernel<<<dim3(rows, CT16), 256, 0, s>>>(static_cast<__nv_bfloat16*>(dst), src, CT8, CT16,
+                                                    tiles ? (K + 63) / 64 : 0);
   return cudaGetLastError();
+}
+
+size_t f8_packed_bytes(int N, int K, bool tiles) {
+  if (!tiles) return packed_bytes(N, K, 1);
+  return (static_cast<size_t>(N) + kQ4GroupRows - 1) / kQ4GroupRows * ((static_cast<size_t>(K) + 63) / 64) * 1024;
 }
 
 size_t q4_packed_bytes(int N, int K, bool tiles) {
@@ -650,11 +671,11 @@ size_t q4_packed_bytes(int N, int K, bool tiles) {
 cudaError_t launch_q4_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
                            int mode, int N, int K, int nq, int nkv, int d, int layout, cudaStream_t s) {
   const int CT = (K + kQ4Chunk - 1) / kQ4Chunk;
-  const int rows = layout == Q4_TILES   ? kQ4GroupRows * ((N + kQ4GroupRows - 1) / kQ4GroupRows)
-                   : layout == Q4_PAIRS ? 2 * ((N + 1) / 2)
+  const int rows = layout == LAYOUT_TILES   ? kQ4GroupRows * ((N + kQ4GroupRows - 1) / kQ4GroupRows)
+                   : layout == LAYOUT_PAIRS ? 2 * ((N + 1) / 2)
                                         : N;
   if (rows <= 0 || CT <= 0) return cudaSuccess;
-  if (layout == Q4_TILES) {
+  if (layout == LAYOUT_TILES) {
     const cudaError_t e = cudaMemsetAsync(dst, 0, q4_packed_bytes(N, K, true), s);
     if (e != cudaSuccess) return e;
   }
@@ -666,14 +687,16 @@ cudaError_t launch_q4_pack(uint8_t* dst, float* scales, const void* src0, const 
 }
 
 cudaError_t launch_quant_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
-                              int mode, int N, int K, int nq, int nkv, int d, bool packed, cudaStream_t s) {
+                              int mode, int N, int K, int nq, int nkv, int d, int layout, cudaStream_t s) {
   const int CT = (K + 511) / 512;
-  const int rows = packed ? 2 * ((N + 1) / 2) : N;
+  const int rows = layout == LAYOUT_TILES   ? kQ4GroupRows * ((N + kQ4GroupRows - 1) / kQ4GroupRows)
+                   : layout == LAYOUT_PAIRS ? 2 * ((N + 1) / 2)
+                                            : N;
   if (rows <= 0) return cudaSuccess;
   quant_pack_kernel<<<rows, 256, 0, s>>>(dst, scales, static_cast<const __nv_bfloat16*>(src0),
                                          static_cast<const __nv_bfloat16*>(src1),
                                          static_cast<const __nv_bfloat16*>(src2), mode, N, K, CT, nq, nkv, d,
-                                         packed ? 1 : 0);
+                                         layout);
   return cudaGetLastError();
 }
 

@@ -131,23 +131,28 @@ size_t packed_smem_bytes(const PackedGemvArgs& a);
 //                each head ordered (0, d/2), (1, d/2 + 1), ... (split-half RoPE pairs)
 //   PACK_GATEUP: row 2i = src0 row i, row 2i + 1 = src1 row i
 enum PackMode : int { PACK_PLAIN = 0, PACK_QKV = 1, PACK_GATEUP = 2 };
+// Layouts of quantized packed matrices (described with kWfmtQ4): plain
+// row-major codes, pair units, or 16-row tile units for the tensor cores.
+enum { LAYOUT_PLAIN = 0, LAYOUT_PAIRS = 1, LAYOUT_TILES = 2 };
 // fp8 (E4M3) rows with one fp32 scale per row from bf16 sources (the row mapping
-// of launch_pack); packed: the pair/chunk layout with 512 codes per chunk,
-// else row-major codes [N][K].  scales get one entry per (padded) row.
+// of launch_pack); LAYOUT_PAIRS: the pair/chunk layout with 512 codes per
+// chunk; LAYOUT_TILES: fp8 tile units; LAYOUT_PLAIN: row-major codes [N][K].
+// scales get one entry per (padded) row.
 cudaError_t launch_quant_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
-                              int mode, int N, int K, int nq, int nkv, int d, bool packed, cudaStream_t s);
+                              int mode, int N, int K, int nq, int nkv, int d, int layout, cudaStream_t s);
+size_t f8_packed_bytes(int N, int K, bool tiles);
 // int4 block quantization (symmetric, codes in [-7, 7], s = max|w| / 7 per 64
 // weights of a row, nearest with ties to even) of bf16 sources, with the row
-// mapping of launch_pack.  layout Q4_PAIRS / Q4_TILES: the int4 pair or tile
+// mapping of launch_pack.  layout LAYOUT_PAIRS / LAYOUT_TILES: the int4 pair or tile
 // units (described with kWfmtQ4; dst only, scales unused; tiles: dst is
-// cleared first); Q4_PLAIN: int8 codes [N][K] and scales [N][ceil(K / 64)].
-enum { Q4_PLAIN = 0, Q4_PAIRS = 1, Q4_TILES = 2 };
+// cleared first); LAYOUT_PLAIN: int8 codes [N][K] and scales [N][ceil(K / 64)].
 cudaError_t launch_q4_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
                            int mode, int N, int K, int nq, int nkv, int d, int layout, cudaStream_t s);
 size_t q4_packed_bytes(int N, int K, bool tiles);
-// The fp8 codes of a packed matrix (512 per chunk and row) as bf16 values (exact:
-// every E4M3 value is a bf16 value) in the bf16 packed layout (256 per chunk and row).
-cudaError_t launch_f8_expand(void* dst, const uint8_t* src, int N, int K, cudaStream_t s);
+// The fp8 codes of a packed matrix (pair units of 512 per chunk and row, or
+// tile units) as bf16 values (exact: every E4M3 value is a bf16 value) in the
+// bf16 packed layout (256 per chunk and row).
+cudaError_t launch_f8_expand(void* dst, const uint8_t* src, int N, int K, bool tiles, cudaStream_t s);
 cudaError_t launch_pack(void* dst, const void* src0, const void* src1, const void* src2, int mode, int N, int K,
                         int wbytes, int nq, int nkv, int d, cudaStream_t s);
 
@@ -341,15 +346,24 @@ constexpr int kMegaMaxLayers = 64;            // norm-gain pointers kept in shar
 // kernel: the bytes of one weight for fp32 (4), bf16 (2) and fp8 E4M3 (1), or
 // kWfmtQ4 for int4 codes with one fp32 scale per 64 weights of a row.
 //
-// int4 matrices come in two layouts.  Pair units (QKV, o_proj, down): a
-// 512-weight chunk of both rows of a pair -- row 0's 256 bytes of codes (the
-// code of weight 2i in the low nibble of byte i), row 1's, then row 0's 8 block
-// scales and row 1's.  Tile units (gate/up and lm_head, q4_tiled kinds, whose
-// many rows keep 16-row ownership balanced over the SMs), for the tensor
-// cores: one unit holds one 64-weight block of 16 packed rows (8 row pairs, a
-// "tile"), units ordered tile-major, block minor.  Tile row m (the A row of mma.sync m16n8k16) is packed row
-// 2 (m % 8) + m / 8 of the group, so rows m and m + 8 are the two rows of pair
-// m % 8.  Bytes 0..511: 32 lanes x 4 words, word j (MMA j: weights 16j ..
+// fp8 and int4 matrices come in two layouts.  Pair units (QKV, o_proj, down):
+// a 512-weight chunk of both rows of a pair -- fp8: row 0's 512 codes, then
+// row 1's; int4: row 0's 256 bytes of codes (the code of weight 2i in the low
+// nibble of byte i), row 1's, then row 0's 8 block scales and row 1's.  Tile
+// units (gate/up and lm_head, the tiled_kind kinds, whose many rows keep
+// 16-row ownership balanced over the SMs), for the tensor cores: one unit
+// holds one 64-weight block of 16 packed rows (8 row pairs, a "tile"), units
+// ordered tile-major, block minor.  Tile row m (the A row of mma.sync
+// m16n8k16) is packed row 2 (m % 8) + m / 8 of the tile, so rows m and m + 8
+// are the two rows of pair m % 8.
+//
+// fp8 tile unit (1024 bytes): for MMA j (weights 16j .. 16j + 15 of the
+// block), lane 4 g + t's 8 codes -- rows g, g, g + 8, g + 8 at positions
+// 2t, 2t + 1, then the same rows at 2t + 8, 2t + 9 -- sit at byte
+// 512 (j / 2) + 16 lane + 8 (j % 2); each code pair converts to one A fragment
+// register (fp8x2 -> f16x2, exact).
+//
+// int4 tile unit: bytes 0..511: 32 lanes x 4 words, word j (MMA j: weights 16j ..
 // 16j + 15 of the block) of lane 4 g + t holding the eight nibbles (code + 8)
 // of rows g and g + 8 at block positions 16j + {2t, 2t + 1, 2t + 8, 2t + 9},
 // at bit 4 (m >= 8) + 8 (position >= 2t + 8) + 16 (odd position) -- so that
@@ -362,8 +376,8 @@ constexpr int kQ4Chunk = 512;  // weights of a row handled by one CTA of the qua
 constexpr int kQ4Unit = 576;
 constexpr int kQ4GroupRows = 16;
 // GEMV kinds of the persistent step (0 QKV, 1 o_proj, 2 gate/up, 3 down,
-// 4 lm_head) whose int4 weights use the tile layout
-__host__ __device__ constexpr bool q4_tiled(int kind) { return kind == 2 || kind == 4; }
+// 4 lm_head) whose fp8 and int4 weights use the tile layout
+__host__ __device__ constexpr bool tiled_kind(int kind) { return kind == 2 || kind == 4; }
 
 bool mega_supported(int wfmt, int head_dim, int rep, int kv_dtype);
 cudaError_t mega_init_attrs(int wfmt, int head_dim, int rep, int kv_dtype);

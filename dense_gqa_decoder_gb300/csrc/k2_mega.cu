@@ -224,6 +224,27 @@ __device__ __forceinline__ void q4_tile_mma(uint32_t w, const uint32_t* xf, int 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y));
 }
 
+// One mma.sync m16n8k16 over 16 weights of the 16 rows of an fp8 tile: the
+// lane's two tile words (layout with kWfmtQ4) hold its 8 E4M3 codes, each pair
+// converted to an A fragment register (exact); B as in q4_tile_mma.
+__device__ __forceinline__ void f8_tile_mma(uint32_t w0, uint32_t w1, const uint32_t* xf, int lane, float* d) {
+  uint32_t a[4];
+  const uint32_t w[2] = {w0, w1};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2_raw h =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i >> 1] >> (16 * (i & 1))), __NV_E4M3);
+    a[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  uint2 b = make_uint2(0u, 0u);
+  if (lane < 8) b = *reinterpret_cast<const uint2*>(xf + 2 * lane);
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y));
+}
+
 // ---- static description of the step ------------------------------------------------
 // GEMV kinds: 0 QKV, 1 o_proj, 2 gate/up, 3 down, 4 lm_head.  Row ranges do not
 // depend on the layer, so they are computed once per launch (shared memory).
@@ -582,9 +603,10 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
   float* xs = reinterpret_cast<float*>(smem + kMegaRingBytes);
   uint8_t* ring = smem + static_cast<size_t>(warp) * NS * SB;
   const GRange r = g_range<SU>(d, sh, warp);
-  // int4 gate/up and lm_head: r.p0 / r.p1 count 16-row tiles (8 pairs each);
-  // P0 / P1 are pairs
-  const bool tiles = Q4 && q4_tiled(d.kind);
+  // fp8 / int4 gate/up and lm_head: r.p0 / r.p1 count 16-row tiles (8 pairs
+  // each); P0 / P1 are pairs
+  constexpr bool F8 = std::is_same<PT, __nv_fp8_e4m3>::value;
+  const bool tiles = (Q4 || F8) && tiled_kind(d.kind);
   const int npairs = (d.N + 1) / 2;
   const int P0 = tiles ? r.p0 * (kQ4GroupRows / 2) : r.p0;
   const int P1 = tiles ? min(r.p1 * (kQ4GroupRows / 2), npairs) : r.p1;
@@ -672,7 +694,7 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
       }
     }
     if (tiles) {
-      // the B fragments of the int4 tile MMAs: per 16 inputs, word (4 h + t) * 2 + r
+      // the B fragments of the tile MMAs: per 16 inputs, word (4 h + t) * 2 + r
       // of lane 4 h + t holds inputs 2t + 8r, 2t + 8r + 1 as fp16 (h = 0: high
       // halves, h = 1: low halves)
       uint32_t* xf = reinterpret_cast<uint32_t*>(xs);
@@ -738,10 +760,11 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
   };
 
   if (tiles) {
-    // int4 tiles: unit (tile gi of the CTA's range, block b); lane 4 g + t
+    // tiles: unit (tile gi of the CTA's range, block b); lane 4 g + t
     // accumulates rows g and g + 8 of the tile -- pair 8 gi + g -- in acc0 / acc1
-    // (meaningful for t = 0); a tile split between warps leaves records of
-    // its 8 pairs, summed in warp order below
+    // (meaningful for t = 0; fp8: scaled by the rows' scales when the tile
+    // ends); a tile split between warps leaves records of its 8 pairs, summed
+    // in warp order below
     const uint32_t* xf = reinterpret_cast<const uint32_t*>(xs);
     constexpr int TP = kQ4GroupRows / 2;  // pairs per tile
     const int g8 = lane >> 2;
@@ -762,20 +785,35 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
 #pragma unroll 2
       for (int j = 0; j < n; ++j) {
         const uint8_t* ub = buf + j * UNIT;
-        const uint4 cw = *reinterpret_cast<const uint4*>(ub + lane * 16);
-        const float2 sc = *reinterpret_cast<const float2*>(ub + 512 + g8 * 8);
         const uint32_t* xb = xf + b * 64;  // the block's four 16-input B fragments
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};  // two MMA chains
-        q4_tile_mma(cw.x, xb, lane, d0);
-        q4_tile_mma(cw.y, xb + 16, lane, d1);
-        q4_tile_mma(cw.z, xb + 32, lane, d0);
-        q4_tile_mma(cw.w, xb + 48, lane, d1);
-        acc0 = fmaf(sc.x, (d0[0] + d0[1]) + (d1[0] + d1[1]), acc0);
-        acc1 = fmaf(sc.y, (d0[2] + d0[3]) + (d1[2] + d1[3]), acc1);
+        if constexpr (Q4) {
+          const uint4 cw = *reinterpret_cast<const uint4*>(ub + lane * 16);
+          const float2 sc = *reinterpret_cast<const float2*>(ub + 512 + g8 * 8);
+          q4_tile_mma(cw.x, xb, lane, d0);
+          q4_tile_mma(cw.y, xb + 16, lane, d1);
+          q4_tile_mma(cw.z, xb + 32, lane, d0);
+          q4_tile_mma(cw.w, xb + 48, lane, d1);
+          acc0 = fmaf(sc.x, (d0[0] + d0[1]) + (d1[0] + d1[1]), acc0);
+          acc1 = fmaf(sc.y, (d0[2] + d0[3]) + (d1[2] + d1[3]), acc1);
+        } else {
+          const uint4 c01 = *reinterpret_cast<const uint4*>(ub + lane * 16);
+          const uint4 c23 = *reinterpret_cast<const uint4*>(ub + 512 + lane * 16);
+          f8_tile_mma(c01.x, c01.y, xb, lane, d0);
+          f8_tile_mma(c01.z, c01.w, xb + 16, lane, d1);
+          f8_tile_mma(c23.x, c23.y, xb + 32, lane, d0);
+          f8_tile_mma(c23.z, c23.w, xb + 48, lane, d1);
+          acc0 += (d0[0] + d0[1]) + (d1[0] + d1[1]);
+          acc1 += (d0[2] + d0[3]) + (d1[2] + d1[3]);
+        }
         ++b;
         const bool tile_end = (b == CT);
         if (tile_end || u0 + j + 1 == r.ub) {
           const int pl = gi * TP + g8;  // the pair within the CTA's pairs
+          if (d.scale != nullptr && (lane & 3) == 0 && P0 + pl < npairs) {  // fp8 row scales
+            acc0 *= __ldg(d.scale + 2 * (P0 + pl));
+            acc1 *= __ldg(d.scale + 2 * (P0 + pl) + 1);
+          }
           if (whole && tile_end) {
             if ((lane & 3) == 0 && P0 + pl < npairs) finish(P0 + pl, acc0, acc1);
           } else {
@@ -1516,8 +1554,8 @@ __global__ void __launch_bounds__(MT, 1) mega_decode_kernel(const __grid_constan
     const int N = kind == 0 ? qkv_n : kind == 2 ? 2 * a.inter : kind == 4 ? a.vocab : a.hidden;
     const int CT = kind == 0 ? a.g_qkv.CT : kind == 1 ? a.g_o.CT : kind == 2 ? a.g_gu.CT
                  : kind == 3 ? a.g_down.CT : a.g_lm.CT;
-    // int4 tiled kinds own rows in tiles of 16: the split counts tiles as its "pairs"
-    const bool tl = std::is_same<PT, q4_block64>::value && q4_tiled(kind);
+    // fp8 / int4 tiled kinds own rows in tiles of 16: the split counts tiles as its "pairs"
+    const bool tl = (std::is_same<PT, q4_block64>::value || std::is_same<PT, __nv_fp8_e4m3>::value) && tiled_kind(kind);
     sh.wr[kind][w] = g_split(tl ? 2 * ((N + kQ4GroupRows - 1) / kQ4GroupRows) : N, CT, cta, G, w);
   }
   if (tid == 5 * MW) sh.item = a_split(a, min(cta, a.nkv * a.nsplit - 1), pos + 1);
