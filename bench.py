@@ -72,6 +72,10 @@ def parse():
     p.add_argument("--prefill-split", type=int, default=1, choices=[0, 1],
                    help="K2_OPT_PREFILL_SPLIT for the prefill: 1 = activations as bf16 hi + lo halves "
                         "(the default), 0 = single bf16 activations")
+    p.add_argument("--phase-timeline", default="",
+                   help="after the timed steps, trace a few persistent steps (K2_OPT_TRACE: per-CTA clock stamps "
+                        "at every phase's start, input ready, last slot and end), write the per-phase table to "
+                        "this path and add a summary to the JSON line; the traced steps are not timed")
     p.add_argument("--no-configs", action="store_true",
                    help="skip the sub-records of the int8-KV context-8192 and batch-16 context-8192 workloads "
                         "that the default run adds to its line")
@@ -81,6 +85,74 @@ def parse():
 # ---------------------------------------------------------------------------
 # helpers
 # ---------------------------------------------------------------------------
+PHASE_KINDS = ("qkv", "attention", "o_proj", "gate_up", "down")
+
+
+def phase_timeline(ctx, s, tok, stream, sm_mhz, path, steps=6):
+    """Per-phase timeline of the persistent step from K2_OPT_TRACE stamps.
+
+    Each CTA c stamps its SM clock at phase q's start, input ready, last slot
+    consumed and end, plus one (globaltimer, clock) pair at its own start that
+    places its clock on the common time axis.  Per phase: the critical time
+    (the phase's last end minus the previous phase's last end) and, over CTAs,
+    the head (start to input ready: waiting for the previous phase's words and
+    the norm), body (the weight or K/V slots) and tail (combining and writing
+    the outputs).  The stamps cost time themselves: read the shares, not the
+    absolute step time."""
+    import numpy as np
+    import torch
+    from dense_gqa_decoder_gb300 import k2
+    G = ctx.info().persistent_grid
+    nq = 5 * s.n_layers + 1
+    buf = torch.zeros((nq + 1) * G * 4, dtype=torch.int64, device="cuda")
+    ctx.set_option(k2.K2_OPT_TRACE, buf.data_ptr())
+    runs = []
+    for _ in range(steps):
+        buf.zero_()
+        with torch.cuda.stream(stream):
+            ctx.decode_step(tok, 1, tok, stream=stream)
+        stream.synchronize()
+        runs.append(buf.view(nq + 1, G, 4).cpu().numpy().astype(np.float64))
+    ctx.set_option(k2.K2_OPT_TRACE, 0)
+    if ctx.sync_status(stream) != k2.K2_OK:
+        raise RuntimeError("device guard in the traced steps: " + ctx.last_error())
+    ghz = sm_mhz / 1e3
+    kinds = list(PHASE_KINDS) + ["lm_head"]
+    acc = {k: {"crit": [], "head_med": [], "head_max": [], "body_med": [], "body_max": [], "tail_med": [],
+               "tail_max": []} for k in kinds}
+    step_us = []
+    for R in runs[2:]:  # the first traced steps re-capture the graph
+        T = (R[:-1] - R[-1:, :, 1:2]) / ghz + R[-1:, :, 0:1]  # ns on the common axis
+        T -= T[0, :, 0].min()
+        prev = 0.0
+        for q in range(nq):
+            k = kinds[q % 5] if q < nq - 1 else "lm_head"
+            st, rd, bd, en = T[q, :, 0], T[q, :, 1], T[q, :, 2], T[q, :, 3]
+            d = acc[k]
+            d["crit"].append(en.max() - prev)
+            prev = en.max()
+            for name, v in (("head", rd - st), ("body", bd - rd), ("tail", en - bd)):
+                d[name + "_med"].append(float(np.median(v)))
+                d[name + "_max"].append(float(v.max()))
+        step_us.append(prev / 1e3)
+    out = {"traced_step_us": float(np.mean(step_us)), "sm_mhz": sm_mhz, "per_layer_us": {}, "lm_head_us": {}}
+    lines = ["| phase | critical (us) | share of step | head med / max | body med / max | tail med / max |",
+             "|---|---|---|---|---|---|"]
+    total = float(np.mean(step_us))
+    for k in kinds:
+        d = {n: float(np.mean(v)) / 1e3 for n, v in acc[k].items()}
+        reps = s.n_layers if k != "lm_head" else 1
+        share = d["crit"] * reps / total
+        lines.append(f"| {k} | {d['crit']:.2f} | {100 * share:.1f} % | {d['head_med']:.2f} / {d['head_max']:.2f} | "
+                     f"{d['body_med']:.2f} / {d['body_max']:.2f} | {d['tail_med']:.2f} / {d['tail_max']:.2f} |")
+        (out["lm_head_us"] if k == "lm_head" else out["per_layer_us"])[k] = round(d["crit"], 3)
+    if path:
+        with open(path, "w") as f:
+            f.write(f"traced step {total:.1f} us (SM clock {sm_mhz:.0f} MHz), {s.n_layers} layers; "
+                    f"times per phase in us, the layer phases averaged over layers\n\n" + "\n".join(lines) + "\n")
+    return out
+
+
 def prefill_note(args):
     if args.weights == "f8":
         return ("fp8: the same tensor-core GEMMs over bf16 copies of the E4M3 codes, each row's scale applied in "
@@ -546,6 +618,9 @@ def run_ours(args, world, rank, local, pg):
         "clocks": clk,
         "cpu_baseline": cpu,
     }
+    if args.phase_timeline and persistent:
+        line["phase_timeline"] = phase_timeline(ctx, s, tok, stream, clk.get("sm_mhz") or 2070.0,
+                                                args.phase_timeline)
     default = (args.kv == "f16" and args.ctx == CTX and args.weights == "bf16" and not sampled and not args.layers)
     if default and not args.no_configs:
         # the two larger workloads, each on a fresh context over the same weights

@@ -44,6 +44,7 @@ struct Layout {
   size_t hist, slog, sscr, sample_row;             // token history, sampling logits and scratch
   size_t sqkv, so, sgu, sdown, slm;                // fp8 weights: per-row scales (first layer)
   size_t sqkv_layer, so_layer, sgu_layer, sdown_layer;
+  size_t dq[4], dq_bytes[4];  // int4 prefill: matrix m of the current layer, bf16 hi then lo
   size_t vlog, vids, varg, vpv, vpi;               // speculative verification: logits, ids, argmax
   // tensor-core prefill of up to `pchunk` tokens at a time (bf16 weights)
   int pchunk;
@@ -132,7 +133,7 @@ Layout layout_of(const k2_config& c) {
     l.sdown = take(l.sdown_layer * s.L);
     l.slm = take(rows(s.V, 4));
   }
-  l.pchunk = (c.weight_dtype == K2_BF16 || c.weight_dtype == K2_F8)
+  l.pchunk = (c.weight_dtype == K2_BF16 || c.weight_dtype == K2_F8 || c.weight_dtype == K2_Q4)
                  ? static_cast<int>(align_up(std::min(kPrefillChunk, s.ctx), 128))
                  : 0;
   {
@@ -179,6 +180,13 @@ Layout layout_of(const k2_config& c) {
     l.to = take(l.to_layer * s.L);
     l.tgu = take(l.tgu_layer * s.L);
     l.tdown = take(l.tdown_layer * s.L);
+  }
+  if (c.weight_dtype == K2_Q4 && l.pchunk > 0) {  // one layer's weights as bf16 hi / lo, rebuilt per layer
+    const int Ns[4] = {s.qkv_n, s.H, 2 * s.I, s.H}, Ks[4] = {s.H, s.nq * s.d, s.H, s.I};
+    for (int m = 0; m < 4; ++m) {
+      l.dq_bytes[m] = align_up(packed_bytes(Ns[m], Ks[m], 2), kAlign);
+      l.dq[m] = take(2 * l.dq_bytes[m]);
+    }
   }
   l.repack_bytes = o - scratch_end;
   const size_t kv_start = o;
@@ -281,6 +289,7 @@ struct k2_ctx {
   bool use_tc_decode = true; // batched decode (batch >= 2)
   std::vector<std::array<uint8_t, kTcMapBytes>> tmw;  // 4 per layer
   std::array<uint8_t, kTcMapBytes> tm_xh{}, tm_xl{}, tm_oh{}, tm_ol{}, tm_ah{}, tm_al{}, tm_lm{};
+  std::array<std::array<uint8_t, kTcMapBytes>, 4> tm_wlo{};  // int4: the weights' low halves
   // the same activation buffers in 16-token tiles (batched decode)
   std::array<uint8_t, kTcMapBytes> tb_xh{}, tb_xl{}, tb_oh{}, tb_ol{}, tb_ah{}, tb_al{};
   // fp16 caches: the tensor maps of each layer's K and V for the tensor-core decode attention
@@ -309,7 +318,12 @@ struct k2_ctx {
   // the bf16 weights of the prefill GEMMs (m: 0 QKV, 1 o_proj, 2 gate/up, 3 down) and,
   // for fp8 weights, their row scales
   bool f8() const { return cfg.weight_dtype == K2_F8; }
+  bool q4() const { return cfg.weight_dtype == K2_Q4; }
+  // int4: the dequantized halves of matrix m (rebuilt for every layer)
+  void* dq_hi(int m) const { return ws + lay.dq[m]; }
+  void* dq_lo(int m) const { return ws + lay.dq[m] + lay.dq_bytes[m]; }
   void* tcw(int l, int m) const {
+    if (q4()) return dq_hi(m);
     if (!f8()) return m == 0 ? wqkv(l) : m == 1 ? wop(l) : m == 2 ? wgu(l) : wdown(l);
     const size_t base[4] = {lay.tqkv, lay.to, lay.tgu, lay.tdown};
     const size_t stride[4] = {lay.tqkv_layer, lay.to_layer, lay.tgu_layer, lay.tdown_layer};
@@ -748,8 +762,9 @@ cudaError_t plan_mega(k2_ctx* c, cudaStream_t st) {
   return cudaSuccess;
 }
 
-// Tensor maps of the tensor-core prefill (bf16 weights, or fp8 weights through
-// bf16 copies of their codes; a supported attention shape).  Leaves tc_ok
+// Tensor maps of the tensor-core prefill (bf16 weights, fp8 weights through
+// bf16 copies of their codes, or int4 weights through one layer at a time
+// dequantized into bf16 halves; a supported attention shape).  Leaves tc_ok
 // false when it cannot run; tc_full (batched decode, speculation: a bf16
 // lm_head) only for bf16 weights.
 cudaError_t plan_tc_prefill(k2_ctx* c) {
@@ -767,6 +782,11 @@ cudaError_t plan_tc_prefill(k2_ctx* c) {
         !tc_encode_weight(c->tmw[4 * l + 3].data(), c->tcw(l, 3), s.H, s.I))
       return cudaSuccess;
   }
+  if (c->q4()) {
+    const int Ns[4] = {s.qkv_n, s.H, 2 * s.I, s.H}, Ks[4] = {s.H, s.nq * s.d, s.H, s.I};
+    for (int m = 0; m < 4; ++m)
+      if (!tc_encode_weight(c->tm_wlo[m].data(), c->dq_lo(m), Ns[m], Ks[m])) return cudaSuccess;
+  }
   const int P = c->lay.pchunk;
   bool ok = true;
   for (int tt : {128, 16}) {
@@ -781,7 +801,7 @@ cudaError_t plan_tc_prefill(k2_ctx* c) {
   if (16 * 2 * static_cast<size_t>(s.I) > static_cast<size_t>(P) * s.qkv_n) return cudaSuccess;
   if (!ok) return cudaSuccess;
   c->tc_ok = true;
-  c->tc_full = !c->f8() && tc_encode_weight(c->tm_lm.data(), c->wlm(), s.V, s.H);
+  c->tc_full = !quantized(c->cfg.weight_dtype) && tc_encode_weight(c->tm_lm.data(), c->wlm(), s.V, s.H);
   return cudaSuccess;
 }
 
@@ -804,6 +824,21 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   const size_t head_row0 = static_cast<size_t>(seq) * s.nkv * c->lay.cap;
   const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(s.d)));
   // rs: the weight rows' scales (fp8 codes), else null
+  // int4: before its GEMM, each matrix of the layer is dequantized into bf16
+  // halves (c->dq_*), and the GEMM adds the low halves' products
+  const bool q4 = c->q4();
+  const void* wlo = nullptr;
+  auto dequant = [&](int l, int m) {
+    if (!q4) {
+      wlo = nullptr;
+      return cudaSuccess;
+    }
+    wlo = c->tm_wlo[m].data();
+    const void* srcs[4] = {c->wqkv(l), c->wop(l), c->wgu(l), c->wdown(l)};
+    const int Ns[4] = {s.qkv_n, s.H, 2 * s.I, s.H}, Ks[4] = {s.H, s.nq * s.d, s.H, s.I};
+    return launch_q4_dequant(c->dq_hi(m), c->dq_lo(m), static_cast<const uint8_t*>(srcs[m]), Ns[m], Ks[m],
+                             tiled_kind(m), st);
+  };
   auto gemm = [&](const void* mw, const float* rs, const void* mh, const void* ml, int N, int K, int mode, float* out,
                   __nv_bfloat16* oh, __nv_bfloat16* ol, int ldo) {
     TcGemmArgs g = {};
@@ -820,12 +855,13 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.out_lo = ol;
     g.guard = c->guard;
     g.row_scale = rs;
-    return launch_tc_gemm(mw, mh, ml, g, st);
+    return launch_tc_gemm(mw, wlo, mh, ml, g, st);
   };
   // a block of at most 16 tokens (a speculative verification) streams every
   // weight matrix with the stream-K kernel over 16-token tiles, one CTA per
-  // SM: the 128-token tiles would leave most SMs idle
-  const bool small = n <= 16;
+  // SM: the 128-token tiles would leave most SMs idle (int4 weights keep the
+  // 128-token tiles, the only ones with a low-half weight operand)
+  const bool small = n <= 16 && !q4;
   const int tt = small ? 16 : 128;
   auto gemm_sk = [&](const void* mw, const float* rs, const void* mh, const void* ml, int N, int K, int mode, float* out,
                      int ldo) {
@@ -843,12 +879,12 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.row_scale = rs;
     cudaError_t e = cudaSuccess;
     if (mode == TC_STORE) e = cudaMemsetAsync(out, 0, sizeof(float) * static_cast<size_t>(n) * ldo, st);
-    if (!e) e = launch_tc_gemm_sk(mw, mh, ml, g, c->sms, st);
+    if (!e) e = launch_tc_gemm_sk(mw, wlo, mh, ml, g, c->sms, st);
     return e;
   };
   // without the split (blocks over 16 tokens only) the low-half maps are null:
   // the GEMMs read the high halves alone
-  const bool split = small || c->pf_split;
+  const bool split = small || c->pf_split || q4;  // int4: the low-half weight MMA needs the activations' halves
   const void* m_xh = small ? c->tb_xh.data() : c->tm_xh.data();
   const void* m_xl = small ? c->tb_xl.data() : split ? c->tm_xl.data() : nullptr;
   const void* m_oh = small ? c->tb_oh.data() : c->tm_oh.data();
@@ -860,6 +896,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
                                     c->hist + static_cast<size_t>(seq) * c->lay.cap, 0, nullptr, pos0, d_pos0, st);
   for (int l = 0; l < s.L && !e; ++l) {
     if (!e) e = launch_norm_rows(X, n, c->attn_norm[l], s.gb, xh, xl, s.H, s.G, c->cfg.eps, st);
+    if (!e) e = dequant(l, 0);
     if (!e)
       e = small ? gemm_sk(c->tmw[4 * l].data(), c->tcs(l, 0), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, s.qkv_n)
                 : gemm(c->tmw[4 * l].data(), c->tcs(l, 0), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, nullptr, nullptr,
@@ -907,8 +944,10 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
                               head_row0, c->lay.cap, scale, st);
     }
     // o_proj and down have few row tiles: stream-K over one CTA per SM
+    if (!e) e = dequant(l, 1);
     if (!e) e = gemm_sk(c->tmw[4 * l + 1].data(), c->tcs(l, 1), m_oh, m_ol, s.H, s.nq * s.d, TC_RESID, X, s.H);
     if (!e) e = launch_norm_rows(X, n, c->mlp_norm[l], s.gb, xh, xl, s.H, s.G, c->cfg.eps, st);
+    if (!e) e = dequant(l, 2);
     if (!e) {
       if (small) {  // gate/up rows to fp32 (the QKV buffer is free by now), then SwiGLU rows
         e = gemm_sk(c->tmw[4 * l + 2].data(), c->tcs(l, 2), m_xh, m_xl, 2 * s.I, s.H, TC_STORE, qkv, 2 * s.I);
@@ -918,6 +957,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
                  split ? al : nullptr, s.I);
       }
     }
+    if (!e) e = dequant(l, 3);
     if (!e) e = gemm_sk(c->tmw[4 * l + 3].data(), c->tcs(l, 3), m_ah, m_al, s.H, s.I, TC_RESID, X, s.H);
   }
   return e;
@@ -955,7 +995,7 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
     g.splits = 1;
     g.out = out;
     g.guard = c->guard;
-    return launch_tc_gemm_sk(mw, mh, ml, g, c->sms, st, true);
+    return launch_tc_gemm_sk(mw, nullptr, mh, ml, g, c->sms, st, true);
   };
   // the final norm clears the logits unless the caller's buffer is not 16-byte aligned
   const bool lg_aligned = reinterpret_cast<uintptr_t>(logits) % 16 == 0 && (static_cast<size_t>(B) * s.V) % 4 == 0;
@@ -1008,15 +1048,16 @@ cudaError_t prefill_tc(k2_ctx* c, int seq, const int* d_tokens, int n, int* d_ne
   const int P = c->lay.pchunk;
   cudaError_t e = cudaSuccess;
   int last = 0;
-  // fp8 weights: the lm_head exists only as fp8 rows, so the last token takes
-  // the persistent step (which ends in the lm_head and argmax)
-  const int nb = c->f8() ? n - 1 : n;
+  // fp8 / int4 weights: the lm_head exists only in their packed form, so the
+  // last token takes the persistent step (which ends in the lm_head and argmax)
+  const bool quant = quantized(c->cfg.weight_dtype);
+  const int nb = quant ? n - 1 : n;
   for (int b0 = 0; b0 < nb && !e; b0 += P) {
     last = std::min(P, nb - b0);
     e = prefill_block(c, seq, d_tokens + b0, last, c->len[seq] + b0, st);
   }
   if (e) return e;
-  if (c->f8()) {
+  if (quant) {
     if ((e = launch_advance_by(c->seq_len, seq, nb, st)) != cudaSuccess) return e;
     Launcher ln{c, st, false};
     enqueue_token(c, ln, seq, d_tokens + nb, nullptr, d_next, d_logits, true);
@@ -1065,7 +1106,7 @@ cudaError_t verify_block(k2_ctx* c, int seq, const int* d_tokens, int n, int* d_
     g.splits = 1;
     g.out = logits;
     g.guard = c->guard;
-    e = launch_tc_gemm_sk(c->tm_lm.data(), c->tb_xh.data(), c->tb_xl.data(), g, c->sms, st);
+    e = launch_tc_gemm_sk(c->tm_lm.data(), nullptr, c->tb_xh.data(), c->tb_xl.data(), g, c->sms, st);
   }
   if (!e)
     e = launch_argmax_rows(logits, n, s.V, d_argmax, reinterpret_cast<float*>(c->ws + c->lay.vpv),

@@ -653,6 +653,47 @@ cudaError_t launch_f8_expand(void* dst, const uint8_t* src, int N, int K, bool t
   return cudaGetLastError();
 }
 
+// The int4 weights of a packed matrix (pair or tile units) dequantized for
+// the tensor-core prefill: w = code * scale (fp32, as the decode step scales
+// each block), split into bf16 halves w_hi = bf16(w), w_lo = bf16(w - w_hi), in
+// the bf16 packed layout (pairs of rows in 256-weight chunks).  One CTA of 256
+// threads per (packed row R, bf16 chunk c): weight k = 256 c + t.
+__global__ void __launch_bounds__(256) q4_dequant_kernel(__nv_bfloat16* __restrict__ hi, __nv_bfloat16* __restrict__ lo,
+                                                         const uint8_t* __restrict__ src, int K, int CT16, int tiles) {
+  const int R = blockIdx.x, c = blockIdx.y, k = c * 256 + threadIdx.x;
+  float w = 0.f;
+  if (k < K) {
+    if (tiles) {
+      const int nb = (K + kQ4Block - 1) / kQ4Block;
+      const int rl = R % kQ4GroupRows, pair = rl >> 1, member = rl & 1;
+      const int kb = k & 63, j = kb >> 4, kk = kb & 15, t = (kk & 7) >> 1, hi8 = kk >> 3, odd = kk & 1;
+      const uint8_t* unit = src + (static_cast<size_t>(R / kQ4GroupRows) * nb + (k >> 6)) * kQ4Unit;
+      const uint32_t word = *reinterpret_cast<const uint32_t*>(unit + (pair * 4 + t) * 16 + j * 4);
+      const int code = static_cast<int>((word >> (4 * member + 8 * hi8 + 16 * odd)) & 15u) - 8;
+      w = static_cast<float>(code) * *reinterpret_cast<const float*>(unit + 512 + pair * 8 + member * 4);
+    } else {
+      const int CT = (K + kQ4Chunk - 1) / kQ4Chunk, i = k % kQ4Chunk;
+      const uint8_t* unit = src + (static_cast<size_t>(R >> 1) * CT + k / kQ4Chunk) * kQ4Unit;
+      const uint8_t b = unit[(R & 1) * (kQ4Chunk / 2) + (i >> 1)];
+      const int code = static_cast<int>((i & 1) ? (b >> 4) : (b & 15u)) - 8;
+      w = static_cast<float>(code) *
+          *reinterpret_cast<const float*>(unit + kQ4Chunk + (R & 1) * (kQ4Chunk / kQ4Block) * 4 + (i / kQ4Block) * 4);
+    }
+  }
+  const __nv_bfloat16 h = __float2bfloat16_rn(w);
+  const size_t o = (static_cast<size_t>(R >> 1) * CT16 + c) * 512 + (R & 1) * 256 + threadIdx.x;
+  hi[o] = h;
+  lo[o] = __float2bfloat16_rn(w - __bfloat162float(h));
+}
+
+cudaError_t launch_q4_dequant(void* hi, void* lo, const uint8_t* src, int N, int K, bool tiles, cudaStream_t s) {
+  const int CT16 = (K + 255) / 256, rows = 2 * ((N + 1) / 2);
+  if (rows <= 0 || CT16 <= 0) return cudaSuccess;
+  q4_dequant_kernel<<<dim3(rows, CT16), 256, 0, s>>>(static_cast<__nv_bfloat16*>(hi), static_cast<__nv_bfloat16*>(lo),
+                                                     src, K, CT16, tiles ? 1 : 0);
+  return cudaGetLastError();
+}
+
 size_t f8_packed_bytes(int N, int K, bool tiles) {
   if (!tiles) return packed_bytes(N, K, 1);
   return (static_cast<size_t>(N) + kQ4GroupRows - 1) / kQ4GroupRows * ((static_cast<size_t>(K) + 63) / 64) * 1024;

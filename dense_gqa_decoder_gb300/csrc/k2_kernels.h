@@ -149,6 +149,10 @@ size_t f8_packed_bytes(int N, int K, bool tiles);
 cudaError_t launch_q4_pack(uint8_t* dst, float* scales, const void* src0, const void* src1, const void* src2,
                            int mode, int N, int K, int nq, int nkv, int d, int layout, cudaStream_t s);
 size_t q4_packed_bytes(int N, int K, bool tiles);
+// int4 packed weights (pair or tile units) as bf16 hi / lo halves of code * scale
+// in the bf16 packed layout (packed_bytes(N, K, 2) bytes each), for the
+// tensor-core prefill
+cudaError_t launch_q4_dequant(void* hi, void* lo, const uint8_t* src, int N, int K, bool tiles, cudaStream_t s);
 // The fp8 codes of a packed matrix (pair units of 512 per chunk and row, or
 // tile units) as bf16 values (exact: every E4M3 value is a bf16 value) in the
 // bf16 packed layout (256 per chunk and row).
@@ -429,14 +433,15 @@ bool tc_encode_weight(void* map, const void* packed, int N, int K);  // bf16 pac
 bool tc_encode_act(void* map, const void* buf, int rows, int K, int tile_tokens);  // bf16 [rows][K]
 cudaError_t tc_gemm_init_attrs();
 // mapXl (the activations' low halves) null: one MMA per K step on the high
-// halves alone (tile_tokens 128 only)
-cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a,
-                           cudaStream_t s);
+// halves alone (tile_tokens 128 only).  mapWl (nullable; tile_tokens 128 with
+// mapXl): the weights' low halves, a third MMA per K step (w_lo . x_hi).
+cudaError_t launch_tc_gemm(const void* mapW, const void* mapWl, const void* mapXh, const void* mapXl,
+                           const TcGemmArgs& a, cudaStream_t s);
 // stream-K persistent variant (tile_tokens 16; TC_STORE into a zeroed target or TC_RESID), `ctas` CTAs.
 // pdl: programmatic dependent launch; the first weight stages are requested before
 // the kernel waits for its predecessor (weights never depend on an earlier kernel)
-cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a, int ctas,
-                              cudaStream_t s, bool pdl = false);
+cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* mapXh, const void* mapXl,
+                              const TcGemmArgs& a, int ctas, cudaStream_t s, bool pdl = false);
 // Causal prefill attention on the tensor cores (tcgen05, fp16 caches): the n
 // query tokens of a block at positions pos0 .. pos0 + n - 1 (Q [n][nq * D] fp32,
 // rotated) against every cached key of their sequence up to their own position,

@@ -12,7 +12,11 @@
 // precision the decode step's fp32 activations have, while W stays the model's
 // bf16.  Without the low half (LO = false: no map for it) each K step issues
 // one MMA on x_hi alone -- activations in the model's dtype, half the MMAs and
-// half the activation bytes -- and the ring holds more stages.
+// half the activation bytes -- and the ring holds more stages.  With a second
+// weight map (WL = true: W = w_hi + w_lo, the int4 weights dequantized to two
+// bf16 halves) each K step also issues w_lo . x_hi, so the product keeps ~16
+// bits of every weight too (w_lo . x_lo, below both halves' rounding, is left
+// out).
 //
 // One CTA per 128-row x 128-token tile, 128 threads: thread 0 issues the TMA
 // loads into a 4-stage ring (mbarrier complete_tx), thread 32 issues the MMAs
@@ -33,13 +37,17 @@ namespace {
 
 constexpr int BM = 128, BK = 64;
 // tile shapes: 128 tokens for prefill, 16 for a batched decode step
-template <int BN_, bool LO_ = true>
+template <int BN_, bool LO_ = true, bool WL_ = false>
 struct Tile {
   static constexpr int BN = BN_;
   static constexpr bool LO = LO_;  // the activations' low half is a second B operand
-  static constexpr int STAGES = BN_ >= 128 ? (LO_ ? 4 : 6) : 8;
+  static constexpr bool WL = WL_;  // the weights' low half is a second A operand
   static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + (LO_ ? 2 : 1) * B_BYTES;
+  static constexpr int OFF_AL = A_BYTES;                       // stage: A, [A lo], B, [B lo]
+  static constexpr int OFF_B = (WL_ ? 2 : 1) * A_BYTES;
+  static constexpr int OFF_BL = OFF_B + B_BYTES;
+  static constexpr int STAGE_BYTES = OFF_B + (LO_ ? 2 : 1) * B_BYTES;
+  static constexpr int STAGES = BN_ >= 128 ? (192 * 1024) / STAGE_BYTES : 8;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment of the ring to 1024 B
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;             // allocation: a power of two >= 32
   // instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major
@@ -106,11 +114,12 @@ __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
-template <int BN_, bool LO>
+template <int BN_, bool LO, bool WL>
 __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                         const __grid_constant__ CUtensorMap tmWl,
                                                          const __grid_constant__ CUtensorMap tmXh,
                                                          const __grid_constant__ CUtensorMap tmXl, const TcGemmArgs a) {
-  using C = Tile<BN_, LO>;
+  using C = Tile<BN_, LO, WL>;
   constexpr int BN = C::BN, STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -155,8 +164,9 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
       uint8_t* st = smem + s * STAGE_BYTES;
       const int kk = (kb + k) * BK;
       tma_4d(st, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
-      tma_2d(st + A_BYTES, &tmXh, kk, n0, &full[s]);
-      if constexpr (LO) tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[s]);
+      if constexpr (WL) tma_4d(st + C::OFF_AL, &tmWl, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
+      tma_2d(st + C::OFF_B, &tmXh, kk, n0, &full[s]);
+      if constexpr (LO) tma_2d(st + C::OFF_BL, &tmXl, kk, n0, &full[s]);
     }
     // copies still in flight must land before the CTA ends: wait for the
     // last ones the MMA thread may not have consumed (bounded)
@@ -172,9 +182,10 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
       uint8_t* st = smem + s * STAGE_BYTES;
 #pragma unroll
       for (int j = 0; j < BK / 16; ++j) {
-        const uint64_t ad = smem_desc(st + j * 32);
-        mma(tmem, ad, smem_desc(st + A_BYTES + j * 32), C::IDESC, (k | j) != 0);
-        if constexpr (LO) mma(tmem, ad, smem_desc(st + A_BYTES + B_BYTES + j * 32), C::IDESC, 1u);
+        const uint64_t ad = smem_desc(st + j * 32), bd = smem_desc(st + C::OFF_B + j * 32);
+        mma(tmem, ad, bd, C::IDESC, (k | j) != 0);
+        if constexpr (LO) mma(tmem, ad, smem_desc(st + C::OFF_BL + j * 32), C::IDESC, 1u);
+        if constexpr (WL) mma(tmem, smem_desc(st + C::OFF_AL + j * 32), bd, C::IDESC, 1u);
       }
       mma_commit(&empty[s]);
     }
@@ -230,12 +241,13 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
 // w reads TMEM lanes 32 (w % 4) ..), so accumulation and write-back overlap.
 // Output: atomicAdd into out (TC_RESID adds to the residual; TC_STORE expects
 // a zeroed target).
-template <int BN_, bool LO>
+template <int BN_, bool LO, bool WL>
 __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                            const __grid_constant__ CUtensorMap tmWl,
                                                             const __grid_constant__ CUtensorMap tmXh,
                                                             const __grid_constant__ CUtensorMap tmXl,
                                                             const TcGemmArgs a) {
-  using C = Tile<BN_, LO>;
+  using C = Tile<BN_, LO, WL>;
   constexpr int BN = C::BN, STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES, COLS = C::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
@@ -287,6 +299,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
       where(g0 + j, m0, n0, kk);
       mbar_arrive_expect_tx(&full[j], STAGE_BYTES);
       tma_4d(smem + j * STAGE_BYTES, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[j]);
+      if constexpr (WL) tma_4d(smem + j * STAGE_BYTES + C::OFF_AL, &tmWl, kk & 255, 0, kk >> 8, m0 >> 1, &full[j]);
     }
     pdl_wait();
     pdl_trigger();
@@ -294,8 +307,8 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
       int m0, n0, kk;
       where(g0 + j, m0, n0, kk);
       uint8_t* st = smem + j * STAGE_BYTES;
-      tma_2d(st + A_BYTES, &tmXh, kk, n0, &full[j]);
-      if constexpr (LO) tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[j]);
+      tma_2d(st + C::OFF_B, &tmXh, kk, n0, &full[j]);
+      if constexpr (LO) tma_2d(st + C::OFF_BL, &tmXl, kk, n0, &full[j]);
     }
     long long g = g0 + pre;
     int i = pre;
@@ -310,8 +323,9 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
       mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
       uint8_t* st = smem + s * STAGE_BYTES;
       tma_4d(st, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
-      tma_2d(st + A_BYTES, &tmXh, kk, n0, &full[s]);
-      if constexpr (LO) tma_2d(st + A_BYTES + B_BYTES, &tmXl, kk, n0, &full[s]);
+      if constexpr (WL) tma_4d(st + C::OFF_AL, &tmWl, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
+      tma_2d(st + C::OFF_B, &tmXh, kk, n0, &full[s]);
+      if constexpr (LO) tma_2d(st + C::OFF_BL, &tmXl, kk, n0, &full[s]);
     }
     for (int j = max(0, i - STAGES); j < i; ++j) mbar_wait(&full[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u);
   } else if (threadIdx.x == 32) {  // MMA issuer
@@ -335,9 +349,10 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
       const uint32_t acc = tmem + b * COLS;
 #pragma unroll
       for (int j = 0; j < BK / 16; ++j) {
-        const uint64_t ad = smem_desc(st + j * 32);
-        mma(acc, ad, smem_desc(st + A_BYTES + j * 32), C::IDESC, (!first || j != 0) ? 1u : 0u);
-        if constexpr (LO) mma(acc, ad, smem_desc(st + A_BYTES + B_BYTES + j * 32), C::IDESC, 1u);
+        const uint64_t ad = smem_desc(st + j * 32), bd = smem_desc(st + C::OFF_B + j * 32);
+        mma(acc, ad, bd, C::IDESC, (!first || j != 0) ? 1u : 0u);
+        if constexpr (LO) mma(acc, ad, smem_desc(st + C::OFF_BL + j * 32), C::IDESC, 1u);
+        if constexpr (WL) mma(acc, smem_desc(st + C::OFF_AL + j * 32), bd, C::IDESC, 1u);
       }
       mma_commit(&empty[s]);
       first = false;
@@ -842,62 +857,70 @@ cudaError_t smem_attr(K kern, int bytes) {
 }
 
 cudaError_t tc_gemm_init_attrs() {
-  cudaError_t e = smem_attr(tc_gemm_kernel<128, true>, Tile<128, true>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<128, false>, Tile<128, false>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<16, true>, Tile<16, true>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<16, true>, Tile<16, true>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true>, Tile<128, true>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, false>, Tile<128, false>::SMEM_BYTES);
+  cudaError_t e = smem_attr(tc_gemm_kernel<128, true, false>, Tile<128, true, false>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<128, false, false>, Tile<128, false, false>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<128, true, true>, Tile<128, true, true>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<16, true, false>, Tile<16, true, false>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<16, true, false>, Tile<16, true, false>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, false>, Tile<128, true, false>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, false, false>, Tile<128, false, false>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, true>, Tile<128, true, true>::SMEM_BYTES);
   return e;
 }
 
-cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a, int ctas,
-                              cudaStream_t s, bool pdl) {
+cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* mapXh, const void* mapXl,
+                              const TcGemmArgs& a, int ctas, cudaStream_t s, bool pdl) {
   if (a.T <= 0) return cudaSuccess;
   if ((a.tile_tokens != 16 && a.tile_tokens != 128) || a.mode == TC_SWIGLU || ctas < 1) return cudaErrorInvalidValue;
   const int tt = a.tile_tokens;
-  const bool lo = mapXl != nullptr;
-  if (tt == 16 && !lo) return cudaErrorInvalidValue;
+  const bool lo = mapXl != nullptr, wl = mapWl != nullptr;
+  if ((tt == 16 && (!lo || wl)) || (wl && !lo)) return cudaErrorInvalidValue;
   const long long total =
       static_cast<long long>((2 * ((a.N + 1) / 2) + BM - 1) / BM) * ((a.T + tt - 1) / tt) * a.ksteps;
   const int grid = static_cast<int>(std::min<long long>(ctas, total));
   const CUtensorMap& w = *static_cast<const CUtensorMap*>(mapW);
+  const CUtensorMap& wlo = *static_cast<const CUtensorMap*>(wl ? mapWl : mapW);  // unread without it
   const CUtensorMap& xh = *static_cast<const CUtensorMap*>(mapXh);
   const CUtensorMap& xl = *static_cast<const CUtensorMap*>(lo ? mapXl : mapXh);  // unread without the low half
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = tt == 16 ? Tile<16, true>::SMEM_BYTES
-                                  : (lo ? Tile<128, true>::SMEM_BYTES : Tile<128, false>::SMEM_BYTES);
+  cfg.dynamicSmemBytes = tt == 16 ? Tile<16, true, false>::SMEM_BYTES
+                         : wl     ? Tile<128, true, true>::SMEM_BYTES
+                         : lo     ? Tile<128, true, false>::SMEM_BYTES
+                                  : Tile<128, false, false>::SMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (tt == 16) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<16, true>, w, xh, xl, a);
-  if (lo) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true>, w, xh, xl, a);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, false>, w, xh, xl, a);
+  if (tt == 16) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<16, true, false>, w, wlo, xh, xl, a);
+  if (wl) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true, true>, w, wlo, xh, xl, a);
+  if (lo) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true, false>, w, wlo, xh, xl, a);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, false, false>, w, wlo, xh, xl, a);
 }
 
-cudaError_t launch_tc_gemm(const void* mapW, const void* mapXh, const void* mapXl, const TcGemmArgs& a,
-                           cudaStream_t s) {
+cudaError_t launch_tc_gemm(const void* mapW, const void* mapWl, const void* mapXh, const void* mapXl,
+                           const TcGemmArgs& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   if (a.splits < 1 || (a.splits > 1 && a.mode == TC_SWIGLU)) return cudaErrorInvalidValue;
-  const bool lo = mapXl != nullptr;
+  const bool lo = mapXl != nullptr, wl = mapWl != nullptr;
+  if (wl && (!lo || a.tile_tokens != 128)) return cudaErrorInvalidValue;
   const CUtensorMap& w = *static_cast<const CUtensorMap*>(mapW);
+  const CUtensorMap& wlo = *static_cast<const CUtensorMap*>(wl ? mapWl : mapW);  // unread without it
   const CUtensorMap& xh = *static_cast<const CUtensorMap*>(mapXh);
   const CUtensorMap& xl = *static_cast<const CUtensorMap*>(lo ? mapXl : mapXh);  // unread without the low half
   const int rows = (2 * ((a.N + 1) / 2) + BM - 1) / BM;
-  if (a.tile_tokens == 16 && lo) {
-    tc_gemm_kernel<16, true><<<dim3((a.T + 15) / 16, rows, a.splits), 128, Tile<16, true>::SMEM_BYTES, s>>>(w, xh, xl,
-                                                                                                            a);
+  const dim3 g16((a.T + 15) / 16, rows, a.splits), g128((a.T + 127) / 128, rows, a.splits);
+  if (a.tile_tokens == 16 && lo && !wl) {
+    tc_gemm_kernel<16, true, false><<<g16, 128, Tile<16, true, false>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
+  } else if (a.tile_tokens == 128 && wl) {
+    tc_gemm_kernel<128, true, true><<<g128, 128, Tile<128, true, true>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
   } else if (a.tile_tokens == 128 && lo) {
-    tc_gemm_kernel<128, true>
-        <<<dim3((a.T + 127) / 128, rows, a.splits), 128, Tile<128, true>::SMEM_BYTES, s>>>(w, xh, xl, a);
+    tc_gemm_kernel<128, true, false><<<g128, 128, Tile<128, true, false>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
   } else if (a.tile_tokens == 128) {
-    tc_gemm_kernel<128, false>
-        <<<dim3((a.T + 127) / 128, rows, a.splits), 128, Tile<128, false>::SMEM_BYTES, s>>>(w, xh, xl, a);
+    tc_gemm_kernel<128, false, false><<<g128, 128, Tile<128, false, false>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
   } else {
     return cudaErrorInvalidValue;
   }

@@ -76,8 +76,11 @@ typedef enum { K2_F32 = 0, K2_BF16 = 1, K2_F16 = 2, K2_I8 = 3, K2_F8 = 4, K2_Q4 
  * decodes on the persistent step only and is refused where that step is not
  * available.  Prompts of >= 8 tokens with K2_F8 weights run through the
  * tensor-core GEMMs over bf16 copies of the codes (exact), each row's scale
- * applied to its outputs, the last token through the persistent step; K2_Q4
- * prompts are appended one persistent step per token.  max_context = KV rows per sequence (prompt + generated tokens);
+ * applied to its outputs, the last token through the persistent step; with
+ * K2_Q4 weights each layer's matrices are first dequantized (code * scale)
+ * into bf16 high and low halves in a one-layer scratch, and the GEMMs add the
+ * low halves' products (~16 bits of every weight), the last token again
+ * through the persistent step.  max_context = KV rows per sequence (prompt + generated tokens);
  * max_batch = number of independent sequences. */
 typedef struct {
   int32_t hidden, n_layers, n_heads, n_kv_heads, head_dim, intermediate, norm_groups, vocab;
@@ -379,8 +382,10 @@ typedef enum {
   K2_OPT_PERSISTENT = 3,  /* 1 (default): batch-1 tokens run as one persistent cooperative kernel
                              (one CTA per SM, dataflow waits between the phases of a layer) when the
                              shape allows; 0: always the chain of per-step kernels */
-  K2_OPT_TC_PREFILL = 4,  /* 1 (default): bf16 and fp8 models prefill prompts of >= 8 tokens with
-                             tensor-core GEMMs over blocks of up to 2048 tokens; 0: one decode step per token */
+  K2_OPT_TC_PREFILL = 4,  /* 1 (default): bf16, fp8 and int4 models prefill prompts of >= 8 tokens with
+                             tensor-core GEMMs over blocks of up to 2048 tokens (int4: each layer's weights
+                             dequantized into bf16 hi + lo halves first, three MMAs per K step); 0: one
+                             decode step per token */
   K2_OPT_TC_DECODE = 5,   /* 1 (default): a bf16 decode step of batch >= 2 reads the weights once for
                              all sequences (tensor-core GEMMs, N = batch); 0: one token at a time */
   K2_OPT_WAIT_LIMIT_US = 6, /* how long (microseconds, 1 .. 1000000; default 1000000) a CTA of the
