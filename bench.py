@@ -158,8 +158,9 @@ def prefill_note(args):
         return ("fp8: the same tensor-core GEMMs over bf16 copies of the E4M3 codes, each row's scale applied in "
                 "the GEMM epilogue; the last prompt token takes the fp8 decode step")
     if args.weights == "q4":
-        return ("int4: no tensor-core GEMM path (block scales along K): the prompt runs through the decode step, "
-                "one token at a time")
+        return ("int4: each layer's codes * block scales dequantized into bf16 high and low halves, then the "
+                "tensor-core GEMMs with three MMAs per K step (w_hi x_hi, w_hi x_lo, w_lo x_hi); the last prompt "
+                "token takes the int4 decode step")
     if args.prefill_split:
         return ("useful FLOPs (2 per weight x token + causal attention); the GEMMs issue twice the linear MMAs "
                 "(activations as bf16 hi + lo halves); attention (fp16 KV) issues tcgen05 MMAs on fp16 hi + lo "
