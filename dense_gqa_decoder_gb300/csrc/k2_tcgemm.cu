@@ -37,23 +37,31 @@ namespace {
 
 constexpr int BM = 128, BK = 64;
 // tile shapes: 128 tokens for prefill, 16 for a batched decode step
-template <int BN_, bool LO_ = true, bool WL_ = false>
+// KPS_: K steps per ring stage.  A TMA copy group is taken in by an SM at a
+// rate that grows with the bytes requested together (measured: one 16 KB box
+// ~69 GB/s, two ~121, four ~142 from L2), not with the number of stages in
+// flight, so the non-persistent prefill kernel fills each stage with two K
+// steps (one barrier, twice the boxes).
+template <int BN_, bool LO_ = true, bool WL_ = false, int KPS_ = 1>
 struct Tile {
   static constexpr int BN = BN_;
   static constexpr bool LO = LO_;  // the activations' low half is a second B operand
   static constexpr bool WL = WL_;  // the weights' low half is a second A operand
+  static constexpr int KPS = KPS_;
   static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
-  static constexpr int OFF_AL = A_BYTES;                       // stage: A, [A lo], B, [B lo]
+  static constexpr int OFF_AL = A_BYTES;                       // one K step: A, [A lo], B, [B lo]
   static constexpr int OFF_B = (WL_ ? 2 : 1) * A_BYTES;
   static constexpr int OFF_BL = OFF_B + B_BYTES;
-  static constexpr int STAGE_BYTES = OFF_B + (LO_ ? 2 : 1) * B_BYTES;
+  static constexpr int STEP_BYTES = OFF_B + (LO_ ? 2 : 1) * B_BYTES;
+  static constexpr int STAGE_BYTES = KPS_ * STEP_BYTES;
   static constexpr int STAGES = BN_ >= 128 ? (192 * 1024) / STAGE_BYTES : 8;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // + alignment of the ring to 1024 B
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;             // allocation: a power of two >= 32
   // instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major
   static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
                                     (static_cast<uint32_t>(BM >> 4) << 24);
-  static_assert(STAGE_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+  static_assert(STEP_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+  static_assert(STAGES >= 2, "a ring of at least two stages");
 };
 
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* m, int c0, int c1, uint64_t* bar) {
@@ -109,6 +117,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// the tile of the non-persistent kernel: two K steps per stage where both fit twice
+template <int BN, bool LO, bool WL>
+using TileG = Tile<BN, LO, WL, (BN >= 128 && !WL) ? 2 : 1>;
+
 __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(v);
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
@@ -119,9 +131,9 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
                                                          const __grid_constant__ CUtensorMap tmWl,
                                                          const __grid_constant__ CUtensorMap tmXh,
                                                          const __grid_constant__ CUtensorMap tmXl, const TcGemmArgs a) {
-  using C = Tile<BN_, LO, WL>;
-  constexpr int BN = C::BN, STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES;
-  constexpr int STAGE_BYTES = C::STAGE_BYTES;
+  using C = TileG<BN_, LO, WL>;
+  constexpr int BN = C::BN, STAGES = C::STAGES, KPS = C::KPS;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES, STEP_BYTES = C::STEP_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -152,40 +164,47 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
   const int kb = static_cast<int>((static_cast<long long>(a.ksteps) * blockIdx.z) / a.splits);
   const int ke = static_cast<int>((static_cast<long long>(a.ksteps) * (blockIdx.z + 1)) / a.splits);
   const int nk = ke - kb;
+  const int nf = (nk + KPS - 1) / KPS;  // stage fills: KPS K steps each, the last one maybe fewer
   if (threadIdx.x == 0) {  // TMA producer
-    int k = 0;
-    for (; k < nk; ++k) {
-      const int s = k % STAGES;
-      if (k >= STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>((k / STAGES) - 1) & 1u)) {
+    int f = 0;
+    for (; f < nf; ++f) {
+      const int s = f % STAGES;
+      if (f >= STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>((f / STAGES) - 1) & 1u)) {
         atomicOr(a.guard, GUARD_TIMEOUT);
         break;
       }
-      mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-      uint8_t* st = smem + s * STAGE_BYTES;
-      const int kk = (kb + k) * BK;
-      tma_4d(st, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
-      if constexpr (WL) tma_4d(st + C::OFF_AL, &tmWl, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
-      tma_2d(st + C::OFF_B, &tmXh, kk, n0, &full[s]);
-      if constexpr (LO) tma_2d(st + C::OFF_BL, &tmXl, kk, n0, &full[s]);
+      const int cnt = min(KPS, nk - f * KPS);
+      mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cnt * STEP_BYTES));
+      for (int q = 0; q < cnt; ++q) {
+        uint8_t* st = smem + s * STAGE_BYTES + q * STEP_BYTES;
+        const int kk = (kb + f * KPS + q) * BK;
+        tma_4d(st, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
+        if constexpr (WL) tma_4d(st + C::OFF_AL, &tmWl, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
+        tma_2d(st + C::OFF_B, &tmXh, kk, n0, &full[s]);
+        if constexpr (LO) tma_2d(st + C::OFF_BL, &tmXl, kk, n0, &full[s]);
+      }
     }
     // copies still in flight must land before the CTA ends: wait for the
     // last ones the MMA thread may not have consumed (bounded)
-    for (int j = max(0, k - STAGES); j < k; ++j) mbar_wait(&full[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u);
+    for (int j = max(0, f - STAGES); j < f; ++j) mbar_wait(&full[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u);
   } else if (threadIdx.x == 32) {  // MMA issuer
-    for (int k = 0; k < nk; ++k) {
-      const int s = k % STAGES;
-      if (!mbar_wait(&full[s], static_cast<uint32_t>(k / STAGES) & 1u)) {
+    for (int f = 0; f < nf; ++f) {
+      const int s = f % STAGES;
+      if (!mbar_wait(&full[s], static_cast<uint32_t>(f / STAGES) & 1u)) {
         atomicOr(a.guard, GUARD_TIMEOUT);
         break;
       }
       tc_after();
-      uint8_t* st = smem + s * STAGE_BYTES;
+      const int cnt = min(KPS, nk - f * KPS);
+      for (int q = 0; q < cnt; ++q) {
+        uint8_t* st = smem + s * STAGE_BYTES + q * STEP_BYTES;
 #pragma unroll
-      for (int j = 0; j < BK / 16; ++j) {
-        const uint64_t ad = smem_desc(st + j * 32), bd = smem_desc(st + C::OFF_B + j * 32);
-        mma(tmem, ad, bd, C::IDESC, (k | j) != 0);
-        if constexpr (LO) mma(tmem, ad, smem_desc(st + C::OFF_BL + j * 32), C::IDESC, 1u);
-        if constexpr (WL) mma(tmem, smem_desc(st + C::OFF_AL + j * 32), bd, C::IDESC, 1u);
+        for (int j = 0; j < BK / 16; ++j) {
+          const uint64_t ad = smem_desc(st + j * 32), bd = smem_desc(st + C::OFF_B + j * 32);
+          mma(tmem, ad, bd, C::IDESC, (f | q | j) != 0);
+          if constexpr (LO) mma(tmem, ad, smem_desc(st + C::OFF_BL + j * 32), C::IDESC, 1u);
+          if constexpr (WL) mma(tmem, smem_desc(st + C::OFF_AL + j * 32), bd, C::IDESC, 1u);
+        }
       }
       mma_commit(&empty[s]);
     }
@@ -857,10 +876,10 @@ cudaError_t smem_attr(K kern, int bytes) {
 }
 
 cudaError_t tc_gemm_init_attrs() {
-  cudaError_t e = smem_attr(tc_gemm_kernel<128, true, false>, Tile<128, true, false>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<128, false, false>, Tile<128, false, false>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<128, true, true>, Tile<128, true, true>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<16, true, false>, Tile<16, true, false>::SMEM_BYTES);
+  cudaError_t e = smem_attr(tc_gemm_kernel<128, true, false>, TileG<128, true, false>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<128, false, false>, TileG<128, false, false>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<128, true, true>, TileG<128, true, true>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<16, true, false>, TileG<16, true, false>::SMEM_BYTES);
   if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<16, true, false>, Tile<16, true, false>::SMEM_BYTES);
   if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, false>, Tile<128, true, false>::SMEM_BYTES);
   if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, false, false>, Tile<128, false, false>::SMEM_BYTES);
@@ -914,13 +933,13 @@ cudaError_t launch_tc_gemm(const void* mapW, const void* mapWl, const void* mapX
   const int rows = (2 * ((a.N + 1) / 2) + BM - 1) / BM;
   const dim3 g16((a.T + 15) / 16, rows, a.splits), g128((a.T + 127) / 128, rows, a.splits);
   if (a.tile_tokens == 16 && lo && !wl) {
-    tc_gemm_kernel<16, true, false><<<g16, 128, Tile<16, true, false>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
+    tc_gemm_kernel<16, true, false><<<g16, 128, TileG<16, true, false>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
   } else if (a.tile_tokens == 128 && wl) {
-    tc_gemm_kernel<128, true, true><<<g128, 128, Tile<128, true, true>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
+    tc_gemm_kernel<128, true, true><<<g128, 128, TileG<128, true, true>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
   } else if (a.tile_tokens == 128 && lo) {
-    tc_gemm_kernel<128, true, false><<<g128, 128, Tile<128, true, false>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
+    tc_gemm_kernel<128, true, false><<<g128, 128, TileG<128, true, false>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
   } else if (a.tile_tokens == 128) {
-    tc_gemm_kernel<128, false, false><<<g128, 128, Tile<128, false, false>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
+    tc_gemm_kernel<128, false, false><<<g128, 128, TileG<128, false, false>::SMEM_BYTES, s>>>(w, wlo, xh, xl, a);
   } else {
     return cudaErrorInvalidValue;
   }
