@@ -668,10 +668,17 @@ __device__ bool g_phase(const MegaArgs& a, int q, const GDesc& d, const u64* xt,
             if (q == grp) ssq[q] += t;
         }
       }
+      if (a.groups <= 2) {  // the model's two groups: half the shuffles
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
+        for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ssq[q] += __shfl_xor_sync(0xffffffffu, ssq[q], o);
+          for (int q = 0; q < 2; ++q) ssq[q] += __shfl_xor_sync(0xffffffffu, ssq[q], o);
+      } else {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) ssq[q] += __shfl_xor_sync(0xffffffffu, ssq[q], o);
+      }
       if (lane == 0)
         for (int q = 0; q < 4; ++q) sh.ss[warp][q] = ssq[q];
       __syncthreads();
