@@ -35,9 +35,20 @@ def mio():
     return model_io
 
 
+# hidden 200 (three full 64-weight blocks and a partial one), intermediate 328,
+# an odd vocab of 301 (the last 16-row tile holds 13 rows, the last pair one)
+ODD = ki.ModelShape(hidden=200, n_layers=2, n_heads=4, n_kv_heads=1, head_dim=64, intermediate=328,
+                    norm_groups=2, vocab=301, eps=1e-6, rope_theta=10000.0, weight_dtype="bf16")
+
+
+@pytest.mark.parametrize("shape", ["ragged", "odd"])
 @pytest.mark.parametrize("weights", ["bf16", "f8", "q4"])
-def test_ragged_reduction_lengths_match_the_oracle(k2, mio, weights):
-    s = RAGGED
+def test_ragged_reduction_lengths_match_the_oracle(k2, mio, weights, shape):
+    """Every packed format (pair units, and the fp8 / int4 tile units of
+    gate/up and the lm_head) over reduction lengths and row counts that end
+    inside a chunk, a 64-weight block or a 16-row tile, against the oracle
+    over the same (quantized) weights."""
+    s = RAGGED if shape == "ragged" else ODD
     ctx, host = mio.build_context(s, max_context=64, kv_dtype="f16", gain_scale=0.1, keep_host=True,
                                   weights=None if weights == "bf16" else weights)
     assert ctx.info().persistent_grid > 0
