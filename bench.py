@@ -69,9 +69,10 @@ def parse():
     p.add_argument("--batch", type=int, default=1,
                    help="> 1: aggregate decode throughput of that many sequences per step (each prefilled "
                         "with --ctx random tokens); the default 1 is the batch-1 metric")
-    p.add_argument("--prefill-split", type=int, default=1, choices=[0, 1],
-                   help="K2_OPT_PREFILL_SPLIT for the prefill: 1 = activations as bf16 hi + lo halves "
-                        "(the default), 0 = single bf16 activations")
+    p.add_argument("--prefill-split", type=int, default=1, choices=[0, 1, 2],
+                   help="K2_OPT_PREFILL_SPLIT for the prefill: 1 = activations as bf16 hi + lo halves and the "
+                        "attention's queries / probabilities as fp16 hi + lo (the default), 0 = all single, "
+                        "2 = GEMM activations split, attention single")
     p.add_argument("--phase-timeline", default="",
                    help="after the timed steps, trace a few persistent steps (K2_OPT_TRACE: per-CTA clock stamps "
                         "at every phase's start, input ready, last slot and end), write the per-phase table to "

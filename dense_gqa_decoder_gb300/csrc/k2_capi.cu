@@ -279,7 +279,7 @@ struct k2_ctx {
   KvMaps pf_maps = {};    // the tcgen05 prefill attention's tensor maps of the caches (64-row boxes)
   bool pf_tc = false;     // fp16 cache of a supported shape: prefill attention on tcgen05
   bool use_pf_tc = true;  // option K2_OPT_PREFILL_ATTN
-  bool pf_split = true;   // option K2_OPT_PREFILL_SPLIT
+  int pf_split = 1;       // option K2_OPT_PREFILL_SPLIT (0, 1, 2)
   std::vector<LayerPtrs> ltab;
   // tensor-core prefill: TMA tensor maps (weights per layer: qkv, o, gate/up,
   // down; activations: normed input, attention output, SwiGLU output, hi/lo)
@@ -884,7 +884,9 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   };
   // without the split (blocks over 16 tokens only) the low-half maps are null:
   // the GEMMs read the high halves alone
-  const bool split = small || c->pf_split || q4;  // int4: the low-half weight MMA needs the activations' halves
+  // int4: the low-half weight MMA needs the activations' halves
+  const bool split = small || c->pf_split != 0 || q4;
+  const bool attn_split = small || c->pf_split == 1;  // 2: the GEMMs split, the attention's Q and P single
   const void* m_xh = small ? c->tb_xh.data() : c->tm_xh.data();
   const void* m_xl = small ? c->tb_xl.data() : split ? c->tm_xl.data() : nullptr;
   const void* m_oh = small ? c->tb_oh.data() : c->tm_oh.data();
@@ -928,7 +930,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
       pa.Q = Q;
       pa.oh = xh;
       pa.ol = split ? xl : nullptr;
-      pa.split = split ? 1 : 0;
+      pa.split = attn_split ? 1 : 0;
       pa.n = n;
       pa.nq = s.nq;
       pa.nkv = s.nkv;
@@ -1661,7 +1663,10 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
       c->l2_mask = static_cast<int>(value);
       break;
     case K2_OPT_PREFILL_ATTN: c->use_pf_tc = value != 0; break;
-    case K2_OPT_PREFILL_SPLIT: c->pf_split = value != 0; break;
+    case K2_OPT_PREFILL_SPLIT:
+      if (value < 0 || value > 2) return c->fail(K2_ERR_ARG, "prefill split %lld outside [0, 2]", (long long)value);
+      c->pf_split = static_cast<int>(value);
+      break;
     case K2_OPT_TRACE:
       if (value < 0 || value % 8) return c->fail(K2_ERR_ARG, "trace buffer must be 8-byte aligned (or 0)");
       c->trace = reinterpret_cast<unsigned long long*>(static_cast<uintptr_t>(value));

@@ -448,7 +448,8 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* m
 // through `maps` (the K and V caches of every layer, boxes of 64 dims x 64 rows);
 // the attention output goes to oh / ol [n][nq * D] as bf16 hi / lo halves.
 // split: queries and probabilities enter the MMAs as fp16 hi + lo halves (two
-// MMAs each), else as single fp16 values and only oh is written.
+// MMAs each), else as single fp16 values; ol (nullable) receives the output's
+// bf16 low halves.
 struct PrefillAttnArgs {
   const float* Q;
   __nv_bfloat16* oh;

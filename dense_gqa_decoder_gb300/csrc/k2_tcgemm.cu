@@ -760,7 +760,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
   const float l_sum = l_part + xmax[hf ^ 1][row];
   if (!bad && have_o) {
-    // this half of the row: O / sum, as bf16 hi + lo
+    // this half of the row: O / sum, as bf16 hi (+ lo when the GEMM that follows takes it)
     const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
     const size_t ob = static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D + hf * DH;
 #pragma unroll 1
@@ -774,7 +774,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
           split_bf16(__uint_as_float(ov[j]) * inv, h0, l0);
           split_bf16(__uint_as_float(ov[j + 1]) * inv, h1, l1);
           *reinterpret_cast<__nv_bfloat162*>(a.oh + ob + c + j) = __nv_bfloat162(h0, h1);
-          if constexpr (SPLIT) *reinterpret_cast<__nv_bfloat162*>(a.ol + ob + c + j) = __nv_bfloat162(l0, l1);
+          if (a.ol != nullptr) *reinterpret_cast<__nv_bfloat162*>(a.ol + ob + c + j) = __nv_bfloat162(l0, l1);
         }
       }
     }

@@ -413,12 +413,14 @@ typedef enum {
   K2_OPT_PREFILL_SPLIT = 12 /* tensor-core prefill of blocks over 16 tokens: 1 (default) feeds the GEMMs each
                              fp32 activation as two bf16 halves (hi + lo, two MMAs: the decode step's
                              precision) and the tcgen05 attention its queries and probabilities as two
-                             fp16 halves; 0 feeds single bf16 activations and single fp16 queries and
-                             probabilities (the model dtype; half the MMAs).  Decode steps and blocks of
-                             up to 16 tokens always keep the halves.  Measured on the 36-layer 3.7B
-                             shape (512-token prompt, 256 greedy steps, fp16 KV): 0 is 18 % faster
-                             but gives 96.5 % teacher-forced agreement and 2.1e-2 relative L2 on the
-                             prefill's logits, below the bf16 parity bars that 1 holds (100 %, 4.5e-4). */
+                             fp16 halves; 2 keeps the GEMMs' halves but gives the attention single fp16
+                             queries and probabilities; 0 feeds single bf16 activations and single fp16
+                             queries and probabilities (the model dtype; half the MMAs).  Decode steps and
+                             blocks of up to 16 tokens always keep the halves; int4 weights keep the GEMMs'.
+                             Measured on the 36-layer 3.7B shape (512-token prompt, 256 greedy steps, fp16
+                             KV): 1 gives 100 % teacher-forced agreement, relative L2 4.3e-4 (4.5e-4 on the
+                             prefill's logits); 2 is 5 % faster, 100 %, 5.1e-4 (1.4e-3); 0 is 18 % faster
+                             but 96.5 %, 1.1e-2 (2.1e-2), below the bf16 parity bars. */
 } k2_option;
 k2_status k2_set_option(k2_ctx* ctx, int32_t option, int64_t value);
 
