@@ -45,6 +45,16 @@ namespace k2 {
 
 namespace {
 
+// the merged output element: fp32 and / or the bf16 hi / lo pair a GEMM takes
+__device__ __forceinline__ void store_out(const AttnArgs& a, size_t i, float v) {
+  if (a.out != nullptr) a.out[i] = v;
+  if (a.out_hi != nullptr) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    a.out_hi[i] = h;
+    a.out_lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+}
+
 template <typename KVT>
 struct KVTraits;
 template <>
@@ -413,7 +423,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const Attn
       Ls = fmaf(ld_peer(peer_addr(&cpart[REP + h], s2)), w, Ls);
       O = fmaf(ld_peer(peer_addr(&cpart[2 * REP + idx], s2)), w, O);
     }
-    a.out[static_cast<size_t>(b) * a.nq * D + (g * REP + h) * D + (idx - h * D)] = O / Ls;
+    store_out(a, static_cast<size_t>(b) * a.nq * D + (g * REP + h) * D + (idx - h * D), O / Ls);
   }
   cluster_sync_all();  // peers read this CTA's cpart until here
 }
@@ -723,7 +733,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_tc_kernel(const _
       Ls = fmaf(ld_peer(peer_addr(&cpart[REP + h], s2)), w, Ls);
       O = fmaf(ld_peer(peer_addr(&cpart[2 * REP + idx], s2)), w, O);
     }
-    a.out[static_cast<size_t>(b) * a.nq * D + (g * REP + h) * D + (idx - h * D)] = O / Ls;
+    store_out(a, static_cast<size_t>(b) * a.nq * D + (g * REP + h) * D + (idx - h * D), O / Ls);
   }
   cluster_sync_all();  // peers read this CTA's cpart until here
 }

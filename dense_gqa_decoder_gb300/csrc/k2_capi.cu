@@ -893,7 +893,6 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   const void* m_ol = small ? c->tb_ol.data() : split ? c->tm_ol.data() : nullptr;
   const void* m_ah = small ? c->tb_ah.data() : c->tm_ah.data();
   const void* m_al = small ? c->tb_al.data() : split ? c->tm_al.data() : nullptr;
-  float* O32 = Q + static_cast<size_t>(16) * s.nq * s.d;  // small blocks: the attention output after 16 query rows
   cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.gb, X, s.H, s.V, c->guard,
                                     c->hist + static_cast<size_t>(seq) * c->lay.cap, 0, nullptr, pos0, d_pos0, st);
   for (int l = 0; l < s.L && !e; ++l) {
@@ -921,10 +920,11 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
       at.block_seq = seq;
       at.pos_base = pos0;
       at.pos_base_dev = d_pos0;
-      at.out = O32;
+      at.out = nullptr;  // the merged output goes straight to the o_proj GEMM's bf16 halves
+      at.out_hi = xh;
+      at.out_lo = xl;
       attn_maps(c, at, l);
       e = launch_attn(at, s.d, s.rep, kvdt, attn_splits(c, n), n, st, false);
-      if (!e) e = launch_rows_hilo(O32, xh, xl, n, s.nq * s.d, st);
     } else if (!e && c->pf_tc && c->use_pf_tc) {
       PrefillAttnArgs pa = {};
       pa.Q = Q;
@@ -1018,10 +1018,12 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
       at.ks = c->ks(l);
       at.vs = c->vs(l);
       at.seq0 = 0;
+      at.out = nullptr;  // the merged output goes straight to the o_proj GEMM's bf16 halves
+      at.out_hi = xh;
+      at.out_lo = xl;
       attn_maps(c, at, l);
       e = launch_attn(at, s.d, s.rep, kvdt, asplits, B, st, true);
     }
-    if (!e) e = launch_rows_hilo(c->attn_out, xh, xl, B, s.nq * s.d, st, true);
     if (!e) e = gemm(c->tmw[4 * l + 1].data(), c->tb_oh.data(), c->tb_ol.data(), s.H, s.nq * s.d, TC_RESID, X, s.H);
     if (!e)
       e = launch_norm_rows(X, B, c->mlp_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st, true, gout,

@@ -176,7 +176,9 @@ struct AttnArgs {
   int nq, nkv;
   const int* seq_len;
   int seq0;             // sequences seq0 .. seq0 + gridDim.z - 1
-  float* out;           // [batch][nq*D]
+  float* out;           // [batch][nq*D] fp32 (nullable when out_hi is given)
+  __nv_bfloat16* out_hi;  // nullable: the output also as bf16 hi = bf16(o), lo = bf16(o - hi)
+  __nv_bfloat16* out_lo;  //   (the activations of a tensor-core GEMM), [batch][nq*D]
   float scale;          // 1/sqrt(D)
   uint32_t slot_bytes;  // one warp's tile slot
   unsigned* guard;
