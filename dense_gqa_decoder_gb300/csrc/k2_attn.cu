@@ -45,6 +45,18 @@ namespace k2 {
 
 namespace {
 
+// element d of head h (q heads, then k, then v) of a token's projections in
+// natural order: read as is, or from the QKV GEMM's packed rows (dims i and
+// i + D/2 side by side) with q and k rotated by split-half RoPE at position pos
+__device__ __forceinline__ float qkv_at(const AttnArgs& a, const float* qkv, int h, int d, int D, int pos) {
+  if (a.rope == nullptr) return qkv[h * D + d];
+  const int half = D / 2, i = d < half ? d : d - half;
+  const float x = qkv[h * D + 2 * i], y = qkv[h * D + 2 * i + 1];
+  if (h >= a.nq + a.nkv) return d < half ? x : y;  // v: not rotated
+  const float2 cs = a.rope[static_cast<size_t>(pos) * half + i];
+  return d < half ? x * cs.x - y * cs.y : y * cs.x + x * cs.y;
+}
+
 // the merged output element: fp32 and / or the bf16 hi / lo pair a GEMM takes
 __device__ __forceinline__ void store_out(const AttnArgs& a, size_t i, float v) {
   if (a.out != nullptr) a.out[i] = v;
@@ -199,7 +211,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const Attn
 #pragma unroll
   for (int h = 0; h < REP; ++h)
 #pragma unroll
-    for (int e = 0; e < QD; ++e) q[h][e] = qkv[(g * REP + h) * D + kl * QD + e] * a.scale;
+    for (int e = 0; e < QD; ++e) q[h][e] = qkv_at(a, qkv, g * REP + h, kl * QD + e, D, pos) * a.scale;
   pdl_trigger();
 
   float m[REP], l[REP], acc[REP][DPL];
@@ -237,17 +249,18 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const Attn
         break;
       }
       for (int kv = 0; kv < 2; ++kv) {
-        const float* src = qkv + (kv == 0 ? a.nq * D : (a.nq + a.nkv) * D) + g * D;
+        const int hs = (kv == 0 ? a.nq : a.nq + a.nkv) + g;  // this KV head's k (or v) among the heads
+        auto src = [&](int i) { return qkv_at(a, qkv, hs, i, D, pos); };
         KVT* dst = reinterpret_cast<KVT*>(kv == 0 ? a.kc_w : a.vc_w) + (head_row + pos) * D;
         KVT* row = reinterpret_cast<KVT*>(slot + kv * KVB + jr * ROWB);
         if constexpr (I8) {
           float amax = 0.f;
-          for (int i = lane; i < D; i += 32) amax = fmaxf(amax, fabsf(src[i]));
+          for (int i = lane; i < D; i += 32) amax = fmaxf(amax, fabsf(src(i)));
           amax = warp_max(amax);
           const __half sh = __float2half_rn(fminf(amax / 127.0f, 65504.0f));
           const float sf = __half2float(sh);
           for (int i = lane; i < D; i += 32) {
-            float cq = sf > 0.f ? rintf(src[i] / sf) : 0.f;
+            float cq = sf > 0.f ? rintf(src(i) / sf) : 0.f;
             cq = fminf(fmaxf(cq, -127.f), 127.f);
             const int8_t ci = static_cast<int8_t>(cq);
             dst[i] = ci;
@@ -259,14 +272,14 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_kernel(const Attn
           }
         } else if constexpr (std::is_same<KVT, __half>::value) {
           for (int i = lane; i < D; i += 32) {
-            const __half hv = __float2half_rn(src[i]);
+            const __half hv = __float2half_rn(src(i));
             dst[i] = hv;
             row[i] = hv;
           }
         } else {
           for (int i = lane; i < D; i += 32) {
-            dst[i] = src[i];
-            row[i] = src[i];
+            dst[i] = src(i);
+            row[i] = src(i);
           }
         }
       }
@@ -520,14 +533,15 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_tc_kernel(const _
   const float* qkv = a.qkv + static_cast<size_t>(b) * a.qkv_stride;
   uint32_t qa[KS][2];
   {
-    const float* qh = qkv + (g * REP + hq) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int d = 16 * ks + 8 * hf + 2 * tq;
         uint32_t hi = 0u, lo = 0u;
-        if (live) split_half2(qh[d] * a.scale, qh[d + 1] * a.scale, hi, lo);
+        if (live)
+          split_half2(qkv_at(a, qkv, g * REP + hq, d, D, pos) * a.scale,
+                      qkv_at(a, qkv, g * REP + hq, d + 1, D, pos) * a.scale, hi, lo);
         qa[ks][hf] = rem ? lo : hi;
       }
   }
@@ -561,11 +575,11 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_decode_tc_kernel(const _
         break;
       }
       for (int kv = 0; kv < 2; ++kv) {
-        const float* src = qkv + (kv == 0 ? a.nq * D : (a.nq + a.nkv) * D) + g * D;
+        const int hs = (kv == 0 ? a.nq : a.nq + a.nkv) + g;  // this KV head's k (or v) among the heads
         __half* dst = reinterpret_cast<__half*>(kv == 0 ? a.kc_w : a.vc_w) + (head_row + pos) * D;
         uint8_t* base = kv == 0 ? ksl : vsl;
         for (int i = lane; i < D; i += 32) {
-          const __half hv = __float2half_rn(src[i]);
+          const __half hv = __float2half_rn(qkv_at(a, qkv, hs, i, D, pos));
           dst[i] = hv;
           *reinterpret_cast<__half*>(base + (i >> 6) * T::BOX + swz(jr, (i & 63) >> 3) + (i & 7) * 2) = hv;
         }

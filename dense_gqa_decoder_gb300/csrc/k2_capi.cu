@@ -1009,10 +1009,12 @@ cudaError_t decode_batched(k2_ctx* c, cudaStream_t st, const int* d_tokens, int 
       e = launch_norm_rows(X, B, c->attn_norm[l], s.wb, xh, xl, s.H, s.G, c->cfg.eps, st, true, gout,
                            static_cast<size_t>(B) * s.qkv_n);
     if (!e) e = gemm(c->tmw[4 * l].data(), c->tb_xh.data(), c->tb_xl.data(), s.qkv_n, s.H, TC_STORE, gout, s.qkv_n);
-    if (!e)
-      e = launch_rope_batch(gout, c->qkv, c->rope, c->seq_len, B, s.nq, s.nkv, s.d, c->lay.cap, c->guard, st, true);
     if (!e) {
+      // the attention reads the QKV GEMM's packed rows and rotates q and k itself
       AttnArgs at = c->p_attn;
+      at.qkv = gout;
+      at.qkv_stride = s.qkv_n;
+      at.rope = c->rope;
       at.kc = at.kc_w = c->kc(l);
       at.vc = at.vc_w = c->vc(l);
       at.ks = c->ks(l);

@@ -173,6 +173,10 @@ struct AttnArgs {
   int cap;
   const float* qkv;  // [batch][qkv_stride] fp32: q (nq*D, rotated) | k (nkv*D, rotated) | v (nkv*D)
   int qkv_stride;
+  // non-null: qkv holds the QKV GEMM's packed rows instead (each head's dims
+  // as pairs (i, i + D/2) side by side, not rotated) and the kernel rotates q
+  // and k at the token's position with this table [cap][D/2] (cos, sin)
+  const float2* rope;
   int nq, nkv;
   const int* seq_len;
   int seq0;             // sequences seq0 .. seq0 + gridDim.z - 1
@@ -490,8 +494,6 @@ cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, co
                                 const void* vs, __nv_bfloat16* oh, __nv_bfloat16* ol, int n, int nq, int nkv, int D,
                                 int pos0, size_t head_row0, int cap, float scale, cudaStream_t s);
 cudaError_t launch_advance_by(int* seq_len, int seq, int n, cudaStream_t s);
-cudaError_t launch_rope_batch(const float* packed, float* nat, const float2* rope, const int* seq_len, int B, int nq,
-                              int nkv, int D, int cap, unsigned* guard, cudaStream_t s, bool pdl = false);
 cudaError_t launch_swiglu_rows(const float* gu, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int I, cudaStream_t s,
                                bool pdl = false);
 cudaError_t launch_rows_hilo(const float* x, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int K, cudaStream_t s,

@@ -502,37 +502,6 @@ constexpr size_t attn_smem() {
 
 __global__ void advance_by_kernel(int* seq_len, int seq, int n) { seq_len[seq] += n; }
 
-// Batched decode: token b belongs to sequence b at position seq_len[b].  The
-// QKV GEMM output (rows of every head in the packed order (i, i + d/2)) becomes
-// q | k | v in natural order with split-half RoPE at each token's position.
-__global__ void rope_batch_kernel(const float* __restrict__ packed, float* __restrict__ nat,
-                                  const float2* __restrict__ rope, const int* __restrict__ seq_len, int nq, int nkv,
-                                  int D, int cap, unsigned* guard) {
-  const int b = blockIdx.x;
-  const int qkv_n = (nq + 2 * nkv) * D, half = D / 2;
-  pdl_wait();
-  pdl_trigger();
-  int pos = seq_len[b];
-  if (pos < 0 || pos >= cap) {
-    if (threadIdx.x == 0) atomicOr(guard, GUARD_POS);
-    pos = 0;
-  }
-  const float* src = packed + static_cast<size_t>(b) * qkv_n;
-  float* dst = nat + static_cast<size_t>(b) * qkv_n;
-  for (int idx = threadIdx.x; idx < (nq + 2 * nkv) * half; idx += blockDim.x) {
-    const int h = idx / half, i = idx - h * half;
-    float a = src[h * D + 2 * i], c = src[h * D + 2 * i + 1];
-    if (h < nq + nkv) {
-      const float2 cs = rope[static_cast<size_t>(pos) * half + i];
-      const float ra = a * cs.x - c * cs.y, rc = c * cs.x + a * cs.y;
-      a = ra;
-      c = rc;
-    }
-    dst[h * D + i] = a;
-    dst[h * D + i + half] = c;
-  }
-}
-
 // gate/up GEMM rows (2p, 2p+1) = (gate_p, up_p) -> silu(gate) * up as bf16 hi/lo
 __global__ void swiglu_rows_kernel(const float* __restrict__ gu, __nv_bfloat16* __restrict__ oh,
                                    __nv_bfloat16* __restrict__ ol, int I) {
@@ -752,11 +721,6 @@ cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, co
   K2_PREFILL_ATTN_SHAPES(K2_PA_LAUNCH)
 #undef K2_PA_LAUNCH
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_rope_batch(const float* packed, float* nat, const float2* rope, const int* seq_len, int B, int nq,
-                              int nkv, int D, int cap, unsigned* guard, cudaStream_t s, bool pdl) {
-  return launch_k(rope_batch_kernel, dim3(B), dim3(1024), 0, s, pdl, packed, nat, rope, seq_len, nq, nkv, D, cap, guard);
 }
 
 cudaError_t launch_swiglu_rows(const float* gu, __nv_bfloat16* oh, __nv_bfloat16* ol, int rows, int I, cudaStream_t s,
