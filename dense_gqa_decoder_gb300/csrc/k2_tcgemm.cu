@@ -467,7 +467,8 @@ EncodeTiled encode_fn() {
 // fp16), and the final division by the sum makes the result exact anyway.
 // K/V tiles are double-buffered: the tile after next is requested as soon as a
 // stage is consumed.
-constexpr int kPaRows = 128, kPaKeys = 64, kPaThreads = 256;
+// 8 softmax warps (two per TMEM lane group) and one issuer warp
+constexpr int kPaRows = 128, kPaKeys = 64, kPaSoftWarps = 8, kPaThreads = 32 * (kPaSoftWarps + 1);
 constexpr float kRescaleLog = 8.0f;
 
 template <int D>
@@ -528,9 +529,11 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t full[2], sbar[2], obar[2];
+  __shared__ __align__(8) uint64_t full[2], sbar[2], obar[2], sfree[2], pready[2];
   __shared__ uint32_t tmem_slot;
   __shared__ float xmax[2][kPaRows];  // each half's tile maximum per row
+  __shared__ int pbad[kPaSoftWarps];   // a softmax warp's verdict, read by its pair partner
+  __shared__ int issued[3];            // the issuer's count of K/V tiles, S and P.V issued
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = (warp & 3) * 32 + lane;  // TMEM lane = query row
   const int hf = warp >> 2;                // which 32 of the 64 scores (and half of O) this thread takes
@@ -548,9 +551,13 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
       mbar_init(&full[b], 1);
       mbar_init(&sbar[b], 1);
       mbar_init(&obar[b], 1);
+      mbar_init(&sfree[b], kPaSoftWarps);
+      mbar_init(&pready[b], kPaSoftWarps);
     }
     fence_mbar_init();
   }
+  if (tid < kPaSoftWarps) pbad[tid] = 0;
+  if (tid < 3) issued[tid] = 0;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
                  "r"(Sm::TMEM_COLS)
@@ -558,7 +565,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   // this row's half of Q (pre-scaled by 1 / sqrt(D)) as fp16 hi + lo, swizzled
-  {
+  if (warp < kPaSoftWarps) {
     const float* q = a.Q + static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D;
 #pragma unroll
     for (int cc = 0; cc < D / 16; ++cc) {
@@ -585,7 +592,8 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
       tma_3d(base + (NA + at) * Sm::KT, &maps.v, 64 * at, krow0 + kt * kPaKeys, a.layer, &full[st]);
     }
   };
-  if (tid == 0) {
+  const bool issuer = tid == kPaSoftWarps * 32;  // lane 0 of the last warp issues every copy and MMA
+  if (issuer) {
     if (nkt > 0) issue_tile(0);
     if (nkt > 1) issue_tile(1);
   }
@@ -605,161 +613,208 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
     }
     mma_commit(&sbar[kt & 1]);
   };
+  // the issuer: P.V of tile kt (hi and lo halves of P) into O
+  auto issue_pv = [&](int kt) {
+    const int b = kt & 1;
+    const uint8_t* ph = smem + Sm::OFF_P + (2 * b) * Sm::P;
+    const uint8_t* vt = smem + Sm::OFF_VT + b * Sm::VT;
+#pragma unroll
+    for (int j = 0; j < kPaKeys / 16; ++j) {
+      const uint64_t vd = smem_desc(vt + j * 32);
+      mma(tmem, smem_desc(ph + j * 32), vd, Sm::IDESC_O, (kt > 0 || j > 0) ? 1u : 0u);
+      if constexpr (SPLIT) mma(tmem, smem_desc(ph + Sm::P + j * 32), vd, Sm::IDESC_O, 1u);
+    }
+    mma_commit(&obar[b]);
+  };
   const uint32_t lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
   const uint32_t t_o = tmem + lanes + hf * DH;                             // this thread's half of O
 
   float m_ref = -INFINITY, l_part = 0.f;  // the row's reference maximum; this half's sum of p
   bool bad = false;
-  int kt = 0, s_issued = 0, o_issued = 0;
-  if (tid == 0 && nkt > 0) {
-    if (mbar_wait(&full[0], 0)) {
-      tc_after();
-      issue_s(0);
-      s_issued = 1;
-    } else {
-      bad = true;
-    }
-  }
-  for (; kt < nkt; ++kt) {
-    const int b = kt & 1;
-    // thread 0: S of the next tile goes to the tensor pipe before this tile's softmax
-    if (tid == 0 && !bad && kt + 1 < nkt) {
-      if (mbar_wait(&full[(kt + 1) & 1], static_cast<uint32_t>((kt + 1) >> 1) & 1u)) {
+  if (warp == kPaSoftWarps) {
+    // The issuer: S of tile kt once its K/V stage has landed and its S buffer
+    // has been read (tile kt - 2); then P.V of tile kt - 1 once all softmax
+    // warps have written its P and V^T, and the copy of tile kt + 1 into the
+    // stage tile kt - 1 used.  The softmax warps never wait for one another.
+    if (issuer) {
+      int t_is = min(nkt, 2), s_is = 0, o_is = 0;
+      for (int kt = 0; kt < nkt && !bad; ++kt) {
+        const int b = kt & 1;
+        if (!mbar_wait(&full[b], static_cast<uint32_t>(kt >> 1) & 1u) ||
+            (kt >= 2 && !mbar_wait(&sfree[b], static_cast<uint32_t>((kt - 2) >> 1) & 1u))) {
+          bad = true;
+          break;
+        }
         tc_after();
-        issue_s(kt + 1);
-        s_issued = kt + 2;
+        issue_s(kt);
+        s_is = kt + 1;
+        if (kt >= 1) {
+          if (!mbar_wait(&pready[(kt - 1) & 1], static_cast<uint32_t>((kt - 1) >> 1) & 1u)) {
+            bad = true;
+            break;
+          }
+          tc_after();
+          issue_pv(kt - 1);
+          o_is = kt;
+          if (kt + 1 < nkt) {
+            issue_tile(kt + 1);
+            t_is = kt + 2;
+          }
+        }
+      }
+      if (!bad && nkt > 0) {
+        if (mbar_wait(&pready[(nkt - 1) & 1], static_cast<uint32_t>((nkt - 1) >> 1) & 1u)) {
+          tc_after();
+          issue_pv(nkt - 1);
+          o_is = nkt;
+        } else {
+          bad = true;
+        }
+      }
+      issued[0] = t_is;
+      issued[1] = s_is;
+      issued[2] = o_is;
+    }
+  } else {
+    for (int kt = 0; kt < nkt; ++kt) {
+      const int b = kt & 1;
+      // this tile's K/V stage has landed; the P.V of two tiles ago, which read
+      // buffers b, is done
+      if (!mbar_wait(&full[b], static_cast<uint32_t>(kt >> 1) & 1u)) bad = true;
+      if (kt >= 2 && !mbar_wait(&obar[b], static_cast<uint32_t>((kt - 2) >> 1) & 1u)) bad = true;
+      bad = __any_sync(0xffffffffu, bad);
+      // V^T [dim][key] from the V rows [key][dim]: 8x8 blocks, transposed on the
+      // way through registers; keys past the CTA's last one become zeros
+      if (!bad) {
+        const uint8_t* vst = smem + Sm::OFF_ST + b * Sm::STAGE + NA * Sm::KT;
+        uint8_t* vt = smem + Sm::OFF_VT + b * Sm::VT;
+        const int kvalid = kend - kt * kPaKeys;
+        constexpr int NBLK = (kPaKeys / 8) * (D / 8);
+        for (int bi = warp * 4; bi < NBLK; bi += 4 * kPaSoftWarps) {
+          const int m = lane >> 3, r8 = lane & 7;
+          const int blk = bi + m, kb = blk / (D / 8), db = blk - kb * (D / 8);
+          const int key = 8 * kb + r8;
+          uint32_t r[4];
+          ldsm_x4_t(smem_u32(vst + (db >> 3) * Sm::KT + sw128(key, 8 * (db & 7))), r[0], r[1], r[2], r[3]);
+          // lane (gq, tq) holds keys 8kb + 2tq, +1 of dim 8db + gq, for each of the 4 blocks
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int k0i = 8 * ((bi + i) / (D / 8)) + 2 * (lane & 3);
+            if (k0i >= kvalid) r[i] = 0u;
+            else if (k0i + 1 >= kvalid) r[i] &= 0x0000FFFFu;
+          }
+          stsm_x4(smem_u32(vt + sw128(8 * db + r8, 8 * kb)), r[0], r[1], r[2], r[3]);
+        }
+      }
+      // this thread's 32 scores of the row; then the S buffer is free for tile kt + 2
+      if (!mbar_wait(&sbar[b], static_cast<uint32_t>(kt >> 1) & 1u)) bad = true;
+      bad = __any_sync(0xffffffffu, bad);
+      tc_after();
+      float sv[32];
+      if (!bad) {
+        uint32_t raw[32];
+        tmem_ld32(tmem + lanes + D + 64 * b + 32 * hf, raw);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(raw[j]);
       } else {
-        bad = true;
-      }
-    }
-    // this tile's K/V stage has landed (its S was issued only then); the P.V
-    // of two tiles ago, which read buffers b, is done
-    if (!mbar_wait(&full[b], static_cast<uint32_t>(kt >> 1) & 1u)) bad = true;
-    if (kt >= 2 && !mbar_wait(&obar[b], static_cast<uint32_t>((kt - 2) >> 1) & 1u)) bad = true;
-    // V^T [dim][key] from the V rows [key][dim]: 8x8 blocks, transposed on the
-    // way through registers; keys past the CTA's last one become zeros
-    {
-      const uint8_t* vst = smem + Sm::OFF_ST + b * Sm::STAGE + NA * Sm::KT;
-      uint8_t* vt = smem + Sm::OFF_VT + b * Sm::VT;
-      const int kvalid = kend - kt * kPaKeys;
-      constexpr int NBLK = (kPaKeys / 8) * (D / 8);
-      for (int bi = warp * 4; bi < NBLK; bi += 4 * (kPaThreads / 32)) {
-        const int m = lane >> 3, r8 = lane & 7;
-        const int blk = bi + m, kb = blk / (D / 8), db = blk - kb * (D / 8);
-        const int key = 8 * kb + r8;
-        uint32_t r[4];
-        ldsm_x4_t(smem_u32(vst + (db >> 3) * Sm::KT + sw128(key, 8 * (db & 7))), r[0], r[1], r[2], r[3]);
-        // lane (gq, tq) holds keys 8kb + 2tq, +1 of dim 8db + gq, for each of the 4 blocks
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int k0i = 8 * ((bi + i) / (D / 8)) + 2 * (lane & 3);
-          if (k0i >= kvalid) r[i] = 0u;
-          else if (k0i + 1 >= kvalid) r[i] &= 0x0000FFFFu;
+        for (int j = 0; j < 32; ++j) sv[j] = -INFINITY;
+      }
+      tc_before();
+      __syncwarp();
+      if (lane == 0 && !bad) mbar_arrive(&sfree[b]);
+      float mx = -INFINITY;
+      const int last = row_ok ? qpos - kt * kPaKeys - 32 * hf : -1;  // this half's last visible column
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        sv[j] = j <= last ? sv[j] : -INFINITY;
+        mx = fmaxf(mx, sv[j]);
+      }
+      // the row's other half is taken by warp w ^ 4: a barrier of those two
+      // warps, which also share their verdicts, so both leave together
+      xmax[hf][row] = mx;
+      if (lane == 0) pbad[warp] = bad ? 1 : 0;
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+      if (pbad[warp ^ 4] != 0) bad = true;
+      const float mt = fmaxf(mx, xmax[hf ^ 1][row]);
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");  // xmax / pbad reused next tile
+      if (bad) break;
+      // the reference maximum moves only when a tile's maximum exceeds it by kRescaleLog
+      const bool move = row_ok && mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog);
+      const float alpha = move ? (m_ref == -INFINITY ? 0.f : expf(m_ref - mt)) : 1.f;
+      if (move) {
+        l_part *= alpha;
+        m_ref = mt;
+      }
+      if (kt > 0 && __any_sync(0xffffffffu, move)) {  // this half of O *= alpha (a warp-wide access)
+        // every earlier P.V must be done: the one of the previous tile may still run
+        const bool ok = mbar_wait(&obar[b ^ 1], static_cast<uint32_t>((kt - 1) >> 1) & 1u);
+        if (__any_sync(0xffffffffu, !ok)) {
+          // the partner warp learns it at the next tile's exchange, where both
+          // leave (leaving here could strand it at that barrier)
+          bad = true;
+          continue;
         }
-        stsm_x4(smem_u32(vt + sw128(8 * db + r8, 8 * kb)), r[0], r[1], r[2], r[3]);
-      }
-    }
-    // this thread's 32 scores of the row
-    if (!mbar_wait(&sbar[b], static_cast<uint32_t>(kt >> 1) & 1u)) bad = true;
-    tc_after();
-    float sv[32];
-    {
-      uint32_t raw[32];
-      tmem_ld32(tmem + lanes + D + 64 * b + 32 * hf, raw);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(raw[j]);
-    }
-    float mx = -INFINITY;
-    const int last = row_ok ? qpos - kt * kPaKeys - 32 * hf : -1;  // this half's last visible column
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      sv[j] = j <= last ? sv[j] : -INFINITY;
-      mx = fmaxf(mx, sv[j]);
-    }
-    // the row's other half is taken by warp w ^ 4: a barrier of those two warps
-    xmax[hf][row] = mx;
-    asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
-    const float mt = fmaxf(mx, xmax[hf ^ 1][row]);
-    // the reference maximum moves only when a tile's maximum exceeds it by kRescaleLog
-    const bool move = row_ok && mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog);
-    const float alpha = move ? (m_ref == -INFINITY ? 0.f : expf(m_ref - mt)) : 1.f;
-    if (move) {
-      l_part *= alpha;
-      m_ref = mt;
-    }
-    if (kt > 0 && __any_sync(0xffffffffu, move)) {  // this half of O *= alpha (a warp-wide access)
-      // every earlier P.V must be done: the one of the previous tile may still run
-      if (!mbar_wait(&obar[b ^ 1], static_cast<uint32_t>((kt - 1) >> 1) & 1u)) bad = true;
-      tc_after();
-      uint32_t ov[32];
+        tc_after();
+        uint32_t ov[32];
 #pragma unroll 1
-      for (int c = 0; c < DH; c += 32) {
-        tmem_ld32(t_o + c, ov);
+        for (int c = 0; c < DH; c += 32) {
+          tmem_ld32(t_o + c, ov);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-        tmem_st32(t_o + c, ov);
-      }
-    }
-    // P = exp(s - m_ref) as fp16 hi + lo, this half's 32 keys
-    {
-      uint8_t* ph = smem + Sm::OFF_P + (2 * b) * Sm::P;
-      uint8_t* pl = ph + Sm::P;
-      const float mr = m_ref == -INFINITY ? 0.f : m_ref;  // a row with no visible key yet: all p are 0
-      float ps = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          // masked columns are -inf: __expf gives 0
-          const float p0 = __expf(sv[8 * c + 2 * e] - mr), p1 = __expf(sv[8 * c + 2 * e + 1] - mr);
-          ps += p0 + p1;
-          split_half2(p0, p1, hi[e], lo[e]);
+          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+          tmem_st32(t_o + c, ov);
         }
-        const uint32_t off = sw128(row, 32 * hf + 8 * c);
-        *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        if constexpr (SPLIT) *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      l_part += ps;
-    }
-    fence_proxy_async();  // P and V^T (generic stores) before the MMAs read them
-    tc_before();
-    if (__syncthreads_or(bad)) break;
-    if (tid == 0) {  // O += P.V^T (hi and lo halves of P)
-      tc_after();
-      const uint8_t* ph = smem + Sm::OFF_P + (2 * b) * Sm::P;
-      const uint8_t* vt = smem + Sm::OFF_VT + b * Sm::VT;
+      // P = exp(s - m_ref) as fp16 hi + lo, this half's 32 keys
+      {
+        uint8_t* ph = smem + Sm::OFF_P + (2 * b) * Sm::P;
+        uint8_t* pl = ph + Sm::P;
+        const float mr = m_ref == -INFINITY ? 0.f : m_ref;  // a row with no visible key yet: all p are 0
+        float ps = 0.f;
 #pragma unroll
-      for (int j = 0; j < kPaKeys / 16; ++j) {
-        const uint64_t vd = smem_desc(vt + j * 32);
-        mma(tmem, smem_desc(ph + j * 32), vd, Sm::IDESC_O, (kt > 0 || j > 0) ? 1u : 0u);
-        if constexpr (SPLIT) mma(tmem, smem_desc(ph + Sm::P + j * 32), vd, Sm::IDESC_O, 1u);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            // masked columns are -inf: __expf gives 0
+            const float p0 = __expf(sv[8 * c + 2 * e] - mr), p1 = __expf(sv[8 * c + 2 * e + 1] - mr);
+            ps += p0 + p1;
+            split_half2(p0, p1, hi[e], lo[e]);
+          }
+          const uint32_t off = sw128(row, 32 * hf + 8 * c);
+          *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          if constexpr (SPLIT) *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        l_part += ps;
       }
-      mma_commit(&obar[b]);
-      // this stage is consumed (S done, V transposed): the tile after next goes there
-      if (kt + 2 < nkt) issue_tile(kt + 2);
+      fence_proxy_async();  // P and V^T (generic stores) before the MMAs read them
+      tc_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pready[b]);
     }
-    o_issued = kt + 1;
   }
   bad = __syncthreads_or(bad) != 0;  // one verdict for the CTA
+  const int t_issued = issued[0], s_issued = issued[1], o_issued = issued[2];
   // copies and MMAs still in flight end before the CTA's memory goes away (bounded waits)
-  if (bad) {
-    if (tid == 0) {
-      atomicOr(a.guard, GUARD_TIMEOUT);
-      for (int k = kt; k < min(nkt, kt + 2); ++k) (void)mbar_wait(&full[k & 1], static_cast<uint32_t>(k >> 1) & 1u);
-      if (s_issued > kt + 1) (void)mbar_wait(&sbar[(kt + 1) & 1], static_cast<uint32_t>((kt + 1) >> 1) & 1u);
-    }
+  if (bad && issuer) {
+    atomicOr(a.guard, GUARD_TIMEOUT);
+    for (int k = max(0, t_issued - 2); k < t_issued; ++k)
+      (void)mbar_wait(&full[k & 1], static_cast<uint32_t>(k >> 1) & 1u);
+    if (s_issued > 0) (void)mbar_wait(&sbar[(s_issued - 1) & 1], static_cast<uint32_t>((s_issued - 1) >> 1) & 1u);
   }
   bool have_o = o_issued > 0;
   for (int k = max(0, o_issued - 2); k < o_issued; ++k)
     if (!mbar_wait(&obar[k & 1], static_cast<uint32_t>(k >> 1) & 1u)) have_o = false;
   have_o = __syncthreads_and(have_o) != 0;  // the tensor-memory reads below are warp-wide
   tc_after();
-  // the row's sum: both halves
-  xmax[hf][row] = l_part;
-  asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
-  const float l_sum = l_part + xmax[hf ^ 1][row];
-  if (!bad && have_o) {
+  // the row's sum: both halves (softmax warps only)
+  float l_sum = 0.f;
+  if (warp < kPaSoftWarps) {
+    xmax[hf][row] = l_part;
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+    l_sum = l_part + xmax[hf ^ 1][row];
+  }
+  if (warp < kPaSoftWarps && !bad && have_o) {
     // this half of the row: O / sum, as bf16 hi (+ lo when the GEMM that follows takes it)
     const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
     const size_t ob = static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D + hf * DH;
@@ -778,7 +833,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
         }
       }
     }
-  } else if (tid == 0 && !bad && o_issued > 0) {
+  } else if (issuer && !bad && o_issued > 0 && !have_o) {
     atomicOr(a.guard, GUARD_TIMEOUT);
   }
   tc_before();
