@@ -593,13 +593,13 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
     }
   };
   const bool issuer = tid == kPaSoftWarps * 32;  // lane 0 of the last warp issues every copy and MMA
+  tc_before();
+  __syncthreads();  // the barriers (initialised by thread 0) and Q are ready
+  tc_after();
   if (issuer) {
     if (nkt > 0) issue_tile(0);
     if (nkt > 1) issue_tile(1);
   }
-  tc_before();
-  __syncthreads();
-  tc_after();
   const uint32_t tmem = tmem_slot;
   // thread 0: S of tile kt = Q.K^T into S buffer kt & 1 (hi and lo halves of Q)
   auto issue_s = [&](int kt) {
