@@ -73,6 +73,9 @@ def parse():
                    help="K2_OPT_PREFILL_SPLIT for the prefill: 1 = activations as bf16 hi + lo halves and the "
                         "attention's queries / probabilities as fp16 hi + lo (the default), 0 = all single, "
                         "2 = GEMM activations split, attention single")
+    p.add_argument("--prefill-gemm", type=int, default=1, choices=[0, 1],
+                   help="K2_OPT_PREFILL_GEMM: 1 = QKV and gate/up on the persistent kernel over whole tiles "
+                        "(the default), 0 = one CTA per tile")
     p.add_argument("--phase-timeline", default="",
                    help="after the timed steps, trace a few persistent steps (K2_OPT_TRACE: per-CTA clock stamps "
                         "at every phase's start, input ready, last slot and end), write the per-phase table to "
@@ -501,6 +504,7 @@ def run_ours(args, world, rank, local, pg):
     prompt = torch.from_numpy(ki.prompt_ids(s.vocab, args.ctx, seed=1 + rank)).cuda()
     # prefill: one untimed warm-up on a short prompt, then the timed prompt
     ctx.set_option(k2.K2_OPT_PREFILL_SPLIT, args.prefill_split)
+    ctx.set_option(k2.K2_OPT_PREFILL_GEMM, args.prefill_gemm)
     with torch.cuda.stream(stream):
         ctx.prefill(0, prompt[:256], tok, stream=stream)
     stream.synchronize()
@@ -625,7 +629,7 @@ def run_ours(args, world, rank, local, pg):
         "prefill": {"tokens": T, "ms": prefill_ms, "tok_per_s": T / (prefill_ms * 1e-3),
                     "algorithmic_tflop": (pf_linear + pf_attn) / 1e12,
                     "achieved_tflops": pf_tflops, "peak_tflops": tc_peak, "frac": pf_tflops / tc_peak,
-                    "split": bool(args.prefill_split),
+                    "split": bool(args.prefill_split), "persistent_gemm": bool(args.prefill_gemm),
                     "note": prefill_note(args)},
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
         "clocks": clk,

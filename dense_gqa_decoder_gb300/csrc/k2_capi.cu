@@ -280,6 +280,7 @@ struct k2_ctx {
   bool pf_tc = false;     // fp16 cache of a supported shape: prefill attention on tcgen05
   bool use_pf_tc = true;  // option K2_OPT_PREFILL_ATTN
   int pf_split = 1;       // option K2_OPT_PREFILL_SPLIT (0, 1, 2)
+  bool pf_whole = true;   // option K2_OPT_PREFILL_GEMM
   std::vector<LayerPtrs> ltab;
   // tensor-core prefill: TMA tensor maps (weights per layer: qkv, o, gate/up,
   // down; activations: normed input, attention output, SwiGLU output, hi/lo)
@@ -855,7 +856,9 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.out_lo = ol;
     g.guard = c->guard;
     g.row_scale = rs;
-    return launch_tc_gemm(mw, wlo, mh, ml, g, st);
+    if (!c->pf_whole) return launch_tc_gemm(mw, wlo, mh, ml, g, st);
+    g.whole = 1;
+    return launch_tc_gemm_sk(mw, wlo, mh, ml, g, c->sms, st);
   };
   // a block of at most 16 tokens (a speculative verification) streams every
   // weight matrix with the stream-K kernel over 16-token tiles, one CTA per
@@ -1667,6 +1670,7 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
       c->l2_mask = static_cast<int>(value);
       break;
     case K2_OPT_PREFILL_ATTN: c->use_pf_tc = value != 0; break;
+    case K2_OPT_PREFILL_GEMM: c->pf_whole = value != 0; break;
     case K2_OPT_PREFILL_SPLIT:
       if (value < 0 || value > 2) return c->fail(K2_ERR_ARG, "prefill split %lld outside [0, 2]", (long long)value);
       c->pf_split = static_cast<int>(value);

@@ -428,6 +428,8 @@ struct TcGemmArgs {
   int tile_tokens;  // 128 (prefill) or 16 (batched decode): must match the activation maps
   int splits;  // split-K: blockIdx.z takes K steps [ksteps*z/splits, ksteps*(z+1)/splits) and
                // adds its partial with atomicAdd (TC_STORE / TC_RESID only; 1 = no split)
+  int whole;   // persistent kernel: 1 = each CTA takes whole tiles (b, b + grid, ...) and the
+               // epilogue stores / adds / applies SwiGLU; 0 = stream-K shares with atomicAdd
   float* out;
   __nv_bfloat16* out_hi;
   __nv_bfloat16* out_lo;   // TC_SWIGLU: nullable (only the high half is written)
@@ -443,7 +445,8 @@ cudaError_t tc_gemm_init_attrs();
 // mapXl): the weights' low halves, a third MMA per K step (w_lo . x_hi).
 cudaError_t launch_tc_gemm(const void* mapW, const void* mapWl, const void* mapXh, const void* mapXl,
                            const TcGemmArgs& a, cudaStream_t s);
-// stream-K persistent variant (tile_tokens 16; TC_STORE into a zeroed target or TC_RESID), `ctas` CTAs.
+// persistent variant, `ctas` CTAs: stream-K (whole = 0; TC_STORE into a zeroed target or TC_RESID)
+// or whole tiles (whole = 1; any mode, tile_tokens 128 or 16).
 // pdl: programmatic dependent launch; the first weight stages are requested before
 // the kernel waits for its predecessor (weights never depend on an earlier kernel)
 cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* mapXh, const void* mapXl,

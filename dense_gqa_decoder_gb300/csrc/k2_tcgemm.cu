@@ -252,23 +252,30 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
 }
 
-// Stream-K variant for small token counts (batched decode): one persistent
-// CTA per SM takes an equal share of all (row tile, K step) pairs, so every SM
-// streams the same number of weight bytes; a tile cut by a share boundary is
-// finished with fp32 atomicAdd from both sides.  Warp 0 loads, warp 1 issues
-// the MMAs into one of two TMEM accumulators, warps 2-5 drain the other (warp
-// w reads TMEM lanes 32 (w % 4) ..), so accumulation and write-back overlap.
-// Output: atomicAdd into out (TC_RESID adds to the residual; TC_STORE expects
-// a zeroed target).
-template <int BN_, bool LO, bool WL>
+// Persistent variant: one CTA per SM, warp 0 loads, warp 1 issues the MMAs
+// into one of two TMEM accumulators, warps 2-5 drain the other (warp w reads
+// TMEM lanes 32 (w % 4) ..), so accumulation and write-back overlap.  The work
+// is a sequence of ring fills of KPS K steps each, over (row tile, token tile)
+// pairs ordered tokens-fastest, in one of two shares:
+//  - stream-K (a.whole == 0; few row tiles: o_proj, down, the batched decode):
+//    an equal share of all (tile, fill) pairs per CTA, so every SM streams the
+//    same number of weight bytes; a tile cut by a share boundary is finished
+//    with fp32 atomicAdd from both sides (TC_RESID adds to the residual,
+//    TC_STORE expects a zeroed target);
+//  - whole tiles (a.whole == 1; many tiles: the prefill's QKV and gate/up):
+//    CTA b takes tiles b, b + grid, b + 2 grid, ... (at any moment the CTAs
+//    share a few weight row tiles and all token tiles in L2), and the
+//    epilogue of one tile -- a plain store, the residual add or SwiGLU --
+//    runs while the next tile's K steps stream in.
+template <int BN_, bool LO, bool WL, int KPS>
 __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constant__ CUtensorMap tmW,
                                                             const __grid_constant__ CUtensorMap tmWl,
                                                             const __grid_constant__ CUtensorMap tmXh,
                                                             const __grid_constant__ CUtensorMap tmXl,
                                                             const TcGemmArgs a) {
-  using C = Tile<BN_, LO, WL>;
-  constexpr int BN = C::BN, STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES;
-  constexpr int STAGE_BYTES = C::STAGE_BYTES, COLS = C::TMEM_COLS;
+  using C = Tile<BN_, LO, WL, KPS>;
+  constexpr int BN = C::BN, STAGES = C::STAGES, STAGE_BYTES = C::STAGE_BYTES, STEP_BYTES = C::STEP_BYTES;
+  constexpr int COLS = C::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -277,9 +284,26 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tok_tiles = (a.T + BN - 1) / BN;
   const int row_tiles = (2 * ((a.N + 1) / 2) + BM - 1) / BM;
-  const int kpt = a.ksteps;
-  const long long total = static_cast<long long>(row_tiles) * tok_tiles * kpt;
-  const long long g0 = total * blockIdx.x / gridDim.x, g1 = total * (blockIdx.x + 1) / gridDim.x;
+  const int fpt = a.ksteps / KPS;  // ring fills per tile (ksteps is a multiple of 4)
+  const long long tiles = static_cast<long long>(row_tiles) * tok_tiles;
+  // this CTA's fills i = 0 .. cnt - 1 and the (tile, fill) each stands for
+  long long g0 = 0, cnt = 0;
+  if (a.whole) {
+    cnt = tiles > blockIdx.x ? ((tiles - 1 - blockIdx.x) / gridDim.x + 1) * fpt : 0;
+  } else {
+    const long long total = tiles * fpt;
+    g0 = total * blockIdx.x / gridDim.x;
+    cnt = total * (blockIdx.x + 1) / gridDim.x - g0;
+  }
+  auto at = [&](long long i, long long& tile, int& k) {
+    if (a.whole) {
+      tile = blockIdx.x + (i / fpt) * gridDim.x;
+      k = static_cast<int>(i % fpt);
+    } else {
+      tile = (g0 + i) / fpt;
+      k = static_cast<int>(g0 + i - tile * fpt);
+    }
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -302,80 +326,82 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
   tc_after();
   const uint32_t tmem = tmem_slot;
   if (threadIdx.x == 0) {  // TMA producer
+    // fill i of this CTA into stage memory st: its weight and / or activation boxes
+    auto load = [&](uint8_t* st, long long i, bool w, bool x, uint64_t* bar) {
+      long long tile;
+      int k;
+      at(i, tile, k);
+      const int m0 = static_cast<int>(tile / tok_tiles) * BM, n0 = static_cast<int>(tile % tok_tiles) * BN;
+#pragma unroll
+      for (int q = 0; q < KPS; ++q) {
+        uint8_t* sq = st + q * STEP_BYTES;
+        const int kk = (k * KPS + q) * BK;
+        if (w) {
+          tma_4d(sq, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, bar);
+          if constexpr (WL) tma_4d(sq + C::OFF_AL, &tmWl, kk & 255, 0, kk >> 8, m0 >> 1, bar);
+        }
+        if (x) {
+          tma_2d(sq + C::OFF_B, &tmXh, kk, n0, bar);
+          if constexpr (LO) tma_2d(sq + C::OFF_BL, &tmXl, kk, n0, bar);
+        }
+      }
+    };
     // Under programmatic dependent launch the weights of the first stages are
     // requested before waiting for the previous kernel (they never depend on
     // it); the activations of those stages follow once it has completed.
-    auto where = [&](long long gg, int& m0, int& n0, int& kk) {
-      const long long tile = gg / kpt;
-      const int k = static_cast<int>(gg - tile * kpt);
-      m0 = static_cast<int>(tile / tok_tiles) * BM;
-      n0 = static_cast<int>(tile % tok_tiles) * BN;
-      kk = k * BK;
-    };
-    const int pre = static_cast<int>(min(static_cast<long long>(STAGES), g1 - g0));
+    const int pre = static_cast<int>(min(static_cast<long long>(STAGES), cnt));
     for (int j = 0; j < pre; ++j) {
-      int m0, n0, kk;
-      where(g0 + j, m0, n0, kk);
       mbar_arrive_expect_tx(&full[j], STAGE_BYTES);
-      tma_4d(smem + j * STAGE_BYTES, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[j]);
-      if constexpr (WL) tma_4d(smem + j * STAGE_BYTES + C::OFF_AL, &tmWl, kk & 255, 0, kk >> 8, m0 >> 1, &full[j]);
+      load(smem + j * STAGE_BYTES, j, true, false, &full[j]);
     }
     pdl_wait();
     pdl_trigger();
-    for (int j = 0; j < pre; ++j) {
-      int m0, n0, kk;
-      where(g0 + j, m0, n0, kk);
-      uint8_t* st = smem + j * STAGE_BYTES;
-      tma_2d(st + C::OFF_B, &tmXh, kk, n0, &full[j]);
-      if constexpr (LO) tma_2d(st + C::OFF_BL, &tmXl, kk, n0, &full[j]);
-    }
-    long long g = g0 + pre;
-    int i = pre;
-    for (; g < g1; ++g, ++i) {
-      const int s = i % STAGES;
+    for (int j = 0; j < pre; ++j) load(smem + j * STAGE_BYTES, j, false, true, &full[j]);
+    long long i = pre;
+    for (; i < cnt; ++i) {
+      const int s = static_cast<int>(i % STAGES);
       if (i >= STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>((i / STAGES) - 1) & 1u)) {
         atomicOr(a.guard, GUARD_TIMEOUT);
         break;
       }
-      int m0, n0, kk;
-      where(g, m0, n0, kk);
       mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-      uint8_t* st = smem + s * STAGE_BYTES;
-      tma_4d(st, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
-      if constexpr (WL) tma_4d(st + C::OFF_AL, &tmWl, kk & 255, 0, kk >> 8, m0 >> 1, &full[s]);
-      tma_2d(st + C::OFF_B, &tmXh, kk, n0, &full[s]);
-      if constexpr (LO) tma_2d(st + C::OFF_BL, &tmXl, kk, n0, &full[s]);
+      load(smem + s * STAGE_BYTES, i, true, true, &full[s]);
     }
-    for (int j = max(0, i - STAGES); j < i; ++j) mbar_wait(&full[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u);
+    for (long long j = max(0ll, i - STAGES); j < i; ++j)
+      mbar_wait(&full[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u);
   } else if (threadIdx.x == 32) {  // MMA issuer
-    int i = 0, piece = 0;
+    int piece = 0;
     bool first = true;
-    for (long long g = g0; g < g1; ++g, ++i) {
-      const long long tile = g / kpt;
-      const int k = static_cast<int>(g - tile * kpt);
+    for (long long i = 0; i < cnt; ++i) {
+      long long tile;
+      int k;
+      at(i, tile, k);
       const int b = piece & 1;
       if (first && piece >= 2 && !mbar_wait(&acce[b], static_cast<uint32_t>((piece >> 1) - 1) & 1u)) {
         atomicOr(a.guard, GUARD_TIMEOUT);
         break;
       }
-      const int s = i % STAGES;
+      const int s = static_cast<int>(i % STAGES);
       if (!mbar_wait(&full[s], static_cast<uint32_t>(i / STAGES) & 1u)) {
         atomicOr(a.guard, GUARD_TIMEOUT);
         break;
       }
       tc_after();
-      uint8_t* st = smem + s * STAGE_BYTES;
       const uint32_t acc = tmem + b * COLS;
 #pragma unroll
-      for (int j = 0; j < BK / 16; ++j) {
-        const uint64_t ad = smem_desc(st + j * 32), bd = smem_desc(st + C::OFF_B + j * 32);
-        mma(acc, ad, bd, C::IDESC, (!first || j != 0) ? 1u : 0u);
-        if constexpr (LO) mma(acc, ad, smem_desc(st + C::OFF_BL + j * 32), C::IDESC, 1u);
-        if constexpr (WL) mma(acc, smem_desc(st + C::OFF_AL + j * 32), bd, C::IDESC, 1u);
+      for (int q = 0; q < KPS; ++q) {
+        uint8_t* st = smem + s * STAGE_BYTES + q * STEP_BYTES;
+#pragma unroll
+        for (int j = 0; j < BK / 16; ++j) {
+          const uint64_t ad = smem_desc(st + j * 32), bd = smem_desc(st + C::OFF_B + j * 32);
+          mma(acc, ad, bd, C::IDESC, (!first || q != 0 || j != 0) ? 1u : 0u);
+          if constexpr (LO) mma(acc, ad, smem_desc(st + C::OFF_BL + j * 32), C::IDESC, 1u);
+          if constexpr (WL) mma(acc, smem_desc(st + C::OFF_AL + j * 32), bd, C::IDESC, 1u);
+        }
       }
       mma_commit(&empty[s]);
       first = false;
-      if (k == kpt - 1 || g == g1 - 1) {  // this CTA's piece of the tile ends
+      if (k == fpt - 1 || i == cnt - 1) {  // this CTA's piece of the tile ends
         mma_commit(&accf[b]);
         ++piece;
         first = true;
@@ -385,10 +411,12 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
     const int lg = (warp & 3) * 32;  // the TMEM lanes (tile rows) this warp may read
     pdl_wait();  // the output (residual or zeroed target) is the previous kernels'
     int piece = 0;
-    long long g = g0;
-    while (g < g1) {
-      const long long tile = g / kpt;
-      const long long end = min(g1, (tile + 1) * kpt);
+    long long i = 0;
+    while (i < cnt) {
+      long long tile;
+      int k;
+      at(i, tile, k);
+      const long long iend = min(cnt, i + (fpt - k));
       const int b = piece & 1;
       const bool ok = mbar_wait(&accf[b], static_cast<uint32_t>(piece >> 1) & 1u);
       if (__any_sync(0xffffffffu, !ok)) {
@@ -408,15 +436,45 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
       if (lane == 0) mbar_arrive(&acce[b]);
       const int row = static_cast<int>(tile / tok_tiles) * BM + lg + lane;
       const int n0 = static_cast<int>(tile % tok_tiles) * BN;
-      if (row < a.N) {
-        const float rs = a.row_scale != nullptr ? __ldg(a.row_scale + row) : 1.f;
+      const float rs = (a.row_scale != nullptr && row < a.N) ? __ldg(a.row_scale + row) : 1.f;
+      if (!a.whole) {
+        if (row < a.N) {
 #pragma unroll
-        for (int j = 0; j < BN; ++j)
-          if (n0 + j < a.T)
-            atomicAdd(a.out + static_cast<size_t>(n0 + j) * a.ldo + row,
-                      a.row_scale != nullptr ? __uint_as_float(v[j]) * rs : __uint_as_float(v[j]));
+          for (int j = 0; j < BN; ++j)
+            if (n0 + j < a.T) atomicAdd(a.out + static_cast<size_t>(n0 + j) * a.ldo + row, __uint_as_float(v[j]) * rs);
+        }
+      } else if (a.mode == TC_SWIGLU) {
+        // rows (2p, 2p+1) = (gate_p, up_p) sit in adjacent lanes; per pair of
+        // columns (j, j+1) the even lane finishes column j and the odd lane
+        // column j+1, each after one exchange
+        const bool odd = lane & 1;
+#pragma unroll
+        for (int j = 0; j < BN; j += 2) {
+          const float a0 = __uint_as_float(v[j]) * rs, a1 = __uint_as_float(v[j + 1]) * rs;
+          const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
+          const float g = odd ? recv : a0, u = odd ? a1 : recv;
+          const int t = n0 + j + (odd ? 1 : 0);
+          if (t < a.T && row < a.N) {
+            const float y = g * __frcp_rn(1.0f + __expf(-g)) * u;
+            __nv_bfloat16 hi, lo;
+            split_bf16(y, hi, lo);
+            const size_t o = static_cast<size_t>(t) * a.ldo + (row >> 1);
+            a.out_hi[o] = hi;
+            if (a.out_lo != nullptr) a.out_lo[o] = lo;
+          }
+        }
+      } else if (row < a.N) {
+#pragma unroll
+        for (int j = 0; j < BN; ++j) {
+          if (n0 + j < a.T) {
+            float* o = a.out + static_cast<size_t>(n0 + j) * a.ldo + row;
+            const float y = __uint_as_float(v[j]) * rs;
+            if (a.mode == TC_RESID) *o += y;
+            else *o = y;
+          }
+        }
       }
-      g = end;
+      i = iend;
       ++piece;
     }
   }
@@ -935,23 +993,28 @@ cudaError_t tc_gemm_init_attrs() {
   if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<128, false, false>, TileG<128, false, false>::SMEM_BYTES);
   if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<128, true, true>, TileG<128, true, true>::SMEM_BYTES);
   if (e == cudaSuccess) e = smem_attr(tc_gemm_kernel<16, true, false>, TileG<16, true, false>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<16, true, false>, Tile<16, true, false>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, false>, Tile<128, true, false>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, false, false>, Tile<128, false, false>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, true>, Tile<128, true, true>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<16, true, false, 1>, Tile<16, true, false, 1>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, false, 1>, Tile<128, true, false, 1>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, false, false, 1>, Tile<128, false, false, 1>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, true, 1>, Tile<128, true, true, 1>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, false, 2>, Tile<128, true, false, 2>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, false, false, 2>, Tile<128, false, false, 2>::SMEM_BYTES);
   return e;
 }
 
 cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* mapXh, const void* mapXl,
                               const TcGemmArgs& a, int ctas, cudaStream_t s, bool pdl) {
   if (a.T <= 0) return cudaSuccess;
-  if ((a.tile_tokens != 16 && a.tile_tokens != 128) || a.mode == TC_SWIGLU || ctas < 1) return cudaErrorInvalidValue;
+  if ((a.tile_tokens != 16 && a.tile_tokens != 128) || (a.mode == TC_SWIGLU && !a.whole) || ctas < 1 ||
+      a.ksteps % 4 != 0)
+    return cudaErrorInvalidValue;
   const int tt = a.tile_tokens;
   const bool lo = mapXl != nullptr, wl = mapWl != nullptr;
   if ((tt == 16 && (!lo || wl)) || (wl && !lo)) return cudaErrorInvalidValue;
-  const long long total =
-      static_cast<long long>((2 * ((a.N + 1) / 2) + BM - 1) / BM) * ((a.T + tt - 1) / tt) * a.ksteps;
-  const int grid = static_cast<int>(std::min<long long>(ctas, total));
+  // whole tiles fill each ring stage with two K steps (larger copy groups) where two fit twice
+  const bool two = a.whole && tt == 128 && !wl;
+  const long long tiles = static_cast<long long>((2 * ((a.N + 1) / 2) + BM - 1) / BM) * ((a.T + tt - 1) / tt);
+  const int grid = static_cast<int>(std::min<long long>(ctas, a.whole ? tiles : tiles * a.ksteps));
   const CUtensorMap& w = *static_cast<const CUtensorMap*>(mapW);
   const CUtensorMap& wlo = *static_cast<const CUtensorMap*>(wl ? mapWl : mapW);  // unread without it
   const CUtensorMap& xh = *static_cast<const CUtensorMap*>(mapXh);
@@ -959,20 +1022,23 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* m
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = tt == 16 ? Tile<16, true, false>::SMEM_BYTES
-                         : wl     ? Tile<128, true, true>::SMEM_BYTES
-                         : lo     ? Tile<128, true, false>::SMEM_BYTES
-                                  : Tile<128, false, false>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = tt == 16 ? Tile<16, true, false, 1>::SMEM_BYTES
+                         : wl     ? Tile<128, true, true, 1>::SMEM_BYTES
+                         : two    ? (lo ? Tile<128, true, false, 2>::SMEM_BYTES : Tile<128, false, false, 2>::SMEM_BYTES)
+                         : lo     ? Tile<128, true, false, 1>::SMEM_BYTES
+                                  : Tile<128, false, false, 1>::SMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (tt == 16) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<16, true, false>, w, wlo, xh, xl, a);
-  if (wl) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true, true>, w, wlo, xh, xl, a);
-  if (lo) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true, false>, w, wlo, xh, xl, a);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, false, false>, w, wlo, xh, xl, a);
+  if (tt == 16) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<16, true, false, 1>, w, wlo, xh, xl, a);
+  if (wl) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true, true, 1>, w, wlo, xh, xl, a);
+  if (two && lo) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true, false, 2>, w, wlo, xh, xl, a);
+  if (two) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, false, false, 2>, w, wlo, xh, xl, a);
+  if (lo) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true, false, 1>, w, wlo, xh, xl, a);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, false, false, 1>, w, wlo, xh, xl, a);
 }
 
 cudaError_t launch_tc_gemm(const void* mapW, const void* mapWl, const void* mapXh, const void* mapXl,

@@ -20,7 +20,7 @@ K2_STATE_HEADER_BYTES = 96
 K2_F32, K2_BF16, K2_F16, K2_I8, K2_F8, K2_Q4 = range(6)
 (K2_OPT_PDL, K2_OPT_GRAPH, K2_OPT_ATTN_SPLITS, K2_OPT_PERSISTENT, K2_OPT_TC_PREFILL, K2_OPT_TC_DECODE,
  K2_OPT_WAIT_LIMIT_US, K2_OPT_STALL_PHASE, K2_OPT_L2_AHEAD, K2_OPT_L2_AHEAD_PHASES, K2_OPT_TRACE,
- K2_OPT_PREFILL_ATTN, K2_OPT_PREFILL_SPLIT) = range(13)
+ K2_OPT_PREFILL_ATTN, K2_OPT_PREFILL_SPLIT, K2_OPT_PREFILL_GEMM) = range(14)
 KERNEL_CLASSES = ("embed", "qkv", "attn", "o_proj", "gate_up", "down", "lm_head", "step", "sample")
 DTYPES = {"f32": K2_F32, "bf16": K2_BF16, "f16": K2_F16, "i8": K2_I8, "f8": K2_F8, "q4": K2_Q4}
 

@@ -410,7 +410,7 @@ typedef enum {
   K2_OPT_PREFILL_ATTN = 11, /* prefill attention of fp16 caches (head_dim 64 / 128, 4 query heads per KV head):
                              1 (default) on the 5th-generation tensor cores (tcgen05, S and O in tensor
                              memory), 0 on mma.sync */
-  K2_OPT_PREFILL_SPLIT = 12 /* tensor-core prefill of blocks over 16 tokens: 1 (default) feeds the GEMMs each
+  K2_OPT_PREFILL_SPLIT = 12, /* tensor-core prefill of blocks over 16 tokens: 1 (default) feeds the GEMMs each
                              fp32 activation as two bf16 halves (hi + lo, two MMAs: the decode step's
                              precision) and the tcgen05 attention its queries and probabilities as two
                              fp16 halves; 2 keeps the GEMMs' halves but gives the attention single fp16
@@ -421,6 +421,10 @@ typedef enum {
                              KV): 1 gives 100 % teacher-forced agreement, relative L2 4.3e-4 (4.5e-4 on the
                              prefill's logits); 2 is 5 % faster, 100 %, 5.1e-4 (1.4e-3); 0 is 18 % faster
                              but 96.5 %, 1.1e-2 (2.1e-2), below the bf16 parity bars. */
+  K2_OPT_PREFILL_GEMM = 13 /* tensor-core prefill of blocks over 16 tokens, QKV and gate/up GEMMs: 1 (default)
+                             one persistent CTA per SM over whole 128 x 128 tiles, two TMEM accumulators so
+                             that a tile's epilogue (store, SwiGLU) overlaps the next tile's K steps; 0 one
+                             CTA per tile (the epilogue after its own K steps) */
 } k2_option;
 k2_status k2_set_option(k2_ctx* ctx, int32_t option, int64_t value);
 

@@ -226,3 +226,34 @@ def test_prefill_without_split_against_oracle(k2, mio, kv, shape, first, n):
     print(f"{shape} kv={kv} first={first} n={n}: split rel_l2={r1:.3e}, single rel_l2={r0:.3e}")
     assert r0 <= (2e-2 if kv == "f16" else 5e-2)
     assert t0 == O.argmax_first(ref)
+
+
+@pytest.mark.parametrize("shape,first,n", [("k2_layer", 50, 1000), ("medium", 0, 333), ("medium", 129, 2100)])
+def test_persistent_prefill_gemm_against_per_tile_and_oracle(k2, mio, shape, first, n):
+    """K2_OPT_PREFILL_GEMM: QKV and gate/up on the persistent kernel over whole
+    tiles (1, the default: the SwiGLU epilogue of one tile overlaps the next
+    tile's K steps) against one CTA per tile (0) and the oracle's full
+    recompute; ragged token tiles, and a prompt longer than one 2048-token
+    block after cached rows."""
+    s = ki.SHAPES[shape]
+    pre = ki.prompt_ids(s.vocab, first, seed=93) if first else None
+    prompt = ki.prompt_ids(s.vocab, n, seed=94)
+    out = {}
+    for mode in (1, 0):
+        ctx, host = mio.build_context(s, max_context=first + n + 8, kv_dtype="f16", gain_scale=0.1, keep_host=True)
+        ctx.set_option(k2.K2_OPT_PREFILL_GEMM, mode)
+        if pre is not None:
+            prefill(k2, ctx, pre, s.vocab, True)
+        tok, lg = prefill(k2, ctx, prompt, s.vocab, True)
+        hid = k2.device_view(ctx.hidden_view(0), s.hidden, torch.float32).cpu().numpy().copy()
+        out[mode] = (tok, lg, hid)
+        assert ctx.sync_status() == k2.K2_OK
+    seq = prompt if pre is None else np.concatenate([pre, prompt])
+    ref = O.OracleModel(s, lambda nm, l: host[(nm, l)], "f16").forward_full(seq)
+    (t1, l1, h1), (t0, l0, h0) = out[1], out[0]
+    assert rel_l2(l1, ref) <= 2e-4
+    assert rel_l2(l0, ref) <= 2e-4
+    # same MMAs in the same order; only the SwiGLU epilogue's exp / reciprocal differ
+    assert rel_l2(l1, l0) <= 1e-4
+    assert rel_l2(h1, h0) <= 1e-4
+    assert t1 == t0 == O.argmax_first(ref)
