@@ -40,7 +40,7 @@ constexpr int BM = 128, BK = 64;
 // KPS_: K steps per ring stage.  A TMA copy group is taken in by an SM at a
 // rate that grows with the bytes requested together (measured: one 16 KB box
 // ~69 GB/s, two ~121, four ~142 from L2), not with the number of stages in
-// flight, so the non-persistent prefill kernel fills each stage with two K
+// flight, so the prefill kernels (128-token tiles) fill each stage with two K
 // steps (one barrier, twice the boxes).
 template <int BN_, bool LO_ = true, bool WL_ = false, int KPS_ = 1>
 struct Tile {
@@ -1011,8 +1011,9 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* m
   const int tt = a.tile_tokens;
   const bool lo = mapXl != nullptr, wl = mapWl != nullptr;
   if ((tt == 16 && (!lo || wl)) || (wl && !lo)) return cudaErrorInvalidValue;
-  // whole tiles fill each ring stage with two K steps (larger copy groups) where two fit twice
-  const bool two = a.whole && tt == 128 && !wl;
+  // 128-token tiles fill each ring stage with two K steps (larger copy groups: measured on the
+  // 4096-token prefill, 85.0 -> 80.2 ms with the stream-K o_proj / down so too) where two fit twice
+  const bool two = tt == 128 && !wl;
   const long long tiles = static_cast<long long>((2 * ((a.N + 1) / 2) + BM - 1) / BM) * ((a.T + tt - 1) / tt);
   const int grid = static_cast<int>(std::min<long long>(ctas, a.whole ? tiles : tiles * a.ksteps));
   const CUtensorMap& w = *static_cast<const CUtensorMap*>(mapW);
