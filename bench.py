@@ -69,10 +69,11 @@ def parse():
     p.add_argument("--batch", type=int, default=1,
                    help="> 1: aggregate decode throughput of that many sequences per step (each prefilled "
                         "with --ctx random tokens); the default 1 is the batch-1 metric")
-    p.add_argument("--prefill-split", type=int, default=1, choices=[0, 1, 2],
-                   help="K2_OPT_PREFILL_SPLIT for the prefill: 1 = activations as bf16 hi + lo halves and the "
-                        "attention's queries / probabilities as fp16 hi + lo (the default), 0 = all single, "
-                        "2 = GEMM activations split, attention single")
+    p.add_argument("--prefill-split", type=int, default=3, choices=[0, 1, 2, 3],
+                   help="K2_OPT_PREFILL_SPLIT for the prefill: 3 = single fp16 operands throughout (weights "
+                        "converted to fp16 per layer; the library's default), 1 = activations as bf16 hi + lo "
+                        "halves and the attention's queries / probabilities as fp16 hi + lo, 0 = all single "
+                        "(bf16 GEMMs), 2 = GEMM activations split, attention single")
     p.add_argument("--prefill-gemm", type=int, default=1, choices=[0, 1],
                    help="K2_OPT_PREFILL_GEMM: 1 = QKV and gate/up on the persistent kernel over whole tiles "
                         "(the default), 0 = one CTA per tile")
@@ -165,6 +166,10 @@ def prefill_note(args):
         return ("int4: each layer's codes * block scales dequantized into bf16 high and low halves, then the "
                 "tensor-core GEMMs with three MMAs per K step (w_hi x_hi, w_hi x_lo, w_lo x_hi); the last prompt "
                 "token takes the int4 decode step")
+    if args.prefill_split == 3:
+        return ("useful FLOPs (2 per weight x token + causal attention); every contraction on single fp16 "
+                "operands (the bf16 weights converted to fp16 per layer, exact in fp16's normal range; fp16 "
+                "activations, queries and probabilities), one MMA per K step, S and O in tensor memory")
     if args.prefill_split:
         return ("useful FLOPs (2 per weight x token + causal attention); the GEMMs issue twice the linear MMAs "
                 "(activations as bf16 hi + lo halves); attention (fp16 KV) issues tcgen05 MMAs on fp16 hi + lo "
@@ -629,7 +634,7 @@ def run_ours(args, world, rank, local, pg):
         "prefill": {"tokens": T, "ms": prefill_ms, "tok_per_s": T / (prefill_ms * 1e-3),
                     "algorithmic_tflop": (pf_linear + pf_attn) / 1e12,
                     "achieved_tflops": pf_tflops, "peak_tflops": tc_peak, "frac": pf_tflops / tc_peak,
-                    "split": bool(args.prefill_split), "persistent_gemm": bool(args.prefill_gemm),
+                    "split_mode": args.prefill_split, "persistent_gemm": bool(args.prefill_gemm),
                     "note": prefill_note(args)},
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
         "clocks": clk,

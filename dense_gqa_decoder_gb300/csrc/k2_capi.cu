@@ -45,6 +45,7 @@ struct Layout {
   size_t sqkv, so, sgu, sdown, slm;                // fp8 weights: per-row scales (first layer)
   size_t sqkv_layer, so_layer, sgu_layer, sdown_layer;
   size_t dq[4], dq_bytes[4];  // int4 prefill: matrix m of the current layer, bf16 hi then lo
+  size_t w16[4];              // bf16 weights, fp16 prefill: matrix m of the current layer as fp16
   size_t vlog, vids, varg, vpv, vpi;               // speculative verification: logits, ids, argmax
   // tensor-core prefill of up to `pchunk` tokens at a time (bf16 weights)
   int pchunk;
@@ -181,6 +182,12 @@ Layout layout_of(const k2_config& c) {
     l.tgu = take(l.tgu_layer * s.L);
     l.tdown = take(l.tdown_layer * s.L);
   }
+  if (c.weight_dtype == K2_BF16 && l.pchunk > 0) {  // one layer's weights as fp16, rebuilt per layer
+    l.w16[0] = take(l.wqkv_layer);
+    l.w16[1] = take(l.wo_layer);
+    l.w16[2] = take(l.wgu_layer);
+    l.w16[3] = take(l.wdown_layer);
+  }
   if (c.weight_dtype == K2_Q4 && l.pchunk > 0) {  // one layer's weights as bf16 hi / lo, rebuilt per layer
     const int Ns[4] = {s.qkv_n, s.H, 2 * s.I, s.H}, Ks[4] = {s.H, s.nq * s.d, s.H, s.I};
     for (int m = 0; m < 4; ++m) {
@@ -279,7 +286,7 @@ struct k2_ctx {
   KvMaps pf_maps = {};    // the tcgen05 prefill attention's tensor maps of the caches (64-row boxes)
   bool pf_tc = false;     // fp16 cache of a supported shape: prefill attention on tcgen05
   bool use_pf_tc = true;  // option K2_OPT_PREFILL_ATTN
-  int pf_split = 1;       // option K2_OPT_PREFILL_SPLIT (0, 1, 2)
+  int pf_split = 3;       // option K2_OPT_PREFILL_SPLIT (0 .. 3)
   bool pf_whole = true;   // option K2_OPT_PREFILL_GEMM
   std::vector<LayerPtrs> ltab;
   // tensor-core prefill: TMA tensor maps (weights per layer: qkv, o, gate/up,
@@ -291,6 +298,7 @@ struct k2_ctx {
   std::vector<std::array<uint8_t, kTcMapBytes>> tmw;  // 4 per layer
   std::array<uint8_t, kTcMapBytes> tm_xh{}, tm_xl{}, tm_oh{}, tm_ol{}, tm_ah{}, tm_al{}, tm_lm{};
   std::array<std::array<uint8_t, kTcMapBytes>, 4> tm_wlo{};  // int4: the weights' low halves
+  std::array<std::array<uint8_t, kTcMapBytes>, 4> tm_w16{};  // bf16 weights: one layer's fp16 copy
   // the same activation buffers in 16-token tiles (batched decode)
   std::array<uint8_t, kTcMapBytes> tb_xh{}, tb_xl{}, tb_oh{}, tb_ol{}, tb_ah{}, tb_al{};
   // fp16 caches: the tensor maps of each layer's K and V for the tensor-core decode attention
@@ -788,6 +796,11 @@ cudaError_t plan_tc_prefill(k2_ctx* c) {
     for (int m = 0; m < 4; ++m)
       if (!tc_encode_weight(c->tm_wlo[m].data(), c->dq_lo(m), Ns[m], Ks[m])) return cudaSuccess;
   }
+  if (c->cfg.weight_dtype == K2_BF16) {  // the tensor maps copy bytes: a bf16 map reads the fp16 copy as well
+    const int Ns[4] = {s.qkv_n, s.H, 2 * s.I, s.H}, Ks[4] = {s.H, s.nq * s.d, s.H, s.I};
+    for (int m = 0; m < 4; ++m)
+      if (!tc_encode_weight(c->tm_w16[m].data(), c->ws + c->lay.w16[m], Ns[m], Ks[m])) return cudaSuccess;
+  }
   const int P = c->lay.pchunk;
   bool ok = true;
   for (int tt : {128, 16}) {
@@ -828,8 +841,27 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   // int4: before its GEMM, each matrix of the layer is dequantized into bf16
   // halves (c->dq_*), and the GEMM adds the low halves' products
   const bool q4 = c->q4();
+  // a block of at most 16 tokens (a speculative verification) streams every
+  // weight matrix with the stream-K kernel over 16-token tiles, one CTA per
+  // SM: the 128-token tiles would leave most SMs idle (int4 weights keep the
+  // 128-token tiles, the only ones with a low-half weight operand)
+  const bool small = n <= 16 && !q4;
+  // fp16 operands (option K2_OPT_PREFILL_SPLIT = 3: bf16 weights, fp16 caches on
+  // the tcgen05 attention, blocks over 16 tokens): each matrix of the layer is
+  // converted to fp16 (exact in fp16's normal range) before its GEMM, and the
+  // activations enter as single fp16; elsewhere 3 acts as 1
+  const bool f16 = c->pf_split == 3 && c->cfg.weight_dtype == K2_BF16 && !small && c->pf_tc && c->use_pf_tc;
+  const int mode = f16 ? 3 : c->pf_split == 3 ? 1 : c->pf_split;
+  auto wmap = [&](int l, int m) -> const void* { return f16 ? c->tm_w16[m].data() : c->tmw[4 * l + m].data(); };
   const void* wlo = nullptr;
   auto dequant = [&](int l, int m) {
+    if (f16) {
+      const void* srcs[4] = {c->wqkv(l), c->wop(l), c->wgu(l), c->wdown(l)};
+      const int Ns[4] = {s.qkv_n, s.H, 2 * s.I, s.H}, Ks[4] = {s.H, s.nq * s.d, s.H, s.I};
+      return launch_bf16_to_f16(reinterpret_cast<__half*>(c->ws + c->lay.w16[m]),
+                                static_cast<const __nv_bfloat16*>(srcs[m]), packed_bytes(Ns[m], Ks[m], 2) / 2,
+                                c->guard, st);
+    }
     if (!q4) {
       wlo = nullptr;
       return cudaSuccess;
@@ -856,15 +888,11 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.out_lo = ol;
     g.guard = c->guard;
     g.row_scale = rs;
+    g.f16 = f16 ? 1 : 0;
     if (!c->pf_whole) return launch_tc_gemm(mw, wlo, mh, ml, g, st);
     g.whole = 1;
     return launch_tc_gemm_sk(mw, wlo, mh, ml, g, c->sms, st);
   };
-  // a block of at most 16 tokens (a speculative verification) streams every
-  // weight matrix with the stream-K kernel over 16-token tiles, one CTA per
-  // SM: the 128-token tiles would leave most SMs idle (int4 weights keep the
-  // 128-token tiles, the only ones with a low-half weight operand)
-  const bool small = n <= 16 && !q4;
   const int tt = small ? 16 : 128;
   auto gemm_sk = [&](const void* mw, const float* rs, const void* mh, const void* ml, int N, int K, int mode, float* out,
                      int ldo) {
@@ -880,6 +908,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.out = out;
     g.guard = c->guard;
     g.row_scale = rs;
+    g.f16 = f16 ? 1 : 0;
     cudaError_t e = cudaSuccess;
     if (mode == TC_STORE) e = cudaMemsetAsync(out, 0, sizeof(float) * static_cast<size_t>(n) * ldo, st);
     if (!e) e = launch_tc_gemm_sk(mw, wlo, mh, ml, g, c->sms, st);
@@ -888,8 +917,8 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   // without the split (blocks over 16 tokens only) the low-half maps are null:
   // the GEMMs read the high halves alone
   // int4: the low-half weight MMA needs the activations' halves
-  const bool split = small || c->pf_split != 0 || q4;
-  const bool attn_split = small || c->pf_split == 1;  // 2: the GEMMs split, the attention's Q and P single
+  const bool split = !f16 && (small || mode != 0 || q4);
+  const bool attn_split = small || mode == 1;  // 2, 3: the attention's Q and P single
   const void* m_xh = small ? c->tb_xh.data() : c->tm_xh.data();
   const void* m_xl = small ? c->tb_xl.data() : split ? c->tm_xl.data() : nullptr;
   const void* m_oh = small ? c->tb_oh.data() : c->tm_oh.data();
@@ -899,12 +928,13 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.gb, X, s.H, s.V, c->guard,
                                     c->hist + static_cast<size_t>(seq) * c->lay.cap, 0, nullptr, pos0, d_pos0, st);
   for (int l = 0; l < s.L && !e; ++l) {
-    if (!e) e = launch_norm_rows(X, n, c->attn_norm[l], s.gb, xh, xl, s.H, s.G, c->cfg.eps, st);
+    if (!e)
+      e = launch_norm_rows(X, n, c->attn_norm[l], s.gb, xh, xl, s.H, s.G, c->cfg.eps, st, false, nullptr, 0, nullptr,
+                           f16, c->guard);
     if (!e) e = dequant(l, 0);
     if (!e)
-      e = small ? gemm_sk(c->tmw[4 * l].data(), c->tcs(l, 0), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, s.qkv_n)
-                : gemm(c->tmw[4 * l].data(), c->tcs(l, 0), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, nullptr, nullptr,
-                       s.qkv_n);
+      e = small ? gemm_sk(wmap(l, 0), c->tcs(l, 0), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, s.qkv_n)
+                : gemm(wmap(l, 0), c->tcs(l, 0), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, nullptr, nullptr, s.qkv_n);
     if (!e)
       e = launch_rope_append(qkv, Q, c->rope, kvdt, c->kc(l), c->vc(l), c->ks(l), c->vs(l), n, s.nq, s.nkv, s.d,
                              pos0, d_pos0, head_row0, c->lay.cap, st);
@@ -934,6 +964,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
       pa.oh = xh;
       pa.ol = split ? xl : nullptr;
       pa.split = attn_split ? 1 : 0;
+      pa.f16out = f16 ? 1 : 0;
       pa.n = n;
       pa.nq = s.nq;
       pa.nkv = s.nkv;
@@ -950,20 +981,22 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     }
     // o_proj and down have few row tiles: stream-K over one CTA per SM
     if (!e) e = dequant(l, 1);
-    if (!e) e = gemm_sk(c->tmw[4 * l + 1].data(), c->tcs(l, 1), m_oh, m_ol, s.H, s.nq * s.d, TC_RESID, X, s.H);
-    if (!e) e = launch_norm_rows(X, n, c->mlp_norm[l], s.gb, xh, xl, s.H, s.G, c->cfg.eps, st);
+    if (!e) e = gemm_sk(wmap(l, 1), c->tcs(l, 1), m_oh, m_ol, s.H, s.nq * s.d, TC_RESID, X, s.H);
+    if (!e)
+      e = launch_norm_rows(X, n, c->mlp_norm[l], s.gb, xh, xl, s.H, s.G, c->cfg.eps, st, false, nullptr, 0, nullptr,
+                           f16, c->guard);
     if (!e) e = dequant(l, 2);
     if (!e) {
       if (small) {  // gate/up rows to fp32 (the QKV buffer is free by now), then SwiGLU rows
-        e = gemm_sk(c->tmw[4 * l + 2].data(), c->tcs(l, 2), m_xh, m_xl, 2 * s.I, s.H, TC_STORE, qkv, 2 * s.I);
+        e = gemm_sk(wmap(l, 2), c->tcs(l, 2), m_xh, m_xl, 2 * s.I, s.H, TC_STORE, qkv, 2 * s.I);
         if (!e) e = launch_swiglu_rows(qkv, ah, al, n, s.I, st);
       } else {
-        e = gemm(c->tmw[4 * l + 2].data(), c->tcs(l, 2), m_xh, m_xl, 2 * s.I, s.H, TC_SWIGLU, nullptr, ah,
-                 split ? al : nullptr, s.I);
+        e = gemm(wmap(l, 2), c->tcs(l, 2), m_xh, m_xl, 2 * s.I, s.H, TC_SWIGLU, nullptr, ah, split ? al : nullptr,
+                 s.I);
       }
     }
     if (!e) e = dequant(l, 3);
-    if (!e) e = gemm_sk(c->tmw[4 * l + 3].data(), c->tcs(l, 3), m_ah, m_al, s.H, s.I, TC_RESID, X, s.H);
+    if (!e) e = gemm_sk(wmap(l, 3), c->tcs(l, 3), m_ah, m_al, s.H, s.I, TC_RESID, X, s.H);
   }
   return e;
 }
@@ -1617,6 +1650,7 @@ k2_status k2_sync_status(k2_ctx* c, void* stream) {
   if (g & GUARD_TIMEOUT) why += " bounded-wait-timeout";
   if (g & GUARD_NAN) why += " nan-logit";
   if (g & GUARD_POS) why += " position-outside-cache";
+  if (g & GUARD_RANGE) why += " beyond-fp16-range";
   return c->fail(K2_ERR_DEVICE_GUARD, "device guard 0x%x:%s", g, why.c_str());
 }
 
@@ -1672,7 +1706,7 @@ k2_status k2_set_option(k2_ctx* c, int32_t option, int64_t value) {
     case K2_OPT_PREFILL_ATTN: c->use_pf_tc = value != 0; break;
     case K2_OPT_PREFILL_GEMM: c->pf_whole = value != 0; break;
     case K2_OPT_PREFILL_SPLIT:
-      if (value < 0 || value > 2) return c->fail(K2_ERR_ARG, "prefill split %lld outside [0, 2]", (long long)value);
+      if (value < 0 || value > 3) return c->fail(K2_ERR_ARG, "prefill split %lld outside [0, 3]", (long long)value);
       c->pf_split = static_cast<int>(value);
       break;
     case K2_OPT_TRACE:

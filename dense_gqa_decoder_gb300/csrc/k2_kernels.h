@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -15,6 +16,7 @@ enum : uint32_t {
   GUARD_TIMEOUT = 2u,  // a bounded wait ran out
   GUARD_NAN = 4u,      // a NaN logit
   GUARD_POS = 8u,      // a position outside the cache
+  GUARD_RANGE = 16u,   // a weight or activation outside the fp16 range (fp16 prefill operands)
 };
 
 // ---------------------------------------------------------------------------
@@ -428,6 +430,8 @@ struct TcGemmArgs {
   int tile_tokens;  // 128 (prefill) or 16 (batched decode): must match the activation maps
   int splits;  // split-K: blockIdx.z takes K steps [ksteps*z/splits, ksteps*(z+1)/splits) and
                // adds its partial with atomicAdd (TC_STORE / TC_RESID only; 1 = no split)
+  int f16;     // 1: fp16 operands (the weights' fp16 copy, single fp16 activations: no low-half map);
+               // TC_SWIGLU then writes fp16 into out_hi
   int whole;   // persistent kernel: 1 = each CTA takes whole tiles (b, b + grid, ...) and the
                // epilogue stores / adds / applies SwiGLU; 0 = stream-K shares with atomicAdd
   float* out;
@@ -471,6 +475,7 @@ struct PrefillAttnArgs {
   float scale;
   unsigned* guard;
   int split;
+  int f16out;  // 1: the output is written as single fp16 into oh (ol unused)
 };
 bool prefill_attn_tc_supported(int head_dim, int rep);
 cudaError_t prefill_attn_tc_init_attrs();
@@ -483,12 +488,18 @@ cudaError_t prefill_init_attrs();
 cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbytes, float* X, int H, int vocab,
                               unsigned* guard, int* hist, int hist_stride, const int* pos, int pos0,
                               const int* pos0_dev, cudaStream_t s, bool pdl = false);
-// GroupedRMSNorm rows -> bf16 hi/lo; zero (nullable, zero_floats a multiple of 4,
-// 16-byte aligned): extra CTAs clear it (the output of the GEMM that follows);
-// copy (nullable): the rows of X are also copied there
+// GroupedRMSNorm rows -> bf16 hi/lo (f16: single fp16 into oh, ol unused, a value
+// beyond the fp16 range raises GUARD_RANGE in guard); zero (nullable, zero_floats a
+// multiple of 4, 16-byte aligned): extra CTAs clear it (the output of the GEMM that
+// follows); copy (nullable): the rows of X are also copied there
 cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes, __nv_bfloat16* oh,
                              __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s, bool pdl = false,
-                             float* zero = nullptr, size_t zero_floats = 0, float* copy = nullptr);
+                             float* zero = nullptr, size_t zero_floats = 0, float* copy = nullptr, bool f16 = false,
+                             unsigned* guard = nullptr);
+// n bf16 values -> fp16 (round to nearest even; exact in fp16's normal range); a value
+// beyond +-65504 is clamped there and raises GUARD_RANGE in guard.  n a multiple of 8,
+// both buffers 16-byte aligned.
+cudaError_t launch_bf16_to_f16(__half* dst, const __nv_bfloat16* src, size_t n, unsigned* guard, cudaStream_t s);
 // pos0_dev (nullable): read the first position from device memory instead of pos0
 cudaError_t launch_rope_append(const float* qkv, float* Q, const float2* rope, int kv_dtype, void* kc, void* vc,
                                void* ks, void* vs, int n, int nq, int nkv, int D, int pos0, const int* pos0_dev,

@@ -47,11 +47,12 @@ __global__ void embed_rows_kernel(const int* __restrict__ tokens, const WT* __re
 }
 
 // GroupedRMSNorm of one row (k2-burn README, "Model shape": layernorm groups),
-// written as bf16 hi/lo
+// written as bf16 hi/lo, or (f16) as single fp16 into oh
 template <typename WT>
 __global__ void norm_rows_kernel(const float* __restrict__ X, const WT* __restrict__ gain, __nv_bfloat16* __restrict__ oh,
                                  __nv_bfloat16* __restrict__ ol, int H, int groups, float eps, int rows,
-                                 float4* __restrict__ zero, size_t zero_n4, float* __restrict__ copy) {
+                                 float4* __restrict__ zero, size_t zero_n4, float* __restrict__ copy, int f16,
+                                 unsigned* __restrict__ guard) {
   __shared__ float part[32][4];
   __shared__ float rs[4];
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -84,14 +85,45 @@ __global__ void norm_rows_kernel(const float* __restrict__ X, const WT* __restri
     rs[tid] = 1.0f / sqrtf(s / static_cast<float>(gsz) + eps);
   }
   __syncthreads();
+  bool range = false;
   for (int i = tid; i < H; i += blockDim.x) {
     const float y = x[i] * rs[i / gsz] * to_f32(gain[i]);
-    __nv_bfloat16 hi, lo;
-    split_bf16(y, hi, lo);
-    oh[static_cast<size_t>(t) * H + i] = hi;
-    ol[static_cast<size_t>(t) * H + i] = lo;
+    if (f16) {
+      range |= !(fabsf(y) <= 65504.f);
+      reinterpret_cast<__half*>(oh)[static_cast<size_t>(t) * H + i] = __float2half_rn(y);
+    } else {
+      __nv_bfloat16 hi, lo;
+      split_bf16(y, hi, lo);
+      oh[static_cast<size_t>(t) * H + i] = hi;
+      ol[static_cast<size_t>(t) * H + i] = lo;
+    }
     if (copy) copy[static_cast<size_t>(t) * H + i] = x[i];
   }
+  if (range && guard != nullptr) atomicOr(guard, GUARD_RANGE);
+}
+
+// bf16 -> fp16, eight values per thread and step
+__global__ void bf16_to_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n8,
+                                   unsigned* __restrict__ guard) {
+  bool range = false;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // a bf16 is the high half of the fp32 with the same value
+      float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
+      range |= !(fabsf(a) <= 65504.f) || !(fabsf(b) <= 65504.f);
+      a = fminf(fmaxf(a, -65504.f), 65504.f);
+      b = fminf(fmaxf(b, -65504.f), 65504.f);
+      const __half2 h = __floats2half2_rn(a, b);
+      o[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (range) atomicOr(guard, GUARD_RANGE);
 }
 
 // split-half RoPE on the QKV GEMM output (rows of every head in the packed
@@ -658,9 +690,20 @@ cudaError_t launch_embed_rows(const int* tokens, int n, const void* E, int wbyte
                   vocab, guard, hist, hist_stride, pos, pos0, pos0_dev);
 }
 
+cudaError_t launch_bf16_to_f16(__half* dst, const __nv_bfloat16* src, size_t n, unsigned* guard, cudaStream_t s) {
+  if (n % 8 || reinterpret_cast<uintptr_t>(dst) % 16 || reinterpret_cast<uintptr_t>(src) % 16)
+    return cudaErrorInvalidValue;
+  const size_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  const int grid = static_cast<int>(std::min<size_t>((n8 + 255) / 256, 152 * 8));
+  bf16_to_f16_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), n8,
+                                          guard);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes, __nv_bfloat16* oh,
                              __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s, bool pdl, float* zero,
-                             size_t zero_floats, float* copy) {
+                             size_t zero_floats, float* copy, bool f16, unsigned* guard) {
   if (zero_floats % 4 || (zero_floats && reinterpret_cast<uintptr_t>(zero) % 16)) return cudaErrorInvalidValue;
   const size_t n4 = zero_floats / 4;
   // extra CTAs (up to one per 8192 float4s, at most 64) clear the next GEMM's output
@@ -668,9 +711,9 @@ cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes
   if (wbytes == 2)
     return launch_k(norm_rows_kernel<__nv_bfloat16>, dim3(n + zc), dim3(512), 0, s, pdl, X,
                     static_cast<const __nv_bfloat16*>(gain), oh, ol, H, groups, eps, n,
-                    reinterpret_cast<float4*>(zero), n4, copy);
+                    reinterpret_cast<float4*>(zero), n4, copy, f16 ? 1 : 0, guard);
   return launch_k(norm_rows_kernel<float>, dim3(n + zc), dim3(512), 0, s, pdl, X, static_cast<const float*>(gain), oh,
-                  ol, H, groups, eps, n, reinterpret_cast<float4*>(zero), n4, copy);
+                  ol, H, groups, eps, n, reinterpret_cast<float4*>(zero), n4, copy, f16 ? 1 : 0, guard);
 }
 
 cudaError_t launch_rope_append(const float* qkv, float* Q, const float2* rope, int kv_dtype, void* kc, void* vc,

@@ -121,6 +121,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
 template <int BN, bool LO, bool WL>
 using TileG = Tile<BN, LO, WL, (BN >= 128 && !WL) ? 2 : 1>;
 
+// the instruction descriptor with fp16 A and B (a.f16) instead of bf16: the
+// A / B type fields (bits 7-9, 10-12) are 0 for fp16, 1 for bf16
+__device__ __forceinline__ uint32_t idesc_for(uint32_t bf16_desc, int f16) {
+  return f16 ? (bf16_desc & ~((7u << 7) | (7u << 10))) : bf16_desc;
+}
+// SwiGLU of one (gate, up) pair into output o: bf16 hi (+ lo), or single fp16 (f16)
+__device__ __forceinline__ void swiglu_store(const TcGemmArgs& a, size_t o, float g, float u) {
+  const float y = g * __frcp_rn(1.0f + __expf(-g)) * u;
+  if (a.f16) {
+    if (!(fabsf(y) <= 65504.f)) atomicOr(a.guard, GUARD_RANGE);
+    reinterpret_cast<__half*>(a.out_hi)[o] = __float2half_rn(y);
+    return;
+  }
+  __nv_bfloat16 hi = __float2bfloat16_rn(y);
+  a.out_hi[o] = hi;
+  if (a.out_lo != nullptr) a.out_lo[o] = __float2bfloat16_rn(y - __bfloat162float(hi));
+}
 __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(v);
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
@@ -196,14 +213,15 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
       }
       tc_after();
       const int cnt = min(KPS, nk - f * KPS);
+      const uint32_t idesc = idesc_for(C::IDESC, a.f16);
       for (int q = 0; q < cnt; ++q) {
         uint8_t* st = smem + s * STAGE_BYTES + q * STEP_BYTES;
 #pragma unroll
         for (int j = 0; j < BK / 16; ++j) {
           const uint64_t ad = smem_desc(st + j * 32), bd = smem_desc(st + C::OFF_B + j * 32);
-          mma(tmem, ad, bd, C::IDESC, (f | q | j) != 0);
-          if constexpr (LO) mma(tmem, ad, smem_desc(st + C::OFF_BL + j * 32), C::IDESC, 1u);
-          if constexpr (WL) mma(tmem, smem_desc(st + C::OFF_AL + j * 32), bd, C::IDESC, 1u);
+          mma(tmem, ad, bd, idesc, (f | q | j) != 0);
+          if constexpr (LO) mma(tmem, ad, smem_desc(st + C::OFF_BL + j * 32), idesc, 1u);
+          if constexpr (WL) mma(tmem, smem_desc(st + C::OFF_AL + j * 32), bd, idesc, 1u);
         }
       }
       mma_commit(&empty[s]);
@@ -228,13 +246,7 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
         const float acc = a.row_scale != nullptr ? __uint_as_float(v[j]) * rs : __uint_as_float(v[j]);
         if (a.mode == TC_SWIGLU) {  // rows (2p, 2p+1) = (gate_p, up_p): adjacent lanes
           const float up = __shfl_xor_sync(0xffffffffu, acc, 1);
-          if (!(lane & 1) && t < a.T && row < a.N) {
-            const float y = acc / (1.0f + expf(-acc)) * up;
-            __nv_bfloat16 hi, lo;
-            split_bf16(y, hi, lo);
-            a.out_hi[static_cast<size_t>(t) * a.ldo + (row >> 1)] = hi;
-            if (a.out_lo != nullptr) a.out_lo[static_cast<size_t>(t) * a.ldo + (row >> 1)] = lo;
-          }
+          if (!(lane & 1) && t < a.T && row < a.N) swiglu_store(a, static_cast<size_t>(t) * a.ldo + (row >> 1), acc, up);
         } else if (t < a.T && row < a.N) {
           float* o = a.out + static_cast<size_t>(t) * a.ldo + row;
           if (a.splits > 1) atomicAdd(o, acc);  // partial sums of a split K (the STORE target is zeroed)
@@ -251,6 +263,18 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
 }
+
+// a position in a persistent CTA's work: tile, and fill k of it; after the
+// tile's last fill the next tile is `step` further on
+struct Cursor {
+  int tile, k, fpt, step;
+  __device__ __forceinline__ void next() {
+    if (++k == fpt) {
+      k = 0;
+      tile += step;
+    }
+  }
+};
 
 // Persistent variant: one CTA per SM, warp 0 loads, warp 1 issues the MMAs
 // into one of two TMEM accumulators, warps 2-5 drain the other (warp w reads
@@ -285,25 +309,20 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
   const int tok_tiles = (a.T + BN - 1) / BN;
   const int row_tiles = (2 * ((a.N + 1) / 2) + BM - 1) / BM;
   const int fpt = a.ksteps / KPS;  // ring fills per tile (ksteps is a multiple of 4)
-  const long long tiles = static_cast<long long>(row_tiles) * tok_tiles;
-  // this CTA's fills i = 0 .. cnt - 1 and the (tile, fill) each stands for
-  long long g0 = 0, cnt = 0;
+  const int tiles = row_tiles * tok_tiles;
+  // this CTA's fills i = 0 .. cnt - 1, walked by a cursor (tile, fill k)
+  // that each role advances itself (no division in the loops)
+  int cnt = 0;
+  Cursor first{0, 0, fpt, 1};
   if (a.whole) {
-    cnt = tiles > blockIdx.x ? ((tiles - 1 - blockIdx.x) / gridDim.x + 1) * fpt : 0;
+    cnt = tiles > static_cast<int>(blockIdx.x) ? ((tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1) * fpt : 0;
+    first = Cursor{static_cast<int>(blockIdx.x), 0, fpt, static_cast<int>(gridDim.x)};
   } else {
-    const long long total = tiles * fpt;
-    g0 = total * blockIdx.x / gridDim.x;
-    cnt = total * (blockIdx.x + 1) / gridDim.x - g0;
+    const long long total = static_cast<long long>(tiles) * fpt;
+    const long long g0 = total * blockIdx.x / gridDim.x;
+    cnt = static_cast<int>(total * (blockIdx.x + 1) / gridDim.x - g0);
+    first = Cursor{static_cast<int>(g0 / fpt), static_cast<int>(g0 % fpt), fpt, 1};
   }
-  auto at = [&](long long i, long long& tile, int& k) {
-    if (a.whole) {
-      tile = blockIdx.x + (i / fpt) * gridDim.x;
-      k = static_cast<int>(i % fpt);
-    } else {
-      tile = (g0 + i) / fpt;
-      k = static_cast<int>(g0 + i - tile * fpt);
-    }
-  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -326,16 +345,14 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
   tc_after();
   const uint32_t tmem = tmem_slot;
   if (threadIdx.x == 0) {  // TMA producer
-    // fill i of this CTA into stage memory st: its weight and / or activation boxes
-    auto load = [&](uint8_t* st, long long i, bool w, bool x, uint64_t* bar) {
-      long long tile;
-      int k;
-      at(i, tile, k);
-      const int m0 = static_cast<int>(tile / tok_tiles) * BM, n0 = static_cast<int>(tile % tok_tiles) * BN;
+    // the fill at cursor c into stage memory st: its weight and / or activation boxes
+    auto load = [&](uint8_t* st, const Cursor& c, bool w, bool x, uint64_t* bar) {
+      const int rt = c.tile / tok_tiles;
+      const int m0 = rt * BM, n0 = (c.tile - rt * tok_tiles) * BN;
 #pragma unroll
       for (int q = 0; q < KPS; ++q) {
         uint8_t* sq = st + q * STEP_BYTES;
-        const int kk = (k * KPS + q) * BK;
+        const int kk = (c.k * KPS + q) * BK;
         if (w) {
           tma_4d(sq, &tmW, kk & 255, 0, kk >> 8, m0 >> 1, bar);
           if constexpr (WL) tma_4d(sq + C::OFF_AL, &tmWl, kk & 255, 0, kk >> 8, m0 >> 1, bar);
@@ -349,74 +366,80 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
     // Under programmatic dependent launch the weights of the first stages are
     // requested before waiting for the previous kernel (they never depend on
     // it); the activations of those stages follow once it has completed.
-    const int pre = static_cast<int>(min(static_cast<long long>(STAGES), cnt));
-    for (int j = 0; j < pre; ++j) {
+    const int pre = min(STAGES, cnt);
+    Cursor c = first;
+    for (int j = 0; j < pre; ++j, c.next()) {
       mbar_arrive_expect_tx(&full[j], STAGE_BYTES);
-      load(smem + j * STAGE_BYTES, j, true, false, &full[j]);
+      load(smem + j * STAGE_BYTES, c, true, false, &full[j]);
     }
     pdl_wait();
     pdl_trigger();
-    for (int j = 0; j < pre; ++j) load(smem + j * STAGE_BYTES, j, false, true, &full[j]);
-    long long i = pre;
-    for (; i < cnt; ++i) {
-      const int s = static_cast<int>(i % STAGES);
-      if (i >= STAGES && !mbar_wait(&empty[s], static_cast<uint32_t>((i / STAGES) - 1) & 1u)) {
+    c = first;
+    for (int j = 0; j < pre; ++j, c.next()) load(smem + j * STAGE_BYTES, c, false, true, &full[j]);
+    int i = pre, s = pre % STAGES;
+    uint32_t ph = pre / STAGES;  // how often the ring wrapped before fill i
+    for (; i < cnt; ++i, c.next()) {
+      if (i >= STAGES && !mbar_wait(&empty[s], (ph - 1) & 1u)) {
         atomicOr(a.guard, GUARD_TIMEOUT);
         break;
       }
       mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-      load(smem + s * STAGE_BYTES, i, true, true, &full[s]);
+      load(smem + s * STAGE_BYTES, c, true, true, &full[s]);
+      if (++s == STAGES) {
+        s = 0;
+        ++ph;
+      }
     }
-    for (long long j = max(0ll, i - STAGES); j < i; ++j)
-      mbar_wait(&full[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u);
+    for (int j = max(0, i - STAGES); j < i; ++j) mbar_wait(&full[j % STAGES], static_cast<uint32_t>(j / STAGES) & 1u);
   } else if (threadIdx.x == 32) {  // MMA issuer
-    int piece = 0;
-    bool first = true;
-    for (long long i = 0; i < cnt; ++i) {
-      long long tile;
-      int k;
-      at(i, tile, k);
+    int piece = 0, s = 0, k = first.k;
+    uint32_t ph = 0;
+    bool start = true;  // the first fill of a piece: the accumulator is overwritten
+    for (int i = 0; i < cnt; ++i) {
       const int b = piece & 1;
-      if (first && piece >= 2 && !mbar_wait(&acce[b], static_cast<uint32_t>((piece >> 1) - 1) & 1u)) {
+      if (start && piece >= 2 && !mbar_wait(&acce[b], static_cast<uint32_t>((piece >> 1) - 1) & 1u)) {
         atomicOr(a.guard, GUARD_TIMEOUT);
         break;
       }
-      const int s = static_cast<int>(i % STAGES);
-      if (!mbar_wait(&full[s], static_cast<uint32_t>(i / STAGES) & 1u)) {
+      if (!mbar_wait(&full[s], ph & 1u)) {
         atomicOr(a.guard, GUARD_TIMEOUT);
         break;
       }
       tc_after();
       const uint32_t acc = tmem + b * COLS;
+      const uint32_t idesc = idesc_for(C::IDESC, a.f16);
 #pragma unroll
       for (int q = 0; q < KPS; ++q) {
         uint8_t* st = smem + s * STAGE_BYTES + q * STEP_BYTES;
 #pragma unroll
         for (int j = 0; j < BK / 16; ++j) {
           const uint64_t ad = smem_desc(st + j * 32), bd = smem_desc(st + C::OFF_B + j * 32);
-          mma(acc, ad, bd, C::IDESC, (!first || q != 0 || j != 0) ? 1u : 0u);
-          if constexpr (LO) mma(acc, ad, smem_desc(st + C::OFF_BL + j * 32), C::IDESC, 1u);
-          if constexpr (WL) mma(acc, smem_desc(st + C::OFF_AL + j * 32), bd, C::IDESC, 1u);
+          mma(acc, ad, bd, idesc, (!start || q != 0 || j != 0) ? 1u : 0u);
+          if constexpr (LO) mma(acc, ad, smem_desc(st + C::OFF_BL + j * 32), idesc, 1u);
+          if constexpr (WL) mma(acc, smem_desc(st + C::OFF_AL + j * 32), bd, idesc, 1u);
         }
       }
       mma_commit(&empty[s]);
-      first = false;
+      start = false;
       if (k == fpt - 1 || i == cnt - 1) {  // this CTA's piece of the tile ends
         mma_commit(&accf[b]);
         ++piece;
-        first = true;
+        start = true;
+      }
+      if (++k == fpt) k = 0;
+      if (++s == STAGES) {
+        s = 0;
+        ++ph;
       }
     }
   } else if (warp >= 2) {  // epilogue: drain each piece's accumulator
     const int lg = (warp & 3) * 32;  // the TMEM lanes (tile rows) this warp may read
     pdl_wait();  // the output (residual or zeroed target) is the previous kernels'
-    int piece = 0;
-    long long i = 0;
+    int piece = 0, i = 0;
+    Cursor c = first;
     while (i < cnt) {
-      long long tile;
-      int k;
-      at(i, tile, k);
-      const long long iend = min(cnt, i + (fpt - k));
+      const int len = min(cnt - i, fpt - c.k);  // this piece's fills
+      const int tile = c.tile;
       const int b = piece & 1;
       const bool ok = mbar_wait(&accf[b], static_cast<uint32_t>(piece >> 1) & 1u);
       if (__any_sync(0xffffffffu, !ok)) {
@@ -434,8 +457,9 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
       tc_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce[b]);
-      const int row = static_cast<int>(tile / tok_tiles) * BM + lg + lane;
-      const int n0 = static_cast<int>(tile % tok_tiles) * BN;
+      const int rt = tile / tok_tiles;
+      const int row = rt * BM + lg + lane;
+      const int n0 = (tile - rt * tok_tiles) * BN;
       const float rs = (a.row_scale != nullptr && row < a.N) ? __ldg(a.row_scale + row) : 1.f;
       if (!a.whole) {
         if (row < a.N) {
@@ -454,14 +478,7 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
           const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
           const float g = odd ? recv : a0, u = odd ? a1 : recv;
           const int t = n0 + j + (odd ? 1 : 0);
-          if (t < a.T && row < a.N) {
-            const float y = g * __frcp_rn(1.0f + __expf(-g)) * u;
-            __nv_bfloat16 hi, lo;
-            split_bf16(y, hi, lo);
-            const size_t o = static_cast<size_t>(t) * a.ldo + (row >> 1);
-            a.out_hi[o] = hi;
-            if (a.out_lo != nullptr) a.out_lo[o] = lo;
-          }
+          if (t < a.T && row < a.N) swiglu_store(a, static_cast<size_t>(t) * a.ldo + (row >> 1), g, u);
         }
       } else if (row < a.N) {
 #pragma unroll
@@ -474,7 +491,12 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
           }
         }
       }
-      i = iend;
+      i += len;
+      c.k += len;
+      if (c.k == fpt) {
+        c.k = 0;
+        c.tile += c.step;
+      }
       ++piece;
     }
   }
@@ -880,7 +902,12 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
     for (int c = 0; c < DH; c += 32) {
       uint32_t ov[32];
       tmem_ld32(t_o + c, ov);
-      if (row_ok) {
+      if (row_ok && a.f16out) {  // single fp16 (attention outputs are averages of V rows: inside its range)
+#pragma unroll
+        for (int j = 0; j < 32; j += 2)
+          *reinterpret_cast<__half2*>(reinterpret_cast<__half*>(a.oh) + ob + c + j) =
+              __floats2half2_rn(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+      } else if (row_ok) {
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           __nv_bfloat16 h0, l0, h1, l1;

@@ -38,9 +38,13 @@ def device_weights(shape: ki.ModelShape, seed: int = 0, gain_scale: float = 0.0,
 
 
 def build_context(shape: ki.ModelShape, max_context: int, max_batch: int = 1, kv_dtype: str = "f16",
-                  seed: int = 0, gain_scale: float = 0.0, keep_host: bool = False, weights: str = None):
-    """weights="f8" / "q4": the shape's bf16 weights stored as fp8 / int4 by the library."""
+                  seed: int = 0, gain_scale: float = 0.0, keep_host: bool = False, weights: str = None,
+                  prefill_split: int = None):
+    """weights="f8" / "q4": the shape's bf16 weights stored as fp8 / int4 by the library.
+    prefill_split: K2_OPT_PREFILL_SPLIT for the context (None: the library's default)."""
     dev, host = device_weights(shape, seed=seed, gain_scale=gain_scale, keep_host=keep_host)
     cfg = k2.make_config(shape, max_context=max_context, max_batch=max_batch, kv_dtype=kv_dtype, weights=weights)
     ctx = k2.Context(cfg, dev)
+    if prefill_split is not None:
+        ctx.set_option(k2.K2_OPT_PREFILL_SPLIT, prefill_split)
     return ctx, host

@@ -171,7 +171,9 @@ def repetitive_prompt(vocab, seed):
 def test_speculative_matches_oracle_teacher_forced(k2, mio, kv, tol, agree):
     s = ki.MEDIUM
     prompt = repetitive_prompt(s.vocab, seed=40)
-    ctx, host = mio.build_context(s, max_context=160, kv_dtype=kv, gain_scale=0.1, keep_host=True)
+    # the 2e-4 bar is the split prefill's (bf16 hi + lo activations)
+    ctx, host = mio.build_context(s, max_context=160, kv_dtype=kv, gain_scale=0.1, keep_host=True,
+                                  prefill_split=1)
     nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
     ctx.prefill(0, torch.tensor(prompt, dtype=torch.int32, device="cuda"), nxt)
     seq = list(prompt) + [int(nxt.item())]

@@ -105,7 +105,9 @@ def test_gate3_incremental_equals_full_prefix_on_gpu(k2, mio):
 @pytest.mark.parametrize("kv,splits,tol", [("f16", 0, 2e-4), ("f16", 7, 2e-4), ("i8", 0, 5e-2), ("f32", 2, 2e-4)])
 def test_medium_bf16_teacher_forced(k2, mio, kv, splits, tol):
     s = ki.MEDIUM
-    ctx, host = mio.build_context(s, max_context=160, kv_dtype=kv, gain_scale=0.1, keep_host=True)
+    # the 2e-4 bar is the split prefill's (bf16 hi + lo activations)
+    ctx, host = mio.build_context(s, max_context=160, kv_dtype=kv, gain_scale=0.1, keep_host=True,
+                                  prefill_split=1)
     if splits:
         ctx.set_option(k2.K2_OPT_ATTN_SPLITS, splits)
     prompt = ki.prompt_ids(s.vocab, 70, seed=11)  # crosses a 64-key tile
@@ -250,7 +252,10 @@ def test_persistent_step_matches_kernel_chain(k2, mio, shape_name, kv):
     prompt = ki.prompt_ids(s.vocab, 37, seed=13)
     outs = []
     for persistent in (1, 0):
-        ctx, _ = mio.build_context(s, max_context=80, kv_dtype=kv)
+        # the split prefill: with single fp16 operands the order of the prefill's
+        # fp32 atomic additions, which differs run to run, can move an activation
+        # across an fp16 rounding boundary and the 1e-4 bar here is for the decode paths
+        ctx, _ = mio.build_context(s, max_context=80, kv_dtype=kv, prefill_split=1)
         ctx.set_option(k2.K2_OPT_PERSISTENT, persistent)
         if persistent:
             assert ctx.info().persistent_grid > 0

@@ -29,7 +29,7 @@ def _teacher_forced(s, host, seq, start):
     return _ORACLE[key]
 
 
-@pytest.mark.parametrize("split", [1, 0, 2])
+@pytest.mark.parametrize("split", [1, 0, 2, 3])
 def test_full_3p7b_prefill512_decode256_teacher_forced(split):
     """split = 0 (K2_OPT_PREFILL_SPLIT off): the 512-token prefill feeds the
     GEMMs single bf16 activations and the attention single fp16 queries and
@@ -38,8 +38,9 @@ def test_full_3p7b_prefill512_decode256_teacher_forced(split):
     logits relative L2 1.1e-2 over the 257 predictions and 2.1e-2 on the
     prefill's own logits -- which is why the split is the default.  The test
     keeps the measured cost of dropping it bounded (agreement >= 0.9, relative
-    L2 <= 3e-2), holds split = 1 to the bars and to 1e-3 and split = 2 (the
-    GEMMs split, the attention single) to the bars."""
+    L2 <= 3e-2), holds split = 1 to the bars and to 1e-3, and split = 2 (the
+    GEMMs split, the attention single) and split = 3 (single fp16 operands
+    throughout: fp16 copies of the weights, fp16 activations) to the bars."""
     from dense_gqa_decoder_gb300 import k2, model_io
     s = ki.K2_3P7B
     n_prompt, n_new = 512, 256
@@ -68,7 +69,9 @@ def test_full_3p7b_prefill512_decode256_teacher_forced(split):
         assert agree >= 0.99, agree
         assert rel <= 2e-2
         assert rel <= 1e-3, rel
-    elif split == 2:  # the GEMMs split, the attention's queries and probabilities single fp16
+    elif split in (2, 3):
+        # 2: the GEMMs split, the attention's queries and probabilities single
+        # fp16; 3: every prefill contraction on single fp16 operands
         assert agree >= 0.99, agree
         assert rel <= 2e-2, rel
     else:

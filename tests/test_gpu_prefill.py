@@ -32,8 +32,11 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / np.linalg.norm(b))
 
 
-def prefill(k2, ctx, prompt, vocab, tc):
+def prefill(k2, ctx, prompt, vocab, tc, split=1):
+    """split: K2_OPT_PREFILL_SPLIT; 1 (bf16 hi + lo activations) unless a test
+    asks for another mode: the 2e-4 bars of this file are that mode's."""
     ctx.set_option(k2.K2_OPT_TC_PREFILL, 1 if tc else 0)
+    ctx.set_option(k2.K2_OPT_PREFILL_SPLIT, split)
     nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
     logits = torch.empty(vocab, dtype=torch.float32, device="cuda")
     ctx.prefill(0, torch.tensor(prompt, dtype=torch.int32, device="cuda"), nxt, logits)
@@ -135,7 +138,8 @@ def test_batched_decode_matches_one_token_at_a_time_and_oracle(k2, mio, kv):
     prompts = [ki.prompt_ids(s.vocab, n, seed=60 + b) for b, n in enumerate((23, 40, 9, 71))]
     runs = {}
     for batched in (True, False):
-        ctx, host = mio.build_context(s, max_context=128, max_batch=B, kv_dtype=kv, gain_scale=0.1, keep_host=True)
+        ctx, host = mio.build_context(s, max_context=128, max_batch=B, kv_dtype=kv, gain_scale=0.1, keep_host=True,
+                                      prefill_split=1)
         ctx.set_option(k2.K2_OPT_TC_DECODE, 1 if batched else 0)
         nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
         logits = torch.empty(B * s.vocab, dtype=torch.float32, device="cuda")
@@ -214,10 +218,9 @@ def test_prefill_without_split_against_oracle(k2, mio, kv, shape, first, n):
     out = {}
     for split in (1, 0):
         ctx, host = mio.build_context(s, max_context=first + n + 8, kv_dtype=kv, gain_scale=0.1, keep_host=True)
-        ctx.set_option(k2.K2_OPT_PREFILL_SPLIT, split)
         if pre is not None:
-            prefill(k2, ctx, pre, s.vocab, True)
-        out[split] = prefill(k2, ctx, prompt, s.vocab, True)
+            prefill(k2, ctx, pre, s.vocab, True, split)
+        out[split] = prefill(k2, ctx, prompt, s.vocab, True, split)
         assert ctx.sync_status() == k2.K2_OK
     seq = prompt if pre is None else np.concatenate([pre, prompt])
     ref = O.OracleModel(s, lambda nm, l: host[(nm, l)], kv).forward_full(seq)
@@ -257,3 +260,54 @@ def test_persistent_prefill_gemm_against_per_tile_and_oracle(k2, mio, shape, fir
     assert rel_l2(l1, l0) <= 1e-4
     assert rel_l2(h1, h0) <= 1e-4
     assert t1 == t0 == O.argmax_first(ref)
+
+
+@pytest.mark.parametrize("shape,first,n", [("k2_layer", 50, 1000), ("medium", 0, 333), ("medium", 129, 2100)])
+def test_fp16_operand_prefill_against_oracle(k2, mio, shape, first, n):
+    """K2_OPT_PREFILL_SPLIT = 3: every prefill contraction on single fp16
+    operands (each weight matrix converted to fp16 per layer, fp16 activations,
+    queries and probabilities).  fp16 keeps 11 significant bits (unit roundoff
+    2^-11 = 4.9e-4); each layer rounds its four GEMM inputs and the attention's
+    queries and probabilities once, so the logits are held to 5e-3 of the
+    oracle's full recompute (10 roundoffs) and to the same argmax; the split
+    run (1) of the same prompt stays within 2e-4."""
+    s = ki.SHAPES[shape]
+    pre = ki.prompt_ids(s.vocab, first, seed=95) if first else None
+    prompt = ki.prompt_ids(s.vocab, n, seed=96)
+    out = {}
+    for split in (3, 1):
+        ctx, host = mio.build_context(s, max_context=first + n + 8, kv_dtype="f16", gain_scale=0.1, keep_host=True)
+        if pre is not None:
+            prefill(k2, ctx, pre, s.vocab, True, split)
+        out[split] = prefill(k2, ctx, prompt, s.vocab, True, split)
+        assert ctx.sync_status() == k2.K2_OK
+    seq = prompt if pre is None else np.concatenate([pre, prompt])
+    ref = O.OracleModel(s, lambda nm, l: host[(nm, l)], "f16").forward_full(seq)
+    (t3, l3), (t1, l1) = out[3], out[1]
+    r3, r1 = rel_l2(l3, ref), rel_l2(l1, ref)
+    print(f"{shape} first={first} n={n}: fp16 rel_l2={r3:.3e}, split rel_l2={r1:.3e}")
+    assert r3 <= 5e-3
+    assert r1 <= 2e-4
+    assert t3 == t1 == O.argmax_first(ref)
+
+
+def test_fp16_operand_prefill_flags_weights_beyond_fp16(k2, mio):
+    """A weight beyond fp16's range (1e5 in one W_up entry): the fp16-operand
+    prefill raises the device guard ("beyond-fp16-range") instead of running on
+    an infinity; the split prefill of the same model does not."""
+    s = ki.MEDIUM
+    prompt = ki.prompt_ids(s.vocab, 100, seed=97)
+    for split in (3, 1):
+        dev, _ = mio.device_weights(s, gain_scale=0.1)
+        dev["w_up"][0][0, 0] = 1.0e5
+        ctx = k2.Context(k2.make_config(s, max_context=128, kv_dtype="f16"), dev)
+        ctx.set_option(k2.K2_OPT_PREFILL_SPLIT, split)
+        nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ctx.prefill(0, torch.tensor(prompt, dtype=torch.int32, device="cuda"), nxt)
+        torch.cuda.synchronize()
+        st = ctx.sync_status()
+        if split == 3:
+            assert st == k2.K2_ERR_DEVICE_GUARD
+            assert "beyond-fp16-range" in ctx.last_error()
+        else:
+            assert st == k2.K2_OK

@@ -50,7 +50,7 @@ def test_ragged_reduction_lengths_match_the_oracle(k2, mio, weights, shape):
     over the same (quantized) weights."""
     s = RAGGED if shape == "ragged" else ODD
     ctx, host = mio.build_context(s, max_context=64, kv_dtype="f16", gain_scale=0.1, keep_host=True,
-                                  weights=None if weights == "bf16" else weights)
+                                  weights=None if weights == "bf16" else weights, prefill_split=1)
     assert ctx.info().persistent_grid > 0
     prompt = ki.prompt_ids(s.vocab, 20, seed=95)
     nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
