@@ -301,6 +301,9 @@ struct k2_ctx {
   std::array<std::array<uint8_t, kTcMapBytes>, 4> tm_w16{};  // bf16 weights: one layer's fp16 copy
   // the same activation buffers in 16-token tiles (batched decode)
   std::array<uint8_t, kTcMapBytes> tb_xh{}, tb_xl{}, tb_oh{}, tb_ol{}, tb_ah{}, tb_al{};
+  // and in 256-token tiles (fp16-operand prefill of long blocks: single activations)
+  std::array<uint8_t, kTcMapBytes> tw_xh{}, tw_oh{}, tw_ah{};
+  bool tw_ok = false;
   // fp16 caches: the tensor maps of each layer's K and V for the tensor-core decode attention
   std::vector<std::array<uint8_t, kTcMapBytes>> tm_k, tm_v;
   std::map<std::tuple<int, const void*, const void*, const void*, void*>, cudaGraphExec_t> graphs;
@@ -802,6 +805,9 @@ cudaError_t plan_tc_prefill(k2_ctx* c) {
       if (!tc_encode_weight(c->tm_w16[m].data(), c->ws + c->lay.w16[m], Ns[m], Ks[m])) return cudaSuccess;
   }
   const int P = c->lay.pchunk;
+  c->tw_ok = P > 512 && tc_encode_act(c->tw_xh.data(), c->ws + c->lay.pxh, P, s.H, 256) &&
+             tc_encode_act(c->tw_oh.data(), c->ws + c->lay.pxh, P, s.nq * s.d, 256) &&
+             tc_encode_act(c->tw_ah.data(), c->ws + c->lay.pah, P, s.I, 256);
   bool ok = true;
   for (int tt : {128, 16}) {
     ok = ok && tc_encode_act((tt == 128 ? c->tm_xh : c->tb_xh).data(), c->ws + c->lay.pxh, P, s.H, tt) &&
@@ -852,6 +858,9 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   // activations enter as single fp16; elsewhere 3 acts as 1
   const bool f16 = c->pf_split == 3 && c->cfg.weight_dtype == K2_BF16 && !small && c->pf_tc && c->use_pf_tc;
   const int mode = f16 ? 3 : c->pf_split == 3 ? 1 : c->pf_split;
+  // long fp16 blocks: 256-token tiles (each SM receives 1.5x the bytes of a
+  // 128-token tile per K step for twice its MMAs)
+  const bool wide = f16 && n > 512 && c->pf_whole && c->tw_ok;
   auto wmap = [&](int l, int m) -> const void* { return f16 ? c->tm_w16[m].data() : c->tmw[4 * l + m].data(); };
   const void* wlo = nullptr;
   auto dequant = [&](int l, int m) {
@@ -881,7 +890,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.ksteps = 4 * ((K + 255) / 256);
     g.mode = mode;
     g.ldo = ldo;
-    g.tile_tokens = 128;
+    g.tile_tokens = wide ? 256 : 128;
     g.splits = 1;
     g.out = out;
     g.out_hi = oh;
@@ -903,7 +912,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.ksteps = 4 * ((K + 255) / 256);
     g.mode = mode;
     g.ldo = ldo;
-    g.tile_tokens = tt;
+    g.tile_tokens = wide ? 256 : tt;
     g.splits = 1;
     g.out = out;
     g.guard = c->guard;
@@ -919,11 +928,11 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   // int4: the low-half weight MMA needs the activations' halves
   const bool split = !f16 && (small || mode != 0 || q4);
   const bool attn_split = small || mode == 1;  // 2, 3: the attention's Q and P single
-  const void* m_xh = small ? c->tb_xh.data() : c->tm_xh.data();
+  const void* m_xh = small ? c->tb_xh.data() : wide ? c->tw_xh.data() : c->tm_xh.data();
   const void* m_xl = small ? c->tb_xl.data() : split ? c->tm_xl.data() : nullptr;
-  const void* m_oh = small ? c->tb_oh.data() : c->tm_oh.data();
+  const void* m_oh = small ? c->tb_oh.data() : wide ? c->tw_oh.data() : c->tm_oh.data();
   const void* m_ol = small ? c->tb_ol.data() : split ? c->tm_ol.data() : nullptr;
-  const void* m_ah = small ? c->tb_ah.data() : c->tm_ah.data();
+  const void* m_ah = small ? c->tb_ah.data() : wide ? c->tw_ah.data() : c->tm_ah.data();
   const void* m_al = small ? c->tb_al.data() : split ? c->tm_al.data() : nullptr;
   cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.gb, X, s.H, s.V, c->guard,
                                     c->hist + static_cast<size_t>(seq) * c->lay.cap, 0, nullptr, pos0, d_pos0, st);

@@ -447,47 +447,57 @@ __global__ void __launch_bounds__(192, 1) tc_gemm_sk_kernel(const __grid_constan
         break;
       }
       tc_after();
-      uint32_t v[BN];
-      if constexpr (BN == 16) {
-        tmem_ld16(tmem + b * COLS + (static_cast<uint32_t>(lg) << 16), v);
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN; c += 32) tmem_ld32(tmem + b * COLS + (static_cast<uint32_t>(lg) << 16) + c, v + c);
-      }
-      tc_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce[b]);
       const int rt = tile / tok_tiles;
       const int row = rt * BM + lg + lane;
-      const int n0 = (tile - rt * tok_tiles) * BN;
+      const int n0t = (tile - rt * tok_tiles) * BN;
       const float rs = (a.row_scale != nullptr && row < a.N) ? __ldg(a.row_scale + row) : 1.f;
-      if (!a.whole) {
-        if (row < a.N) {
+      // the accumulator in parts of at most 128 columns (registers); the
+      // buffer is released once its last part is in registers
+      constexpr int PART = BN > 128 ? 128 : BN;
+#pragma unroll 1
+      for (int p0 = 0; p0 < BN; p0 += PART) {
+        uint32_t v[PART];
+        if constexpr (PART == 16) {
+          tmem_ld16(tmem + b * COLS + (static_cast<uint32_t>(lg) << 16) + p0, v);
+        } else {
 #pragma unroll
-          for (int j = 0; j < BN; ++j)
-            if (n0 + j < a.T) atomicAdd(a.out + static_cast<size_t>(n0 + j) * a.ldo + row, __uint_as_float(v[j]) * rs);
+          for (int c = 0; c < PART; c += 32)
+            tmem_ld32(tmem + b * COLS + (static_cast<uint32_t>(lg) << 16) + p0 + c, v + c);
         }
-      } else if (a.mode == TC_SWIGLU) {
-        // rows (2p, 2p+1) = (gate_p, up_p) sit in adjacent lanes; per pair of
-        // columns (j, j+1) the even lane finishes column j and the odd lane
-        // column j+1, each after one exchange
-        const bool odd = lane & 1;
-#pragma unroll
-        for (int j = 0; j < BN; j += 2) {
-          const float a0 = __uint_as_float(v[j]) * rs, a1 = __uint_as_float(v[j + 1]) * rs;
-          const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
-          const float g = odd ? recv : a0, u = odd ? a1 : recv;
-          const int t = n0 + j + (odd ? 1 : 0);
-          if (t < a.T && row < a.N) swiglu_store(a, static_cast<size_t>(t) * a.ldo + (row >> 1), g, u);
+        if (p0 + PART == BN) {
+          tc_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce[b]);
         }
-      } else if (row < a.N) {
+        const int n0 = n0t + p0;
+        if (!a.whole) {
+          if (row < a.N) {
 #pragma unroll
-        for (int j = 0; j < BN; ++j) {
-          if (n0 + j < a.T) {
-            float* o = a.out + static_cast<size_t>(n0 + j) * a.ldo + row;
-            const float y = __uint_as_float(v[j]) * rs;
-            if (a.mode == TC_RESID) *o += y;
-            else *o = y;
+            for (int j = 0; j < PART; ++j)
+              if (n0 + j < a.T) atomicAdd(a.out + static_cast<size_t>(n0 + j) * a.ldo + row, __uint_as_float(v[j]) * rs);
+          }
+        } else if (a.mode == TC_SWIGLU) {
+          // rows (2p, 2p+1) = (gate_p, up_p) sit in adjacent lanes; per pair of
+          // columns (j, j+1) the even lane finishes column j and the odd lane
+          // column j+1, each after one exchange
+          const bool odd = lane & 1;
+#pragma unroll
+          for (int j = 0; j < PART; j += 2) {
+            const float a0 = __uint_as_float(v[j]) * rs, a1 = __uint_as_float(v[j + 1]) * rs;
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
+            const float g = odd ? recv : a0, u = odd ? a1 : recv;
+            const int t = n0 + j + (odd ? 1 : 0);
+            if (t < a.T && row < a.N) swiglu_store(a, static_cast<size_t>(t) * a.ldo + (row >> 1), g, u);
+          }
+        } else if (row < a.N) {
+#pragma unroll
+          for (int j = 0; j < PART; ++j) {
+            if (n0 + j < a.T) {
+              float* o = a.out + static_cast<size_t>(n0 + j) * a.ldo + row;
+              const float y = __uint_as_float(v[j]) * rs;
+              if (a.mode == TC_RESID) *o += y;
+              else *o = y;
+            }
           }
         }
       }
@@ -943,7 +953,7 @@ bool tc_encode_weight(void* map, const void* packed, int N, int K) {
 
 bool tc_encode_act(void* map, const void* buf, int rows, int K, int tile_tokens) {
   EncodeTiled enc = encode_fn();
-  if (!enc || K % 8 != 0 || (tile_tokens != 16 && tile_tokens != 128)) return false;
+  if (!enc || K % 8 != 0 || (tile_tokens != 16 && tile_tokens != 128 && tile_tokens != 256)) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
   cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(tile_tokens)}, es[2] = {1, 1};
@@ -1026,18 +1036,19 @@ cudaError_t tc_gemm_init_attrs() {
   if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, true, 1>, Tile<128, true, true, 1>::SMEM_BYTES);
   if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, false, 2>, Tile<128, true, false, 2>::SMEM_BYTES);
   if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, false, false, 2>, Tile<128, false, false, 2>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<256, false, false, 2>, Tile<256, false, false, 2>::SMEM_BYTES);
   return e;
 }
 
 cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* mapXh, const void* mapXl,
                               const TcGemmArgs& a, int ctas, cudaStream_t s, bool pdl) {
   if (a.T <= 0) return cudaSuccess;
-  if ((a.tile_tokens != 16 && a.tile_tokens != 128) || (a.mode == TC_SWIGLU && !a.whole) || ctas < 1 ||
-      a.ksteps % 4 != 0)
+  if ((a.tile_tokens != 16 && a.tile_tokens != 128 && a.tile_tokens != 256) || (a.mode == TC_SWIGLU && !a.whole) ||
+      ctas < 1 || a.ksteps % 4 != 0)
     return cudaErrorInvalidValue;
   const int tt = a.tile_tokens;
   const bool lo = mapXl != nullptr, wl = mapWl != nullptr;
-  if ((tt == 16 && (!lo || wl)) || (wl && !lo)) return cudaErrorInvalidValue;
+  if ((tt == 16 && (!lo || wl)) || (wl && !lo) || (tt == 256 && (lo || wl))) return cudaErrorInvalidValue;
   // 128-token tiles fill each ring stage with two K steps (larger copy groups: measured on the
   // 4096-token prefill, 85.0 -> 80.2 ms with the stream-K o_proj / down so too) where two fit twice
   const bool two = tt == 128 && !wl;
@@ -1050,8 +1061,9 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* m
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = tt == 16 ? Tile<16, true, false, 1>::SMEM_BYTES
-                         : wl     ? Tile<128, true, true, 1>::SMEM_BYTES
+  cfg.dynamicSmemBytes = tt == 16    ? Tile<16, true, false, 1>::SMEM_BYTES
+                         : tt == 256 ? Tile<256, false, false, 2>::SMEM_BYTES
+                         : wl        ? Tile<128, true, true, 1>::SMEM_BYTES
                          : two    ? (lo ? Tile<128, true, false, 2>::SMEM_BYTES : Tile<128, false, false, 2>::SMEM_BYTES)
                          : lo     ? Tile<128, true, false, 1>::SMEM_BYTES
                                   : Tile<128, false, false, 1>::SMEM_BYTES;
@@ -1062,6 +1074,7 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* m
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   if (tt == 16) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<16, true, false, 1>, w, wlo, xh, xl, a);
+  if (tt == 256) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<256, false, false, 2>, w, wlo, xh, xl, a);
   if (wl) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true, true, 1>, w, wlo, xh, xl, a);
   if (two && lo) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true, false, 2>, w, wlo, xh, xl, a);
   if (two) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, false, false, 2>, w, wlo, xh, xl, a);
