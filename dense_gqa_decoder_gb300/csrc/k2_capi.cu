@@ -45,7 +45,7 @@ struct Layout {
   size_t sqkv, so, sgu, sdown, slm;                // fp8 weights: per-row scales (first layer)
   size_t sqkv_layer, so_layer, sgu_layer, sdown_layer;
   size_t dq[4], dq_bytes[4];  // int4 prefill: matrix m of the current layer, bf16 hi then lo
-  size_t w16[4];              // bf16 weights, fp16 prefill: matrix m of the current layer as fp16
+  size_t w16[2][4];           // bf16 weights, fp16 prefill: matrix m of layers of parity 0 / 1 as fp16
   size_t vlog, vids, varg, vpv, vpi;               // speculative verification: logits, ids, argmax
   // tensor-core prefill of up to `pchunk` tokens at a time (bf16 weights)
   int pchunk;
@@ -182,11 +182,13 @@ Layout layout_of(const k2_config& c) {
     l.tgu = take(l.tgu_layer * s.L);
     l.tdown = take(l.tdown_layer * s.L);
   }
-  if (c.weight_dtype == K2_BF16 && l.pchunk > 0) {  // one layer's weights as fp16, rebuilt per layer
-    l.w16[0] = take(l.wqkv_layer);
-    l.w16[1] = take(l.wo_layer);
-    l.w16[2] = take(l.wgu_layer);
-    l.w16[3] = take(l.wdown_layer);
+  if (c.weight_dtype == K2_BF16 && l.pchunk > 0) {  // two layers' weights as fp16, rebuilt per layer
+    for (int b = 0; b < 2; ++b) {
+      l.w16[b][0] = take(l.wqkv_layer);
+      l.w16[b][1] = take(l.wo_layer);
+      l.w16[b][2] = take(l.wgu_layer);
+      l.w16[b][3] = take(l.wdown_layer);
+    }
   }
   if (c.weight_dtype == K2_Q4 && l.pchunk > 0) {  // one layer's weights as bf16 hi / lo, rebuilt per layer
     const int Ns[4] = {s.qkv_n, s.H, 2 * s.I, s.H}, Ks[4] = {s.H, s.nq * s.d, s.H, s.I};
@@ -298,7 +300,17 @@ struct k2_ctx {
   std::vector<std::array<uint8_t, kTcMapBytes>> tmw;  // 4 per layer
   std::array<uint8_t, kTcMapBytes> tm_xh{}, tm_xl{}, tm_oh{}, tm_ol{}, tm_ah{}, tm_al{}, tm_lm{};
   std::array<std::array<uint8_t, kTcMapBytes>, 4> tm_wlo{};  // int4: the weights' low halves
-  std::array<std::array<uint8_t, kTcMapBytes>, 4> tm_w16{};  // bf16 weights: one layer's fp16 copy
+  // bf16 weights, fp16-operand prefill: the fp16 copies of layers of parity 0 / 1, converted on a
+  // second stream while the previous layer computes (events: copy b ready, copy b read)
+  std::array<std::array<std::array<uint8_t, kTcMapBytes>, 4>, 2> tm_w16{};
+  bool w16_ok = false;
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_conv[2] = {}, ev_used[2] = {};
+  ~k2_ctx() {
+    if (side) cudaStreamDestroy(side);
+    for (cudaEvent_t ev : {ev_fork, ev_join, ev_conv[0], ev_conv[1], ev_used[0], ev_used[1]})
+      if (ev) cudaEventDestroy(ev);
+  }
   // the same activation buffers in 16-token tiles (batched decode)
   std::array<uint8_t, kTcMapBytes> tb_xh{}, tb_xl{}, tb_oh{}, tb_ol{}, tb_ah{}, tb_al{};
   // and in 256-token tiles (fp16-operand prefill of long blocks: single activations)
@@ -801,8 +813,14 @@ cudaError_t plan_tc_prefill(k2_ctx* c) {
   }
   if (c->cfg.weight_dtype == K2_BF16) {  // the tensor maps copy bytes: a bf16 map reads the fp16 copy as well
     const int Ns[4] = {s.qkv_n, s.H, 2 * s.I, s.H}, Ks[4] = {s.H, s.nq * s.d, s.H, s.I};
-    for (int m = 0; m < 4; ++m)
-      if (!tc_encode_weight(c->tm_w16[m].data(), c->ws + c->lay.w16[m], Ns[m], Ks[m])) return cudaSuccess;
+    bool ok = true;
+    for (int b = 0; b < 2; ++b)
+      for (int m = 0; m < 4; ++m)
+        ok = ok && tc_encode_weight(c->tm_w16[b][m].data(), c->ws + c->lay.w16[b][m], Ns[m], Ks[m]);
+    ok = ok && cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t* ev : {&c->ev_fork, &c->ev_join, &c->ev_conv[0], &c->ev_conv[1], &c->ev_used[0], &c->ev_used[1]})
+      ok = ok && cudaEventCreateWithFlags(ev, cudaEventDisableTiming) == cudaSuccess;
+    c->w16_ok = ok;
   }
   const int P = c->lay.pchunk;
   c->tw_ok = P > 512 && tc_encode_act(c->tw_xh.data(), c->ws + c->lay.pxh, P, s.H, 256) &&
@@ -856,21 +874,29 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   // the tcgen05 attention, blocks over 16 tokens): each matrix of the layer is
   // converted to fp16 (exact in fp16's normal range) before its GEMM, and the
   // activations enter as single fp16; elsewhere 3 acts as 1
-  const bool f16 = c->pf_split == 3 && c->cfg.weight_dtype == K2_BF16 && !small && c->pf_tc && c->use_pf_tc;
+  const bool f16 =
+      c->pf_split == 3 && c->cfg.weight_dtype == K2_BF16 && !small && c->pf_tc && c->use_pf_tc && c->w16_ok;
   const int mode = f16 ? 3 : c->pf_split == 3 ? 1 : c->pf_split;
   // long fp16 blocks: 256-token tiles (each SM receives 1.5x the bytes of a
   // 128-token tile per K step for twice its MMAs)
   const bool wide = f16 && n > 512 && c->pf_whole && c->tw_ok;
-  auto wmap = [&](int l, int m) -> const void* { return f16 ? c->tm_w16[m].data() : c->tmw[4 * l + m].data(); };
+  auto wmap = [&](int l, int m) -> const void* {
+    return f16 ? c->tm_w16[l & 1][m].data() : c->tmw[4 * l + m].data();
+  };
+  // fp16: layer l's four matrices into copy l & 1 on the second stream
+  auto convert_layer = [&](int l) {
+    const void* srcs[4] = {c->wqkv(l), c->wop(l), c->wgu(l), c->wdown(l)};
+    const int Ns[4] = {s.qkv_n, s.H, 2 * s.I, s.H}, Ks[4] = {s.H, s.nq * s.d, s.H, s.I};
+    cudaError_t e = cudaSuccess;
+    for (int m = 0; m < 4 && !e; ++m)
+      e = launch_bf16_to_f16(reinterpret_cast<__half*>(c->ws + c->lay.w16[l & 1][m]),
+                             static_cast<const __nv_bfloat16*>(srcs[m]), packed_bytes(Ns[m], Ks[m], 2) / 2, c->guard,
+                             c->side);
+    return e ? e : cudaEventRecord(c->ev_conv[l & 1], c->side);
+  };
   const void* wlo = nullptr;
   auto dequant = [&](int l, int m) {
-    if (f16) {
-      const void* srcs[4] = {c->wqkv(l), c->wop(l), c->wgu(l), c->wdown(l)};
-      const int Ns[4] = {s.qkv_n, s.H, 2 * s.I, s.H}, Ks[4] = {s.H, s.nq * s.d, s.H, s.I};
-      return launch_bf16_to_f16(reinterpret_cast<__half*>(c->ws + c->lay.w16[m]),
-                                static_cast<const __nv_bfloat16*>(srcs[m]), packed_bytes(Ns[m], Ks[m], 2) / 2,
-                                c->guard, st);
-    }
+    if (f16) return cudaSuccess;  // converted ahead on the second stream
     if (!q4) {
       wlo = nullptr;
       return cudaSuccess;
@@ -936,7 +962,15 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
   const void* m_al = small ? c->tb_al.data() : split ? c->tm_al.data() : nullptr;
   cudaError_t e = launch_embed_rows(d_tokens, n, c->embed, s.gb, X, s.H, s.V, c->guard,
                                     c->hist + static_cast<size_t>(seq) * c->lay.cap, 0, nullptr, pos0, d_pos0, st);
+  if (f16 && !e) {
+    // the second stream starts after the work already on st (an earlier
+    // prefill may still read the copies) and converts the first two layers
+    e = cudaEventRecord(c->ev_fork, st);
+    if (!e) e = cudaStreamWaitEvent(c->side, c->ev_fork, 0);
+    for (int l = 0; l < std::min(2, s.L) && !e; ++l) e = convert_layer(l);
+  }
   for (int l = 0; l < s.L && !e; ++l) {
+    if (f16 && !e) e = cudaStreamWaitEvent(st, c->ev_conv[l & 1], 0);
     if (!e)
       e = launch_norm_rows(X, n, c->attn_norm[l], s.gb, xh, xl, s.H, s.G, c->cfg.eps, st, false, nullptr, 0, nullptr,
                            f16, c->guard);
@@ -1006,6 +1040,16 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     }
     if (!e) e = dequant(l, 3);
     if (!e) e = gemm_sk(wmap(l, 3), c->tcs(l, 3), m_ah, m_al, s.H, s.I, TC_RESID, X, s.H);
+    if (f16 && !e && l + 2 < s.L) {  // copy l & 1 is free once layer l's GEMMs have run: layer l + 2 goes there
+      e = cudaEventRecord(c->ev_used[l & 1], st);
+      if (!e) e = cudaStreamWaitEvent(c->side, c->ev_used[l & 1], 0);
+      if (!e) e = convert_layer(l + 2);
+    }
+  }
+  if (f16) {  // st waits for everything issued on the second stream (a failed call included)
+    cudaError_t j = cudaEventRecord(c->ev_join, c->side);
+    if (!j) j = cudaStreamWaitEvent(st, c->ev_join, 0);
+    if (!e) e = j;
   }
   return e;
 }

@@ -47,8 +47,8 @@ def test_workspace_bytes_valid_and_invalid(k2):
     # fp32 QKV output and rotated queries
     P = 2048
     prefill = P * (2560 * 4 + 2 * 4096 * 2 + 2 * 10240 * 2 + 6144 * 4 + 4096 * 4)
-    # and one layer's projections as fp16 (the fp16-operand prefill converts a layer at a time)
-    prefill += (6144 * 2560 + 2560 * 4096 + 20480 * 2560 + 2560 * 10240) * 2
+    # and two layers' projections as fp16 (the fp16-operand prefill converts a layer ahead)
+    prefill += 2 * (6144 * 2560 + 2560 * 4096 + 20480 * 2560 + 2560 * 10240) * 2
     assert packed + kv + prefill < n < packed + kv + prefill + 64 * 2 ** 20
     for bad in (dict(head_dim=96), dict(n_heads=30), dict(hidden=2561), dict(norm_groups=0),
                 dict(vocab=0), dict(head_dim=127)):
