@@ -46,13 +46,29 @@ __global__ void embed_rows_kernel(const int* __restrict__ tokens, const WT* __re
   for (int i = threadIdx.x; i < H; i += blockDim.x) X[static_cast<size_t>(t) * H + i] = to_f32(e[i]);
 }
 
-// GroupedRMSNorm of one row (k2-burn README, "Model shape": layernorm groups),
-// written as bf16 hi/lo, or (f16) as single fp16 into oh
+// GroupedRMSNorm of one row per CTA (k2-burn README, "Model shape": layernorm
+// groups), written as bf16 hi/lo, or (f16) as single fp16 into oh.  H is a
+// multiple of 4 (every caller's activations are tensor-map rows: a multiple of
+// 8); the launch gives each thread one float4 of the row where H <= 4096.
 template <typename WT>
-__global__ void norm_rows_kernel(const float* __restrict__ X, const WT* __restrict__ gain, __nv_bfloat16* __restrict__ oh,
-                                 __nv_bfloat16* __restrict__ ol, int H, int groups, float eps, int rows,
-                                 float4* __restrict__ zero, size_t zero_n4, float* __restrict__ copy, int f16,
-                                 unsigned* __restrict__ guard) {
+__device__ __forceinline__ float4 load4_gain(const WT* g, int i);
+template <>
+__device__ __forceinline__ float4 load4_gain<__nv_bfloat16>(const __nv_bfloat16* g, int i) {
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(g + i));
+  return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y << 16),
+                     __uint_as_float(v.y & 0xFFFF0000u));
+}
+template <>
+__device__ __forceinline__ float4 load4_gain<float>(const float* g, int i) {
+  return __ldg(reinterpret_cast<const float4*>(g + i));
+}
+
+template <typename WT>
+__global__ void __launch_bounds__(1024)
+    norm_rows_kernel(const float* __restrict__ X, const WT* __restrict__ gain, __nv_bfloat16* __restrict__ oh,
+                     __nv_bfloat16* __restrict__ ol, int H, int groups, float eps, int rows,
+                     float4* __restrict__ zero, size_t zero_n4, float* __restrict__ copy, int f16,
+                     unsigned* __restrict__ guard) {
   __shared__ float part[32][4];
   __shared__ float rs[4];
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -67,12 +83,16 @@ __global__ void norm_rows_kernel(const float* __restrict__ X, const WT* __restri
   const float* x = X + static_cast<size_t>(t) * H;
   const int gsz = H / groups;
   float ss[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int i = tid; i < H; i += blockDim.x) {
-    const float v = x[i];
-    const int g = i / gsz;
+  for (int i = tid * 4; i < H; i += blockDim.x * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(x + i);
+    const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (q == g) ss[q] += v * v;
+    for (int j = 0; j < 4; ++j) {
+      const int g = (i + j) / gsz;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q == g) ss[q] += e[j] * e[j];
+    }
   }
 #pragma unroll
   for (int q = 0; q < 4; ++q) ss[q] = warp_sum(ss[q]);
@@ -80,24 +100,38 @@ __global__ void norm_rows_kernel(const float* __restrict__ X, const WT* __restri
     for (int q = 0; q < 4; ++q) part[warp][q] = ss[q];
   __syncthreads();
   if (tid < groups) {
-    float s = 0.f;
-    for (int w = 0; w < static_cast<int>(blockDim.x / 32); ++w) s += part[w][tid];
-    rs[tid] = 1.0f / sqrtf(s / static_cast<float>(gsz) + eps);
+    float sum = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x / 32); ++w) sum += part[w][tid];
+    rs[tid] = 1.0f / sqrtf(sum / static_cast<float>(gsz) + eps);
   }
   __syncthreads();
   bool range = false;
-  for (int i = tid; i < H; i += blockDim.x) {
-    const float y = x[i] * rs[i / gsz] * to_f32(gain[i]);
+  for (int i = tid * 4; i < H; i += blockDim.x * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(x + i);  // the same thread's load above: an L1 hit
+    const float4 gn = load4_gain<WT>(gain, i);
+    const float e[4] = {v.x, v.y, v.z, v.w}, gg[4] = {gn.x, gn.y, gn.z, gn.w};
+    float y[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) y[j] = e[j] * rs[(i + j) / gsz] * gg[j];
+    const size_t o = static_cast<size_t>(t) * H + i;
     if (f16) {
-      range |= !(fabsf(y) <= 65504.f);
-      reinterpret_cast<__half*>(oh)[static_cast<size_t>(t) * H + i] = __float2half_rn(y);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) range |= !(fabsf(y[j]) <= 65504.f);
+      const __half2 a = __floats2half2_rn(y[0], y[1]), b = __floats2half2_rn(y[2], y[3]);
+      uint2 w;
+      w.x = *reinterpret_cast<const uint32_t*>(&a);
+      w.y = *reinterpret_cast<const uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(oh) + o) = w;
     } else {
-      __nv_bfloat16 hi, lo;
-      split_bf16(y, hi, lo);
-      oh[static_cast<size_t>(t) * H + i] = hi;
-      ol[static_cast<size_t>(t) * H + i] = lo;
+      __nv_bfloat16 hi[4], lo[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) split_bf16(y[j], hi[j], lo[j]);
+      *reinterpret_cast<__nv_bfloat162*>(oh + o) = __nv_bfloat162(hi[0], hi[1]);
+      *reinterpret_cast<__nv_bfloat162*>(oh + o + 2) = __nv_bfloat162(hi[2], hi[3]);
+      *reinterpret_cast<__nv_bfloat162*>(ol + o) = __nv_bfloat162(lo[0], lo[1]);
+      *reinterpret_cast<__nv_bfloat162*>(ol + o + 2) = __nv_bfloat162(lo[2], lo[3]);
     }
-    if (copy) copy[static_cast<size_t>(t) * H + i] = x[i];
+    if (copy) *reinterpret_cast<float4*>(copy + o) = v;
   }
   if (range && guard != nullptr) atomicOr(guard, GUARD_RANGE);
 }
@@ -704,15 +738,19 @@ cudaError_t launch_bf16_to_f16(__half* dst, const __nv_bfloat16* src, size_t n, 
 cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes, __nv_bfloat16* oh,
                              __nv_bfloat16* ol, int H, int groups, float eps, cudaStream_t s, bool pdl, float* zero,
                              size_t zero_floats, float* copy, bool f16, unsigned* guard) {
-  if (zero_floats % 4 || (zero_floats && reinterpret_cast<uintptr_t>(zero) % 16)) return cudaErrorInvalidValue;
+  if (zero_floats % 4 || (zero_floats && reinterpret_cast<uintptr_t>(zero) % 16) || H % 4 || groups < 1 || groups > 4)
+    return cudaErrorInvalidValue;
   const size_t n4 = zero_floats / 4;
   // extra CTAs (up to one per 8192 float4s, at most 64) clear the next GEMM's output
   const int zc = n4 ? static_cast<int>(std::min<size_t>(64, (n4 + 8191) / 8192)) : 0;
+  // one float4 per thread (H <= 4096), in whole warps
+  const int threads = std::min(1024, std::max(32, (H / 4 + 31) / 32 * 32));
   if (wbytes == 2)
-    return launch_k(norm_rows_kernel<__nv_bfloat16>, dim3(n + zc), dim3(512), 0, s, pdl, X,
+    return launch_k(norm_rows_kernel<__nv_bfloat16>, dim3(n + zc), dim3(threads), 0, s, pdl, X,
                     static_cast<const __nv_bfloat16*>(gain), oh, ol, H, groups, eps, n,
                     reinterpret_cast<float4*>(zero), n4, copy, f16 ? 1 : 0, guard);
-  return launch_k(norm_rows_kernel<float>, dim3(n + zc), dim3(512), 0, s, pdl, X, static_cast<const float*>(gain), oh,
+  return launch_k(norm_rows_kernel<float>, dim3(n + zc), dim3(threads), 0, s, pdl, X,
+                  static_cast<const float*>(gain), oh,
                   ol, H, groups, eps, n, reinterpret_cast<float4*>(zero), n4, copy, f16 ? 1 : 0, guard);
 }
 
