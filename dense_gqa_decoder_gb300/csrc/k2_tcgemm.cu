@@ -545,21 +545,30 @@ EncodeTiled encode_fn() {
 //               memory, and write their halves of P = exp(s - m) as fp16 hi + lo
 //               (SPLIT = false: fp16 P alone);
 //   O += P.V^T  (tcgen05.mma M=128 N=D, O in TMEM).
-// Every operand is K-major with the 128-byte swizzle (the layout of the GEMMs'
-// descriptors): Q and P are written so by the threads, K arrives so by TMA, and
-// V (TMA rows [key][dim]) is transposed into [dim][key] with ldmatrix.trans /
-// stmatrix.  The tensor pipe never waits for the softmax: S of the next tile is
-// issued (into the other of two S buffers) before this tile's softmax, and P,
-// V^T are double-buffered, so P.V of one tile overlaps the next one's softmax.
+// Q, K and P are K-major with the 128-byte swizzle (the layout of the GEMMs'
+// descriptors): Q and P are written so by the threads, K arrives so by TMA; V
+// enters P.V as it arrives, [key][dim] rows, through an MN-major descriptor
+// (dims contiguous: 64-dim swizzle atoms LBO apart, 8-key groups SBO apart).
+// The tensor pipe never waits for the softmax: S of the next tile is issued
+// (into the other of two S buffers) before this tile's softmax, and P is
+// double-buffered, so P.V of one tile overlaps the next one's softmax.  Scores
+// are kept in base 2 (Q carries log2(e)), so p = 2^(s - m) is one ex2 each.
 // A row's reference maximum only moves when a tile's maximum exceeds it by
-// more than kRescaleLog (then O and the row's sums are rescaled in TMEM);
-// otherwise p = exp(s - m) may exceed 1 (at most e^kRescaleLog, well inside
-// fp16), and the final division by the sum makes the result exact anyway.
-// K/V tiles are double-buffered: the tile after next is requested as soon as a
-// stage is consumed.
+// more than kRescaleLog2 (then O and the row's sums are rescaled in TMEM);
+// otherwise p may exceed 1 (at most 2^kRescaleLog2, well inside fp16), and the
+// final division by the sum makes the result exact anyway.  K/V tiles rotate
+// through three stages: the next tile is requested once the P.V that read the
+// stage it reuses is done.
 // 8 softmax warps (two per TMEM lane group) and one issuer warp
 constexpr int kPaRows = 128, kPaKeys = 64, kPaSoftWarps = 8, kPaThreads = 32 * (kPaSoftWarps + 1);
-constexpr float kRescaleLog = 8.0f;
+constexpr int kPaStages = 3;
+constexpr float kRescaleLog2 = 11.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float ex2(float x) {  // 2^x (the SFU's approximation; 2^-inf = 0)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 template <int D>
 struct PaSmem {
@@ -567,23 +576,31 @@ struct PaSmem {
   static constexpr int Q = kPaRows * 128;             // one atom of the 128 query rows (16 KB)
   static constexpr int KT = kPaKeys * 128;            // one atom of a 64-key K (or V) tile (8 KB)
   static constexpr int STAGE = 2 * NA * KT;           // K and V of one tile
-  static constexpr int VT = D * 128;                  // V^T [D][64 keys]
   static constexpr int P = kPaRows * 128;             // P [128][64 keys] (one half)
   static constexpr int OFF_QH = 0, OFF_QL = OFF_QH + NA * Q;
-  static constexpr int OFF_ST = OFF_QL + NA * Q;      // two stages
-  static constexpr int OFF_VT = OFF_ST + 2 * STAGE;   // two V^T buffers
-  static constexpr int OFF_P = OFF_VT + 2 * VT;       // two buffers of P hi, P lo
+  static constexpr int OFF_ST = OFF_QL + NA * Q;      // kPaStages stages
+  static constexpr int OFF_P = OFF_ST + kPaStages * STAGE;  // two buffers of P hi, P lo
   static constexpr int BYTES = OFF_P + 4 * P;
   static constexpr int DYN = BYTES + 1024;            // + alignment to 1024 B
   static constexpr int TMEM_COLS = D + 128 <= 128 ? 128 : 256;  // O [D], then S [64] x 2
-  // instruction descriptors (kind::f16): fp16 A and B, fp32 D, K-major, M = 128
+  // instruction descriptors (kind::f16): fp16 A and B, fp32 D, M = 128; S: both K-major;
+  // O: B (V) MN-major (bit 16)
   static constexpr uint32_t IDESC_S = (1u << 4) | (static_cast<uint32_t>(kPaKeys >> 3) << 17) | (8u << 24);
-  static constexpr uint32_t IDESC_O = (1u << 4) | (static_cast<uint32_t>(D >> 3) << 17) | (8u << 24);
+  static constexpr uint32_t IDESC_O =
+      (1u << 4) | (1u << 16) | (static_cast<uint32_t>(D >> 3) << 17) | (8u << 24);
 };
 
 // byte offset of element (row r, column e) in a K-major 128-byte-swizzled block of 64 columns
 __device__ __forceinline__ uint32_t sw128(int r, int e) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((((e >> 3) ^ (r & 7)) & 7) << 4) + (e & 7) * 2);
+}
+// shared-memory matrix descriptor, MN-major with the 128-byte swizzle: rows of
+// 128 bytes along K (8-row groups sbo bytes apart), 64-element atoms along MN
+// lbo bytes apart
+__device__ __forceinline__ uint64_t smem_desc_mn(const void* p, uint32_t lbo, uint32_t sbo) {
+  const uint64_t addr = (smem_u32(p) & 0x3FFFFu) >> 4;
+  return addr | (static_cast<uint64_t>(lbo >> 4) << 16) | (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
 }
 __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* m, int c0, int c1, int c2, uint64_t* bar) {
   asm volatile(
@@ -591,11 +608,6 @@ __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* m, int c0, 
           smem_u32(dst)),
       "l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
-}
-__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
-               "r"(r2), "r"(r3)
-               : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
   asm volatile(
@@ -619,7 +631,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t full[2], sbar[2], obar[2], sfree[2], pready[2];
+  __shared__ __align__(8) uint64_t full[kPaStages], sbar[2], obar[2], sfree[2], pready[2];
   __shared__ uint32_t tmem_slot;
   __shared__ float xmax[2][kPaRows];  // each half's tile maximum per row
   __shared__ int pbad[kPaSoftWarps];   // a softmax warp's verdict, read by its pair partner
@@ -637,8 +649,8 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   const int krow0 = a.head_row0 + g * a.cap;      // tensor row of key 0 of this KV head
 
   if (tid == 0) {
+    for (int st = 0; st < kPaStages; ++st) mbar_init(&full[st], 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&full[b], 1);
       mbar_init(&sbar[b], 1);
       mbar_init(&obar[b], 1);
       mbar_init(&sfree[b], kPaSoftWarps);
@@ -662,7 +674,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
       const int c = hf * (D / 16) + cc;  // 8-dim chunk
       float v[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = row_ok ? q[8 * c + e] * a.scale : 0.f;
+      for (int e = 0; e < 8; ++e) v[e] = row_ok ? q[8 * c + e] * (a.scale * kLog2e) : 0.f;  // base-2 scores
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) split_half2(v[2 * e], v[2 * e + 1], hi[e], lo[e]);
@@ -673,7 +685,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   }
   fence_proxy_async();  // generic stores (Q) before the MMAs read them
   auto issue_tile = [&](int kt) {
-    const int st = kt & 1;
+    const int st = kt % kPaStages;
     uint8_t* base = smem + Sm::OFF_ST + st * Sm::STAGE;
     mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(Sm::STAGE));
 #pragma unroll
@@ -693,7 +705,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   const uint32_t tmem = tmem_slot;
   // thread 0: S of tile kt = Q.K^T into S buffer kt & 1 (hi and lo halves of Q)
   auto issue_s = [&](int kt) {
-    const uint8_t* kst = smem + Sm::OFF_ST + (kt & 1) * Sm::STAGE;
+    const uint8_t* kst = smem + Sm::OFF_ST + (kt % kPaStages) * Sm::STAGE;
     const uint32_t ts = tmem + D + 64 * (kt & 1);
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) {
@@ -703,14 +715,14 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
     }
     mma_commit(&sbar[kt & 1]);
   };
-  // the issuer: P.V of tile kt (hi and lo halves of P) into O
+  // the issuer: P.V of tile kt (hi and lo halves of P) into O, V straight from its stage
   auto issue_pv = [&](int kt) {
     const int b = kt & 1;
     const uint8_t* ph = smem + Sm::OFF_P + (2 * b) * Sm::P;
-    const uint8_t* vt = smem + Sm::OFF_VT + b * Sm::VT;
+    const uint8_t* vst = smem + Sm::OFF_ST + (kt % kPaStages) * Sm::STAGE + NA * Sm::KT;
 #pragma unroll
     for (int j = 0; j < kPaKeys / 16; ++j) {
-      const uint64_t vd = smem_desc(vt + j * 32);
+      const uint64_t vd = smem_desc_mn(vst + j * 16 * 128, Sm::KT, 8 * 128);  // keys 16j .. 16j + 15
       mma(tmem, smem_desc(ph + j * 32), vd, Sm::IDESC_O, (kt > 0 || j > 0) ? 1u : 0u);
       if constexpr (SPLIT) mma(tmem, smem_desc(ph + Sm::P + j * 32), vd, Sm::IDESC_O, 1u);
     }
@@ -724,13 +736,14 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   if (warp == kPaSoftWarps) {
     // The issuer: S of tile kt once its K/V stage has landed and its S buffer
     // has been read (tile kt - 2); then P.V of tile kt - 1 once all softmax
-    // warps have written its P and V^T, and the copy of tile kt + 1 into the
-    // stage tile kt - 1 used.  The softmax warps never wait for one another.
+    // warps have written its P, and the copy of tile kt + 1 into the stage of
+    // tile kt - 2 once that tile's P.V is done.  The softmax warps never wait
+    // for one another.
     if (issuer) {
       int t_is = min(nkt, 2), s_is = 0, o_is = 0;
       for (int kt = 0; kt < nkt && !bad; ++kt) {
         const int b = kt & 1;
-        if (!mbar_wait(&full[b], static_cast<uint32_t>(kt >> 1) & 1u) ||
+        if (!mbar_wait(&full[kt % kPaStages], static_cast<uint32_t>(kt / kPaStages) & 1u) ||
             (kt >= 2 && !mbar_wait(&sfree[b], static_cast<uint32_t>((kt - 2) >> 1) & 1u))) {
           bad = true;
           break;
@@ -747,6 +760,10 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
           issue_pv(kt - 1);
           o_is = kt;
           if (kt + 1 < nkt) {
+            if (kt >= 2 && !mbar_wait(&obar[b], static_cast<uint32_t>((kt - 2) >> 1) & 1u)) {
+              bad = true;
+              break;
+            }
             issue_tile(kt + 1);
             t_is = kt + 2;
           }
@@ -768,34 +785,24 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   } else {
     for (int kt = 0; kt < nkt; ++kt) {
       const int b = kt & 1;
-      // this tile's K/V stage has landed; the P.V of two tiles ago, which read
-      // buffers b, is done
-      if (!mbar_wait(&full[b], static_cast<uint32_t>(kt >> 1) & 1u)) bad = true;
+      // the P.V of two tiles ago, which read P buffer b, is done
       if (kt >= 2 && !mbar_wait(&obar[b], static_cast<uint32_t>((kt - 2) >> 1) & 1u)) bad = true;
-      bad = __any_sync(0xffffffffu, bad);
-      // V^T [dim][key] from the V rows [key][dim]: 8x8 blocks, transposed on the
-      // way through registers; keys past the CTA's last one become zeros
-      if (!bad) {
-        const uint8_t* vst = smem + Sm::OFF_ST + b * Sm::STAGE + NA * Sm::KT;
-        uint8_t* vt = smem + Sm::OFF_VT + b * Sm::VT;
-        const int kvalid = kend - kt * kPaKeys;
-        constexpr int NBLK = (kPaKeys / 8) * (D / 8);
-        for (int bi = warp * 4; bi < NBLK; bi += 4 * kPaSoftWarps) {
-          const int m = lane >> 3, r8 = lane & 7;
-          const int blk = bi + m, kb = blk / (D / 8), db = blk - kb * (D / 8);
-          const int key = 8 * kb + r8;
-          uint32_t r[4];
-          ldsm_x4_t(smem_u32(vst + (db >> 3) * Sm::KT + sw128(key, 8 * (db & 7))), r[0], r[1], r[2], r[3]);
-          // lane (gq, tq) holds keys 8kb + 2tq, +1 of dim 8db + gq, for each of the 4 blocks
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int k0i = 8 * ((bi + i) / (D / 8)) + 2 * (lane & 3);
-            if (k0i >= kvalid) r[i] = 0u;
-            else if (k0i + 1 >= kvalid) r[i] &= 0x0000FFFFu;
+      // the CTA's last tile: V rows past its last key (stale cache rows, maybe
+      // not even finite) become zeros, since P.V multiplies them by p = 0
+      const int kvalid = kend - kt * kPaKeys;
+      if (kvalid < kPaKeys) {
+        if (!mbar_wait(&full[kt % kPaStages], static_cast<uint32_t>(kt / kPaStages) & 1u)) bad = true;
+        if (!__any_sync(0xffffffffu, bad)) {
+          uint8_t* vst = smem + Sm::OFF_ST + (kt % kPaStages) * Sm::STAGE + NA * Sm::KT;
+          const int chunks = (kPaKeys - kvalid) * 8;  // 16-byte chunks per 64-dim atom
+          for (int i = tid; i < NA * chunks; i += 32 * kPaSoftWarps) {
+            const int at = i / chunks, r = i - at * chunks;
+            *reinterpret_cast<uint4*>(vst + at * Sm::KT + (kvalid + r / 8) * 128 + (r & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
           }
-          stsm_x4(smem_u32(vt + sw128(8 * db + r8, 8 * kb)), r[0], r[1], r[2], r[3]);
         }
       }
+      bad = __any_sync(0xffffffffu, bad);
       // this thread's 32 scores of the row; then the S buffer is free for tile kt + 2
       if (!mbar_wait(&sbar[b], static_cast<uint32_t>(kt >> 1) & 1u)) bad = true;
       bad = __any_sync(0xffffffffu, bad);
@@ -815,11 +822,12 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
       if (lane == 0 && !bad) mbar_arrive(&sfree[b]);
       float mx = -INFINITY;
       const int last = row_ok ? qpos - kt * kPaKeys - 32 * hf : -1;  // this half's last visible column
+      if (__any_sync(0xffffffffu, last < 31)) {  // a column to mask in this warp's rows
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        sv[j] = j <= last ? sv[j] : -INFINITY;
-        mx = fmaxf(mx, sv[j]);
+        for (int j = 0; j < 32; ++j) sv[j] = j <= last ? sv[j] : -INFINITY;
       }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mx = fmaxf(mx, sv[j]);
       // the row's other half is taken by warp w ^ 4: a barrier of those two
       // warps, which also share their verdicts, so both leave together
       xmax[hf][row] = mx;
@@ -829,9 +837,9 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
       const float mt = fmaxf(mx, xmax[hf ^ 1][row]);
       asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");  // xmax / pbad reused next tile
       if (bad) break;
-      // the reference maximum moves only when a tile's maximum exceeds it by kRescaleLog
-      const bool move = row_ok && mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog);
-      const float alpha = move ? (m_ref == -INFINITY ? 0.f : expf(m_ref - mt)) : 1.f;
+      // the reference maximum moves only when a tile's maximum exceeds it by kRescaleLog2
+      const bool move = row_ok && mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog2);
+      const float alpha = move ? (m_ref == -INFINITY ? 0.f : ex2(m_ref - mt)) : 1.f;
       if (move) {
         l_part *= alpha;
         m_ref = mt;
@@ -855,7 +863,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
           tmem_st32(t_o + c, ov);
         }
       }
-      // P = exp(s - m_ref) as fp16 hi + lo, this half's 32 keys
+      // P = 2^(s - m_ref) as fp16 hi + lo, this half's 32 keys
       {
         uint8_t* ph = smem + Sm::OFF_P + (2 * b) * Sm::P;
         uint8_t* pl = ph + Sm::P;
@@ -866,8 +874,8 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            // masked columns are -inf: __expf gives 0
-            const float p0 = __expf(sv[8 * c + 2 * e] - mr), p1 = __expf(sv[8 * c + 2 * e + 1] - mr);
+            // masked columns are -inf: 2^-inf = 0
+            const float p0 = ex2(sv[8 * c + 2 * e] - mr), p1 = ex2(sv[8 * c + 2 * e + 1] - mr);
             ps += p0 + p1;
             split_half2(p0, p1, hi[e], lo[e]);
           }
@@ -877,7 +885,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
         }
         l_part += ps;
       }
-      fence_proxy_async();  // P and V^T (generic stores) before the MMAs read them
+      fence_proxy_async();  // P and the zeroed V rows (generic stores) before the MMAs read them
       tc_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pready[b]);
@@ -888,8 +896,8 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   // copies and MMAs still in flight end before the CTA's memory goes away (bounded waits)
   if (bad && issuer) {
     atomicOr(a.guard, GUARD_TIMEOUT);
-    for (int k = max(0, t_issued - 2); k < t_issued; ++k)
-      (void)mbar_wait(&full[k & 1], static_cast<uint32_t>(k >> 1) & 1u);
+    for (int k = max(0, t_issued - kPaStages); k < t_issued; ++k)
+      (void)mbar_wait(&full[k % kPaStages], static_cast<uint32_t>(k / kPaStages) & 1u);
     if (s_issued > 0) (void)mbar_wait(&sbar[(s_issued - 1) & 1], static_cast<uint32_t>((s_issued - 1) >> 1) & 1u);
   }
   bool have_o = o_issued > 0;
