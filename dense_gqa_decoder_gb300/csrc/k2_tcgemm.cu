@@ -539,11 +539,12 @@ EncodeTiled encode_fn() {
 //   S = Q.K^T   (tcgen05.mma M=128 N=64, S in TMEM): Q as fp16 hi + lo halves
 //               (two MMAs per k-step: ~22 bits of every query; SPLIT = false:
 //               fp16 Q alone, one MMA), K the fp16 cache;
-//   softmax     row r (TMEM lane r) is shared by the two warps that may read
-//               lane group r / 32: each takes 32 of the tile's 64 scores
-//               (tcgen05.ld), the two exchange their maxima through shared
-//               memory, and write their halves of P = exp(s - m) as fp16 hi + lo
-//               (SPLIT = false: fp16 P alone);
+//   softmax     row r (TMEM lane r) is shared by the NQ warps that may read
+//               lane group r / 32 (NQ = 4 for head_dim 128, 2 for 64): each
+//               takes 64 / NQ of the tile's 64 scores (tcgen05.ld), they
+//               exchange their maxima through shared memory, and write their
+//               parts of P = 2^(s - m) as fp16 hi + lo (SPLIT = false: fp16 P
+//               alone);
 //   O += P.V^T  (tcgen05.mma M=128 N=D, O in TMEM).
 // Q, K and P are K-major with the 128-byte swizzle (the layout of the GEMMs'
 // descriptors): Q and P are written so by the threads, K arrives so by TMA; V
@@ -557,11 +558,11 @@ EncodeTiled encode_fn() {
 // more than kRescaleLog2 (then O and the row's sums are rescaled in TMEM);
 // otherwise p may exceed 1 (at most 2^kRescaleLog2, well inside fp16), and the
 // final division by the sum makes the result exact anyway.  K/V tiles rotate
-// through three stages: the next tile is requested once the P.V that read the
-// stage it reuses is done.
-// 8 softmax warps (two per TMEM lane group) and one issuer warp
-constexpr int kPaRows = 128, kPaKeys = 64, kPaSoftWarps = 8, kPaThreads = 32 * (kPaSoftWarps + 1);
-constexpr int kPaStages = 3;
+// through STAGES stages (4 with single-operand Q and P, 3 with hi + lo): tile
+// kt + STAGES - 2 is requested once the P.V that read the stage it reuses (of
+// tile kt - 2) is done, so each copy has STAGES - 2 softmax passes to land.
+// 4 NQ softmax warps (NQ per TMEM lane group) and one issuer warp
+constexpr int kPaRows = 128, kPaKeys = 64, kPaMaxSoftWarps = 16;
 constexpr float kRescaleLog2 = 11.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 __device__ __forceinline__ float ex2(float x) {  // 2^x (the SFU's approximation; 2^-inf = 0)
@@ -570,17 +571,24 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x (the SFU's approximation
   return y;
 }
 
-template <int D>
+template <int D, bool SPLIT>
 struct PaSmem {
+  // softmax warps per TMEM lane group (4, a quarter row each, measured slower:
+  // 4096-token prefill 52.4 against 50.3 ms)
+  static constexpr int NQ = 2;
+  static constexpr int SOFT = 4 * NQ, THREADS = 32 * (SOFT + 1);
   static constexpr int NA = D / 64;                   // 64-dim swizzle atoms per row
   static constexpr int Q = kPaRows * 128;             // one atom of the 128 query rows (16 KB)
   static constexpr int KT = kPaKeys * 128;            // one atom of a 64-key K (or V) tile (8 KB)
   static constexpr int STAGE = 2 * NA * KT;           // K and V of one tile
   static constexpr int P = kPaRows * 128;             // P [128][64 keys] (one half)
+  static constexpr int PB = (SPLIT ? 2 : 1) * P;       // one P buffer: hi (+ lo)
+  static constexpr int STAGES = SPLIT ? 3 : 4;        // K/V stages (5 measured no faster than 4)
+  static constexpr int PD = STAGES - 2;               // tiles requested ahead of the one being scored
   static constexpr int OFF_QH = 0, OFF_QL = OFF_QH + NA * Q;
-  static constexpr int OFF_ST = OFF_QL + NA * Q;      // kPaStages stages
-  static constexpr int OFF_P = OFF_ST + kPaStages * STAGE;  // two buffers of P hi, P lo
-  static constexpr int BYTES = OFF_P + 4 * P;
+  static constexpr int OFF_ST = OFF_QL + (SPLIT ? NA * Q : 0);  // STAGES stages
+  static constexpr int OFF_P = OFF_ST + STAGES * STAGE;        // two P buffers
+  static constexpr int BYTES = OFF_P + 2 * PB;
   static constexpr int DYN = BYTES + 1024;            // + alignment to 1024 B
   static constexpr int TMEM_COLS = D + 128 <= 128 ? 128 : 256;  // O [D], then S [64] x 2
   // instruction descriptors (kind::f16): fp16 A and B, fp32 D, M = 128; S: both K-major;
@@ -622,23 +630,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
 }
 
 template <int D, int REP, bool SPLIT>
-__global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __grid_constant__ KvMaps maps,
+__global__ void __launch_bounds__(PaSmem<D, SPLIT>::THREADS, 1) prefill_attn_tc_kernel(const __grid_constant__ KvMaps maps,
                                                                         const PrefillAttnArgs a) {
-  using Sm = PaSmem<D>;
+  using Sm = PaSmem<D, SPLIT>;
   constexpr int NA = Sm::NA;
   constexpr int QT = kPaRows / REP;  // tokens per CTA
-  constexpr int DH = D / 2;          // O columns per half
+  constexpr int NQ = Sm::NQ, kPaSoftWarps = Sm::SOFT, kPaStages = Sm::STAGES;
+  constexpr int CW = kPaKeys / NQ;   // score columns per thread and tile
+  constexpr int DH = D / NQ;         // O columns per thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) uint64_t full[kPaStages], sbar[2], obar[2], sfree[2], pready[2];
   __shared__ uint32_t tmem_slot;
-  __shared__ float xmax[2][kPaRows];  // each half's tile maximum per row
-  __shared__ int pbad[kPaSoftWarps];   // a softmax warp's verdict, read by its pair partner
+  __shared__ float xmax[NQ][kPaRows];    // each part's tile maximum per row
+  __shared__ int pbad[kPaMaxSoftWarps];  // a softmax warp's verdict, read by the warps sharing its rows
   __shared__ int issued[3];            // the issuer's count of K/V tiles, S and P.V issued
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = (warp & 3) * 32 + lane;  // TMEM lane = query row
-  const int hf = warp >> 2;                // which 32 of the 64 scores (and half of O) this thread takes
+  const int hf = warp >> 2;                // which CW of the 64 scores (and DH columns of O) this thread takes
   const int t0 = blockIdx.x * QT, g = blockIdx.y;
   const int nt = min(QT, a.n - t0);
   const int tq = row / REP, hh = row - tq * REP;  // token t0 + tq, query head g * REP + hh
@@ -670,8 +680,8 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   if (warp < kPaSoftWarps) {
     const float* q = a.Q + static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D;
 #pragma unroll
-    for (int cc = 0; cc < D / 16; ++cc) {
-      const int c = hf * (D / 16) + cc;  // 8-dim chunk
+    for (int cc = 0; cc < D / (8 * NQ); ++cc) {
+      const int c = hf * (D / (8 * NQ)) + cc;  // 8-dim chunk
       float v[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = row_ok ? q[8 * c + e] * (a.scale * kLog2e) : 0.f;  // base-2 scores
@@ -698,10 +708,8 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   tc_before();
   __syncthreads();  // the barriers (initialised by thread 0) and Q are ready
   tc_after();
-  if (issuer) {
-    if (nkt > 0) issue_tile(0);
-    if (nkt > 1) issue_tile(1);
-  }
+  if (issuer)
+    for (int kt = 0; kt <= Sm::PD && kt < nkt; ++kt) issue_tile(kt);
   const uint32_t tmem = tmem_slot;
   // thread 0: S of tile kt = Q.K^T into S buffer kt & 1 (hi and lo halves of Q)
   auto issue_s = [&](int kt) {
@@ -718,7 +726,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
   // the issuer: P.V of tile kt (hi and lo halves of P) into O, V straight from its stage
   auto issue_pv = [&](int kt) {
     const int b = kt & 1;
-    const uint8_t* ph = smem + Sm::OFF_P + (2 * b) * Sm::P;
+    const uint8_t* ph = smem + Sm::OFF_P + b * Sm::PB;
     const uint8_t* vst = smem + Sm::OFF_ST + (kt % kPaStages) * Sm::STAGE + NA * Sm::KT;
 #pragma unroll
     for (int j = 0; j < kPaKeys / 16; ++j) {
@@ -729,18 +737,18 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
     mma_commit(&obar[b]);
   };
   const uint32_t lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
-  const uint32_t t_o = tmem + lanes + hf * DH;                             // this thread's half of O
+  const uint32_t t_o = tmem + lanes + hf * DH;                             // this thread's part of O
 
   float m_ref = -INFINITY, l_part = 0.f;  // the row's reference maximum; this half's sum of p
   bool bad = false;
   if (warp == kPaSoftWarps) {
     // The issuer: S of tile kt once its K/V stage has landed and its S buffer
     // has been read (tile kt - 2); then P.V of tile kt - 1 once all softmax
-    // warps have written its P, and the copy of tile kt + 1 into the stage of
+    // warps have written its P, and the copy of tile kt + PD into the stage of
     // tile kt - 2 once that tile's P.V is done.  The softmax warps never wait
     // for one another.
     if (issuer) {
-      int t_is = min(nkt, 2), s_is = 0, o_is = 0;
+      int t_is = min(nkt, Sm::PD + 1), s_is = 0, o_is = 0;
       for (int kt = 0; kt < nkt && !bad; ++kt) {
         const int b = kt & 1;
         if (!mbar_wait(&full[kt % kPaStages], static_cast<uint32_t>(kt / kPaStages) & 1u) ||
@@ -759,13 +767,13 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
           tc_after();
           issue_pv(kt - 1);
           o_is = kt;
-          if (kt + 1 < nkt) {
+          if (kt + Sm::PD < nkt) {
             if (kt >= 2 && !mbar_wait(&obar[b], static_cast<uint32_t>((kt - 2) >> 1) & 1u)) {
               bad = true;
               break;
             }
-            issue_tile(kt + 1);
-            t_is = kt + 2;
+            issue_tile(kt + Sm::PD);
+            t_is = kt + Sm::PD + 1;
           }
         }
       }
@@ -807,35 +815,40 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
       if (!mbar_wait(&sbar[b], static_cast<uint32_t>(kt >> 1) & 1u)) bad = true;
       bad = __any_sync(0xffffffffu, bad);
       tc_after();
-      float sv[32];
+      float sv[CW];
       if (!bad) {
-        uint32_t raw[32];
-        tmem_ld32(tmem + lanes + D + 64 * b + 32 * hf, raw);
+        uint32_t raw[CW];
+        if constexpr (CW == 32) tmem_ld32(tmem + lanes + D + 64 * b + CW * hf, raw);
+        else tmem_ld16(tmem + lanes + D + 64 * b + CW * hf, raw);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(raw[j]);
+        for (int j = 0; j < CW; ++j) sv[j] = __uint_as_float(raw[j]);
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = -INFINITY;
+        for (int j = 0; j < CW; ++j) sv[j] = -INFINITY;
       }
       tc_before();
       __syncwarp();
       if (lane == 0 && !bad) mbar_arrive(&sfree[b]);
       float mx = -INFINITY;
-      const int last = row_ok ? qpos - kt * kPaKeys - 32 * hf : -1;  // this half's last visible column
-      if (__any_sync(0xffffffffu, last < 31)) {  // a column to mask in this warp's rows
+      const int last = row_ok ? qpos - kt * kPaKeys - CW * hf : -1;  // this part's last visible column
+      if (__any_sync(0xffffffffu, last < CW - 1)) {  // a column to mask in this warp's rows
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = j <= last ? sv[j] : -INFINITY;
+        for (int j = 0; j < CW; ++j) sv[j] = j <= last ? sv[j] : -INFINITY;
       }
 #pragma unroll
-      for (int j = 0; j < 32; ++j) mx = fmaxf(mx, sv[j]);
-      // the row's other half is taken by warp w ^ 4: a barrier of those two
-      // warps, which also share their verdicts, so both leave together
+      for (int j = 0; j < CW; ++j) mx = fmaxf(mx, sv[j]);
+      // the row's other parts are taken by warps w + 4q: a barrier of those NQ
+      // warps, which also share their verdicts, so all of them leave together
       xmax[hf][row] = mx;
       if (lane == 0) pbad[warp] = bad ? 1 : 0;
-      asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
-      if (pbad[warp ^ 4] != 0) bad = true;
-      const float mt = fmaxf(mx, xmax[hf ^ 1][row]);
-      asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");  // xmax / pbad reused next tile
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "r"(32 * NQ) : "memory");
+      float mt = mx;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (pbad[(warp & 3) + 4 * q] != 0) bad = true;
+        mt = fmaxf(mt, xmax[q][row]);
+      }
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "r"(32 * NQ) : "memory");  // xmax / pbad reused next tile
       if (bad) break;
       // the reference maximum moves only when a tile's maximum exceeds it by kRescaleLog2
       const bool move = row_ok && mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog2);
@@ -863,14 +876,14 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
           tmem_st32(t_o + c, ov);
         }
       }
-      // P = 2^(s - m_ref) as fp16 hi + lo, this half's 32 keys
+      // P = 2^(s - m_ref) as fp16 hi + lo, this part's CW keys
       {
-        uint8_t* ph = smem + Sm::OFF_P + (2 * b) * Sm::P;
+        uint8_t* ph = smem + Sm::OFF_P + b * Sm::PB;
         uint8_t* pl = ph + Sm::P;
         const float mr = m_ref == -INFINITY ? 0.f : m_ref;  // a row with no visible key yet: all p are 0
         float ps = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < CW / 8; ++c) {
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -879,7 +892,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
             ps += p0 + p1;
             split_half2(p0, p1, hi[e], lo[e]);
           }
-          const uint32_t off = sw128(row, 32 * hf + 8 * c);
+          const uint32_t off = sw128(row, CW * hf + 8 * c);
           *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           if constexpr (SPLIT) *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
@@ -905,15 +918,16 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_tc_kernel(const __
     if (!mbar_wait(&obar[k & 1], static_cast<uint32_t>(k >> 1) & 1u)) have_o = false;
   have_o = __syncthreads_and(have_o) != 0;  // the tensor-memory reads below are warp-wide
   tc_after();
-  // the row's sum: both halves (softmax warps only)
+  // the row's sum: all its parts (softmax warps only)
   float l_sum = 0.f;
   if (warp < kPaSoftWarps) {
     xmax[hf][row] = l_part;
-    asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
-    l_sum = l_part + xmax[hf ^ 1][row];
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "r"(32 * NQ) : "memory");
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) l_sum += xmax[q][row];
   }
   if (warp < kPaSoftWarps && !bad && have_o) {
-    // this half of the row: O / sum, as bf16 hi (+ lo when the GEMM that follows takes it)
+    // this part of the row: O / sum, as bf16 hi (+ lo when the GEMM that follows takes it), or fp16
     const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
     const size_t ob = static_cast<size_t>(t0 + tq) * a.nq * D + (g * REP + hh) * D + hf * DH;
 #pragma unroll 1
@@ -1005,10 +1019,10 @@ cudaError_t prefill_attn_tc_init_attrs() {
   const auto set = [](const void* k, int bytes) {
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   };
-  cudaError_t e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<128, 4, true>), PaSmem<128>::DYN);
-  if (e == cudaSuccess) e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<128, 4, false>), PaSmem<128>::DYN);
-  if (e == cudaSuccess) e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<64, 4, true>), PaSmem<64>::DYN);
-  if (e == cudaSuccess) e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<64, 4, false>), PaSmem<64>::DYN);
+  cudaError_t e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<128, 4, true>), PaSmem<128, true>::DYN);
+  if (e == cudaSuccess) e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<128, 4, false>), PaSmem<128, false>::DYN);
+  if (e == cudaSuccess) e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<64, 4, true>), PaSmem<64, true>::DYN);
+  if (e == cudaSuccess) e = set(reinterpret_cast<const void*>(prefill_attn_tc_kernel<64, 4, false>), PaSmem<64, false>::DYN);
   return e;
 }
 
@@ -1018,13 +1032,13 @@ cudaError_t launch_prefill_attn_tc(const KvMaps& maps, const PrefillAttnArgs& a,
   if (!prefill_attn_tc_supported(head_dim, rep) || (a.split && a.ol == nullptr)) return cudaErrorInvalidValue;
   const dim3 grid((a.n + kPaRows / rep - 1) / (kPaRows / rep), a.nkv);
   if (head_dim == 128 && a.split)
-    prefill_attn_tc_kernel<128, 4, true><<<grid, kPaThreads, PaSmem<128>::DYN, s>>>(maps, a);
+    prefill_attn_tc_kernel<128, 4, true><<<grid, PaSmem<128, true>::THREADS, PaSmem<128, true>::DYN, s>>>(maps, a);
   else if (head_dim == 128)
-    prefill_attn_tc_kernel<128, 4, false><<<grid, kPaThreads, PaSmem<128>::DYN, s>>>(maps, a);
+    prefill_attn_tc_kernel<128, 4, false><<<grid, PaSmem<128, false>::THREADS, PaSmem<128, false>::DYN, s>>>(maps, a);
   else if (a.split)
-    prefill_attn_tc_kernel<64, 4, true><<<grid, kPaThreads, PaSmem<64>::DYN, s>>>(maps, a);
+    prefill_attn_tc_kernel<64, 4, true><<<grid, PaSmem<64, true>::THREADS, PaSmem<64, true>::DYN, s>>>(maps, a);
   else
-    prefill_attn_tc_kernel<64, 4, false><<<grid, kPaThreads, PaSmem<64>::DYN, s>>>(maps, a);
+    prefill_attn_tc_kernel<64, 4, false><<<grid, PaSmem<64, false>::THREADS, PaSmem<64, false>::DYN, s>>>(maps, a);
   return cudaGetLastError();
 }
 
