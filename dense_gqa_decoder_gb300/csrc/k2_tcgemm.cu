@@ -649,7 +649,9 @@ __global__ void __launch_bounds__(PaSmem<D, SPLIT>::THREADS, 1) prefill_attn_tc_
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = (warp & 3) * 32 + lane;  // TMEM lane = query row
   const int hf = warp >> 2;                // which CW of the 64 scores (and DH columns of O) this thread takes
-  const int t0 = blockIdx.x * QT, g = blockIdx.y;
+  // the last query blocks (the most keys) are scheduled first, so the final
+  // wave holds the short ones
+  const int t0 = (gridDim.x - 1 - blockIdx.x) * QT, g = blockIdx.y;
   const int nt = min(QT, a.n - t0);
   const int tq = row / REP, hh = row - tq * REP;  // token t0 + tq, query head g * REP + hh
   const bool row_ok = tq < nt;
