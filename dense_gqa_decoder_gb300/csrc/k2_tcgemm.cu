@@ -1060,7 +1060,7 @@ cudaError_t tc_gemm_init_attrs() {
   if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, true, 1>, Tile<128, true, true, 1>::SMEM_BYTES);
   if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, true, false, 2>, Tile<128, true, false, 2>::SMEM_BYTES);
   if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<128, false, false, 2>, Tile<128, false, false, 2>::SMEM_BYTES);
-  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<256, false, false, 2>, Tile<256, false, false, 2>::SMEM_BYTES);
+  if (e == cudaSuccess) e = smem_attr(tc_gemm_sk_kernel<256, false, false, 1>, Tile<256, false, false, 1>::SMEM_BYTES);
   return e;
 }
 
@@ -1074,7 +1074,8 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* m
   const bool lo = mapXl != nullptr, wl = mapWl != nullptr;
   if ((tt == 16 && (!lo || wl)) || (wl && !lo) || (tt == 256 && (lo || wl))) return cudaErrorInvalidValue;
   // 128-token tiles fill each ring stage with two K steps (larger copy groups: measured on the
-  // 4096-token prefill, 85.0 -> 80.2 ms with the stream-K o_proj / down so too) where two fit twice
+  // 4096-token prefill, 85.0 -> 80.2 ms with the stream-K o_proj / down so too) where two fit
+  // twice; 256-token tiles take one K step (48 KB) per stage, four stages (49.5 -> 48.8 ms)
   const bool two = tt == 128 && !wl;
   const long long tiles = static_cast<long long>((2 * ((a.N + 1) / 2) + BM - 1) / BM) * ((a.T + tt - 1) / tt);
   const int grid = static_cast<int>(std::min<long long>(ctas, a.whole ? tiles : tiles * a.ksteps));
@@ -1086,7 +1087,7 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* m
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = tt == 16    ? Tile<16, true, false, 1>::SMEM_BYTES
-                         : tt == 256 ? Tile<256, false, false, 2>::SMEM_BYTES
+                         : tt == 256 ? Tile<256, false, false, 1>::SMEM_BYTES
                          : wl        ? Tile<128, true, true, 1>::SMEM_BYTES
                          : two    ? (lo ? Tile<128, true, false, 2>::SMEM_BYTES : Tile<128, false, false, 2>::SMEM_BYTES)
                          : lo     ? Tile<128, true, false, 1>::SMEM_BYTES
@@ -1098,7 +1099,7 @@ cudaError_t launch_tc_gemm_sk(const void* mapW, const void* mapWl, const void* m
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   if (tt == 16) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<16, true, false, 1>, w, wlo, xh, xl, a);
-  if (tt == 256) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<256, false, false, 2>, w, wlo, xh, xl, a);
+  if (tt == 256) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<256, false, false, 1>, w, wlo, xh, xl, a);
   if (wl) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true, true, 1>, w, wlo, xh, xl, a);
   if (two && lo) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, true, false, 2>, w, wlo, xh, xl, a);
   if (two) return cudaLaunchKernelEx(&cfg, tc_gemm_sk_kernel<128, false, false, 2>, w, wlo, xh, xl, a);
