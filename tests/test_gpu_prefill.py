@@ -231,13 +231,16 @@ def test_prefill_without_split_against_oracle(k2, mio, kv, shape, first, n):
     assert t0 == O.argmax_first(ref)
 
 
+@pytest.mark.parametrize("split", [1, 3])
 @pytest.mark.parametrize("shape,first,n", [("k2_layer", 50, 1000), ("medium", 0, 333), ("medium", 129, 2100)])
-def test_persistent_prefill_gemm_against_per_tile_and_oracle(k2, mio, shape, first, n):
+def test_persistent_prefill_gemm_against_per_tile_and_oracle(k2, mio, shape, first, n, split):
     """K2_OPT_PREFILL_GEMM: QKV and gate/up on the persistent kernel over whole
     tiles (1, the default: the SwiGLU epilogue of one tile overlaps the next
-    tile's K steps) against one CTA per tile (0) and the oracle's full
-    recompute; ragged token tiles, and a prompt longer than one 2048-token
-    block after cached rows."""
+    tile's K steps; 256-token tiles for fp16 blocks over 512 tokens) against
+    one CTA per tile (0) and the oracle's full recompute; ragged token tiles,
+    and a prompt longer than one 2048-token block after cached rows.  split:
+    the bf16 hi + lo activations (1) or single fp16 operands (3, whose bars are
+    those of test_fp16_operand_prefill_against_oracle)."""
     s = ki.SHAPES[shape]
     pre = ki.prompt_ids(s.vocab, first, seed=93) if first else None
     prompt = ki.prompt_ids(s.vocab, n, seed=94)
@@ -246,19 +249,22 @@ def test_persistent_prefill_gemm_against_per_tile_and_oracle(k2, mio, shape, fir
         ctx, host = mio.build_context(s, max_context=first + n + 8, kv_dtype="f16", gain_scale=0.1, keep_host=True)
         ctx.set_option(k2.K2_OPT_PREFILL_GEMM, mode)
         if pre is not None:
-            prefill(k2, ctx, pre, s.vocab, True)
-        tok, lg = prefill(k2, ctx, prompt, s.vocab, True)
+            prefill(k2, ctx, pre, s.vocab, True, split)
+        tok, lg = prefill(k2, ctx, prompt, s.vocab, True, split)
         hid = k2.device_view(ctx.hidden_view(0), s.hidden, torch.float32).cpu().numpy().copy()
         out[mode] = (tok, lg, hid)
         assert ctx.sync_status() == k2.K2_OK
     seq = prompt if pre is None else np.concatenate([pre, prompt])
     ref = O.OracleModel(s, lambda nm, l: host[(nm, l)], "f16").forward_full(seq)
     (t1, l1, h1), (t0, l0, h0) = out[1], out[0]
-    assert rel_l2(l1, ref) <= 2e-4
-    assert rel_l2(l0, ref) <= 2e-4
-    # same MMAs in the same order; only the SwiGLU epilogue's exp / reciprocal differ
-    assert rel_l2(l1, l0) <= 1e-4
-    assert rel_l2(h1, h0) <= 1e-4
+    bar = 2e-4 if split == 1 else 5e-3
+    assert rel_l2(l1, ref) <= bar
+    assert rel_l2(l0, ref) <= bar
+    # the same products; the tile shapes, the order of the fp32 additions and
+    # (fp16) the activations they round differ: well inside the bars' margin
+    close = 1e-4 if split == 1 else 2e-3
+    assert rel_l2(l1, l0) <= close
+    assert rel_l2(h1, h0) <= close
     assert t1 == t0 == O.argmax_first(ref)
 
 
