@@ -419,8 +419,8 @@ typedef enum {
                              blocks of up to 16 tokens always keep the halves; int4 weights keep the GEMMs'.
                              Measured on the 36-layer 3.7B shape (512-token prompt, 256 greedy steps, fp16
                              KV): 1 gives 100 % teacher-forced agreement, relative L2 4.3e-4 (4.5e-4 on the
-                             prefill's logits); 2 is 5 % faster, 100 %, 5.1e-4 (1.4e-3); 0 is 18 % faster
-                             but 96.5 %, 1.1e-2 (2.1e-2), below the bf16 parity bars.  3 (bf16 weights, fp16
+                             prefill's logits); 2 gives 100 %, 5.1e-4 (1.4e-3); 0 gives 94.9-96.5 %,
+                             1.1e-2 (2.1e-2), below the bf16 parity bars.  3 (bf16 weights, fp16
                              caches) runs every prefill contraction on single fp16 operands: each weight
                              matrix is converted to fp16 per layer (exact in fp16's normal range, values
                              beyond +-65504 raise the device guard), the activations enter as fp16 (11
