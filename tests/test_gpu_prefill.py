@@ -268,7 +268,8 @@ def test_persistent_prefill_gemm_against_per_tile_and_oracle(k2, mio, shape, fir
     assert t1 == t0 == O.argmax_first(ref)
 
 
-@pytest.mark.parametrize("shape,first,n", [("k2_layer", 50, 1000), ("medium", 0, 333), ("medium", 129, 2100)])
+@pytest.mark.parametrize("shape,first,n", [("k2_layer", 50, 1000), ("medium", 0, 333), ("medium", 129, 2100),
+                                           ("medium", 0, 512), ("medium", 7, 513)])
 def test_fp16_operand_prefill_against_oracle(k2, mio, shape, first, n):
     """K2_OPT_PREFILL_SPLIT = 3: every prefill contraction on single fp16
     operands (each weight matrix converted to fp16 per layer, fp16 activations,
@@ -276,7 +277,8 @@ def test_fp16_operand_prefill_against_oracle(k2, mio, shape, first, n):
     2^-11 = 4.9e-4); each layer rounds its four GEMM inputs and the attention's
     queries and probabilities once, so the logits are held to 5e-3 of the
     oracle's full recompute (10 roundoffs) and to the same argmax; the split
-    run (1) of the same prompt stays within 2e-4."""
+    run (1) of the same prompt stays within 2e-4.  Blocks of more than 512
+    tokens take 256-token GEMM tiles: 512 and 513 tokens sit on either side."""
     s = ki.SHAPES[shape]
     pre = ki.prompt_ids(s.vocab, first, seed=95) if first else None
     prompt = ki.prompt_ids(s.vocab, n, seed=96)
