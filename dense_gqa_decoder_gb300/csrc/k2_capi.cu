@@ -926,7 +926,10 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.f16 = f16 ? 1 : 0;
     if (!c->pf_whole) return launch_tc_gemm(mw, wlo, mh, ml, g, st);
     g.whole = 1;
-    return launch_tc_gemm_sk(mw, wlo, mh, ml, g, c->sms, st);
+    // programmatic dependent launch: the GEMM requests its first weight stages
+    // while the kernel before it (a norm, which lets dependents start at once)
+    // still runs, and waits for it before reading the activations
+    return launch_tc_gemm_sk(mw, wlo, mh, ml, g, c->sms, st, c->pdl);
   };
   const int tt = small ? 16 : 128;
   auto gemm_sk = [&](const void* mw, const float* rs, const void* mh, const void* ml, int N, int K, int mode, float* out,
@@ -946,7 +949,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
     g.f16 = f16 ? 1 : 0;
     cudaError_t e = cudaSuccess;
     if (mode == TC_STORE) e = cudaMemsetAsync(out, 0, sizeof(float) * static_cast<size_t>(n) * ldo, st);
-    if (!e) e = launch_tc_gemm_sk(mw, wlo, mh, ml, g, c->sms, st);
+    if (!e) e = launch_tc_gemm_sk(mw, wlo, mh, ml, g, c->sms, st, c->pdl && !small);
     return e;
   };
   // without the split (blocks over 16 tokens only) the low-half maps are null:
