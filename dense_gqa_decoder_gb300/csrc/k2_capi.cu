@@ -983,7 +983,7 @@ cudaError_t prefill_block(k2_ctx* c, int seq, const int* d_tokens, int n, int po
                 : gemm(wmap(l, 0), c->tcs(l, 0), m_xh, m_xl, s.qkv_n, s.H, TC_STORE, qkv, nullptr, nullptr, s.qkv_n);
     if (!e)
       e = launch_rope_append(qkv, Q, c->rope, kvdt, c->kc(l), c->vc(l), c->ks(l), c->vs(l), n, s.nq, s.nkv, s.d,
-                             pos0, d_pos0, head_row0, c->lay.cap, st);
+                             pos0, d_pos0, head_row0, c->lay.cap, st, c->pdl);
     if (!e && small) {
       // few queries over a long history: the decode attention in block mode
       // splits every query's keys over a cluster of CTAs

@@ -503,7 +503,7 @@ cudaError_t launch_bf16_to_f16(__half* dst, const __nv_bfloat16* src, size_t n, 
 // pos0_dev (nullable): read the first position from device memory instead of pos0
 cudaError_t launch_rope_append(const float* qkv, float* Q, const float2* rope, int kv_dtype, void* kc, void* vc,
                                void* ks, void* vs, int n, int nq, int nkv, int D, int pos0, const int* pos0_dev,
-                               size_t head_row0, int cap, cudaStream_t s);
+                               size_t head_row0, int cap, cudaStream_t s, bool pdl = false);
 cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, const void* vc, const void* ks,
                                 const void* vs, __nv_bfloat16* oh, __nv_bfloat16* ol, int n, int nq, int nkv, int D,
                                 int pos0, size_t head_row0, int cap, float scale, cudaStream_t s);

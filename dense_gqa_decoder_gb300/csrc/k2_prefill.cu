@@ -168,6 +168,8 @@ __global__ void rope_append_kernel(const float* __restrict__ qkv, float* __restr
                                    __half* __restrict__ vs, int nq, int nkv, int D, int pos0, const int* pos0_dev,
                                    size_t head_row0, int cap) {
   extern __shared__ float rows[];  // [2 * nkv][D]: this token's K and V rows
+  pdl_wait();  // qkv comes from the previous kernel
+  pdl_trigger();
   const int t = blockIdx.x, tid = threadIdx.x;
   const int qkv_n = (nq + 2 * nkv) * D, half = D / 2, pos = (pos0_dev ? *pos0_dev : pos0) + t;
   const float* src = qkv + static_cast<size_t>(t) * qkv_n;
@@ -756,24 +758,22 @@ cudaError_t launch_norm_rows(const float* X, int n, const void* gain, int wbytes
 
 cudaError_t launch_rope_append(const float* qkv, float* Q, const float2* rope, int kv_dtype, void* kc, void* vc,
                                void* ks, void* vs, int n, int nq, int nkv, int D, int pos0, const int* pos0_dev,
-                               size_t head_row0, int cap, cudaStream_t s) {
+                               size_t head_row0, int cap, cudaStream_t s, bool pdl) {
   const size_t smem = sizeof(float) * 2 * nkv * D;
   switch (kv_dtype) {
     case 0:
-      rope_append_kernel<float><<<n, 256, smem, s>>>(qkv, Q, rope, static_cast<float*>(kc), static_cast<float*>(vc),
-                                                     nullptr, nullptr, nq, nkv, D, pos0, pos0_dev, head_row0, cap);
-      break;
+      return launch_k(rope_append_kernel<float>, dim3(n), dim3(256), smem, s, pdl, qkv, Q, rope, static_cast<float*>(kc),
+                      static_cast<float*>(vc), static_cast<__half*>(nullptr), static_cast<__half*>(nullptr), nq, nkv, D,
+                      pos0, pos0_dev, head_row0, cap);
     case 2:
-      rope_append_kernel<__half><<<n, 256, smem, s>>>(qkv, Q, rope, static_cast<__half*>(kc),
-                                                      static_cast<__half*>(vc), nullptr, nullptr, nq, nkv, D, pos0,
-                                                      pos0_dev, head_row0, cap);
-      break;
+      return launch_k(rope_append_kernel<__half>, dim3(n), dim3(256), smem, s, pdl, qkv, Q, rope,
+                      static_cast<__half*>(kc), static_cast<__half*>(vc), static_cast<__half*>(nullptr),
+                      static_cast<__half*>(nullptr), nq, nkv, D, pos0, pos0_dev, head_row0, cap);
     default:
-      rope_append_kernel<int8_t><<<n, 256, smem, s>>>(qkv, Q, rope, static_cast<int8_t*>(kc),
-                                                      static_cast<int8_t*>(vc), static_cast<__half*>(ks),
-                                                      static_cast<__half*>(vs), nq, nkv, D, pos0, pos0_dev, head_row0, cap);
+      return launch_k(rope_append_kernel<int8_t>, dim3(n), dim3(256), smem, s, pdl, qkv, Q, rope,
+                      static_cast<int8_t*>(kc), static_cast<int8_t*>(vc), static_cast<__half*>(ks),
+                      static_cast<__half*>(vs), nq, nkv, D, pos0, pos0_dev, head_row0, cap);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_attn(const float* Q, int kv_dtype, const void* kc, const void* vc, const void* ks,

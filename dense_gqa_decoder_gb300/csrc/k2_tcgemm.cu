@@ -646,6 +646,9 @@ __global__ void __launch_bounds__(PaSmem<D, SPLIT>::THREADS, 1) prefill_attn_tc_
   __shared__ float xmax[NQ][kPaRows];    // each part's tile maximum per row
   __shared__ int pbad[kPaMaxSoftWarps];  // a softmax warp's verdict, read by the warps sharing its rows
   __shared__ int issued[3];            // the issuer's count of K/V tiles, S and P.V issued
+  // the GEMM that reads this kernel's output may launch at once and request its
+  // weights on SMs this grid leaves idle (it waits for this grid before reading)
+  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = (warp & 3) * 32 + lane;  // TMEM lane = query row
   const int hf = warp >> 2;                // which CW of the 64 scores (and DH columns of O) this thread takes
