@@ -427,8 +427,9 @@ typedef enum {
                              significant bits, 3 more than bf16), one MMA per K step; elsewhere (fp8 / int4
                              weights, int8 or fp32 caches) 3 acts as 1.  3 is the default: on the same
                              model and test it gives 99.2-100 % agreement, relative L2 2.1e-3 (3.6e-3 on
-                             the prefill's logits), and a 4096-token prompt takes 48.0 ms against 73.3 ms
-                             with 1 and 66.3 ms with 2 (1 and 2 measured before the GEMMs ran under PDL). */
+                             the prefill's logits), and a 4096-token prompt takes 46.5 ms against 73.3 ms
+                             with 1 and 66.3 ms with 2 (1 and 2 measured before the prefill kernels ran
+                             under PDL). */
   K2_OPT_PREFILL_GEMM = 13 /* tensor-core prefill of blocks over 16 tokens, QKV and gate/up GEMMs: 1 (default)
                              one persistent CTA per SM over whole 128 x 128 tiles, two TMEM accumulators so
                              that a tile's epilogue (store, SwiGLU) overlaps the next tile's K steps; 0 one
