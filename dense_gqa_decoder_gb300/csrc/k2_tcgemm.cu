@@ -6,24 +6,25 @@
 // are dense contractions.  W is a packed projection matrix (pairs of rows in
 // 512-byte chunks, the same copy the decode step streams); a 4-D TMA tensor
 // map (element, row-in-pair, chunk, pair) reads it as ordinary 128-row K-major
-// tiles.  X is kept as two bf16 matrices whose sum is the fp32 activation
-// (x_hi = bf16(x), x_lo = bf16(x - x_hi)); each K step issues one MMA per
-// half, so the product keeps ~16 mantissa bits of the activation, the
-// precision the decode step's fp32 activations have, while W stays the model's
-// bf16.  Without the low half (LO = false: no map for it) each K step issues
-// one MMA on x_hi alone -- activations in the model's dtype, half the MMAs and
-// half the activation bytes -- and the ring holds more stages.  With a second
-// weight map (WL = true: W = w_hi + w_lo, the int4 weights dequantized to two
-// bf16 halves) each K step also issues w_lo . x_hi, so the product keeps ~16
-// bits of every weight too (w_lo . x_lo, below both halves' rounding, is left
-// out).
+// tiles.  The operands are one of:
+//  - single fp16 (the default prefill, f16 = 1): W the fp16 copy of the bf16
+//    weights, X single fp16 activations; one MMA per K step;
+//  - bf16 W and X as two bf16 matrices whose sum is the fp32 activation
+//    (x_hi = bf16(x), x_lo = bf16(x - x_hi)), one MMA per half, so the product
+//    keeps ~16 mantissa bits of the activation; without the low half (LO =
+//    false) one MMA on x_hi alone;
+//  - with a second weight map (WL = true: W = w_hi + w_lo, the int4 weights
+//    dequantized to two bf16 halves) each K step also issues w_lo . x_hi
+//    (w_lo . x_lo, below both halves' rounding, is left out).
 //
-// One CTA per 128-row x 128-token tile, 128 threads: thread 0 issues the TMA
-// loads into a 4-stage ring (mbarrier complete_tx), thread 32 issues the MMAs
-// (128x128x16, bf16 in, fp32 accumulate) and frees each stage with
-// tcgen05.commit, then all four warps read the accumulator tile out of TMEM
-// (warp w owns TMEM lanes 32w..32w+31 = rows) and apply the epilogue.  Every
-// wait is bounded; a timeout sets the guard word and skips the accumulator.
+// Two kernels.  tc_gemm_sk_kernel (the prefill's and the batched decode's):
+// one persistent CTA per SM; warp 0 issues the TMA loads into a ring, thread
+// 32 the MMAs into one of two TMEM accumulators, warps 2-5 drain the other and
+// apply the epilogue (store, residual add, SwiGLU), over whole tiles or
+// stream-K shares (below).  tc_gemm_kernel: one CTA per 128-row x 128-token
+// tile, the epilogue after its own K steps (option K2_OPT_PREFILL_GEMM = 0).
+// Every wait is bounded; a timeout sets the guard word and skips the
+// accumulator.
 #include <cuda.h>
 
 #include <algorithm>
