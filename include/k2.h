@@ -35,8 +35,9 @@
  *   - A non-zero k2_status means the call had no effect on the context and
  *     enqueued no work; k2_last_error(ctx) says why.  Faults detected on the
  *     device (a token id outside the vocabulary, a NaN logit, a bounded wait
- *     that ran out) never trap: they set a device guard word that
- *     k2_sync_status reports.
+ *     that ran out, a position outside the cache, a weight or activation
+ *     beyond fp16's range in the fp16-operand prefill) never trap: they set a
+ *     device guard word that k2_sync_status reports.
  */
 #ifndef K2_H
 #define K2_H

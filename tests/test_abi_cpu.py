@@ -81,3 +81,21 @@ def test_calls_on_null_context_are_refused(k2):
     assert k2.LIB.k2_kv_reset(None, -1, None) == k2.K2_ERR_ARG
     assert k2.LIB.k2_sync_status(None, None) == k2.K2_ERR_ARG
     k2.LIB.k2_free(None)
+
+
+def header_enum(name):
+    """name -> value of the members of the typedef enum `name` in include/k2.h."""
+    text = open(os.path.join(ROOT, "include", "k2.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    body = re.search(r"typedef enum\s*\{([^}]*)\}\s*" + name + r"\s*;", text, flags=re.S).group(1)
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(K2_[A-Z0-9_]+)\s*=\s*(\d+)", body)}
+
+
+@pytest.mark.parametrize("enum", ["k2_status", "k2_dtype", "k2_option"])
+def test_binding_constants_match_the_header(k2, enum):
+    """Every status, dtype and option number the header declares has the same
+    value in the Python binding (the binding passes bare integers)."""
+    members = header_enum(enum)
+    assert len(members) >= 6
+    for n, v in members.items():
+        assert getattr(k2, n) == v, n
